@@ -1,0 +1,423 @@
+"""CPU oracle of the Gated DeltaNet layer core -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA library
+and never imports it; inputs arrive as numpy arrays (bf16 tensors as their
+uint16 bit patterns) and every result is computed here, in float64, in the
+order the pages give.
+
+Pages followed (each function names its passage):
+  [GD-RS]  "mlex 0.1.2, src/models/gated_delta.rs" -- GatedDeltaNet::load,
+           GatedDeltaNet::forward.
+  [QD-TS]  "mlx-bun 0.4.0 -> 1.0.0, package/src/model/qwen3-delta.ts" -- the
+           numerics table at its head, the gated_delta_step kernel source and
+           its masked specialization, computeG, gatedDeltaUpdate.
+
+Readings taken where the pages are silent or disagree (each is listed, with
+its reason, in the design notes of the repository):
+  * q, k, v are computed in high precision from the bf16 inputs and rounded
+    ONCE to bf16 (round-to-nearest-even) when stored.
+  * beta is kept in full precision (f32 on the device, f64 here), as [GD-RS]
+    casts b to f32 before the sigmoid.
+  * softplus(x) = max(x, 0) + log1p(exp(-|x|)), the stable form of
+    log(1 + e^x) (computeG builds it as logaddexp(x, 0)).
+  * rms-norm has no weight: x / sqrt(mean(x^2) + 1e-6); q is then scaled by
+    1/Dk and k by 1/sqrt(Dk) (GatedDeltaNet::forward, q/k normalisation).
+  * A masked step does not enter the conv window, writes zero q/k/v/y and
+    leaves both states untouched ("skip" reading of the masked kernel).
+
+Pinned by ``tests/test_oracle_pins.py`` against closed forms, invariants,
+library routines and hand-derived values in ``tests/golden/``.  The chunked
+form (``chunked_head``) is pinned against the sequential definition.
+"""
+from __future__ import annotations
+
+import concurrent.futures
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Iterable, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libgdn_oracle.so")
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+# --------------------------------------------------------------------------
+# build / load of the C part (the sequential recurrence)
+# --------------------------------------------------------------------------
+def build_oracle(force: bool = False) -> str:
+    """Compile gdn_oracle.c with gcc (plain -O2, IEEE double, no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+                               "-ffp-contract=off", "-o", tmp, _SRC])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            build_oracle()
+            lib = ctypes.CDLL(_LIB_PATH)
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.oracle_delta_rule_head.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   dp, dp, dp, dp, dp,
+                                                   ctypes.POINTER(ctypes.c_uint8), dp, dp]
+            lib.oracle_delta_rule_head.restype = None
+            _lib = lib
+    return _lib
+
+
+def _dptr(a: np.ndarray):
+    assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+# --------------------------------------------------------------------------
+# bf16 <-> f64 (the activation dtype of [QD-TS]'s numerics table)
+# --------------------------------------------------------------------------
+_BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64 values (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(x) -> np.ndarray:
+    """float64 -> bf16 bit patterns, one round-to-nearest-even step.
+
+    bf16 keeps 8 significant bits and the f32 exponent range: a value in
+    [2^(e-1), 2^e) is rounded to a multiple of 2^(e-8); below 2^-126 the grid
+    is the subnormal quantum 2^-133.  ``np.rint`` rounds halves to even."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)
+    qexp = np.maximum(e - 8, -133)
+    with np.errstate(over="ignore", invalid="ignore"):
+        r = np.rint(np.ldexp(a, -qexp))
+        val = np.ldexp(r, qexp)
+    val = np.where(val > _BF16_MAX, np.inf, val)
+    bits = (val.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    bits = np.where(np.signbit(x), bits | np.uint16(0x8000), bits)
+    bits = np.where(np.isnan(x), np.uint16(0x7FC0), bits)
+    return bits.astype(np.uint16)
+
+
+def round_bf16(x) -> np.ndarray:
+    return bf16_to_f64(f64_to_bf16(x))
+
+
+def round_f32(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# a4: gates  ([GD-RS] forward: beta and g; [QD-TS] computeG)
+# --------------------------------------------------------------------------
+def softplus(x):
+    """log(1 + e^x) in the overflow-free form max(x, 0) + log1p(e^-|x|)."""
+    x = np.asarray(x, dtype=np.float64)
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def sigmoid(x):
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-x))
+
+
+def gating(a_bits, b_bits, A_log, dt_bias):
+    """g = exp(-exp(A_log) * softplus(a + dt_bias)), beta = sigmoid(b).
+
+    a, b: bf16 bits [..., Hv]; A_log, dt_bias: f32 [Hv].  Returns float64
+    arrays shaped like a."""
+    a = bf16_to_f64(a_bits)
+    b = bf16_to_f64(b_bits)
+    A_log = np.asarray(A_log, dtype=np.float64)
+    dt_bias = np.asarray(dt_bias, dtype=np.float64)
+    g = np.exp(-np.exp(A_log) * softplus(a + dt_bias))
+    beta = sigmoid(b)
+    return g, beta
+
+
+# --------------------------------------------------------------------------
+# a1-a3: conv window, depthwise conv + SiLU, q/k rms-norm and scaling
+# ([GD-RS] forward: conv_state concat/slice, conv1d + silu, split, rms_norm)
+# --------------------------------------------------------------------------
+def silu(u):
+    u = np.asarray(u, dtype=np.float64)
+    return u * sigmoid(u)
+
+
+def conv_silu_channels(state_rows, x_rows, w, valid=None):
+    """Causal depthwise conv over [conv_state || new tokens] followed by SiLU.
+
+    state_rows: [K-1, Cs] f64, oldest first; x_rows: [T, Cs] f64;
+    w: [Cs, K] f64, tap K-1 multiplies the current token (MLX conv1d is a
+    cross-correlation: out[t] = sum_j w[j] * X[t + j]).  valid: [T] bool or
+    None.  Masked tokens do not enter the window; their output is zero.
+    Returns (out [T, Cs] f64, new_state [K-1, Cs] f64 = last K-1 window rows)."""
+    state_rows = np.asarray(state_rows, dtype=np.float64)
+    x_rows = np.asarray(x_rows, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T, Cs = x_rows.shape
+    K = w.shape[1]
+    idx = np.arange(T) if valid is None else np.nonzero(np.asarray(valid))[0]
+    n = len(idx)
+    X = np.concatenate([state_rows, x_rows[idx]], axis=0)   # [K-1+n, Cs]
+    u = np.zeros((n, Cs), dtype=np.float64)
+    for j in range(K):
+        u += w[:, j][None, :] * X[j:j + n]
+    out = np.zeros((T, Cs), dtype=np.float64)
+    out[idx] = silu(u)
+    new_state = X[n:n + K - 1].copy()
+    return out, new_state
+
+
+def rms_normalize(x, eps):
+    """x / sqrt(mean(x^2) + eps) over the last axis, no weight."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def _channel_ranges(d):
+    kd = d.Hk * d.Dk
+    return {
+        "q": lambda hk: np.arange(hk * d.Dk, (hk + 1) * d.Dk),
+        "k": lambda hk: kd + np.arange(hk * d.Dk, (hk + 1) * d.Dk),
+        "v": lambda hv: 2 * kd + np.arange(hv * d.Dv, (hv + 1) * d.Dv),
+    }
+
+
+def conv_head(d, part, head, b, qkv_bits, conv_w_bits, conv_state_bits, mask):
+    """q, k or v of one head of batch row b: bf16 bits [T, D] plus the new
+    conv_state rows of that head's channels (bf16 bits [K-1, D]).
+
+    q = rms(x_q) / Dk, k = rms(x_k) / sqrt(Dk), v = x_v; one bf16 rounding."""
+    ch = _channel_ranges(d)[part](head)
+    x_rows = bf16_to_f64(np.asarray(qkv_bits)[b][:, ch])
+    if conv_state_bits is None:
+        st = np.zeros((d.K - 1, len(ch)))
+    else:
+        st = bf16_to_f64(np.asarray(conv_state_bits)[b][:, ch])
+    w = bf16_to_f64(np.asarray(conv_w_bits)[ch])
+    valid = None if mask is None else np.asarray(mask)[b] != 0
+    x, new_st = conv_silu_channels(st, x_rows, w, valid)
+    if part == "q":
+        x = rms_normalize(x, d.eps_qk) * (1.0 / d.Dk)
+    elif part == "k":
+        x = rms_normalize(x, d.eps_qk) * float(d.Dk) ** -0.5
+    return f64_to_bf16(x), f64_to_bf16(new_st)
+
+
+def conv_update(d, qkv_bits, conv_w_bits, conv_state_bits=None, mask=None):
+    """Full a1-a3 for all rows: returns q, k [B,T,Hk,Dk], v [B,T,Hv,Dv] (bf16
+    bits) and the new conv_state [B,K-1,C] (bf16 bits)."""
+    B, T = d.B, d.T
+    q = np.zeros((B, T, d.Hk, d.Dk), np.uint16)
+    k = np.zeros((B, T, d.Hk, d.Dk), np.uint16)
+    v = np.zeros((B, T, d.Hv, d.Dv), np.uint16)
+    new_cs = np.zeros((B, d.K - 1, d.C), np.uint16)
+    rng = _channel_ranges(d)
+    for b in range(B):
+        for hk in range(d.Hk):
+            q[b, :, hk], new_cs[b][:, rng["q"](hk)] = conv_head(d, "q", hk, b, qkv_bits, conv_w_bits,
+                                                               conv_state_bits, mask)
+            k[b, :, hk], new_cs[b][:, rng["k"](hk)] = conv_head(d, "k", hk, b, qkv_bits, conv_w_bits,
+                                                               conv_state_bits, mask)
+        for hv in range(d.Hv):
+            v[b, :, hv], new_cs[b][:, rng["v"](hv)] = conv_head(d, "v", hv, b, qkv_bits, conv_w_bits,
+                                                               conv_state_bits, mask)
+    return q, k, v, new_cs
+
+
+# --------------------------------------------------------------------------
+# a5/a6: the recurrence ([GD-RS] per-timestep loop; [QD-TS] gated_delta_step)
+# --------------------------------------------------------------------------
+def k_head_of(d, hv: int) -> int:
+    """GQA: v-head hv reads k-head hv / (Hv/Hk) (consecutive v-heads share a
+    k-head; [QD-TS] kernel index math, [GD-RS] repeat_axis)."""
+    return hv // (d.Hv // d.Hk)
+
+
+def head_recurrence(q, k, v, g, beta, S0, mask=None):
+    """One head, sequential in t, in the C part.  q, k [T,Dk], v [T,Dv],
+    g, beta [T] (float64), S0 [Dv,Dk] float64, mask [T] or None.
+    Returns (y [T,Dv], S_T [Dv,Dk]) in float64."""
+    lib = _load()
+    q = np.ascontiguousarray(q, np.float64)
+    k = np.ascontiguousarray(k, np.float64)
+    v = np.ascontiguousarray(v, np.float64)
+    g = np.ascontiguousarray(g, np.float64)
+    beta = np.ascontiguousarray(beta, np.float64)
+    S = np.array(S0, dtype=np.float64, order="C", copy=True)
+    T, Dk = q.shape
+    Dv = v.shape[1]
+    assert k.shape == (T, Dk) and v.shape == (T, Dv) and S.shape == (Dv, Dk)
+    y = np.zeros((T, Dv), np.float64)
+    if mask is not None:
+        m = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+        mp = m.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+    else:
+        m, mp = None, None
+    lib.oracle_delta_rule_head(T, Dk, Dv, _dptr(q), _dptr(k), _dptr(v), _dptr(g), _dptr(beta),
+                               mp, _dptr(S), _dptr(y))
+    return y, S
+
+
+def _default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def recurrence(d, q_bits, k_bits, v_bits, g, beta, state_in=None, mask=None,
+               pairs: Optional[Iterable] = None, threads: Optional[int] = None):
+    """a5 + a6 over (b, hv) pairs (default: all), one thread per pair.
+
+    q_bits, k_bits [B,T,Hk,Dk], v_bits [B,T,Hv,Dv] bf16 bits; g, beta
+    [B,T,Hv] float64; state_in [B,Hv,Dv,Dk] (None = zeros).
+    Returns y [B,T,Hv,Dv] float64 (rows of pairs not computed are NaN) and
+    state_out [B,Hv,Dv,Dk] float64 (pairs not computed keep state_in)."""
+    if pairs is None:
+        pairs = [(b, hv) for b in range(d.B) for hv in range(d.Hv)]
+    pairs = list(pairs)
+    if state_in is None:
+        state_out = np.zeros((d.B, d.Hv, d.Dv, d.Dk), np.float64)
+    else:
+        state_out = np.array(state_in, dtype=np.float64, copy=True)
+    y = np.full((d.B, d.T, d.Hv, d.Dv), np.nan, np.float64)
+
+    def one(pair):
+        b, hv = pair
+        hk = k_head_of(d, hv)
+        yy, S = head_recurrence(bf16_to_f64(q_bits[b, :, hk]), bf16_to_f64(k_bits[b, :, hk]),
+                                bf16_to_f64(v_bits[b, :, hv]), g[b, :, hv], beta[b, :, hv],
+                                state_out[b, hv], None if mask is None else mask[b])
+        y[b, :, hv] = yy
+        state_out[b, hv] = S
+
+    n = threads or _default_threads()
+    if n <= 1 or len(pairs) <= 1:
+        for p in pairs:
+            one(p)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+            list(ex.map(one, pairs))
+    return y, state_out
+
+
+# --------------------------------------------------------------------------
+# the whole core for a set of (b, hv) pairs: a1..a6
+# --------------------------------------------------------------------------
+def layer_core(d, qkv_bits, conv_w_bits, a_bits, b_bits, A_log, dt_bias, conv_state_bits=None,
+         state_in=None, mask=None, pairs: Optional[Sequence] = None, threads: Optional[int] = None):
+    """conv -> SiLU -> q/k norm -> gates -> recurrence, as GatedDeltaNet::forward
+    of [GD-RS] orders them.  With ``pairs`` only those (b, hv) heads (and the
+    conv channels they read) are computed.  Returns a dict with q, k, v (bf16
+    bits, zero where not computed), g, beta (float64), y (float64, NaN where not
+    computed), y_bf16 (bits), state (float64), conv_state (bf16 bits, only when
+    every head was computed)."""
+    full = pairs is None
+    if full:
+        q, k, v, new_cs = conv_update(d, qkv_bits, conv_w_bits, conv_state_bits, mask)
+    else:
+        q = np.zeros((d.B, d.T, d.Hk, d.Dk), np.uint16)
+        k = np.zeros((d.B, d.T, d.Hk, d.Dk), np.uint16)
+        v = np.zeros((d.B, d.T, d.Hv, d.Dv), np.uint16)
+        new_cs = None
+        done_k = set()
+        for (b, hv) in pairs:
+            hk = k_head_of(d, hv)
+            if (b, hk) not in done_k:
+                q[b, :, hk], _ = conv_head(d, "q", hk, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
+                k[b, :, hk], _ = conv_head(d, "k", hk, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
+                done_k.add((b, hk))
+            v[b, :, hv], _ = conv_head(d, "v", hv, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
+    g, beta = gating(a_bits, b_bits, A_log, dt_bias)
+    y, S = recurrence(d, q, k, v, g, beta, state_in, mask, pairs, threads)
+    y_bits = f64_to_bf16(np.nan_to_num(y))
+    return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "y": y, "y_bf16": y_bits,
+            "state": S, "conv_state": new_cs}
+
+
+def decode(d, steps_inputs, conv_w_bits, A_log, dt_bias, conv_state_bits, state_in,
+           row_mask=None, pairs=None, threads=None):
+    """Carried single-token steps: each step is ``core`` with T = 1, the conv
+    state carried as bf16 and the recurrent state carried as f32 (the storage
+    types of the cache slots).  steps_inputs: list of dicts with qkv [B,1,C],
+    a, b [B,1,Hv] bf16 bits.  Returns (list of y_bf16 [B,Hv,Dv], state f64,
+    conv_state bits)."""
+    d1 = d.with_(T=1)
+    cs = None if conv_state_bits is None else np.array(conv_state_bits, copy=True)
+    st = None if state_in is None else round_f32(state_in)
+    mask = None if row_mask is None else np.asarray(row_mask).reshape(d.B, 1)
+    ys = []
+    for inp in steps_inputs:
+        out = layer_core(d1, inp["qkv"], conv_w_bits, inp["a"], inp["b"], A_log, dt_bias, cs, st, mask,
+                   pairs, threads)
+        ys.append(out["y_bf16"][:, 0])
+        st = round_f32(out["state"])
+        if pairs is None:
+            cs = out["conv_state"]
+    return ys, st, cs
+
+
+# --------------------------------------------------------------------------
+# a7: the chunked (WY / UT-transform) form, derived from the recurrence.
+# Not on the pages; pinned against head_recurrence.
+# --------------------------------------------------------------------------
+def chunked_head(q, k, v, g, beta, S0, mask=None, chunk=64):
+    """Same result as head_recurrence, computed chunk by chunk.
+
+    Per chunk of n steps with start state S0 and log-decay prefix sums
+    lg_r = sum_{i<=r} log g_i (gamma_r = exp(lg_r)):
+      A[r,i] = beta_r exp(lg_r - lg_i) (k_r . k_i)  for i < r
+      Tm     = (I + A)^-1                         (unit lower triangular)
+      U      = Tm diag(beta) V,   W = Tm diag(beta gamma) K
+      Dl     = U - W S0^T                          (row r = delta_r)
+      Y      = diag(gamma) Q S0^T + (M o Q K^T) Dl,  M[r,i] = exp(lg_r - lg_i), i <= r
+      S_C    = gamma_n S0 + Dl^T diag(exp(lg_n - lg)) K
+    Masked steps enter with g = 1, beta = 0 and their y is set to zero."""
+    from scipy.linalg import solve_triangular
+
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    g = np.asarray(g, np.float64).copy()
+    beta = np.asarray(beta, np.float64).copy()
+    T = q.shape[0]
+    valid = np.ones(T, bool) if mask is None else (np.asarray(mask) != 0)
+    g[~valid] = 1.0
+    beta[~valid] = 0.0
+    S = np.array(S0, dtype=np.float64, copy=True)
+    y = np.zeros((T, v.shape[1]), np.float64)
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(c0 + chunk, T))
+        Qc, Kc, Vc, gc, bc = q[sl], k[sl], v[sl], g[sl], beta[sl]
+        n = Qc.shape[0]
+        lg = np.cumsum(np.log(gc))
+        gam = np.exp(lg)
+        ratio = np.exp(lg[:, None] - lg[None, :])
+        A = np.tril(bc[:, None] * ratio * (Kc @ Kc.T), -1)
+        Tm = solve_triangular(np.eye(n) + A, np.eye(n), lower=True, unit_diagonal=True)
+        U = Tm @ (bc[:, None] * Vc)
+        W = Tm @ ((bc * gam)[:, None] * Kc)
+        Dl = U - W @ S.T
+        M = np.tril(ratio)
+        Y = gam[:, None] * (Qc @ S.T) + (M * (Qc @ Kc.T)) @ Dl
+        S = gam[-1] * S + Dl.T @ (np.exp(lg[-1] - lg)[:, None] * Kc)
+        y[sl] = Y
+    y[~valid] = 0.0
+    return y, S
