@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Throughput of the Gated DeltaNet core on one GB300 (or N, weak scaling).
+
+Headline ("step" = one pass of the whole hot path over one batch): one fused
+decode step of the batched-decode workload (B=128, Hk=16, Hv=32, Dk=Dv=128,
+K=4: conv window + conv + SiLU + q/k norm + gates + recurrence on a 256 MiB
+f32 state), carried step after step.  value = state GB/s (state bytes read +
+written per step / device time per step).  The JSON line also carries the
+roofline of the decode kernel (all algorithmic bytes / kernel time vs the
+measured HBM copy peak), the end-to-end rate through the public API with
+host buffers, the prefill tokens/s of the single-sequence and ragged prefill
+workloads, and the CPU oracle's rate on a bounded sample.
+
+--impl reference runs the reference arm: the CPU oracle, timed on this
+host's cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from gated_deltanet_linear_04_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "GDN decode state GB/s (% HBM peak) and prefill tokens/s on 1 GB300"
+HEADLINE = "decode_b128"
+
+
+# ---------------------------------------------------------------------------
+# byte / flop accounting (algorithmic, per unit)
+# ---------------------------------------------------------------------------
+def decode_bytes(d: wl.Dims) -> dict:
+    state = d.B * d.Hv * d.Dv * d.Dk * 4
+    conv_state = d.B * (d.K - 1) * d.C * 2
+    return {
+        "state_rw": 2 * state,
+        "conv_state_rw": 2 * conv_state,
+        "qkv": d.B * d.C * 2,
+        "ab": 2 * d.B * d.Hv * 2,
+        "y": d.B * d.Hv * d.Dv * 2,
+        "params": d.C * d.K * 2 + 2 * d.Hv * 4,
+    }
+
+
+def recurrence_flops_per_token(d: wl.Dims) -> int:
+    # decay (1), kv dot (2), update (2), output dot (2) per state element
+    return 7 * d.Dk * d.Dv * d.Hv
+
+
+# ---------------------------------------------------------------------------
+# environment: peaks, clocks, ranks
+# ---------------------------------------------------------------------------
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms; keeps the
+    samples that fall inside [start, stop]."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = [l for (t, l) in self.lines if self.t0 is not None and self.t0 - 0.06 <= t <= (self.t1 or t) + 0.06]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [x.strip() for x in r.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                mx.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_04_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile: str, src_files) -> float | None:
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (its 'source_hash' line matches)."""
+    p = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_h = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_h or not m_b or m_h.group(1) != source_hash(*src_files):
+        return None
+    return float(m_b.group(1))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (bounded sample)
+# ---------------------------------------------------------------------------
+def oracle_decode_rate(w: wl.Workload, budget_s: float) -> dict:
+    import oracle
+    oracle.build_oracle()
+    d = w.dims
+    inp = wl.workload_inputs(w)
+    cw = wl.bf16_bits(inp["conv_w"])
+    A_log, dt = inp["A_log"].numpy(), inp["dt_bias"].numpy()
+    cs = wl.bf16_bits(inp["conv_state"])
+    st = inp["state"].numpy().astype(np.float64)
+    threads = os.cpu_count() or 1
+    steps, t_used = 0, 0.0
+    while t_used < budget_s and steps < w.steps:
+        s_in = wl.decode_step_inputs(w, steps)
+        sb = [{k: wl.bf16_bits(s_in[k]) for k in ("qkv", "a", "b")}]
+        t0 = time.perf_counter()
+        _, st, cs = oracle.decode(d, sb, cw, A_log, dt, cs, st, threads=threads)
+        t_used += time.perf_counter() - t0
+        steps += 1
+    by = decode_bytes(d)
+    return {"steps": steps, "seconds": t_used, "state_gbs": by["state_rw"] * steps / t_used / 1e9,
+            "tokens_per_s": d.B * steps / t_used, "cores": threads}
+
+
+# ---------------------------------------------------------------------------
+# GPU legs
+# ---------------------------------------------------------------------------
+def bench_decode(gdn, w: wl.Workload, steps: int, warmup: int, dev, sampler) -> dict:
+    d = w.dims
+    d1 = d.with_(T=1)
+    inp = wl.workload_inputs(w)
+    n_in = min(w.steps, steps + warmup)
+    step_in = [wl.decode_step_inputs(w, i) for i in range(n_in)]
+    qkv_h = torch.stack([s["qkv"][:, 0] for s in step_in]).pin_memory()   # [n, B, C]
+    a_h = torch.stack([s["a"][:, 0] for s in step_in]).pin_memory()
+    b_h = torch.stack([s["b"][:, 0] for s in step_in]).pin_memory()
+    qkv, a, b = qkv_h.to(dev), a_h.to(dev), b_h.to(dev)
+    conv_w, A_log, dt_bias = inp["conv_w"].to(dev), inp["A_log"].to(dev), inp["dt_bias"].to(dev)
+    conv_state = inp["conv_state"].to(dev)
+    state = inp["state"].to(dev)
+    y = torch.empty((d.B, d.Hv, d.Dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j = i % n_in
+        gdn.gdn_recurrent_decode(d1, qkv[j], conv_w, conv_state, a[j], b[j], A_log, dt_bias, state, None, y, stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark_start()
+    ev0.record(stream)
+    for i in range(steps):
+        step(warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_stop()
+    ms = ev0.elapsed_time(ev1) / steps
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the decode benchmark")
+
+    # end to end through the public API: pinned host inputs -> device, decode,
+    # y -> pinned host, every step
+    y_h = torch.empty((d.B, d.Hv, d.Dv), dtype=torch.bfloat16).pin_memory()
+    qkv_d = torch.empty_like(qkv[0])
+    a_d, b_d = torch.empty_like(a[0]), torch.empty_like(b[0])
+
+    def e2e_step(i):
+        j = i % n_in
+        qkv_d.copy_(qkv_h[j], non_blocking=True)
+        a_d.copy_(a_h[j], non_blocking=True)
+        b_d.copy_(b_h[j], non_blocking=True)
+        gdn.gdn_recurrent_decode(d1, qkv_d, conv_w, conv_state, a_d, b_d, A_log, dt_bias, state, None, y, stream)
+        y_h.copy_(y, non_blocking=True)
+
+    for i in range(warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    e0.record(stream)
+    for i in range(steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    e2e_ms = max(e0.elapsed_time(e1), t_wall * 1e3) / steps
+    return {"ms": ms, "e2e_ms": e2e_ms,
+            "h2d": qkv_d.numel() * 2 + a_d.numel() * 2 + b_d.numel() * 2, "d2h": y_h.numel() * 2}
+
+
+def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int) -> dict:
+    """Full core (conv + gates + recurrence) over one workload call."""
+    d = w.dims
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + w.index)
+    qkv = torch.randn((d.B, d.T, d.C), generator=gen, device=dev).to(torch.bfloat16)
+    conv_w = (torch.randn((d.C, d.K), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
+    a = torch.randn((d.B, d.T, d.Hv), generator=gen, device=dev).to(torch.bfloat16)
+    b = torch.randn((d.B, d.T, d.Hv), generator=gen, device=dev).to(torch.bfloat16)
+    A_log = torch.log(torch.empty(d.Hv, device=dev).uniform_(1.0, 16.0, generator=gen))
+    dt_bias = torch.randn(d.Hv, generator=gen, device=dev) * 0.5
+    state0 = (torch.randn((d.B, d.Hv, d.Dv, d.Dk), generator=gen, device=dev) * 0.05 if w.state == "normal"
+              else torch.zeros((d.B, d.Hv, d.Dv, d.Dk), device=dev))
+    mask = None
+    n_valid = d.B * d.T
+    if w.ragged:
+        lens = wl.make_lengths(d.B, w.len_lo, w.len_hi, 1000 + w.index + 104729)
+        mask = wl.right_padded_mask(lens, d.T).to(dev)
+        n_valid = int(lens.sum())
+    conv_state = torch.zeros((d.B, d.K - 1, d.C), dtype=torch.bfloat16, device=dev)
+    q = torch.empty((d.B, d.T, d.Hk, d.Dk), dtype=torch.bfloat16, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty((d.B, d.T, d.Hv, d.Dv), dtype=torch.bfloat16, device=dev)
+    g = torch.empty((d.B, d.T, d.Hv), dtype=torch.float32, device=dev)
+    beta = torch.empty_like(g)
+    y = torch.empty((d.B, d.T, d.Hv, d.Dv), dtype=torch.bfloat16, device=dev)
+    s_out = torch.empty_like(state0)
+    nws = gdn.gdn_prefill_workspace_size(d, chunk)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def once(record=False):
+        if record:
+            ev[0].record(stream)
+        gdn.gdn_conv_update(d, qkv, conv_w, conv_state, mask, q, k, v, stream)
+        gdn.gdn_gating(d, a, b, A_log, dt_bias, g, beta, stream)
+        if record:
+            ev[1].record(stream)
+        gdn.gdn_prefill(d, q, k, v, g, beta, state0, s_out, mask, y, chunk, ws if nws else None, stream)
+        if record:
+            ev[2].record(stream)
+
+    once()
+    torch.cuda.synchronize()
+    t_tot, t_rec = 0.0, 0.0
+    for _ in range(iters):
+        once(True)
+        torch.cuda.synchronize()
+        t_tot += ev[0].elapsed_time(ev[2])
+        t_rec += ev[1].elapsed_time(ev[2])
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the prefill benchmark")
+    ms, ms_rec = t_tot / iters, t_rec / iters
+    flops = recurrence_flops_per_token(d) * n_valid
+    return {"workload": w.name, "chunk": chunk, "ms": round(ms, 4), "recurrence_ms": round(ms_rec, 4),
+            "tokens": n_valid, "tokens_per_s": n_valid / (ms / 1e3),
+            "recurrence_tflops": flops / (ms_rec / 1e3) / 1e12}
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    ws, rank, local = dist_env()
+    w = wl.WORKLOADS[HEADLINE]
+    d = w.dims
+    by = decode_bytes(d)
+    alg_bytes = sum(by.values())
+
+    if args.impl == "reference":
+        if ws > 1:
+            torch.distributed.init_process_group("gloo")
+            if rank != 0:
+                torch.distributed.destroy_process_group()
+                return
+        r = oracle_decode_rate(w, args.cpu_budget_s)
+        ms = r["seconds"] / r["steps"] * 1e3
+        line = {"impl": "reference", "metric": METRIC, "value": round(r["state_gbs"], 4), "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": r["steps"], "warmup": 0, "ms_per_step": round(ms, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": w.name, "B": d.B, "Hk": d.Hk, "Hv": d.Hv,
+                                                "Dk": d.Dk, "Dv": d.Dv, "K": d.K},
+                "cpu_baseline": {"value": round(r["state_gbs"], 4), "unit": "GB/s", "cores": r["cores"],
+                                 "kind": "oracle",
+                                 "sample": "first %d carried decode steps of the workload (all %d heads)" % (
+                                     r["steps"], d.B * d.Hv)},
+                "e2e": {"value": round(r["state_gbs"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    from gated_deltanet_linear_04_gb300 import gdn
+    gdn.lib()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+
+    peaks = load_peaks()
+    with ClockSampler(local) as sampler:
+        barrier(ws)
+        res = bench_decode(gdn, w, args.steps, args.warmup, dev, sampler)
+    ms = max_over_ranks(res["ms"], ws)
+    e2e_ms = max_over_ranks(res["e2e_ms"], ws)
+    clocks = sampler.summary()
+
+    prefill = []
+    if not args.no_prefill:
+        for name in ("prefill_t8192", "prefill_ragged"):
+            for chunk in (0, 64):
+                try:
+                    prefill.append(bench_prefill(gdn, wl.WORKLOADS[name], dev, 3, chunk))
+                except gdn.GdnError as e:
+                    if e.status != gdn.GDN_ERR_UNSUPPORTED:
+                        raise
+                    prefill.append({"workload": name, "chunk": chunk, "unavailable": "chunked form not built"})
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        r = oracle_decode_rate(w, args.cpu_budget_s)
+        cpu = {"value": round(r["state_gbs"], 4), "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+               "sample": "first %d carried decode steps of %s (all %d heads), f64 C+numpy oracle" % (
+                   r["steps"], w.name, d.B * d.Hv)}
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+    value = by["state_rw"] * ws / (ms / 1e3) / 1e9
+    achieved = alg_bytes / (ms / 1e3) / 1e9
+    traffic = profiled_traffic("decode_b128_ncu.md", ["decode.cu", "common.cuh"])
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": d.B, "T": 1, "Hk": d.Hk, "Hv": d.Hv, "Dk": d.Dk, "Dv": d.Dv,
+                   "K": d.K, "carried_steps": args.steps, "distinct_step_inputs": min(w.steps, args.steps +
+                                                                                    args.warmup),
+                   "l2": "inputs larger than L2 (512 MiB of state read+written per step)",
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "tokens_per_s": round(d.B * ws / (ms / 1e3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "algorithmic_bytes": alg_bytes, "kernel": "gdn::decode_kernel<128>",
+                     "peak_source": peaks["source"]},
+        "e2e": {"value": round(by["state_rw"] * ws / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "prefill": prefill,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+// The C ABI (include/gdn.h): argument validation, status codes, the per-device
+// error word, tensor-map encoding, and dispatch to the kernels.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gdn {
+
+// One word per device, set by kernels whose bounded waits give up.
+__device__ unsigned g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned *g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+unsigned *error_word() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_err_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<unsigned *>(ptr);
+    }
+    return g_err_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A tensor pointer is acceptable if 16-byte aligned and, when the tensor has
+// elements, not null.
+bool ok_ptr(const void *p, size_t elems) { return aligned16(p) && (elems == 0 || p != nullptr); }
+
+bool supported_d(int d) { return d == 32 || d == 64 || d == 128; }
+
+gdn_status check_dims(const gdn_dims *d, Sizes *s) {
+    if (d == nullptr) return GDN_ERR_INVALID_ARG;
+    if (d->B < 0 || d->T < 0 || d->Hk <= 0 || d->Hv <= 0 || d->Dk <= 0 || d->Dv <= 0 || d->K <= 0)
+        return GDN_ERR_INVALID_ARG;
+    if (d->Hv % d->Hk != 0) return GDN_ERR_INVALID_ARG;
+    if (!(d->eps_qk >= 0.0f)) return GDN_ERR_INVALID_ARG;
+    if (!supported_d(d->Dk) || !supported_d(d->Dv) || d->K < 2 || d->K > 4) return GDN_ERR_UNSUPPORTED;
+    if ((long long)d->B > 65535) return GDN_ERR_UNSUPPORTED;
+    const long long C = 2LL * d->Hk * d->Dk + (long long)d->Hv * d->Dv;
+    if (C > (1LL << 30) || (long long)d->Hv * d->Dv > 65535LL * 128) return GDN_ERR_UNSUPPORTED;
+    *s = Sizes{d->B, d->T, d->Hk, d->Hv, d->Dk, d->Dv, d->K, d->eps_qk};
+    return GDN_OK;
+}
+
+gdn_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    return e == cudaErrorNotSupported ? GDN_ERR_UNSUPPORTED : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+int num_sms() {
+    const int dev = current_device();
+    if (dev < 0) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t rows,
+                    uint64_t cols, uint32_t box_rows, uint32_t box_cols) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * (cuuint64_t)elem_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gdn
+
+using gdn::ok_ptr;
+
+extern "C" {
+
+int gdn_abi_version(void) { return 1; }
+
+const char *gdn_status_string(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument (null/misaligned pointer or bad size)";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: size outside the supported set";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA call failed";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait gave up";
+        default: return "GDN_ERR_UNKNOWN";
+    }
+}
+
+gdn_status gdn_conv_update(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
+                           uint16_t *conv_state, const uint8_t *mask, uint16_t *q, uint16_t *k, uint16_t *v,
+                           gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    const size_t BT = (size_t)s.B * s.T;
+    if (!ok_ptr(qkv, BT * s.C()) || !ok_ptr(conv_w, BT) || !ok_ptr(conv_state, 0) || !ok_ptr(mask, 0) ||
+        !ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT))
+        return GDN_ERR_INVALID_ARG;
+    if (BT == 0) return GDN_OK;
+    return gdn::from_cuda(gdn::launch_conv_update(s, qkv, conv_w, conv_state, mask, q, k, v, (cudaStream_t)stream));
+}
+
+gdn_status gdn_gating(const gdn_dims *dims, const uint16_t *a, const uint16_t *b, const float *A_log,
+                      const float *dt_bias, float *g, float *beta, gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    const size_t n = (size_t)s.B * s.T * s.Hv;
+    if (!ok_ptr(a, n) || !ok_ptr(b, n) || !ok_ptr(A_log, n) || !ok_ptr(dt_bias, n) || !ok_ptr(g, n) ||
+        !ok_ptr(beta, n))
+        return GDN_ERR_INVALID_ARG;
+    if (n == 0) return GDN_OK;
+    return gdn::from_cuda(gdn::launch_gating(s, a, b, A_log, dt_bias, g, beta, (cudaStream_t)stream));
+}
+
+gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
+                                uint16_t *conv_state, const uint16_t *a, const uint16_t *b, const float *A_log,
+                                const float *dt_bias, float *state, const uint8_t *row_mask, uint16_t *y,
+                                gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    if (s.T != 1) return GDN_ERR_INVALID_ARG;
+    if (s.Hv / s.Hk > 16) return GDN_ERR_UNSUPPORTED;
+    const size_t B = (size_t)s.B;
+    if (!ok_ptr(qkv, B) || !ok_ptr(conv_w, B) || !ok_ptr(conv_state, B) || !ok_ptr(a, B) || !ok_ptr(b, B) ||
+        !ok_ptr(A_log, B) || !ok_ptr(dt_bias, B) || !ok_ptr(state, B) || !ok_ptr(row_mask, 0) || !ok_ptr(y, B))
+        return GDN_ERR_INVALID_ARG;
+    if (B == 0) return GDN_OK;
+    return gdn::from_cuda(gdn::launch_decode(s, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y,
+                                             gdn::error_word(), (cudaStream_t)stream));
+}
+
+size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk) {
+    gdn::Sizes s;
+    if (gdn::check_dims(dims, &s) != GDN_OK) return 0;
+    if (chunk == 0) return 0;
+    if (chunk == 64) return gdn::prefill_chunked_workspace(s);
+    return 0;
+}
+
+gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const float *g, const float *beta, const float *state_in, float *state_out,
+                       const uint8_t *mask, uint16_t *y, int chunk, void *workspace, size_t ws_bytes,
+                       gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    if (chunk != 0 && chunk != 64) return GDN_ERR_UNSUPPORTED;
+    const size_t BT = (size_t)s.B * s.T;
+    const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
+    if (!ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT) || !ok_ptr(g, BT) || !ok_ptr(beta, BT) ||
+        !ok_ptr(state_in, 0) || !ok_ptr(state_out, nstate) || !ok_ptr(mask, 0) || !ok_ptr(y, BT))
+        return GDN_ERR_INVALID_ARG;
+    if (s.B == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (s.T == 0) {
+        if (state_in == nullptr) return gdn::from_cuda(cudaMemsetAsync(state_out, 0, nstate * sizeof(float), cs));
+        if (state_in == state_out) return GDN_OK;
+        return gdn::from_cuda(
+            cudaMemcpyAsync(state_out, state_in, nstate * sizeof(float), cudaMemcpyDeviceToDevice, cs));
+    }
+    if (chunk == 0)
+        return gdn::from_cuda(gdn::launch_prefill_seq(s, q, k, v, g, beta, state_in, state_out, mask, y,
+                                                      gdn::error_word(), cs));
+    const size_t need = gdn::prefill_chunked_workspace(s);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need || !gdn::aligned16(workspace)))
+        return GDN_ERR_INVALID_ARG;
+    return gdn::from_cuda(gdn::launch_prefill_chunked(s, q, k, v, g, beta, state_in, state_out, mask, y, workspace,
+                                                      gdn::error_word(), cs));
+}
+
+gdn_status gdn_device_status(gdn_stream stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+    unsigned *w = gdn::error_word();
+    if (w == nullptr) return GDN_ERR_CUDA;
+    unsigned host = 0;
+    if (cudaMemcpy(&host, w, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+    if (host != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GDN_ERR_CUDA;
+        return GDN_ERR_TIMEOUT;
+    }
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,274 @@
+// One fused decode step: conv window + conv + SiLU + q/k rms-norm, the gates,
+// and one step of the gated delta rule, streaming the f32 state once.
+//
+// Definitions: "mlx-bun 0.4.0 -> 1.0.0, package/src/model/qwen3-delta.ts",
+// gated_delta_step (one state row per dv, decay, kv_mem, delta, update, output)
+// and computeG; "mlex 0.1.2, src/models/gated_delta.rs", GatedDeltaNet::forward
+// (conv window, conv1d + silu, q/k normalisation, beta, g).
+//
+// HBM-bound design.  A CTA owns R = Dv/SN consecutive rows of one (b, hv)
+// state ([Dv, Dk] f32, rows contiguous over Dk).  At entry one thread starts
+// 1-D bulk copies (TMA engine) of the whole R x Dk slice into shared memory,
+// in 32-row chunks with one mbarrier each, so all of the slice is in flight
+// while the CTA computes its conv/norm/gates.  Each chunk is then updated in
+// shared memory and written back with a bulk store as soon as it is done.
+//
+// Per row (lane group of Dk/4 lanes, one float4 per lane):
+//   sk = S.k, sq = S.q           (two shuffle sums, reduced together)
+//   delta = beta (v - g sk)      (kv_mem read from the decayed state g S)
+//   y = g sq + delta (k.q)       (= S_new . q, with S_new = g S + delta k^T)
+//   S_new = g S + delta k
+//
+// The G = Hv/Hk v-heads of one k-head share the q/k conv channels.  All CTAs of
+// one (b, hk) form a thread-block cluster; each reads the old conv_state of
+// the q/k channels, arrives on the cluster barrier, and only cluster rank 0
+// writes the new q/k conv_state after waiting on it.  v channels belong to one
+// CTA each and are updated by it.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kChunkRows = 32;
+constexpr int kMaxRows = 128;
+
+struct DecodeParams {
+    const uint16_t *qkv, *conv_w;
+    uint16_t *conv_state;
+    const uint16_t *a, *b;
+    const float *A_log, *dt_bias;
+    float *state;
+    const uint8_t *row_mask;
+    uint16_t *y;
+    unsigned *err;
+    int B, Hk, Hv, Dv, C, K, SN;
+    float eps;
+};
+
+// conv over [conv_state rows 0..K-2, new] for channel c of row b; returns the
+// SiLU output and leaves the shifted window (the new conv_state rows) in nw.
+__device__ __forceinline__ float conv_channel(const DecodeParams &p, int b, int c, uint16_t (&nw)[3]) {
+    const int n = p.K - 1;
+    const uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
+    const uint16_t *w = p.conv_w + (size_t)c * p.K;
+    const uint16_t xnew = p.qkv[(size_t)b * p.C + c];
+    float u = 0.0f;
+    uint16_t prev[3] = {0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+        if (j < n) prev[j] = cs[(size_t)j * p.C];
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+        if (j < n) u = fmaf(bf16_to_f32(w[j]), bf16_to_f32(prev[j]), u);
+    u = fmaf(bf16_to_f32(w[n]), bf16_to_f32(xnew), u);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        if (j < n - 1) nw[j] = prev[j + 1];
+        else if (j == n - 1) nw[j] = xnew;
+        else nw[j] = 0;
+    }
+    return silu(u);
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
+    constexpr int LPR = DK / 4;       // lanes per state row (one float4 each)
+    constexpr int RPP = 32 / LPR;     // rows per warp pass
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = p.Hv / p.Hk;
+    const int R = p.Dv / p.SN;
+    const int rank = blockIdx.x;      // == %cluster_ctarank (cluster spans grid x)
+    const int hv_local = rank / p.SN, slice = rank % p.SN;
+    const int hk = blockIdx.y, b = blockIdx.z;
+    const int hv = hk * G + hv_local;
+    const int r0 = slice * R;
+    uint16_t *yrow = p.y + ((size_t)b * p.Hv + hv) * p.Dv + r0;
+
+    if (p.row_mask != nullptr && p.row_mask[b] == 0) {
+        // whole cluster shares b: every CTA leaves here, no barrier is pending
+        for (int i = tid; i < R; i += kThreads) yrow[i] = 0;
+        return;
+    }
+
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *S = reinterpret_cast<float *>(smem_raw);
+    __shared__ __align__(16) float q_s[DK];
+    __shared__ __align__(16) float k_s[DK];
+    __shared__ float v_s[kMaxRows];
+    __shared__ float y_s[kMaxRows];
+    __shared__ float red[kThreads / 32];
+    __shared__ float gbk[3];
+    __shared__ __align__(8) uint64_t bars[kMaxRows / kChunkRows];
+
+    const int rc = min(R, kChunkRows);
+    const int nch = R / rc;
+    const uint32_t chunk_bytes = (uint32_t)rc * DK * 4;
+    float *gstate = p.state + (((size_t)b * p.Hv + hv) * p.Dv + r0) * DK;
+
+    if (tid == 0) {
+        for (int ch = 0; ch < nch; ++ch) mbar_init(&bars[ch], 1);
+        fence_mbar_init();
+        for (int ch = 0; ch < nch; ++ch) {
+            mbar_expect_tx(&bars[ch], chunk_bytes);
+            bulk_load(S + (size_t)ch * rc * DK, gstate + (size_t)ch * rc * DK, chunk_bytes, &bars[ch]);
+        }
+    }
+
+    // ---- conv + SiLU for the q/k channels of hk and the v channels of the slice
+    uint16_t nw_qk[3] = {0, 0, 0}, nw_v[3] = {0, 0, 0};
+    float xqk = 0.0f;
+    const bool has_qk = tid < 2 * DK;
+    const int c_qk = tid < DK ? hk * DK + tid : p.Hk * DK + hk * DK + (tid - DK);
+    if (has_qk) xqk = conv_channel(p, b, c_qk, nw_qk);
+    const bool has_v = tid < R;
+    const int c_v = 2 * p.Hk * DK + hv * p.Dv + r0 + tid;
+    if (has_v) v_s[tid] = round_bf16(conv_channel(p, b, c_v, nw_v));
+    // every read of the shared (q/k) conv_state of this CTA is done
+    cluster_arrive_release();
+
+    // rms-norm sums: q channels are threads [0, DK), k channels [DK, 2 DK)
+    float ss = warp_sum(has_qk ? xqk * xqk : 0.0f);
+    if (lane == 0) red[warp] = ss;
+    if (tid == 0) {
+        const float x = bf16_to_f32(p.a[(size_t)b * p.Hv + hv]) + p.dt_bias[hv];
+        gbk[0] = expf(-expf(p.A_log[hv]) * softplus(x));
+        gbk[1] = sigmoid(bf16_to_f32(p.b[(size_t)b * p.Hv + hv]));
+    }
+    __syncthreads();
+    if (has_qk) {
+        constexpr int NW = DK / 32;
+        const bool is_q = tid < DK;
+        float tot = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) tot += red[(is_q ? 0 : NW) + w];
+        const float inv_d = 1.0f / (float)DK;
+        const float scale = is_q ? inv_d : 1.0f / sqrtf((float)DK);
+        const float val = round_bf16(xqk * ((1.0f / sqrtf(tot * inv_d + p.eps)) * scale));
+        if (is_q) q_s[tid] = val;
+        else k_s[tid - DK] = val;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float kq = 0.0f;
+        for (int i = lane; i < DK; i += 32) kq = fmaf(k_s[i], q_s[i], kq);
+        kq = warp_sum(kq);
+        if (lane == 0) gbk[2] = kq;
+    }
+    __syncthreads();
+
+    // ---- the recurrence step over the state slice
+    const int sub = lane / LPR, cl = lane % LPR;
+    const float4 kk = reinterpret_cast<const float4 *>(k_s)[cl];
+    const float4 qq = reinterpret_cast<const float4 *>(q_s)[cl];
+    const float g = gbk[0], beta = gbk[1], kq = gbk[2];
+    bool ok_all = true;
+    for (int ch = 0; ch < nch; ++ch) {
+        bool ok = mbar_wait(&bars[ch], 0, p.err);
+        ok = __syncthreads_and(ok) != 0;
+        ok_all = ok_all && ok;
+        if (ok) {
+            for (int rr = warp * RPP + sub; rr < rc; rr += (kThreads / 32) * RPP) {
+                const int row = ch * rc + rr;
+                float4 *sp = reinterpret_cast<float4 *>(S + (size_t)row * DK) + cl;
+                float4 s = *sp;
+                float dk = s.x * kk.x;
+                dk = fmaf(s.y, kk.y, dk);
+                dk = fmaf(s.z, kk.z, dk);
+                dk = fmaf(s.w, kk.w, dk);
+                float dq = s.x * qq.x;
+                dq = fmaf(s.y, qq.y, dq);
+                dq = fmaf(s.z, qq.z, dq);
+                dq = fmaf(s.w, qq.w, dq);
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) {
+                    dk += __shfl_xor_sync(0xffffffffu, dk, o);
+                    dq += __shfl_xor_sync(0xffffffffu, dq, o);
+                }
+                const float delta = beta * (v_s[row] - g * dk);
+                s.x = fmaf(delta, kk.x, g * s.x);
+                s.y = fmaf(delta, kk.y, g * s.y);
+                s.z = fmaf(delta, kk.z, g * s.z);
+                s.w = fmaf(delta, kk.w, g * s.w);
+                *sp = s;
+                if (cl == 0) y_s[row] = fmaf(delta, kq, g * dq);
+            }
+            fence_proxy_async_smem();
+        }
+        __syncthreads();
+        if (ok && tid == 0) {
+            bulk_store(gstate + (size_t)ch * rc * DK, S + (size_t)ch * rc * DK, chunk_bytes);
+            bulk_commit();
+        }
+    }
+
+    if (ok_all)
+        for (int i = tid; i < R; i += kThreads) yrow[i] = f32_to_bf16(y_s[i]);
+
+    // ---- new conv_state: rank 0 writes the shared q/k channels after every
+    // CTA of the cluster has read them; each CTA writes its own v channels.
+    cluster_wait_acquire();
+    const int n = p.K - 1;
+    if (has_qk && rank == 0) {
+        uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c_qk;
+        for (int j = 0; j < n; ++j) cs[(size_t)j * p.C] = nw_qk[j];
+    }
+    if (has_v) {
+        uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c_v;
+        for (int j = 0; j < n; ++j) cs[(size_t)j * p.C] = nw_v[j];
+    }
+    if (tid == 0) bulk_wait_all();
+}
+
+template <int DK>
+cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t st) {
+    const int G = p.Hv / p.Hk;
+    const int R = p.Dv / p.SN;
+    const size_t smem = (size_t)R * DK * sizeof(float);
+    static bool attr_set[2] = {false, false};   // per instantiation; benign race
+    if (!attr_set[0]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(kMaxRows * DK * sizeof(float)));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(decode_kernel<DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        attr_set[0] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G * p.SN, p.Hk, p.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G * p.SN;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<DK>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
+                          const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
+                          float *state, const uint8_t *row_mask, uint16_t *y, unsigned *err, cudaStream_t st) {
+    const int G = s.Hv / s.Hk;
+    // split each head's rows over SN CTAs until the grid covers the GPU twice,
+    // keeping >= 16 rows per CTA and clusters of at most 8 CTAs (16 if G = 16)
+    int SN = 1;
+    const long heads = (long)s.B * s.Hv;
+    while (SN * 2 <= s.Dv / 16 && G * SN * 2 <= 8 && heads * SN < 2L * num_sms()) SN *= 2;
+    DecodeParams p{qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y, err,
+                   s.B, s.Hk, s.Hv, s.Dv, s.C(), s.K, SN, s.eps};
+    switch (s.Dk) {
+        case 32: return launch_decode_t<32>(p, st);
+        case 64: return launch_decode_t<64>(p, st);
+        case 128: return launch_decode_t<128>(p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gdn

@@ -1,0 +1,46 @@
+// Host-side launchers of the GB300 kernels (one translation unit each), called
+// by the C ABI in api.cu after argument validation.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+struct Sizes {
+    int B, T, Hk, Hv, Dk, Dv, K;
+    float eps;
+    int C() const { return 2 * Hk * Dk + Hv * Dv; }
+};
+
+int num_sms();  // SMs of the current device (cached per device)
+
+cudaError_t launch_conv_update(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
+                               const uint8_t *mask, uint16_t *q, uint16_t *k, uint16_t *v, cudaStream_t st);
+
+cudaError_t launch_gating(const Sizes &s, const uint16_t *a, const uint16_t *b, const float *A_log,
+                          const float *dt_bias, float *g, float *beta, cudaStream_t st);
+
+cudaError_t launch_decode(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
+                          const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
+                          float *state, const uint8_t *row_mask, uint16_t *y, unsigned *err, cudaStream_t st);
+
+// Encodes a 2-D row-major bf16/f32 tensor map (rows x cols, box rows x box_cols).
+bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                    uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols);
+
+cudaError_t launch_prefill_seq(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               const float *g, const float *beta, const float *state_in, float *state_out,
+                               const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st);
+
+size_t prefill_chunked_workspace(const Sizes &s);
+
+cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                   const float *g, const float *beta, const float *state_in, float *state_out,
+                                   const uint8_t *mask, uint16_t *y, void *ws, unsigned *err, cudaStream_t st);
+
+}  // namespace gdn

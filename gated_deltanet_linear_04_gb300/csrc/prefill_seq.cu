@@ -1,0 +1,285 @@
+// Sequential-form prefill: the gated delta rule run step by step with the
+// state resident in registers for all T steps.
+//
+// Definition: "mlx-bun 0.4.0 -> 1.0.0, package/src/model/qwen3-delta.ts",
+// gated_delta_step and its masked specialization (state rows per dv, decay,
+// kv_mem, delta, update, output; a masked step writes y = 0 and skips the
+// update); "mlex 0.1.2, src/models/gated_delta.rs", the per-timestep loop.
+//
+// A CTA (4 warps) owns R = 16*RPL rows of one (b, hv) state.  Lane (rg, cg) of
+// warp w holds rows w*4*RPL + rg*RPL + i (i < RPL) and columns
+// [cg*Dk/8, (cg+1)*Dk/8), so a row's dot products are shuffle sums over the 8
+// lanes that share rg.  q/k/v tiles of 64 steps are staged in shared memory by
+// 2-D TMA loads (double buffered, one mbarrier per stage); g, beta and the mask
+// are gathered by plain loads one chunk ahead.  k.q per step is precomputed for
+// the chunk so that y = g (S.q) + delta (k.q) needs no second reduction.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTC = 64;   // steps per staged chunk
+
+struct SeqParams {
+    const float *g, *beta, *state_in;
+    float *state_out;
+    const uint8_t *mask;
+    uint16_t *y;
+    unsigned *err;
+    int B, T, Hk, Hv, Dv;
+};
+
+__host__ __device__ constexpr int align128(int x) { return (x + 127) & ~127; }
+
+template <int DK, int R>
+struct SeqSmem {
+    static constexpr int q_off = 0;
+    static constexpr int k_off = q_off + align128(kTC * DK * 2);
+    static constexpr int v_off = k_off + align128(kTC * DK * 2);
+    static constexpr int g_off = v_off + align128(kTC * R * 2);
+    static constexpr int b_off = g_off + kTC * 4;
+    static constexpr int kq_off = b_off + kTC * 4;
+    static constexpr int m_off = kq_off + kTC * 4;
+    static constexpr int stage_bytes = align128(m_off + kTC * 4);
+    static constexpr int y_off = 2 * stage_bytes;
+    static constexpr int total = y_off + kTC * R * 4;
+    static constexpr uint32_t tx_bytes = (uint32_t)(2 * kTC * DK * 2 + kTC * R * 2);
+};
+
+template <int CW>
+__device__ __forceinline__ void load_row_bf16(const uint16_t *p, float (&o)[CW]) {
+    static_assert(CW % 4 == 0, "");
+#pragma unroll
+    for (int j = 0; j < CW; j += 4) {
+        const uint2 r = *reinterpret_cast<const uint2 *>(p + j);
+        o[j + 0] = __uint_as_float(r.x << 16);
+        o[j + 1] = __uint_as_float(r.x & 0xffff0000u);
+        o[j + 2] = __uint_as_float(r.y << 16);
+        o[j + 3] = __uint_as_float(r.y & 0xffff0000u);
+    }
+}
+
+template <int DK, int RPL>
+__global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                               const __grid_constant__ CUtensorMap tm_k,
+                                                               const __grid_constant__ CUtensorMap tm_v,
+                                                               const SeqParams p) {
+    constexpr int R = 16 * RPL;
+    constexpr int CW = DK / 8;
+    using L = SeqSmem<DK, R>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full_bar[2];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rg = lane >> 3, cg = lane & 7;
+    const int nslice = p.Dv / R;
+    const int slice = blockIdx.x % nslice;
+    const int hv = blockIdx.x / nslice;
+    const int b = blockIdx.y;
+    const int G = p.Hv / p.Hk;
+    const int hk = hv / G;
+    const int r0 = slice * R;
+    const int T = p.T;
+
+    if (tid == 0) {
+        mbar_init(&full_bar[0], 1);
+        mbar_init(&full_bar[1], 1);
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+
+    // state slice -> registers
+    float s[RPL][CW];
+    const size_t head_off = ((size_t)b * p.Hv + hv) * p.Dv;
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+        const int row = r0 + warp * 4 * RPL + rg * RPL + i;
+        if (p.state_in != nullptr) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.state_in + (head_off + row) * DK + cg * CW);
+#pragma unroll
+            for (int j = 0; j < CW / 4; ++j) {
+                const float4 x = src[j];
+                s[i][4 * j] = x.x;
+                s[i][4 * j + 1] = x.y;
+                s[i][4 * j + 2] = x.z;
+                s[i][4 * j + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < CW; ++j) s[i][j] = 0.0f;
+        }
+    }
+    __syncthreads();
+
+    const int nchunks = (T + kTC - 1) / kTC;
+    auto issue = [&](int c, int st) {
+        unsigned char *base = smem + st * L::stage_bytes;
+        if (tid == 0) {
+            mbar_expect_tx(&full_bar[st], L::tx_bytes);
+            const int row = b * T + c * kTC;
+            tma_load_2d(base + L::q_off, &tm_q, hk * DK, row, &full_bar[st]);
+            tma_load_2d(base + L::k_off, &tm_k, hk * DK, row, &full_bar[st]);
+            tma_load_2d(base + L::v_off, &tm_v, hv * p.Dv + r0, row, &full_bar[st]);
+        }
+        if (tid < kTC) {
+            const int t = c * kTC + tid;
+            float gg = 1.0f, bb = 0.0f;
+            int m = 0;
+            if (t < T) {
+                const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
+                gg = p.g[gi];
+                bb = p.beta[gi];
+                m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
+            }
+            reinterpret_cast<float *>(base + L::g_off)[tid] = gg;
+            reinterpret_cast<float *>(base + L::b_off)[tid] = bb;
+            reinterpret_cast<int *>(base + L::m_off)[tid] = m;
+        }
+    };
+
+    if (nchunks > 0) issue(0, 0);
+    float *y_s = reinterpret_cast<float *>(smem + L::y_off);
+    bool ok_all = true;
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int st = c & 1;
+        unsigned char *base = smem + st * L::stage_bytes;
+        if (c + 1 < nchunks) issue(c + 1, st ^ 1);
+        bool ok = mbar_wait(&full_bar[st], (uint32_t)((c >> 1) & 1), p.err);
+        ok = __syncthreads_and(ok) != 0;
+        if (!ok) {
+            ok_all = false;
+            break;
+        }
+        const uint16_t *qs = reinterpret_cast<const uint16_t *>(base + L::q_off);
+        const uint16_t *ks = reinterpret_cast<const uint16_t *>(base + L::k_off);
+        const uint16_t *vs = reinterpret_cast<const uint16_t *>(base + L::v_off);
+        const float *gs = reinterpret_cast<const float *>(base + L::g_off);
+        const float *bs = reinterpret_cast<const float *>(base + L::b_off);
+        float *kqs = reinterpret_cast<float *>(base + L::kq_off);
+        const int *ms = reinterpret_cast<const int *>(base + L::m_off);
+        const int nt = min(kTC, T - c * kTC);
+
+        // k.q per step of the chunk
+        for (int t = warp; t < nt; t += kThreads / 32) {
+            float acc = 0.0f;
+            for (int j = lane; j < DK; j += 32)
+                acc = fmaf(bf16_to_f32(ks[t * DK + j]), bf16_to_f32(qs[t * DK + j]), acc);
+            acc = warp_sum(acc);
+            if (lane == 0) kqs[t] = acc;
+        }
+        __syncthreads();
+
+        for (int t = 0; t < nt; ++t) {
+            if (ms[t] == 0) {
+                if (cg == 0) {
+#pragma unroll
+                    for (int i = 0; i < RPL; ++i) y_s[t * R + warp * 4 * RPL + rg * RPL + i] = 0.0f;
+                }
+                continue;
+            }
+            const float g = gs[t], beta = bs[t], kq = kqs[t];
+            float kf[CW], qf[CW];
+            load_row_bf16<CW>(ks + t * DK + cg * CW, kf);
+            load_row_bf16<CW>(qs + t * DK + cg * CW, qf);
+            float dk[RPL], dq[RPL];
+#pragma unroll
+            for (int i = 0; i < RPL; ++i) {
+                float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+                for (int j = 0; j < CW; j += 2) {
+                    a0 = fmaf(s[i][j], kf[j], a0);
+                    a1 = fmaf(s[i][j + 1], kf[j + 1], a1);
+                    b0 = fmaf(s[i][j], qf[j], b0);
+                    b1 = fmaf(s[i][j + 1], qf[j + 1], b1);
+                }
+                dk[i] = a0 + a1;
+                dq[i] = b0 + b1;
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+                for (int i = 0; i < RPL; ++i) {
+                    dk[i] += __shfl_xor_sync(0xffffffffu, dk[i], o);
+                    dq[i] += __shfl_xor_sync(0xffffffffu, dq[i], o);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RPL; ++i) {
+                const int rl = warp * 4 * RPL + rg * RPL + i;
+                const float vv = bf16_to_f32(vs[t * R + rl]);
+                const float delta = beta * (vv - g * dk[i]);
+#pragma unroll
+                for (int j = 0; j < CW; ++j) s[i][j] = fmaf(delta, kf[j], g * s[i][j]);
+                if (cg == 0) y_s[t * R + rl] = fmaf(delta, kq, g * dq[i]);
+            }
+        }
+        __syncthreads();
+
+        // y tile -> global (bf16), R contiguous outputs per step
+        for (int idx = tid; idx < nt * (R / 2); idx += kThreads) {
+            const int t = idx / (R / 2), pr = idx % (R / 2);
+            const uint32_t packed = (uint32_t)f32_to_bf16(y_s[t * R + 2 * pr]) |
+                                    ((uint32_t)f32_to_bf16(y_s[t * R + 2 * pr + 1]) << 16);
+            uint16_t *dst = p.y + (((size_t)b * T + c * kTC + t) * p.Hv + hv) * p.Dv + r0 + 2 * pr;
+            *reinterpret_cast<uint32_t *>(dst) = packed;
+        }
+    }
+
+    if (!ok_all) return;
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) {
+        const int row = r0 + warp * 4 * RPL + rg * RPL + i;
+        float4 *dst = reinterpret_cast<float4 *>(p.state_out + (head_off + row) * DK + cg * CW);
+#pragma unroll
+        for (int j = 0; j < CW / 4; ++j)
+            dst[j] = make_float4(s[i][4 * j], s[i][4 * j + 1], s[i][4 * j + 2], s[i][4 * j + 3]);
+    }
+}
+
+template <int DK, int RPL>
+cudaError_t launch_seq_t(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const SeqParams &p, cudaStream_t st) {
+    constexpr int R = 16 * RPL;
+    using L = SeqSmem<DK, R>;
+    CUtensorMap tq, tk, tv;
+    const uint64_t rows = (uint64_t)s.B * (uint64_t)(s.T > 0 ? s.T : 1);
+    if (!encode_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * DK, kTC, DK) ||
+        !encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * DK, kTC, DK) ||
+        !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * s.Dv, kTC, R))
+        return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_seq_kernel<DK, RPL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid(s.Hv * (s.Dv / R), s.B);
+    prefill_seq_kernel<DK, RPL><<<grid, kThreads, L::total, st>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_seq(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               const float *g, const float *beta, const float *state_in, float *state_out,
+                               const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st) {
+    SeqParams p{g, beta, state_in, state_out, mask, y, err, s.B, s.T, s.Hk, s.Hv, s.Dv};
+    // 32-row CTAs when there are enough of them to fill the GPU, else 16-row
+    const long ctas32 = (long)s.B * s.Hv * (s.Dv / 32);
+    const bool small = ctas32 < num_sms();
+    switch (s.Dk) {
+        case 32: return small ? launch_seq_t<32, 1>(s, q, k, v, p, st) : launch_seq_t<32, 2>(s, q, k, v, p, st);
+        case 64: return small ? launch_seq_t<64, 1>(s, q, k, v, p, st) : launch_seq_t<64, 2>(s, q, k, v, p, st);
+        case 128:
+            return small ? launch_seq_t<128, 1>(s, q, k, v, p, st) : launch_seq_t<128, 2>(s, q, k, v, p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gdn

@@ -1,0 +1,202 @@
+"""Thin Python binding of the C ABI in include/gdn.h (ctypes).
+
+Argument marshalling only: every function here checks tensor dtypes, devices
+and contiguity, passes raw device pointers and the current CUDA stream to the
+library, and raises ``GdnError`` on a non-zero status.  All arithmetic runs in
+the CUDA kernels of libgdn.so; there is no fallback.  PyTorch provides device
+memory and streams.
+
+The functions named like the ABI (``gdn_conv_update`` ...) take
+caller-allocated outputs; the short names (``conv_update`` ...) allocate
+outputs with torch and return them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libgdn.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = range(5)
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32),
+                ("Dk", ctypes.c_int32), ("Dv", ctypes.c_int32), ("K", ctypes.c_int32), ("eps_qk", ctypes.c_float)]
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_SIGS = {
+    "gdn_conv_update": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gdn_gating": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P]),
+    "gdn_recurrent_decode": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gdn_prefill": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
+                                   ctypes.c_size_t, _P]),
+    "gdn_prefill_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims), ctypes.c_int]),
+    "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gdn_device_status": (ctypes.c_int, [_P]),
+    "gdn_abi_version": (ctypes.c_int, []),
+}
+
+
+def lib():
+    """The loaded libgdn.so.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libgdn.so is not built (%s); run __graft_entry__.build() first" % LIB_PATH)
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+def make_dims(d) -> GdnDims:
+    return GdnDims(int(d.B), int(d.T), int(d.Hk), int(d.Hv), int(d.Dk), int(d.Dv), int(d.K),
+                   float(getattr(d, "eps_qk", 1e-6)))
+
+
+def _ptr(t: Optional[torch.Tensor], dtype: torch.dtype, name: str):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor or None" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.numel() > 0 and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr() or None
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _check(status: int, where: str):
+    if status != GDN_OK:
+        raise GdnError(status, where)
+
+
+BF16, F32, U8 = torch.bfloat16, torch.float32, torch.uint8
+
+
+# ---------------------------------------------------------------------------
+# ABI-named calls (caller-allocated outputs)
+# ---------------------------------------------------------------------------
+def gdn_conv_update(dims, qkv, conv_w, conv_state, mask, q, k, v, stream=None):
+    d = make_dims(dims)
+    _check(lib().gdn_conv_update(ctypes.byref(d), _ptr(qkv, BF16, "qkv"), _ptr(conv_w, BF16, "conv_w"),
+                                 _ptr(conv_state, BF16, "conv_state"), _ptr(mask, U8, "mask"), _ptr(q, BF16, "q"),
+                                 _ptr(k, BF16, "k"), _ptr(v, BF16, "v"), _stream(stream)), "gdn_conv_update")
+
+
+def gdn_gating(dims, a, b, A_log, dt_bias, g, beta, stream=None):
+    d = make_dims(dims)
+    _check(lib().gdn_gating(ctypes.byref(d), _ptr(a, BF16, "a"), _ptr(b, BF16, "b"), _ptr(A_log, F32, "A_log"),
+                            _ptr(dt_bias, F32, "dt_bias"), _ptr(g, F32, "g"), _ptr(beta, F32, "beta"),
+                            _stream(stream)), "gdn_gating")
+
+
+def gdn_recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y, stream=None):
+    d = make_dims(dims)
+    _check(lib().gdn_recurrent_decode(ctypes.byref(d), _ptr(qkv, BF16, "qkv"), _ptr(conv_w, BF16, "conv_w"),
+                                      _ptr(conv_state, BF16, "conv_state"), _ptr(a, BF16, "a"), _ptr(b, BF16, "b"),
+                                      _ptr(A_log, F32, "A_log"), _ptr(dt_bias, F32, "dt_bias"),
+                                      _ptr(state, F32, "state"), _ptr(row_mask, U8, "row_mask"),
+                                      _ptr(y, BF16, "y"), _stream(stream)), "gdn_recurrent_decode")
+
+
+def gdn_prefill_workspace_size(dims, chunk: int) -> int:
+    d = make_dims(dims)
+    return int(lib().gdn_prefill_workspace_size(ctypes.byref(d), int(chunk)))
+
+
+def gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, workspace=None, stream=None):
+    d = make_dims(dims)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ws_ptr = None if workspace is None else (workspace.data_ptr() or None)
+    _check(lib().gdn_prefill(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
+                             _ptr(g, F32, "g"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
+                             _ptr(state_out, F32, "state_out"), _ptr(mask, U8, "mask"), _ptr(y, BF16, "y"),
+                             int(chunk), ws_ptr, ws_bytes, _stream(stream)), "gdn_prefill")
+
+
+def gdn_device_status(stream=None) -> int:
+    return int(lib().gdn_device_status(_stream(stream)))
+
+
+def gdn_abi_version() -> int:
+    return int(lib().gdn_abi_version())
+
+
+# ---------------------------------------------------------------------------
+# allocating conveniences
+# ---------------------------------------------------------------------------
+def conv_update(dims, qkv, conv_w, conv_state=None, mask=None, stream=None):
+    """Returns (q, k, v); conv_state (if given) is updated in place."""
+    dev = qkv.device
+    q = torch.empty((dims.B, dims.T, dims.Hk, dims.Dk), dtype=BF16, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty((dims.B, dims.T, dims.Hv, dims.Dv), dtype=BF16, device=dev)
+    gdn_conv_update(dims, qkv, conv_w, conv_state, mask, q, k, v, stream)
+    return q, k, v
+
+
+def gating(dims, a, b, A_log, dt_bias, stream=None):
+    g = torch.empty((dims.B, dims.T, dims.Hv), dtype=F32, device=a.device)
+    beta = torch.empty_like(g)
+    gdn_gating(dims, a, b, A_log, dt_bias, g, beta, stream)
+    return g, beta
+
+
+def recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask=None, stream=None):
+    """One token; conv_state and state are updated in place.  Returns y [B, Hv, Dv]."""
+    y = torch.empty((dims.B, dims.Hv, dims.Dv), dtype=BF16, device=qkv.device)
+    gdn_recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y, stream)
+    return y
+
+
+def prefill(dims, q, k, v, g, beta, state_in=None, mask=None, chunk=0, state_out=None, stream=None):
+    """Returns (y, state_out)."""
+    dev = q.device
+    y = torch.empty((dims.B, dims.T, dims.Hv, dims.Dv), dtype=BF16, device=dev)
+    if state_out is None:
+        state_out = torch.empty((dims.B, dims.Hv, dims.Dv, dims.Dk), dtype=F32, device=dev)
+    nws = gdn_prefill_workspace_size(dims, chunk)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
+    gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk, ws, stream)
+    return y, state_out
+
+
+def core_prefill(dims, qkv, conv_w, a, b, A_log, dt_bias, conv_state=None, state_in=None, mask=None, chunk=0,
+                 stream=None):
+    """conv -> gates -> recurrence; returns (y, state_out).  conv_state (if
+    given) is updated in place."""
+    q, k, v = conv_update(dims, qkv, conv_w, conv_state, mask, stream)
+    g, beta = gating(dims, a, b, A_log, dt_bias, stream)
+    return prefill(dims, q, k, v, g, beta, state_in, mask, chunk, None, stream)

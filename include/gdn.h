@@ -1,0 +1,157 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet layer core.
+ *
+ * The core is the linear-attention block of Qwen3-Next / Qwen3.5-style models
+ * as defined by "mlex 0.1.2, src/models/gated_delta.rs" (GatedDeltaNet::load and
+ * GatedDeltaNet::forward) and by "mlx-bun 0.4.0 -> 1.0.0,
+ * package/src/model/qwen3-delta.ts" (the numerics table at its head, the
+ * gated_delta_step kernel and its masked specialization, computeG,
+ * gatedDeltaUpdate):
+ *
+ *   conv window   X = [conv_state || qkv] along time, conv_state' = last K-1 rows
+ *   conv + SiLU   u[t,c] = sum_j w[c,j] X[t+j,c] (tap K-1 = current token); x = u*sigmoid(u)
+ *   q/k norm      q = rms(x_q)/Dk, k = rms(x_k)/sqrt(Dk), v = x_v; rms(x) = x/sqrt(mean(x^2)+eps)
+ *   gates         g = exp(-exp(A_log) * softplus(a + dt_bias)), beta = sigmoid(b)
+ *   recurrence    per (b, hv), hk = hv / (Hv/Hk):  S <- g S;  delta = beta (v - S k);
+ *                 S <- S + delta k^T;  y = S q          (S is [Dv, Dk], f32)
+ *   mask          a step with mask 0 writes zero y (and zero q/k/v), does not enter
+ *                 the conv window and leaves both states untouched.
+ *
+ * Conventions shared by every entry point
+ *   - Memory: every pointer is a DEVICE pointer owned by the caller.  The library
+ *     allocates nothing and keeps no state between calls except one device error
+ *     word per device (see gdn_device_status).
+ *   - Types: "bf16" buffers hold bfloat16 bit patterns (uint16_t); "f32" is IEEE
+ *     single.  Every tensor is dense and row-major with the shape given.
+ *   - Alignment: every tensor pointer must be 16-byte aligned, else
+ *     GDN_ERR_INVALID_ARG.
+ *   - Streams: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and the call returns without waiting.  Argument errors are
+ *     reported before anything is enqueued; GDN_ERR_CUDA reports a launch error.
+ *   - Supported sizes: Dk, Dv in {32, 64, 128}; Hv % Hk == 0; 2 <= K <= 4;
+ *     B, T >= 0 (a zero size is a no-op).  Others give GDN_ERR_UNSUPPORTED.
+ *   - Channel order of qkv / conv_state / conv_w: C = 2*Hk*Dk + Hv*Dv channels,
+ *     q heads [0, Hk*Dk), k heads [Hk*Dk, 2*Hk*Dk), v heads [2*Hk*Dk, C), each
+ *     head's channels contiguous.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols keep default visibility even when the library is built
+ * with hidden visibility. */
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+/* A cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st *gdn_stream;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, negative size, Hv % Hk != 0 */
+    GDN_ERR_UNSUPPORTED = 2,   /* a size outside the supported set above */
+    GDN_ERR_CUDA = 3,          /* a CUDA launch or attribute call failed */
+    GDN_ERR_TIMEOUT = 4        /* a bounded on-device wait gave up (see gdn_device_status) */
+} gdn_status;
+
+/* Problem sizes: the fields of GatedDeltaConfig (mlex gated_delta.rs) plus the
+ * batch B and the number of time steps T of this call.  eps_qk is the q/k
+ * rms-norm epsilon (1e-6 on the pages). */
+typedef struct gdn_dims {
+    int32_t B, T, Hk, Hv, Dk, Dv, K;
+    float eps_qk;
+} gdn_dims;
+
+/* Causal depthwise conv + SiLU + q/k rms-norm and scaling, with the rolling
+ * conv state.  (mlex gated_delta.rs, GatedDeltaNet::forward: the conv_state
+ * concat/slice, conv1d with groups = conv_dim, silu, split into q/k/v, rms_norm
+ * and the inv_scale factors.)
+ *   qkv        bf16 [B, T, C]      pre-conv input (in)
+ *   conv_w     bf16 [C, K]         depthwise weights, tap K-1 = current token (in)
+ *   conv_state bf16 [B, K-1, C]    in/out: the K-1 most recent valid raw inputs,
+ *                                  oldest first; NULL = zeros and not returned
+ *   mask       u8   [B, T]         nonzero = valid step; NULL = all valid
+ *   q, k       bf16 [B, T, Hk, Dk] out; v bf16 [B, T, Hv, Dv] out.  One
+ *                                  round-to-nearest-even rounding of the f32
+ *                                  result; masked steps are written as zeros.
+ * qkv must not alias any output. */
+GDN_API gdn_status gdn_conv_update(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
+                           uint16_t *conv_state, const uint8_t *mask,
+                           uint16_t *q, uint16_t *k, uint16_t *v, gdn_stream stream);
+
+/* Gates. (mlex gated_delta.rs, GatedDeltaNet::forward: beta and g; mlx-bun
+ * qwen3-delta.ts, computeG.)
+ *   a, b        bf16 [B, T, Hv] (in);  A_log, dt_bias f32 [Hv] (in)
+ *   g, beta     f32  [B, T, Hv] (out): g = exp(-exp(A_log) softplus(a + dt_bias)),
+ *               beta = sigmoid(b), softplus(x) = max(x,0) + log1p(exp(-|x|)). */
+GDN_API gdn_status gdn_gating(const gdn_dims *dims, const uint16_t *a, const uint16_t *b,
+                      const float *A_log, const float *dt_bias, float *g, float *beta,
+                      gdn_stream stream);
+
+/* One decode step (dims->T must be 1), fully fused: conv window + conv + SiLU
+ * + q/k norm, gates, and the recurrence step, in one kernel that streams the
+ * f32 state once.  (mlx-bun qwen3-delta.ts, gated_delta_step at T = 1;
+ * mlex gated_delta.rs, GatedDeltaNet::forward with a one-token input.)
+ *   qkv        bf16 [B, C] (in)            conv_w bf16 [C, K] (in)
+ *   conv_state bf16 [B, K-1, C] in/out (required)
+ *   a, b       bf16 [B, Hv] (in)           A_log, dt_bias f32 [Hv] (in)
+ *   state      f32  [B, Hv, Dv, Dk] in/out, updated in place
+ *   row_mask   u8   [B] or NULL: a zero row writes y = 0 and leaves both of its
+ *              states untouched
+ *   y          bf16 [B, Hv, Dv] (out)
+ * Supports Hv/Hk <= 16. */
+GDN_API gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
+                                uint16_t *conv_state, const uint16_t *a, const uint16_t *b,
+                                const float *A_log, const float *dt_bias, float *state,
+                                const uint8_t *row_mask, uint16_t *y, gdn_stream stream);
+
+/* The recurrence over T steps (prefill).  (mlx-bun qwen3-delta.ts,
+ * gatedDeltaUpdate and the gated_delta_step kernel with its masked
+ * specialization; mlex gated_delta.rs, the per-timestep loop.)
+ *   q, k       bf16 [B, T, Hk, Dk] (in)    v bf16 [B, T, Hv, Dv] (in)
+ *   g, beta    f32  [B, T, Hv] (in)
+ *   state_in   f32  [B, Hv, Dv, Dk] or NULL (= zeros)
+ *   state_out  f32  [B, Hv, Dv, Dk] (out); may equal state_in
+ *   mask       u8   [B, T] or NULL
+ *   y          bf16 [B, T, Hv, Dv] (out)
+ *   chunk      0 = sequential form (state resident on chip across all T);
+ *              64 = chunked (WY / UT-transform) form on the tensor cores
+ *   workspace  device scratch of at least gdn_prefill_workspace_size() bytes,
+ *              16-byte aligned (may be NULL when that size is 0)
+ */
+GDN_API gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
+                       const uint16_t *v, const float *g, const float *beta,
+                       const float *state_in, float *state_out, const uint8_t *mask,
+                       uint16_t *y, int chunk, void *workspace, size_t ws_bytes,
+                       gdn_stream stream);
+
+/* Bytes of scratch gdn_prefill needs for these sizes and this chunk mode
+ * (0 for the sequential form).  Returns 0 for unsupported arguments. */
+GDN_API size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk);
+
+/* Human-readable name of a status code (static storage). */
+GDN_API const char *gdn_status_string(gdn_status status);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word, which a kernel sets when one of its bounded waits (on an mbarrier or
+ * a tensor-core commit) gives up.  Returns GDN_OK, GDN_ERR_TIMEOUT, or
+ * GDN_ERR_CUDA if the synchronisation itself failed. */
+GDN_API gdn_status gdn_device_status(gdn_stream stream);
+
+/* ABI version of this header (incremented on any signature change). */
+GDN_API int gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

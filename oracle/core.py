@@ -357,7 +357,7 @@ def decode(d, steps_inputs, conv_w_bits, A_log, dt_bias, conv_state_bits, state_
     """Carried single-token steps: each step is ``core`` with T = 1, the conv
     state carried as bf16 and the recurrent state carried as f32 (the storage
     types of the cache slots).  steps_inputs: list of dicts with qkv [B,1,C],
-    a, b [B,1,Hv] bf16 bits.  Returns (list of y_bf16 [B,Hv,Dv], state f64,
+    a, b [B,1,Hv] bf16 bits.  Returns (list of y [B,Hv,Dv] float64, state f64,
     conv_state bits)."""
     d1 = d.with_(T=1)
     cs = None if conv_state_bits is None else np.array(conv_state_bits, copy=True)
@@ -367,7 +367,7 @@ def decode(d, steps_inputs, conv_w_bits, A_log, dt_bias, conv_state_bits, state_
     for inp in steps_inputs:
         out = layer_core(d1, inp["qkv"], conv_w_bits, inp["a"], inp["b"], A_log, dt_bias, cs, st, mask,
                    pairs, threads)
-        ys.append(out["y_bf16"][:, 0])
+        ys.append(out["y"][:, 0])
         st = round_f32(out["state"])
         if pairs is None:
             cs = out["conv_state"]

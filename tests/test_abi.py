@@ -1,0 +1,102 @@
+"""The C-ABI library loads, exports every entry point declared in
+include/gdn.h, and rejects bad arguments on the host before any CUDA call
+(no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_linear_04_gb300.build import build_library
+    build_library()
+    from gated_deltanet_linear_04_gb300 import gdn
+    return gdn.lib()
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", txt)
+
+
+def test_header_declares_the_abi():
+    names = set(declared_functions())
+    for n in ("gdn_conv_update", "gdn_gating", "gdn_recurrent_decode", "gdn_prefill",
+              "gdn_prefill_workspace_size", "gdn_status_string", "gdn_device_status", "gdn_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), "libgdn.so does not export " + n
+
+
+def test_status_strings(lib):
+    from gated_deltanet_linear_04_gb300 import gdn
+    assert gdn.status_string(0) == "GDN_OK"
+    for s in range(1, 5):
+        assert gdn.status_string(s).startswith("GDN_ERR_")
+    assert gdn.gdn_abi_version() == 1
+
+
+def _dims(**kw):
+    from gated_deltanet_linear_04_gb300 import gdn
+    base = dict(B=1, T=8, Hk=1, Hv=2, Dk=32, Dv=32, K=4, eps_qk=1e-6)
+    base.update(kw)
+    return gdn.GdnDims(**base)
+
+
+def _call(lib, name, d, n_ptrs, extra=()):
+    f = getattr(lib, name)
+    return f(ctypes.byref(d), *([None] * n_ptrs), *extra)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({}, 1),                       # null pointers on non-empty tensors
+    ({"Hv": 3}, 1),                # Hv % Hk != 0
+    ({"T": -1}, 1),
+    ({"Dk": 48}, 2),               # unsupported head size
+    ({"Dv": 256}, 2),
+    ({"K": 5}, 2),
+    ({"K": 1}, 2),
+])
+def test_host_validation(lib, kw, expect):
+    d = _dims(**kw)
+    assert _call(lib, "gdn_gating", d, 6, (None,)) == expect
+    assert _call(lib, "gdn_conv_update", d, 7, (None,)) == expect
+
+
+def test_decode_requires_single_step_and_small_groups(lib):
+    d = _dims(T=2)
+    assert _call(lib, "gdn_recurrent_decode", d, 10, (None,)) == 1
+    d = _dims(T=1, Hk=1, Hv=32)
+    assert _call(lib, "gdn_recurrent_decode", d, 10, (None,)) == 2     # Hv/Hk > 16
+
+
+def test_misaligned_pointer_rejected(lib):
+    d = _dims(B=1, T=1)
+    buf = ctypes.create_string_buffer(64)
+    mis = ctypes.addressof(buf) | 1
+    f = lib.gdn_gating
+    assert f(ctypes.byref(d), mis, mis, mis, mis, mis, mis, None) == 1
+
+
+def test_empty_sizes_are_noops(lib):
+    d = _dims(B=0)
+    assert _call(lib, "gdn_gating", d, 6, (None,)) == 0
+    assert _call(lib, "gdn_conv_update", d, 7, (None,)) == 0
+    d = _dims(T=0)
+    assert _call(lib, "gdn_gating", d, 6, (None,)) == 0
+
+
+def test_prefill_chunk_argument(lib):
+    d = _dims()
+    f = lib.gdn_prefill
+    assert f(ctypes.byref(d), *([None] * 9), 32, None, 0, None) == 2    # unsupported chunk size
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 0) == 0

@@ -1,0 +1,292 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small cases compare every output element; the full-size workloads compare
+sampled (b, hv) heads, which the oracle computes one by one, plus properties
+that hold at any size (padded outputs are exactly zero, the conv state holds
+the last raw inputs).  Tolerances: y (bf16) max abs <= 2e-2 and rel L2 <= 1%;
+f32 state rel L2 <= 1e-3; masks, zeros and conv_state copies bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_linear_04_gb300 import workloads as wl
+from tests import _util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    from gated_deltanet_linear_04_gb300.build import build_library
+    build_library()
+    from gated_deltanet_linear_04_gb300 import gdn as g
+    assert torch.cuda.is_available(), "these tests need a GPU"
+    torch.cuda.set_device(0)
+    return g
+
+
+DEV = "cuda:0"
+
+
+def make_mask(kind, B, T, seed):
+    g = torch.Generator().manual_seed(seed)
+    if kind is None:
+        return None
+    if kind == "random":
+        return (torch.rand((B, T), generator=g) < 0.6).to(torch.uint8)
+    if kind == "sparse":
+        return (torch.rand((B, T), generator=g) < 0.04).to(torch.uint8)
+    if kind in ("left", "right"):
+        lens = torch.randint(0, T + 1, (B,), generator=g)
+        t = torch.arange(T)[None, :]
+        m = (t < lens[:, None]) if kind == "right" else (t >= (T - lens)[:, None])
+        return m.to(torch.uint8)
+    if kind == "allmasked_row":
+        m = (torch.rand((B, T), generator=g) < 0.5).to(torch.uint8)
+        m[0] = 0
+        return m
+    raise ValueError(kind)
+
+
+def inputs_for(d, seed, conv_state="normal", state="normal"):
+    p = wl.make_params(d, seed)
+    a = wl.make_activations(d, seed + 1)
+    s = wl.make_states(d, seed + 2, "normal" if conv_state == "none" else conv_state, state)
+    out = dict(p, **a, **s)
+    if conv_state == "none":
+        out["conv_state"] = None
+    return out
+
+
+def to_dev(x):
+    return None if x is None else x.to(DEV)
+
+
+def np_mask(m):
+    return None if m is None else m.numpy()
+
+
+# ---------------------------------------------------------------------------
+# a4 gates
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,T,Hv", [(1, 8, 2), (3, 77, 32), (2, 1, 64), (1, 1000, 5)])
+def test_gating(gdn, B, T, Hv):
+    d = wl.Dims(B=B, T=T, Hk=1, Hv=Hv, Dk=32, Dv=32)
+    inp = inputs_for(d, 11 + T)
+    a = (torch.randn((B, T, Hv), generator=torch.Generator().manual_seed(T)) * 4).to(torch.bfloat16)
+    g, beta = gdn.gating(d, to_dev(a), to_dev(inp["b"]), to_dev(inp["A_log"]), to_dev(inp["dt_bias"]))
+    gr, br = oracle.gating(U.bits(a), U.bits(inp["b"]), inp["A_log"].numpy(), inp["dt_bias"].numpy())
+    assert np.allclose(g.cpu().numpy(), gr, rtol=2e-6, atol=1e-30)
+    assert np.allclose(beta.cpu().numpy(), br, rtol=2e-6, atol=1e-30)
+
+
+# ---------------------------------------------------------------------------
+# a1-a3 conv window + conv + SiLU + q/k norm (+ a6 mask)
+# ---------------------------------------------------------------------------
+CONV_CASES = [
+    # B, T, Hk, Hv, Dk, Dv, K, mask, conv_state
+    (1, 8, 1, 2, 32, 32, 4, None, "zeros"),
+    (2, 37, 2, 4, 64, 32, 4, "random", "normal"),
+    (2, 65, 1, 1, 128, 128, 3, "left", "normal"),
+    (3, 17, 2, 8, 32, 64, 2, "right", "none"),
+    (1, 1, 4, 8, 128, 64, 4, None, "normal"),
+    (2, 100, 2, 4, 128, 128, 4, "sparse", "normal"),
+    (2, 33, 1, 2, 64, 64, 4, "allmasked_row", "normal"),
+    (1, 300, 3, 6, 128, 32, 4, None, "normal"),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,Dk,Dv,K,mk,cs", CONV_CASES)
+def test_conv_update(gdn, B, T, Hk, Hv, Dk, Dv, K, mk, cs):
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, K=K)
+    inp = inputs_for(d, 100 + T, conv_state=cs)
+    mask = make_mask(mk, B, T, 7 + T)
+    cs_dev = to_dev(inp["conv_state"])
+    q, k, v = gdn.conv_update(d, to_dev(inp["qkv"]), to_dev(inp["conv_w"]), cs_dev, to_dev(mask))
+    torch.cuda.synchronize()
+    cs_bits = None if inp["conv_state"] is None else U.bits(inp["conv_state"])
+    qr, kr, vr, csr = oracle.conv_update(d, U.bits(inp["qkv"]), U.bits(inp["conv_w"]), cs_bits, np_mask(mask))
+    for name, got, ref in (("q", q, qr), ("k", k, kr), ("v", v, vr)):
+        gb = U.bits(got)
+        U.assert_bf16_within_one_ulp(gb, ref, name)
+        if mask is not None:
+            assert np.all(gb[mask.numpy() == 0] == 0), name + ": masked steps must be exactly zero"
+    if cs_dev is not None:
+        assert np.array_equal(U.bits(cs_dev), csr), "conv_state must equal the last K-1 valid raw inputs"
+
+
+# ---------------------------------------------------------------------------
+# a5/a6 recurrence, sequential prefill
+# ---------------------------------------------------------------------------
+def recurrence_inputs(d, seed, mask=None, conv_state="normal"):
+    """q/k/v/g/beta produced by the oracle from synthetic layer inputs (the
+    shapes and scales the recurrence sees in the model); g and beta rounded
+    to f32, the device input type."""
+    inp = inputs_for(d, seed, conv_state=conv_state)
+    cs = None if inp["conv_state"] is None else U.bits(inp["conv_state"])
+    q, k, v, _ = oracle.conv_update(d, U.bits(inp["qkv"]), U.bits(inp["conv_w"]), cs, np_mask(mask))
+    g, beta = oracle.gating(U.bits(inp["a"]), U.bits(inp["b"]), inp["A_log"].numpy(), inp["dt_bias"].numpy())
+    g32, b32 = g.astype(np.float32), beta.astype(np.float32)
+    t = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    return {"q": t(q), "k": t(k), "v": t(v), "q_bits": q, "k_bits": k, "v_bits": v,
+            "g": torch.from_numpy(g32), "beta": torch.from_numpy(b32), "state": inp["state"]}
+
+
+SEQ_CASES = [
+    # B, T, Hk, Hv, Dk, Dv, mask, state
+    (1, 8, 1, 2, 32, 32, None, "zeros"),
+    (1, 1, 1, 1, 128, 128, None, "normal"),
+    (2, 63, 2, 4, 128, 128, "random", "normal"),
+    (1, 64, 1, 2, 64, 128, None, "normal"),
+    (2, 65, 2, 2, 128, 64, "right", "normal"),
+    (1, 130, 1, 4, 32, 32, "left", "normal"),
+    (2, 200, 4, 16, 128, 128, "allmasked_row", "normal"),
+    (3, 129, 1, 3, 64, 32, "sparse", "zeros"),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,Dk,Dv,mk,st", SEQ_CASES)
+def test_prefill_sequential(gdn, B, T, Hk, Hv, Dk, Dv, mk, st):
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv)
+    mask = make_mask(mk, B, T, 3 + T)
+    r = recurrence_inputs(d, 200 + T, mask)
+    state_in = r["state"] if st == "normal" else None
+    y, s_out = gdn.prefill(d, to_dev(r["q"]), to_dev(r["k"]), to_dev(r["v"]), to_dev(r["g"]), to_dev(r["beta"]),
+                           to_dev(state_in), to_dev(mask), chunk=0)
+    torch.cuda.synchronize()
+    s0 = None if state_in is None else state_in.numpy().astype(np.float64)
+    yr, sr = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                               r["beta"].numpy().astype(np.float64), s0, np_mask(mask))
+    yg = U.bf16_dev_to_f64(y)
+    U.assert_y_close(yg, yr)
+    U.assert_state_close(s_out.cpu().numpy(), sr)
+    if mask is not None:
+        assert np.all(U.bits(y)[mask.numpy() == 0] == 0), "padded y must be exactly zero"
+        for b in range(B):
+            if mask[b].sum() == 0:
+                ref = np.zeros_like(sr[b]) if s0 is None else state_in[b].numpy()
+                assert np.array_equal(s_out[b].cpu().numpy(), ref), "row without valid steps: state untouched"
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+
+
+def test_prefill_in_place_and_split_is_bitwise(gdn):
+    """state_out may alias state_in; running T1 then T2 steps equals T1+T2
+    steps bit for bit (the sequential form does the same arithmetic)."""
+    d = wl.Dims(B=2, T=150, Hk=2, Hv=4, Dk=128, Dv=128)
+    r = recurrence_inputs(d, 5)
+    full_y, full_s = gdn.prefill(d, *(to_dev(r[x]) for x in ("q", "k", "v", "g", "beta")), to_dev(r["state"]))
+    st = to_dev(r["state"]).clone()
+    ys = []
+    for lo, hi in ((0, 70), (70, 150)):
+        dd = d.with_(T=hi - lo)
+        sl = lambda x: to_dev(r[x][:, lo:hi].contiguous())
+        y, _ = gdn.prefill(dd, sl("q"), sl("k"), sl("v"), sl("g"), sl("beta"), st, None, 0, state_out=st)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(ys, 1), full_y)
+    assert torch.equal(st, full_s)
+
+
+# ---------------------------------------------------------------------------
+# the composed core (configuration "tiny" and masked variants)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("mk", [None, "right", "random"])
+def test_core_prefill_tiny(gdn, mk):
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.workload_inputs(w)
+    d = inp["dims"]
+    mask = make_mask(mk, d.B, d.T, 1)
+    cs = to_dev(inp["conv_state"]).clone()
+    y, s = gdn.core_prefill(d, to_dev(inp["qkv"]), to_dev(inp["conv_w"]), to_dev(inp["a"]), to_dev(inp["b"]),
+                            to_dev(inp["A_log"]), to_dev(inp["dt_bias"]), cs, to_dev(inp["state"]), to_dev(mask))
+    torch.cuda.synchronize()
+    ref = oracle.layer_core(d, U.bits(inp["qkv"]), U.bits(inp["conv_w"]), U.bits(inp["a"]), U.bits(inp["b"]),
+                            inp["A_log"].numpy(), inp["dt_bias"].numpy(), U.bits(inp["conv_state"]),
+                            inp["state"].numpy().astype(np.float64), np_mask(mask))
+    U.assert_y_close(U.bf16_dev_to_f64(y), ref["y"])
+    U.assert_state_close(s.cpu().numpy(), ref["state"])
+    assert np.array_equal(U.bits(cs), ref["conv_state"])
+
+
+def test_state_tolerance_after_4096_steps(gdn):
+    d = wl.Dims(B=1, T=4096, Hk=1, Hv=2, Dk=128, Dv=128)
+    inp = inputs_for(d, 4096)
+    y, s = gdn.core_prefill(d, to_dev(inp["qkv"]), to_dev(inp["conv_w"]), to_dev(inp["a"]), to_dev(inp["b"]),
+                            to_dev(inp["A_log"]), to_dev(inp["dt_bias"]), to_dev(inp["conv_state"]).clone(),
+                            to_dev(inp["state"]))
+    torch.cuda.synchronize()
+    ref = oracle.layer_core(d, U.bits(inp["qkv"]), U.bits(inp["conv_w"]), U.bits(inp["a"]), U.bits(inp["b"]),
+                            inp["A_log"].numpy(), inp["dt_bias"].numpy(), U.bits(inp["conv_state"]),
+                            inp["state"].numpy().astype(np.float64))
+    U.assert_y_close(U.bf16_dev_to_f64(y), ref["y"])
+    U.assert_state_close(s.cpu().numpy(), ref["state"])
+
+
+# ---------------------------------------------------------------------------
+# fused decode
+# ---------------------------------------------------------------------------
+def run_decode_gpu(gdn, d, inp, steps, row_mask=None):
+    cs = to_dev(inp["conv_state"]).clone()
+    st = to_dev(inp["state"]).clone()
+    ys = []
+    for sin in steps:
+        y = gdn.recurrent_decode(d.with_(T=1), to_dev(sin["qkv"][:, 0].contiguous()), to_dev(inp["conv_w"]), cs,
+                                 to_dev(sin["a"][:, 0].contiguous()), to_dev(sin["b"][:, 0].contiguous()),
+                                 to_dev(inp["A_log"]), to_dev(inp["dt_bias"]), st, to_dev(row_mask))
+        ys.append(y)
+    torch.cuda.synchronize()
+    return ys, st, cs
+
+
+DECODE_CASES = [
+    # B, Hk, Hv, Dk, Dv, K, steps, row mask
+    (1, 1, 2, 32, 32, 4, 6, False),
+    (3, 2, 4, 128, 128, 4, 5, True),
+    (2, 16, 32, 128, 128, 4, 3, False),
+    (2, 1, 16, 64, 64, 3, 4, False),      # G = 16: cluster of 16 CTAs
+    (5, 4, 8, 32, 128, 2, 4, True),
+    (1, 2, 16, 128, 64, 4, 3, False),
+]
+
+
+@pytest.mark.parametrize("B,Hk,Hv,Dk,Dv,K,n,rm", DECODE_CASES)
+def test_decode(gdn, B, Hk, Hv, Dk, Dv, K, n, rm):
+    d = wl.Dims(B=B, T=1, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, K=K)
+    inp = inputs_for(d, 300 + B * Hv)
+    steps = [wl.make_activations(d, 400 + i) for i in range(n)]
+    row_mask = None
+    if rm:
+        row_mask = torch.ones(B, dtype=torch.uint8)
+        row_mask[1::2] = 0
+    ys, st, cs = run_decode_gpu(gdn, d, inp, steps, row_mask)
+    sbits = [{k: U.bits(s[k]) for k in ("qkv", "a", "b")} for s in steps]
+    yr, sr, csr = oracle.decode(d, sbits, U.bits(inp["conv_w"]), inp["A_log"].numpy(), inp["dt_bias"].numpy(),
+                                U.bits(inp["conv_state"]), inp["state"].numpy().astype(np.float64),
+                                None if row_mask is None else row_mask.numpy())
+    for i in range(n):
+        U.assert_y_close(U.bf16_dev_to_f64(ys[i]), yr[i], "y step %d" % i)
+    U.assert_state_close(st.cpu().numpy(), sr)
+    assert np.array_equal(U.bits(cs), csr)
+    if row_mask is not None:
+        for b in range(B):
+            if row_mask[b] == 0:
+                assert torch.equal(st[b].cpu(), inp["state"][b]), "masked row: state untouched"
+                assert all(int(y[b].abs().max()) == 0 for y in ys)
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+
+
+def test_decode_steps_match_prefill(gdn):
+    """n single-token decode steps == one prefill over the same n tokens."""
+    d = wl.Dims(B=2, T=9, Hk=2, Hv=4, Dk=128, Dv=128)
+    inp = inputs_for(d, 77)
+    steps = [{k: inp[k][:, t:t + 1] for k in ("qkv", "a", "b")} for t in range(d.T)]
+    ys, st, cs = run_decode_gpu(gdn, d, inp, steps)
+    cs2 = to_dev(inp["conv_state"]).clone()
+    y, s = gdn.core_prefill(d, to_dev(inp["qkv"]), to_dev(inp["conv_w"]), to_dev(inp["a"]), to_dev(inp["b"]),
+                            to_dev(inp["A_log"]), to_dev(inp["dt_bias"]), cs2, to_dev(inp["state"]))
+    torch.cuda.synchronize()
+    U.assert_y_close(U.bf16_dev_to_f64(torch.stack(ys, 1)), U.bf16_dev_to_f64(y))
+    U.assert_state_close(st.cpu().numpy(), s.cpu().numpy().astype(np.float64), tol=1e-5)
+    assert torch.equal(cs, cs2)
