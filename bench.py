@@ -294,7 +294,7 @@ def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int) -> dict:
     mask = None
     n_valid = d.B * d.T
     if w.ragged:
-        lens = wl.make_lengths(d.B, w.len_lo, w.len_hi, 1000 + w.index + 104729)
+        lens = wl.workload_lengths(w)
         mask = wl.right_padded_mask(lens, d.T).to(dev)
         n_valid = int(lens.sum())
     conv_state = torch.zeros((d.B, d.K - 1, d.C), dtype=torch.bfloat16, device=dev)

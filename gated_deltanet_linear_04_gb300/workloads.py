@@ -142,6 +142,12 @@ def random_mask(B: int, T: int, p_valid: float, seed: int) -> torch.Tensor:
     return (torch.rand((B, T), generator=g) < p_valid).to(torch.uint8)
 
 
+def workload_lengths(w: Workload, dims: Optional[Dims] = None) -> torch.Tensor:
+    """Row lengths of a ragged workload (valid prefix of each row)."""
+    d = dims or w.dims
+    return make_lengths(d.B, min(w.len_lo, d.T), min(w.len_hi, d.T), 1000 + w.index + 104729)
+
+
 def workload_inputs(w: Workload, dims: Optional[Dims] = None) -> dict:
     """All per-call tensors of a workload (CPU). ``dims`` may shrink the workload
     (same distributions, other sizes) for parity tests."""
@@ -152,7 +158,7 @@ def workload_inputs(w: Workload, dims: Optional[Dims] = None) -> dict:
     out.update(make_activations(d, seed + 7919))
     out.update(make_states(d, seed + 15485863, w.conv_state, w.state))
     if w.ragged:
-        lens = make_lengths(d.B, min(w.len_lo, d.T), min(w.len_hi, d.T), seed + 104729)
+        lens = workload_lengths(w, d)
         out["lengths"] = lens
         out["mask"] = right_padded_mask(lens, d.T)
     else:

@@ -319,59 +319,109 @@ def recurrence(d, q_bits, k_bits, v_bits, g, beta, state_in=None, mask=None,
 
 
 # --------------------------------------------------------------------------
-# the whole core for a set of (b, hv) pairs: a1..a6
+# the whole core: a1..a6
 # --------------------------------------------------------------------------
+def head_core(d, b, hv, qkv_bits, conv_w_bits, a_bits, b_bits, A_log, dt_bias, conv_state_bits=None,
+              S0=None, mask=None):
+    """a1..a6 for the single head (b, hv): the conv of the q/k channels of
+    k-head hv/(Hv/Hk) and of the v channels of hv, the gates of hv, and the
+    recurrence.  Returns (y [T,Dv] float64, S [Dv,Dk] float64, new conv-state
+    rows {"q", "k", "v": bf16 bits [K-1, D]} of those channels)."""
+    hk = k_head_of(d, hv)
+    q, cq = conv_head(d, "q", hk, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
+    k, ck = conv_head(d, "k", hk, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
+    v, cv = conv_head(d, "v", hv, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
+    g, beta = gating(np.asarray(a_bits)[b, :, hv], np.asarray(b_bits)[b, :, hv], np.asarray(A_log)[hv],
+                     np.asarray(dt_bias)[hv])
+    S0h = np.zeros((d.Dv, d.Dk)) if S0 is None else S0
+    y, S = head_recurrence(bf16_to_f64(q), bf16_to_f64(k), bf16_to_f64(v), g, beta, S0h,
+                           None if mask is None else np.asarray(mask)[b])
+    return y, S, {"q": cq, "k": ck, "v": cv}
+
+
+def _map_threads(fn, items, threads):
+    n = threads or _default_threads()
+    if n <= 1 or len(items) <= 1:
+        return [fn(x) for x in items]
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+        return list(ex.map(fn, items))
+
+
 def layer_core(d, qkv_bits, conv_w_bits, a_bits, b_bits, A_log, dt_bias, conv_state_bits=None,
-         state_in=None, mask=None, pairs: Optional[Sequence] = None, threads: Optional[int] = None):
-    """conv -> SiLU -> q/k norm -> gates -> recurrence, as GatedDeltaNet::forward
-    of [GD-RS] orders them.  With ``pairs`` only those (b, hv) heads (and the
-    conv channels they read) are computed.  Returns a dict with q, k, v (bf16
-    bits, zero where not computed), g, beta (float64), y (float64, NaN where not
-    computed), y_bf16 (bits), state (float64), conv_state (bf16 bits, only when
-    every head was computed)."""
-    full = pairs is None
-    if full:
-        q, k, v, new_cs = conv_update(d, qkv_bits, conv_w_bits, conv_state_bits, mask)
-    else:
-        q = np.zeros((d.B, d.T, d.Hk, d.Dk), np.uint16)
-        k = np.zeros((d.B, d.T, d.Hk, d.Dk), np.uint16)
-        v = np.zeros((d.B, d.T, d.Hv, d.Dv), np.uint16)
-        new_cs = None
-        done_k = set()
-        for (b, hv) in pairs:
-            hk = k_head_of(d, hv)
-            if (b, hk) not in done_k:
-                q[b, :, hk], _ = conv_head(d, "q", hk, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
-                k[b, :, hk], _ = conv_head(d, "k", hk, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
-                done_k.add((b, hk))
-            v[b, :, hv], _ = conv_head(d, "v", hv, b, qkv_bits, conv_w_bits, conv_state_bits, mask)
+               state_in=None, mask=None, pairs: Optional[Sequence] = None, threads: Optional[int] = None):
+    """conv -> SiLU -> q/k norm -> gates -> recurrence, in the order
+    GatedDeltaNet::forward of [GD-RS] gives.
+
+    Without ``pairs``: every head; returns a dict with q, k, v (bf16 bits),
+    g, beta, y (float64 [B,T,Hv,Dv]), y_bf16 (bits), state (float64
+    [B,Hv,Dv,Dk]) and conv_state (bf16 bits [B,K-1,C]).
+    With ``pairs`` (a list of (b, hv)): only those heads and the channels
+    they read; returns {"heads": {(b, hv): {"y", "state", "conv"}}}."""
+    if pairs is not None:
+        def one(pair):
+            b, hv = pair
+            S0 = None if state_in is None else state_in[b, hv]
+            y, S, conv = head_core(d, b, hv, qkv_bits, conv_w_bits, a_bits, b_bits, A_log, dt_bias,
+                                   conv_state_bits, S0, mask)
+            return pair, {"y": y, "state": S, "conv": conv}
+        return {"heads": dict(_map_threads(one, list(pairs), threads))}
+    q, k, v, new_cs = conv_update(d, qkv_bits, conv_w_bits, conv_state_bits, mask)
     g, beta = gating(a_bits, b_bits, A_log, dt_bias)
-    y, S = recurrence(d, q, k, v, g, beta, state_in, mask, pairs, threads)
-    y_bits = f64_to_bf16(np.nan_to_num(y))
-    return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "y": y, "y_bf16": y_bits,
+    y, S = recurrence(d, q, k, v, g, beta, state_in, mask, None, threads)
+    return {"q": q, "k": k, "v": v, "g": g, "beta": beta, "y": y, "y_bf16": f64_to_bf16(y),
             "state": S, "conv_state": new_cs}
 
 
 def decode(d, steps_inputs, conv_w_bits, A_log, dt_bias, conv_state_bits, state_in,
            row_mask=None, pairs=None, threads=None):
-    """Carried single-token steps: each step is ``core`` with T = 1, the conv
-    state carried as bf16 and the recurrent state carried as f32 (the storage
-    types of the cache slots).  steps_inputs: list of dicts with qkv [B,1,C],
-    a, b [B,1,Hv] bf16 bits.  Returns (list of y [B,Hv,Dv] float64, state f64,
-    conv_state bits)."""
+    """Carried single-token steps: each step is ``layer_core`` with T = 1, the
+    conv state carried as bf16 and the recurrent state carried as f32 (the
+    storage types of the cache slots).  steps_inputs: list of dicts with qkv
+    [B,1,C], a, b [B,1,Hv] bf16 bits.
+
+    Without ``pairs`` returns (list of y [B,Hv,Dv] float64, state float64
+    [B,Hv,Dv,Dk], conv_state bits).  With ``pairs`` returns (list of
+    {(b, hv): y [Dv]}, {(b, hv): state [Dv,Dk]}, None)."""
     d1 = d.with_(T=1)
     cs = None if conv_state_bits is None else np.array(conv_state_bits, copy=True)
-    st = None if state_in is None else round_f32(state_in)
     mask = None if row_mask is None else np.asarray(row_mask).reshape(d.B, 1)
     ys = []
-    for inp in steps_inputs:
-        out = layer_core(d1, inp["qkv"], conv_w_bits, inp["a"], inp["b"], A_log, dt_bias, cs, st, mask,
-                   pairs, threads)
-        ys.append(out["y"][:, 0])
-        st = round_f32(out["state"])
-        if pairs is None:
+    if pairs is None:
+        st = None if state_in is None else round_f32(state_in)
+        for inp in steps_inputs:
+            out = layer_core(d1, inp["qkv"], conv_w_bits, inp["a"], inp["b"], A_log, dt_bias, cs, st, mask,
+                             None, threads)
+            ys.append(out["y"][:, 0])
+            st = round_f32(out["state"])
             cs = out["conv_state"]
-    return ys, st, cs
+        return ys, st, cs
+    pairs = list(pairs)
+    st = {p: (np.zeros((d.Dv, d.Dk)) if state_in is None else round_f32(np.asarray(state_in)[p[0], p[1]]))
+          for p in pairs}
+    if cs is None:
+        cs = np.zeros((d.B, d.K - 1, d.C), np.uint16)
+    rng = _channel_ranges(d)
+    for inp in steps_inputs:
+        heads = layer_core(d1, inp["qkv"], conv_w_bits, inp["a"], inp["b"], A_log, dt_bias, cs,
+                           _PairStates(st), mask, pairs, threads)["heads"]
+        ys.append({p: heads[p]["y"][0] for p in pairs})
+        for (b, hv) in pairs:
+            st[(b, hv)] = round_f32(heads[(b, hv)]["state"])
+            hk = k_head_of(d, hv)
+            cs[b][:, rng["q"](hk)] = heads[(b, hv)]["conv"]["q"]
+            cs[b][:, rng["k"](hk)] = heads[(b, hv)]["conv"]["k"]
+            cs[b][:, rng["v"](hv)] = heads[(b, hv)]["conv"]["v"]
+    return ys, st, None
+
+
+class _PairStates:
+    """Read-only state[b, hv] view over a dict of per-head states."""
+
+    def __init__(self, st):
+        self.st = st
+
+    def __getitem__(self, idx):
+        return self.st[idx]
 
 
 # --------------------------------------------------------------------------

@@ -78,7 +78,14 @@ def test_gating(gdn, B, T, Hv):
     a = (torch.randn((B, T, Hv), generator=torch.Generator().manual_seed(T)) * 4).to(torch.bfloat16)
     g, beta = gdn.gating(d, to_dev(a), to_dev(inp["b"]), to_dev(inp["A_log"]), to_dev(inp["dt_bias"]))
     gr, br = oracle.gating(U.bits(a), U.bits(inp["b"]), inp["A_log"].numpy(), inp["dt_bias"].numpy())
-    assert np.allclose(g.cpu().numpy(), gr, rtol=2e-6, atol=1e-30)
+    # g = exp(-z), z = exp(A_log) softplus(a + dt_bias) is formed in f32 with a
+    # few roundings of relative size 2^-24 each, so ln g carries an absolute
+    # error of a few ulps of z: compare ln g against 1e-6 * max(1, z).
+    gg = g.cpu().numpy().astype(np.float64)
+    z = -np.log(gr)
+    live = gr > 1e-36                       # below this f32 underflows
+    assert np.all(np.abs(np.log(gg[live]) + z[live]) <= 1e-6 * np.maximum(1.0, z[live]))
+    assert np.all(gg[~live] <= 1e-36)
     assert np.allclose(beta.cpu().numpy(), br, rtol=2e-6, atol=1e-30)
 
 

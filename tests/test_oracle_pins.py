@@ -369,9 +369,18 @@ def test_core_tiny_and_pair_sampling_agree(oracle_mod):
     full = o.layer_core(*args)
     assert full["y"].shape == (1, 8, 2, 32) and full["state"].shape == (1, 2, 32, 32)
     assert np.all(np.isfinite(full["y"]))
-    part = o.layer_core(*args, pairs=[(0, 1)])
-    assert np.array_equal(part["y"][0, :, 1], full["y"][0, :, 1])
-    assert np.array_equal(part["state"][0, 1], full["state"][0, 1])
+    part = o.layer_core(*args, pairs=[(0, 1)])["heads"][(0, 1)]
+    assert np.array_equal(part["y"], full["y"][0, :, 1])
+    assert np.array_equal(part["state"], full["state"][0, 1])
+    # sampled carried decode == full carried decode on the sampled head
+    steps = [{k: wl.bf16_bits(v) for k, v in wl.decode_step_inputs(w, i, d.with_(T=1)).items()}
+             for i in range(4)]
+    d1 = d.with_(T=1)
+    yf, sf, _ = o.decode(d1, steps, *args[2:3], *args[5:8], args[8])
+    yp, sp, _ = o.decode(d1, steps, *args[2:3], *args[5:8], args[8], pairs=[(0, 1)])
+    for i in range(4):
+        assert np.array_equal(yp[i][(0, 1)], yf[i][0, 1])
+    assert np.array_equal(sp[(0, 1)], sf[0, 1])
 
 
 def test_decode_steps_equal_one_prefill(oracle_mod):
