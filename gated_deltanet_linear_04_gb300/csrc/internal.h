@@ -29,9 +29,10 @@ cudaError_t launch_decode(const Sizes &s, const uint16_t *qkv, const uint16_t *c
                           const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
                           float *state, const uint8_t *row_mask, uint16_t *y, unsigned *err, cudaStream_t st);
 
-// Encodes a 2-D row-major bf16/f32 tensor map (rows x cols, box rows x box_cols).
+// Encodes a 2-D row-major tensor map (rows x cols, box rows x box_cols).
 bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
-                    uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols);
+                    uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 cudaError_t launch_prefill_seq(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                const float *g, const float *beta, const float *state_in, float *state_out,

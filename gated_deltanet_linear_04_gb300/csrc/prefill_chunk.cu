@@ -1,15 +1,508 @@
-// Chunked (WY / UT-transform) prefill on the tensor cores.
+// Chunked (WY / UT-transform) prefill on the 5th-generation tensor cores.
+//
+// The recurrence of "mlex 0.1.2, src/models/gated_delta.rs" (GatedDeltaNet::
+// forward, per-timestep loop) and of the gated_delta_step kernel of "mlx-bun
+// 0.4.0 -> 1.0.0, package/src/model/qwen3-delta.ts" is re-blocked exactly into
+// chunks of 64 steps.  For a chunk with start state S0 ([Dv, Dk]) and
+// log-decay prefix sums lg_r = sum_{i<=r} log g_i:
+//   A[r,i] = beta_r exp(lg_r - lg_i) (k_r . k_i), i < r;   T = (I + A)^-1
+//   U = T diag(beta) V,   W = T diag(beta exp(lg)) K,   D = U - W S0^T
+//   Y = diag(exp(lg)) Q S0^T + (M o Q K^T) D,   M[r,i] = exp(lg_r - lg_i), i <= r
+//   S = exp(lg_63) S0 + D^T diag(exp(lg_63 - lg)) K
+// (A masked step enters with g = 1, beta = 0; its y is written as zero.)
+//
+// Every product is issued in transposed form so that the MMA row count is
+// M = 128 (= Dv or Dk) and the accumulator row is one TMEM lane:
+//   [K;Q] K^T        bf16 x bf16  -> TMEM QK   (rows 0-63 K K^T, 64-127 Q K^T)
+//   U^T = (bV)^T T^T tf32         -> TMEM D
+//   W^T = (bgK)^T T^T tf32        -> TMEM W
+//   D^T += S0 (-W)^T tf32         -> TMEM D    (accumulates onto U^T)
+//   Y^T = S0 (gQ)^T  tf32         -> TMEM Y
+//   Y^T += D^T P^T   tf32         -> TMEM Y
+//   S  += D^T Kc^T   tf32         -> TMEM S    (S pre-scaled by exp(lg_63))
+// The f32 state lives in TMEM across all chunks; its operand copy is rounded to
+// tf32 each chunk (the accumulation itself stays f32).  The 64 x 64 unit
+// lower-triangular inverse T is computed on the CUDA cores by blocked doubling
+// (8x8 diagonal blocks, then 16-, 32-, 64-wide merges X = -T_bb A_ba T_aa).
+// q, k, v tiles arrive by 2-D TMA (k and q 128B-swizzled straight into the
+// MMA operand layout), prefetched one chunk ahead.
+//
+// One CTA (256 threads) owns one (b, hv) head for all T.  Supports Dk = Dv =
+// 128.  Shared memory: 13 slots of 16 KiB reused across the phases of a chunk.
 #include "common.cuh"
 #include "internal.h"
+#include "umma.cuh"
 
 namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kC = 64;          // chunk length
+constexpr int kD = 128;         // Dk = Dv
+constexpr uint32_t kSlot = 16384;
+constexpr int kSlots = 13;
+constexpr uint32_t kSmemBytes = kSlots * kSlot + 1024;
+
+// slot map (byte offsets from the 1024-aligned base)
+constexpr uint32_t S_KQ = 0 * kSlot;    // 2 slots: K rows 0-63 / Q rows 64-127, K-halves of 64
+constexpr uint32_t S_V = 2 * kSlot;     // plain [64][128] bf16
+constexpr uint32_t S_GQ = 3 * kSlot;    // 2 slots: (g Q) [64][128] tf32, 4 K-tiles of 8 KiB
+constexpr uint32_t S_KT = 5 * kSlot;    // 2 slots: Kc^T [128][64] tf32, 2 K-tiles of 16 KiB
+constexpr uint32_t S_BV = 7 * kSlot;    // 2 slots: (b V)^T [128][64]  -> later S0 tiles 0,1 -> D^T
+constexpr uint32_t S_BK = 9 * kSlot;    // 2 slots: (b g K)^T [128][64] -> later S0 tiles 2,3
+constexpr uint32_t S_A = 11 * kSlot;    // A / T plain [64][64] f32     -> later (-W) tiles 0,1 -> P
+constexpr uint32_t S_T = 12 * kSlot;    // Y scratch, then T [64][64] tf32 -> later (-W) tiles 2,3
+constexpr uint32_t S_S0 = S_BV;         // S0 [128][128] tf32, 4 K-tiles of 16 KiB (slots 7-10)
+constexpr uint32_t S_NW = S_A;          // -W [64][128] tf32, 4 K-tiles of 8 KiB (slots 11-12)
+constexpr uint32_t S_DT = S_BV;         // D^T [128][64] tf32, 2 K-tiles of 16 KiB (slots 7-8)
+constexpr uint32_t S_P = S_A;           // P [64][64] tf32, 2 K-tiles of 8 KiB (slot 11)
+
+// TMEM columns
+constexpr uint32_t C_QK = 0, C_D = 64, C_W = 128, C_Y = 192, C_S = 256, kTmemCols = 512;
+
+struct ChunkParams {
+    const float *g, *beta, *state_in;
+    float *state_out;
+    const uint8_t *mask;
+    uint16_t *y;
+    unsigned *err;
+    int B, T, Hk, Hv;
+};
+
+// A / T working matrix, row-major with the column XOR-swizzled by the row so
+// that row-per-thread stores are bank-conflict free.
+__device__ __forceinline__ int aidx(int r, int c) { return r * 64 + (c ^ (r & 31)); }
+
+__device__ __forceinline__ void st_tf32x4(uint8_t *base, uint32_t off, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(base + off) =
+        make_float4(umma::to_tf32(a), umma::to_tf32(b), umma::to_tf32(c), umma::to_tf32(d));
+}
+
+__device__ __forceinline__ float kq_elem(const uint8_t *sm, int row, int dk) {
+    // row 0-63: K, 64-127: Q; bf16, 128B swizzle, K-halves of 64 in two slots
+    const uint16_t *p = reinterpret_cast<const uint16_t *>(
+        sm + S_KQ + (dk >> 6) * kSlot + umma::sw128((uint32_t)row, (uint32_t)(dk & 63) * 2));
+    return bf16_to_f32(*p);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                     const __grid_constant__ CUtensorMap tm_q,
+                                                                     const __grid_constant__ CUtensorMap tm_v,
+                                                                     const ChunkParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float s_g[2][kC], s_b[2][kC];
+    __shared__ int s_m[2][kC];
+    __shared__ float s_lg[kC], s_gam[kC], s_beta[kC], s_bg[kC], s_kc[kC];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3;                 // TMEM lane quarter of this warp
+    const int half = warp >> 2;                // which half of the columns this warp handles
+    const int row = quad * 32 + lane;          // TMEM lane / accumulator row of this thread
+    const int hv = blockIdx.x, b = blockIdx.y;
+    const int hk = hv / (p.Hv / p.Hk);
+    const int T = p.T;
+    const int nchunks = (T + kC - 1) / kC;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - smem_u32(smem_raw));
+    float *As = reinterpret_cast<float *>(sm + S_A);
+    float *Ys = reinterpret_cast<float *>(sm + S_T);
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 0) {
+        umma::tmem_alloc(&tmem_slot, kTmemCols);
+        umma::tmem_relinquish();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+
+    // ---- initial state -> TMEM S (row = dv, columns = dk); half 0: dk 0-63, half 1: 64-127
+    {
+        const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float r[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.state_in != nullptr) x = *reinterpret_cast<const float4 *>(p.state_in + off + c * 32 + j);
+                r[j] = x.x; r[j + 1] = x.y; r[j + 2] = x.z; r[j + 3] = x.w;
+            }
+            umma::tmem_st32(tmem + lane_base + C_S + half * 64 + c * 32, r);
+        }
+        umma::tmem_st_wait();
+    }
+
+    auto issue_loads = [&](int c) {
+        const int st = c & 1;
+        if (tid == 0) {
+            mbar_expect_tx(&bar_tma, 4 * 8192 + 16384);
+            const int rowg = b * T + c * kC;
+            tma_load_2d(sm + S_KQ, &tm_k, hk * kD, rowg, &bar_tma);
+            tma_load_2d(sm + S_KQ + kSlot, &tm_k, hk * kD + 64, rowg, &bar_tma);
+            tma_load_2d(sm + S_KQ + 8192, &tm_q, hk * kD, rowg, &bar_tma);
+            tma_load_2d(sm + S_KQ + kSlot + 8192, &tm_q, hk * kD + 64, rowg, &bar_tma);
+            tma_load_2d(sm + S_V, &tm_v, hv * kD, rowg, &bar_tma);
+        }
+        if (tid < kC) {
+            const int t = c * kC + tid;
+            float gg = 1.0f, bb = 0.0f;
+            int m = 0;
+            if (t < T) {
+                const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
+                m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
+                if (m) {
+                    gg = p.g[gi];
+                    bb = p.beta[gi];
+                }
+            }
+            s_g[st][tid] = gg;
+            s_b[st][tid] = bb;
+            s_m[st][tid] = m;
+        }
+    };
+
+    uint32_t mma_phase = 0;
+    bool ok = true;
+    // bounded wait on the MMA barrier by every thread, agreed across the CTA
+    auto wait_mma = [&]() {
+        bool w = mbar_wait(&bar_mma, mma_phase & 1u, p.err);
+        ++mma_phase;
+        w = __syncthreads_and(w) != 0;
+        umma::fence_after_sync();
+        return w;
+    };
+    // make generic smem writes and TMEM stores visible to the next MMA issue
+    auto publish = [&]() {
+        fence_proxy_async_smem();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+    };
+
+    issue_loads(0);
+    __syncthreads();
+
+    for (int c = 0; c < nchunks && ok; ++c) {
+        const int st = c & 1;
+        const int t0 = c * kC;
+        // ---- S1: chunk inputs, log-decay prefix sums (warp 0)
+        ok = mbar_wait(&bar_tma, (uint32_t)(c & 1), p.err);
+        if (warp == 0) {
+            const float la = logf(s_g[st][2 * lane]), lb = logf(s_g[st][2 * lane + 1]);
+            float incl = la + lb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const float up = __shfl_up_sync(0xffffffffu, incl, 1);
+            const float excl = lane == 0 ? 0.0f : up;
+            const float lg0 = excl + la, lg1 = lg0 + lb;
+            const float last = __shfl_sync(0xffffffffu, incl, 31);
+            s_lg[2 * lane] = lg0;
+            s_lg[2 * lane + 1] = lg1;
+            s_gam[2 * lane] = expf(lg0);
+            s_gam[2 * lane + 1] = expf(lg1);
+            s_kc[2 * lane] = expf(last - lg0);
+            s_kc[2 * lane + 1] = expf(last - lg1);
+            const float b0 = s_b[st][2 * lane], b1 = s_b[st][2 * lane + 1];
+            s_beta[2 * lane] = b0;
+            s_beta[2 * lane + 1] = b1;
+            s_bg[2 * lane] = b0 * expf(lg0);
+            s_bg[2 * lane + 1] = b1 * expf(lg1);
+        }
+        ok = __syncthreads_and(ok) != 0;
+        if (!ok) break;
+
+        // ---- S2: [K;Q] K^T on the tensor core; meanwhile build the tf32 operands
+        if (tid == 0) {
+            umma::fence_after_sync();
+            const uint32_t id = umma::idesc(128, 64, umma::kFmtBF16);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t a = base + S_KQ + (k >> 2) * kSlot + (k & 3) * 32;
+                umma::mma_bf16(tmem + C_QK, umma::desc_sw128(a), umma::desc_sw128(a), id, k > 0);
+            }
+            umma::mma_commit(&bar_mma);
+        }
+        // (g Q)[r][dk]: 2048 float4 groups
+        for (int i = tid; i < kC * kD / 4; i += kThreads) {
+            const int r = i >> 5, dk = (i & 31) * 4;
+            const float gm = s_gam[r];
+            st_tf32x4(sm, S_GQ + (dk >> 5) * 8192 + umma::sw128(r, (dk & 31) * 4), gm * kq_elem(sm, 64 + r, dk),
+                      gm * kq_elem(sm, 64 + r, dk + 1), gm * kq_elem(sm, 64 + r, dk + 2),
+                      gm * kq_elem(sm, 64 + r, dk + 3));
+        }
+        // Kc^T[dk][r] and (b g K)^T[dk][r]: 2048 groups of 4 consecutive r
+        for (int i = tid; i < kD * kC / 4; i += kThreads) {
+            const int dk = i >> 4, r = (i & 15) * 4;
+            const float k0 = kq_elem(sm, r, dk), k1 = kq_elem(sm, r + 1, dk), k2 = kq_elem(sm, r + 2, dk),
+                        k3 = kq_elem(sm, r + 3, dk);
+            const uint32_t off = (r >> 5) * kSlot + umma::sw128(dk, (r & 31) * 4);
+            st_tf32x4(sm, S_KT + off, s_kc[r] * k0, s_kc[r + 1] * k1, s_kc[r + 2] * k2, s_kc[r + 3] * k3);
+            st_tf32x4(sm, S_BK + off, s_bg[r] * k0, s_bg[r + 1] * k1, s_bg[r + 2] * k2, s_bg[r + 3] * k3);
+        }
+        // (b V)^T[dv][i]
+        {
+            const uint16_t *Vs = reinterpret_cast<const uint16_t *>(sm + S_V);
+            for (int i = tid; i < kD * kC / 4; i += kThreads) {
+                const int dv = i >> 4, r = (i & 15) * 4;
+                st_tf32x4(sm, S_BV + (r >> 5) * kSlot + umma::sw128(dv, (r & 31) * 4),
+                          s_beta[r] * bf16_to_f32(Vs[r * kD + dv]), s_beta[r + 1] * bf16_to_f32(Vs[(r + 1) * kD + dv]),
+                          s_beta[r + 2] * bf16_to_f32(Vs[(r + 2) * kD + dv]),
+                          s_beta[r + 3] * bf16_to_f32(Vs[(r + 3) * kD + dv]));
+            }
+        }
+
+        // ---- S3: A from K K^T (lanes 0-63)
+        if (!wait_mma()) { ok = false; break; }
+        if (quad < 2) {
+            float kk[32];
+            umma::tmem_ld32(tmem + lane_base + C_QK + half * 32, kk);
+            umma::tmem_ld_wait();
+            const int r = row;                      // 0..63
+            const float lr = s_lg[r], br = s_beta[r];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int i = half * 32 + j;
+                As[aidx(r, i)] = i < r ? br * expf(lr - s_lg[i]) * kk[j] : 0.0f;
+            }
+        }
+        // K and V tiles are no longer read: prefetch the next chunk
+        umma::fence_before_sync();
+        __syncthreads();
+        if (c + 1 < nchunks) issue_loads(c + 1);
+
+        // ---- S4: T = (I + A)^-1 by blocked doubling, in place in As
+        {
+            float t[8];
+            const int o = (tid >> 3) * 8, j = tid & 7;
+            if (tid < 64) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    float acc = r == j ? 1.0f : 0.0f;
+#pragma unroll
+                    for (int i = 0; i < r; ++i) acc -= As[aidx(o + r, o + i)] * t[i];
+                    t[r] = acc;
+                }
+            }
+            __syncthreads();
+            if (tid < 64) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) As[aidx(o + r, o + j)] = t[r];
+            }
+            __syncthreads();
+        }
+        for (int s = 8; s < 64; s <<= 1) {
+            const int n = 32 * s;       // outputs of this level
+            for (int i = tid; i < n; i += kThreads) {
+                const int pi = i / (s * s), rem = i % (s * s), r = rem / s, cc = rem % s, q0 = pi * 2 * s;
+                float acc = 0.0f;
+                for (int m = cc; m < s; ++m) acc = fmaf(As[aidx(q0 + s + r, q0 + m)], As[aidx(q0 + m, q0 + cc)], acc);
+                Ys[i] = acc;
+            }
+            __syncthreads();
+            for (int i = tid; i < n; i += kThreads) {
+                const int pi = i / (s * s), rem = i % (s * s), r = rem / s, cc = rem % s, q0 = pi * 2 * s;
+                float acc = 0.0f;
+                for (int m = 0; m <= r; ++m)
+                    acc = fmaf(As[aidx(q0 + s + r, q0 + s + m)], Ys[pi * s * s + m * s + cc], acc);
+                As[aidx(q0 + s + r, q0 + cc)] = -acc;
+            }
+            __syncthreads();
+        }
+        // T -> tf32 B operand [r][i] (slot S_T; the Y scratch is dead)
+        for (int i = tid; i < kC * kC / 4; i += kThreads) {
+            const int r = i >> 4, c4 = (i & 15) * 4;
+            st_tf32x4(sm, S_T + (c4 >> 5) * 8192 + umma::sw128(r, (c4 & 31) * 4), As[aidx(r, c4)],
+                      As[aidx(r, c4 + 1)], As[aidx(r, c4 + 2)], As[aidx(r, c4 + 3)]);
+        }
+        publish();
+
+        // ---- S5: U^T and W^T on the tensor core
+        if (tid == 0) {
+            const uint32_t id = umma::idesc(128, 64, umma::kFmtTF32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t kt = k >> 2, ko = (k & 3) * 32;
+                const uint64_t bt = umma::desc_sw128(base + S_T + kt * 8192 + ko);
+                umma::mma_tf32(tmem + C_D, umma::desc_sw128(base + S_BV + kt * kSlot + ko), bt, id, k > 0);
+                umma::mma_tf32(tmem + C_W, umma::desc_sw128(base + S_BK + kt * kSlot + ko), bt, id, k > 0);
+            }
+            umma::mma_commit(&bar_mma);
+        }
+        if (!wait_mma()) { ok = false; break; }
+        // S0 (tf32 copy) -> smem, S <- exp(lg_63) S in TMEM; -W -> smem
+        {
+            const float gl = s_gam[kC - 1];
+#pragma unroll
+            for (int cpart = 0; cpart < 2; ++cpart) {
+                float sv[32];
+                const uint32_t col = C_S + half * 64 + cpart * 32;
+                umma::tmem_ld32(tmem + lane_base + col, sv);
+                umma::tmem_ld_wait();
+                const int dk0 = half * 64 + cpart * 32;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    st_tf32x4(sm, S_S0 + (dk0 >> 5) * kSlot + umma::sw128(row, j * 4), sv[j], sv[j + 1], sv[j + 2],
+                              sv[j + 3]);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sv[j] *= gl;
+                umma::tmem_st32(tmem + lane_base + col, sv);
+            }
+            umma::tmem_st_wait();
+            float wv[32];
+            umma::tmem_ld32(tmem + lane_base + C_W + half * 32, wv);
+            umma::tmem_ld_wait();
+            const int dk = row;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int r = half * 32 + j;
+                *reinterpret_cast<float *>(sm + S_NW + (dk >> 5) * 8192 + umma::sw128(r, (dk & 31) * 4)) =
+                    umma::to_tf32(-wv[j]);
+            }
+        }
+        publish();
+
+        // ---- S6: D^T += S0 (-W)^T ; Y^T = S0 (gQ)^T
+        if (tid == 0) {
+            const uint32_t id = umma::idesc(128, 64, umma::kFmtTF32);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t kt = k >> 2, ko = (k & 3) * 32;
+                const uint64_t a = umma::desc_sw128(base + S_S0 + kt * kSlot + ko);
+                umma::mma_tf32(tmem + C_D, a, umma::desc_sw128(base + S_NW + kt * 8192 + ko), id, true);
+                umma::mma_tf32(tmem + C_Y, a, umma::desc_sw128(base + S_GQ + kt * 8192 + ko), id, k > 0);
+            }
+            umma::mma_commit(&bar_mma);
+        }
+        if (!wait_mma()) { ok = false; break; }
+
+        // ---- S7: D^T -> smem (A operand); P = M o Q K^T -> smem (B operand)
+        {
+            float dv[32];
+            umma::tmem_ld32(tmem + lane_base + C_D + half * 32, dv);
+            umma::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                st_tf32x4(sm, S_DT + half * kSlot + umma::sw128(row, j * 4), dv[j], dv[j + 1], dv[j + 2], dv[j + 3]);
+            if (quad >= 2) {
+                float qk[32];
+                umma::tmem_ld32(tmem + lane_base + C_QK + half * 32, qk);
+                umma::tmem_ld_wait();
+                const int r = row - 64;
+                const float lr = s_lg[r];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float v4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = half * 32 + j + e;
+                        v4[e] = i <= r ? expf(lr - s_lg[i]) * qk[j + e] : 0.0f;
+                    }
+                    st_tf32x4(sm, S_P + half * 8192 + umma::sw128(r, j * 4), v4[0], v4[1], v4[2], v4[3]);
+                }
+            }
+        }
+        publish();
+
+        // ---- S8: Y^T += D^T P^T ; S += D^T Kc^T
+        if (tid == 0) {
+            const uint32_t idy = umma::idesc(128, 64, umma::kFmtTF32);
+            const uint32_t ids = umma::idesc(128, 128, umma::kFmtTF32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t kt = k >> 2, ko = (k & 3) * 32;
+                const uint64_t a = umma::desc_sw128(base + S_DT + kt * kSlot + ko);
+                umma::mma_tf32(tmem + C_Y, a, umma::desc_sw128(base + S_P + kt * 8192 + ko), idy, true);
+                umma::mma_tf32(tmem + C_S, a, umma::desc_sw128(base + S_KT + kt * kSlot + ko), ids, true);
+            }
+            umma::mma_commit(&bar_mma);
+        }
+        if (!wait_mma()) { ok = false; break; }
+
+        // ---- S9: y (row = dv, columns = steps)
+        {
+            float yv[32];
+            umma::tmem_ld32(tmem + lane_base + C_Y + half * 32, yv);
+            umma::tmem_ld_wait();
+            const int dv = row;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int r = half * 32 + j, t = t0 + r;
+                if (t < T) {
+                    const float out = s_m[st][r] ? yv[j] : 0.0f;
+                    p.y[(((size_t)b * T + t) * p.Hv + hv) * kD + dv] = f32_to_bf16(out);
+                }
+            }
+        }
+        umma::fence_before_sync();
+        __syncthreads();
+    }
+
+    // ---- final state (only when every wait succeeded)
+    if (__syncthreads_and(ok)) {
+        const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
+#pragma unroll
+        for (int cpart = 0; cpart < 2; ++cpart) {
+            float sv[32];
+            umma::tmem_ld32(tmem + lane_base + C_S + half * 64 + cpart * 32, sv);
+            umma::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(p.state_out + off + cpart * 32 + j) =
+                    make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+        }
+    } else if (tid == 0) {
+        // a wait gave up: give in-flight MMAs a bounded chance to drain
+        mbar_wait(&bar_mma, mma_phase & 1u, nullptr);
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
 
 size_t prefill_chunked_workspace(const Sizes &) { return 0; }
 
-cudaError_t launch_prefill_chunked(const Sizes &, const uint16_t *, const uint16_t *, const uint16_t *,
-                                   const float *, const float *, const float *, float *, const uint8_t *,
-                                   uint16_t *, void *, unsigned *, cudaStream_t) {
-    return cudaErrorNotSupported;
+cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                   const float *g, const float *beta, const float *state_in, float *state_out,
+                                   const uint8_t *mask, uint16_t *y, void *, unsigned *err, cudaStream_t st) {
+    if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
+    CUtensorMap tk, tq, tv;
+    const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
+    if (!encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    ChunkParams p{g, beta, state_in, state_out, mask, y, err, s.B, s.T, s.Hk, s.Hv};
+    dim3 grid(s.Hv, s.B);
+    prefill_chunk_kernel<<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, p);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

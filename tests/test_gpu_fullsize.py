@@ -92,16 +92,12 @@ def _prefill_case(gdn, name, pairs, chunk):
 
 @pytest.mark.parametrize("chunk", [0, 64])
 def test_prefill_t8192(gdn, chunk):
-    if chunk and gdn.gdn_prefill_workspace_size(wl.WORKLOADS["prefill_t8192"].dims, chunk) == 0:
-        pytest.skip("chunked form not built")
     _prefill_case(gdn, "prefill_t8192", [(0, 0), (0, 13), (0, 31)], chunk)
 
 
 @pytest.mark.parametrize("chunk", [0, 64])
 def test_prefill_ragged(gdn, chunk):
     w = wl.WORKLOADS["prefill_ragged"]
-    if chunk and gdn.gdn_prefill_workspace_size(w.dims, chunk) == 0:
-        pytest.skip("chunked form not built")
     lens = wl.workload_lengths(w)
     order = np.argsort(lens.numpy())
     pairs = [(int(order[0]), 5), (int(order[-1]), 63), (int(order[len(order) // 2]), 30)]

@@ -178,6 +178,50 @@ def test_prefill_sequential(gdn, B, T, Hk, Hv, Dk, Dv, mk, st):
     assert gdn.gdn_device_status() == gdn.GDN_OK
 
 
+CHUNK_CASES = [
+    # B, T, Hk, Hv, mask, state     (chunked form: Dk = Dv = 128)
+    (1, 1, 1, 1, None, "normal"),
+    (1, 63, 1, 2, None, "zeros"),
+    (1, 64, 1, 2, None, "normal"),
+    (2, 65, 2, 4, "random", "normal"),
+    (1, 200, 1, 2, "right", "normal"),
+    (3, 130, 1, 3, "left", "zeros"),
+    (2, 257, 2, 4, "allmasked_row", "normal"),
+    (2, 150, 1, 2, "sparse", "normal"),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,mk,st", CHUNK_CASES)
+def test_prefill_chunked(gdn, B, T, Hk, Hv, mk, st):
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=128, Dv=128)
+    mask = make_mask(mk, B, T, 5 + T)
+    r = recurrence_inputs(d, 500 + T, mask)
+    state_in = r["state"] if st == "normal" else None
+    y, s_out = gdn.prefill(d, to_dev(r["q"]), to_dev(r["k"]), to_dev(r["v"]), to_dev(r["g"]), to_dev(r["beta"]),
+                           to_dev(state_in), to_dev(mask), chunk=64)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    s0 = None if state_in is None else state_in.numpy().astype(np.float64)
+    yr, sr = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                               r["beta"].numpy().astype(np.float64), s0, np_mask(mask))
+    U.assert_y_close(U.bf16_dev_to_f64(y), yr)
+    U.assert_state_close(s_out.cpu().numpy(), sr)
+    if mask is not None:
+        assert np.all(U.bits(y)[mask.numpy() == 0] == 0), "padded y must be exactly zero"
+        for b in range(B):
+            if mask[b].sum() == 0:
+                ref = np.zeros_like(sr[b]) if s0 is None else state_in[b].numpy()
+                assert np.array_equal(s_out[b].cpu().numpy(), ref), "row without valid steps: state untouched"
+
+
+def test_prefill_chunked_rejects_other_head_sizes(gdn):
+    d = wl.Dims(B=1, T=8, Hk=1, Hv=2, Dk=64, Dv=128)
+    r = recurrence_inputs(d, 1)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.prefill(d, *(to_dev(r[x]) for x in ("q", "k", "v", "g", "beta")), None, None, chunk=64)
+    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+
+
 def test_prefill_in_place_and_split_is_bitwise(gdn):
     """state_out may alias state_in; running T1 then T2 steps equals T1+T2
     steps bit for bit (the sequential form does the same arithmetic)."""
