@@ -69,9 +69,57 @@ struct ChunkParams {
     int B, T, Hk, Hv;
 };
 
-// A / T working matrix, row-major with the column XOR-swizzled by the row so
-// that row-per-thread stores are bank-conflict free.
-__device__ __forceinline__ int aidx(int r, int c) { return r * 64 + (c ^ (r & 31)); }
+// A / T working matrix, row-major; groups of 4 columns are XOR-permuted by the
+// row (r % 8) so that row-per-thread float4 stores spread over all banks while
+// each aligned group of 4 stays contiguous for float4 loads.
+__device__ __forceinline__ int aidx(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+// exp of a non-positive log-decay difference: the MUFU exp2 path (relative
+// error ~2^-22, far below the tf32 rounding these values go through).
+__device__ __forceinline__ float decay(float x) { return exp2f(x * 1.4426950408889634f); }
+
+// One merge level of the blocked inverse: for each pair of S x S diagonal
+// blocks (a = [q0, q0+S), b = [q0+S, q0+2S)) of the unit lower triangular
+// T = (I + A)^-1, the lower-left block is X = -T_bb A_ba T_aa.  Each task
+// computes 4 adjacent columns of one row; sums run over full blocks because
+// the triangular factors hold explicit zeros above the diagonal.
+template <int S>
+__device__ __forceinline__ void merge_level(float *As, float *Ys, int tid) {
+    constexpr int G4 = S / 4;
+    constexpr int NT = (32 / S) * S * G4;
+    const int pi = tid / (S * G4), rem = tid % (S * G4), r = rem / G4, c = (rem % G4) * 4, q0 = pi * 2 * S;
+    if (tid < NT) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < S; ++m) {
+            const float a = As[aidx(q0 + S + r, q0 + m)];
+            const float4 t = ld4(As + aidx(q0 + m, q0 + c));
+            acc.x = fmaf(a, t.x, acc.x);
+            acc.y = fmaf(a, t.y, acc.y);
+            acc.z = fmaf(a, t.z, acc.z);
+            acc.w = fmaf(a, t.w, acc.w);
+        }
+        st4(Ys + (pi * S + r) * S + c, acc);
+    }
+    __syncthreads();
+    if (tid < NT) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < S; ++m) {
+            const float t = As[aidx(q0 + S + r, q0 + S + m)];
+            const float4 yv = ld4(Ys + (pi * S + m) * S + c);
+            acc.x = fmaf(t, yv.x, acc.x);
+            acc.y = fmaf(t, yv.y, acc.y);
+            acc.z = fmaf(t, yv.z, acc.z);
+            acc.w = fmaf(t, yv.w, acc.w);
+        }
+        st4(As + aidx(q0 + S + r, q0 + c), make_float4(-acc.x, -acc.y, -acc.z, -acc.w));
+    }
+    __syncthreads();
+}
 
 __device__ __forceinline__ void st_tf32x4(uint8_t *base, uint32_t off, float a, float b, float c, float d) {
     *reinterpret_cast<float4 *>(base + off) =
@@ -94,7 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     __shared__ uint32_t tmem_slot;
     __shared__ float s_g[2][kC], s_b[2][kC];
     __shared__ int s_m[2][kC];
-    __shared__ float s_lg[kC], s_gam[kC], s_beta[kC], s_bg[kC], s_kc[kC];
+    __shared__ __align__(16) float s_lg[kC];
+    __shared__ __align__(16) float s_gam[kC];
+    __shared__ __align__(16) float s_beta[kC];
+    __shared__ __align__(16) float s_bg[kC];
+    __shared__ __align__(16) float s_kc[kC];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;                 // TMEM lane quarter of this warp
@@ -238,32 +290,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             }
             umma::mma_commit(&bar_mma);
         }
-        // (g Q)[r][dk]: 2048 float4 groups
+        // (g Q)[r][dk]: a warp covers one row r, 4 consecutive dk per lane
         for (int i = tid; i < kC * kD / 4; i += kThreads) {
             const int r = i >> 5, dk = (i & 31) * 4;
             const float gm = s_gam[r];
-            st_tf32x4(sm, S_GQ + (dk >> 5) * 8192 + umma::sw128(r, (dk & 31) * 4), gm * kq_elem(sm, 64 + r, dk),
-                      gm * kq_elem(sm, 64 + r, dk + 1), gm * kq_elem(sm, 64 + r, dk + 2),
-                      gm * kq_elem(sm, 64 + r, dk + 3));
+            const uint2 qq = *reinterpret_cast<const uint2 *>(
+                sm + S_KQ + (dk >> 6) * kSlot + umma::sw128(64 + r, (dk & 63) * 2));
+            st_tf32x4(sm, S_GQ + (dk >> 5) * 8192 + umma::sw128(r, (dk & 31) * 4),
+                      gm * __uint_as_float(qq.x << 16), gm * __uint_as_float(qq.x & 0xffff0000u),
+                      gm * __uint_as_float(qq.y << 16), gm * __uint_as_float(qq.y & 0xffff0000u));
         }
-        // Kc^T[dk][r] and (b g K)^T[dk][r]: 2048 groups of 4 consecutive r
+        // Kc^T[dk][r] and (b g K)^T[dk][r]: lanes take consecutive dk (conflict-free
+        // reads along a K row), each thread 4 consecutive r
         for (int i = tid; i < kD * kC / 4; i += kThreads) {
-            const int dk = i >> 4, r = (i & 15) * 4;
+            const int dk = i & (kD - 1), r = (i >> 7) * 4;
             const float k0 = kq_elem(sm, r, dk), k1 = kq_elem(sm, r + 1, dk), k2 = kq_elem(sm, r + 2, dk),
                         k3 = kq_elem(sm, r + 3, dk);
             const uint32_t off = (r >> 5) * kSlot + umma::sw128(dk, (r & 31) * 4);
-            st_tf32x4(sm, S_KT + off, s_kc[r] * k0, s_kc[r + 1] * k1, s_kc[r + 2] * k2, s_kc[r + 3] * k3);
-            st_tf32x4(sm, S_BK + off, s_bg[r] * k0, s_bg[r + 1] * k1, s_bg[r + 2] * k2, s_bg[r + 3] * k3);
+            const float4 kc = ld4(s_kc + r), bg = ld4(s_bg + r);
+            st_tf32x4(sm, S_KT + off, kc.x * k0, kc.y * k1, kc.z * k2, kc.w * k3);
+            st_tf32x4(sm, S_BK + off, bg.x * k0, bg.y * k1, bg.z * k2, bg.w * k3);
         }
         // (b V)^T[dv][i]
         {
             const uint16_t *Vs = reinterpret_cast<const uint16_t *>(sm + S_V);
             for (int i = tid; i < kD * kC / 4; i += kThreads) {
-                const int dv = i >> 4, r = (i & 15) * 4;
+                const int dv = i & (kD - 1), r = (i >> 7) * 4;
+                const float4 be = ld4(s_beta + r);
                 st_tf32x4(sm, S_BV + (r >> 5) * kSlot + umma::sw128(dv, (r & 31) * 4),
-                          s_beta[r] * bf16_to_f32(Vs[r * kD + dv]), s_beta[r + 1] * bf16_to_f32(Vs[(r + 1) * kD + dv]),
-                          s_beta[r + 2] * bf16_to_f32(Vs[(r + 2) * kD + dv]),
-                          s_beta[r + 3] * bf16_to_f32(Vs[(r + 3) * kD + dv]));
+                          be.x * bf16_to_f32(Vs[r * kD + dv]), be.y * bf16_to_f32(Vs[(r + 1) * kD + dv]),
+                          be.z * bf16_to_f32(Vs[(r + 2) * kD + dv]), be.w * bf16_to_f32(Vs[(r + 3) * kD + dv]));
             }
         }
 
@@ -276,9 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             const int r = row;                      // 0..63
             const float lr = s_lg[r], br = s_beta[r];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 32; j += 4) {
                 const int i = half * 32 + j;
-                As[aidx(r, i)] = i < r ? br * expf(lr - s_lg[i]) * kk[j] : 0.0f;
+                const float4 li = ld4(s_lg + i);
+                float4 v;
+                v.x = i < r ? br * decay(lr - li.x) * kk[j] : 0.0f;
+                v.y = i + 1 < r ? br * decay(lr - li.y) * kk[j + 1] : 0.0f;
+                v.z = i + 2 < r ? br * decay(lr - li.z) * kk[j + 2] : 0.0f;
+                v.w = i + 3 < r ? br * decay(lr - li.w) * kk[j + 3] : 0.0f;
+                st4(As + aidx(r, i), v);
             }
         }
         // K and V tiles are no longer read: prefetch the next chunk
@@ -288,14 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
 
         // ---- S4: T = (I + A)^-1 by blocked doubling, in place in As
         {
-            float t[8];
+            // 8 x 8 diagonal blocks by forward substitution: thread (block, column j)
             const int o = (tid >> 3) * 8, j = tid & 7;
+            float t[8];
             if (tid < 64) {
+                float a[8][8];
+#pragma unroll
+                for (int r = 1; r < 8; ++r)
+#pragma unroll
+                    for (int i = 0; i < r; ++i) a[r][i] = As[aidx(o + r, o + i)];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     float acc = r == j ? 1.0f : 0.0f;
 #pragma unroll
-                    for (int i = 0; i < r; ++i) acc -= As[aidx(o + r, o + i)] * t[i];
+                    for (int i = 0; i < r; ++i) acc = fmaf(-a[r][i], t[i], acc);
                     t[r] = acc;
                 }
             }
@@ -306,29 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             }
             __syncthreads();
         }
-        for (int s = 8; s < 64; s <<= 1) {
-            const int n = 32 * s;       // outputs of this level
-            for (int i = tid; i < n; i += kThreads) {
-                const int pi = i / (s * s), rem = i % (s * s), r = rem / s, cc = rem % s, q0 = pi * 2 * s;
-                float acc = 0.0f;
-                for (int m = cc; m < s; ++m) acc = fmaf(As[aidx(q0 + s + r, q0 + m)], As[aidx(q0 + m, q0 + cc)], acc);
-                Ys[i] = acc;
-            }
-            __syncthreads();
-            for (int i = tid; i < n; i += kThreads) {
-                const int pi = i / (s * s), rem = i % (s * s), r = rem / s, cc = rem % s, q0 = pi * 2 * s;
-                float acc = 0.0f;
-                for (int m = 0; m <= r; ++m)
-                    acc = fmaf(As[aidx(q0 + s + r, q0 + s + m)], Ys[pi * s * s + m * s + cc], acc);
-                As[aidx(q0 + s + r, q0 + cc)] = -acc;
-            }
-            __syncthreads();
-        }
+        merge_level<8>(As, Ys, tid);
+        merge_level<16>(As, Ys, tid);
+        merge_level<32>(As, Ys, tid);
         // T -> tf32 B operand [r][i] (slot S_T; the Y scratch is dead)
         for (int i = tid; i < kC * kC / 4; i += kThreads) {
             const int r = i >> 4, c4 = (i & 15) * 4;
-            st_tf32x4(sm, S_T + (c4 >> 5) * 8192 + umma::sw128(r, (c4 & 31) * 4), As[aidx(r, c4)],
-                      As[aidx(r, c4 + 1)], As[aidx(r, c4 + 2)], As[aidx(r, c4 + 3)]);
+            const float4 tv = ld4(As + aidx(r, c4));
+            st_tf32x4(sm, S_T + (c4 >> 5) * 8192 + umma::sw128(r, (c4 & 31) * 4), tv.x, tv.y, tv.z, tv.w);
         }
         publish();
 
@@ -411,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int i = half * 32 + j + e;
-                        v4[e] = i <= r ? expf(lr - s_lg[i]) * qk[j + e] : 0.0f;
+                        v4[e] = i <= r ? decay(lr - s_lg[i]) * qk[j + e] : 0.0f;
                     }
                     st_tf32x4(sm, S_P + half * 8192 + umma::sw128(r, j * 4), v4[0], v4[1], v4[2], v4[3]);
                 }
