@@ -149,6 +149,14 @@ __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrive without release semantics: does not wait for this thread's
+// outstanding memory accesses.  Usable when the only accesses that must be
+// ordered before the other CTAs' post-wait writes are loads whose values have
+// already been consumed (a consumed load has completed).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
