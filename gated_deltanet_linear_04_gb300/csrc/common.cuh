@@ -39,7 +39,26 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ float silu(float u) { return u / (1.0f + expf(-u)); }
+// e^x as 2^(x log2 e) on the hardware base-2 exponential unit (ex2.approx,
+// relative error ~2^-22; results below 2^-126 flush to zero).
+__device__ __forceinline__ float exp_fast(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x * 1.4426950408889634f));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_fast(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// x * sigmoid(x); its result is rounded to bf16 by every caller, so the
+// approximate exponential and reciprocal (each ~1-2 ulp of f32) are invisible
+// except where the f32 value sits on a bf16 rounding boundary.  For x -> -inf
+// the exponential overflows to inf and the reciprocal gives 0, so the result
+// tends to -0 as it should.
+__device__ __forceinline__ float silu(float u) { return u * rcp_fast(1.0f + exp_fast(-u)); }
 
 __device__ __forceinline__ float softplus(float x) {
     return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));

@@ -20,8 +20,9 @@
 //   Y^T = S0 (gQ)^T  tf32         -> TMEM Y
 //   Y^T += D^T P^T   tf32         -> TMEM Y
 //   S  += D^T Kc^T   tf32         -> TMEM S    (S pre-scaled by exp(lg_63))
-// The f32 state lives in TMEM across all chunks; its operand copy is rounded to
-// tf32 each chunk (the accumulation itself stays f32).  The 64 x 64 unit
+// The f32 state lives in TMEM across all chunks and accumulates in f32; the D
+// and Y products read it straight from TMEM as their A operand (the tensor
+// core takes the top 19 bits, i.e. tf32 by truncation).  The 64 x 64 unit
 // lower-triangular inverse T is computed on the CUDA cores by blocked doubling
 // (8x8 diagonal blocks, then 16-, 32-, 64-wide merges X = -T_bb A_ba T_aa).
 // q, k, v tiles arrive by 2-D TMA (k and q 128B-swizzled straight into the
@@ -48,14 +49,14 @@ constexpr uint32_t S_KQ = 0 * kSlot;    // 2 slots: K rows 0-63 / Q rows 64-127,
 constexpr uint32_t S_V = 2 * kSlot;     // plain [64][128] bf16
 constexpr uint32_t S_GQ = 3 * kSlot;    // 2 slots: (g Q) [64][128] tf32, 4 K-tiles of 8 KiB
 constexpr uint32_t S_KT = 5 * kSlot;    // 2 slots: Kc^T [128][64] tf32, 2 K-tiles of 16 KiB
-constexpr uint32_t S_BV = 7 * kSlot;    // 2 slots: (b V)^T [128][64]  -> later S0 tiles 0,1 -> D^T
-constexpr uint32_t S_BK = 9 * kSlot;    // 2 slots: (b g K)^T [128][64] -> later S0 tiles 2,3
+constexpr uint32_t S_BV = 7 * kSlot;    // 2 slots: (b V)^T [128][64]  -> later D^T
+constexpr uint32_t S_BK = 9 * kSlot;    // 2 slots: (b g K)^T [128][64] -> later y staging
 constexpr uint32_t S_A = 11 * kSlot;    // A / T plain [64][64] f32     -> later (-W) tiles 0,1 -> P
 constexpr uint32_t S_T = 12 * kSlot;    // Y scratch, then T [64][64] tf32 -> later (-W) tiles 2,3
-constexpr uint32_t S_S0 = S_BV;         // S0 [128][128] tf32, 4 K-tiles of 16 KiB (slots 7-10)
 constexpr uint32_t S_NW = S_A;          // -W [64][128] tf32, 4 K-tiles of 8 KiB (slots 11-12)
 constexpr uint32_t S_DT = S_BV;         // D^T [128][64] tf32, 2 K-tiles of 16 KiB (slots 7-8)
 constexpr uint32_t S_P = S_A;           // P [64][64] tf32, 2 K-tiles of 8 KiB (slot 11)
+constexpr uint32_t S_YST = S_BK;        // y staging [64][128] bf16 (slot 9, free after the W product)
 
 // TMEM columns
 constexpr uint32_t C_QK = 0, C_D = 64, C_W = 128, C_Y = 192, C_S = 256, kTmemCols = 512;
@@ -77,9 +78,16 @@ __device__ __forceinline__ int aidx(int r, int c) { return r * 64 + (c ^ ((r & 7
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 
-// exp of a non-positive log-decay difference: the MUFU exp2 path (relative
-// error ~2^-22, far below the tf32 rounding these values go through).
-__device__ __forceinline__ float decay(float x) { return exp2f(x * 1.4426950408889634f); }
+// exp of a non-positive log-decay difference with the hardware base-2
+// exponential (ex2.approx: relative error ~2^-22, far below the tf32 rounding
+// these factors go through; results below 2^-126 flush to zero, which is the
+// limit the decay takes anyway).  The precise library exp2f path measured ~3x
+// slower for the 64 x 64 ratio matrices built every chunk.
+__device__ __forceinline__ float decay(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x * 1.4426950408889634f));
+    return r;
+}
 
 // One merge level of the blocked inverse: for each pair of S x S diagonal
 // blocks (a = [q0, q0+S), b = [q0+S, q0+2S)) of the unit lower triangular
@@ -197,8 +205,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         umma::tmem_st_wait();
     }
 
-    auto issue_loads = [&](int c) {
-        const int st = c & 1;
+    // per-step g, beta, mask of a chunk: gathered into registers early (threads
+    // < 64, one step each) and published to shared memory later, so the global
+    // load latency never sits in front of a block barrier
+    float pf_g = 1.0f, pf_b = 0.0f;
+    int pf_m = 0;
+    auto gather_steps = [&](int c) {
+        pf_g = 1.0f;
+        pf_b = 0.0f;
+        pf_m = 0;
+        const int t = c * kC + tid;
+        if (tid < kC && t < T) {
+            const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
+            pf_m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
+            if (pf_m) {
+                pf_g = p.g[gi];
+                pf_b = p.beta[gi];
+            }
+        }
+    };
+    auto publish_steps = [&](int c) {
+        if (tid < kC) {
+            s_g[c & 1][tid] = pf_g;
+            s_b[c & 1][tid] = pf_b;
+            s_m[c & 1][tid] = pf_m;
+        }
+    };
+    auto issue_tma = [&](int c) {
         if (tid == 0) {
             mbar_expect_tx(&bar_tma, 4 * 8192 + 16384);
             const int rowg = b * T + c * kC;
@@ -207,22 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             tma_load_2d(sm + S_KQ + 8192, &tm_q, hk * kD, rowg, &bar_tma);
             tma_load_2d(sm + S_KQ + kSlot + 8192, &tm_q, hk * kD + 64, rowg, &bar_tma);
             tma_load_2d(sm + S_V, &tm_v, hv * kD, rowg, &bar_tma);
-        }
-        if (tid < kC) {
-            const int t = c * kC + tid;
-            float gg = 1.0f, bb = 0.0f;
-            int m = 0;
-            if (t < T) {
-                const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
-                m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
-                if (m) {
-                    gg = p.g[gi];
-                    bb = p.beta[gi];
-                }
-            }
-            s_g[st][tid] = gg;
-            s_b[st][tid] = bb;
-            s_m[st][tid] = m;
         }
     };
 
@@ -244,7 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         umma::fence_after_sync();
     };
 
-    issue_loads(0);
+    issue_tma(0);
+    gather_steps(0);
+    publish_steps(0);
     __syncthreads();
 
     for (int c = 0; c < nchunks && ok; ++c) {
@@ -279,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         ok = __syncthreads_and(ok) != 0;
         if (!ok) break;
 
+        if (c + 1 < nchunks) gather_steps(c + 1);
         // ---- S2: [K;Q] K^T on the tensor core; meanwhile build the tf32 operands
         if (tid == 0) {
             umma::fence_after_sync();
@@ -346,7 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         // K and V tiles are no longer read: prefetch the next chunk
         umma::fence_before_sync();
         __syncthreads();
-        if (c + 1 < nchunks) issue_loads(c + 1);
+        if (c + 1 < nchunks) {
+            issue_tma(c + 1);
+            publish_steps(c + 1);
+        }
 
         // ---- S4: T = (I + A)^-1 by blocked doubling, in place in As
         {
@@ -398,25 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             umma::mma_commit(&bar_mma);
         }
         if (!wait_mma()) { ok = false; break; }
-        // S0 (tf32 copy) -> smem, S <- exp(lg_63) S in TMEM; -W -> smem
+        // -W -> smem (B operand of the D update)
         {
-            const float gl = s_gam[kC - 1];
-#pragma unroll
-            for (int cpart = 0; cpart < 2; ++cpart) {
-                float sv[32];
-                const uint32_t col = C_S + half * 64 + cpart * 32;
-                umma::tmem_ld32(tmem + lane_base + col, sv);
-                umma::tmem_ld_wait();
-                const int dk0 = half * 64 + cpart * 32;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    st_tf32x4(sm, S_S0 + (dk0 >> 5) * kSlot + umma::sw128(row, j * 4), sv[j], sv[j + 1], sv[j + 2],
-                              sv[j + 3]);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) sv[j] *= gl;
-                umma::tmem_st32(tmem + lane_base + col, sv);
-            }
-            umma::tmem_st_wait();
             float wv[32];
             umma::tmem_ld32(tmem + lane_base + C_W + half * 32, wv);
             umma::tmem_ld_wait();
@@ -435,27 +441,40 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             const uint32_t id = umma::idesc(128, 64, umma::kFmtTF32);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const uint32_t kt = k >> 2, ko = (k & 3) * 32;
-                const uint64_t a = umma::desc_sw128(base + S_S0 + kt * kSlot + ko);
-                umma::mma_tf32(tmem + C_D, a, umma::desc_sw128(base + S_NW + kt * 8192 + ko), id, true);
-                umma::mma_tf32(tmem + C_Y, a, umma::desc_sw128(base + S_GQ + kt * 8192 + ko), id, k > 0);
+                // A = the f32 state itself, read from TMEM (used as tf32)
+                const uint32_t kt = k >> 2, ko = (k & 3) * 32, a = tmem + C_S + 8 * k;
+                umma::mma_tf32_tmem_a(tmem + C_D, a, umma::desc_sw128(base + S_NW + kt * 8192 + ko), id, true);
+                umma::mma_tf32_tmem_a(tmem + C_Y, a, umma::desc_sw128(base + S_GQ + kt * 8192 + ko), id, k > 0);
             }
             umma::mma_commit(&bar_mma);
         }
         if (!wait_mma()) { ok = false; break; }
 
-        // ---- S7: D^T -> smem (A operand); P = M o Q K^T -> smem (B operand)
+        // ---- S7: D^T -> smem (A operand); P = M o Q K^T -> smem (B operand);
+        // S <- exp(lg_63) S in TMEM (the D and Y products have read S already)
         {
-            float dv[32];
+            const float gl = s_gam[kC - 1];
+#pragma unroll
+            for (int cpart = 0; cpart < 2; ++cpart) {
+                float sv[32];
+                const uint32_t col = C_S + half * 64 + cpart * 32;
+                umma::tmem_ld32(tmem + lane_base + col, sv);
+                umma::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sv[j] *= gl;
+                umma::tmem_st32(tmem + lane_base + col, sv);
+            }
+        }
+        {
+            // both TMEM reads in flight before the one wait
+            float dv[32], qk[32];
             umma::tmem_ld32(tmem + lane_base + C_D + half * 32, dv);
+            if (quad >= 2) umma::tmem_ld32(tmem + lane_base + C_QK + half * 32, qk);
             umma::tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
                 st_tf32x4(sm, S_DT + half * kSlot + umma::sw128(row, j * 4), dv[j], dv[j + 1], dv[j + 2], dv[j + 3]);
             if (quad >= 2) {
-                float qk[32];
-                umma::tmem_ld32(tmem + lane_base + C_QK + half * 32, qk);
-                umma::tmem_ld_wait();
                 const int r = row - 64;
                 const float lr = s_lg[r];
 #pragma unroll
@@ -487,23 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         }
         if (!wait_mma()) { ok = false; break; }
 
-        // ---- S9: y (row = dv, columns = steps)
+        // ---- S9: y through a shared staging tile [64 steps][128 dv] bf16, then
+        // 16-byte stores of the valid steps (masked steps are zero)
         {
             float yv[32];
             umma::tmem_ld32(tmem + lane_base + C_Y + half * 32, yv);
             umma::tmem_ld_wait();
-            const int dv = row;
+            uint16_t *Yst = reinterpret_cast<uint16_t *>(sm + S_YST);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const int r = half * 32 + j, t = t0 + r;
-                if (t < T) {
-                    const float out = s_m[st][r] ? yv[j] : 0.0f;
-                    p.y[(((size_t)b * T + t) * p.Hv + hv) * kD + dv] = f32_to_bf16(out);
-                }
+                const int r = half * 32 + j;
+                Yst[r * kD + row] = s_m[st][r] ? f32_to_bf16(yv[j]) : (uint16_t)0;
             }
         }
         umma::fence_before_sync();
         __syncthreads();
+        {
+            const int nv = min(kC, T - t0);
+            for (int i = tid; i < nv * (kD / 8); i += kThreads) {
+                const int r = i / (kD / 8), c8 = (i % (kD / 8)) * 8;
+                *reinterpret_cast<uint4 *>(p.y + (((size_t)b * T + t0 + r) * p.Hv + hv) * kD + c8) =
+                    *reinterpret_cast<const uint4 *>(sm + S_YST + (r * kD + c8) * 2);
+            }
+        }
     }
 
     // ---- final state (only when every wait succeeded)
