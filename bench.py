@@ -278,6 +278,83 @@ def bench_decode(gdn, w: wl.Workload, steps: int, warmup: int, dev, sampler) -> 
             "h2d": qkv_d.numel() * 2 + a_d.numel() * 2 + b_d.numel() * 2, "d2h": y_h.numel() * 2}
 
 
+def bench_decode_small(gdn, w: wl.Workload, dev, reps: int = 3) -> dict:
+    """Single-sequence decode: the workload's carried steps (1024), launched
+    back to back and as one captured CUDA graph (launch overhead removed).
+    The 2 MiB state stays in L2, so its GB/s is not an HBM-roofline figure."""
+    d = w.dims
+    d1 = d.with_(T=1)
+    inp = wl.workload_inputs(w)
+    steps = [wl.decode_step_inputs(w, i) for i in range(w.steps)]
+    qkv = torch.stack([x["qkv"][:, 0] for x in steps]).to(dev)
+    a = torch.stack([x["a"][:, 0] for x in steps]).to(dev)
+    b = torch.stack([x["b"][:, 0] for x in steps]).to(dev)
+    conv_w, A_log, dt_bias = inp["conv_w"].to(dev), inp["A_log"].to(dev), inp["dt_bias"].to(dev)
+    cs0, st0 = inp["conv_state"].to(dev), inp["state"].to(dev)
+    cs, st = cs0.clone(), st0.clone()
+    y = torch.empty((w.steps, d.B, d.Hv, d.Dv), dtype=torch.bfloat16, device=dev)
+
+    def run(stream):
+        for i in range(w.steps):
+            gdn.gdn_recurrent_decode(d1, qkv[i], conv_w, cs, a[i], b[i], A_log, dt_bias, st, None, y[i], stream)
+
+    stream = torch.cuda.current_stream()
+    run(stream)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    t_eager = []
+    for _ in range(reps):
+        cs.copy_(cs0); st.copy_(st0)
+        ev[0].record(stream); run(stream); ev[1].record(stream)
+        torch.cuda.synchronize()
+        t_eager.append(ev[0].elapsed_time(ev[1]))
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            run(torch.cuda.current_stream())
+    stream.wait_stream(side)
+    t_graph = []
+    for _ in range(reps):
+        cs.copy_(cs0); st.copy_(st0)
+        ev[0].record(stream); g.replay(); ev[1].record(stream)
+        torch.cuda.synchronize()
+        t_graph.append(ev[0].elapsed_time(ev[1]))
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the single-sequence decode benchmark")
+    by = sum(decode_bytes(d).values())
+    us_e, us_g = min(t_eager) * 1e3 / w.steps, min(t_graph) * 1e3 / w.steps
+    return {"workload": w.name, "steps": w.steps, "us_per_step_eager": round(us_e, 3),
+            "us_per_step_graph": round(us_g, 3), "tokens_per_s_graph": round(d.B / (us_g / 1e6), 1),
+            "gbs_graph_l2_resident": round(by / (us_g / 1e6) / 1e9, 1)}
+
+
+def bench_rmsnorm_gated(gdn, w: wl.Workload, dev, iters: int = 5) -> dict:
+    """The RMSNormGated output over a whole prefill output (B*T*Hv rows of Dv):
+    HBM-bound, 6 bytes per element (y and z in, out)."""
+    d = w.dims
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2000 + w.index)
+    y = (torch.randn((d.B, d.T, d.Hv, d.Dv), generator=gen, device=dev) * 0.1).to(torch.bfloat16)
+    z = torch.randn((d.B, d.T, d.Hv, d.Dv), generator=gen, device=dev).to(torch.bfloat16)
+    nw = torch.empty(d.Dv, device=dev).uniform_(0.5, 1.5, generator=gen)
+    out = torch.empty_like(y)
+    stream = torch.cuda.current_stream()
+    gdn.gdn_rmsnorm_gated(d, y, z, nw, 1e-6, out, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        gdn.gdn_rmsnorm_gated(d, y, z, nw, 1e-6, out, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    nbytes = 3 * y.numel() * 2 + d.Dv * 4
+    del y, z, out
+    return {"workload": w.name, "ms": round(ms, 4), "bytes": nbytes, "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+
+
 def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int) -> dict:
     """Full core (conv + gates + recurrence) over one workload call."""
     d = w.dims
@@ -399,8 +476,12 @@ def main():
     e2e_ms = max_over_ranks(res["e2e_ms"], ws)
     clocks = sampler.summary()
 
+    small_decode = None
+    gated_norm = None
     prefill = []
     if not args.no_prefill:
+        small_decode = bench_decode_small(gdn, wl.WORKLOADS["decode_b1"], dev)
+        gated_norm = bench_rmsnorm_gated(gdn, wl.WORKLOADS["prefill_ragged"], dev)
         for name in ("prefill_t8192", "prefill_ragged"):
             for chunk in (0, 64):
                 try:
@@ -443,6 +524,8 @@ def main():
         "gpu_launches": args.steps,
         "clocks": clocks,
         "prefill": prefill,
+        "decode_b1": small_decode,
+        "rmsnorm_gated": gated_norm,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

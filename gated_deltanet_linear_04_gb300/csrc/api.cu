@@ -203,6 +203,18 @@ gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *
                                                       gdn::error_word(), cs));
 }
 
+gdn_status gdn_rmsnorm_gated(const gdn_dims *dims, const uint16_t *y, const uint16_t *z, const float *norm_w,
+                             float norm_eps, uint16_t *out, gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    if (!(norm_eps >= 0.0f)) return GDN_ERR_INVALID_ARG;
+    const size_t n = (size_t)s.B * s.T * s.Hv;
+    if (!ok_ptr(y, n) || !ok_ptr(z, n) || !ok_ptr(norm_w, n) || !ok_ptr(out, n)) return GDN_ERR_INVALID_ARG;
+    if (n == 0) return GDN_OK;
+    return gdn::from_cuda(gdn::launch_rmsnorm_gated(s, y, z, norm_w, norm_eps, out, (cudaStream_t)stream));
+}
+
 gdn_status gdn_device_status(gdn_stream stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
     unsigned *w = gdn::error_word();

@@ -45,6 +45,7 @@ _SIGS = {
     "gdn_prefill": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
                                    ctypes.c_size_t, _P]),
     "gdn_prefill_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims), ctypes.c_int]),
+    "gdn_rmsnorm_gated": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, ctypes.c_float, _P, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_device_status": (ctypes.c_int, [_P]),
     "gdn_abi_version": (ctypes.c_int, []),
@@ -146,6 +147,13 @@ def gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, w
                              int(chunk), ws_ptr, ws_bytes, _stream(stream)), "gdn_prefill")
 
 
+def gdn_rmsnorm_gated(dims, y, z, norm_w, norm_eps, out, stream=None):
+    d = make_dims(dims)
+    _check(lib().gdn_rmsnorm_gated(ctypes.byref(d), _ptr(y, BF16, "y"), _ptr(z, BF16, "z"),
+                                   _ptr(norm_w, F32, "norm_w"), float(norm_eps), _ptr(out, BF16, "out"),
+                                   _stream(stream)), "gdn_rmsnorm_gated")
+
+
 def gdn_device_status(stream=None) -> int:
     return int(lib().gdn_device_status(_stream(stream)))
 
@@ -191,6 +199,13 @@ def prefill(dims, q, k, v, g, beta, state_in=None, mask=None, chunk=0, state_out
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
     gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk, ws, stream)
     return y, state_out
+
+
+def rmsnorm_gated(dims, y, z, norm_w, norm_eps=1e-6, stream=None):
+    """Returns out = bf16(silu(z) * w * rms_normalize(y)) shaped like y."""
+    out = torch.empty_like(y)
+    gdn_rmsnorm_gated(dims, y, z, norm_w, norm_eps, out, stream)
+    return out
 
 
 def core_prefill(dims, qkv, conv_w, a, b, A_log, dt_bias, conv_state=None, state_in=None, mask=None, chunk=0,

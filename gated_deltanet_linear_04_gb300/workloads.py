@@ -113,6 +113,15 @@ def make_activations(d: Dims, seed: int) -> dict:
     return {"qkv": qkv, "a": a, "b": b}
 
 
+def make_gate_inputs(d: Dims, seed: int) -> dict:
+    """Inputs of the RMSNormGated output: z [B, T, Hv, Dv] bf16 N(0, 1) (the
+    in_proj_z output) and the norm weight [Dv] f32 U[0.5, 1.5]."""
+    g = _gen(seed)
+    z = _normal_bf16((d.B, d.T, d.Hv, d.Dv), 1.0, g)
+    norm_w = torch.empty(d.Dv, dtype=torch.float32).uniform_(0.5, 1.5, generator=g)
+    return {"z": z, "norm_w": norm_w}
+
+
 def make_states(d: Dims, seed: int, conv_state: str, state: str) -> dict:
     g = _gen(seed)
     if conv_state == "normal":

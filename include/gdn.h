@@ -134,6 +134,18 @@ GDN_API gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const ui
                        uint16_t *y, int chunk, void *workspace, size_t ws_bytes,
                        gdn_stream stream);
 
+/* RMSNormGated output of the layer, applied to the recurrence output y.
+ * (mlex gated_delta.rs, GatedDeltaNet::forward: rms_norm of y in f32 with
+ * norm_eps, times the norm weight, times silu(z), cast to the activation dtype.)
+ *   y, z       bf16 [B, T, Hv, Dv] (in); z is the in_proj_z output
+ *   norm_w     f32  [Dv] (in)
+ *   out        bf16 [B, T, Hv, Dv] (out), per (b, t, hv) row:
+ *              out = bf16( silu(z) * w * y / sqrt(mean_Dv(y^2) + norm_eps) )
+ * Only dims->B, T, Hv, Dv are used (the others must still be valid).  out may
+ * alias y. */
+GDN_API gdn_status gdn_rmsnorm_gated(const gdn_dims *dims, const uint16_t *y, const uint16_t *z,
+                                     const float *norm_w, float norm_eps, uint16_t *out, gdn_stream stream);
+
 /* Bytes of scratch gdn_prefill needs for these sizes and this chunk mode
  * (0 for the sequential form).  Returns 0 for unsupported arguments. */
 GDN_API size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk);

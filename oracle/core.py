@@ -425,6 +425,20 @@ class _PairStates:
 
 
 # --------------------------------------------------------------------------
+# f-1: RMSNormGated output ([GD-RS] forward, after the recurrence)
+# --------------------------------------------------------------------------
+def rmsnorm_gated(y_bits, z_bits, norm_w, eps):
+    """out = bf16( silu(z) * w * y / sqrt(mean(y^2) + eps) ), the mean over the
+    last axis (Dv of one head), everything in float64 from the bf16 y and z
+    and the f32 weight [Dv]; one bf16 rounding at the end."""
+    y = bf16_to_f64(y_bits)
+    z = bf16_to_f64(z_bits)
+    w = np.asarray(norm_w, dtype=np.float64)
+    normed = rms_normalize(y, eps) * w
+    return f64_to_bf16(silu(z) * normed)
+
+
+# --------------------------------------------------------------------------
 # a7: the chunked (WY / UT-transform) form, derived from the recurrence.
 # Not on the pages; pinned against head_recurrence.
 # --------------------------------------------------------------------------

@@ -341,3 +341,37 @@ def test_decode_steps_match_prefill(gdn):
     U.assert_y_close(U.bf16_dev_to_f64(torch.stack(ys, 1)), U.bf16_dev_to_f64(y))
     U.assert_state_close(st.cpu().numpy(), s.cpu().numpy().astype(np.float64), tol=1e-5)
     assert torch.equal(cs, cs2)
+
+
+# ---------------------------------------------------------------------------
+# f-1 RMSNormGated output
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,T,Hv,Dv", [(1, 8, 2, 32), (2, 37, 4, 64), (3, 65, 32, 128), (1, 1, 64, 128)])
+def test_rmsnorm_gated(gdn, B, T, Hv, Dv):
+    d = wl.Dims(B=B, T=T, Hk=1, Hv=Hv, Dk=32, Dv=Dv)
+    gi = wl.make_gate_inputs(d, 600 + T)
+    y = (torch.randn((B, T, Hv, Dv), generator=torch.Generator().manual_seed(T)) * 0.1).to(torch.bfloat16)
+    y[0, 0] = 0                                       # a masked step's row
+    out = gdn.rmsnorm_gated(d, to_dev(y), to_dev(gi["z"]), to_dev(gi["norm_w"]), 1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.rmsnorm_gated(U.bits(y), U.bits(gi["z"]), gi["norm_w"].numpy(), 1e-6)
+    U.assert_bf16_within_one_ulp(U.bits(out), ref, "rmsnorm_gated")
+    assert np.all(U.bits(out)[0, 0] == 0)
+
+
+def test_core_then_rmsnorm_gated_tiny(gdn):
+    """The full layer core followed by the gated norm, against the oracle."""
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.workload_inputs(w)
+    d = inp["dims"]
+    gi = wl.make_gate_inputs(d, 7)
+    y, _ = gdn.core_prefill(d, to_dev(inp["qkv"]), to_dev(inp["conv_w"]), to_dev(inp["a"]), to_dev(inp["b"]),
+                            to_dev(inp["A_log"]), to_dev(inp["dt_bias"]), to_dev(inp["conv_state"]).clone(),
+                            to_dev(inp["state"]))
+    out = gdn.rmsnorm_gated(d, y, to_dev(gi["z"]), to_dev(gi["norm_w"]), 1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.layer_core(d, U.bits(inp["qkv"]), U.bits(inp["conv_w"]), U.bits(inp["a"]), U.bits(inp["b"]),
+                            inp["A_log"].numpy(), inp["dt_bias"].numpy(), U.bits(inp["conv_state"]),
+                            inp["state"].numpy().astype(np.float64))
+    ref_out = oracle.rmsnorm_gated(ref["y_bf16"], U.bits(gi["z"]), gi["norm_w"].numpy(), 1e-6)
+    U.assert_y_close(U.bf16_dev_to_f64(out), oracle.bf16_to_f64(ref_out), "gated output")

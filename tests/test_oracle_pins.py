@@ -400,3 +400,37 @@ def test_decode_steps_equal_one_prefill(oracle_mod):
         assert np.array_equal(out["y"][:, 0], full["y"][:, t])
         cs, st = out["conv_state"], out["state"]
     assert np.array_equal(st, full["state"]) and np.array_equal(cs, full["conv_state"])
+
+
+# ----------------------------------------------------------------------------
+# f-1 RMSNormGated: pinned to torch's rms_norm and silu (float64 on the CPU)
+# ----------------------------------------------------------------------------
+def test_rmsnorm_gated_against_torch(oracle_mod):
+    o = oracle_mod
+    rng = np.random.default_rng(21)
+    Dv = 64
+    y = o.f64_to_bf16(rng.standard_normal((3, 5, 4, Dv)) * 0.1)
+    z = o.f64_to_bf16(rng.standard_normal((3, 5, 4, Dv)))
+    w = rng.uniform(0.5, 1.5, Dv).astype(np.float32)
+    eps = 1e-6
+    got = o.rmsnorm_gated(y, z, w, eps)
+    yt = torch.from_numpy(o.bf16_to_f64(y))
+    zt = torch.from_numpy(o.bf16_to_f64(z))
+    ref = torch.nn.functional.silu(zt) * torch.nn.functional.rms_norm(
+        yt, (Dv,), weight=torch.from_numpy(w.astype(np.float64)), eps=eps)
+    ref_bits = ref.to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    # one rounding from f64 vs f64 -> f32 -> bf16: equal except on exact f32 ties
+    assert np.mean(got == ref_bits) > 0.999
+
+
+def test_rmsnorm_gated_closed_forms(oracle_mod):
+    o = oracle_mod
+    Dv = 32
+    y = o.f64_to_bf16(np.full((1, Dv), -0.5))          # constant row: y / rms(y) = -1 (eps negligible)
+    z = o.f64_to_bf16(np.full((1, Dv), 8.0))           # silu(8) = 8 sigmoid(8)
+    w = np.linspace(0.5, 2.0, Dv).astype(np.float32)
+    out = o.bf16_to_f64(o.rmsnorm_gated(y, z, w, 1e-6))
+    expect = -(8.0 / (1.0 + math.exp(-8.0))) * w.astype(np.float64) / math.sqrt(1.0 + 4e-6)
+    assert np.allclose(out, expect, rtol=2 ** -8)
+    zero = o.bf16_to_f64(o.rmsnorm_gated(o.f64_to_bf16(np.zeros((2, Dv))), z.repeat(2, 0), w, 1e-6))
+    assert np.all(zero == 0.0)                          # a zero row (masked step) stays zero
