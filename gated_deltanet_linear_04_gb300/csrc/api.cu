@@ -164,6 +164,24 @@ gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qkv, const
                                              gdn::error_word(), (cudaStream_t)stream));
 }
 
+gdn_status gdn_decode_window(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
+                             uint16_t *conv_state, const uint16_t *a, const uint16_t *b, const float *A_log,
+                             const float *dt_bias, float *state, const int32_t *keep, uint16_t *y,
+                             gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    if (s.T < 1 || s.T > 8) return GDN_ERR_UNSUPPORTED;
+    if (s.Hv / s.Hk > 16) return GDN_ERR_UNSUPPORTED;
+    const size_t B = (size_t)s.B;
+    if (!ok_ptr(qkv, B) || !ok_ptr(conv_w, B) || !ok_ptr(conv_state, B) || !ok_ptr(a, B) || !ok_ptr(b, B) ||
+        !ok_ptr(A_log, B) || !ok_ptr(dt_bias, B) || !ok_ptr(state, B) || !ok_ptr(keep, 0) || !ok_ptr(y, B))
+        return GDN_ERR_INVALID_ARG;
+    if (B == 0) return GDN_OK;
+    return gdn::from_cuda(gdn::launch_decode_window(s, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep,
+                                                    y, gdn::error_word(), (cudaStream_t)stream));
+}
+
 size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk) {
     gdn::Sizes s;
     if (gdn::check_dims(dims, &s) != GDN_OK) return 0;

@@ -29,6 +29,10 @@ cudaError_t launch_decode(const Sizes &s, const uint16_t *qkv, const uint16_t *c
                           const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
                           float *state, const uint8_t *row_mask, uint16_t *y, unsigned *err, cudaStream_t st);
 
+cudaError_t launch_decode_window(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
+                                 const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
+                                 float *state, const int32_t *keep, uint16_t *y, unsigned *err, cudaStream_t st);
+
 // Encodes a 2-D row-major tensor map (rows x cols, box rows x box_cols).
 bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
                     uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,

@@ -45,6 +45,7 @@ _SIGS = {
     "gdn_prefill": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
                                    ctypes.c_size_t, _P]),
     "gdn_prefill_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims), ctypes.c_int]),
+    "gdn_decode_window": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_rmsnorm_gated": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, ctypes.c_float, _P, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_device_status": (ctypes.c_int, [_P]),
@@ -132,6 +133,15 @@ def gdn_recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, st
                                       _ptr(y, BF16, "y"), _stream(stream)), "gdn_recurrent_decode")
 
 
+def gdn_decode_window(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep, y, stream=None):
+    d = make_dims(dims)
+    _check(lib().gdn_decode_window(ctypes.byref(d), _ptr(qkv, BF16, "qkv"), _ptr(conv_w, BF16, "conv_w"),
+                                   _ptr(conv_state, BF16, "conv_state"), _ptr(a, BF16, "a"), _ptr(b, BF16, "b"),
+                                   _ptr(A_log, F32, "A_log"), _ptr(dt_bias, F32, "dt_bias"),
+                                   _ptr(state, F32, "state"), _ptr(keep, torch.int32, "keep"), _ptr(y, BF16, "y"),
+                                   _stream(stream)), "gdn_decode_window")
+
+
 def gdn_prefill_workspace_size(dims, chunk: int) -> int:
     d = make_dims(dims)
     return int(lib().gdn_prefill_workspace_size(ctypes.byref(d), int(chunk)))
@@ -186,6 +196,14 @@ def recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state,
     """One token; conv_state and state are updated in place.  Returns y [B, Hv, Dv]."""
     y = torch.empty((dims.B, dims.Hv, dims.Dv), dtype=BF16, device=qkv.device)
     gdn_recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y, stream)
+    return y
+
+
+def decode_window(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep=None, stream=None):
+    """dims.T tokens per row; conv_state and state advance by keep[b] (default
+    all) tokens in place.  Returns y [B, T, Hv, Dv]."""
+    y = torch.empty((dims.B, dims.T, dims.Hv, dims.Dv), dtype=BF16, device=qkv.device)
+    gdn_decode_window(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep, y, stream)
     return y
 
 

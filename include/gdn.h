@@ -114,6 +114,26 @@ GDN_API gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qk
                                 const float *A_log, const float *dt_bias, float *state,
                                 const uint8_t *row_mask, uint16_t *y, gdn_stream stream);
 
+/* Multi-token decode window for speculative verification: dims->T (1..8)
+ * new tokens per row, fused like gdn_recurrent_decode (one pass over the f32
+ * state).  y is written for all T tokens; conv_state and state are advanced by
+ * exactly keep[b] leading tokens of row b, so a verify call with keep = NULL
+ * (all tokens) or a commit call with the accepted counts gives the state after
+ * the accepted prefix.  (mlx-bun qwen3-delta.ts, SsmSpecRound and
+ * specRoundRollback: a window of S tokens whose first `keep` are kept, the
+ * state after them being the same arithmetic prefix; gated_delta_step.)
+ *   qkv        bf16 [B, T, C] (in)          conv_w bf16 [C, K] (in)
+ *   conv_state bf16 [B, K-1, C] in/out      a, b bf16 [B, T, Hv] (in)
+ *   A_log, dt_bias f32 [Hv] (in)            state f32 [B, Hv, Dv, Dk] in/out
+ *   keep       int32 [B] or NULL (= T); values are clamped to [0, T]; 0 leaves
+ *              both states untouched (y is still produced)
+ *   y          bf16 [B, T, Hv, Dv] (out)
+ * Supports Hv/Hk <= 16; dims->T outside 1..8 gives GDN_ERR_UNSUPPORTED. */
+GDN_API gdn_status gdn_decode_window(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
+                                     uint16_t *conv_state, const uint16_t *a, const uint16_t *b,
+                                     const float *A_log, const float *dt_bias, float *state,
+                                     const int32_t *keep, uint16_t *y, gdn_stream stream);
+
 /* The recurrence over T steps (prefill).  (mlx-bun qwen3-delta.ts,
  * gatedDeltaUpdate and the gated_delta_step kernel with its masked
  * specialization; mlex gated_delta.rs, the per-timestep loop.)

@@ -375,3 +375,66 @@ def test_core_then_rmsnorm_gated_tiny(gdn):
                             inp["state"].numpy().astype(np.float64))
     ref_out = oracle.rmsnorm_gated(ref["y_bf16"], U.bits(gi["z"]), gi["norm_w"].numpy(), 1e-6)
     U.assert_y_close(U.bf16_dev_to_f64(out), oracle.bf16_to_f64(ref_out), "gated output")
+
+
+# ---------------------------------------------------------------------------
+# f-2 multi-token decode window (speculative verify / accepted-prefix commit)
+# ---------------------------------------------------------------------------
+WINDOW_CASES = [
+    # B, Hk, Hv, Dk, Dv, K, T, keep
+    (2, 2, 4, 128, 128, 4, 4, None),
+    (3, 1, 2, 64, 64, 3, 5, [0, 2, 5]),
+    (2, 16, 32, 128, 128, 4, 8, [8, 3]),
+    (1, 1, 16, 32, 128, 2, 1, [1]),
+    (4, 2, 8, 128, 64, 4, 7, [7, 0, 1, 6]),
+]
+
+
+@pytest.mark.parametrize("B,Hk,Hv,Dk,Dv,K,T,keep", WINDOW_CASES)
+def test_decode_window(gdn, B, Hk, Hv, Dk, Dv, K, T, keep):
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, K=K)
+    inp = inputs_for(d, 700 + B * T)
+    keep_t = None if keep is None else torch.tensor(keep, dtype=torch.int32)
+    cs = to_dev(inp["conv_state"]).clone()
+    st = to_dev(inp["state"]).clone()
+    y = gdn.decode_window(d, to_dev(inp["qkv"]), to_dev(inp["conv_w"]), cs, to_dev(inp["a"]), to_dev(inp["b"]),
+                          to_dev(inp["A_log"]), to_dev(inp["dt_bias"]), st, to_dev(keep_t))
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    args = (U.bits(inp["qkv"]), U.bits(inp["conv_w"]), U.bits(inp["a"]), U.bits(inp["b"]), inp["A_log"].numpy(),
+            inp["dt_bias"].numpy(), U.bits(inp["conv_state"]), inp["state"].numpy().astype(np.float64))
+    full = oracle.layer_core(d, *args)
+    U.assert_y_close(U.bf16_dev_to_f64(y), full["y"], "window y")
+    st_h, cs_h = st.cpu().numpy(), U.bits(cs)
+    for bb in range(B):
+        kb = T if keep is None else keep[bb]
+        if kb == 0:
+            assert np.array_equal(st_h[bb], inp["state"][bb].numpy()), "keep 0: state untouched"
+            assert np.array_equal(cs_h[bb], U.bits(inp["conv_state"])[bb]), "keep 0: conv_state untouched"
+            continue
+        dr = d.with_(B=1, T=kb)
+        row = lambda x: np.ascontiguousarray(x[bb:bb + 1, :kb])
+        ref = oracle.layer_core(dr, row(args[0]), args[1], row(args[2]), row(args[3]), args[4], args[5],
+                                np.ascontiguousarray(args[6][bb:bb + 1]), args[7][bb:bb + 1])
+        U.assert_state_close(st_h[bb], ref["state"][0], "state after %d kept tokens" % kb)
+        assert np.array_equal(cs_h[bb], ref["conv_state"][0]), "conv_state after the kept prefix"
+
+
+def test_decode_window_commit_equals_single_steps(gdn):
+    """A window committed with keep = k gives the states that k single-token
+    decode steps give (conv_state bit for bit, state within f32 rounding)."""
+    d = wl.Dims(B=2, T=6, Hk=2, Hv=4, Dk=128, Dv=128)
+    inp = inputs_for(d, 77)
+    keep = [4, 6]
+    cs_w, st_w = to_dev(inp["conv_state"]).clone(), to_dev(inp["state"]).clone()
+    gdn.decode_window(d, to_dev(inp["qkv"]), to_dev(inp["conv_w"]), cs_w, to_dev(inp["a"]), to_dev(inp["b"]),
+                      to_dev(inp["A_log"]), to_dev(inp["dt_bias"]), st_w, to_dev(torch.tensor(keep, dtype=torch.int32)))
+    for bb, kb in enumerate(keep):
+        d1 = d.with_(B=1)
+        sub = {k: inp[k][bb:bb + 1] for k in ("qkv", "a", "b")}
+        steps = [{k: sub[k][:, t:t + 1] for k in sub} for t in range(kb)]
+        one = {"conv_state": inp["conv_state"][bb:bb + 1], "state": inp["state"][bb:bb + 1],
+               "conv_w": inp["conv_w"], "A_log": inp["A_log"], "dt_bias": inp["dt_bias"]}
+        _, st1, cs1 = run_decode_gpu(gdn, d1, one, steps)
+        assert torch.equal(cs1[0], cs_w[bb])
+        U.assert_state_close(st_w[bb].cpu().numpy(), st1[0].cpu().numpy().astype(np.float64), tol=1e-5)
