@@ -330,6 +330,40 @@ def bench_decode_small(gdn, w: wl.Workload, dev, reps: int = 3) -> dict:
             "gbs_graph_l2_resident": round(by / (us_g / 1e6) / 1e9, 1)}
 
 
+def bench_decode_window(gdn, w: wl.Workload, dev, T: int = 4, iters: int = 20) -> dict:
+    """Speculative-verify window: T tokens per row of the batched-decode
+    workload in one fused kernel, all T committed (the state is streamed once
+    per window instead of once per token)."""
+    d = w.dims.with_(T=T)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000 + w.index)
+    qkv = torch.randn((d.B, T, d.C), generator=gen, device=dev).to(torch.bfloat16)
+    a = torch.randn((d.B, T, d.Hv), generator=gen, device=dev).to(torch.bfloat16)
+    b = torch.randn((d.B, T, d.Hv), generator=gen, device=dev).to(torch.bfloat16)
+    conv_w = (torch.randn((d.C, d.K), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
+    A_log = torch.log(torch.empty(d.Hv, device=dev).uniform_(1.0, 16.0, generator=gen))
+    dt_bias = torch.randn(d.Hv, generator=gen, device=dev) * 0.5
+    cs = torch.randn((d.B, d.K - 1, d.C), generator=gen, device=dev).to(torch.bfloat16)
+    st = torch.randn((d.B, d.Hv, d.Dv, d.Dk), generator=gen, device=dev) * 0.05
+    y = torch.empty((d.B, T, d.Hv, d.Dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        gdn.gdn_decode_window(d, qkv, conv_w, cs, a, b, A_log, dt_bias, st, None, y, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        gdn.gdn_decode_window(d, qkv, conv_w, cs, a, b, A_log, dt_bias, st, None, y, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the decode-window benchmark")
+    ms = e0.elapsed_time(e1) / iters
+    state_rw = 2 * d.B * d.Hv * d.Dv * d.Dk * 4
+    return {"workload": w.name, "window": T, "us_per_window": round(ms * 1e3, 2),
+            "tokens_per_s": round(d.B * T / (ms / 1e3), 1), "state_gbs": round(state_rw / (ms / 1e3) / 1e9, 1)}
+
+
 def bench_rmsnorm_gated(gdn, w: wl.Workload, dev, iters: int = 5) -> dict:
     """The RMSNormGated output over a whole prefill output (B*T*Hv rows of Dv):
     HBM-bound, 6 bytes per element (y and z in, out)."""
@@ -478,10 +512,12 @@ def main():
 
     small_decode = None
     gated_norm = None
+    window = None
     prefill = []
     if not args.no_prefill:
         small_decode = bench_decode_small(gdn, wl.WORKLOADS["decode_b1"], dev)
         gated_norm = bench_rmsnorm_gated(gdn, wl.WORKLOADS["prefill_ragged"], dev)
+        window = bench_decode_window(gdn, w, dev)
         for name in ("prefill_t8192", "prefill_ragged"):
             for chunk in (0, 64):
                 try:
@@ -526,6 +562,7 @@ def main():
         "prefill": prefill,
         "decode_b1": small_decode,
         "rmsnorm_gated": gated_norm,
+        "decode_window": window,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
