@@ -233,6 +233,29 @@ gdn_status gdn_rmsnorm_gated(const gdn_dims *dims, const uint16_t *y, const uint
     return gdn::from_cuda(gdn::launch_rmsnorm_gated(s, y, z, norm_w, norm_eps, out, (cudaStream_t)stream));
 }
 
+gdn_status gdn_prefill_vec(const gdn_dims *dims, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           const float *g_vec, const float *beta, const float *state_in, float *state_out,
+                           const uint8_t *mask, uint16_t *y, gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    const size_t BT = (size_t)s.B * s.T;
+    const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
+    if (!ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT) || !ok_ptr(g_vec, BT) || !ok_ptr(beta, BT) ||
+        !ok_ptr(state_in, 0) || !ok_ptr(state_out, nstate) || !ok_ptr(mask, 0) || !ok_ptr(y, BT))
+        return GDN_ERR_INVALID_ARG;
+    if (s.B == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (s.T == 0) {
+        if (state_in == nullptr) return gdn::from_cuda(cudaMemsetAsync(state_out, 0, nstate * sizeof(float), cs));
+        if (state_in == state_out) return GDN_OK;
+        return gdn::from_cuda(
+            cudaMemcpyAsync(state_out, state_in, nstate * sizeof(float), cudaMemcpyDeviceToDevice, cs));
+    }
+    return gdn::from_cuda(gdn::launch_prefill_seq_vec(s, q, k, v, g_vec, beta, state_in, state_out, mask, y,
+                                                      gdn::error_word(), cs));
+}
+
 gdn_status gdn_device_status(gdn_stream stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
     unsigned *w = gdn::error_word();

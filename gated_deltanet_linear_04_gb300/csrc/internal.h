@@ -45,6 +45,10 @@ cudaError_t launch_prefill_seq(const Sizes &s, const uint16_t *q, const uint16_t
 cudaError_t launch_rmsnorm_gated(const Sizes &s, const uint16_t *y, const uint16_t *z, const float *norm_w,
                                  float eps, uint16_t *out, cudaStream_t st);
 
+cudaError_t launch_prefill_seq_vec(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                   const float *g_vec, const float *beta, const float *state_in, float *state_out,
+                                   const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st);
+
 size_t prefill_chunked_workspace(const Sizes &s);
 
 cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,

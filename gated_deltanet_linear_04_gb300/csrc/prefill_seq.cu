@@ -33,7 +33,7 @@ struct SeqParams {
 
 __host__ __device__ constexpr int align128(int x) { return (x + 127) & ~127; }
 
-template <int DK, int R>
+template <int DK, int R, bool VEC>
 struct SeqSmem {
     static constexpr int q_off = 0;
     static constexpr int k_off = q_off + align128(kTC * DK * 2);
@@ -42,10 +42,12 @@ struct SeqSmem {
     static constexpr int b_off = g_off + kTC * 4;
     static constexpr int kq_off = b_off + kTC * 4;
     static constexpr int m_off = kq_off + kTC * 4;
-    static constexpr int stage_bytes = align128(m_off + kTC * 4);
+    // per-channel gate tile [kTC][DK] f32 (vectorized gating only)
+    static constexpr int gv_off = align128(m_off + kTC * 4);
+    static constexpr int stage_bytes = VEC ? align128(gv_off + kTC * DK * 4) : align128(m_off + kTC * 4);
     static constexpr int y_off = 2 * stage_bytes;
     static constexpr int total = y_off + kTC * R * 4;
-    static constexpr uint32_t tx_bytes = (uint32_t)(2 * kTC * DK * 2 + kTC * R * 2);
+    static constexpr uint32_t tx_bytes = (uint32_t)(2 * kTC * DK * 2 + kTC * R * 2 + (VEC ? kTC * DK * 4 : 0));
 };
 
 template <int CW>
@@ -61,14 +63,17 @@ __device__ __forceinline__ void load_row_bf16(const uint16_t *p, float (&o)[CW])
     }
 }
 
-template <int DK, int RPL>
+// VEC: vectorized gating, one decay factor per key channel (g [B, T, Hv, Dk],
+// staged by TMA with q/k/v); the state columns are decayed before the dots.
+template <int DK, int RPL, bool VEC>
 __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                const __grid_constant__ CUtensorMap tm_k,
                                                                const __grid_constant__ CUtensorMap tm_v,
+                                                               const __grid_constant__ CUtensorMap tm_g,
                                                                const SeqParams p) {
     constexpr int R = 16 * RPL;
     constexpr int CW = DK / 8;
-    using L = SeqSmem<DK, R>;
+    using L = SeqSmem<DK, R, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full_bar[2];
 
@@ -124,6 +129,7 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
             tma_load_2d(base + L::q_off, &tm_q, hk * DK, row, &full_bar[st]);
             tma_load_2d(base + L::k_off, &tm_k, hk * DK, row, &full_bar[st]);
             tma_load_2d(base + L::v_off, &tm_v, hv * p.Dv + r0, row, &full_bar[st]);
+            if constexpr (VEC) tma_load_2d(base + L::gv_off, &tm_g, hv * DK, row, &full_bar[st]);
         }
         if (tid < kTC) {
             const int t = c * kTC + tid;
@@ -131,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
             int m = 0;
             if (t < T) {
                 const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
-                gg = p.g[gi];
+                if constexpr (!VEC) gg = p.g[gi];
                 bb = p.beta[gi];
                 m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
             }
@@ -182,10 +188,27 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
                 }
                 continue;
             }
-            const float g = gs[t], beta = bs[t], kq = kqs[t];
+            float g = gs[t];
+            const float beta = bs[t], kq = kqs[t];
             float kf[CW], qf[CW];
             load_row_bf16<CW>(ks + t * DK + cg * CW, kf);
             load_row_bf16<CW>(qs + t * DK + cg * CW, qf);
+            if constexpr (VEC) {
+                // decay each state column by its own factor, then proceed with g = 1
+                const float *gt = reinterpret_cast<const float *>(base + L::gv_off) + t * DK + cg * CW;
+#pragma unroll
+                for (int j = 0; j < CW; j += 4) {
+                    const float4 gv = *reinterpret_cast<const float4 *>(gt + j);
+#pragma unroll
+                    for (int i = 0; i < RPL; ++i) {
+                        s[i][j] *= gv.x;
+                        s[i][j + 1] *= gv.y;
+                        s[i][j + 2] *= gv.z;
+                        s[i][j + 3] *= gv.w;
+                    }
+                }
+                g = 1.0f;
+            }
             float dk[RPL], dq[RPL];
 #pragma unroll
             for (int i = 0; i < RPL; ++i) {
@@ -241,27 +264,51 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
     }
 }
 
-template <int DK, int RPL>
+template <int DK, int RPL, bool VEC>
 cudaError_t launch_seq_t(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                          const SeqParams &p, cudaStream_t st) {
     constexpr int R = 16 * RPL;
-    using L = SeqSmem<DK, R>;
-    CUtensorMap tq, tk, tv;
+    using L = SeqSmem<DK, R, VEC>;
+    CUtensorMap tq, tk, tv, tg;
     const uint64_t rows = (uint64_t)s.B * (uint64_t)(s.T > 0 ? s.T : 1);
     if (!encode_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * DK, kTC, DK) ||
         !encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * DK, kTC, DK) ||
         !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * s.Dv, kTC, R))
         return cudaErrorInvalidValue;
+    if constexpr (VEC) {
+        if (!encode_tmap_2d(&tg, p.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rows, (uint64_t)s.Hv * DK, kTC, DK))
+            return cudaErrorInvalidValue;
+    } else {
+        tg = tq;   // unused
+    }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_seq_kernel<DK, RPL>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_seq_kernel<DK, RPL, VEC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(s.Hv * (s.Dv / R), s.B);
-    prefill_seq_kernel<DK, RPL><<<grid, kThreads, L::total, st>>>(tq, tk, tv, p);
+    prefill_seq_kernel<DK, RPL, VEC><<<grid, kThreads, L::total, st>>>(tq, tk, tv, tg, p);
     return cudaGetLastError();
+}
+
+template <bool VEC>
+cudaError_t launch_seq_any(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           const SeqParams &p, cudaStream_t st) {
+    // 32-row CTAs when there are enough of them to fill the GPU, else 16-row
+    const long ctas32 = (long)s.B * s.Hv * (s.Dv / 32);
+    const bool small = ctas32 < num_sms();
+    switch (s.Dk) {
+        case 32:
+            return small ? launch_seq_t<32, 1, VEC>(s, q, k, v, p, st) : launch_seq_t<32, 2, VEC>(s, q, k, v, p, st);
+        case 64:
+            return small ? launch_seq_t<64, 1, VEC>(s, q, k, v, p, st) : launch_seq_t<64, 2, VEC>(s, q, k, v, p, st);
+        case 128:
+            return small ? launch_seq_t<128, 1, VEC>(s, q, k, v, p, st)
+                         : launch_seq_t<128, 2, VEC>(s, q, k, v, p, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -270,16 +317,14 @@ cudaError_t launch_prefill_seq(const Sizes &s, const uint16_t *q, const uint16_t
                                const float *g, const float *beta, const float *state_in, float *state_out,
                                const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st) {
     SeqParams p{g, beta, state_in, state_out, mask, y, err, s.B, s.T, s.Hk, s.Hv, s.Dv};
-    // 32-row CTAs when there are enough of them to fill the GPU, else 16-row
-    const long ctas32 = (long)s.B * s.Hv * (s.Dv / 32);
-    const bool small = ctas32 < num_sms();
-    switch (s.Dk) {
-        case 32: return small ? launch_seq_t<32, 1>(s, q, k, v, p, st) : launch_seq_t<32, 2>(s, q, k, v, p, st);
-        case 64: return small ? launch_seq_t<64, 1>(s, q, k, v, p, st) : launch_seq_t<64, 2>(s, q, k, v, p, st);
-        case 128:
-            return small ? launch_seq_t<128, 1>(s, q, k, v, p, st) : launch_seq_t<128, 2>(s, q, k, v, p, st);
-        default: return cudaErrorInvalidValue;
-    }
+    return launch_seq_any<false>(s, q, k, v, p, st);
+}
+
+cudaError_t launch_prefill_seq_vec(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                   const float *g_vec, const float *beta, const float *state_in, float *state_out,
+                                   const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st) {
+    SeqParams p{g_vec, beta, state_in, state_out, mask, y, err, s.B, s.T, s.Hk, s.Hv, s.Dv};
+    return launch_seq_any<true>(s, q, k, v, p, st);
 }
 
 }  // namespace gdn

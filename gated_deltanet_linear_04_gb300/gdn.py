@@ -44,6 +44,7 @@ _SIGS = {
     "gdn_recurrent_decode": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_prefill": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
                                    ctypes.c_size_t, _P]),
+    "gdn_prefill_vec": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_prefill_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims), ctypes.c_int]),
     "gdn_decode_window": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_rmsnorm_gated": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, ctypes.c_float, _P, _P]),
@@ -164,6 +165,14 @@ def gdn_rmsnorm_gated(dims, y, z, norm_w, norm_eps, out, stream=None):
                                    _stream(stream)), "gdn_rmsnorm_gated")
 
 
+def gdn_prefill_vec(dims, q, k, v, g_vec, beta, state_in, state_out, mask, y, stream=None):
+    d = make_dims(dims)
+    _check(lib().gdn_prefill_vec(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
+                                 _ptr(g_vec, F32, "g_vec"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
+                                 _ptr(state_out, F32, "state_out"), _ptr(mask, U8, "mask"), _ptr(y, BF16, "y"),
+                                 _stream(stream)), "gdn_prefill_vec")
+
+
 def gdn_device_status(stream=None) -> int:
     return int(lib().gdn_device_status(_stream(stream)))
 
@@ -224,6 +233,14 @@ def rmsnorm_gated(dims, y, z, norm_w, norm_eps=1e-6, stream=None):
     out = torch.empty_like(y)
     gdn_rmsnorm_gated(dims, y, z, norm_w, norm_eps, out, stream)
     return out
+
+
+def prefill_vec(dims, q, k, v, g_vec, beta, state_in=None, mask=None, stream=None):
+    """Vectorized gating (g_vec [B, T, Hv, Dk]); returns (y, state_out)."""
+    y = torch.empty((dims.B, dims.T, dims.Hv, dims.Dv), dtype=BF16, device=q.device)
+    state_out = torch.empty((dims.B, dims.Hv, dims.Dv, dims.Dk), dtype=F32, device=q.device)
+    gdn_prefill_vec(dims, q, k, v, g_vec, beta, state_in, state_out, mask, y, stream)
+    return y, state_out
 
 
 def core_prefill(dims, qkv, conv_w, a, b, A_log, dt_bias, conv_state=None, state_in=None, mask=None, chunk=0,

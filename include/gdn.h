@@ -166,6 +166,17 @@ GDN_API gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const ui
 GDN_API gdn_status gdn_rmsnorm_gated(const gdn_dims *dims, const uint16_t *y, const uint16_t *z,
                                      const float *norm_w, float norm_eps, uint16_t *out, gdn_stream stream);
 
+/* The recurrence with vectorized gating: one decay factor per key channel,
+ * S <- S diag(g_t) in place of S <- g_t S (the variant the qwen3-delta.ts
+ * page of mlx-bun names beside the scalar one; the rest of the step as in
+ * gdn_prefill).  Sequential form.
+ *   g_vec      f32  [B, T, Hv, Dk] (in): the per-channel decay factors
+ *   other arguments as gdn_prefill (q, k, v, beta, state_in, state_out, mask, y) */
+GDN_API gdn_status gdn_prefill_vec(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
+                                   const uint16_t *v, const float *g_vec, const float *beta,
+                                   const float *state_in, float *state_out, const uint8_t *mask,
+                                   uint16_t *y, gdn_stream stream);
+
 /* Bytes of scratch gdn_prefill needs for these sizes and this chunk mode
  * (0 for the sequential form).  Returns 0 for unsupported arguments. */
 GDN_API size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk);

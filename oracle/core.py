@@ -75,6 +75,8 @@ def _load():
                                                    dp, dp, dp, dp, dp,
                                                    ctypes.POINTER(ctypes.c_uint8), dp, dp]
             lib.oracle_delta_rule_head.restype = None
+            lib.oracle_delta_rule_head_vec.argtypes = lib.oracle_delta_rule_head.argtypes
+            lib.oracle_delta_rule_head_vec.restype = None
             _lib = lib
     return _lib
 
@@ -276,6 +278,46 @@ def head_recurrence(q, k, v, g, beta, S0, mask=None):
     lib.oracle_delta_rule_head(T, Dk, Dv, _dptr(q), _dptr(k), _dptr(v), _dptr(g), _dptr(beta),
                                mp, _dptr(S), _dptr(y))
     return y, S
+
+
+def head_recurrence_vec(q, k, v, g, beta, S0, mask=None):
+    """Vectorized gating (one decay per key channel): g [T, Dk]; otherwise as
+    head_recurrence.  Returns (y [T,Dv], S_T [Dv,Dk]) in float64."""
+    lib = _load()
+    q = np.ascontiguousarray(q, np.float64)
+    k = np.ascontiguousarray(k, np.float64)
+    v = np.ascontiguousarray(v, np.float64)
+    g = np.ascontiguousarray(g, np.float64)
+    beta = np.ascontiguousarray(beta, np.float64)
+    S = np.array(S0, dtype=np.float64, order="C", copy=True)
+    T, Dk = q.shape
+    Dv = v.shape[1]
+    assert g.shape == (T, Dk) and S.shape == (Dv, Dk)
+    y = np.zeros((T, Dv), np.float64)
+    m = None if mask is None else np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    mp = None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+    lib.oracle_delta_rule_head_vec(T, Dk, Dv, _dptr(q), _dptr(k), _dptr(v), _dptr(g), _dptr(beta), mp, _dptr(S),
+                                   _dptr(y))
+    return y, S
+
+
+def recurrence_vec(d, q_bits, k_bits, v_bits, g, beta, state_in=None, mask=None, threads=None):
+    """All (b, hv) heads with vectorized gating g [B,T,Hv,Dk] (float64)."""
+    pairs = [(b, hv) for b in range(d.B) for hv in range(d.Hv)]
+    state_out = np.zeros((d.B, d.Hv, d.Dv, d.Dk)) if state_in is None else np.array(state_in, np.float64)
+    y = np.zeros((d.B, d.T, d.Hv, d.Dv))
+
+    def one(pair):
+        b, hv = pair
+        hk = k_head_of(d, hv)
+        yy, S = head_recurrence_vec(bf16_to_f64(q_bits[b, :, hk]), bf16_to_f64(k_bits[b, :, hk]),
+                                    bf16_to_f64(v_bits[b, :, hv]), g[b, :, hv], beta[b, :, hv], state_out[b, hv],
+                                    None if mask is None else mask[b])
+        y[b, :, hv] = yy
+        state_out[b, hv] = S
+
+    _map_threads(one, pairs, threads)
+    return y, state_out
 
 
 def _default_threads() -> int:

@@ -56,3 +56,42 @@ void oracle_delta_rule_head(int T, int Dk, int Dv,
         }
     }
 }
+
+/*
+ * Vectorized gating: the decay is one factor per key channel, g [T, Dk]
+ * (the variant the qwen3-delta.ts page names beside the scalar one):
+ *   S <- S diag(g_t), then the same kv_mem / delta / update / output steps.
+ */
+void oracle_delta_rule_head_vec(int T, int Dk, int Dv,
+                                const double *q, const double *k, const double *v,
+                                const double *g, const double *beta,
+                                const uint8_t *mask, double *S, double *y)
+{
+    for (int t = 0; t < T; ++t) {
+        const double *qt = q + (size_t)t * Dk;
+        const double *kt = k + (size_t)t * Dk;
+        const double *vt = v + (size_t)t * Dv;
+        const double *gt = g + (size_t)t * Dk;
+        double *yt = y + (size_t)t * Dv;
+        if (mask != NULL && mask[t] == 0) {
+            for (int i = 0; i < Dv; ++i) yt[i] = 0.0;
+            continue;
+        }
+        /* S <- S diag(g_t): column j scaled by g_t[j] */
+        for (int i = 0; i < Dv; ++i)
+            for (int j = 0; j < Dk; ++j) S[(size_t)i * Dk + j] *= gt[j];
+        for (int i = 0; i < Dv; ++i) {
+            double *Si = S + (size_t)i * Dk;
+            double kv = 0.0;
+            for (int j = 0; j < Dk; ++j) kv += Si[j] * kt[j];
+            double delta = beta[t] * (vt[i] - kv);
+            for (int j = 0; j < Dk; ++j) Si[j] += delta * kt[j];
+        }
+        for (int i = 0; i < Dv; ++i) {
+            const double *Si = S + (size_t)i * Dk;
+            double acc = 0.0;
+            for (int j = 0; j < Dk; ++j) acc += Si[j] * qt[j];
+            yt[i] = acc;
+        }
+    }
+}

@@ -438,3 +438,46 @@ def test_decode_window_commit_equals_single_steps(gdn):
         _, st1, cs1 = run_decode_gpu(gdn, d1, one, steps)
         assert torch.equal(cs1[0], cs_w[bb])
         U.assert_state_close(st_w[bb].cpu().numpy(), st1[0].cpu().numpy().astype(np.float64), tol=1e-5)
+
+
+# ---------------------------------------------------------------------------
+# f-3 vectorized gating (one decay per key channel), sequential form
+# ---------------------------------------------------------------------------
+VEC_CASES = [
+    # B, T, Hk, Hv, Dk, Dv, mask
+    (1, 8, 1, 2, 32, 32, None),
+    (2, 65, 2, 4, 128, 128, "random"),
+    (1, 130, 1, 2, 64, 128, "right"),
+    (3, 40, 1, 3, 128, 32, "allmasked_row"),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,Dk,Dv,mk", VEC_CASES)
+def test_prefill_vec_gating(gdn, B, T, Hk, Hv, Dk, Dv, mk):
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv)
+    mask = make_mask(mk, B, T, 9 + T)
+    r = recurrence_inputs(d, 800 + T, mask)
+    gv = torch.rand((B, T, Hv, Dk), generator=torch.Generator().manual_seed(T)) * 0.7 + 0.3
+    y, s = gdn.prefill_vec(d, to_dev(r["q"]), to_dev(r["k"]), to_dev(r["v"]), to_dev(gv), to_dev(r["beta"]),
+                           to_dev(r["state"]), to_dev(mask))
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    yr, sr = oracle.recurrence_vec(d, r["q_bits"], r["k_bits"], r["v_bits"], gv.numpy().astype(np.float64),
+                                   r["beta"].numpy().astype(np.float64), r["state"].numpy().astype(np.float64),
+                                   np_mask(mask))
+    U.assert_y_close(U.bf16_dev_to_f64(y), yr)
+    U.assert_state_close(s.cpu().numpy(), sr)
+    if mask is not None:
+        assert np.all(U.bits(y)[mask.numpy() == 0] == 0)
+
+
+def test_prefill_vec_with_equal_channels_matches_scalar(gdn):
+    d = wl.Dims(B=2, T=100, Hk=2, Hv=4, Dk=128, Dv=128)
+    r = recurrence_inputs(d, 5)
+    gvec = r["g"][..., None].expand(d.B, d.T, d.Hv, d.Dk).contiguous()
+    args = [to_dev(r[x]) for x in ("q", "k", "v")]
+    y1, s1 = gdn.prefill(d, *args, to_dev(r["g"]), to_dev(r["beta"]), to_dev(r["state"]))
+    y2, s2 = gdn.prefill_vec(d, *args, to_dev(gvec), to_dev(r["beta"]), to_dev(r["state"]))
+    torch.cuda.synchronize()
+    U.assert_y_close(U.bf16_dev_to_f64(y2), U.bf16_dev_to_f64(y1))
+    U.assert_state_close(s2.cpu().numpy(), s1.cpu().numpy().astype(np.float64), tol=1e-5)

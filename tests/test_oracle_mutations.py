@@ -20,6 +20,8 @@ C_MUTATIONS = {
     "beta_dropped": ("double delta = beta[t] * (vt[i] - kv);", "double delta = (vt[i] - kv);"),
 }
 
+VEC_MUTATION = ("S[(size_t)i * Dk + j] *= gt[j];", "S[(size_t)i * Dk + j] *= gt[i % Dk];")
+
 C_PINS = [
     pins.test_scalar_recurrence_golden,
     pins.test_full_write_makes_state_map_k_to_v,
@@ -31,9 +33,10 @@ C_PINS = [
 
 def _build_mutant(tmp_path, name, old, new):
     src = open(oc._SRC).read()
-    assert src.count(old) == 1, name
+    # the scalar-gate function comes first in the file; plant the mistake there
+    assert src.count(old) >= 1, name
     path = tmp_path / f"{name}.c"
-    path.write_text(src.replace(old, new))
+    path.write_text(src.replace(old, new, 1))
     so = tmp_path / f"lib{name}.so"
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(so), str(path)])
     lib = ctypes.CDLL(str(so))
@@ -103,3 +106,23 @@ def test_q_scale_mutation_is_caught(monkeypatch):
 
     monkeypatch.setattr(oc, "rms_normalize", wrong_norm)
     assert _some_pin_fails([pins.test_qk_norm_and_scale], oracle_mod=oc)
+
+
+def test_vec_gating_row_instead_of_column_is_caught(tmp_path, monkeypatch):
+    src = open(oc._SRC).read()
+    old, new = VEC_MUTATION
+    assert src.count(old) == 1
+    path = tmp_path / "vec.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / "libvec.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(so), str(path)])
+    lib = ctypes.CDLL(str(so))
+    dp = ctypes.POINTER(ctypes.c_double)
+    for name in ("oracle_delta_rule_head", "oracle_delta_rule_head_vec"):
+        f = getattr(lib, name)
+        f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_uint8),
+                      dp, dp]
+        f.restype = None
+    monkeypatch.setattr(oc, "_lib", lib)
+    assert _some_pin_fails([lambda oracle_mod: pins.test_vec_gating_brute_force(oracle_mod, 5, 6),
+                            pins.test_vec_gating_zero_channel_forgets_that_column], oracle_mod=oc)

@@ -434,3 +434,47 @@ def test_rmsnorm_gated_closed_forms(oracle_mod):
     assert np.allclose(out, expect, rtol=2 ** -8)
     zero = o.bf16_to_f64(o.rmsnorm_gated(o.f64_to_bf16(np.zeros((2, Dv))), z.repeat(2, 0), w, 1e-6))
     assert np.all(zero == 0.0)                          # a zero row (masked step) stays zero
+
+
+# ----------------------------------------------------------------------------
+# f-3 vectorized gating (one decay factor per key channel)
+# ----------------------------------------------------------------------------
+def test_vec_gating_with_equal_channels_is_the_scalar_recurrence(oracle_mod):
+    o = oracle_mod
+    rng = np.random.default_rng(31)
+    q, k, v, g, beta, S0 = _rand_head(rng, 30, 16, 12)
+    y, S = o.head_recurrence(q, k, v, g, beta, S0)
+    yv, Sv = o.head_recurrence_vec(q, k, v, np.repeat(g[:, None], 16, axis=1), beta, S0)
+    assert np.array_equal(y, yv) and np.array_equal(S, Sv)
+
+
+@pytest.mark.parametrize("Dk,Dv", [(4, 3), (5, 6)])
+def test_vec_gating_brute_force(oracle_mod, Dk, Dv):
+    """S_T = S0 P_1..P_T + sum_t beta_t v_t k_t^T P_{t+1}..P_T with
+    P_t = diag(g_t) (I - beta_t k_t k_t^T)."""
+    o = oracle_mod
+    rng = np.random.default_rng(32 + Dk)
+    T = 6
+    q, k, v, _, beta, S0 = _rand_head(rng, T, Dk, Dv, unit_k=False)
+    G = rng.uniform(0.3, 1.0, (T, Dk))
+    y, S = o.head_recurrence_vec(q, k, v, G, beta, S0)
+    I = np.eye(Dk)
+    P = [np.diag(G[t]) @ (I - beta[t] * np.outer(k[t], k[t])) for t in range(T)]
+    Sb = S0.copy()
+    for t in range(T):
+        Sb = Sb @ P[t] + beta[t] * np.outer(v[t], k[t])
+        assert np.allclose(y[t], Sb @ q[t], rtol=1e-12, atol=1e-13)
+    assert np.allclose(S, Sb, rtol=1e-12, atol=1e-13)
+
+
+def test_vec_gating_zero_channel_forgets_that_column(oracle_mod):
+    o = oracle_mod
+    rng = np.random.default_rng(33)
+    q, k, v, _, beta, S0 = _rand_head(rng, 1, 8, 5, unit_k=False)
+    G = np.ones((1, 8))
+    G[0, 3] = 0.0
+    _, S = o.head_recurrence_vec(q, k, v, G, beta, S0)
+    Sd = S0.copy()
+    Sd[:, 3] = 0.0
+    delta = beta[0] * (v[0] - Sd @ k[0])
+    assert np.allclose(S, Sd + np.outer(delta, k[0]), rtol=1e-14, atol=1e-15)
