@@ -147,6 +147,10 @@ GDN_API gdn_status gdn_decode_window(const gdn_dims *dims, const uint16_t *qkv, 
  *              64 = chunked (WY / UT-transform) form on the tensor cores
  *   workspace  device scratch of at least gdn_prefill_workspace_size() bytes,
  *              16-byte aligned (may be NULL when that size is 0)
+ * The chunked form reads q, k, v of masked steps (their contribution is then
+ * cancelled exactly), so those entries must hold finite values; the zeros
+ * gdn_conv_update writes there qualify.  It supports Dk = Dv = 128 (other
+ * sizes give GDN_ERR_UNSUPPORTED).
  */
 GDN_API gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
                        const uint16_t *v, const float *g, const float *beta,
