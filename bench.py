@@ -248,19 +248,41 @@ def bench_decode(gdn, w: wl.Workload, steps: int, warmup: int, dev, sampler) -> 
     if gdn.gdn_device_status() != gdn.GDN_OK:
         raise RuntimeError("device error word set during the decode benchmark")
 
-    # end to end through the public API: pinned host inputs -> device, decode,
-    # y -> pinned host, every step
-    y_h = torch.empty((d.B, d.Hv, d.Dv), dtype=torch.bfloat16).pin_memory()
-    qkv_d = torch.empty_like(qkv[0])
-    a_d, b_d = torch.empty_like(a[0]), torch.empty_like(b[0])
+    # end to end through the public API: every step copies its inputs from
+    # pinned host memory and reads its y back to pinned host memory.  As a
+    # serving loop would, the copies run on their own streams, double-buffered
+    # and ordered by events, so step i+1's inputs travel while step i computes.
+    nbuf = 2
+    y_h = [torch.empty((d.B, d.Hv, d.Dv), dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
+    qkv_d = [torch.empty_like(qkv[0]) for _ in range(nbuf)]
+    a_d = [torch.empty_like(a[0]) for _ in range(nbuf)]
+    b_d = [torch.empty_like(b[0]) for _ in range(nbuf)]
+    y_d = [torch.empty_like(y) for _ in range(nbuf)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_done = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+    for k in range(nbuf):          # every event starts in the completed state
+        ev_done[k].record(stream)
+        ev_out[k].record(stream)
 
     def e2e_step(i):
-        j = i % n_in
-        qkv_d.copy_(qkv_h[j], non_blocking=True)
-        a_d.copy_(a_h[j], non_blocking=True)
-        b_d.copy_(b_h[j], non_blocking=True)
-        gdn.gdn_recurrent_decode(d1, qkv_d, conv_w, conv_state, a_d, b_d, A_log, dt_bias, state, None, y, stream)
-        y_h.copy_(y, non_blocking=True)
+        j, k = i % n_in, i % nbuf
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_done[k])            # step i-2 has finished reading slot k
+            qkv_d[k].copy_(qkv_h[j], non_blocking=True)
+            a_d[k].copy_(a_h[j], non_blocking=True)
+            b_d[k].copy_(b_h[j], non_blocking=True)
+            ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        stream.wait_event(ev_out[k])                # y slot k has been read back
+        gdn.gdn_recurrent_decode(d1, qkv_d[k], conv_w, conv_state, a_d[k], b_d[k], A_log, dt_bias, state, None,
+                                 y_d[k], stream)
+        ev_done[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[k])
+            y_h[k].copy_(y_d[k], non_blocking=True)
+            ev_out[k].record(s_out)
 
     for i in range(warmup):
         e2e_step(i)
@@ -268,12 +290,17 @@ def bench_decode(gdn, w: wl.Workload, steps: int, warmup: int, dev, sampler) -> 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall = time.perf_counter()
     e0.record(stream)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
     for i in range(steps):
         e2e_step(i)
+    for k in range(nbuf):
+        stream.wait_event(ev_out[k])
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     e2e_ms = max(e0.elapsed_time(e1), t_wall * 1e3) / steps
+    qkv_d, a_d, b_d, y_h = qkv_d[0], a_d[0], b_d[0], y_h[0]
     return {"ms": ms, "e2e_ms": e2e_ms,
             "h2d": qkv_d.numel() * 2 + a_d.numel() * 2 + b_d.numel() * 2, "d2h": y_h.numel() * 2}
 
