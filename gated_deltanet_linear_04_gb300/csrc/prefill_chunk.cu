@@ -30,8 +30,11 @@
 //
 // One CTA (256 threads) owns one (b, hv) head for all T.  Supports Dk = Dv =
 // 128.  Shared memory: 13 slots of 16 KiB reused across the phases of a chunk.
+// Chunks whose 64 steps are all masked are skipped: their y is written zero and
+// their inputs are never staged.
 #include "common.cuh"
 #include "internal.h"
+#include "mask_scan.cuh"
 #include "umma.cuh"
 
 namespace gdn {
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     __shared__ __align__(16) float s_beta[kC];
     __shared__ __align__(16) float s_bg[kC];
     __shared__ __align__(16) float s_kc[kC];
+    __shared__ uint32_t scan_bits[ChunkScan<kThreads>::kWords];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3;                 // TMEM lane quarter of this warp
@@ -224,11 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             }
         }
     };
-    auto publish_steps = [&](int c) {
+    auto publish_steps = [&](int slot) {
         if (tid < kC) {
-            s_g[c & 1][tid] = pf_g;
-            s_b[c & 1][tid] = pf_b;
-            s_m[c & 1][tid] = pf_m;
+            s_g[slot][tid] = pf_g;
+            s_b[slot][tid] = pf_b;
+            s_m[slot][tid] = pf_m;
         }
     };
     auto issue_tma = [&](int c) {
@@ -261,16 +265,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         umma::fence_after_sync();
     };
 
-    issue_tma(0);
-    gather_steps(0);
-    publish_steps(0);
+    ChunkScan<kThreads> scan(p.mask == nullptr ? nullptr : p.mask + (size_t)b * T, T, scan_bits);
+    uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * kD + (size_t)hv * kD;
+    const size_t y_stride = (size_t)p.Hv * kD;
+    int c = scan.next_active(0);
+    zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), kD);
+    if (c < nchunks) {
+        issue_tma(c);
+        gather_steps(c);
+        publish_steps(0);
+    }
     __syncthreads();
 
-    for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c & 1;
+    // `it` counts the chunks actually processed: it picks the step-slot and
+    // the TMA barrier's phase
+    for (int it = 0; c < nchunks && ok; ++it) {
+        const int st = it & 1;
         const int t0 = c * kC;
         // ---- S1: chunk inputs, log-decay prefix sums (warp 0)
-        ok = mbar_wait(&bar_tma, (uint32_t)(c & 1), p.err);
+        ok = mbar_wait(&bar_tma, (uint32_t)(it & 1), p.err);
         if (warp == 0) {
             const float la = logf(s_g[st][2 * lane]), lb = logf(s_g[st][2 * lane + 1]);
             float incl = la + lb;
@@ -298,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         ok = __syncthreads_and(ok) != 0;
         if (!ok) break;
 
-        if (c + 1 < nchunks) gather_steps(c + 1);
+        const int cn = scan.next_active(c + 1);
+        if (cn < nchunks) gather_steps(cn);
         // ---- S2: [K;Q] K^T on the tensor core; meanwhile build the tf32 operands
         if (tid == 0) {
             umma::fence_after_sync();
@@ -366,9 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         // K and V tiles are no longer read: prefetch the next chunk
         umma::fence_before_sync();
         __syncthreads();
-        if (c + 1 < nchunks) {
-            issue_tma(c + 1);
-            publish_steps(c + 1);
+        if (cn < nchunks) {
+            issue_tma(cn);
+            publish_steps(st ^ 1);
         }
 
         // ---- S4: T = (I + A)^-1 by blocked doubling, in place in As
@@ -529,6 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
                     *reinterpret_cast<const uint4 *>(sm + S_YST + (r * kD + c8) * 2);
             }
         }
+        zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), kD);
+        c = cn;
     }
 
     // ---- final state (only when every wait succeeded)

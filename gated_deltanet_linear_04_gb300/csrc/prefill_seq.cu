@@ -13,8 +13,10 @@
 // 2-D TMA loads (double buffered, one mbarrier per stage); g, beta and the mask
 // are gathered by plain loads one chunk ahead.  k.q per step is precomputed for
 // the chunk so that y = g (S.q) + delta (k.q) needs no second reduction.
+// Chunks whose 64 steps are all masked are skipped (zero y, no staging).
 #include "common.cuh"
 #include "internal.h"
+#include "mask_scan.cuh"
 
 namespace gdn {
 namespace {
@@ -65,7 +67,9 @@ __device__ __forceinline__ void load_row_bf16(const uint16_t *p, float (&o)[CW])
 
 // VEC: vectorized gating, one decay factor per key channel (g [B, T, Hv, Dk],
 // staged by TMA with q/k/v); the state columns are decayed before the dots.
-template <int DK, int RPL, bool VEC>
+// MASKED: a step mask is given; wholly masked chunks are skipped.  (Without a
+// mask the chunk loop is the plain one, compiled without the search.)
+template <int DK, int RPL, bool VEC, bool MASKED>
 __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                const __grid_constant__ CUtensorMap tm_k,
                                                                const __grid_constant__ CUtensorMap tm_v,
@@ -76,6 +80,7 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
     using L = SeqSmem<DK, R, VEC>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full_bar[2];
+    __shared__ uint32_t scan_bits[ChunkScan<kThreads>::kWords];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rg = lane >> 3, cg = lane & 7;
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
                 const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
                 if constexpr (!VEC) gg = p.g[gi];
                 bb = p.beta[gi];
-                m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
+                m = MASKED ? (p.mask[(size_t)b * T + t] != 0) : 1;
             }
             reinterpret_cast<float *>(base + L::g_off)[tid] = gg;
             reinterpret_cast<float *>(base + L::b_off)[tid] = bb;
@@ -147,15 +152,27 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
         }
     };
 
-    if (nchunks > 0) issue(0, 0);
+    ChunkScan<kThreads> scan(MASKED ? p.mask + (size_t)b * T : nullptr, T, scan_bits);
+    uint16_t *y_row0 = p.y + ((size_t)b * T * p.Hv + hv) * p.Dv + r0;
+    const size_t y_stride = (size_t)p.Hv * p.Dv;
+    int c = 0;
+    if constexpr (MASKED) {
+        c = scan.next_active(0);
+        if (c > 0) zero_y_rows(y_row0, y_stride, 0, min(c * kTC, T), R);
+    }
+    if (c < nchunks) issue(c, 0);
     float *y_s = reinterpret_cast<float *>(smem + L::y_off);
     bool ok_all = true;
 
-    for (int c = 0; c < nchunks; ++c) {
-        const int st = c & 1;
+    // `it` counts the chunks actually processed: it picks the stage and the
+    // stage barrier's phase
+    for (int it = 0; c < nchunks; ++it) {
+        const int st = it & 1;
         unsigned char *base = smem + st * L::stage_bytes;
-        if (c + 1 < nchunks) issue(c + 1, st ^ 1);
-        bool ok = mbar_wait(&full_bar[st], (uint32_t)((c >> 1) & 1), p.err);
+        int cn = c + 1;
+        if constexpr (MASKED) cn = scan.next_active(c + 1);
+        if (cn < nchunks) issue(cn, st ^ 1);
+        bool ok = mbar_wait(&full_bar[st], (uint32_t)((it >> 1) & 1), p.err);
         ok = __syncthreads_and(ok) != 0;
         if (!ok) {
             ok_all = false;
@@ -251,6 +268,10 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
             uint16_t *dst = p.y + (((size_t)b * T + c * kTC + t) * p.Hv + hv) * p.Dv + r0 + 2 * pr;
             *reinterpret_cast<uint32_t *>(dst) = packed;
         }
+        if constexpr (MASKED) {
+            if (cn > c + 1) zero_y_rows(y_row0, y_stride, min((c + 1) * kTC, T), min(cn * kTC, T), R);
+        }
+        c = cn;
     }
 
     if (!ok_all) return;
@@ -264,8 +285,8 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
     }
 }
 
-template <int DK, int RPL, bool VEC>
-cudaError_t launch_seq_t(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+template <int DK, int RPL, bool VEC, bool MASKED>
+cudaError_t launch_seq_m(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                          const SeqParams &p, cudaStream_t st) {
     constexpr int R = 16 * RPL;
     using L = SeqSmem<DK, R, VEC>;
@@ -283,14 +304,21 @@ cudaError_t launch_seq_t(const Sizes &s, const uint16_t *q, const uint16_t *k, c
     }
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_seq_kernel<DK, RPL, VEC>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_seq_kernel<DK, RPL, VEC, MASKED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(s.Hv * (s.Dv / R), s.B);
-    prefill_seq_kernel<DK, RPL, VEC><<<grid, kThreads, L::total, st>>>(tq, tk, tv, tg, p);
+    prefill_seq_kernel<DK, RPL, VEC, MASKED><<<grid, kThreads, L::total, st>>>(tq, tk, tv, tg, p);
     return cudaGetLastError();
+}
+
+template <int DK, int RPL, bool VEC>
+cudaError_t launch_seq_t(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const SeqParams &p, cudaStream_t st) {
+    return p.mask != nullptr ? launch_seq_m<DK, RPL, VEC, true>(s, q, k, v, p, st)
+                             : launch_seq_m<DK, RPL, VEC, false>(s, q, k, v, p, st);
 }
 
 template <bool VEC>

@@ -43,6 +43,11 @@ def make_mask(kind, B, T, seed):
         t = torch.arange(T)[None, :]
         m = (t < lens[:, None]) if kind == "right" else (t >= (T - lens)[:, None])
         return m.to(torch.uint8)
+    if kind == "blocks":
+        # about half of the 64-step chunks wholly masked, the rest partly
+        nch = (T + 63) // 64
+        keep = (torch.rand((B, nch), generator=g) < 0.5).repeat_interleave(64, dim=1)[:, :T]
+        return ((torch.rand((B, T), generator=g) < 0.8) & keep).to(torch.uint8)
     if kind == "allmasked_row":
         m = (torch.rand((B, T), generator=g) < 0.5).to(torch.uint8)
         m[0] = 0
@@ -151,6 +156,8 @@ SEQ_CASES = [
     (1, 130, 1, 4, 32, 32, "left", "normal"),
     (2, 200, 4, 16, 128, 128, "allmasked_row", "normal"),
     (3, 129, 1, 3, 64, 32, "sparse", "zeros"),
+    (3, 333, 1, 2, 128, 128, "blocks", "normal"),   # rows 1, 2 of the mask not 16-byte aligned
+    (2, 640, 2, 4, 64, 64, "blocks", "zeros"),
 ]
 
 
@@ -188,6 +195,8 @@ CHUNK_CASES = [
     (3, 130, 1, 3, "left", "zeros"),
     (2, 257, 2, 4, "allmasked_row", "normal"),
     (2, 150, 1, 2, "sparse", "normal"),
+    (3, 333, 1, 2, "blocks", "normal"),
+    (2, 640, 1, 2, "blocks", "zeros"),
 ]
 
 
@@ -212,6 +221,32 @@ def test_prefill_chunked(gdn, B, T, Hk, Hv, mk, st):
             if mask[b].sum() == 0:
                 ref = np.zeros_like(sr[b]) if s0 is None else state_in[b].numpy()
                 assert np.array_equal(s_out[b].cpu().numpy(), ref), "row without valid steps: state untouched"
+
+
+@pytest.mark.parametrize("chunk", [0, 64])
+def test_prefill_masked_chunks_across_scan_windows(gdn, chunk):
+    # long rows that are mostly masked: the search for the next chunk with a
+    # valid step crosses several windows of the chunk bitmap, and row 1's mask
+    # starts off a 16-byte boundary
+    B, T = 2, 17000
+    d = wl.Dims(B=B, T=T, Hk=1, Hv=1, Dk=128, Dv=128)
+    mask = torch.zeros((B, T), dtype=torch.uint8)
+    for a, e in [(50, 120), (8300, 8400), (16500, 16600), (16990, 17000)]:
+        mask[0, a:e] = 1
+    mask[1, :200] = 1
+    mask[1, 16900:] = 1
+    mask[1, 12000] = 1
+    r = recurrence_inputs(d, 4321, mask)
+    y, s_out = gdn.prefill(d, to_dev(r["q"]), to_dev(r["k"]), to_dev(r["v"]), to_dev(r["g"]), to_dev(r["beta"]),
+                           to_dev(r["state"]), to_dev(mask), chunk=chunk)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    yr, sr = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                               r["beta"].numpy().astype(np.float64), r["state"].numpy().astype(np.float64),
+                               np_mask(mask))
+    U.assert_y_close(U.bf16_dev_to_f64(y), yr)
+    U.assert_state_close(s_out.cpu().numpy(), sr)
+    assert np.all(U.bits(y)[mask.numpy() == 0] == 0), "masked y must be exactly zero"
 
 
 def test_prefill_chunked_rejects_other_head_sizes(gdn):
