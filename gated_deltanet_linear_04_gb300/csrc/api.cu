@@ -185,9 +185,8 @@ gdn_status gdn_decode_window(const gdn_dims *dims, const uint16_t *qkv, const ui
 size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk) {
     gdn::Sizes s;
     if (gdn::check_dims(dims, &s) != GDN_OK) return 0;
-    if (chunk == 0) return 0;
-    if (chunk == 64) return gdn::prefill_chunked_workspace(s);
-    return 0;
+    if (chunk != 0 && chunk != 64) return 0;
+    return gdn::row_order_workspace(s);
 }
 
 gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -198,10 +197,13 @@ gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *
     gdn_status st = gdn::check_dims(dims, &s);
     if (st != GDN_OK) return st;
     if (chunk != 0 && chunk != 64) return GDN_ERR_UNSUPPORTED;
+    if (chunk == 64 && (s.Dk != 128 || s.Dv != 128)) return GDN_ERR_UNSUPPORTED;
     const size_t BT = (size_t)s.B * s.T;
     const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
     if (!ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT) || !ok_ptr(g, BT) || !ok_ptr(beta, BT) ||
         !ok_ptr(state_in, 0) || !ok_ptr(state_out, nstate) || !ok_ptr(mask, 0) || !ok_ptr(y, BT))
+        return GDN_ERR_INVALID_ARG;
+    if (workspace != nullptr && (ws_bytes < gdn::row_order_workspace(s) || !gdn::aligned16(workspace)))
         return GDN_ERR_INVALID_ARG;
     if (s.B == 0) return GDN_OK;
     cudaStream_t cs = (cudaStream_t)stream;
@@ -211,13 +213,17 @@ gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *
         return gdn::from_cuda(
             cudaMemcpyAsync(state_out, state_in, nstate * sizeof(float), cudaMemcpyDeviceToDevice, cs));
     }
+    // rows of a masked batch longest first (scheduling only; results identical)
+    const int *order = nullptr;
+    if (mask != nullptr && workspace != nullptr && s.B > 1) {
+        cudaError_t e = gdn::launch_row_order(s, mask, workspace, cs);
+        if (e != cudaSuccess) return gdn::from_cuda(e);
+        order = static_cast<const int *>(workspace);
+    }
     if (chunk == 0)
-        return gdn::from_cuda(gdn::launch_prefill_seq(s, q, k, v, g, beta, state_in, state_out, mask, y,
+        return gdn::from_cuda(gdn::launch_prefill_seq(s, q, k, v, g, beta, state_in, state_out, mask, order, y,
                                                       gdn::error_word(), cs));
-    const size_t need = gdn::prefill_chunked_workspace(s);
-    if (need > 0 && (workspace == nullptr || ws_bytes < need || !gdn::aligned16(workspace)))
-        return GDN_ERR_INVALID_ARG;
-    return gdn::from_cuda(gdn::launch_prefill_chunked(s, q, k, v, g, beta, state_in, state_out, mask, y, workspace,
+    return gdn::from_cuda(gdn::launch_prefill_chunked(s, q, k, v, g, beta, state_in, state_out, mask, order, y,
                                                       gdn::error_word(), cs));
 }
 

@@ -38,9 +38,17 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtyp
                     uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
+// Row order for masked prefill (row_order.cu): order[i] = the row the i-th
+// row slot of a prefill launch processes, longest (most chunks holding a
+// valid step) first.  Scratch: row_order_workspace(s) bytes, order at offset 0.
+size_t row_order_workspace(const Sizes &s);
+cudaError_t launch_row_order(const Sizes &s, const uint8_t *mask, void *ws, cudaStream_t st);
+
+// `order` (optional, with a mask): row slot -> batch row, see above.
 cudaError_t launch_prefill_seq(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                const float *g, const float *beta, const float *state_in, float *state_out,
-                               const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st);
+                               const uint8_t *mask, const int *order, uint16_t *y, unsigned *err,
+                               cudaStream_t st);
 
 cudaError_t launch_rmsnorm_gated(const Sizes &s, const uint16_t *y, const uint16_t *z, const float *norm_w,
                                  float eps, uint16_t *out, cudaStream_t st);
@@ -49,10 +57,9 @@ cudaError_t launch_prefill_seq_vec(const Sizes &s, const uint16_t *q, const uint
                                    const float *g_vec, const float *beta, const float *state_in, float *state_out,
                                    const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st);
 
-size_t prefill_chunked_workspace(const Sizes &s);
-
 cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                    const float *g, const float *beta, const float *state_in, float *state_out,
-                                   const uint8_t *mask, uint16_t *y, void *ws, unsigned *err, cudaStream_t st);
+                                   const uint8_t *mask, const int *order, uint16_t *y, unsigned *err,
+                                   cudaStream_t st);
 
 }  // namespace gdn

@@ -17,6 +17,26 @@
 
 namespace gdn {
 
+// True if chunk `ch` (steps [64 ch, min(64 ch + 64, T))) of a mask row holds a
+// valid (non-zero) step.
+__device__ __forceinline__ bool chunk_has_valid(const uint8_t *mrow, int T, int ch) {
+    const int t0 = ch * 64, n = min(64, T - t0);
+    const uint8_t *p = mrow + t0;
+    if (n == 64 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+        const uint4 *p16 = reinterpret_cast<const uint4 *>(p);
+        uint32_t acc = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 w = p16[i];
+            acc |= w.x | w.y | w.z | w.w;
+        }
+        return acc != 0;
+    }
+    uint32_t acc = 0;
+    for (int i = 0; i < n; ++i) acc |= p[i];
+    return acc != 0;
+}
+
 template <int NT>
 struct ChunkScan {
     static_assert(NT % 32 == 0, "window is a whole number of warps");
@@ -31,28 +51,10 @@ struct ChunkScan {
     __device__ ChunkScan(const uint8_t *mask_row, int T_, uint32_t *shared_bits)
         : mrow(mask_row), T(T_), nchunks((T_ + kStep - 1) / kStep), bits(shared_bits), wb(-(1 << 30)) {}
 
-    __device__ __forceinline__ bool chunk_has_valid(int ch) const {
-        const int t0 = ch * kStep, n = min(kStep, T - t0);
-        const uint8_t *p = mrow + t0;
-        if (n == kStep && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
-            const uint4 *p16 = reinterpret_cast<const uint4 *>(p);
-            uint32_t acc = 0;
-#pragma unroll
-            for (int i = 0; i < kStep / 16; ++i) {
-                const uint4 w = p16[i];
-                acc |= w.x | w.y | w.z | w.w;
-            }
-            return acc != 0;
-        }
-        uint32_t acc = 0;
-        for (int i = 0; i < n; ++i) acc |= p[i];
-        return acc != 0;
-    }
-
     __device__ __forceinline__ void scan(int from) {
         __syncthreads();   // every thread is done with the previous window
         const int ch = from + (int)threadIdx.x;
-        const bool any = ch < nchunks && chunk_has_valid(ch);
+        const bool any = ch < nchunks && chunk_has_valid(mrow, T, ch);
         const unsigned bal = __ballot_sync(0xffffffffu, any);
         if ((threadIdx.x & 31u) == 0) bits[threadIdx.x >> 5] = bal;
         wb = from;

@@ -68,6 +68,7 @@ struct ChunkParams {
     const float *g, *beta, *state_in;
     float *state_out;
     const uint8_t *mask;
+    const int *order;   // row slot -> batch row (optional, with a mask)
     uint16_t *y;
     unsigned *err;
     int B, T, Hk, Hv;
@@ -164,7 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     const int quad = warp & 3;                 // TMEM lane quarter of this warp
     const int half = warp >> 2;                // which half of the columns this warp handles
     const int row = quad * 32 + lane;          // TMEM lane / accumulator row of this thread
-    const int hv = blockIdx.x, b = blockIdx.y;
+    const int hv = blockIdx.x;
+    const int b = p.order != nullptr ? p.order[blockIdx.y] : (int)blockIdx.y;
     const int hk = hv / (p.Hv / p.Hk);
     const int T = p.T;
     const int nchunks = (T + kC - 1) / kC;
@@ -571,11 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
 
 }  // namespace
 
-size_t prefill_chunked_workspace(const Sizes &) { return 0; }
-
 cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                    const float *g, const float *beta, const float *state_in, float *state_out,
-                                   const uint8_t *mask, uint16_t *y, void *, unsigned *err, cudaStream_t st) {
+                                   const uint8_t *mask, const int *order, uint16_t *y, unsigned *err,
+                                   cudaStream_t st) {
     if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
     CUtensorMap tk, tq, tv;
     const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
@@ -593,7 +594,8 @@ cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    ChunkParams p{g, beta, state_in, state_out, mask, y, err, s.B, s.T, s.Hk, s.Hv};
+    ChunkParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y, err,
+                  s.B, s.T, s.Hk, s.Hv};
     dim3 grid(s.Hv, s.B);
     prefill_chunk_kernel<<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, p);
     return cudaGetLastError();

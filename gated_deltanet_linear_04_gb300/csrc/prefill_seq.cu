@@ -28,6 +28,7 @@ struct SeqParams {
     const float *g, *beta, *state_in;
     float *state_out;
     const uint8_t *mask;
+    const int *order;   // row slot -> batch row (optional, with a mask)
     uint16_t *y;
     unsigned *err;
     int B, T, Hk, Hv, Dv;
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) prefill_seq_kernel(const __grid_cons
     const int nslice = p.Dv / R;
     const int slice = blockIdx.x % nslice;
     const int hv = blockIdx.x / nslice;
-    const int b = blockIdx.y;
+    const int b = (MASKED && p.order != nullptr) ? p.order[blockIdx.y] : (int)blockIdx.y;
     const int G = p.Hv / p.Hk;
     const int hk = hv / G;
     const int r0 = slice * R;
@@ -343,15 +344,16 @@ cudaError_t launch_seq_any(const Sizes &s, const uint16_t *q, const uint16_t *k,
 
 cudaError_t launch_prefill_seq(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                const float *g, const float *beta, const float *state_in, float *state_out,
-                               const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st) {
-    SeqParams p{g, beta, state_in, state_out, mask, y, err, s.B, s.T, s.Hk, s.Hv, s.Dv};
+                               const uint8_t *mask, const int *order, uint16_t *y, unsigned *err,
+                               cudaStream_t st) {
+    SeqParams p{g, beta, state_in, state_out, mask, order, y, err, s.B, s.T, s.Hk, s.Hv, s.Dv};
     return launch_seq_any<false>(s, q, k, v, p, st);
 }
 
 cudaError_t launch_prefill_seq_vec(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                    const float *g_vec, const float *beta, const float *state_in, float *state_out,
                                    const uint8_t *mask, uint16_t *y, unsigned *err, cudaStream_t st) {
-    SeqParams p{g_vec, beta, state_in, state_out, mask, y, err, s.B, s.T, s.Hk, s.Hv, s.Dv};
+    SeqParams p{g_vec, beta, state_in, state_out, mask, nullptr, y, err, s.B, s.T, s.Hk, s.Hv, s.Dv};
     return launch_seq_any<true>(s, q, k, v, p, st);
 }
 

@@ -216,14 +216,18 @@ def decode_window(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, ke
     return y
 
 
-def prefill(dims, q, k, v, g, beta, state_in=None, mask=None, chunk=0, state_out=None, stream=None):
-    """Returns (y, state_out)."""
+def prefill(dims, q, k, v, g, beta, state_in=None, mask=None, chunk=0, state_out=None, stream=None,
+            order_rows=True):
+    """Returns (y, state_out).  With a mask and order_rows, a workspace is
+    passed so that rows are scheduled longest first (same results)."""
     dev = q.device
     y = torch.empty((dims.B, dims.T, dims.Hv, dims.Dv), dtype=BF16, device=dev)
     if state_out is None:
         state_out = torch.empty((dims.B, dims.Hv, dims.Dv, dims.Dk), dtype=F32, device=dev)
-    nws = gdn_prefill_workspace_size(dims, chunk)
-    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
+    ws = None
+    if mask is not None and order_rows:
+        nws = gdn_prefill_workspace_size(dims, chunk)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
     gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk, ws, stream)
     return y, state_out
 

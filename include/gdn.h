@@ -145,8 +145,16 @@ GDN_API gdn_status gdn_decode_window(const gdn_dims *dims, const uint16_t *qkv, 
  *   y          bf16 [B, T, Hv, Dv] (out)
  *   chunk      0 = sequential form (state resident on chip across all T);
  *              64 = chunked (WY / UT-transform) form on the tensor cores
- *   workspace  device scratch of at least gdn_prefill_workspace_size() bytes,
- *              16-byte aligned (may be NULL when that size is 0)
+ *   workspace  optional device scratch of at least gdn_prefill_workspace_size()
+ *              bytes, 16-byte aligned, or NULL.  With a mask, the call first
+ *              writes there the order in which rows are handed to the kernel's
+ *              CTAs (most chunks holding a valid step first), so that the
+ *              longest rows of a ragged batch do not start last; with NULL the
+ *              rows go in index order.  The results are the same either way.
+ *              A workspace that is too small or misaligned gives
+ *              GDN_ERR_INVALID_ARG.  It must not be in use by another call
+ *              still running on another stream.
+ * Wholly masked 64-step chunks cost only their zero y stores.
  * The chunked form reads q, k, v of masked steps (their contribution is then
  * cancelled exactly), so those entries must hold finite values; the zeros
  * gdn_conv_update writes there qualify.  It supports Dk = Dv = 128 (other
@@ -181,8 +189,9 @@ GDN_API gdn_status gdn_prefill_vec(const gdn_dims *dims, const uint16_t *q, cons
                                    const float *state_in, float *state_out, const uint8_t *mask,
                                    uint16_t *y, gdn_stream stream);
 
-/* Bytes of scratch gdn_prefill needs for these sizes and this chunk mode
- * (0 for the sequential form).  Returns 0 for unsupported arguments. */
+/* Bytes of the optional gdn_prefill workspace for these sizes and this chunk
+ * mode (0 or 64): about 8 bytes per batch row, rounded up to 256.  Returns 0
+ * for invalid or unsupported arguments. */
 GDN_API size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk);
 
 /* Human-readable name of a status code (static storage). */

@@ -99,4 +99,9 @@ def test_prefill_chunk_argument(lib):
     d = _dims()
     f = lib.gdn_prefill
     assert f(ctypes.byref(d), *([None] * 9), 32, None, 0, None) == 2    # unsupported chunk size
-    assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 0) == 0
+    # the optional row-order workspace: a few bytes per batch row, whole 256s
+    n0 = lib.gdn_prefill_workspace_size(ctypes.byref(d), 0)
+    assert n0 > 0 and n0 % 256 == 0 and n0 >= 8 * d.B
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 64) == n0
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 32) == 0
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(_dims(B=0)), 0) == 0

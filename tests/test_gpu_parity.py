@@ -249,6 +249,39 @@ def test_prefill_masked_chunks_across_scan_windows(gdn, chunk):
     assert np.all(U.bits(y)[mask.numpy() == 0] == 0), "masked y must be exactly zero"
 
 
+@pytest.mark.parametrize("chunk", [0, 64])
+def test_prefill_row_order(gdn, chunk):
+    # right-padded rows of very different lengths: with a workspace the rows
+    # are handed to CTAs longest first; that changes only which CTA takes which
+    # row, so the outputs are bit-identical to index order (and match the oracle)
+    B, T = 6, 700
+    lens = [30, 700, 0, 333, 64, 699]
+    d = wl.Dims(B=B, T=T, Hk=1, Hv=2, Dk=128, Dv=128)
+    mask = (torch.arange(T)[None, :] < torch.tensor(lens)[:, None]).to(torch.uint8)
+    r = recurrence_inputs(d, 77, mask)
+    dev = [to_dev(r[n]) for n in ("q", "k", "v", "g", "beta")]
+    s_in, m_dev = to_dev(r["state"]), to_dev(mask)
+    y1, s1 = gdn.prefill(d, *dev, state_in=s_in, mask=m_dev, chunk=chunk, order_rows=False)
+    nws = gdn.gdn_prefill_workspace_size(d, chunk)
+    ws = torch.full((nws,), 0xFF, dtype=torch.uint8, device=DEV)
+    y2, s2 = torch.empty_like(y1), torch.empty_like(s1)
+    gdn.gdn_prefill(d, *dev, s_in, s2, m_dev, y2, chunk, ws)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert torch.equal(y1, y2) and torch.equal(s1, s2), "row order must not change results"
+    work = [(n + 63) // 64 for n in lens]
+    assert ws[:4 * B].view(torch.int32).cpu().tolist() == sorted(range(B), key=lambda b: (-work[b], b))
+    yr, sr = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                               r["beta"].numpy().astype(np.float64), r["state"].numpy().astype(np.float64),
+                               np_mask(mask))
+    U.assert_y_close(U.bf16_dev_to_f64(y2), yr)
+    U.assert_state_close(s2.cpu().numpy(), sr)
+    # a workspace below the size asked for is refused before any launch
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_prefill(d, *dev, s_in, s2, m_dev, y2, chunk, ws[:nws - 16])
+    assert e.value.status == gdn.GDN_ERR_INVALID_ARG
+
+
 def test_prefill_chunked_rejects_other_head_sizes(gdn):
     d = wl.Dims(B=1, T=8, Hk=1, Hv=2, Dk=64, Dv=128)
     r = recurrence_inputs(d, 1)
