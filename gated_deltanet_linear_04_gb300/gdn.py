@@ -46,6 +46,8 @@ _SIGS = {
                                    ctypes.c_size_t, _P]),
     "gdn_prefill_vec": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_prefill_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims), ctypes.c_int]),
+    "gdn_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(GdnDims)] + [ctypes.c_void_p] * 9 +
+                            [ctypes.c_int, ctypes.c_void_p]),
     "gdn_decode_window": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_rmsnorm_gated": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, ctypes.c_float, _P, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -156,6 +158,16 @@ def gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, w
                              _ptr(g, F32, "g"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
                              _ptr(state_out, F32, "state_out"), _ptr(mask, U8, "mask"), _ptr(y, BF16, "y"),
                              int(chunk), ws_ptr, ws_bytes, _stream(stream)), "gdn_prefill")
+
+
+def gdn_prefill_noalloc(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, stream=None):
+    """gdn_prefill with the library's own fixed scratch (no workspace, no
+    allocation); for callers that cannot allocate device memory."""
+    d = make_dims(dims)
+    _check(lib().gdn_prefill_noalloc(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
+                                     _ptr(g, F32, "g"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
+                                     _ptr(state_out, F32, "state_out"), _ptr(mask, U8, "mask"),
+                                     _ptr(y, BF16, "y"), int(chunk), _stream(stream)), "gdn_prefill_noalloc")
 
 
 def gdn_rmsnorm_gated(dims, y, z, norm_w, norm_eps, out, stream=None):

@@ -189,6 +189,26 @@ GDN_API gdn_status gdn_prefill_vec(const gdn_dims *dims, const uint16_t *q, cons
                                    const float *state_in, float *state_out, const uint8_t *mask,
                                    uint16_t *y, gdn_stream stream);
 
+/* gdn_prefill for callers that cannot allocate device memory.  Not an
+ * operation of the method (the pages have no counterpart): a variant of the
+ * call above for code that may not call cudaMalloc, such as a runtime that
+ * hands out all device memory from its own pool, a loop that must never
+ * synchronise the device, or a binding with no device allocator.  Same
+ * arguments, results and errors as gdn_prefill, minus the workspace: the
+ * row-order scratch lives in a fixed 32 KiB array inside the library, held on
+ * every GPU that loads the library until the process exits.
+ *   dims->B above GDN_NOALLOC_MAX_ROWS gives GDN_ERR_UNSUPPORTED.
+ * The first call on each device looks up that array's device address
+ * (cudaGetSymbolAddress, with that device current); make it before capturing
+ * any stream.  All calls share the array: calls that overlap on the GPU (other
+ * streams, other host threads) race on it, so order them.  Nothing in it needs
+ * clearing between calls.  No allocation is made by this call. */
+#define GDN_NOALLOC_MAX_ROWS 4096
+GDN_API gdn_status gdn_prefill_noalloc(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
+                                       const uint16_t *v, const float *g, const float *beta,
+                                       const float *state_in, float *state_out, const uint8_t *mask,
+                                       uint16_t *y, int chunk, gdn_stream stream);
+
 /* Bytes of the optional gdn_prefill workspace for these sizes and this chunk
  * mode (0 or 64): about 8 bytes per batch row, rounded up to 256.  Returns 0
  * for invalid or unsupported arguments. */

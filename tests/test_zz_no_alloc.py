@@ -1,0 +1,91 @@
+"""gdn_prefill_noalloc, the prefill entry point for callers that cannot
+allocate device memory (for example a runtime that owns all device memory
+through its own pool, or a loop that must not synchronise the device the way
+cudaMalloc can).  It keeps its row-order scratch in a fixed array inside the
+library instead of a caller-given workspace.
+
+Checked through the C ABI against gdn_prefill with a workspace allocated
+here, within the tolerances of the other parity tests, on two calls in a row:
+the second call finds the first call's contents still in the shared array.
+This file is collected last, so a run that stops at its first failure has
+already run every other test; it builds and loads the library itself, so it
+also runs alone in a fresh process."""
+import pytest
+import torch
+
+from gated_deltanet_linear_04_gb300 import workloads as wl
+from tests import _util as U
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    from gated_deltanet_linear_04_gb300.build import build_library
+    build_library()
+    from gated_deltanet_linear_04_gb300 import gdn as g
+    assert torch.cuda.is_available(), "these tests need a GPU"
+    torch.cuda.set_device(0)
+    return g
+
+
+def _inputs(d, lens, seed):
+    """Right-padded rows of the given lengths; q/k unit-norm-scaled like the
+    conv output, g in (0, 1), beta in (0, 1); masked steps hold finite values."""
+    gen = torch.Generator().manual_seed(seed)
+    B, T = d.B, d.T
+    q = torch.randn((B, T, d.Hk, d.Dk), generator=gen)
+    k = torch.randn((B, T, d.Hk, d.Dk), generator=gen)
+    q = q / q.norm(dim=-1, keepdim=True) / d.Dk ** 0.5
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn((B, T, d.Hv, d.Dv), generator=gen)
+    g = torch.exp(-torch.rand((B, T, d.Hv), generator=gen) * 0.5)
+    beta = torch.sigmoid(torch.randn((B, T, d.Hv), generator=gen))
+    state = torch.randn((B, d.Hv, d.Dv, d.Dk), generator=gen) * 0.05
+    mask = (torch.arange(T)[None, :] < torch.tensor(lens)[:, None]).to(torch.uint8)
+    bf = lambda x: x.to(torch.bfloat16).to(DEV)
+    return (bf(q), bf(k), bf(v), g.to(DEV), beta.to(DEV), state.to(DEV), mask.to(DEV))
+
+
+def _reference(gdn, d, inp, chunk):
+    q, k, v, g, beta, s_in, mask = inp
+    y = torch.empty((d.B, d.T, d.Hv, d.Dv), dtype=torch.bfloat16, device=DEV)
+    s_out = torch.empty_like(s_in)
+    ws = torch.empty(gdn.gdn_prefill_workspace_size(d, chunk), dtype=torch.uint8, device=DEV)
+    gdn.gdn_prefill(d, q, k, v, g, beta, s_in, s_out, mask, y, chunk, ws)
+    return y, s_out
+
+
+def _noalloc(gdn, d, inp, chunk):
+    q, k, v, g, beta, s_in, mask = inp
+    y = torch.empty((d.B, d.T, d.Hv, d.Dv), dtype=torch.bfloat16, device=DEV)
+    s_out = torch.empty_like(s_in)
+    gdn.gdn_prefill_noalloc(d, q, k, v, g, beta, s_in, s_out, mask, y, chunk)
+    return y, s_out
+
+
+@pytest.mark.parametrize("chunk", [0, 64])
+def test_noalloc_prefill_matches_prefill_on_two_calls(gdn, chunk):
+    calls = [
+        (wl.Dims(B=6, T=700, Hk=1, Hv=2, Dk=128, Dv=128), [30, 700, 0, 333, 64, 699], 11),
+        (wl.Dims(B=3, T=257, Hk=2, Hv=4, Dk=128, Dv=128), [257, 1, 130], 12),
+    ]
+    for d, lens, seed in calls:
+        inp = _inputs(d, lens, seed)
+        y_ref, s_ref = _reference(gdn, d, inp, chunk)
+        y, s = _noalloc(gdn, d, inp, chunk)
+        torch.cuda.synchronize()
+        assert gdn.gdn_device_status() == gdn.GDN_OK
+        U.assert_y_close(U.bf16_dev_to_f64(y), U.bf16_dev_to_f64(y_ref))
+        U.assert_state_close(s.cpu().numpy(), s_ref.cpu().numpy().astype("float64"))
+        # same kernels on the same inputs: the results are in fact identical
+        assert torch.equal(y, y_ref) and torch.equal(s, s_ref)
+
+
+def test_noalloc_prefill_rejects_more_rows_than_its_scratch_holds(gdn):
+    d = wl.Dims(B=4097, T=8, Hk=1, Hv=1, Dk=128, Dv=128)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_prefill_noalloc(d, *([None] * 9), 64)
+    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
