@@ -13,11 +13,13 @@
 //
 // Same layout as the single-token kernel: a cluster per (b, hk) group of the
 // G v-heads x SN row slices, each CTA bulk-copies its R x Dk state slice into
-// shared memory while it computes the conv/norm/gates of the T tokens.  A
-// warp walks its rows through all T tokens with the row in registers; after
-// token keep-1 it writes the row back to shared memory, so the slice stored
-// at the end is the state after the kept prefix (nothing is stored when keep
-// is 0).
+// shared memory while it computes the conv/norm/gates of the T tokens.  Eight
+// lanes walk a row through all T tokens with the row in registers (a warp
+// takes four rows at once, so a row's dot products are 3-level shuffle sums;
+// lane l holds the row's 16-byte column groups l, l + 8, ..., which keeps
+// each quarter-warp's shared-memory accesses on distinct banks); after token
+// keep-1 the row is written back to shared memory, so the slice stored at the
+// end is the state after the kept prefix (nothing is stored when keep is 0).
 #include "common.cuh"
 #include "internal.h"
 
@@ -42,65 +44,52 @@ struct WindowParams {
     float eps;
 };
 
-// Raw inputs of one channel over the window: the K-1 stored rows, the T new
-// tokens, the taps.
-struct ChanIn {
-    uint16_t prev[3];
-    uint16_t xs[kMaxT];
-    uint16_t w[4];
-};
-
-__device__ __forceinline__ void load_chan(const WindowParams &p, int b, int c, ChanIn &in) {
-    const int n = p.K - 1;
+// SiLU(conv) of the T new tokens of channel c.  The window is held as
+// x[0 .. K-1) = the stored rows (oldest first) and x[K-1 + t] = token t, so
+// token t's taps j = 0 .. K-1 read x[t + j] (its own value on tap K-1).
+template <int K>
+__device__ __forceinline__ void conv_tokens(const WindowParams &p, int b, int c, float (&out)[kMaxT]) {
+    constexpr int n = K - 1;
+    float x[n + kMaxT];
     const uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
 #pragma unroll
-    for (int j = 0; j < 3; ++j) in.prev[j] = j < n ? cs[(size_t)j * p.C] : (uint16_t)0;
+    for (int j = 0; j < n; ++j) x[j] = bf16_to_f32(cs[(size_t)j * p.C]);
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) in.xs[t] = t < p.T ? p.qkv[((size_t)b * p.T + t) * p.C + c] : (uint16_t)0;
-    const uint16_t *w = p.conv_w + (size_t)c * p.K;
+    for (int t = 0; t < kMaxT; ++t)
+        x[n + t] = t < p.T ? bf16_to_f32(p.qkv[((size_t)b * p.T + t) * p.C + c]) : 0.0f;
+    float w[K];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) in.w[j] = j < p.K ? w[j] : (uint16_t)0;
-}
-
-// SiLU(conv) of token t: taps over [prev rows || tokens], current token on tap K-1.
-__device__ __forceinline__ float conv_at(int K, const ChanIn &in, int t) {
-    const int n = K - 1;
-    float u = 0.0f;
+    for (int j = 0; j < K; ++j) w[j] = bf16_to_f32(p.conv_w[(size_t)c * K + j]);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (j < K) {
-            const int pos = t - n + j;              // < 0: stored row n + pos
-            uint16_t xv = 0;
+    for (int t = 0; t < kMaxT; ++t) {
+        float u = 0.0f;
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-                if (pos < 0 && n + pos == q) xv = in.prev[q];
-#pragma unroll
-            for (int q = 0; q < kMaxT; ++q)
-                if (pos == q) xv = in.xs[q];
-            u = fmaf(bf16_to_f32(in.w[j]), bf16_to_f32(xv), u);
-        }
+        for (int j = 0; j < K; ++j) u = fmaf(w[j], x[t + j], u);
+        out[t] = silu(u);
     }
-    return silu(u);
 }
 
-// Row j (0..K-2) of the conv state after the first `keep` tokens.
-__device__ __forceinline__ uint16_t conv_state_after(int K, const ChanIn &in, int keep, int j) {
-    const int n = K - 1;
-    const int pos = keep - n + j;                   // index into [prev || tokens] shifted by n
-    uint16_t v = 0;
+// conv_state of channel c after the first `keep` (>= 1) tokens: row j is
+// window entry keep + j, i.e. stored row keep + j while that is < K-1, else
+// token keep + j - (K-1).  Rows are written in increasing j, and row j reads
+// a stored row > j, so the rows it reads are still the old ones.
+template <int K>
+__device__ __forceinline__ void write_conv_state(const WindowParams &p, int b, int c, int keep) {
+    constexpr int n = K - 1;
+    uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
 #pragma unroll
-    for (int q = 0; q < 3; ++q)
-        if (pos < 0 && n + pos == q) v = in.prev[q];
-#pragma unroll
-    for (int q = 0; q < kMaxT; ++q)
-        if (pos == q) v = in.xs[q];
-    return v;
+    for (int j = 0; j < n; ++j) {
+        const int pos = keep + j;
+        const uint16_t v = pos < n ? cs[(size_t)pos * p.C] : p.qkv[((size_t)b * p.T + (pos - n)) * p.C + c];
+        cs[(size_t)j * p.C] = v;
+    }
 }
 
-template <int DK>
-__global__ void __launch_bounds__(kThreads) window_kernel(const WindowParams p) {
-    constexpr int LPR = DK / 4;
-    constexpr int RPP = 32 / LPR;
+template <int DK, int K>
+__global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams p) {
+    constexpr int LPR = 8;             // lanes per row
+    constexpr int RPP = 32 / LPR;      // rows per warp pass
+    constexpr int NG = DK / 4 / LPR;   // 16-byte column groups per lane
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.Hv / p.Hk;
     const int R = p.Dv / p.SN;
@@ -142,15 +131,20 @@ __global__ void __launch_bounds__(kThreads) window_kernel(const WindowParams p) 
     const int c_qk = tid < DK ? hk * DK + tid : p.Hk * DK + hk * DK + (tid - DK);
     const bool has_v = tid < R;
     const int c_v = 2 * p.Hk * DK + hv * p.Dv + r0 + tid;
-    ChanIn in_qk{}, in_v{};
-    if (has_qk) load_chan(p, b, c_qk, in_qk);
-    if (has_v) load_chan(p, b, c_v, in_v);
     float xqk[kMaxT];
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
-        xqk[t] = (has_qk && t < T) ? conv_at(p.K, in_qk, t) : 0.0f;
-        if (has_v && t < T) v_s[t][tid] = round_bf16(conv_at(p.K, in_v, t));
+    for (int t = 0; t < kMaxT; ++t) xqk[t] = 0.0f;
+    if (has_qk) conv_tokens<K>(p, b, c_qk, xqk);
+    if (has_v) {
+        float xv[kMaxT];
+        conv_tokens<K>(p, b, c_v, xv);
+#pragma unroll
+        for (int t = 0; t < kMaxT; ++t)
+            if (t < T) v_s[t][tid] = round_bf16(xv[t]);
     }
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t)
+        if (t >= T) xqk[t] = 0.0f;
     cluster_arrive_relaxed();      // the shared q/k conv_state has been read
 #pragma unroll
     for (int t = 0; t < kMaxT; ++t) {
@@ -201,32 +195,47 @@ __global__ void __launch_bounds__(kThreads) window_kernel(const WindowParams p) 
         if (!ok) continue;
         for (int rr = warp * RPP + sub; rr < rc; rr += (kThreads / 32) * RPP) {
             const int row = ch * rc + rr;
-            float4 *sp = reinterpret_cast<float4 *>(S + (size_t)row * DK) + cl;
-            float4 s = *sp;
+            float4 *sp = reinterpret_cast<float4 *>(S + (size_t)row * DK);
+            float4 s[NG];
+#pragma unroll
+            for (int j = 0; j < NG; ++j) s[j] = sp[j * LPR + cl];
             for (int t = 0; t < T; ++t) {
-                const float4 kk = reinterpret_cast<const float4 *>(k_s[t])[cl];
-                const float4 qq = reinterpret_cast<const float4 *>(q_s[t])[cl];
+                const float4 *k4 = reinterpret_cast<const float4 *>(k_s[t]);
+                const float4 *q4 = reinterpret_cast<const float4 *>(q_s[t]);
                 const float g = gq[t][0], beta = gq[t][1], kq = gq[t][2];
-                float dk = s.x * kk.x;
-                dk = fmaf(s.y, kk.y, dk);
-                dk = fmaf(s.z, kk.z, dk);
-                dk = fmaf(s.w, kk.w, dk);
-                float dq = s.x * qq.x;
-                dq = fmaf(s.y, qq.y, dq);
-                dq = fmaf(s.z, qq.z, dq);
-                dq = fmaf(s.w, qq.w, dq);
+                float dk0 = 0.0f, dk1 = 0.0f, dq0 = 0.0f, dq1 = 0.0f;
+#pragma unroll
+                for (int j = 0; j < NG; ++j) {
+                    const float4 kk = k4[j * LPR + cl], qq = q4[j * LPR + cl];
+                    dk0 = fmaf(s[j].x, kk.x, dk0);
+                    dk1 = fmaf(s[j].y, kk.y, dk1);
+                    dk0 = fmaf(s[j].z, kk.z, dk0);
+                    dk1 = fmaf(s[j].w, kk.w, dk1);
+                    dq0 = fmaf(s[j].x, qq.x, dq0);
+                    dq1 = fmaf(s[j].y, qq.y, dq1);
+                    dq0 = fmaf(s[j].z, qq.z, dq0);
+                    dq1 = fmaf(s[j].w, qq.w, dq1);
+                }
+                float dk = dk0 + dk1, dq = dq0 + dq1;
 #pragma unroll
                 for (int o = LPR / 2; o > 0; o >>= 1) {
                     dk += __shfl_xor_sync(0xffffffffu, dk, o);
                     dq += __shfl_xor_sync(0xffffffffu, dq, o);
                 }
                 const float delta = beta * (v_s[t][row] - g * dk);
-                s.x = fmaf(delta, kk.x, g * s.x);
-                s.y = fmaf(delta, kk.y, g * s.y);
-                s.z = fmaf(delta, kk.z, g * s.z);
-                s.w = fmaf(delta, kk.w, g * s.w);
+#pragma unroll
+                for (int j = 0; j < NG; ++j) {
+                    const float4 kk = k4[j * LPR + cl];
+                    s[j].x = fmaf(delta, kk.x, g * s[j].x);
+                    s[j].y = fmaf(delta, kk.y, g * s[j].y);
+                    s[j].z = fmaf(delta, kk.z, g * s[j].z);
+                    s[j].w = fmaf(delta, kk.w, g * s[j].w);
+                }
                 if (cl == 0) y_s[t][row] = fmaf(delta, kq, g * dq);
-                if (t == keep - 1) *sp = s;       // the state after the kept prefix
+                if (t == keep - 1) {              // the state after the kept prefix
+#pragma unroll
+                    for (int j = 0; j < NG; ++j) sp[j * LPR + cl] = s[j];
+                }
             }
         }
     }
@@ -245,30 +254,23 @@ __global__ void __launch_bounds__(kThreads) window_kernel(const WindowParams p) 
     // ---- conv_state after the kept prefix: rank 0 writes the shared q/k
     // channels once every CTA of the cluster has read them
     cluster_wait_acquire();
-    const int n = p.K - 1;
     if (keep > 0) {
-        if (has_qk && rank == 0) {
-            uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c_qk;
-            for (int j = 0; j < n; ++j) cs[(size_t)j * p.C] = conv_state_after(p.K, in_qk, keep, j);
-        }
-        if (has_v) {
-            uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c_v;
-            for (int j = 0; j < n; ++j) cs[(size_t)j * p.C] = conv_state_after(p.K, in_v, keep, j);
-        }
+        if (has_qk && rank == 0) write_conv_state<K>(p, b, c_qk, keep);
+        if (has_v) write_conv_state<K>(p, b, c_v, keep);
     }
     if (tid == 0) bulk_wait_all();
 }
 
-template <int DK>
+template <int DK, int K>
 cudaError_t launch_t(const WindowParams &p, cudaStream_t st) {
     const int G = p.Hv / p.Hk;
     const int R = p.Dv / p.SN;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(window_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(window_kernel<DK, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)(kMaxRows * DK * sizeof(float)));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(window_kernel<DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(window_kernel<DK, K>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -284,7 +286,7 @@ cudaError_t launch_t(const WindowParams &p, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, window_kernel<DK>, p);
+    return cudaLaunchKernelEx(&cfg, window_kernel<DK, K>, p);
 }
 
 }  // namespace
@@ -299,10 +301,16 @@ cudaError_t launch_decode_window(const Sizes &s, const uint16_t *qkv, const uint
     while (SN * 2 <= s.Dv / 16 && G * SN * 2 <= 8 && heads * SN < 2L * num_sms()) SN *= 2;
     WindowParams p{qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep, y, err,
                    s.B, s.T, s.Hk, s.Hv, s.Dv, s.C(), s.K, SN, s.eps};
-    switch (s.Dk) {
-        case 32: return launch_t<32>(p, st);
-        case 64: return launch_t<64>(p, st);
-        case 128: return launch_t<128>(p, st);
+    switch (s.Dk * 8 + s.K) {
+        case 32 * 8 + 2: return launch_t<32, 2>(p, st);
+        case 32 * 8 + 3: return launch_t<32, 3>(p, st);
+        case 32 * 8 + 4: return launch_t<32, 4>(p, st);
+        case 64 * 8 + 2: return launch_t<64, 2>(p, st);
+        case 64 * 8 + 3: return launch_t<64, 3>(p, st);
+        case 64 * 8 + 4: return launch_t<64, 4>(p, st);
+        case 128 * 8 + 2: return launch_t<128, 2>(p, st);
+        case 128 * 8 + 3: return launch_t<128, 3>(p, st);
+        case 128 * 8 + 4: return launch_t<128, 4>(p, st);
         default: return cudaErrorInvalidValue;
     }
 }

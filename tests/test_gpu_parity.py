@@ -455,6 +455,7 @@ WINDOW_CASES = [
     (2, 16, 32, 128, 128, 4, 8, [8, 3]),
     (1, 1, 16, 32, 128, 2, 1, [1]),
     (4, 2, 8, 128, 64, 4, 7, [7, 0, 1, 6]),
+    (2, 1, 2, 32, 32, 3, 3, [1, 3]),          # keep < K-1: a kept row comes from the old conv_state
 ]
 
 
