@@ -357,6 +357,55 @@ def bench_decode_small(gdn, w: wl.Workload, dev, reps: int = 3) -> dict:
             "gbs_graph_l2_resident": round(by / (us_g / 1e6) / 1e9, 1)}
 
 
+def bench_decode_gated(gdn, w: wl.Workload, dev, iters: int = 200) -> dict:
+    """One decode step of the batched-decode workload with the layer's gated
+    RMS norm: the gated entry point vs decode followed by the separate norm
+    kernel (the state is carried across the steps either way)."""
+    d = w.dims.with_(T=1)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4000 + w.index)
+    qkv = torch.randn((d.B, d.C), generator=gen, device=dev).to(torch.bfloat16)
+    a = torch.randn((d.B, d.Hv), generator=gen, device=dev).to(torch.bfloat16)
+    b = torch.randn((d.B, d.Hv), generator=gen, device=dev).to(torch.bfloat16)
+    conv_w = (torch.randn((d.C, d.K), generator=gen, device=dev) * 0.5).to(torch.bfloat16)
+    A_log = torch.log(torch.empty(d.Hv, device=dev).uniform_(1.0, 16.0, generator=gen))
+    dt_bias = torch.randn(d.Hv, generator=gen, device=dev) * 0.5
+    cs = torch.randn((d.B, d.K - 1, d.C), generator=gen, device=dev).to(torch.bfloat16)
+    st = torch.randn((d.B, d.Hv, d.Dv, d.Dk), generator=gen, device=dev) * 0.05
+    z = torch.randn((d.B, d.Hv, d.Dv), generator=gen, device=dev).to(torch.bfloat16)
+    norm_w = torch.empty(d.Dv, device=dev).uniform_(0.5, 1.5, generator=gen)
+    y = torch.empty((d.B, d.Hv, d.Dv), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(y)
+    stream = torch.cuda.current_stream()
+
+    def step(fused):
+        if fused:
+            gdn.gdn_recurrent_decode_gated(d, qkv, conv_w, cs, a, b, A_log, dt_bias, st, None, z, norm_w, 1e-6,
+                                           out, stream)
+        else:
+            gdn.gdn_recurrent_decode(d, qkv, conv_w, cs, a, b, A_log, dt_bias, st, None, y, stream)
+            gdn.gdn_rmsnorm_gated(d, y, z, norm_w, 1e-6, out, stream)
+
+    us = {}
+    for fused in (True, False):
+        for _ in range(3):
+            step(fused)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            step(fused)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us[fused] = e0.elapsed_time(e1) / iters * 1e3
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the gated decode benchmark")
+    state_rw = 2 * d.B * d.Hv * d.Dv * d.Dk * 4
+    return {"workload": w.name, "us_per_step_gdn_recurrent_decode_gated": round(us[True], 2),
+            "us_per_step_decode_then_norm": round(us[False], 2),
+            "state_gbs_gated": round(state_rw / (us[True] / 1e6) / 1e9, 1)}
+
+
 def bench_decode_window(gdn, w: wl.Workload, dev, T: int = 4, iters: int = 20) -> dict:
     """Speculative-verify window: T tokens per row of the batched-decode
     workload in one fused kernel, all T committed (the state is streamed once
@@ -471,9 +520,39 @@ def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int) -> dict:
         raise RuntimeError("device error word set during the prefill benchmark")
     ms, ms_rec = t_tot / iters, t_rec / iters
     flops = recurrence_flops_per_token(d) * n_valid
+
+    # the layer's gated RMS norm on top of the recurrence: the gated entry
+    # point (the norm in the chunked kernel's epilogue when the heads fill the
+    # GPU) vs the recurrence followed by the separate norm kernel
+    z = (torch.randn((d.B, d.T, d.Hv, d.Dv), generator=gen, device=dev)).to(torch.bfloat16)
+    norm_w = torch.empty(d.Dv, device=dev).uniform_(0.5, 1.5, generator=gen)
+    out = torch.empty_like(y)
+
+    def gated(fused):
+        if fused:
+            gdn.gdn_prefill_gated(d, q, k, v, g, beta, state0, s_out, mask, z, norm_w, 1e-6, out, chunk,
+                                  ws if nws else None, stream)
+        else:
+            gdn.gdn_prefill(d, q, k, v, g, beta, state0, s_out, mask, y, chunk, ws if nws else None, stream)
+            gdn.gdn_rmsnorm_gated(d, y, z, norm_w, 1e-6, out, stream)
+
+    t_g = {}
+    for fused in (True, False):
+        gated(fused)
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for _ in range(iters):
+            gated(fused)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        t_g[fused] = ev[0].elapsed_time(ev[1]) / iters
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the gated prefill benchmark")
     return {"workload": w.name, "chunk": chunk, "ms": round(ms, 4), "recurrence_ms": round(ms_rec, 4),
             "tokens": n_valid, "tokens_per_s": n_valid / (ms / 1e3),
-            "recurrence_tflops": flops / (ms_rec / 1e3) / 1e12}
+            "recurrence_tflops": flops / (ms_rec / 1e3) / 1e12,
+            "recurrence_gated_norm_ms": {"gdn_prefill_gated": round(t_g[True], 4),
+                                         "prefill_then_norm": round(t_g[False], 4)}}
 
 
 # ---------------------------------------------------------------------------
@@ -540,11 +619,13 @@ def main():
     small_decode = None
     gated_norm = None
     window = None
+    decode_gated = None
     prefill = []
     if not args.no_prefill:
         small_decode = bench_decode_small(gdn, wl.WORKLOADS["decode_b1"], dev)
         gated_norm = bench_rmsnorm_gated(gdn, wl.WORKLOADS["prefill_ragged"], dev)
         window = bench_decode_window(gdn, w, dev)
+        decode_gated = bench_decode_gated(gdn, w, dev)
         for name in ("prefill_t8192", "prefill_ragged"):
             for chunk in (0, 64):
                 try:
@@ -590,6 +671,7 @@ def main():
         "decode_b1": small_decode,
         "rmsnorm_gated": gated_norm,
         "decode_window": window,
+        "decode_gated_norm": decode_gated,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -100,6 +100,60 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtyp
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// gdn_prefill and gdn_prefill_gated: z == nullptr gives y, else the gated norm.
+static gdn_status prefill_impl(const gdn_dims *dims, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               const float *g, const float *beta, const float *state_in, float *state_out,
+                               const uint8_t *mask, uint16_t *y, const uint16_t *z, const float *norm_w,
+                               float norm_eps, int chunk, void *workspace, size_t ws_bytes, gdn_stream stream) {
+    Sizes s;
+    gdn_status st = check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    if (chunk != 0 && chunk != 64) return GDN_ERR_UNSUPPORTED;
+    if (chunk == 64 && (s.Dk != 128 || s.Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    const size_t BT = (size_t)s.B * s.T;
+    const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
+    if (!ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT) || !ok_ptr(g, BT) || !ok_ptr(beta, BT) ||
+        !ok_ptr(state_in, 0) || !ok_ptr(state_out, nstate) || !ok_ptr(mask, 0) || !ok_ptr(y, BT))
+        return GDN_ERR_INVALID_ARG;
+    if (z != nullptr && (!ok_ptr(norm_w, 1) || !(norm_eps >= 0.0f))) return GDN_ERR_INVALID_ARG;
+    if (workspace != nullptr && (ws_bytes < row_order_workspace(s) || !aligned16(workspace)))
+        return GDN_ERR_INVALID_ARG;
+    if (s.B == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (s.T == 0) {
+        if (state_in == nullptr) return from_cuda(cudaMemsetAsync(state_out, 0, nstate * sizeof(float), cs));
+        if (state_in == state_out) return GDN_OK;
+        return from_cuda(
+            cudaMemcpyAsync(state_out, state_in, nstate * sizeof(float), cudaMemcpyDeviceToDevice, cs));
+    }
+    // rows of a masked batch longest first (scheduling only; results identical)
+    const int *order = nullptr;
+    if (mask != nullptr && workspace != nullptr && s.B > 1) {
+        cudaError_t e = launch_row_order(s, mask, workspace, cs);
+        if (e != cudaSuccess) return from_cuda(e);
+        order = static_cast<const int *>(workspace);
+    }
+    if (chunk == 0) {
+        // the sequential kernel spreads a head's rows over several CTAs: y goes
+        // to the output buffer and the gated norm runs over it in place
+        cudaError_t e = launch_prefill_seq(s, q, k, v, g, beta, state_in, state_out, mask, order, y,
+                                           error_word(), cs);
+        if (e == cudaSuccess && z != nullptr) e = launch_rmsnorm_gated(s, y, z, norm_w, norm_eps, y, cs);
+        return from_cuda(e);
+    }
+    // Chunked form: the norm in the kernel's epilogue when there are at least
+    // as many heads as SMs.  With fewer, each head's chain of chunks is the
+    // critical path and the epilogue lengthens every link of it, while a
+    // separate norm kernel spreads over the whole GPU (measured at B = 1,
+    // Hv = 32, T = 8192: 1.52 ms fused against 1.41 ms; at B = 8, Hv = 64,
+    // ragged T = 16384: 4.54 ms fused against 5.20 ms).
+    const bool fuse = z != nullptr && (long)s.B * s.Hv >= num_sms();
+    cudaError_t e = launch_prefill_chunked(s, q, k, v, g, beta, state_in, state_out, mask, order, y,
+                                           fuse ? z : nullptr, norm_w, norm_eps, error_word(), cs);
+    if (e == cudaSuccess && z != nullptr && !fuse) e = launch_rmsnorm_gated(s, y, z, norm_w, norm_eps, y, cs);
+    return from_cuda(e);
+}
+
 }  // namespace gdn
 
 using gdn::ok_ptr;
@@ -161,7 +215,28 @@ gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qkv, const
         return GDN_ERR_INVALID_ARG;
     if (B == 0) return GDN_OK;
     return gdn::from_cuda(gdn::launch_decode(s, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y,
-                                             gdn::error_word(), (cudaStream_t)stream));
+                                             nullptr, nullptr, 0.0f, gdn::error_word(), (cudaStream_t)stream));
+}
+
+gdn_status gdn_recurrent_decode_gated(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
+                                      uint16_t *conv_state, const uint16_t *a, const uint16_t *b,
+                                      const float *A_log, const float *dt_bias, float *state,
+                                      const uint8_t *row_mask, const uint16_t *z, const float *norm_w,
+                                      float norm_eps, uint16_t *out, gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    if (s.T != 1) return GDN_ERR_INVALID_ARG;
+    if (s.Hv / s.Hk > 16) return GDN_ERR_UNSUPPORTED;
+    if (!(norm_eps >= 0.0f)) return GDN_ERR_INVALID_ARG;
+    const size_t B = (size_t)s.B;
+    if (!ok_ptr(qkv, B) || !ok_ptr(conv_w, B) || !ok_ptr(conv_state, B) || !ok_ptr(a, B) || !ok_ptr(b, B) ||
+        !ok_ptr(A_log, B) || !ok_ptr(dt_bias, B) || !ok_ptr(state, B) || !ok_ptr(row_mask, 0) || !ok_ptr(z, B) ||
+        !ok_ptr(norm_w, B) || !ok_ptr(out, B))
+        return GDN_ERR_INVALID_ARG;
+    if (B == 0) return GDN_OK;
+    return gdn::from_cuda(gdn::launch_decode(s, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, out,
+                                             z, norm_w, norm_eps, gdn::error_word(), (cudaStream_t)stream));
 }
 
 gdn_status gdn_decode_window(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
@@ -193,38 +268,18 @@ gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *
                        const float *g, const float *beta, const float *state_in, float *state_out,
                        const uint8_t *mask, uint16_t *y, int chunk, void *workspace, size_t ws_bytes,
                        gdn_stream stream) {
-    gdn::Sizes s;
-    gdn_status st = gdn::check_dims(dims, &s);
-    if (st != GDN_OK) return st;
-    if (chunk != 0 && chunk != 64) return GDN_ERR_UNSUPPORTED;
-    if (chunk == 64 && (s.Dk != 128 || s.Dv != 128)) return GDN_ERR_UNSUPPORTED;
-    const size_t BT = (size_t)s.B * s.T;
-    const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
-    if (!ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT) || !ok_ptr(g, BT) || !ok_ptr(beta, BT) ||
-        !ok_ptr(state_in, 0) || !ok_ptr(state_out, nstate) || !ok_ptr(mask, 0) || !ok_ptr(y, BT))
-        return GDN_ERR_INVALID_ARG;
-    if (workspace != nullptr && (ws_bytes < gdn::row_order_workspace(s) || !gdn::aligned16(workspace)))
-        return GDN_ERR_INVALID_ARG;
-    if (s.B == 0) return GDN_OK;
-    cudaStream_t cs = (cudaStream_t)stream;
-    if (s.T == 0) {
-        if (state_in == nullptr) return gdn::from_cuda(cudaMemsetAsync(state_out, 0, nstate * sizeof(float), cs));
-        if (state_in == state_out) return GDN_OK;
-        return gdn::from_cuda(
-            cudaMemcpyAsync(state_out, state_in, nstate * sizeof(float), cudaMemcpyDeviceToDevice, cs));
-    }
-    // rows of a masked batch longest first (scheduling only; results identical)
-    const int *order = nullptr;
-    if (mask != nullptr && workspace != nullptr && s.B > 1) {
-        cudaError_t e = gdn::launch_row_order(s, mask, workspace, cs);
-        if (e != cudaSuccess) return gdn::from_cuda(e);
-        order = static_cast<const int *>(workspace);
-    }
-    if (chunk == 0)
-        return gdn::from_cuda(gdn::launch_prefill_seq(s, q, k, v, g, beta, state_in, state_out, mask, order, y,
-                                                      gdn::error_word(), cs));
-    return gdn::from_cuda(gdn::launch_prefill_chunked(s, q, k, v, g, beta, state_in, state_out, mask, order, y,
-                                                      gdn::error_word(), cs));
+    return gdn::prefill_impl(dims, q, k, v, g, beta, state_in, state_out, mask, y, nullptr, nullptr, 0.0f, chunk,
+                        workspace, ws_bytes, stream);
+}
+
+gdn_status gdn_prefill_gated(const gdn_dims *dims, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             const float *g, const float *beta, const float *state_in, float *state_out,
+                             const uint8_t *mask, const uint16_t *z, const float *norm_w, float norm_eps,
+                             uint16_t *out, int chunk, void *workspace, size_t ws_bytes, gdn_stream stream) {
+    const size_t BT = dims == nullptr ? 0 : (size_t)(dims->B > 0 ? dims->B : 0) * (size_t)(dims->T > 0 ? dims->T : 0);
+    if (!gdn::ok_ptr(z, BT) || z == nullptr) return GDN_ERR_INVALID_ARG;
+    return gdn::prefill_impl(dims, q, k, v, g, beta, state_in, state_out, mask, out, z, norm_w, norm_eps, chunk,
+                        workspace, ws_bytes, stream);
 }
 
 gdn_status gdn_rmsnorm_gated(const gdn_dims *dims, const uint16_t *y, const uint16_t *z, const float *norm_w,

@@ -24,6 +24,17 @@
 // the q/k channels, arrives on the cluster barrier, and only cluster rank 0
 // writes the new q/k conv_state after waiting on it.  v channels belong to one
 // CTA each and are updated by it.
+//
+// NORM variant: the step's output is the layer's RMSNormGated of y ("mlex
+// 0.1.2, src/models/gated_delta.rs", GatedDeltaNet::forward: f32 rms_norm of
+// the bf16 y over Dv, times the norm weight, times silu(z), cast to bf16)
+// instead of y.  It runs only where one CTA holds all Dv rows of a head
+// (SN = 1).  With the rows spread over several CTAs the per-head sum needs an
+// exchange between them, and every microsecond that adds to a CTA's life
+// costs about nine at this occupancy (the state streams through a fixed
+// number of CTA slots): measured 115 us per step on the batched-decode
+// workload against 102 us for this kernel followed by the separate norm
+// kernel, so that pair is used there instead.
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,7 +52,10 @@ struct DecodeParams {
     const float *A_log, *dt_bias;
     float *state;
     const uint8_t *row_mask;
-    uint16_t *y;
+    uint16_t *y;              // y, or the gated-norm output for the NORM variant
+    const uint16_t *z;        // NORM: gate input [B, Hv, Dv]
+    const float *norm_w;      // NORM: weight [Dv]
+    float norm_eps;
     unsigned *err;
     int B, Hk, Hv, Dv, C, K, SN;
     float eps;
@@ -87,8 +101,8 @@ __device__ __forceinline__ float conv_apply(int K, const ConvIn &in, uint16_t (&
     return silu(u);
 }
 
-template <int DK>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) {
+template <int DK, bool NORM>
+__global__ void __launch_bounds__(kThreads, 6) decode_kernel(const DecodeParams p) {
     constexpr int LPR = DK / 4;       // lanes per state row (one float4 each)
     constexpr int RPP = 32 / LPR;     // rows per warp pass
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -144,6 +158,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     if (has_v) load_conv(p, b, c_v, in_v);
     if (has_qk) xqk = conv_apply(p.K, in_qk, nw_qk);
     if (has_v) v_s[tid] = round_bf16(conv_apply(p.K, in_v, nw_v));
+    // NORM: z and the weight of this thread's row, fetched now so that their
+    // latency hides behind the state copy
+    float zv = 0.0f, wv = 0.0f;
+    if constexpr (NORM) {
+        if (tid < R) {
+            zv = bf16_to_f32(p.z[((size_t)b * p.Hv + hv) * p.Dv + r0 + tid]);
+            wv = p.norm_w[r0 + tid];
+        }
+    }
     // every read of the shared (q/k) conv_state of this CTA has been consumed
     // above, so a relaxed arrive suffices (a release arrive would also wait for
     // this thread's unrelated outstanding accesses)
@@ -224,8 +247,23 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
         bulk_commit();
     }
 
-    if (ok_all)
-        for (int i = tid; i < R; i += kThreads) yrow[i] = f32_to_bf16(y_s[i]);
+    if constexpr (!NORM) {
+        if (ok_all)
+            for (int i = tid; i < R; i += kThreads) yrow[i] = f32_to_bf16(y_s[i]);
+    } else {
+        // gated RMS norm of the head's bf16 y over all Dv rows
+        const float yv = tid < R ? round_bf16(y_s[tid]) : 0.0f;
+        const float ss = warp_sum(yv * yv);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
+        if (tid < R && ok_all) {
+            const float rs = 1.0f / sqrtf(tot * (1.0f / (float)p.Dv) + p.norm_eps);
+            yrow[tid] = f32_to_bf16(silu(zv) * ((yv * rs) * wv));
+        }
+    }
 
     // ---- new conv_state: rank 0 writes the shared q/k channels after every
     // CTA of the cluster has read them; each CTA writes its own v channels.
@@ -242,19 +280,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p) 
     if (tid == 0) bulk_wait_all();
 }
 
-template <int DK>
+template <int DK, bool NORM>
 cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t st) {
     const int G = p.Hv / p.Hk;
     const int R = p.Dv / p.SN;
     const size_t smem = (size_t)R * DK * sizeof(float);
-    static bool attr_set[2] = {false, false};   // per instantiation; benign race
-    if (!attr_set[0]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static bool attr_set = false;   // per instantiation; benign race
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DK, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)(kMaxRows * DK * sizeof(float)));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(decode_kernel<DK>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(decode_kernel<DK, NORM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
-        attr_set[0] = true;
+        attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G * p.SN, p.Hk, p.B);
@@ -268,14 +306,15 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<DK>, p);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<DK, NORM>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
                           const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
-                          float *state, const uint8_t *row_mask, uint16_t *y, unsigned *err, cudaStream_t st) {
+                          float *state, const uint8_t *row_mask, uint16_t *y, const uint16_t *z,
+                          const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st) {
     const int G = s.Hv / s.Hk;
     // Split each head's rows over SN CTAs: at least 2 when rows allow (smaller
     // CTAs keep more of them, at different phases, resident per SM: measured
@@ -285,12 +324,25 @@ cudaError_t launch_decode(const Sizes &s, const uint16_t *qkv, const uint16_t *c
     int SN = (s.Dv >= 64 && G * 2 <= 8) ? 2 : 1;
     const long heads = (long)s.B * s.Hv;
     while (SN * 2 <= s.Dv / 16 && G * SN * 2 <= 8 && heads * SN < 2L * num_sms()) SN *= 2;
-    DecodeParams p{qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y, err,
+    DecodeParams p{qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y, z, norm_w, norm_eps, err,
                    s.B, s.Hk, s.Hv, s.Dv, s.C(), s.K, SN, s.eps};
+    const bool norm = z != nullptr && SN == 1;
+    if (z != nullptr && SN > 1) {
+        // rows of a head over several CTAs: y into the output, then the norm in place
+        cudaError_t e = cudaSuccess;
+        switch (s.Dk) {
+            case 32: e = launch_decode_t<32, false>(p, st); break;
+            case 64: e = launch_decode_t<64, false>(p, st); break;
+            case 128: e = launch_decode_t<128, false>(p, st); break;
+            default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaSuccess) return e;
+        return launch_rmsnorm_gated(s, y, z, norm_w, norm_eps, y, st);
+    }
     switch (s.Dk) {
-        case 32: return launch_decode_t<32>(p, st);
-        case 64: return launch_decode_t<64>(p, st);
-        case 128: return launch_decode_t<128>(p, st);
+        case 32: return norm ? launch_decode_t<32, true>(p, st) : launch_decode_t<32, false>(p, st);
+        case 64: return norm ? launch_decode_t<64, true>(p, st) : launch_decode_t<64, false>(p, st);
+        case 128: return norm ? launch_decode_t<128, true>(p, st) : launch_decode_t<128, false>(p, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -27,7 +27,8 @@ cudaError_t launch_gating(const Sizes &s, const uint16_t *a, const uint16_t *b, 
 
 cudaError_t launch_decode(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
                           const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
-                          float *state, const uint8_t *row_mask, uint16_t *y, unsigned *err, cudaStream_t st);
+                          float *state, const uint8_t *row_mask, uint16_t *y, const uint16_t *z,
+                          const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st);
 
 cudaError_t launch_decode_window(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
                                  const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
@@ -59,7 +60,7 @@ cudaError_t launch_prefill_seq_vec(const Sizes &s, const uint16_t *q, const uint
 
 cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                    const float *g, const float *beta, const float *state_in, float *state_out,
-                                   const uint8_t *mask, const int *order, uint16_t *y, unsigned *err,
-                                   cudaStream_t st);
+                                   const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
+                                   const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st);
 
 }  // namespace gdn

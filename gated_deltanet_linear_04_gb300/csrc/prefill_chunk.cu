@@ -32,6 +32,12 @@
 // 128.  Shared memory: 13 slots of 16 KiB reused across the phases of a chunk.
 // Chunks whose 64 steps are all masked are skipped: their y is written zero and
 // their inputs are never staged.
+//
+// NORM variant: each chunk's output is the layer's RMSNormGated of y ("mlex
+// 0.1.2, src/models/gated_delta.rs", GatedDeltaNet::forward: f32 rms_norm of
+// the bf16 y over Dv, times the norm weight, times silu(z), cast to bf16),
+// computed from the bf16 y staging tile with the z tile brought in by TMA,
+// so y itself never goes to memory.
 #include "common.cuh"
 #include "internal.h"
 #include "mask_scan.cuh"
@@ -60,6 +66,7 @@ constexpr uint32_t S_NW = S_A;          // -W [64][128] tf32, 4 K-tiles of 8 KiB
 constexpr uint32_t S_DT = S_BV;         // D^T [128][64] tf32, 2 K-tiles of 16 KiB (slots 7-8)
 constexpr uint32_t S_P = S_A;           // P [64][64] tf32, 2 K-tiles of 8 KiB (slot 11)
 constexpr uint32_t S_YST = S_BK;        // y staging [64][128] bf16 (slot 9, free after the W product)
+constexpr uint32_t S_Z = S_GQ;          // NORM: z tile [64][128] bf16 (slot 3, free after the S0 products)
 
 // TMEM columns
 constexpr uint32_t C_QK = 0, C_D = 64, C_W = 128, C_Y = 192, C_S = 256, kTmemCols = 512;
@@ -69,7 +76,9 @@ struct ChunkParams {
     float *state_out;
     const uint8_t *mask;
     const int *order;   // row slot -> batch row (optional, with a mask)
-    uint16_t *y;
+    uint16_t *y;        // y, or the gated-norm output for the NORM variant
+    const float *norm_w;
+    float norm_eps;
     unsigned *err;
     int B, T, Hk, Hv;
 };
@@ -145,12 +154,15 @@ __device__ __forceinline__ float kq_elem(const uint8_t *sm, int row, int dk) {
     return bf16_to_f32(*p);
 }
 
+template <bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                      const __grid_constant__ CUtensorMap tm_q,
                                                                      const __grid_constant__ CUtensorMap tm_v,
+                                                                     const __grid_constant__ CUtensorMap tm_z,
                                                                      const ChunkParams p) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+    __shared__ __align__(8) uint64_t bar_tma, bar_mma, bar_z;
+    __shared__ float s_w[NORM ? kD : 1];
     __shared__ uint32_t tmem_slot;
     __shared__ float s_g[2][kC], s_b[2][kC];
     __shared__ int s_m[2][kC];
@@ -179,10 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_z, 1);
         fence_mbar_init();
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_v);
+        if constexpr (NORM) prefetch_tmap(&tm_z);
+    }
+    if constexpr (NORM) {
+        for (int i = tid; i < kD; i += kThreads) s_w[i] = p.norm_w[i];
     }
     if (warp == 0) {
         umma::tmem_alloc(&tmem_slot, kTmemCols);
@@ -251,6 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
 
     uint32_t mma_phase = 0;
     bool ok = true;
+    bool z_pending = false;     // thread 0: a z copy was issued and not yet waited on
+    uint32_t z_parity = 0;
     // bounded wait on the MMA barrier by every thread, agreed across the CTA
     auto wait_mma = [&]() {
         bool w = mbar_wait(&bar_mma, mma_phase & 1u, p.err);
@@ -468,6 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
 
         // ---- S7: D^T -> smem (A operand); P = M o Q K^T -> smem (B operand);
         // S <- exp(lg_63) S in TMEM (the D and Y products have read S already)
+        if constexpr (NORM) {
+            // the gQ slot is free now: bring in this chunk's z tile
+            if (tid == 0) {
+                mbar_expect_tx(&bar_z, 16384);
+                tma_load_2d(sm + S_Z, &tm_z, hv * kD, b * T + t0, &bar_z);
+                z_pending = true;
+                z_parity = (uint32_t)(it & 1);
+            }
+        }
         {
             const float gl = s_gam[kC - 1];
 #pragma unroll
@@ -537,6 +565,50 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         }
         umma::fence_before_sync();
         __syncthreads();
+        if constexpr (NORM) {
+            // gated RMS norm per step: 4 threads per step, each covering the
+            // 16-byte column groups qd, qd + 4, qd + 8, qd + 12 of the row
+            if (!mbar_wait(&bar_z, (uint32_t)(it & 1), p.err)) ok = false;
+            z_pending = false;
+            const int r = tid >> 2, qd = tid & 3;
+            uint8_t *yrow = sm + S_YST + r * kD * 2;
+            const uint8_t *zrow = sm + S_Z + r * kD * 2;
+            float ss = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(yrow + (j * 4 + qd) * 16);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+                    ss = fmaf(lo, lo, ss);
+                    ss = fmaf(hi, hi, ss);
+                }
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            const float rs = 1.0f / sqrtf(ss * (1.0f / (float)kD) + p.norm_eps);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c16 = j * 4 + qd;
+                const uint4 u = *reinterpret_cast<const uint4 *>(yrow + c16 * 16);
+                const uint4 zz = *reinterpret_cast<const uint4 *>(zrow + c16 * 16);
+                const uint32_t yw[4] = {u.x, u.y, u.z, u.w}, zw[4] = {zz.x, zz.y, zz.z, zz.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int dv = c16 * 8 + 2 * e;
+                    const float y0 = __uint_as_float(yw[e] << 16), y1 = __uint_as_float(yw[e] & 0xffff0000u);
+                    const float z0 = __uint_as_float(zw[e] << 16), z1 = __uint_as_float(zw[e] & 0xffff0000u);
+                    const float o0 = silu(z0) * ((y0 * rs) * s_w[dv]);
+                    const float o1 = silu(z1) * ((y1 * rs) * s_w[dv + 1]);
+                    o[e] = (uint32_t)f32_to_bf16(o0) | ((uint32_t)f32_to_bf16(o1) << 16);
+                }
+                *reinterpret_cast<uint4 *>(yrow + c16 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            ok = __syncthreads_and(ok) != 0;
+            if (!ok) break;
+        }
         {
             const int nv = min(kC, T - t0);
             for (int i = tid; i < nv * (kD / 8); i += kThreads) {
@@ -563,22 +635,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
                     make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
         }
     } else if (tid == 0) {
-        // a wait gave up: give in-flight MMAs a bounded chance to drain
+        // a wait gave up: give in-flight MMAs (and a z copy) a bounded chance to drain
         mbar_wait(&bar_mma, mma_phase & 1u, nullptr);
+        if (z_pending) mbar_wait(&bar_z, z_parity, nullptr);
     }
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
+template <bool NORM>
+cudaError_t set_smem_attr() {
+    static bool attr_set = false;   // per instantiation; benign race
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel<NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                    const float *g, const float *beta, const float *state_in, float *state_out,
-                                   const uint8_t *mask, const int *order, uint16_t *y, unsigned *err,
-                                   cudaStream_t st) {
+                                   const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
+                                   const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st) {
     if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
-    CUtensorMap tk, tq, tv;
+    CUtensorMap tk, tq, tv, tz;
     const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
     if (!encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -587,17 +672,19 @@ cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint
         !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    ChunkParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y, err,
+    tz = tv;   // unused without the norm
+    if (z != nullptr && !encode_tmap_2d(&tz, z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC,
+                                        kD, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaError_t e = z != nullptr ? set_smem_attr<true>() : set_smem_attr<false>();
+    if (e != cudaSuccess) return e;
+    ChunkParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y, norm_w, norm_eps, err,
                   s.B, s.T, s.Hk, s.Hv};
     dim3 grid(s.Hv, s.B);
-    prefill_chunk_kernel<<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, p);
+    if (z != nullptr)
+        prefill_chunk_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, tz, p);
+    else
+        prefill_chunk_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, tz, p);
     return cudaGetLastError();
 }
 

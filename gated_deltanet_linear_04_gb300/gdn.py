@@ -44,6 +44,10 @@ _SIGS = {
     "gdn_recurrent_decode": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_prefill": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P,
                                    ctypes.c_size_t, _P]),
+    "gdn_recurrent_decode_gated": (ctypes.c_int, [ctypes.POINTER(GdnDims)] + [_P] * 11 +
+                                   [ctypes.c_float, _P, _P]),
+    "gdn_prefill_gated": (ctypes.c_int, [ctypes.POINTER(GdnDims)] + [_P] * 10 +
+                          [ctypes.c_float, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "gdn_prefill_vec": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_prefill_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims), ctypes.c_int]),
     "gdn_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(GdnDims)] + [ctypes.c_void_p] * 9 +
@@ -160,6 +164,30 @@ def gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, w
                              int(chunk), ws_ptr, ws_bytes, _stream(stream)), "gdn_prefill")
 
 
+def gdn_recurrent_decode_gated(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, z, norm_w,
+                               norm_eps, out, stream=None):
+    d = make_dims(dims)
+    _check(lib().gdn_recurrent_decode_gated(ctypes.byref(d), _ptr(qkv, BF16, "qkv"), _ptr(conv_w, BF16, "conv_w"),
+                                            _ptr(conv_state, BF16, "conv_state"), _ptr(a, BF16, "a"),
+                                            _ptr(b, BF16, "b"), _ptr(A_log, F32, "A_log"),
+                                            _ptr(dt_bias, F32, "dt_bias"), _ptr(state, F32, "state"),
+                                            _ptr(row_mask, U8, "row_mask"), _ptr(z, BF16, "z"),
+                                            _ptr(norm_w, F32, "norm_w"), float(norm_eps), _ptr(out, BF16, "out"),
+                                            _stream(stream)), "gdn_recurrent_decode_gated")
+
+
+def gdn_prefill_gated(dims, q, k, v, g, beta, state_in, state_out, mask, z, norm_w, norm_eps, out, chunk=0,
+                      workspace=None, stream=None):
+    d = make_dims(dims)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ws_ptr = None if workspace is None else (workspace.data_ptr() or None)
+    _check(lib().gdn_prefill_gated(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
+                                   _ptr(g, F32, "g"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
+                                   _ptr(state_out, F32, "state_out"), _ptr(mask, U8, "mask"), _ptr(z, BF16, "z"),
+                                   _ptr(norm_w, F32, "norm_w"), float(norm_eps), _ptr(out, BF16, "out"),
+                                   int(chunk), ws_ptr, ws_bytes, _stream(stream)), "gdn_prefill_gated")
+
+
 def gdn_prefill_noalloc(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, stream=None):
     """gdn_prefill with the library's own fixed scratch (no workspace, no
     allocation); for callers that cannot allocate device memory."""
@@ -242,6 +270,30 @@ def prefill(dims, q, k, v, g, beta, state_in=None, mask=None, chunk=0, state_out
         ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
     gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk, ws, stream)
     return y, state_out
+
+
+def recurrent_decode_gated(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, z, norm_w, norm_eps=1e-6,
+                           row_mask=None, stream=None):
+    """One token with the gated norm fused; returns out [B, Hv, Dv]."""
+    out = torch.empty((dims.B, dims.Hv, dims.Dv), dtype=BF16, device=qkv.device)
+    gdn_recurrent_decode_gated(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, z, norm_w,
+                               norm_eps, out, stream)
+    return out
+
+
+def prefill_gated(dims, q, k, v, g, beta, z, norm_w, norm_eps=1e-6, state_in=None, mask=None, chunk=0,
+                  state_out=None, stream=None):
+    """Returns (out, state_out), out the gated norm of y."""
+    dev = q.device
+    out = torch.empty((dims.B, dims.T, dims.Hv, dims.Dv), dtype=BF16, device=dev)
+    if state_out is None:
+        state_out = torch.empty((dims.B, dims.Hv, dims.Dv, dims.Dk), dtype=F32, device=dev)
+    ws = None
+    if mask is not None:
+        nws = gdn_prefill_workspace_size(dims, chunk)
+        ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
+    gdn_prefill_gated(dims, q, k, v, g, beta, state_in, state_out, mask, z, norm_w, norm_eps, out, chunk, ws, stream)
+    return out, state_out
 
 
 def rmsnorm_gated(dims, y, z, norm_w, norm_eps=1e-6, stream=None):

@@ -114,6 +114,30 @@ GDN_API gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qk
                                 const float *A_log, const float *dt_bias, float *state,
                                 const uint8_t *row_mask, uint16_t *y, gdn_stream stream);
 
+/* gdn_recurrent_decode followed by the layer's RMSNormGated.  The norm runs
+ * in the decode kernel's epilogue when one CTA holds all Dv rows of a head
+ * (for example Hv/Hk = 16 or Dv = 32 with few heads); when a head's rows are
+ * spread over several CTAs, the decode kernel writes y into `out` and a
+ * second kernel normalises it in place, which measured faster than an
+ * exchange of partial sums between the CTAs.  (mlex gated_delta.rs,
+ * GatedDeltaNet::forward: the f32 rms_norm of y over Dv with norm_eps, times
+ * the norm weight, times silu(z), cast to bf16.)  Per (b, hv):
+ *   out = bf16( silu(z) * norm_w * yb / sqrt(mean_Dv(yb^2) + norm_eps) )
+ * where yb is the bf16-rounded recurrence output (the y gdn_recurrent_decode
+ * would write), so the result equals gdn_recurrent_decode followed by
+ * gdn_rmsnorm_gated up to f32 summation order.
+ *   z          bf16 [B, Hv, Dv] (in): the in_proj_z output of the token
+ *   norm_w     f32  [Dv] (in);  norm_eps >= 0
+ *   out        bf16 [B, Hv, Dv] (out); a zero row of row_mask gives zeros
+ *              (its y is 0; the sign of a zero follows silu(z) * norm_w)
+ * Other arguments and limits as gdn_recurrent_decode. */
+GDN_API gdn_status gdn_recurrent_decode_gated(const gdn_dims *dims, const uint16_t *qkv,
+                                              const uint16_t *conv_w, uint16_t *conv_state,
+                                              const uint16_t *a, const uint16_t *b, const float *A_log,
+                                              const float *dt_bias, float *state, const uint8_t *row_mask,
+                                              const uint16_t *z, const float *norm_w, float norm_eps,
+                                              uint16_t *out, gdn_stream stream);
+
 /* Multi-token decode window for speculative verification: dims->T (1..8)
  * new tokens per row, fused like gdn_recurrent_decode (one pass over the f32
  * state).  y is written for all T tokens; conv_state and state are advanced by
@@ -165,6 +189,27 @@ GDN_API gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const ui
                        const float *state_in, float *state_out, const uint8_t *mask,
                        uint16_t *y, int chunk, void *workspace, size_t ws_bytes,
                        gdn_stream stream);
+
+/* gdn_prefill with the layer's RMSNormGated applied to y before it is
+ * stored.  (mlex gated_delta.rs, GatedDeltaNet::forward: the f32 rms_norm of
+ * y over Dv with norm_eps, times the norm weight, times silu(z), cast to bf16.)
+ * Per (b, t, hv):
+ *   out = bf16( silu(z) * norm_w * yb / sqrt(mean_Dv(yb^2) + norm_eps) )
+ * with yb the bf16 y that gdn_prefill would write (so a masked step, yb = 0,
+ * gives a zero).  chunk = 64 runs the norm in the chunked kernel's epilogue
+ * (y never goes to memory) when B * Hv is at least the GPU's SM count; with
+ * fewer heads, and for chunk = 0 (whose kernel spreads a head's rows over
+ * several CTAs), y is written to `out` and a second kernel normalises it in
+ * place, which measured faster there.
+ *   z          bf16 [B, T, Hv, Dv] (in): the in_proj_z output
+ *   norm_w     f32  [Dv] (in);  norm_eps >= 0
+ *   out        bf16 [B, T, Hv, Dv] (out)
+ * Other arguments, the workspace and the limits as gdn_prefill. */
+GDN_API gdn_status gdn_prefill_gated(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
+                                     const uint16_t *v, const float *g, const float *beta,
+                                     const float *state_in, float *state_out, const uint8_t *mask,
+                                     const uint16_t *z, const float *norm_w, float norm_eps, uint16_t *out,
+                                     int chunk, void *workspace, size_t ws_bytes, gdn_stream stream);
 
 /* RMSNormGated output of the layer, applied to the recurrence output y.
  * (mlex gated_delta.rs, GatedDeltaNet::forward: rms_norm of y in f32 with

@@ -36,6 +36,23 @@ def assert_y_close(y_gpu, y_ref, what="y"):
     return err, rel
 
 
+def assert_out_close(o_gpu, o_ref, what="out"):
+    """The gated-norm output, y normalised to unit RMS per head row and
+    scaled by silu(z) * w: values reach a few units, where one bf16 ulp is
+    already 2^-6 .. 2^-5, so the y bound applies relative to max(1, |ref|)
+    elementwise (an absolute bound for values below 1), with the same 1%
+    relative L2 over the whole tensor."""
+    o = np.asarray(o_gpu, np.float64)
+    r = np.asarray(o_ref, np.float64)
+    assert o.shape == r.shape, (o.shape, r.shape)
+    assert np.all(np.isfinite(o)), what + ": non-finite output"
+    err = (np.abs(o - r) / np.maximum(1.0, np.abs(r))).max() if o.size else 0.0
+    rel = rel_l2(o, r) if o.size else 0.0
+    assert err <= Y_MAX_ABS and rel <= Y_REL_L2, "%s: max scaled err %.3e (<= %.0e), rel L2 %.3e (<= %.0e)" % (
+        what, err, Y_MAX_ABS, rel, Y_REL_L2)
+    return err, rel
+
+
 def assert_state_close(s_gpu, s_ref, what="state", tol=STATE_REL_L2):
     s = np.asarray(s_gpu, np.float64)
     r = np.asarray(s_ref, np.float64)

@@ -427,6 +427,86 @@ def test_rmsnorm_gated(gdn, B, T, Hv, Dv):
     assert np.all(U.bf16_dev_to_f64(out[0, 0]) == 0.0)   # +0 or -0 (silu(z) < 0 times 0)
 
 
+# f-1 fused: the gated norm in the decode and prefill epilogues
+GATED_DECODE_CASES = [
+    # B, Hk, Hv, Dk, Dv, K, row mask
+    (3, 2, 4, 128, 128, 4, True),      # two row slices per head: sums exchanged in the cluster
+    (2, 1, 16, 64, 64, 3, False),      # G = 16: one slice per head
+    (4, 4, 4, 32, 32, 2, False),       # G = 1: several slices per head
+    (2, 16, 32, 128, 128, 4, False),
+]
+
+
+@pytest.mark.parametrize("B,Hk,Hv,Dk,Dv,K,rm", GATED_DECODE_CASES)
+def test_decode_gated(gdn, B, Hk, Hv, Dk, Dv, K, rm):
+    d = wl.Dims(B=B, T=1, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, K=K)
+    inp = inputs_for(d, 900 + B * Hv)
+    gi = wl.make_gate_inputs(d, 950 + B)
+    z, w, eps = gi["z"][:, 0].contiguous(), gi["norm_w"], 1e-6
+    row_mask = None
+    if rm:
+        row_mask = torch.ones(B, dtype=torch.uint8)
+        row_mask[1] = 0
+    args = [to_dev(inp["qkv"][:, 0].contiguous()), to_dev(inp["conv_w"])]
+    gates = [to_dev(inp["a"][:, 0].contiguous()), to_dev(inp["b"][:, 0].contiguous()), to_dev(inp["A_log"]),
+             to_dev(inp["dt_bias"])]
+    cs1, st1 = to_dev(inp["conv_state"]).clone(), to_dev(inp["state"]).clone()
+    out = gdn.recurrent_decode_gated(d, *args, cs1, *gates, st1, to_dev(z), to_dev(w), eps, to_dev(row_mask))
+    cs2, st2 = to_dev(inp["conv_state"]).clone(), to_dev(inp["state"]).clone()
+    y = gdn.recurrent_decode(d, *args, cs2, *gates, st2, to_dev(row_mask))
+    out2 = gdn.rmsnorm_gated(d, y, to_dev(z), to_dev(w), eps)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert torch.equal(st1, st2) and torch.equal(cs1, cs2), "the states are those of the plain step"
+    U.assert_bf16_within_one_ulp(U.bits(out), U.bits(out2), "fused vs decode + rmsnorm_gated")
+    sb = [{k: U.bits(inp[k]) for k in ("qkv", "a", "b")}]
+    yr, _, _ = oracle.decode(d, sb, U.bits(inp["conv_w"]), inp["A_log"].numpy(), inp["dt_bias"].numpy(),
+                             U.bits(inp["conv_state"]), inp["state"].numpy().astype(np.float64),
+                             None if row_mask is None else row_mask.numpy())
+    ref = oracle.rmsnorm_gated(oracle.f64_to_bf16(yr[0]), U.bits(z), w.numpy(), eps)
+    U.assert_out_close(U.bf16_dev_to_f64(out), oracle.bf16_to_f64(ref), "gated decode output")
+    if rm:
+        assert np.all(U.bf16_dev_to_f64(out[1]) == 0.0), "a masked row gives zeros"
+
+
+GATED_PREFILL_CASES = [
+    # chunk, B, T, Hk, Hv, Dk, Dv, mask
+    (64, 2, 200, 1, 2, 128, 128, "right"),
+    (64, 3, 130, 2, 4, 128, 128, "random"),
+    (64, 1, 64, 1, 1, 128, 128, None),
+    (64, 3, 333, 1, 2, 128, 128, "blocks"),
+    (64, 2, 70, 16, 80, 128, 128, "random"),     # B * Hv >= the SM count: the norm in the kernel's epilogue
+    (64, 1, 160, 8, 160, 128, 128, "blocks"),
+    (0, 2, 100, 2, 4, 64, 32, "random"),
+    (0, 1, 77, 1, 2, 128, 128, None),
+]
+
+
+@pytest.mark.parametrize("chunk,B,T,Hk,Hv,Dk,Dv,mk", GATED_PREFILL_CASES)
+def test_prefill_gated(gdn, chunk, B, T, Hk, Hv, Dk, Dv, mk):
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv)
+    mask = make_mask(mk, B, T, 11 + T)
+    r = recurrence_inputs(d, 1500 + T, mask)
+    gi = wl.make_gate_inputs(d, 1600 + T)
+    eps = 1e-6
+    dev = [to_dev(r[n]) for n in ("q", "k", "v", "g", "beta")]
+    z, w = to_dev(gi["z"]), to_dev(gi["norm_w"])
+    out, s1 = gdn.prefill_gated(d, *dev, z, w, eps, state_in=to_dev(r["state"]), mask=to_dev(mask), chunk=chunk)
+    y, s2 = gdn.prefill(d, *dev, state_in=to_dev(r["state"]), mask=to_dev(mask), chunk=chunk)
+    out2 = gdn.rmsnorm_gated(d, y, z, w, eps)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert torch.equal(s1, s2), "the state is that of the plain prefill"
+    U.assert_bf16_within_one_ulp(U.bits(out), U.bits(out2), "fused vs prefill + rmsnorm_gated")
+    yr, _ = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                              r["beta"].numpy().astype(np.float64), r["state"].numpy().astype(np.float64),
+                              np_mask(mask))
+    ref = oracle.rmsnorm_gated(oracle.f64_to_bf16(yr), U.bits(gi["z"]), gi["norm_w"].numpy(), eps)
+    U.assert_out_close(U.bf16_dev_to_f64(out), oracle.bf16_to_f64(ref), "gated prefill output")
+    if mask is not None:
+        assert np.all(U.bf16_dev_to_f64(out)[mask.numpy() == 0] == 0.0), "masked steps give a zero"
+
+
 def test_core_then_rmsnorm_gated_tiny(gdn):
     """The full layer core followed by the gated norm, against the oracle."""
     w = wl.WORKLOADS["tiny"]
@@ -442,7 +522,7 @@ def test_core_then_rmsnorm_gated_tiny(gdn):
                             inp["A_log"].numpy(), inp["dt_bias"].numpy(), U.bits(inp["conv_state"]),
                             inp["state"].numpy().astype(np.float64))
     ref_out = oracle.rmsnorm_gated(ref["y_bf16"], U.bits(gi["z"]), gi["norm_w"].numpy(), 1e-6)
-    U.assert_y_close(U.bf16_dev_to_f64(out), oracle.bf16_to_f64(ref_out), "gated output")
+    U.assert_out_close(U.bf16_dev_to_f64(out), oracle.bf16_to_f64(ref_out), "gated output")
 
 
 # ---------------------------------------------------------------------------
