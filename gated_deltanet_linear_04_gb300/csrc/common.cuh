@@ -136,6 +136,13 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Wait until every committed bulk store has finished reading its shared-memory
+// source (the global writes may still be in flight; they complete with the
+// grid).  Enough before a CTA exits or reuses the buffer.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy / tensor core) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 6) decode_kernel(const DecodeParams 
         uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c_v;
         for (int j = 0; j < n; ++j) cs[(size_t)j * p.C] = nw_v[j];
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_read();   // the slice has been read out of shared memory
 }
 
 template <int DK, bool NORM>

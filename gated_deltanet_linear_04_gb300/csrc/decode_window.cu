@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
         if (has_qk && rank == 0) write_conv_state<K>(p, b, c_qk, keep);
         if (has_v) write_conv_state<K>(p, b, c_v, keep);
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_read();   // the slice has been read out of shared memory
 }
 
 template <int DK, int K>
