@@ -40,6 +40,32 @@ struct ConvParams {
     float eps;
 };
 
+// Continues a backward scan for the most recent valid steps of row b: nf
+// holds `found` positions (newest first), the scan resumes below `cur`.
+// Positions older than the first valid token become conv_state codes (< 0,
+// -1 = newest stored row).  Warp-collective.
+__device__ __forceinline__ void scan_halo(const uint8_t *mask, int b, int T, int cur, int found, int lane,
+                                          int (&nf)[kMaxHalo]) {
+    while (found < kMaxHalo && cur > 0) {
+        const int base = max(cur - 32, 0);
+        const int len = cur - base;
+        const bool m = lane < len && mask[(size_t)b * T + base + lane] != 0;
+        unsigned ball = __ballot_sync(0xffffffffu, m);
+        while (ball != 0u && found < kMaxHalo) {
+            const int hi = 31 - __clz(ball);
+#pragma unroll
+            for (int r = 0; r < kMaxHalo; ++r)
+                if (r == found) nf[r] = base + hi;
+            ++found;
+            ball &= ~(1u << hi);
+        }
+        cur = base;
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxHalo; ++r)
+        if (r >= found) nf[r] = -(r - found + 1);
+}
+
 // Positions of the kMaxHalo most recent valid steps strictly before `t_end` of
 // row b, oldest first.  A code >= 0 is a token index; a code < 0 names
 // conv_state row (K-1+code) (-1 = newest stored row).  Warp-collective.
@@ -125,10 +151,18 @@ __device__ __forceinline__ void conv_segment(const ConvParams &p, int kind, int 
     const int c = c0 + lane * CPL;
     const int nt = min(kTile, p.T - t0);
 
-    unsigned valid;
+    // One mask load for the tile and the 24 steps before it: lanes 0-23 read
+    // steps t0-24 .. t0-1 (candidates for the window rows before the tile),
+    // lanes 24-31 the tile itself.
+    constexpr int kPre = 32 - kTile;
+    unsigned valid, prev = 0u;
     if (p.mask != nullptr) {
-        const bool m = lane < nt && p.mask[(size_t)b * p.T + t0 + lane] != 0;
-        valid = __ballot_sync(0xffffffffu, m);
+        const int t = t0 - kPre + lane;
+        const bool in = lane < kPre ? t >= 0 : lane - kPre < nt;
+        const bool m = in && p.mask[(size_t)b * p.T + t] != 0;
+        const unsigned ball = __ballot_sync(0xffffffffu, m);
+        valid = ball >> kPre;
+        prev = ball & ((1u << kPre) - 1u);
     } else {
         valid = nt >= 32 ? 0xffffffffu : ((1u << nt) - 1u);
     }
@@ -150,9 +184,30 @@ __device__ __forceinline__ void conv_segment(const ConvParams &p, int kind, int 
             w[i][j] = jj >= 0 ? bf16_to_f32(p.conv_w[(size_t)(c + i) * p.K + jj]) : 0.0f;
         }
 
-    // window of the K-1 valid rows before the tile (zeros for unused slots)
+    // window of the K-1 valid rows before the tile (zeros for unused slots):
+    // the newest valid steps among the 24 already seen, the rest (rarely
+    // needed) by scanning further back
     int codes[kMaxHalo];
-    find_halo(p.mask, b, p.T, t0, lane, codes);
+    if (p.mask == nullptr) {
+#pragma unroll
+        for (int j = 0; j < kMaxHalo; ++j) codes[j] = t0 - kMaxHalo + j;
+    } else {
+        int nf[kMaxHalo] = {0, 0, 0};
+        int found = 0;
+        unsigned pb = prev;
+#pragma unroll
+        for (int r = 0; r < kMaxHalo; ++r) {
+            if (pb != 0u) {
+                const int hi = 31 - __clz(pb);
+                nf[r] = t0 - kPre + hi;
+                pb &= ~(1u << hi);
+                found = r + 1;
+            }
+        }
+        if (found < kMaxHalo) scan_halo(p.mask, b, p.T, t0 - kPre, found, lane, nf);
+#pragma unroll
+        for (int j = 0; j < kMaxHalo; ++j) codes[j] = nf[kMaxHalo - 1 - j];
+    }
     float win[kMaxHalo][CPL];
 #pragma unroll
     for (int j = 0; j < kMaxHalo; ++j) {
