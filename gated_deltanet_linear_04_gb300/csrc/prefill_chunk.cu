@@ -4,7 +4,7 @@
 // forward, per-timestep loop) and of the gated_delta_step kernel of "mlx-bun
 // 0.4.0 -> 1.0.0, package/src/model/qwen3-delta.ts" is re-blocked exactly into
 // chunks of 64 steps.  For a chunk with start state S0 ([Dv, Dk]) and
-// log-decay prefix sums lg_r = sum_{i<=r} log g_i:
+// log-decay prefix sums lg_r = sum_{i<=r} log g_i (held in base 2 below):
 //   A[r,i] = beta_r exp(lg_r - lg_i) (k_r . k_i), i < r;   T = (I + A)^-1
 //   U = T diag(beta) V,   W = T diag(beta exp(lg)) K,   D = U - W S0^T
 //   Y = diag(exp(lg)) Q S0^T + (M o Q K^T) D,   M[r,i] = exp(lg_r - lg_i), i <= r
@@ -91,15 +91,27 @@ __device__ __forceinline__ int aidx(int r, int c) { return r * 64 + (c ^ ((r & 7
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
 
-// exp of a non-positive log-decay difference with the hardware base-2
-// exponential (ex2.approx: relative error ~2^-22, far below the tf32 rounding
-// these factors go through; results below 2^-126 flush to zero, which is the
-// limit the decay takes anyway).  The precise library exp2f path measured ~3x
-// slower for the 64 x 64 ratio matrices built every chunk.
+// Log-decay prefix sums are kept in base 2 (lg_r = sum_{i<=r} log2 g_i).
+// 2^x of a non-positive difference with the hardware base-2 exponential
+// (ex2.approx: relative error ~2^-22, far below the tf32 rounding these
+// factors go through; results below 2^-126 flush to zero, which is the limit
+// the decay takes anyway).  The precise library exp2f path measured ~3x slower
+// for the 64 x 64 ratio matrices built every chunk.
 __device__ __forceinline__ float decay(float x) {
     float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x * 1.4426950408889634f));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
+}
+
+// log2 of a gate value with the hardware base-2 logarithm (lg2.approx, not
+// flushing subnormal inputs), clamped at -250: a gate of exactly 0 (or one
+// that underflowed) then decays everything before it to 2^-250, which is 0
+// in f32, instead of making the prefix sums -inf and their differences NaN.
+// A gate of exactly 1 (every masked step) gives exactly 0.
+__device__ __forceinline__ float log2_gate(float g) {
+    float r;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(r) : "f"(g));
+    return g == 1.0f ? 0.0f : fmaxf(r, -250.0f);
 }
 
 // One merge level of the blocked inverse: for each pair of S x S diagonal
@@ -306,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         // ---- S1: chunk inputs, log-decay prefix sums (warp 0)
         ok = mbar_wait(&bar_tma, (uint32_t)(it & 1), p.err);
         if (warp == 0) {
-            const float la = logf(s_g[st][2 * lane]), lb = logf(s_g[st][2 * lane + 1]);
+            const float la = log2_gate(s_g[st][2 * lane]), lb = log2_gate(s_g[st][2 * lane + 1]);
             float incl = la + lb;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -319,15 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             const float last = __shfl_sync(0xffffffffu, incl, 31);
             s_lg[2 * lane] = lg0;
             s_lg[2 * lane + 1] = lg1;
-            s_gam[2 * lane] = expf(lg0);
-            s_gam[2 * lane + 1] = expf(lg1);
-            s_kc[2 * lane] = expf(last - lg0);
-            s_kc[2 * lane + 1] = expf(last - lg1);
+            const float e0 = decay(lg0), e1 = decay(lg1);
+            s_gam[2 * lane] = e0;
+            s_gam[2 * lane + 1] = e1;
+            s_kc[2 * lane] = decay(last - lg0);
+            s_kc[2 * lane + 1] = decay(last - lg1);
             const float b0 = s_b[st][2 * lane], b1 = s_b[st][2 * lane + 1];
             s_beta[2 * lane] = b0;
             s_beta[2 * lane + 1] = b1;
-            s_bg[2 * lane] = b0 * expf(lg0);
-            s_bg[2 * lane + 1] = b1 * expf(lg1);
+            s_bg[2 * lane] = b0 * e0;
+            s_bg[2 * lane + 1] = b1 * e1;
         }
         ok = __syncthreads_and(ok) != 0;
         if (!ok) break;

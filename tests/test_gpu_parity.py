@@ -282,6 +282,26 @@ def test_prefill_row_order(gdn, chunk):
     assert e.value.status == gdn.GDN_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("chunk", [0, 64])
+def test_prefill_zero_gates(gdn, chunk):
+    # a gate of exactly 0 forgets everything before it; the chunked form works
+    # with log g, so it must not turn the zero into -inf and NaN
+    d = wl.Dims(B=2, T=150, Hk=1, Hv=2, Dk=128, Dv=128)
+    r = recurrence_inputs(d, 777)
+    g = r["g"].clone()
+    g[0, [5, 64, 100], :] = 0.0
+    g[1, 130, 1] = 0.0
+    g[1, 63, 0] = 0.0
+    dev = [to_dev(r[n]) for n in ("q", "k", "v")]
+    y, s_out = gdn.prefill(d, *dev, to_dev(g), to_dev(r["beta"]), state_in=to_dev(r["state"]), chunk=chunk)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    yr, sr = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], g.numpy().astype(np.float64),
+                               r["beta"].numpy().astype(np.float64), r["state"].numpy().astype(np.float64))
+    U.assert_y_close(U.bf16_dev_to_f64(y), yr)
+    U.assert_state_close(s_out.cpu().numpy(), sr)
+
+
 def test_prefill_chunked_rejects_other_head_sizes(gdn):
     d = wl.Dims(B=1, T=8, Hk=1, Hv=2, Dk=64, Dv=128)
     r = recurrence_inputs(d, 1)
