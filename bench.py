@@ -562,7 +562,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
-    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="only the headline decode (no other sections)")
+    ap.add_argument("--parts", default="decode_b1,rmsnorm,window,decode_gated,prefill",
+                    help="comma-separated sections to run after the headline decode")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -621,11 +623,16 @@ def main():
     window = None
     decode_gated = None
     prefill = []
-    if not args.no_prefill:
+    parts = set() if args.no_prefill else set(args.parts.split(","))
+    if "decode_b1" in parts:
         small_decode = bench_decode_small(gdn, wl.WORKLOADS["decode_b1"], dev)
+    if "rmsnorm" in parts:
         gated_norm = bench_rmsnorm_gated(gdn, wl.WORKLOADS["prefill_ragged"], dev)
+    if "window" in parts:
         window = bench_decode_window(gdn, w, dev)
+    if "decode_gated" in parts:
         decode_gated = bench_decode_gated(gdn, w, dev)
+    if "prefill" in parts:
         for name in ("prefill_t8192", "prefill_ragged"):
             for chunk in (0, 64):
                 try:
