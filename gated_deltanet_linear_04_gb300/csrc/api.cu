@@ -141,6 +141,16 @@ static gdn_status prefill_impl(const gdn_dims *dims, const uint16_t *q, const ui
         if (e == cudaSuccess && z != nullptr) e = launch_rmsnorm_gated(s, y, z, norm_w, norm_eps, y, cs);
         return from_cuda(e);
     }
+    // Chunked form with few heads and a workspace of the full size: two passes
+    // (the state-independent work of every chunk spread over the GPU first)
+    const size_t ws_order = row_order_workspace(s);
+    if (prefill_two_pass_pays(s) && workspace != nullptr &&
+        ws_bytes >= ws_order + prefill_two_pass_workspace(s)) {
+        cudaError_t e = launch_prefill_two_pass(s, q, k, v, g, beta, state_in, state_out, mask, order, y,
+                                                static_cast<char *>(workspace) + ws_order, error_word(), cs);
+        if (e == cudaSuccess && z != nullptr) e = launch_rmsnorm_gated(s, y, z, norm_w, norm_eps, y, cs);
+        return from_cuda(e);
+    }
     // Chunked form: the norm in the kernel's epilogue when there are at least
     // as many heads as SMs.  With fewer, each head's chain of chunks is the
     // critical path and the epilogue lengthens every link of it, while a
@@ -261,7 +271,10 @@ size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk) {
     gdn::Sizes s;
     if (gdn::check_dims(dims, &s) != GDN_OK) return 0;
     if (chunk != 0 && chunk != 64) return 0;
-    return gdn::row_order_workspace(s);
+    size_t n = gdn::row_order_workspace(s);
+    if (chunk == 64 && s.Dk == 128 && s.Dv == 128 && s.B > 0 && s.T > 0 && gdn::prefill_two_pass_pays(s))
+        n += gdn::prefill_two_pass_workspace(s);
+    return n;
 }
 
 gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *k, const uint16_t *v,

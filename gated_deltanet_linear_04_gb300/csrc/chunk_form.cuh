@@ -1,0 +1,399 @@
+// Building blocks of the chunked (WY / UT-transform) form of the gated delta
+// rule on the 5th-generation tensor cores, shared by the single-pass kernel
+// (prefill_chunk.cu) and the two-pass kernels (prefill_chunk2.cu).
+//
+// The recurrence of "mlex 0.1.2, src/models/gated_delta.rs" (GatedDeltaNet::
+// forward, per-timestep loop) and of the gated_delta_step kernel of "mlx-bun
+// 0.4.0 -> 1.0.0, package/src/model/qwen3-delta.ts", re-blocked exactly into
+// chunks of 64 steps.  For a chunk with start state S0 ([Dv, Dk]) and base-2
+// log-decay prefix sums lg_r = sum_{i<=r} log2 g_i:
+//   A[r,i] = beta_r 2^(lg_r - lg_i) (k_r . k_i), i < r;   T = (I + A)^-1
+//   U = T diag(beta) V,   W = T diag(beta 2^lg) K,   D = U - W S0^T
+//   Y = diag(2^lg) Q S0^T + (M o Q K^T) D,   M[r,i] = 2^(lg_r - lg_i), i <= r
+//   S = 2^lg_63 S0 + D^T diag(2^(lg_63 - lg)) K
+// (a masked step enters with g = 1, beta = 0).  Every product is issued in
+// transposed form so that the MMA row count is M = 128 (= Dv or Dk) and an
+// accumulator row is one TMEM lane:
+//   [K;Q] K^T        bf16 x bf16  -> QK columns (rows 0-63 K K^T, 64-127 Q K^T)
+//   U^T = (bV)^T T^T tf32         -> D columns
+//   W^T = (bgK)^T T^T tf32        -> W columns
+//   D^T += S0 (-W)^T tf32         -> D columns (accumulates onto U^T)
+//   Y^T = S0 (gQ)^T  tf32         -> Y columns
+//   Y^T += D^T P^T   tf32         -> Y columns
+//   S  += D^T Kc^T   tf32         -> S columns (S pre-scaled by 2^lg_63)
+// The state products read S straight from TMEM as their A operand (tf32 by
+// truncation); every other f32 operand is rounded to tf32 (cvt.rna) when it
+// is written to shared memory.
+//
+// Threads: 256 (8 warps).  Warp w reaches TMEM lanes [32 (w % 4), +32): its
+// thread `row` = 32 (w % 4) + lane is one accumulator row; `half` = w / 4
+// picks which 32-column half of a 64-column accumulator it handles.
+//
+// Shared-memory tiles (offsets relative to a 1024-byte aligned base):
+//   KQ  bf16, K rows 0-63 / Q rows 64-127, two 128B-swizzled K-halves of 64
+//   V   plain [64][128] bf16
+//   GQ  (g Q) [64][128] tf32, 4 swizzled K-tiles of 8 KiB
+//   KT  Kc^T [128][64] tf32, 2 swizzled K-tiles of 16 KiB (as BV, BK, DT)
+//   NW  -W [64][128] tf32, 4 K-tiles of 8 KiB
+//   P   [64][64] tf32, 2 K-tiles of 8 KiB
+#pragma once
+
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+namespace chunkform {
+
+constexpr int kThreads = 256;
+constexpr int kC = 64;          // chunk length
+constexpr int kD = 128;         // Dk = Dv
+constexpr uint32_t kSlot = 16384;
+
+// TMEM columns
+constexpr uint32_t C_QK = 0, C_D = 64, C_W = 128, C_Y = 192, C_S = 256;
+
+// A / T working matrix, row-major; groups of 4 columns are XOR-permuted by the
+// row (r % 8) so that row-per-thread float4 stores spread over all banks while
+// each aligned group of 4 stays contiguous for float4 loads.
+__device__ __forceinline__ int aidx(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+// 2^x of a non-positive log-decay difference with the hardware base-2
+// exponential (ex2.approx: relative error ~2^-22, far below the tf32 rounding
+// these factors go through; results below 2^-126 flush to zero, which is the
+// limit the decay takes anyway).  The precise library exp2f path measured ~3x
+// slower for the 64 x 64 ratio matrices built every chunk.
+__device__ __forceinline__ float decay(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// log2 of a gate value with the hardware base-2 logarithm (lg2.approx, not
+// flushing subnormal inputs), clamped at -250: a gate of exactly 0 (or one
+// that underflowed) then decays everything before it to 2^-250, which is 0
+// in f32, instead of making the prefix sums -inf and their differences NaN.
+// A gate of exactly 1 (every masked step) gives exactly 0.
+__device__ __forceinline__ float log2_gate(float g) {
+    float r;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(r) : "f"(g));
+    return g == 1.0f ? 0.0f : fmaxf(r, -250.0f);
+}
+
+__device__ __forceinline__ void st_tf32x4(uint8_t *base, uint32_t off, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(base + off) =
+        make_float4(umma::to_tf32(a), umma::to_tf32(b), umma::to_tf32(c), umma::to_tf32(d));
+}
+
+// ---------------------------------------------------------------------------
+// per-step factors (warp 0): lg (base-2 prefix sums), gamma = 2^lg,
+// kc = 2^(lg_63 - lg), beta, beta * gamma
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void step_factors(int lane, const float *g, const float *beta, float *s_lg,
+                                             float *s_gam, float *s_kc, float *s_beta, float *s_bg) {
+    const float la = log2_gate(g[2 * lane]), lb = log2_gate(g[2 * lane + 1]);
+    float incl = la + lb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    const float up = __shfl_up_sync(0xffffffffu, incl, 1);
+    const float excl = lane == 0 ? 0.0f : up;
+    const float lg0 = excl + la, lg1 = lg0 + lb;
+    const float last = __shfl_sync(0xffffffffu, incl, 31);
+    s_lg[2 * lane] = lg0;
+    s_lg[2 * lane + 1] = lg1;
+    const float e0 = decay(lg0), e1 = decay(lg1);
+    s_gam[2 * lane] = e0;
+    s_gam[2 * lane + 1] = e1;
+    s_kc[2 * lane] = decay(last - lg0);
+    s_kc[2 * lane + 1] = decay(last - lg1);
+    const float b0 = beta[2 * lane], b1 = beta[2 * lane + 1];
+    s_beta[2 * lane] = b0;
+    s_beta[2 * lane + 1] = b1;
+    s_bg[2 * lane] = b0 * e0;
+    s_bg[2 * lane + 1] = b1 * e1;
+}
+
+// ---------------------------------------------------------------------------
+// operand builds (all threads)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float kq_elem(const uint8_t *sm, uint32_t kq_off, int row, int dk) {
+    // row 0-63: K, 64-127: Q; bf16, 128B swizzle, K-halves of 64 in two slots
+    const uint16_t *p = reinterpret_cast<const uint16_t *>(
+        sm + kq_off + (dk >> 6) * kSlot + umma::sw128((uint32_t)row, (uint32_t)(dk & 63) * 2));
+    return bf16_to_f32(*p);
+}
+
+// (g Q)[r][dk]: a warp covers one row r, 4 consecutive dk per lane
+__device__ __forceinline__ void build_gq(uint8_t *sm, uint32_t kq_off, uint32_t gq_off, const float *s_gam,
+                                         int tid) {
+    for (int i = tid; i < kC * kD / 4; i += kThreads) {
+        const int r = i >> 5, dk = (i & 31) * 4;
+        const float gm = s_gam[r];
+        const uint2 qq = *reinterpret_cast<const uint2 *>(
+            sm + kq_off + (dk >> 6) * kSlot + umma::sw128(64 + r, (dk & 63) * 2));
+        st_tf32x4(sm, gq_off + (dk >> 5) * 8192 + umma::sw128(r, (dk & 31) * 4), gm * __uint_as_float(qq.x << 16),
+                  gm * __uint_as_float(qq.x & 0xffff0000u), gm * __uint_as_float(qq.y << 16),
+                  gm * __uint_as_float(qq.y & 0xffff0000u));
+    }
+}
+
+// Kc^T[dk][r] and (b g K)^T[dk][r]: lanes take consecutive dk (conflict-free
+// reads along a K row), each thread 4 consecutive r
+__device__ __forceinline__ void build_kt_bk(uint8_t *sm, uint32_t kq_off, uint32_t kt_off, uint32_t bk_off,
+                                            const float *s_kc, const float *s_bg, int tid) {
+    for (int i = tid; i < kD * kC / 4; i += kThreads) {
+        const int dk = i & (kD - 1), r = (i >> 7) * 4;
+        const float k0 = kq_elem(sm, kq_off, r, dk), k1 = kq_elem(sm, kq_off, r + 1, dk),
+                    k2 = kq_elem(sm, kq_off, r + 2, dk), k3 = kq_elem(sm, kq_off, r + 3, dk);
+        const uint32_t off = (r >> 5) * kSlot + umma::sw128(dk, (r & 31) * 4);
+        const float4 kc = ld4(s_kc + r), bg = ld4(s_bg + r);
+        st_tf32x4(sm, kt_off + off, kc.x * k0, kc.y * k1, kc.z * k2, kc.w * k3);
+        st_tf32x4(sm, bk_off + off, bg.x * k0, bg.y * k1, bg.z * k2, bg.w * k3);
+    }
+}
+
+// (b V)^T[dv][i]
+__device__ __forceinline__ void build_bv(uint8_t *sm, uint32_t v_off, uint32_t bv_off, const float *s_beta,
+                                         int tid) {
+    const uint16_t *Vs = reinterpret_cast<const uint16_t *>(sm + v_off);
+    for (int i = tid; i < kD * kC / 4; i += kThreads) {
+        const int dv = i & (kD - 1), r = (i >> 7) * 4;
+        const float4 be = ld4(s_beta + r);
+        st_tf32x4(sm, bv_off + (r >> 5) * kSlot + umma::sw128(dv, (r & 31) * 4),
+                  be.x * bf16_to_f32(Vs[r * kD + dv]), be.y * bf16_to_f32(Vs[(r + 1) * kD + dv]),
+                  be.z * bf16_to_f32(Vs[(r + 2) * kD + dv]), be.w * bf16_to_f32(Vs[(r + 3) * kD + dv]));
+    }
+}
+
+// A from the K K^T rows (0-63) of the QK accumulator; threads of TMEM quads 0-1
+__device__ __forceinline__ void build_a(uint32_t qk_tmem, float *As, const float *s_lg, const float *s_beta,
+                                        int row, int half) {
+    float kk[32];
+    umma::tmem_ld32(qk_tmem + half * 32, kk);
+    umma::tmem_ld_wait();
+    const int r = row;   // 0..63
+    const float lr = s_lg[r], br = s_beta[r];
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        const int i = half * 32 + j;
+        const float4 li = ld4(s_lg + i);
+        float4 v;
+        v.x = i < r ? br * decay(lr - li.x) * kk[j] : 0.0f;
+        v.y = i + 1 < r ? br * decay(lr - li.y) * kk[j + 1] : 0.0f;
+        v.z = i + 2 < r ? br * decay(lr - li.z) * kk[j + 2] : 0.0f;
+        v.w = i + 3 < r ? br * decay(lr - li.w) * kk[j + 3] : 0.0f;
+        st4(As + aidx(r, i), v);
+    }
+}
+
+// P = M o Q K^T from the Q K^T row (64-127) of the QK accumulator held in
+// registers (threads of TMEM quads 2-3)
+__device__ __forceinline__ void p_tile(const float (&qk)[32], uint8_t *sm, uint32_t p_off, const float *s_lg,
+                                       int row, int half) {
+    const int r = row - 64;
+    const float lr = s_lg[r];
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        float v4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = half * 32 + j + e;
+            v4[e] = i <= r ? decay(lr - s_lg[i]) * qk[j + e] : 0.0f;
+        }
+        st_tf32x4(sm, p_off + half * 8192 + umma::sw128(r, j * 4), v4[0], v4[1], v4[2], v4[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// T = (I + A)^-1 in place, by blocked doubling (all threads; block barriers)
+// ---------------------------------------------------------------------------
+
+// One merge level: for each pair of S x S diagonal blocks (a = [q0, q0+S),
+// b = [q0+S, q0+2S)) of the unit lower triangular T, the lower-left block is
+// X = -T_bb A_ba T_aa.  Each task computes 4 adjacent columns of one row; sums
+// run over full blocks because the triangular factors hold explicit zeros
+// above the diagonal.
+template <int S>
+__device__ __forceinline__ void merge_level(float *As, float *Ys, int tid) {
+    constexpr int G4 = S / 4;
+    constexpr int NT = (32 / S) * S * G4;
+    const int pi = tid / (S * G4), rem = tid % (S * G4), r = rem / G4, c = (rem % G4) * 4, q0 = pi * 2 * S;
+    if (tid < NT) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < S; ++m) {
+            const float a = As[aidx(q0 + S + r, q0 + m)];
+            const float4 t = ld4(As + aidx(q0 + m, q0 + c));
+            acc.x = fmaf(a, t.x, acc.x);
+            acc.y = fmaf(a, t.y, acc.y);
+            acc.z = fmaf(a, t.z, acc.z);
+            acc.w = fmaf(a, t.w, acc.w);
+        }
+        st4(Ys + (pi * S + r) * S + c, acc);
+    }
+    __syncthreads();
+    if (tid < NT) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < S; ++m) {
+            const float t = As[aidx(q0 + S + r, q0 + S + m)];
+            const float4 yv = ld4(Ys + (pi * S + m) * S + c);
+            acc.x = fmaf(t, yv.x, acc.x);
+            acc.y = fmaf(t, yv.y, acc.y);
+            acc.z = fmaf(t, yv.z, acc.z);
+            acc.w = fmaf(t, yv.w, acc.w);
+        }
+        st4(As + aidx(q0 + S + r, q0 + c), make_float4(-acc.x, -acc.y, -acc.z, -acc.w));
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void invert_unit_lower(float *As, float *Ys, int tid) {
+    {
+        // 8 x 8 diagonal blocks by forward substitution: thread (block, column j)
+        const int o = (tid >> 3) * 8, j = tid & 7;
+        float t[8];
+        if (tid < 64) {
+            float a[8][8];
+#pragma unroll
+            for (int r = 1; r < 8; ++r)
+#pragma unroll
+                for (int i = 0; i < r; ++i) a[r][i] = As[aidx(o + r, o + i)];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                float acc = r == j ? 1.0f : 0.0f;
+#pragma unroll
+                for (int i = 0; i < r; ++i) acc = fmaf(-a[r][i], t[i], acc);
+                t[r] = acc;
+            }
+        }
+        __syncthreads();
+        if (tid < 64) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) As[aidx(o + r, o + j)] = t[r];
+        }
+        __syncthreads();
+    }
+    merge_level<8>(As, Ys, tid);
+    merge_level<16>(As, Ys, tid);
+    merge_level<32>(As, Ys, tid);
+}
+
+// T -> tf32 B operand [r][i] (2 K-tiles of 8 KiB)
+__device__ __forceinline__ void t_to_tf32(const float *As, uint8_t *sm, uint32_t t_off, int tid) {
+    for (int i = tid; i < kC * kC / 4; i += kThreads) {
+        const int r = i >> 4, c4 = (i & 15) * 4;
+        const float4 tv = ld4(As + aidx(r, c4));
+        st_tf32x4(sm, t_off + (c4 >> 5) * 8192 + umma::sw128(r, (c4 & 31) * 4), tv.x, tv.y, tv.z, tv.w);
+    }
+}
+
+// -W (tf32) from the W accumulator: thread `row` is dk, its half covers 32 r
+__device__ __forceinline__ void neg_w_tile(uint32_t w_tmem, uint8_t *sm, uint32_t nw_off, int row, int half) {
+    float wv[32];
+    umma::tmem_ld32(w_tmem + half * 32, wv);
+    umma::tmem_ld_wait();
+    const int dk = row;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int r = half * 32 + j;
+        *reinterpret_cast<float *>(sm + nw_off + (dk >> 5) * 8192 + umma::sw128(r, (dk & 31) * 4)) =
+            umma::to_tf32(-wv[j]);
+    }
+}
+
+// D^T (tf32 A operand) from a D accumulator row held in registers
+__device__ __forceinline__ void dt_tile(const float (&dv)[32], uint8_t *sm, uint32_t dt_off, int row, int half) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+        st_tf32x4(sm, dt_off + half * kSlot + umma::sw128(row, j * 4), dv[j], dv[j + 1], dv[j + 2], dv[j + 3]);
+}
+
+// S <- gl S in TMEM (the products that read S0 must have completed)
+__device__ __forceinline__ void decay_state(uint32_t s_tmem, float gl, int half) {
+#pragma unroll
+    for (int cpart = 0; cpart < 2; ++cpart) {
+        float sv[32];
+        const uint32_t col = half * 64 + cpart * 32;
+        umma::tmem_ld32(s_tmem + col, sv);
+        umma::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] *= gl;
+        umma::tmem_st32(s_tmem + col, sv);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// tensor-core issue (one thread; the caller commits)
+// ---------------------------------------------------------------------------
+// [K;Q] K^T (bf16, M = 128, N = 64, K = 128)
+__device__ __forceinline__ void issue_kq(uint32_t tmem, uint32_t base, uint32_t kq_off) {
+    const uint32_t id = umma::idesc(128, 64, umma::kFmtBF16);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t a = base + kq_off + (k >> 2) * kSlot + (k & 3) * 32;
+        umma::mma_bf16(tmem + C_QK, umma::desc_sw128(a), umma::desc_sw128(a), id, k > 0);
+    }
+}
+
+// U^T = (bV)^T T^T and W^T = (bgK)^T T^T (tf32, M = 128, N = 64, K = 64)
+__device__ __forceinline__ void issue_uw(uint32_t tmem, uint32_t base, uint32_t t_off, uint32_t bv_off,
+                                         uint32_t bk_off) {
+    const uint32_t id = umma::idesc(128, 64, umma::kFmtTF32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t kt = k >> 2, ko = (k & 3) * 32;
+        const uint64_t bt = umma::desc_sw128(base + t_off + kt * 8192 + ko);
+        umma::mma_tf32(tmem + C_D, umma::desc_sw128(base + bv_off + kt * kSlot + ko), bt, id, k > 0);
+        umma::mma_tf32(tmem + C_W, umma::desc_sw128(base + bk_off + kt * kSlot + ko), bt, id, k > 0);
+    }
+}
+
+// D^T += S0 (-W)^T and Y^T = S0 (gQ)^T, S0 read from TMEM (tf32, K = 128)
+__device__ __forceinline__ void issue_s0_products(uint32_t tmem, uint32_t base, uint32_t nw_off,
+                                                  uint32_t gq_off) {
+    const uint32_t id = umma::idesc(128, 64, umma::kFmtTF32);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const uint32_t kt = k >> 2, ko = (k & 3) * 32, a = tmem + C_S + 8 * k;
+        umma::mma_tf32_tmem_a(tmem + C_D, a, umma::desc_sw128(base + nw_off + kt * 8192 + ko), id, true);
+        umma::mma_tf32_tmem_a(tmem + C_Y, a, umma::desc_sw128(base + gq_off + kt * 8192 + ko), id, k > 0);
+    }
+}
+
+// Y^T += D^T P^T and S += D^T Kc^T (tf32, K = 64)
+__device__ __forceinline__ void issue_dt_products(uint32_t tmem, uint32_t base, uint32_t dt_off, uint32_t p_off,
+                                                  uint32_t kt_off) {
+    const uint32_t idy = umma::idesc(128, 64, umma::kFmtTF32);
+    const uint32_t ids = umma::idesc(128, 128, umma::kFmtTF32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t kt = k >> 2, ko = (k & 3) * 32;
+        const uint64_t a = umma::desc_sw128(base + dt_off + kt * kSlot + ko);
+        umma::mma_tf32(tmem + C_Y, a, umma::desc_sw128(base + p_off + kt * 8192 + ko), idy, true);
+        umma::mma_tf32(tmem + C_S, a, umma::desc_sw128(base + kt_off + kt * kSlot + ko), ids, true);
+    }
+}
+
+// y of the chunk from the Y accumulator into a bf16 staging tile [64 steps][128 dv]
+// (masked steps are written as zeros)
+__device__ __forceinline__ void stage_y(uint32_t y_tmem, uint8_t *sm, uint32_t yst_off, const int *s_m, int row,
+                                        int half) {
+    float yv[32];
+    umma::tmem_ld32(y_tmem + half * 32, yv);
+    umma::tmem_ld_wait();
+    uint16_t *Yst = reinterpret_cast<uint16_t *>(sm + yst_off);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int r = half * 32 + j;
+        Yst[r * kD + row] = s_m[r] ? f32_to_bf16(yv[j]) : (uint16_t)0;
+    }
+}
+
+}  // namespace chunkform
+}  // namespace gdn

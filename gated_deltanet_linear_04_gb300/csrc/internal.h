@@ -63,4 +63,15 @@ cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint
                                    const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
                                    const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st);
 
+// Two-pass chunked form (prefill_chunk2.cu) for batches with fewer heads than
+// SMs: bytes of its workspace blobs, whether it is the faster form for these
+// sizes, and the launch (blobs: 16-byte aligned, prefill_two_pass_workspace
+// bytes).
+size_t prefill_two_pass_workspace(const Sizes &s);
+bool prefill_two_pass_pays(const Sizes &s);
+cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                    const float *g, const float *beta, const float *state_in, float *state_out,
+                                    const uint8_t *mask, const int *order, uint16_t *y, void *blobs,
+                                    unsigned *err, cudaStream_t st);
+
 }  // namespace gdn

@@ -1,0 +1,469 @@
+// Chunked (WY / UT-transform) prefill in two passes, for batches with fewer
+// heads than the GPU has SMs.
+//
+// In the single-pass kernel one CTA walks all chunks of its head in order, so
+// with few heads (one sequence of 32 heads on 152 SMs) most SMs idle and the
+// serial chain of chunks sets the time.  Most of a chunk's work does not
+// depend on the state: the step factors, the operand builds, A, the inverse
+// T = (I + A)^-1, U^T, W^T and P (the products of chunk_form.cuh that do not
+// read S0).  Pass 1 does that work for every (b, hv, chunk) at once, one CTA
+// each, and writes the results to the workspace as images of the shared-memory
+// tiles the products read.  Pass 2 keeps one CTA per head walking the chunks
+// in order, but per chunk it only bulk-copies the images back and runs the
+// state products (D^T += S0 (-W)^T with U^T as the accumulator's start,
+// Y^T = S0 (gQ)^T, then Y^T += D^T P^T and S += D^T Kc^T) and the output.
+// Both passes run the single-pass kernel's arithmetic on the same operand
+// bits, so y and the state are bit-identical to it.
+//
+// Workspace blob per (b, hv, chunk), laid out like pass 2's shared memory so
+// that one 1-D bulk copy brings in each group:
+//   group A  [GQ 32 KiB][-W 32 KiB][U^T 32 KiB][meta 1 KiB: 2^lg_63]
+//   group B  [Kc^T 32 KiB][P 16 KiB]
+// U^T is plain f32 [128 dv][64 steps] with each row's 16-byte groups permuted
+// (group j stored at j ^ (dv % 16)) so that a warp's row-per-thread accesses
+// spread over the banks.  Wholly masked chunks are skipped by both passes.
+#include "chunk_form.cuh"
+#include "common.cuh"
+#include "internal.h"
+#include "mask_scan.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace chunkform;
+
+// blob layout
+constexpr uint32_t B_GQ = 0, B_NW = 32768, B_UT = 65536, B_META = 98304;
+constexpr uint32_t kGroupA = 98304 + 1024;
+constexpr uint32_t B_KT = kGroupA, B_P = kGroupA + 32768;
+constexpr uint32_t kGroupB = 32768 + 16384;
+constexpr size_t kBlobBytes = (size_t)kGroupA + kGroupB;
+
+// pass 1 shared memory: the single-pass slot map (13 slots of 16 KiB); after
+// the products that read them, K/Q/V and (bV)^T hold P, U^T and -W
+constexpr uint32_t P1_KQ = 0 * kSlot, P1_V = 2 * kSlot, P1_GQ = 3 * kSlot, P1_KT = 5 * kSlot,
+                   P1_BV = 7 * kSlot, P1_BK = 9 * kSlot, P1_A = 11 * kSlot, P1_T = 12 * kSlot;
+constexpr uint32_t P1_P = P1_KQ;          // slot 0, after [K;Q] K^T and the builds
+constexpr uint32_t P1_UT = 1 * kSlot;     // slots 1-2, after the U/W products
+constexpr uint32_t P1_NW = P1_BV;         // slots 7-8, after the U product
+constexpr uint32_t kP1Smem = 13 * kSlot + 1024;
+
+// pass 2 shared memory: group A and group B images, then D^T and y staging
+constexpr uint32_t P2_GQ = B_GQ, P2_NW = B_NW, P2_UT = B_UT, P2_META = B_META;
+constexpr uint32_t P2_KT = kGroupA, P2_P = kGroupA + 32768;
+constexpr uint32_t P2_DT = kGroupA + kGroupB;            // 32 KiB
+constexpr uint32_t P2_YST = P2_DT + 32768;               // 16 KiB
+constexpr uint32_t kP2Smem = P2_YST + 16384 + 1024;
+
+struct TwoPassParams {
+    const float *g, *beta, *state_in;
+    float *state_out;
+    const uint8_t *mask;
+    const int *order;   // row slot -> batch row (optional, with a mask)
+    uint16_t *y;
+    uint8_t *blobs;
+    unsigned *err;
+    int B, T, Hk, Hv, nchunks;
+};
+
+__device__ __forceinline__ uint8_t *blob_at(const TwoPassParams &p, int b, int hv, int c) {
+    return p.blobs + (((size_t)b * p.Hv + hv) * p.nchunks + c) * kBlobBytes;
+}
+
+// U^T row of thread `row`, 16-byte group j, in the permuted plain layout
+__device__ __forceinline__ uint32_t ut_off(int row, int j) { return (uint32_t)(row * 256 + ((j ^ (row & 15)) * 16)); }
+
+// ---------------------------------------------------------------------------
+// pass 1: the state-independent part of one chunk
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                  const __grid_constant__ CUtensorMap tm_q,
+                                                                  const __grid_constant__ CUtensorMap tm_v,
+                                                                  const TwoPassParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float s_g[kC], s_b[kC];
+    __shared__ __align__(16) float s_lg[kC];
+    __shared__ __align__(16) float s_gam[kC];
+    __shared__ __align__(16) float s_beta[kC];
+    __shared__ __align__(16) float s_bg[kC];
+    __shared__ __align__(16) float s_kc[kC];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2, row = quad * 32 + lane;
+    const int c = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+    const int hk = hv / (p.Hv / p.Hk);
+    const int T = p.T, t0 = c * kC;
+
+    // the chunk's gates; a wholly masked chunk is skipped here and in pass 2
+    float gg = 1.0f, bb = 0.0f;
+    int m = 0;
+    if (tid < kC && t0 + tid < T) {
+        const size_t gi = ((size_t)b * T + t0 + tid) * p.Hv + hv;
+        m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t0 + tid] != 0);
+        if (m) {
+            gg = p.g[gi];
+            bb = p.beta[gi];
+        }
+    }
+    if (!__syncthreads_or(m)) return;
+    if (tid < kC) {
+        s_g[tid] = gg;
+        s_b[tid] = bb;
+    }
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - smem_u32(smem_raw));
+    float *As = reinterpret_cast<float *>(sm + P1_A);
+    float *Ys = reinterpret_cast<float *>(sm + P1_T);
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        mbar_expect_tx(&bar_tma, 4 * 8192 + 16384);
+        const int rowg = b * T + t0;
+        tma_load_2d(sm + P1_KQ, &tm_k, hk * kD, rowg, &bar_tma);
+        tma_load_2d(sm + P1_KQ + kSlot, &tm_k, hk * kD + 64, rowg, &bar_tma);
+        tma_load_2d(sm + P1_KQ + 8192, &tm_q, hk * kD, rowg, &bar_tma);
+        tma_load_2d(sm + P1_KQ + kSlot + 8192, &tm_q, hk * kD + 64, rowg, &bar_tma);
+        tma_load_2d(sm + P1_V, &tm_v, hv * kD, rowg, &bar_tma);
+    }
+    if (warp == 0) {
+        umma::tmem_alloc(&tmem_slot, 256);   // QK, D (U^T), W columns
+        umma::tmem_relinquish();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
+
+    uint32_t mma_phase = 0;
+    auto wait_mma = [&]() {
+        bool w = mbar_wait(&bar_mma, mma_phase & 1u, p.err);
+        ++mma_phase;
+        w = __syncthreads_and(w) != 0;
+        umma::fence_after_sync();
+        return w;
+    };
+    auto publish = [&]() {
+        fence_proxy_async_smem();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+    };
+
+    bool ok = mbar_wait(&bar_tma, 0, p.err);
+    if (warp == 0) step_factors(lane, s_g, s_b, s_lg, s_gam, s_kc, s_beta, s_bg);
+    ok = __syncthreads_and(ok) != 0;
+    if (ok) {
+        if (tid == 0) {
+            umma::fence_after_sync();
+            issue_kq(tmem, base, P1_KQ);
+            umma::mma_commit(&bar_mma);
+        }
+        build_gq(sm, P1_KQ, P1_GQ, s_gam, tid);
+        build_kt_bk(sm, P1_KQ, P1_KT, P1_BK, s_kc, s_bg, tid);
+        build_bv(sm, P1_V, P1_BV, s_beta, tid);
+        ok = wait_mma();
+    }
+    if (ok) {
+        // A from K K^T (quads 0-1); P from Q K^T (quads 2-3) into the dead K/Q slot
+        if (quad < 2) {
+            build_a(lane_tmem + C_QK, As, s_lg, s_beta, row, half);
+        } else {
+            float qk[32];
+            umma::tmem_ld32(lane_tmem + C_QK + half * 32, qk);
+            umma::tmem_ld_wait();
+            p_tile(qk, sm, P1_P, s_lg, row, half);
+        }
+        __syncthreads();
+        invert_unit_lower(As, Ys, tid);
+        t_to_tf32(As, sm, P1_T, tid);
+        publish();
+        if (tid == 0) {
+            issue_uw(tmem, base, P1_T, P1_BV, P1_BK);
+            umma::mma_commit(&bar_mma);
+        }
+        ok = wait_mma();
+    }
+    if (ok) {
+        neg_w_tile(lane_tmem + C_W, sm, P1_NW, row, half);
+        float uv[32];
+        umma::tmem_ld32(lane_tmem + C_D + half * 32, uv);
+        umma::tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            *reinterpret_cast<float4 *>(sm + P1_UT + ut_off(row, half * 8 + jj)) =
+                make_float4(uv[4 * jj], uv[4 * jj + 1], uv[4 * jj + 2], uv[4 * jj + 3]);
+        fence_proxy_async_smem();
+        umma::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            uint8_t *blob = blob_at(p, b, hv, c);
+            *reinterpret_cast<float *>(blob + B_META) = s_gam[kC - 1];
+            bulk_store(blob + B_GQ, sm + P1_GQ, 32768);
+            bulk_store(blob + B_NW, sm + P1_NW, 32768);
+            bulk_store(blob + B_UT, sm + P1_UT, 32768);
+            bulk_store(blob + B_KT, sm + P1_KT, 32768);
+            bulk_store(blob + B_P, sm + P1_P, 16384);
+            bulk_commit();
+            bulk_wait_read();
+        }
+    } else if (tid == 0) {
+        // a wait gave up: give in-flight MMAs a bounded chance to drain
+        mbar_wait(&bar_mma, mma_phase & 1u, nullptr);
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// pass 2: the chunk chain of one head, state products only
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_a, bar_b, bar_mma;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_m[2][kC];
+    __shared__ uint32_t scan_bits[ChunkScan<kThreads>::kWords];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2, row = quad * 32 + lane;
+    (void)lane;
+    const int hv = blockIdx.x;
+    const int b = p.order != nullptr ? p.order[blockIdx.y] : (int)blockIdx.y;
+    const int T = p.T;
+    const int nchunks = p.nchunks;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (base - smem_u32(smem_raw));
+
+    if (tid == 0) {
+        mbar_init(&bar_a, 1);
+        mbar_init(&bar_b, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        umma::tmem_alloc(&tmem_slot, 512);
+        umma::tmem_relinquish();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
+
+    // initial state -> TMEM S (row = dv, columns = dk); half 0: dk 0-63, half 1: 64-127
+    {
+        const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            float r[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.state_in != nullptr) x = *reinterpret_cast<const float4 *>(p.state_in + off + cc * 32 + j);
+                r[j] = x.x; r[j + 1] = x.y; r[j + 2] = x.z; r[j + 3] = x.w;
+            }
+            umma::tmem_st32(lane_tmem + C_S + half * 64 + cc * 32, r);
+        }
+        umma::tmem_st_wait();
+    }
+
+    int pf_m = 0;
+    auto gather_mask = [&](int c) {
+        const int t = c * kC + tid;
+        pf_m = (tid < kC && t < T) ? (p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0)) : 0;
+    };
+    // thread 0 only: outstanding copies, for the drain after a failed wait
+    bool a_pending = false, b_pending = false;
+    uint32_t a_parity = 0, b_parity = 0;
+    auto load_a = [&](int c, int it) {
+        if (tid == 0) {
+            mbar_expect_tx(&bar_a, kGroupA);
+            bulk_load(sm + P2_GQ, blob_at(p, b, hv, c), kGroupA, &bar_a);
+            a_pending = true;
+            a_parity = (uint32_t)(it & 1);
+        }
+    };
+    auto load_b = [&](int c, int it) {
+        if (tid == 0) {
+            mbar_expect_tx(&bar_b, kGroupB);
+            bulk_load(sm + P2_KT, blob_at(p, b, hv, c) + kGroupA, kGroupB, &bar_b);
+            b_pending = true;
+            b_parity = (uint32_t)(it & 1);
+        }
+    };
+
+    uint32_t mma_phase = 0;
+    bool ok = true;
+    auto wait_mma = [&]() {
+        bool w = mbar_wait(&bar_mma, mma_phase & 1u, p.err);
+        ++mma_phase;
+        w = __syncthreads_and(w) != 0;
+        umma::fence_after_sync();
+        return w;
+    };
+    auto publish = [&]() {
+        fence_proxy_async_smem();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+    };
+
+    ChunkScan<kThreads> scan(p.mask == nullptr ? nullptr : p.mask + (size_t)b * T, T, scan_bits);
+    uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * kD + (size_t)hv * kD;
+    const size_t y_stride = (size_t)p.Hv * kD;
+    int c = scan.next_active(0);
+    zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), kD);
+    if (c < nchunks) {
+        load_a(c, 0);
+        load_b(c, 0);
+        gather_mask(c);
+        if (tid < kC) s_m[0][tid] = pf_m;
+    }
+    __syncthreads();
+
+    for (int it = 0; c < nchunks && ok; ++it) {
+        const int st = it & 1;
+        const int t0 = c * kC;
+        ok = __syncthreads_and(mbar_wait(&bar_a, (uint32_t)(it & 1), p.err)) != 0;
+        if (tid == 0) a_pending = false;
+        if (!ok) break;
+        const int cn = scan.next_active(c + 1);
+        if (cn < nchunks) gather_mask(cn);
+
+        // U^T -> the D accumulator, which the S0 (-W)^T product then adds to
+        {
+            float r[32];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const float4 v = *reinterpret_cast<const float4 *>(sm + P2_UT + ut_off(row, half * 8 + jj));
+                r[4 * jj] = v.x; r[4 * jj + 1] = v.y; r[4 * jj + 2] = v.z; r[4 * jj + 3] = v.w;
+            }
+            umma::tmem_st32(lane_tmem + C_D + half * 32, r);
+            umma::tmem_st_wait();
+        }
+        const float gl = *reinterpret_cast<const float *>(sm + P2_META);
+        publish();
+        if (tid == 0) {
+            issue_s0_products(tmem, base, P2_NW, P2_GQ);
+            umma::mma_commit(&bar_mma);
+        }
+        if (!wait_mma()) { ok = false; break; }
+        // group A has been consumed: fetch the next chunk's
+        if (cn < nchunks) load_a(cn, it + 1);
+
+        decay_state(lane_tmem + C_S, gl, half);
+        {
+            float dv[32];
+            umma::tmem_ld32(lane_tmem + C_D + half * 32, dv);
+            umma::tmem_ld_wait();
+            dt_tile(dv, sm, P2_DT, row, half);
+        }
+        publish();
+        ok = __syncthreads_and(mbar_wait(&bar_b, (uint32_t)(it & 1), p.err)) != 0;
+        if (tid == 0) b_pending = false;
+        if (!ok) break;
+        if (tid == 0) {
+            umma::fence_after_sync();
+            issue_dt_products(tmem, base, P2_DT, P2_P, P2_KT);
+            umma::mma_commit(&bar_mma);
+        }
+        if (!wait_mma()) { ok = false; break; }
+        if (cn < nchunks) load_b(cn, it + 1);
+
+        stage_y(lane_tmem + C_Y, sm, P2_YST, s_m[st], row, half);
+        umma::fence_before_sync();
+        __syncthreads();
+        {
+            const int nv = min(kC, T - t0);
+            for (int i = tid; i < nv * (kD / 8); i += kThreads) {
+                const int r = i / (kD / 8), c8 = (i % (kD / 8)) * 8;
+                *reinterpret_cast<uint4 *>(p.y + (((size_t)b * T + t0 + r) * p.Hv + hv) * kD + c8) =
+                    *reinterpret_cast<const uint4 *>(sm + P2_YST + (r * kD + c8) * 2);
+            }
+        }
+        if (tid < kC) s_m[st ^ 1][tid] = pf_m;
+        zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), kD);
+        c = cn;
+    }
+
+    if (__syncthreads_and(ok)) {
+        const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
+#pragma unroll
+        for (int cpart = 0; cpart < 2; ++cpart) {
+            float sv[32];
+            umma::tmem_ld32(lane_tmem + C_S + half * 64 + cpart * 32, sv);
+            umma::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(p.state_out + off + cpart * 32 + j) =
+                    make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+        }
+    } else if (tid == 0) {
+        // a wait gave up: give in-flight MMAs and copies a bounded chance to drain
+        mbar_wait(&bar_mma, mma_phase & 1u, nullptr);
+        if (a_pending) mbar_wait(&bar_a, a_parity, nullptr);
+        if (b_pending) mbar_wait(&bar_b, b_parity, nullptr);
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(tmem, 512);
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, uint32_t bytes, bool &done) {
+    if (!done) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        done = true;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t prefill_two_pass_workspace(const Sizes &s) {
+    const size_t nchunks = ((size_t)s.T + kC - 1) / kC;
+    return (size_t)s.B * s.Hv * nchunks * kBlobBytes;
+}
+
+bool prefill_two_pass_pays(const Sizes &s) { return (long)s.B * s.Hv < num_sms(); }
+
+cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                    const float *g, const float *beta, const float *state_in, float *state_out,
+                                    const uint8_t *mask, const int *order, uint16_t *y, void *blobs,
+                                    unsigned *err, cudaStream_t st) {
+    if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
+    CUtensorMap tk, tq, tv;
+    const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
+    if (!encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    static bool set1 = false, set2 = false;
+    cudaError_t e = set_smem(chunk_prep_kernel, kP1Smem, set1);
+    if (e != cudaSuccess) return e;
+    e = set_smem(chunk_state_kernel, kP2Smem, set2);
+    if (e != cudaSuccess) return e;
+    const int nchunks = (s.T + kC - 1) / kC;
+    TwoPassParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y,
+                    static_cast<uint8_t *>(blobs), err, s.B, s.T, s.Hk, s.Hv, nchunks};
+    chunk_prep_kernel<<<dim3(nchunks, s.Hv, s.B), kThreads, kP1Smem, st>>>(tk, tq, tv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    chunk_state_kernel<<<dim3(s.Hv, s.B), kThreads, kP2Smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -257,15 +257,16 @@ def decode_window(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, ke
 
 
 def prefill(dims, q, k, v, g, beta, state_in=None, mask=None, chunk=0, state_out=None, stream=None,
-            order_rows=True):
-    """Returns (y, state_out).  With a mask and order_rows, a workspace is
-    passed so that rows are scheduled longest first (same results)."""
+            use_workspace=True):
+    """Returns (y, state_out).  With use_workspace, the workspace the sizes ask
+    for is passed (row order for masked batches; the two-pass chunked form
+    for few heads); the results are the same either way."""
     dev = q.device
     y = torch.empty((dims.B, dims.T, dims.Hv, dims.Dv), dtype=BF16, device=dev)
     if state_out is None:
         state_out = torch.empty((dims.B, dims.Hv, dims.Dv, dims.Dk), dtype=F32, device=dev)
     ws = None
-    if mask is not None and order_rows:
+    if use_workspace:
         nws = gdn_prefill_workspace_size(dims, chunk)
         ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
     gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk, ws, stream)
@@ -288,10 +289,8 @@ def prefill_gated(dims, q, k, v, g, beta, z, norm_w, norm_eps=1e-6, state_in=Non
     out = torch.empty((dims.B, dims.T, dims.Hv, dims.Dv), dtype=BF16, device=dev)
     if state_out is None:
         state_out = torch.empty((dims.B, dims.Hv, dims.Dv, dims.Dk), dtype=F32, device=dev)
-    ws = None
-    if mask is not None:
-        nws = gdn_prefill_workspace_size(dims, chunk)
-        ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
+    nws = gdn_prefill_workspace_size(dims, chunk)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
     gdn_prefill_gated(dims, q, k, v, g, beta, state_in, state_out, mask, z, norm_w, norm_eps, out, chunk, ws, stream)
     return out, state_out
 

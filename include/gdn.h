@@ -174,8 +174,15 @@ GDN_API gdn_status gdn_decode_window(const gdn_dims *dims, const uint16_t *qkv, 
  *              writes there the order in which rows are handed to the kernel's
  *              CTAs (most chunks holding a valid step first), so that the
  *              longest rows of a ragged batch do not start last; with NULL the
- *              rows go in index order.  The results are the same either way.
- *              A workspace that is too small or misaligned gives
+ *              rows go in index order.  With chunk = 64 and fewer heads
+ *              (B * Hv) than the GPU has SMs, the size also covers the
+ *              two-pass chunked form (about 145 KiB per head and chunk of 64
+ *              steps): the state-independent work of all chunks first runs
+ *              over the whole GPU and is kept there, then one pass per head
+ *              applies it to the state.  The results are the same, bit for
+ *              bit, whichever way the call runs.  A workspace smaller than
+ *              the two-pass size but at least the row-order size runs the
+ *              single pass; a smaller or misaligned one gives
  *              GDN_ERR_INVALID_ARG.  It must not be in use by another call
  *              still running on another stream.
  * Wholly masked 64-step chunks cost only their zero y stores.

@@ -261,7 +261,7 @@ def test_prefill_row_order(gdn, chunk):
     r = recurrence_inputs(d, 77, mask)
     dev = [to_dev(r[n]) for n in ("q", "k", "v", "g", "beta")]
     s_in, m_dev = to_dev(r["state"]), to_dev(mask)
-    y1, s1 = gdn.prefill(d, *dev, state_in=s_in, mask=m_dev, chunk=chunk, order_rows=False)
+    y1, s1 = gdn.prefill(d, *dev, state_in=s_in, mask=m_dev, chunk=chunk, use_workspace=False)
     nws = gdn.gdn_prefill_workspace_size(d, chunk)
     ws = torch.full((nws,), 0xFF, dtype=torch.uint8, device=DEV)
     y2, s2 = torch.empty_like(y1), torch.empty_like(s1)
@@ -276,9 +276,10 @@ def test_prefill_row_order(gdn, chunk):
                                np_mask(mask))
     U.assert_y_close(U.bf16_dev_to_f64(y2), yr)
     U.assert_state_close(s2.cpu().numpy(), sr)
-    # a workspace below the size asked for is refused before any launch
+    # a workspace below the row-order size is refused before any launch
+    n_order = gdn.gdn_prefill_workspace_size(d, 0)
     with pytest.raises(gdn.GdnError) as e:
-        gdn.gdn_prefill(d, *dev, s_in, s2, m_dev, y2, chunk, ws[:nws - 16])
+        gdn.gdn_prefill(d, *dev, s_in, s2, m_dev, y2, chunk, ws[:n_order - 16])
     assert e.value.status == gdn.GDN_ERR_INVALID_ARG
 
 
@@ -300,6 +301,44 @@ def test_prefill_zero_gates(gdn, chunk):
                                r["beta"].numpy().astype(np.float64), r["state"].numpy().astype(np.float64))
     U.assert_y_close(U.bf16_dev_to_f64(y), yr)
     U.assert_state_close(s_out.cpu().numpy(), sr)
+
+
+TWO_PASS_CASES = [
+    # B, T, Hk, Hv, mask, state   (B * Hv below the SM count: the two-pass form)
+    (1, 200, 1, 2, None, "normal"),
+    (1, 64, 1, 1, None, "zeros"),
+    (2, 333, 1, 3, "random", "normal"),
+    (3, 700, 2, 4, "blocks", "normal"),
+    (2, 257, 2, 4, "right", "zeros"),
+    (2, 150, 1, 2, "allmasked_row", "normal"),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,mk,st", TWO_PASS_CASES)
+def test_prefill_two_pass_equals_single_pass(gdn, B, T, Hk, Hv, mk, st):
+    # the two-pass chunked form runs the single pass's arithmetic on the same
+    # operand bits: bit-identical y and state (and so the oracle's tolerance)
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=128, Dv=128)
+    mask = make_mask(mk, B, T, 21 + T)
+    r = recurrence_inputs(d, 2100 + T, mask)
+    dev = [to_dev(r[n]) for n in ("q", "k", "v", "g", "beta")]
+    s_in = to_dev(r["state"]) if st == "normal" else None
+    n_full, n_order = gdn.gdn_prefill_workspace_size(d, 64), gdn.gdn_prefill_workspace_size(d, 0)
+    assert n_full > n_order, "these sizes should ask for the two-pass workspace"
+    y1, s1 = gdn.prefill(d, *dev, state_in=s_in, mask=to_dev(mask), chunk=64, use_workspace=False)
+    ws = torch.full((n_full,), 0xAB, dtype=torch.uint8, device=DEV)
+    y2 = torch.empty_like(y1)
+    s2 = torch.empty_like(s1)
+    gdn.gdn_prefill(d, *dev, s_in, s2, to_dev(mask), y2, 64, ws)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert torch.equal(y1, y2), "two-pass y differs from the single pass"
+    assert torch.equal(s1, s2), "two-pass state differs from the single pass"
+    s0 = None if s_in is None else r["state"].numpy().astype(np.float64)
+    yr, sr = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                               r["beta"].numpy().astype(np.float64), s0, np_mask(mask))
+    U.assert_y_close(U.bf16_dev_to_f64(y2), yr)
+    U.assert_state_close(s2.cpu().numpy(), sr)
 
 
 def test_prefill_chunked_rejects_other_head_sizes(gdn):
