@@ -6,14 +6,25 @@
 // serial chain of chunks sets the time.  Most of a chunk's work does not
 // depend on the state: the step factors, the operand builds, A, the inverse
 // T = (I + A)^-1, U^T, W^T and P (the products of chunk_form.cuh that do not
-// read S0).  Pass 1 does that work for every (b, hv, chunk) at once, one CTA
-// each, and writes the results to the workspace as images of the shared-memory
-// tiles the products read.  Pass 2 keeps one CTA per head walking the chunks
-// in order, but per chunk it only bulk-copies the images back and runs the
-// state products (D^T += S0 (-W)^T with U^T as the accumulator's start,
+// read S0).  Pass 1 ("prep") does that work for every (b, hv, chunk) and
+// writes the results to the workspace as images of the shared-memory tiles
+// the products read.  Pass 2 ("state") keeps one CTA per head walking the
+// chunks in order, but per chunk it only bulk-copies the images back and runs
+// the state products (D^T += S0 (-W)^T with U^T as the accumulator's start,
 // Y^T = S0 (gQ)^T, then Y^T += D^T P^T and S += D^T Kc^T) and the output.
 // Both passes run the single-pass kernel's arithmetic on the same operand
 // bits, so y and the state are bit-identical to it.
+//
+// Two launch forms:
+//   * separate: the prep kernel (one CTA per chunk, whole GPU), then the state
+//     kernel (one CTA per head);
+//   * overlapped, when the heads take at most a quarter of the SMs: one
+//     cooperative launch of one CTA per SM (all resident at once) in which the
+//     first B*Hv CTAs run the state chains while the others produce the chunk
+//     images in chunk order; each image is published with a ready flag
+//     (bulk stores complete, proxy fence, release store) that the state CTA
+//     acquires before its bulk load.  Every wait is bounded and sets the
+//     device error word if it gives up.
 //
 // Workspace blob per (b, hv, chunk), laid out like pass 2's shared memory so
 // that one 1-D bulk copy brings in each group:
@@ -21,7 +32,8 @@
 //   group B  [Kc^T 32 KiB][P 16 KiB]
 // U^T is plain f32 [128 dv][64 steps] with each row's 16-byte groups permuted
 // (group j stored at j ^ (dv % 16)) so that a warp's row-per-thread accesses
-// spread over the banks.  Wholly masked chunks are skipped by both passes.
+// spread over the banks.  After the blobs come the ready flags (one int per
+// blob).  Wholly masked chunks are skipped by both passes.
 #include "chunk_form.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -55,6 +67,7 @@ constexpr uint32_t P2_KT = kGroupA, P2_P = kGroupA + 32768;
 constexpr uint32_t P2_DT = kGroupA + kGroupB;            // 32 KiB
 constexpr uint32_t P2_YST = P2_DT + 32768;               // 16 KiB
 constexpr uint32_t kP2Smem = P2_YST + 16384 + 1024;
+constexpr uint32_t kFusedSmem = kP1Smem > kP2Smem ? kP1Smem : kP2Smem;
 
 struct TwoPassParams {
     const float *g, *beta, *state_in;
@@ -63,39 +76,72 @@ struct TwoPassParams {
     const int *order;   // row slot -> batch row (optional, with a mask)
     uint16_t *y;
     uint8_t *blobs;
+    int *ready;         // overlapped form: one flag per blob (zeroed before launch); else null
     unsigned *err;
     int B, T, Hk, Hv, nchunks;
 };
 
-__device__ __forceinline__ uint8_t *blob_at(const TwoPassParams &p, int b, int hv, int c) {
-    return p.blobs + (((size_t)b * p.Hv + hv) * p.nchunks + c) * kBlobBytes;
+// Static shared memory of both roles.
+struct TwoPassShared {
+    uint64_t bar0, bar1, bar2;   // prep: TMA, MMA.  state: group A, group B, MMA
+    uint32_t tmem_slot;
+    float s_g[kC], s_b[kC];
+    __align__(16) float s_lg[kC];
+    __align__(16) float s_gam[kC];
+    __align__(16) float s_beta[kC];
+    __align__(16) float s_bg[kC];
+    __align__(16) float s_kc[kC];
+    int s_m[2][kC];
+    uint32_t scan_bits[ChunkScan<kThreads>::kWords];
+};
+
+__device__ __forceinline__ size_t blob_index(const TwoPassParams &p, int b, int hv, int c) {
+    return ((size_t)b * p.Hv + hv) * p.nchunks + c;
 }
 
 // U^T row of thread `row`, 16-byte group j, in the permuted plain layout
 __device__ __forceinline__ uint32_t ut_off(int row, int j) { return (uint32_t)(row * 256 + ((j ^ (row & 15)) * 16)); }
 
-// ---------------------------------------------------------------------------
-// pass 1: the state-independent part of one chunk
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                                  const __grid_constant__ CUtensorMap tm_q,
-                                                                  const __grid_constant__ CUtensorMap tm_v,
-                                                                  const TwoPassParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
-    __shared__ uint32_t tmem_slot;
-    __shared__ float s_g[kC], s_b[kC];
-    __shared__ __align__(16) float s_lg[kC];
-    __shared__ __align__(16) float s_gam[kC];
-    __shared__ __align__(16) float s_beta[kC];
-    __shared__ __align__(16) float s_bg[kC];
-    __shared__ __align__(16) float s_kc[kC];
+// Publish a blob whose bulk stores this thread has seen complete: order the
+// async-proxy writes before a release store of the flag.
+__device__ __forceinline__ void publish_ready(int *flag) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
 
+// Bounded wait (acquire) for a blob's flag, then order it before the
+// async-proxy bulk load that reads the blob.
+__device__ __forceinline__ bool wait_ready(const int *flag, unsigned *err) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v != 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        __nanosleep(64);
+    }
+    if (err) atomicOr(err, kErrMbarTimeout);
+    return false;
+}
+
+// ---------------------------------------------------------------------------
+// pass 1: the state-independent part of chunk c of head (b, hv).  The caller
+// has initialised sh.bar0 / sh.bar1 and allocated >= 256 TMEM columns; the
+// phases count completions of those barriers across calls.  Returns false if
+// a wait gave up.  Ends with a block barrier, shared memory free again.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensorMap *tm_k, const CUtensorMap *tm_q,
+                                          const CUtensorMap *tm_v, TwoPassShared &sh, uint8_t *sm, uint32_t base,
+                                          uint32_t tmem, int c, int b, int hv, uint32_t &tma_phase,
+                                          uint32_t &mma_phase) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2, row = quad * 32 + lane;
-    const int c = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
     const int T = p.T, t0 = c * kC;
+    const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
+    float *As = reinterpret_cast<float *>(sm + P1_A);
+    float *Ys = reinterpret_cast<float *>(sm + P1_T);
 
     // the chunk's gates; a wholly masked chunk is skipped here and in pass 2
     float gg = 1.0f, bb = 0.0f;
@@ -108,42 +154,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
             bb = p.beta[gi];
         }
     }
-    if (!__syncthreads_or(m)) return;
+    if (!__syncthreads_or(m)) return true;
     if (tid < kC) {
-        s_g[tid] = gg;
-        s_b[tid] = bb;
+        sh.s_g[tid] = gg;
+        sh.s_b[tid] = bb;
     }
-
-    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    uint8_t *sm = smem_raw + (base - smem_u32(smem_raw));
-    float *As = reinterpret_cast<float *>(sm + P1_A);
-    float *Ys = reinterpret_cast<float *>(sm + P1_T);
-
     if (tid == 0) {
-        mbar_init(&bar_tma, 1);
-        mbar_init(&bar_mma, 1);
-        fence_mbar_init();
-        mbar_expect_tx(&bar_tma, 4 * 8192 + 16384);
+        mbar_expect_tx(&sh.bar0, 4 * 8192 + 16384);
         const int rowg = b * T + t0;
-        tma_load_2d(sm + P1_KQ, &tm_k, hk * kD, rowg, &bar_tma);
-        tma_load_2d(sm + P1_KQ + kSlot, &tm_k, hk * kD + 64, rowg, &bar_tma);
-        tma_load_2d(sm + P1_KQ + 8192, &tm_q, hk * kD, rowg, &bar_tma);
-        tma_load_2d(sm + P1_KQ + kSlot + 8192, &tm_q, hk * kD + 64, rowg, &bar_tma);
-        tma_load_2d(sm + P1_V, &tm_v, hv * kD, rowg, &bar_tma);
+        tma_load_2d(sm + P1_KQ, tm_k, hk * kD, rowg, &sh.bar0);
+        tma_load_2d(sm + P1_KQ + kSlot, tm_k, hk * kD + 64, rowg, &sh.bar0);
+        tma_load_2d(sm + P1_KQ + 8192, tm_q, hk * kD, rowg, &sh.bar0);
+        tma_load_2d(sm + P1_KQ + kSlot + 8192, tm_q, hk * kD + 64, rowg, &sh.bar0);
+        tma_load_2d(sm + P1_V, tm_v, hv * kD, rowg, &sh.bar0);
     }
-    if (warp == 0) {
-        umma::tmem_alloc(&tmem_slot, 256);   // QK, D (U^T), W columns
-        umma::tmem_relinquish();
-    }
-    umma::fence_before_sync();
     __syncthreads();
-    umma::fence_after_sync();
-    const uint32_t tmem = tmem_slot;
-    const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
 
-    uint32_t mma_phase = 0;
     auto wait_mma = [&]() {
-        bool w = mbar_wait(&bar_mma, mma_phase & 1u, p.err);
+        bool w = mbar_wait(&sh.bar1, mma_phase & 1u, p.err);
         ++mma_phase;
         w = __syncthreads_and(w) != 0;
         umma::fence_after_sync();
@@ -156,29 +184,30 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
         umma::fence_after_sync();
     };
 
-    bool ok = mbar_wait(&bar_tma, 0, p.err);
-    if (warp == 0) step_factors(lane, s_g, s_b, s_lg, s_gam, s_kc, s_beta, s_bg);
+    bool ok = mbar_wait(&sh.bar0, tma_phase & 1u, p.err);
+    ++tma_phase;
+    if (warp == 0) step_factors(lane, sh.s_g, sh.s_b, sh.s_lg, sh.s_gam, sh.s_kc, sh.s_beta, sh.s_bg);
     ok = __syncthreads_and(ok) != 0;
     if (ok) {
         if (tid == 0) {
             umma::fence_after_sync();
             issue_kq(tmem, base, P1_KQ);
-            umma::mma_commit(&bar_mma);
+            umma::mma_commit(&sh.bar1);
         }
-        build_gq(sm, P1_KQ, P1_GQ, s_gam, tid);
-        build_kt_bk(sm, P1_KQ, P1_KT, P1_BK, s_kc, s_bg, tid);
-        build_bv(sm, P1_V, P1_BV, s_beta, tid);
+        build_gq(sm, P1_KQ, P1_GQ, sh.s_gam, tid);
+        build_kt_bk(sm, P1_KQ, P1_KT, P1_BK, sh.s_kc, sh.s_bg, tid);
+        build_bv(sm, P1_V, P1_BV, sh.s_beta, tid);
         ok = wait_mma();
     }
     if (ok) {
         // A from K K^T (quads 0-1); P from Q K^T (quads 2-3) into the dead K/Q slot
         if (quad < 2) {
-            build_a(lane_tmem + C_QK, As, s_lg, s_beta, row, half);
+            build_a(lane_tmem + C_QK, As, sh.s_lg, sh.s_beta, row, half);
         } else {
             float qk[32];
             umma::tmem_ld32(lane_tmem + C_QK + half * 32, qk);
             umma::tmem_ld_wait();
-            p_tile(qk, sm, P1_P, s_lg, row, half);
+            p_tile(qk, sm, P1_P, sh.s_lg, row, half);
         }
         __syncthreads();
         invert_unit_lower(As, Ys, tid);
@@ -186,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
         publish();
         if (tid == 0) {
             issue_uw(tmem, base, P1_T, P1_BV, P1_BK);
-            umma::mma_commit(&bar_mma);
+            umma::mma_commit(&sh.bar1);
         }
         ok = wait_mma();
     }
@@ -203,60 +232,42 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
         umma::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            uint8_t *blob = blob_at(p, b, hv, c);
-            *reinterpret_cast<float *>(blob + B_META) = s_gam[kC - 1];
+            const size_t bi = blob_index(p, b, hv, c);
+            uint8_t *blob = p.blobs + bi * kBlobBytes;
+            *reinterpret_cast<float *>(blob + B_META) = sh.s_gam[kC - 1];
             bulk_store(blob + B_GQ, sm + P1_GQ, 32768);
             bulk_store(blob + B_NW, sm + P1_NW, 32768);
             bulk_store(blob + B_UT, sm + P1_UT, 32768);
             bulk_store(blob + B_KT, sm + P1_KT, 32768);
             bulk_store(blob + B_P, sm + P1_P, 16384);
             bulk_commit();
-            bulk_wait_read();
+            if (p.ready != nullptr) {
+                bulk_wait_all();                       // the writes are done, not only read out
+                __threadfence();                       // ... and so is the meta store
+                publish_ready(p.ready + bi);
+            } else {
+                bulk_wait_read();
+            }
         }
     } else if (tid == 0) {
         // a wait gave up: give in-flight MMAs a bounded chance to drain
-        mbar_wait(&bar_mma, mma_phase & 1u, nullptr);
+        mbar_wait(&sh.bar1, mma_phase & 1u, nullptr);
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(tmem, 256);
+    return ok;
 }
 
 // ---------------------------------------------------------------------------
-// pass 2: the chunk chain of one head, state products only
+// pass 2: the chunk chain of head (b, hv), state products only.  The caller
+// has initialised sh.bar0-2 and allocated 512 TMEM columns.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_a, bar_b, bar_mma;
-    __shared__ uint32_t tmem_slot;
-    __shared__ int s_m[2][kC];
-    __shared__ uint32_t scan_bits[ChunkScan<kThreads>::kWords];
-
+__device__ __forceinline__ void state_head(const TwoPassParams &p, TwoPassShared &sh, uint8_t *sm, uint32_t base,
+                                           uint32_t tmem, int b, int hv) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2, row = quad * 32 + lane;
-    (void)lane;
-    const int hv = blockIdx.x;
-    const int b = p.order != nullptr ? p.order[blockIdx.y] : (int)blockIdx.y;
     const int T = p.T;
     const int nchunks = p.nchunks;
-
-    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    uint8_t *sm = smem_raw + (base - smem_u32(smem_raw));
-
-    if (tid == 0) {
-        mbar_init(&bar_a, 1);
-        mbar_init(&bar_b, 1);
-        mbar_init(&bar_mma, 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        umma::tmem_alloc(&tmem_slot, 512);
-        umma::tmem_relinquish();
-    }
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    const uint32_t tmem = tmem_slot;
     const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
 
     // initial state -> TMEM S (row = dv, columns = dk); half 0: dk 0-63, half 1: 64-127
@@ -275,27 +286,33 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
         }
         umma::tmem_st_wait();
     }
+    (void)lane;
 
     int pf_m = 0;
     auto gather_mask = [&](int c) {
         const int t = c * kC + tid;
         pf_m = (tid < kC && t < T) ? (p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0)) : 0;
     };
-    // thread 0 only: outstanding copies, for the drain after a failed wait
-    bool a_pending = false, b_pending = false;
+    // thread 0 only: outstanding copies, for the drain after a failed wait;
+    // after one flag wait has given up (error word set) no further one is made,
+    // so a failed producer costs one bounded wait, not one per chunk
+    bool a_pending = false, b_pending = false, flag_gave_up = false;
     uint32_t a_parity = 0, b_parity = 0;
     auto load_a = [&](int c, int it) {
         if (tid == 0) {
-            mbar_expect_tx(&bar_a, kGroupA);
-            bulk_load(sm + P2_GQ, blob_at(p, b, hv, c), kGroupA, &bar_a);
+            const size_t bi = blob_index(p, b, hv, c);
+            if (p.ready != nullptr && !flag_gave_up) flag_gave_up = !wait_ready(p.ready + bi, p.err);
+            mbar_expect_tx(&sh.bar0, kGroupA);
+            bulk_load(sm + P2_GQ, p.blobs + bi * kBlobBytes, kGroupA, &sh.bar0);
             a_pending = true;
             a_parity = (uint32_t)(it & 1);
         }
     };
     auto load_b = [&](int c, int it) {
         if (tid == 0) {
-            mbar_expect_tx(&bar_b, kGroupB);
-            bulk_load(sm + P2_KT, blob_at(p, b, hv, c) + kGroupA, kGroupB, &bar_b);
+            // group B of chunk c is loaded after group A, whose flag covers the whole blob
+            mbar_expect_tx(&sh.bar1, kGroupB);
+            bulk_load(sm + P2_KT, p.blobs + blob_index(p, b, hv, c) * kBlobBytes + kGroupA, kGroupB, &sh.bar1);
             b_pending = true;
             b_parity = (uint32_t)(it & 1);
         }
@@ -304,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
     uint32_t mma_phase = 0;
     bool ok = true;
     auto wait_mma = [&]() {
-        bool w = mbar_wait(&bar_mma, mma_phase & 1u, p.err);
+        bool w = mbar_wait(&sh.bar2, mma_phase & 1u, p.err);
         ++mma_phase;
         w = __syncthreads_and(w) != 0;
         umma::fence_after_sync();
@@ -317,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
         umma::fence_after_sync();
     };
 
-    ChunkScan<kThreads> scan(p.mask == nullptr ? nullptr : p.mask + (size_t)b * T, T, scan_bits);
+    ChunkScan<kThreads> scan(p.mask == nullptr ? nullptr : p.mask + (size_t)b * T, T, sh.scan_bits);
     uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * kD + (size_t)hv * kD;
     const size_t y_stride = (size_t)p.Hv * kD;
     int c = scan.next_active(0);
@@ -326,14 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
         load_a(c, 0);
         load_b(c, 0);
         gather_mask(c);
-        if (tid < kC) s_m[0][tid] = pf_m;
+        if (tid < kC) sh.s_m[0][tid] = pf_m;
     }
     __syncthreads();
 
     for (int it = 0; c < nchunks && ok; ++it) {
         const int st = it & 1;
         const int t0 = c * kC;
-        ok = __syncthreads_and(mbar_wait(&bar_a, (uint32_t)(it & 1), p.err)) != 0;
+        ok = __syncthreads_and(mbar_wait(&sh.bar0, (uint32_t)(it & 1), p.err)) != 0;
         if (tid == 0) a_pending = false;
         if (!ok) break;
         const int cn = scan.next_active(c + 1);
@@ -354,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
         publish();
         if (tid == 0) {
             issue_s0_products(tmem, base, P2_NW, P2_GQ);
-            umma::mma_commit(&bar_mma);
+            umma::mma_commit(&sh.bar2);
         }
         if (!wait_mma()) { ok = false; break; }
         // group A has been consumed: fetch the next chunk's
@@ -368,18 +385,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
             dt_tile(dv, sm, P2_DT, row, half);
         }
         publish();
-        ok = __syncthreads_and(mbar_wait(&bar_b, (uint32_t)(it & 1), p.err)) != 0;
+        ok = __syncthreads_and(mbar_wait(&sh.bar1, (uint32_t)(it & 1), p.err)) != 0;
         if (tid == 0) b_pending = false;
         if (!ok) break;
         if (tid == 0) {
             umma::fence_after_sync();
             issue_dt_products(tmem, base, P2_DT, P2_P, P2_KT);
-            umma::mma_commit(&bar_mma);
+            umma::mma_commit(&sh.bar2);
         }
         if (!wait_mma()) { ok = false; break; }
         if (cn < nchunks) load_b(cn, it + 1);
 
-        stage_y(lane_tmem + C_Y, sm, P2_YST, s_m[st], row, half);
+        stage_y(lane_tmem + C_Y, sm, P2_YST, sh.s_m[st], row, half);
         umma::fence_before_sync();
         __syncthreads();
         {
@@ -390,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
                     *reinterpret_cast<const uint4 *>(sm + P2_YST + (r * kD + c8) * 2);
             }
         }
-        if (tid < kC) s_m[st ^ 1][tid] = pf_m;
+        if (tid < kC) sh.s_m[st ^ 1][tid] = pf_m;
         zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), kD);
         c = cn;
     }
@@ -409,13 +426,100 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
         }
     } else if (tid == 0) {
         // a wait gave up: give in-flight MMAs and copies a bounded chance to drain
-        mbar_wait(&bar_mma, mma_phase & 1u, nullptr);
-        if (a_pending) mbar_wait(&bar_a, a_parity, nullptr);
-        if (b_pending) mbar_wait(&bar_b, b_parity, nullptr);
+        mbar_wait(&sh.bar2, mma_phase & 1u, nullptr);
+        if (a_pending) mbar_wait(&sh.bar0, a_parity, nullptr);
+        if (b_pending) mbar_wait(&sh.bar1, b_parity, nullptr);
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// kernels
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint8_t *aligned_base(uint8_t *raw, uint32_t &base) {
+    base = (smem_u32(raw) + 1023u) & ~1023u;
+    return raw + (base - smem_u32(raw));
+}
+
+// barriers and TMEM of a CTA; returns the TMEM base
+__device__ __forceinline__ uint32_t cta_setup(TwoPassShared &sh, uint32_t tmem_cols) {
+    if (threadIdx.x == 0) {
+        mbar_init(&sh.bar0, 1);
+        mbar_init(&sh.bar1, 1);
+        mbar_init(&sh.bar2, 1);
+        fence_mbar_init();
+    }
+    if ((threadIdx.x >> 5) == 0) {
+        umma::tmem_alloc(&sh.tmem_slot, tmem_cols);
+        umma::tmem_relinquish();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    return sh.tmem_slot;
+}
+
+__device__ __forceinline__ void cta_teardown(uint32_t tmem, uint32_t tmem_cols) {
+    if ((threadIdx.x >> 5) == 0) umma::tmem_dealloc(tmem, tmem_cols);
+}
+
+// separate form, pass 1: one CTA per (chunk, hv, b)
+__global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                  const __grid_constant__ CUtensorMap tm_q,
+                                                                  const __grid_constant__ CUtensorMap tm_v,
+                                                                  const TwoPassParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ TwoPassShared sh;
+    uint32_t base;
+    uint8_t *sm = aligned_base(smem_raw, base);
+    const uint32_t tmem = cta_setup(sh, 256);
+    uint32_t tma_phase = 0, mma_phase = 0;
+    prep_unit(p, &tm_k, &tm_q, &tm_v, sh, sm, base, tmem, blockIdx.x, blockIdx.z, blockIdx.y, tma_phase, mma_phase);
+    cta_teardown(tmem, 256);
+}
+
+// separate form, pass 2: one CTA per (hv, row slot)
+__global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ TwoPassShared sh;
+    uint32_t base;
+    uint8_t *sm = aligned_base(smem_raw, base);
+    const uint32_t tmem = cta_setup(sh, 512);
+    const int b = p.order != nullptr ? p.order[blockIdx.y] : (int)blockIdx.y;
+    state_head(p, sh, sm, base, tmem, b, blockIdx.x);
+    cta_teardown(tmem, 512);
+}
+
+// overlapped form (cooperative launch, all CTAs resident): CTAs [0, n_heads)
+// run the state chains, the others produce the chunk images in chunk order
+__global__ void __launch_bounds__(kThreads, 1) chunk_overlap_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                     const __grid_constant__ CUtensorMap tm_q,
+                                                                     const __grid_constant__ CUtensorMap tm_v,
+                                                                     const TwoPassParams p, const int n_heads) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ TwoPassShared sh;
+    uint32_t base;
+    uint8_t *sm = aligned_base(smem_raw, base);
+    const bool is_state = (int)blockIdx.x < n_heads;
+    const uint32_t cols = is_state ? 512u : 256u;
+    const uint32_t tmem = cta_setup(sh, cols);
+    if (is_state) {
+        const int slot = blockIdx.x / p.Hv, hv = blockIdx.x % p.Hv;
+        const int b = p.order != nullptr ? p.order[slot] : slot;
+        state_head(p, sh, sm, base, tmem, b, hv);
+    } else {
+        const int n_prep = (int)gridDim.x - n_heads;
+        const long n_units = (long)p.nchunks * n_heads;
+        uint32_t tma_phase = 0, mma_phase = 0;
+        for (long u = (long)blockIdx.x - n_heads; u < n_units; u += n_prep) {
+            const int c = (int)(u / n_heads), h = (int)(u % n_heads);
+            if (!prep_unit(p, &tm_k, &tm_q, &tm_v, sh, sm, base, tmem, c, h / p.Hv, h % p.Hv, tma_phase,
+                           mma_phase))
+                break;
+        }
+    }
+    cta_teardown(tmem, cols);
 }
 
 template <typename K>
@@ -428,11 +532,13 @@ cudaError_t set_smem(K kernel, uint32_t bytes, bool &done) {
     return cudaSuccess;
 }
 
+size_t blob_count(const Sizes &s) { return (size_t)s.B * s.Hv * (((size_t)s.T + kC - 1) / kC); }
+
 }  // namespace
 
 size_t prefill_two_pass_workspace(const Sizes &s) {
-    const size_t nchunks = ((size_t)s.T + kC - 1) / kC;
-    return (size_t)s.B * s.Hv * nchunks * kBlobBytes;
+    const size_t n = blob_count(s);
+    return n * kBlobBytes + ((n * sizeof(int) + 255) & ~(size_t)255);
 }
 
 bool prefill_two_pass_pays(const Sizes &s) { return (long)s.B * s.Hv < num_sms(); }
@@ -451,14 +557,40 @@ cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uin
         !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    static bool set1 = false, set2 = false;
+    static bool set1 = false, set2 = false, set3 = false;
     cudaError_t e = set_smem(chunk_prep_kernel, kP1Smem, set1);
-    if (e != cudaSuccess) return e;
-    e = set_smem(chunk_state_kernel, kP2Smem, set2);
+    if (e == cudaSuccess) e = set_smem(chunk_state_kernel, kP2Smem, set2);
+    if (e == cudaSuccess) e = set_smem(chunk_overlap_kernel, kFusedSmem, set3);
     if (e != cudaSuccess) return e;
     const int nchunks = (s.T + kC - 1) / kC;
+    const int n_heads = s.B * s.Hv;
+    const size_t n_blobs = blob_count(s);
     TwoPassParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y,
-                    static_cast<uint8_t *>(blobs), err, s.B, s.T, s.Hk, s.Hv, nchunks};
+                    static_cast<uint8_t *>(blobs), nullptr, err, s.B, s.T, s.Hk, s.Hv, nchunks};
+
+    // Overlapped form when the producers (all SMs but the heads') outnumber
+    // the heads about three to one: a chunk image takes the producers roughly
+    // three times as long as the state pass takes to consume one.
+    int per_sm = 0;
+    if (4 * n_heads <= num_sms() &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_overlap_kernel, kThreads, kFusedSmem) ==
+            cudaSuccess &&
+        per_sm >= 1) {
+        p.ready = reinterpret_cast<int *>(static_cast<uint8_t *>(blobs) + n_blobs * kBlobBytes);
+        e = cudaMemsetAsync(p.ready, 0, n_blobs * sizeof(int), st);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(num_sms() * per_sm);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kFusedSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, chunk_overlap_kernel, tk, tq, tv, p, n_heads);
+    }
     chunk_prep_kernel<<<dim3(nchunks, s.Hv, s.B), kThreads, kP1Smem, st>>>(tk, tq, tv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -311,6 +311,8 @@ TWO_PASS_CASES = [
     (3, 700, 2, 4, "blocks", "normal"),
     (2, 257, 2, 4, "right", "zeros"),
     (2, 150, 1, 2, "allmasked_row", "normal"),
+    (2, 100, 4, 24, "random", "normal"),     # 48 heads: the two passes as separate launches
+    (1, 130, 8, 64, None, "zeros"),
 ]
 
 
