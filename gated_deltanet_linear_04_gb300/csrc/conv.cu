@@ -27,7 +27,8 @@
 namespace gdn {
 namespace {
 
-constexpr int kTile = 8;        // tokens per warp task (8: measured 1.3x faster than 16 at 4 CTAs/SM)
+constexpr int kTask = 32;       // tokens per warp task
+constexpr int kSub = 8;         // tokens per sub-tile (one sub-tile's rows in flight ahead)
 constexpr int kWarps = 8;       // head segments per CTA
 constexpr int kMaxHalo = 3;     // K - 1 for the largest supported K (4)
 
@@ -39,32 +40,6 @@ struct ConvParams {
     int B, T, Hk, Hv, C, K;
     float eps;
 };
-
-// Continues a backward scan for the most recent valid steps of row b: nf
-// holds `found` positions (newest first), the scan resumes below `cur`.
-// Positions older than the first valid token become conv_state codes (< 0,
-// -1 = newest stored row).  Warp-collective.
-__device__ __forceinline__ void scan_halo(const uint8_t *mask, int b, int T, int cur, int found, int lane,
-                                          int (&nf)[kMaxHalo]) {
-    while (found < kMaxHalo && cur > 0) {
-        const int base = max(cur - 32, 0);
-        const int len = cur - base;
-        const bool m = lane < len && mask[(size_t)b * T + base + lane] != 0;
-        unsigned ball = __ballot_sync(0xffffffffu, m);
-        while (ball != 0u && found < kMaxHalo) {
-            const int hi = 31 - __clz(ball);
-#pragma unroll
-            for (int r = 0; r < kMaxHalo; ++r)
-                if (r == found) nf[r] = base + hi;
-            ++found;
-            ball &= ~(1u << hi);
-        }
-        cur = base;
-    }
-#pragma unroll
-    for (int r = 0; r < kMaxHalo; ++r)
-        if (r >= found) nf[r] = -(r - found + 1);
-}
 
 // Positions of the kMaxHalo most recent valid steps strictly before `t_end` of
 // row b, oldest first.  A code >= 0 is a token index; a code < 0 names
@@ -80,7 +55,17 @@ __device__ __forceinline__ void find_halo(const uint8_t *mask, int b, int T, int
 #pragma unroll
         for (int r = 0; r < kMaxHalo; ++r) nf[r] = 0;
         int cur = t_end;
+        const uint8_t *mrow = mask + (size_t)b * T;
         while (found < kMaxHalo && cur > 0) {
+            // 128-step blocks without a valid step (the padding of a short
+            // row) are skipped four mask bytes per lane at a time
+            if (cur >= 128 && (reinterpret_cast<uintptr_t>(mrow + cur - 128) & 3u) == 0) {
+                const uint32_t wv = *reinterpret_cast<const uint32_t *>(mrow + cur - 128 + 4 * lane);
+                if (__ballot_sync(0xffffffffu, wv != 0u) == 0u) {
+                    cur -= 128;
+                    continue;
+                }
+            }
             const int base = max(cur - 32, 0);
             const int len = cur - base;
             const bool m = lane < len && mask[(size_t)b * T + base + lane] != 0;
@@ -142,27 +127,50 @@ __device__ __forceinline__ void store_zero(uint16_t *p) {
     else *p = 0;
 }
 
-// One head segment of D channels (c0 = first channel) over one token tile.
+template <int CPL> struct RawRow;
+template <> struct RawRow<4> { using type = uint2; };
+template <> struct RawRow<2> { using type = uint32_t; };
+template <> struct RawRow<1> { using type = uint16_t; };
+
+template <int CPL>
+__device__ __forceinline__ typename RawRow<CPL>::type load_raw(const uint16_t *p) {
+    return *reinterpret_cast<const typename RawRow<CPL>::type *>(p);
+}
+
+template <int CPL>
+__device__ __forceinline__ void unpack(const typename RawRow<CPL>::type &r, float (&o)[CPL]) {
+    if constexpr (CPL == 4) {
+        o[0] = __uint_as_float(r.x << 16);
+        o[1] = __uint_as_float(r.x & 0xffff0000u);
+        o[2] = __uint_as_float(r.y << 16);
+        o[3] = __uint_as_float(r.y & 0xffff0000u);
+    } else if constexpr (CPL == 2) {
+        o[0] = __uint_as_float(r << 16);
+        o[1] = __uint_as_float(r & 0xffff0000u);
+    } else {
+        o[0] = bf16_to_f32(r);
+    }
+}
+
+// One head segment of D channels (c0 = first channel) over one task of kTask
+// tokens, walked in sub-tiles of kSub: the taps and the K-1 window rows
+// before the task are loaded once; the next sub-tile's rows are in flight
+// while the current one is computed; the window of the last K-1 valid rows
+// travels in registers.
 // kind: 0 = q (rms-norm, scale 1/D), 1 = k (rms-norm, scale 1/sqrt(D)), 2 = v.
 template <int D>
 __device__ __forceinline__ void conv_segment(const ConvParams &p, int kind, int c0, uint16_t *out_base,
                                              int out_head_stride, int b, int t0, int lane) {
     constexpr int CPL = D / 32;
+    constexpr int NS = kTask / kSub;
+    using Raw = typename RawRow<CPL>::type;
     const int c = c0 + lane * CPL;
-    const int nt = min(kTile, p.T - t0);
+    const int nt = min(kTask, p.T - t0);
 
-    // One mask load for the tile and the 24 steps before it: lanes 0-23 read
-    // steps t0-24 .. t0-1 (candidates for the window rows before the tile),
-    // lanes 24-31 the tile itself.
-    constexpr int kPre = 32 - kTile;
-    unsigned valid, prev = 0u;
+    unsigned valid;   // bit i: step t0 + i is valid
     if (p.mask != nullptr) {
-        const int t = t0 - kPre + lane;
-        const bool in = lane < kPre ? t >= 0 : lane - kPre < nt;
-        const bool m = in && p.mask[(size_t)b * p.T + t] != 0;
-        const unsigned ball = __ballot_sync(0xffffffffu, m);
-        valid = ball >> kPre;
-        prev = ball & ((1u << kPre) - 1u);
+        const bool m = lane < nt && p.mask[(size_t)b * p.T + t0 + lane] != 0;
+        valid = __ballot_sync(0xffffffffu, m);
     } else {
         valid = nt >= 32 ? 0xffffffffu : ((1u << nt) - 1u);
     }
@@ -174,112 +182,101 @@ __device__ __forceinline__ void conv_segment(const ConvParams &p, int kind, int 
         return;
     }
 
-    // taps, right-aligned to 4 (tap K-1 of the page's weight -> slot 3)
-    float w[CPL][4];
+    // rows of sub-tile s in flight into buffer `slot` (masked or absent rows read nothing)
+    Raw buf[2][kSub];
+    auto issue = [&](int s, int slot) {
+#pragma unroll
+        for (int r = 0; r < kSub; ++r) {
+            const int tl = s * kSub + r;
+            buf[slot][r] = Raw{};
+            if (tl < nt && ((valid >> tl) & 1u))
+                buf[slot][r] = load_raw<CPL>(p.qkv + ((size_t)b * p.T + t0 + tl) * p.C + c);
+        }
+    };
+    issue(0, 0);
+
+    // taps, right-aligned to 4 (tap K-1 of the page's weight -> slot 3), kept
+    // as bf16 bit patterns (exact; unpacked at use)
+    uint16_t w[CPL][4];
 #pragma unroll
     for (int i = 0; i < CPL; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int jj = j - (4 - p.K);
-            w[i][j] = jj >= 0 ? bf16_to_f32(p.conv_w[(size_t)(c + i) * p.K + jj]) : 0.0f;
+            w[i][j] = jj >= 0 ? p.conv_w[(size_t)(c + i) * p.K + jj] : (uint16_t)0;
         }
 
-    // window of the K-1 valid rows before the tile (zeros for unused slots):
-    // the newest valid steps among the 24 already seen, the rest (rarely
-    // needed) by scanning further back
+    // window of the K-1 valid rows before the task (zeros for unused slots),
+    // kept as the raw bf16 rows
     int codes[kMaxHalo];
-    if (p.mask == nullptr) {
-#pragma unroll
-        for (int j = 0; j < kMaxHalo; ++j) codes[j] = t0 - kMaxHalo + j;
-    } else {
-        int nf[kMaxHalo] = {0, 0, 0};
-        int found = 0;
-        unsigned pb = prev;
-#pragma unroll
-        for (int r = 0; r < kMaxHalo; ++r) {
-            if (pb != 0u) {
-                const int hi = 31 - __clz(pb);
-                nf[r] = t0 - kPre + hi;
-                pb &= ~(1u << hi);
-                found = r + 1;
-            }
-        }
-        if (found < kMaxHalo) scan_halo(p.mask, b, p.T, t0 - kPre, found, lane, nf);
-#pragma unroll
-        for (int j = 0; j < kMaxHalo; ++j) codes[j] = nf[kMaxHalo - 1 - j];
-    }
-    float win[kMaxHalo][CPL];
+    find_halo(p.mask, b, p.T, t0, lane, codes);
+    Raw win[kMaxHalo];
 #pragma unroll
     for (int j = 0; j < kMaxHalo; ++j) {
         const int code = codes[j];
         const bool used = j >= kMaxHalo - (p.K - 1);
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) win[j][i] = 0.0f;
+        win[j] = Raw{};
         if (used) {
             if (code >= 0) {
-                load_bf16<CPL>(p.qkv + ((size_t)b * p.T + code) * p.C + c, win[j]);
+                win[j] = load_raw<CPL>(p.qkv + ((size_t)b * p.T + code) * p.C + c);
             } else if (p.conv_state != nullptr && p.K - 1 + code >= 0) {
-                load_bf16<CPL>(p.conv_state + ((size_t)b * (p.K - 1) + (p.K - 1 + code)) * p.C + c, win[j]);
+                win[j] = load_raw<CPL>(p.conv_state + ((size_t)b * (p.K - 1) + (p.K - 1 + code)) * p.C + c);
             }
-        }
-    }
-
-    // all tile rows in flight at once
-    float xr[kTile][CPL];
-#pragma unroll
-    for (int r = 0; r < kTile; ++r) {
-        if (r < nt && ((valid >> r) & 1u)) {
-            load_bf16<CPL>(p.qkv + ((size_t)b * p.T + t0 + r) * p.C + c, xr[r]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) xr[r][i] = 0.0f;
         }
     }
 
     const float inv_d = 1.0f / (float)D;
     const float scale = kind == 0 ? inv_d : (kind == 1 ? 1.0f / sqrtf((float)D) : 1.0f);
 #pragma unroll
-    for (int r = 0; r < kTile; ++r) {
-        if (r >= nt) break;
-        uint16_t *op = out_ptr(t0 + r);
-        if (!((valid >> r) & 1u)) {
-            store_zero<CPL>(op);
-            continue;
-        }
-        float x[CPL];
-        float ss = 0.0f;
+    for (int s = 0; s < NS; ++s) {
+        if (s * kSub >= nt) break;
+        if (s + 1 < NS) issue(s + 1, (s + 1) & 1);
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            float u = w[i][0] * win[0][i];
-            u = fmaf(w[i][1], win[1][i], u);
-            u = fmaf(w[i][2], win[2][i], u);
-            u = fmaf(w[i][3], xr[r][i], u);
-            x[i] = silu(u);
-            ss = fmaf(x[i], x[i], ss);
-        }
-        if (kind != 2) {
-            ss = warp_sum(ss);
-            const float rs = (1.0f / sqrtf(ss * inv_d + p.eps)) * scale;
+        for (int r = 0; r < kSub; ++r) {
+            const int tl = s * kSub + r;
+            if (tl >= nt) break;
+            uint16_t *op = out_ptr(t0 + tl);
+            if (!((valid >> tl) & 1u)) {
+                store_zero<CPL>(op);
+                continue;
+            }
+            float xr[CPL], w0[CPL], w1[CPL], w2[CPL];
+            unpack<CPL>(buf[s & 1][r], xr);
+            unpack<CPL>(win[0], w0);
+            unpack<CPL>(win[1], w1);
+            unpack<CPL>(win[2], w2);
+            float x[CPL];
+            float ss = 0.0f;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) x[i] *= rs;
-        }
-        store_bf16<CPL>(op, x);
+            for (int i = 0; i < CPL; ++i) {
+                float u = bf16_to_f32(w[i][0]) * w0[i];
+                u = fmaf(bf16_to_f32(w[i][1]), w1[i], u);
+                u = fmaf(bf16_to_f32(w[i][2]), w2[i], u);
+                u = fmaf(bf16_to_f32(w[i][3]), xr[i], u);
+                x[i] = silu(u);
+                ss = fmaf(x[i], x[i], ss);
+            }
+            if (kind != 2) {
+                ss = warp_sum(ss);
+                const float rs = (1.0f / sqrtf(ss * inv_d + p.eps)) * scale;
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            win[0][i] = win[1][i];
-            win[1][i] = win[2][i];
-            win[2][i] = xr[r][i];
+                for (int i = 0; i < CPL; ++i) x[i] *= rs;
+            }
+            store_bf16<CPL>(op, x);
+            win[0] = win[1];
+            win[1] = win[2];
+            win[2] = buf[s & 1][r];
         }
     }
 }
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(kWarps * 32, 4) conv_update_kernel(const ConvParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 3) conv_update_kernel(const ConvParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seg = blockIdx.y * kWarps + warp;
     const int nseg = 2 * p.Hk + p.Hv;
     if (seg >= nseg) return;
-    const int t0 = blockIdx.x * kTile;
+    const int t0 = blockIdx.x * kTask;
     const int b = blockIdx.z;
     if (seg < p.Hk) {
         uint16_t *ob = p.q + ((size_t)b * p.T * p.Hk + seg) * DK;
@@ -335,7 +332,7 @@ __global__ void __launch_bounds__(256) gating_kernel(const uint16_t *__restrict_
 template <int DK, int DV>
 cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t st) {
     const int nseg = 2 * p.Hk + p.Hv;
-    dim3 grid((p.T + kTile - 1) / kTile, (nseg + kWarps - 1) / kWarps, p.B);
+    dim3 grid((p.T + kTask - 1) / kTask, (nseg + kWarps - 1) / kWarps, p.B);
     conv_update_kernel<DK, DV><<<grid, kWarps * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
