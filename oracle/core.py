@@ -77,6 +77,10 @@ def _load():
             lib.oracle_delta_rule_head.restype = None
             lib.oracle_delta_rule_head_vec.argtypes = lib.oracle_delta_rule_head.argtypes
             lib.oracle_delta_rule_head_vec.restype = None
+            lib.oracle_delta_rule_head_bwd.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                       dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_uint8),
+                                                       dp, dp, dp, dp, dp, dp, dp, dp, dp]
+            lib.oracle_delta_rule_head_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -299,6 +303,63 @@ def head_recurrence_vec(q, k, v, g, beta, S0, mask=None):
     lib.oracle_delta_rule_head_vec(T, Dk, Dv, _dptr(q), _dptr(k), _dptr(v), _dptr(g), _dptr(beta), mp, _dptr(S),
                                    _dptr(y))
     return y, S
+
+
+def head_recurrence_bwd(q, k, v, g, beta, S0, dy, dST=None, mask=None):
+    """Gradients of head_recurrence (the exact derivative of the recurrence,
+    taken in reverse, in the C part) given dy [T,Dv] and dST [Dv,Dk] (None =
+    0) of the outputs y and S_T.  Returns a dict of float64 arrays: dq, dk
+    [T,Dk], dv [T,Dv], dg, dbeta [T], dS0 [Dv,Dk]."""
+    lib = _load()
+    q, k, v, g, beta, dy = (np.ascontiguousarray(a, np.float64) for a in (q, k, v, g, beta, dy))
+    T, Dk = q.shape
+    Dv = v.shape[1]
+    S0 = np.zeros((Dv, Dk)) if S0 is None else np.ascontiguousarray(S0, np.float64)
+    dST_a = None if dST is None else np.ascontiguousarray(dST, np.float64)
+    m = None if mask is None else np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    mp = None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+    out = {"dq": np.zeros((T, Dk)), "dk": np.zeros((T, Dk)), "dv": np.zeros((T, Dv)), "dg": np.zeros(T),
+           "dbeta": np.zeros(T), "dS0": np.zeros((Dv, Dk))}
+    rc = lib.oracle_delta_rule_head_bwd(T, Dk, Dv, _dptr(q), _dptr(k), _dptr(v), _dptr(g), _dptr(beta), mp,
+                                        _dptr(S0), _dptr(dy), None if dST_a is None else _dptr(dST_a),
+                                        _dptr(out["dq"]), _dptr(out["dk"]), _dptr(out["dv"]), _dptr(out["dg"]),
+                                        _dptr(out["dbeta"]), _dptr(out["dS0"]))
+    if rc != 0:
+        raise MemoryError("oracle_delta_rule_head_bwd could not allocate its state history")
+    return out
+
+
+def recurrence_bwd(d, q_bits, k_bits, v_bits, g, beta, state_in, dy, dstate_out=None, mask=None, threads=None):
+    """Gradients of ``recurrence`` for all (b, hv) heads: dy [B,T,Hv,Dv] and
+    dstate_out [B,Hv,Dv,Dk] (None = 0) in float64.  q and k are shared by the
+    Hv/Hk v-heads of a k-head, so their gradients are the sums over those
+    heads.  Returns dq, dk [B,T,Hk,Dk], dv [B,T,Hv,Dv], dg, dbeta [B,T,Hv],
+    dstate_in [B,Hv,Dv,Dk] (float64)."""
+    out = {"dq": np.zeros((d.B, d.T, d.Hk, d.Dk)), "dk": np.zeros((d.B, d.T, d.Hk, d.Dk)),
+           "dv": np.zeros((d.B, d.T, d.Hv, d.Dv)), "dg": np.zeros((d.B, d.T, d.Hv)),
+           "dbeta": np.zeros((d.B, d.T, d.Hv)), "dstate_in": np.zeros((d.B, d.Hv, d.Dv, d.Dk))}
+    pairs = [(b, hv) for b in range(d.B) for hv in range(d.Hv)]
+    res = {}
+
+    def one(pair):
+        b, hv = pair
+        hk = k_head_of(d, hv)
+        res[pair] = head_recurrence_bwd(bf16_to_f64(q_bits[b, :, hk]), bf16_to_f64(k_bits[b, :, hk]),
+                                        bf16_to_f64(v_bits[b, :, hv]), g[b, :, hv], beta[b, :, hv],
+                                        None if state_in is None else state_in[b, hv], dy[b, :, hv],
+                                        None if dstate_out is None else dstate_out[b, hv],
+                                        None if mask is None else mask[b])
+
+    _map_threads(one, pairs, threads)
+    for (b, hv), r in sorted(res.items()):
+        hk = k_head_of(d, hv)
+        out["dq"][b, :, hk] += r["dq"]
+        out["dk"][b, :, hk] += r["dk"]
+        out["dv"][b, :, hv] = r["dv"]
+        out["dg"][b, :, hv] = r["dg"]
+        out["dbeta"][b, :, hv] = r["dbeta"]
+        out["dstate_in"][b, hv] = r["dS0"]
+    return out
 
 
 def recurrence_vec(d, q_bits, k_bits, v_bits, g, beta, state_in=None, mask=None, threads=None):

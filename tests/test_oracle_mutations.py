@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import oracle.core as oc
+from tests import test_oracle_bwd_pins as bwd_pins
 from tests import test_oracle_pins as pins
 
 C_MUTATIONS = {
@@ -44,6 +45,9 @@ def _build_mutant(tmp_path, name, old, new):
     lib.oracle_delta_rule_head.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp,
                                            ctypes.POINTER(ctypes.c_uint8), dp, dp]
     lib.oracle_delta_rule_head.restype = None
+    lib.oracle_delta_rule_head_bwd.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp,
+                                               ctypes.POINTER(ctypes.c_uint8), dp, dp, dp, dp, dp, dp, dp, dp, dp]
+    lib.oracle_delta_rule_head_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -62,6 +66,30 @@ def test_c_mutation_is_caught(name, tmp_path, monkeypatch):
     lib = _build_mutant(tmp_path, name, old, new)
     monkeypatch.setattr(oc, "_lib", lib)
     assert _some_pin_fails(C_PINS, oracle_mod=oc), name
+
+
+# plausible mistakes in the backward pass (the forward stays intact, so the
+# finite-difference pins expose them)
+BWD_MUTATIONS = {
+    "bwd_dq_dropped": ("dqt[j] += St[(size_t)i * Dk + j] * dyt[i];", "dqt[j] += 0.0 * dyt[i];"),
+    "bwd_dk_sign": ("dkt[j] -= Sp[(size_t)i * Dk + j] * du[i];", "dkt[j] += Sp[(size_t)i * Dk + j] * du[i];"),
+    "bwd_no_decay_carry": ("for (size_t e = 0; e < n; ++e) dS[e] *= g[t];",
+                           "for (size_t e = 0; e < n; ++e) dS[e] *= 1.0;"),
+    "bwd_dbeta_without_u": ("dbeta[t] += ddel[i] * u[(size_t)t * Dv + i];", "dbeta[t] += ddel[i];"),
+    "bwd_dg_wrong_state": ("acc += dS[e] * Sprev[e];", "acc += dS[e] * St[e];"),
+    "bwd_du_without_beta": ("du[i] = beta[t] * ddel[i];", "du[i] = ddel[i];"),
+}
+
+BWD_PINS = [lambda oracle_mod: bwd_pins._check_fd(oracle_mod, 5, 3, 2, 1, False, True),
+            lambda oracle_mod: bwd_pins._check_fd(oracle_mod, 6, 2, 3, 2, True, True)]
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTATIONS))
+def test_bwd_mutation_is_caught(name, tmp_path, monkeypatch):
+    old, new = BWD_MUTATIONS[name]
+    lib = _build_mutant(tmp_path, name, old, new)
+    monkeypatch.setattr(oc, "_lib", lib)
+    assert _some_pin_fails(BWD_PINS, oracle_mod=oc), name
 
 
 def _mut_gqa_modulo(d, hv):
