@@ -357,6 +357,52 @@ def bench_decode_small(gdn, w: wl.Workload, dev, reps: int = 3) -> dict:
             "gbs_graph_l2_resident": round(by / (us_g / 1e6) / 1e9, 1)}
 
 
+def bench_backward(gdn, w: wl.Workload, dev, iters: int = 3) -> dict:
+    """The backward pass of the recurrence over one workload call (gradients of
+    y and of the final state with respect to q, k, v, g, beta and the initial
+    state), from device-generated inputs of the workload's shapes."""
+    d = w.dims
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5000 + w.index)
+    q = torch.randn((d.B, d.T, d.Hk, d.Dk), generator=gen, device=dev)
+    k = torch.randn((d.B, d.T, d.Hk, d.Dk), generator=gen, device=dev)
+    q = (q / q.norm(dim=-1, keepdim=True) / d.Dk ** 0.5).to(torch.bfloat16)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    v = torch.randn((d.B, d.T, d.Hv, d.Dv), generator=gen, device=dev).to(torch.bfloat16)
+    g = torch.exp(-torch.rand((d.B, d.T, d.Hv), generator=gen, device=dev) * 0.5)
+    beta = torch.sigmoid(torch.randn((d.B, d.T, d.Hv), generator=gen, device=dev))
+    s0 = torch.randn((d.B, d.Hv, d.Dv, d.Dk), generator=gen, device=dev) * 0.05
+    dy = (torch.randn((d.B, d.T, d.Hv, d.Dv), generator=gen, device=dev) * 0.1).to(torch.bfloat16)
+    mask = None
+    n_valid = d.B * d.T
+    if w.ragged:
+        lens = wl.workload_lengths(w)
+        mask = wl.right_padded_mask(lens, d.T).to(dev)
+        n_valid = int(lens.sum())
+    outs = [torch.empty((d.B, d.T, d.Hk, d.Dk), device=dev), torch.empty((d.B, d.T, d.Hk, d.Dk), device=dev),
+            torch.empty((d.B, d.T, d.Hv, d.Dv), device=dev), torch.empty((d.B, d.T, d.Hv), device=dev),
+            torch.empty((d.B, d.T, d.Hv), device=dev), torch.empty((d.B, d.Hv, d.Dv, d.Dk), device=dev)]
+    ws = torch.empty(gdn.gdn_prefill_backward_workspace_size(d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def once():
+        gdn.gdn_prefill_backward(d, q, k, v, g, beta, s0, mask, dy, None, *outs, ws, stream)
+
+    once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        once()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the backward benchmark")
+    ms = e0.elapsed_time(e1) / iters
+    return {"workload": w.name, "ms": round(ms, 4), "tokens": n_valid, "tokens_per_s": round(n_valid / (ms / 1e3), 1),
+            "workspace_mb": round(ws.numel() / 2 ** 20, 1)}
+
+
 def bench_decode_gated(gdn, w: wl.Workload, dev, iters: int = 200) -> dict:
     """One decode step of the batched-decode workload with the layer's gated
     RMS norm: the gated entry point vs decode followed by the separate norm
@@ -563,7 +609,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-prefill", action="store_true", help="only the headline decode (no other sections)")
-    ap.add_argument("--parts", default="decode_b1,rmsnorm,window,decode_gated,prefill",
+    ap.add_argument("--parts", default="decode_b1,rmsnorm,window,decode_gated,prefill,backward",
                     help="comma-separated sections to run after the headline decode")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
@@ -632,6 +678,9 @@ def main():
         window = bench_decode_window(gdn, w, dev)
     if "decode_gated" in parts:
         decode_gated = bench_decode_gated(gdn, w, dev)
+    backward = None
+    if "backward" in parts:
+        backward = [bench_backward(gdn, wl.WORKLOADS[name], dev) for name in ("prefill_t8192", "prefill_ragged")]
     if "prefill" in parts:
         for name in ("prefill_t8192", "prefill_ragged"):
             for chunk in (0, 64):
@@ -679,6 +728,7 @@ def main():
         "rmsnorm_gated": gated_norm,
         "decode_window": window,
         "decode_gated_norm": decode_gated,
+        "backward": backward,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

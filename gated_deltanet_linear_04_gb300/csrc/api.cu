@@ -295,6 +295,43 @@ gdn_status gdn_prefill_gated(const gdn_dims *dims, const uint16_t *q, const uint
                         workspace, ws_bytes, stream);
 }
 
+size_t gdn_prefill_backward_workspace_size(const gdn_dims *dims) {
+    gdn::Sizes s;
+    if (gdn::check_dims(dims, &s) != GDN_OK) return 0;
+    return gdn::backward_workspace(s);
+}
+
+gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                const float *g, const float *beta, const float *state_in, const uint8_t *mask,
+                                const uint16_t *dy, const float *dstate_out, float *dq, float *dk, float *dv,
+                                float *dg, float *dbeta, float *dstate_in, void *workspace, size_t ws_bytes,
+                                gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    const size_t BT = (size_t)s.B * s.T;
+    const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
+    if (!gdn::ok_ptr(q, BT) || !gdn::ok_ptr(k, BT) || !gdn::ok_ptr(v, BT) || !gdn::ok_ptr(g, BT) ||
+        !gdn::ok_ptr(beta, BT) || !gdn::ok_ptr(state_in, 0) || !gdn::ok_ptr(mask, 0) || !gdn::ok_ptr(dy, BT) ||
+        !gdn::ok_ptr(dstate_out, 0) || !gdn::ok_ptr(dq, BT) || !gdn::ok_ptr(dk, BT) || !gdn::ok_ptr(dv, BT) ||
+        !gdn::ok_ptr(dg, BT) || !gdn::ok_ptr(dbeta, BT) || !gdn::ok_ptr(dstate_in, nstate))
+        return GDN_ERR_INVALID_ARG;
+    if (s.B == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (s.T == 0) {
+        // no steps: the initial state's gradient is that of the final state
+        if (dstate_out == nullptr)
+            return gdn::from_cuda(cudaMemsetAsync(dstate_in, 0, nstate * sizeof(float), cs));
+        if (dstate_out == dstate_in) return GDN_OK;
+        return gdn::from_cuda(
+            cudaMemcpyAsync(dstate_in, dstate_out, nstate * sizeof(float), cudaMemcpyDeviceToDevice, cs));
+    }
+    if (workspace == nullptr || ws_bytes < gdn::backward_workspace(s) || !gdn::aligned16(workspace))
+        return GDN_ERR_INVALID_ARG;
+    return gdn::from_cuda(gdn::launch_backward(s, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg,
+                                               dbeta, dstate_in, workspace, cs));
+}
+
 gdn_status gdn_rmsnorm_gated(const gdn_dims *dims, const uint16_t *y, const uint16_t *z, const float *norm_w,
                              float norm_eps, uint16_t *out, gdn_stream stream) {
     gdn::Sizes s;

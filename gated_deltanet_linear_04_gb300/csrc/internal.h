@@ -63,6 +63,14 @@ cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint
                                    const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
                                    const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st);
 
+// Backward pass (backward.cu): workspace bytes and the launch (outputs zeroed
+// by the launch, then accumulated).
+size_t backward_workspace(const Sizes &s);
+cudaError_t launch_backward(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const float *g, const float *beta, const float *state_in, const uint8_t *mask,
+                            const uint16_t *dy, const float *dstate_out, float *dq, float *dk, float *dv,
+                            float *dg, float *dbeta, float *dstate_in, void *ws, cudaStream_t st);
+
 // Two-pass chunked form (prefill_chunk2.cu) for batches with fewer heads than
 // SMs: bytes of its workspace blobs, whether it is the faster form for these
 // sizes, and the launch (blobs: 16-byte aligned, prefill_two_pass_workspace

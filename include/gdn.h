@@ -261,6 +261,33 @@ GDN_API gdn_status gdn_prefill_noalloc(const gdn_dims *dims, const uint16_t *q, 
                                        const float *state_in, float *state_out, const uint8_t *mask,
                                        uint16_t *y, int chunk, gdn_stream stream);
 
+/* Backward pass of the recurrence (training): the gradients of y and of the
+ * final state with respect to q, k, v, g, beta and the initial state.  The
+ * pages define the forward step only (mlex gated_delta.rs, the per-timestep
+ * loop; mlx-bun qwen3-delta.ts, gated_delta_step); this is its exact
+ * derivative.  A masked step has zero gradients for its inputs and passes the
+ * state gradient through.  Sequential form, every step in f32.
+ *   q, k, v, g, beta, state_in, mask  as gdn_prefill (the forward inputs)
+ *   dy         bf16 [B, T, Hv, Dv] (in): gradient of y
+ *   dstate_out f32  [B, Hv, Dv, Dk] (in) or NULL (= 0): gradient of the final state
+ *   dq, dk     f32  [B, T, Hk, Dk] (out): summed over the Hv/Hk v-heads of each k-head
+ *   dv         f32  [B, T, Hv, Dv] (out)
+ *   dg, dbeta  f32  [B, T, Hv] (out)
+ *   dstate_in  f32  [B, Hv, Dv, Dk] (out): gradient of the initial state (also
+ *              when state_in is NULL); may equal dstate_out
+ *   workspace  device scratch of gdn_prefill_backward_workspace_size() bytes,
+ *              16-byte aligned (required when B * T > 0): checkpoints of the
+ *              forward state every 32 steps and a 32-step history per head
+ * The outputs are summed with atomics, so for Hv/Hk > 2 or Dv > 32 their
+ * last bits can differ between runs.  Supports Dk, Dv in {32, 64, 128}. */
+GDN_API size_t gdn_prefill_backward_workspace_size(const gdn_dims *dims);
+GDN_API gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
+                                        const uint16_t *v, const float *g, const float *beta,
+                                        const float *state_in, const uint8_t *mask, const uint16_t *dy,
+                                        const float *dstate_out, float *dq, float *dk, float *dv, float *dg,
+                                        float *dbeta, float *dstate_in, void *workspace, size_t ws_bytes,
+                                        gdn_stream stream);
+
 /* Bytes of the optional gdn_prefill workspace for these sizes and this chunk
  * mode (0 or 64): about 8 bytes per batch row, rounded up to 256.  Returns 0
  * for invalid or unsupported arguments. */

@@ -1,0 +1,73 @@
+"""Parity of the backward pass (gdn_prefill_backward) with the oracle's
+reverse pass, through the C ABI.  Tolerance: each gradient tensor within
+1e-3 relative L2 of the float64 oracle (the f32 state's bound: the reverse
+pass runs the same kind of f32 recurrence, backwards); masked steps exactly
+zero."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_linear_04_gb300 import workloads as wl
+from tests import _util as U
+from tests.test_gpu_parity import gdn, inputs_for, make_mask, np_mask, recurrence_inputs, to_dev  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+GRAD_REL_L2 = 1e-3
+
+BWD_CASES = [
+    # B, T, Hk, Hv, Dk, Dv, mask, state_in, dstate_out
+    (1, 40, 1, 1, 128, 128, None, True, True),
+    (2, 77, 1, 2, 128, 128, "random", True, False),
+    (1, 64, 2, 8, 64, 64, "right", False, True),
+    (3, 33, 1, 4, 32, 32, "blocks", True, True),
+    (2, 100, 2, 4, 128, 64, "allmasked_row", True, True),
+    (1, 130, 1, 1, 64, 128, "sparse", False, False),
+    (1, 1024, 1, 2, 128, 128, "random", True, True),     # long: error growth over many steps
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,Dk,Dv,mk,si,ds", BWD_CASES)
+def test_backward_matches_oracle(gdn, B, T, Hk, Hv, Dk, Dv, mk, si, ds):  # noqa: F811
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv)
+    mask = make_mask(mk, B, T, 31 + T)
+    r = recurrence_inputs(d, 3100 + T, mask)
+    gen = torch.Generator().manual_seed(77 + T)
+    dy = (torch.randn((B, T, Hv, Dv), generator=gen) * 0.1).to(torch.bfloat16)
+    dso = torch.randn((B, Hv, Dv, Dk), generator=gen) * 0.01 if ds else None
+    s_in = r["state"] if si else None
+    out = gdn.prefill_backward(d, to_dev(r["q"]), to_dev(r["k"]), to_dev(r["v"]), to_dev(r["g"]), to_dev(r["beta"]),
+                               to_dev(dy), state_in=to_dev(s_in), mask=to_dev(mask), dstate_out=to_dev(dso))
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    ref = oracle.recurrence_bwd(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                                r["beta"].numpy().astype(np.float64),
+                                None if s_in is None else s_in.numpy().astype(np.float64),
+                                U.bf16_dev_to_f64(dy), None if dso is None else dso.numpy().astype(np.float64),
+                                np_mask(mask))
+    for name, rname in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("dg", "dg"), ("dbeta", "dbeta"),
+                        ("dstate_in", "dstate_in")):
+        got = out[name].cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got)), name
+        if np.abs(ref[rname]).max() == 0.0:
+            assert np.all(got == 0.0), name
+            continue
+        U.assert_state_close(got, ref[rname], name, tol=GRAD_REL_L2)
+    if mask is not None:
+        off = mask.numpy() == 0
+        for name in ("dv", "dg", "dbeta"):
+            assert np.all(out[name].cpu().numpy()[off] == 0.0), name + ": masked steps must be zero"
+
+
+def test_backward_without_steps_passes_the_state_gradient(gdn):  # noqa: F811
+    d = wl.Dims(B=2, T=0, Hk=1, Hv=2, Dk=32, Dv=32)
+    dso = torch.randn((2, 2, 32, 32), generator=torch.Generator().manual_seed(3))
+    empty_bf = torch.empty((2, 0, 1, 32), dtype=torch.bfloat16, device="cuda:0")
+    out = gdn.prefill_backward(d, empty_bf, empty_bf, torch.empty((2, 0, 2, 32), dtype=torch.bfloat16,
+                                                                  device="cuda:0"),
+                               torch.empty((2, 0, 2), device="cuda:0"), torch.empty((2, 0, 2), device="cuda:0"),
+                               torch.empty((2, 0, 2, 32), dtype=torch.bfloat16, device="cuda:0"),
+                               dstate_out=to_dev(dso))
+    torch.cuda.synchronize()
+    assert torch.equal(out["dstate_in"].cpu(), dso)
