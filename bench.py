@@ -717,7 +717,7 @@ def main():
         "tokens_per_s": round(d.B * ws / (ms / 1e3), 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "algorithmic_bytes": alg_bytes, "kernel": "gdn::decode_kernel<128>",
+                     "algorithmic_bytes": alg_bytes, "kernel": "gdn::decode_kernel<128, false>",
                      "peak_source": peaks["source"]},
         "e2e": {"value": round(by["state_rw"] * ws / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
