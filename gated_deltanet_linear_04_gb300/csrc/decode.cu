@@ -68,16 +68,28 @@ struct ConvIn {
     uint16_t w[4];
 };
 
-__device__ __forceinline__ void load_conv(const DecodeParams &p, int b, int c, ConvIn &in) {
-    const int n = p.K - 1;
-    const uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
+// the taps (constant across steps) and the step's data, read separately so
+// that the taps can be fetched before the wait on the previous step's grid
+__device__ __forceinline__ void load_conv_w(const DecodeParams &p, int c, ConvIn &in) {
     const uint16_t *w = p.conv_w + (size_t)c * p.K;
-#pragma unroll
-    for (int j = 0; j < 3; ++j) in.prev[j] = j < n ? cs[(size_t)j * p.C] : (uint16_t)0;
-    in.xnew = p.qkv[(size_t)b * p.C + c];
 #pragma unroll
     for (int j = 0; j < 4; ++j) in.w[j] = j < p.K ? w[j] : (uint16_t)0;
 }
+
+__device__ __forceinline__ void load_conv_data(const DecodeParams &p, int b, int c, ConvIn &in) {
+    const int n = p.K - 1;
+    const uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) in.prev[j] = j < n ? cs[(size_t)j * p.C] : (uint16_t)0;
+    in.xnew = p.qkv[(size_t)b * p.C + c];
+}
+
+// Programmatic dependent launch: the next step's grid may be scheduled as
+// soon as every CTA of this one has started; it then waits (grid_dep_wait)
+// for this grid to finish and its writes to be visible before touching any
+// buffer this grid may write.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // conv over [stored rows, new] followed by SiLU; nw gets the shifted window
 // (the new conv_state rows).
@@ -114,6 +126,17 @@ __global__ void __launch_bounds__(kThreads, 6) decode_kernel(const DecodeParams 
     const int hv = hk * G + hv_local;
     const int r0 = slice * R;
     uint16_t *yrow = p.y + ((size_t)b * p.Hv + hv) * p.Dv + r0;
+    grid_dep_launch();
+
+    // before the wait: only the constant taps (and shared-memory set-up below)
+    const bool has_qk = tid < 2 * DK;
+    const int c_qk = tid < DK ? hk * DK + tid : p.Hk * DK + hk * DK + (tid - DK);
+    const bool has_v = tid < R;
+    const int c_v = 2 * p.Hk * DK + hv * p.Dv + r0 + tid;
+    ConvIn in_qk{}, in_v{};
+    if (has_qk) load_conv_w(p, c_qk, in_qk);
+    if (has_v) load_conv_w(p, c_v, in_v);
+    grid_dep_wait();
 
     if (p.row_mask != nullptr && p.row_mask[b] == 0) {
         // whole cluster shares b: every CTA leaves here, no barrier is pending
@@ -148,14 +171,9 @@ __global__ void __launch_bounds__(kThreads, 6) decode_kernel(const DecodeParams 
     // ---- conv + SiLU for the q/k channels of hk and the v channels of the slice
     uint16_t nw_qk[3] = {0, 0, 0}, nw_v[3] = {0, 0, 0};
     float xqk = 0.0f;
-    const bool has_qk = tid < 2 * DK;
-    const int c_qk = tid < DK ? hk * DK + tid : p.Hk * DK + hk * DK + (tid - DK);
-    const bool has_v = tid < R;
-    const int c_v = 2 * p.Hk * DK + hv * p.Dv + r0 + tid;
     // all raw conv inputs of both channels in flight before any arithmetic
-    ConvIn in_qk{}, in_v{};
-    if (has_qk) load_conv(p, b, c_qk, in_qk);
-    if (has_v) load_conv(p, b, c_v, in_v);
+    if (has_qk) load_conv_data(p, b, c_qk, in_qk);
+    if (has_v) load_conv_data(p, b, c_v, in_v);
     if (has_qk) xqk = conv_apply(p.K, in_qk, nw_qk);
     if (has_v) v_s[tid] = round_bf16(conv_apply(p.K, in_v, nw_v));
     // NORM: z and the weight of this thread's row, fetched now so that their
@@ -299,13 +317,15 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t st) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = G * p.SN;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, decode_kernel<DK, NORM>, p);
 }
 
