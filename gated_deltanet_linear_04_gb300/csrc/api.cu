@@ -295,6 +295,17 @@ gdn_status gdn_prefill_gated(const gdn_dims *dims, const uint16_t *q, const uint
                         workspace, ws_bytes, stream);
 }
 
+gdn_status gdn_selftest_timeout(gdn_stream stream) {
+    cudaStream_t cs = (cudaStream_t)stream;
+    gdn_status st = gdn_device_status(stream);       // start from a clear error word
+    if (st == GDN_ERR_CUDA) return st;
+    cudaError_t e = gdn::launch_selftest_timeout(gdn::error_word(), cs);
+    if (e != cudaSuccess) return gdn::from_cuda(e);
+    st = gdn_device_status(stream);
+    if (st != GDN_ERR_TIMEOUT) return st == GDN_OK ? GDN_ERR_CUDA : st;   // the timeout went unreported
+    return GDN_OK;
+}
+
 size_t gdn_prefill_backward_workspace_size(const gdn_dims *dims) {
     gdn::Sizes s;
     if (gdn::check_dims(dims, &s) != GDN_OK) return 0;

@@ -63,6 +63,9 @@ cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint
                                    const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
                                    const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st);
 
+// Failure-path self-test (selftest.cu): a kernel whose bounded wait runs out.
+cudaError_t launch_selftest_timeout(unsigned *err, cudaStream_t st);
+
 // Backward pass (backward.cu): workspace bytes and the launch (outputs zeroed
 // by the launch, then accumulated).
 size_t backward_workspace(const Sizes &s);

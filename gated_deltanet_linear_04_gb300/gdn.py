@@ -58,6 +58,7 @@ _SIGS = {
     "gdn_rmsnorm_gated": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, ctypes.c_float, _P, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_device_status": (ctypes.c_int, [_P]),
+    "gdn_selftest_timeout": (ctypes.c_int, [_P]),
     "gdn_abi_version": (ctypes.c_int, []),
 }
 
@@ -236,6 +237,10 @@ def gdn_prefill_vec(dims, q, k, v, g_vec, beta, state_in, state_out, mask, y, st
 
 def gdn_device_status(stream=None) -> int:
     return int(lib().gdn_device_status(_stream(stream)))
+
+
+def gdn_selftest_timeout(stream=None) -> int:
+    return int(lib().gdn_selftest_timeout(_stream(stream)))
 
 
 def gdn_abi_version() -> int:

@@ -302,6 +302,14 @@ GDN_API const char *gdn_status_string(gdn_status status);
  * GDN_ERR_CUDA if the synchronisation itself failed. */
 GDN_API gdn_status gdn_device_status(gdn_stream stream);
 
+/* Self-test of the failure path: launches a kernel whose bounded wait (on an
+ * mbarrier nothing arrives on) runs out after a few thousand probes, and
+ * checks that the error word reports it (GDN_ERR_TIMEOUT) and is cleared
+ * again.  Returns GDN_OK when the timeout was reported, GDN_ERR_CUDA when it
+ * was not (or the device failed).  No fault or unbounded wait is involved;
+ * the context stays usable. */
+GDN_API gdn_status gdn_selftest_timeout(gdn_stream stream);
+
 /* ABI version of this header (incremented on any signature change). */
 GDN_API int gdn_abi_version(void);
 

@@ -177,3 +177,19 @@ def test_guard_bands_around_every_output(gdn):
     assert gdn.gdn_device_status() == gdn.GDN_OK
     for buf, pad in bufs:
         assert intact(buf, pad)
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_context_survives(gdn):
+    # failure detection without a fault: a kernel waits on a barrier nothing
+    # arrives on, its bounded wait runs out, the error word reports it
+    assert gdn.gdn_selftest_timeout() == gdn.GDN_OK
+    assert gdn.gdn_device_status() == gdn.GDN_OK, "the error word is cleared once read"
+    # the context is still usable: an identity prefill leaves its state exact
+    d = wl.Dims(B=1, T=70, Hk=1, Hv=2, Dk=128, Dv=128)
+    q, k, v, st = _identity_inputs(d, 5)
+    g = torch.ones((d.B, d.T, d.Hv))
+    beta = torch.zeros((d.B, d.T, d.Hv))
+    y, s = gdn.prefill(d, dev(q), dev(k), dev(v), dev(g), dev(beta), dev(st), None, 64)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert torch.equal(s.cpu(), st)
