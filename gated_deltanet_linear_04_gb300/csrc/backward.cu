@@ -337,13 +337,9 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(const BwdParams p) {
 template <int DK>
 cudaError_t launch_bwd_t(const Sizes &s, const BwdParams &p, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem<DK>);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(backward_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static unsigned long long attr_done = 0;   // per instantiation, one bit per device
+    cudaError_t e = set_max_smem(attr_done, backward_kernel<DK>, smem);
+    if (e != cudaSuccess) return e;
     backward_kernel<DK><<<dim3(s.Dv / kRows, s.Hv, s.B), kThreads, smem, st>>>(p);
     return cudaGetLastError();
 }

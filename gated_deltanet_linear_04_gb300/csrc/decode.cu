@@ -303,15 +303,14 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t st) {
     const int G = p.Hv / p.Hk;
     const int R = p.Dv / p.SN;
     const size_t smem = (size_t)R * DK * sizeof(float);
-    static bool attr_set = false;   // per instantiation; benign race
-    if (!attr_set) {
+    static unsigned long long attr_done = 0;   // per instantiation, one bit per device
+    cudaError_t ae = once_per_device(attr_done, [] {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<DK, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)(kMaxRows * DK * sizeof(float)));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(decode_kernel<DK, NORM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+        return cudaFuncSetAttribute(decode_kernel<DK, NORM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    });
+    if (ae != cudaSuccess) return ae;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G * p.SN, p.Hk, p.B);
     cfg.blockDim = dim3(kThreads);

@@ -265,15 +265,14 @@ template <int DK, int K>
 cudaError_t launch_t(const WindowParams &p, cudaStream_t st) {
     const int G = p.Hv / p.Hk;
     const int R = p.Dv / p.SN;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static unsigned long long attr_done = 0;   // per instantiation, one bit per device
+    cudaError_t ae = once_per_device(attr_done, [] {
         cudaError_t e = cudaFuncSetAttribute(window_kernel<DK, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)(kMaxRows * DK * sizeof(float)));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(window_kernel<DK, K>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+        return cudaFuncSetAttribute(window_kernel<DK, K>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    });
+    if (ae != cudaSuccess) return ae;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G * p.SN, p.Hk, p.B);
     cfg.blockDim = dim3(kThreads);

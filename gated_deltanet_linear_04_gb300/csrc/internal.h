@@ -19,6 +19,31 @@ struct Sizes {
 
 int num_sms();  // SMs of the current device (cached per device)
 
+// Kernel attributes (dynamic shared memory, cluster size) belong to the
+// device context that was current when they were set, so a launcher applies
+// them once per device: `done` holds one bit per device ordinal (0..63; a
+// higher ordinal is set on every call).  Concurrent first calls may both run
+// `apply`, which is harmless.
+template <typename F>
+cudaError_t once_per_device(unsigned long long &done, F &&apply) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit != 0ull && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit) != 0ull) return cudaSuccess;
+    e = apply();
+    if (e == cudaSuccess && bit != 0ull) __atomic_fetch_or(&done, bit, __ATOMIC_RELEASE);
+    return e;
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device.
+template <typename K>
+cudaError_t set_max_smem(unsigned long long &done, K kernel, size_t bytes) {
+    return once_per_device(done, [&] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    });
+}
+
 cudaError_t launch_conv_update(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
                                const uint8_t *mask, uint16_t *q, uint16_t *k, uint16_t *v, cudaStream_t st);
 

@@ -385,14 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
 
 template <bool NORM>
 cudaError_t set_smem_attr() {
-    static bool attr_set = false;   // per instantiation; benign race
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel<NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    return cudaSuccess;
+    static unsigned long long attr_done = 0;   // per instantiation, one bit per device
+    return set_max_smem(attr_done, prefill_chunk_kernel<NORM>, kSmemBytes);
 }
 
 }  // namespace

@@ -522,16 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_overlap_kernel(const __grid
     cta_teardown(tmem, cols);
 }
 
-template <typename K>
-cudaError_t set_smem(K kernel, uint32_t bytes, bool &done) {
-    if (!done) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        if (e != cudaSuccess) return e;
-        done = true;
-    }
-    return cudaSuccess;
-}
-
 size_t blob_count(const Sizes &s) { return (size_t)s.B * s.Hv * (((size_t)s.T + kC - 1) / kC); }
 
 }  // namespace
@@ -557,10 +547,10 @@ cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uin
         !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    static bool set1 = false, set2 = false, set3 = false;
-    cudaError_t e = set_smem(chunk_prep_kernel, kP1Smem, set1);
-    if (e == cudaSuccess) e = set_smem(chunk_state_kernel, kP2Smem, set2);
-    if (e == cudaSuccess) e = set_smem(chunk_overlap_kernel, kFusedSmem, set3);
+    static unsigned long long set1 = 0, set2 = 0, set3 = 0;   // one bit per device
+    cudaError_t e = set_max_smem(set1, chunk_prep_kernel, kP1Smem);
+    if (e == cudaSuccess) e = set_max_smem(set2, chunk_state_kernel, kP2Smem);
+    if (e == cudaSuccess) e = set_max_smem(set3, chunk_overlap_kernel, kFusedSmem);
     if (e != cudaSuccess) return e;
     const int nchunks = (s.T + kC - 1) / kC;
     const int n_heads = s.B * s.Hv;

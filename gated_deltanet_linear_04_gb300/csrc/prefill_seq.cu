@@ -303,13 +303,9 @@ cudaError_t launch_seq_m(const Sizes &s, const uint16_t *q, const uint16_t *k, c
     } else {
         tg = tq;   // unused
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_seq_kernel<DK, RPL, VEC, MASKED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::total);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static unsigned long long attr_done = 0;   // per instantiation, one bit per device
+    cudaError_t ae = set_max_smem(attr_done, prefill_seq_kernel<DK, RPL, VEC, MASKED>, (size_t)L::total);
+    if (ae != cudaSuccess) return ae;
     dim3 grid(s.Hv * (s.Dv / R), s.B);
     prefill_seq_kernel<DK, RPL, VEC, MASKED><<<grid, kThreads, L::total, st>>>(tq, tk, tv, tg, p);
     return cudaGetLastError();
