@@ -44,6 +44,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kChunkRows = 32;
 constexpr int kMaxRows = 128;
+constexpr int kMinCtasPerSm = 6;   // launch bound: 40 registers, 6 CTAs of 32 KiB per SM
 
 struct DecodeParams {
     const uint16_t *qkv, *conv_w;
@@ -114,7 +115,7 @@ __device__ __forceinline__ float conv_apply(int K, const ConvIn &in, uint16_t (&
 }
 
 template <int DK, bool NORM>
-__global__ void __launch_bounds__(kThreads, 6) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm) decode_kernel(const DecodeParams p) {
     constexpr int LPR = DK / 4;       // lanes per state row (one float4 each)
     constexpr int RPP = 32 / LPR;     // rows per warp pass
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -324,7 +325,13 @@ cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t st) {
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    // Programmatic launch pays when the grid spans several waves (the next
+    // step's CTAs fill SMs as this grid's tail drains: 0.855 -> 0.868 of the
+    // HBM copy peak at B=128); a grid that fits in one resident wave gains
+    // nothing and its wait is slower than a plain graph edge (4.69 -> 5.73
+    // us per B=1 step in a CUDA graph), so it launches without it.
+    const long ctas = (long)cfg.gridDim.x * cfg.gridDim.y * cfg.gridDim.z;
+    cfg.numAttrs = ctas > (long)kMinCtasPerSm * num_sms() ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, decode_kernel<DK, NORM>, p);
 }
 
