@@ -13,13 +13,22 @@
 //
 // Same layout as the single-token kernel: a cluster per (b, hk) group of the
 // G v-heads x SN row slices, each CTA bulk-copies its R x Dk state slice into
-// shared memory while it computes the conv/norm/gates of the T tokens.  Eight
-// lanes walk a row through all T tokens with the row in registers (a warp
-// takes four rows at once, so a row's dot products are 3-level shuffle sums;
-// lane l holds the row's 16-byte column groups l, l + 8, ..., which keeps
-// each quarter-warp's shared-memory accesses on distinct banks); after token
-// keep-1 the row is written back to shared memory, so the slice stored at the
-// end is the state after the kept prefix (nothing is stored when keep is 0).
+// shared memory while it computes the conv/norm/gates of the T tokens.  A
+// CTA's life is a chain (inputs -> conv -> norm -> rows -> stores) with the
+// state copy hidden under its first links, and with several CTAs per SM the
+// links also compete for issue slots, so the chain is kept short: the conv
+// windows and taps are loaded at entry (the last warp computes the gates
+// while its loads are in flight), the new conv_state is taken from the window
+// already in registers, the token loops run branch-free to a compile-time
+// bound (4 or 8) over zero-padded tokens, the q/k normalisation factor is
+// formed once per (token, q or k), and each warp forms the k.q products it
+// needs itself.  Eight lanes walk a row through all
+// T tokens with the row in registers (a warp takes four rows at once, so a
+// row's dot products are 3-level shuffle sums; lane l holds the row's 16-byte
+// column groups l, l + 8, ..., which keeps each quarter-warp's shared-memory
+// accesses on distinct banks); after token keep-1 the row is written back to
+// shared memory, so the slice stored at the end is the state after the kept
+// prefix (nothing is stored when keep is 0).
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,6 +36,7 @@ namespace gdn {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 constexpr int kChunkRows = 32;
 constexpr int kMaxRows = 128;
 constexpr int kMaxT = 8;
@@ -44,52 +54,66 @@ struct WindowParams {
     float eps;
 };
 
-// SiLU(conv) of the T new tokens of channel c.  The window is held as
-// x[0 .. K-1) = the stored rows (oldest first) and x[K-1 + t] = token t, so
-// token t's taps j = 0 .. K-1 read x[t + j] (its own value on tap K-1).
-template <int K>
-__device__ __forceinline__ void conv_tokens(const WindowParams &p, int b, int c, float (&out)[kMaxT]) {
-    constexpr int n = K - 1;
-    float x[n + kMaxT];
-    const uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
-#pragma unroll
-    for (int j = 0; j < n; ++j) x[j] = bf16_to_f32(cs[(size_t)j * p.C]);
-#pragma unroll
-    for (int t = 0; t < kMaxT; ++t)
-        x[n + t] = t < p.T ? bf16_to_f32(p.qkv[((size_t)b * p.T + t) * p.C + c]) : 0.0f;
+// The conv window of channel c: x[0 .. K-1) = the stored rows (oldest
+// first), x[K-1 + t] = token t (zero past T), and its K taps, as f32 (bf16
+// widened exactly, so the top 16 bits are the bf16 bit pattern).
+template <int K, int TM>
+struct ConvWindow {
+    float x[K - 1 + TM];
     float w[K];
-#pragma unroll
-    for (int j = 0; j < K; ++j) w[j] = bf16_to_f32(p.conv_w[(size_t)c * K + j]);
-#pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
-        float u = 0.0f;
-#pragma unroll
-        for (int j = 0; j < K; ++j) u = fmaf(w[j], x[t + j], u);
-        out[t] = silu(u);
-    }
-}
 
-// conv_state of channel c after the first `keep` (>= 1) tokens: row j is
-// window entry keep + j, i.e. stored row keep + j while that is < K-1, else
-// token keep + j - (K-1).  Rows are written in increasing j, and row j reads
-// a stored row > j, so the rows it reads are still the old ones.
+    __device__ __forceinline__ void load(const WindowParams &p, int b, int c) {
+        constexpr int n = K - 1;
+        const uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
+#pragma unroll
+        for (int j = 0; j < n; ++j) x[j] = bf16_to_f32(cs[(size_t)j * p.C]);
+#pragma unroll
+        for (int t = 0; t < TM; ++t) x[n + t] = t < p.T ? bf16_to_f32(p.qkv[((size_t)b * p.T + t) * p.C + c]) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) w[j] = bf16_to_f32(p.conv_w[(size_t)c * K + j]);
+    }
+
+    // SiLU(conv) of tokens t < TM: taps j = 0 .. K-1 read x[t + j] (the
+    // token's own value on tap K-1).
+    __device__ __forceinline__ void conv_silu(float (&out)[TM]) const {
+#pragma unroll
+        for (int t = 0; t < TM; ++t) {
+            float u = 0.0f;
+#pragma unroll
+            for (int j = 0; j < K; ++j) u = fmaf(w[j], x[t + j], u);
+            out[t] = silu(u);
+        }
+    }
+
+    // conv_state rows after the first `keep` (0 .. TM) tokens: row j is
+    // window entry keep + j, reached by shifting the rows one entry per kept
+    // token (constant indices only, so the window stays in registers).
+    __device__ __forceinline__ void new_conv_rows(int keep, uint16_t (&rows)[K - 1]) const {
+        float r[K - 1];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) r[j] = x[j];
+#pragma unroll
+        for (int s = 0; s < TM; ++s)
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j) r[j] = s < keep ? x[s + 1 + j] : r[j];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) rows[j] = (uint16_t)(__float_as_uint(r[j]) >> 16);
+    }
+};
+
 template <int K>
-__device__ __forceinline__ void write_conv_state(const WindowParams &p, int b, int c, int keep) {
-    constexpr int n = K - 1;
-    uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
+__device__ __forceinline__ void store_conv_rows(const WindowParams &p, int b, int c, const uint16_t (&rows)[K - 1]) {
+    uint16_t *cs = p.conv_state + (size_t)b * (K - 1) * p.C + c;
 #pragma unroll
-    for (int j = 0; j < n; ++j) {
-        const int pos = keep + j;
-        const uint16_t v = pos < n ? cs[(size_t)pos * p.C] : p.qkv[((size_t)b * p.T + (pos - n)) * p.C + c];
-        cs[(size_t)j * p.C] = v;
-    }
+    for (int j = 0; j < K - 1; ++j) cs[(size_t)j * p.C] = rows[j];
 }
 
-template <int DK, int K>
+template <int DK, int K, int TM>
 __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams p) {
     constexpr int LPR = 8;             // lanes per row
     constexpr int RPP = 32 / LPR;      // rows per warp pass
     constexpr int NG = DK / 4 / LPR;   // 16-byte column groups per lane
+    constexpr int NW = DK / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.Hv / p.Hk;
     const int R = p.Dv / p.SN;
@@ -104,12 +128,14 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float *S = reinterpret_cast<float *>(smem_raw);
-    __shared__ __align__(16) float q_s[kMaxT][DK];
-    __shared__ __align__(16) float k_s[kMaxT][DK];
-    __shared__ float v_s[kMaxT][kMaxRows];
-    __shared__ float y_s[kMaxT][kMaxRows];
-    __shared__ float red[kMaxT][kThreads / 32];
-    __shared__ float gq[kMaxT][3];                 // g, beta, k.q per token
+    __shared__ __align__(16) float q_s[TM][DK];
+    __shared__ __align__(16) float k_s[TM][DK];
+    __shared__ float v_s[TM][kMaxRows];
+    __shared__ float y_s[TM][kMaxRows];
+    __shared__ float red[TM][kWarps];
+    __shared__ float gb_s[TM][2];                  // g, beta per token
+    __shared__ float fac_s[TM][2];                 // q and k normalisation factor per token
+    __shared__ float kq_s[kWarps][TM];             // k.q per token, one copy per warp
     __shared__ __align__(8) uint64_t bars[kMaxRows / kChunkRows];
 
     const int rc = min(R, kChunkRows);
@@ -126,65 +152,83 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
         }
     }
 
-    // ---- conv + SiLU of the T tokens: q/k channels of hk, v channels of the slice
+    // ---- every input load first: the q/k and v conv windows
     const bool has_qk = tid < 2 * DK;
     const int c_qk = tid < DK ? hk * DK + tid : p.Hk * DK + hk * DK + (tid - DK);
     const bool has_v = tid < R;
     const int c_v = 2 * p.Hk * DK + hv * p.Dv + r0 + tid;
-    float xqk[kMaxT];
+    ConvWindow<K, TM> wqk, wv;
+    if (has_qk) wqk.load(p, b, c_qk);
+    if (has_v) wv.load(p, b, c_v);
+    // the gates, on the last warp while its conv window is in flight
+    if (warp == kWarps - 1 && lane < T) {
+        const size_t gi = ((size_t)b * T + lane) * p.Hv + hv;
+        const float x = bf16_to_f32(p.a[gi]) + p.dt_bias[hv];
+        gb_s[lane][0] = expf(-expf(p.A_log[hv]) * softplus(x));
+        gb_s[lane][1] = sigmoid(bf16_to_f32(p.b[gi]));
+    }
+
+    // ---- conv + SiLU (tokens past T are zero throughout, so every token
+    // loop below runs to TM without a branch); the v channels' conv_state is
+    // this CTA's alone and is rewritten at once, the q/k channels' (read by
+    // the whole cluster) by rank 0 at the end
+    float xqk[TM];
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) xqk[t] = 0.0f;
-    if (has_qk) conv_tokens<K>(p, b, c_qk, xqk);
-    if (has_v) {
-        float xv[kMaxT];
-        conv_tokens<K>(p, b, c_v, xv);
-#pragma unroll
-        for (int t = 0; t < kMaxT; ++t)
-            if (t < T) v_s[t][tid] = round_bf16(xv[t]);
+    for (int t = 0; t < TM; ++t) xqk[t] = 0.0f;
+    uint16_t qk_rows[K - 1];
+    if (has_qk) {
+        wqk.conv_silu(xqk);
+        if (keep > 0) wqk.new_conv_rows(keep, qk_rows);
     }
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t)
+    for (int t = 0; t < TM; ++t)
         if (t >= T) xqk[t] = 0.0f;
-    cluster_arrive_relaxed();      // the shared q/k conv_state has been read
+    if (has_v) {
+        float xv[TM];
+        wv.conv_silu(xv);
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) {
-        if (t < T) {
-            const float ss = warp_sum(xqk[t] * xqk[t]);
-            if (lane == 0) red[t][warp] = ss;
+        for (int t = 0; t < TM; ++t) v_s[t][tid] = t < T ? round_bf16(xv[t]) : 0.0f;
+        if (keep > 0) {
+            uint16_t rows[K - 1];
+            wv.new_conv_rows(keep, rows);
+            store_conv_rows<K>(p, b, c_v, rows);
         }
     }
-    if (tid < T) {
-        const size_t gi = ((size_t)b * T + tid) * p.Hv + hv;
-        const float x = bf16_to_f32(p.a[gi]) + p.dt_bias[hv];
-        gq[tid][0] = expf(-expf(p.A_log[hv]) * softplus(x));
-        gq[tid][1] = sigmoid(bf16_to_f32(p.b[gi]));
+    cluster_arrive_relaxed();      // the shared q/k conv_state has been read
+
+    // ---- q/k normalisation: sums of squares 32 channels per warp, one
+    // factor per (token, q or k), then each channel scaled and rounded
+#pragma unroll
+    for (int t = 0; t < TM; ++t) {
+        const float ss = warp_sum(xqk[t] * xqk[t]);
+        if (lane == 0) red[t][warp] = ss;
+    }
+    __syncthreads();
+    if (tid < 2 * TM) {
+        const int t = tid >> 1, part = tid & 1;
+        const float inv_d = 1.0f / (float)DK;
+        float tot = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) tot += red[t][part * NW + w];
+        fac_s[t][part] = (1.0f / sqrtf(tot * inv_d + p.eps)) * (part ? 1.0f / sqrtf((float)DK) : inv_d);
     }
     __syncthreads();
     if (has_qk) {
-        constexpr int NW = DK / 32;
-        const bool is_q = tid < DK;
-        const float inv_d = 1.0f / (float)DK;
-        const float scale = is_q ? inv_d : 1.0f / sqrtf((float)DK);
+        const int part = tid >= DK;
+        float *dst = part ? &k_s[0][tid - DK] : &q_s[0][tid];
 #pragma unroll
-        for (int t = 0; t < kMaxT; ++t) {
-            if (t < T) {
-                float tot = 0.0f;
-#pragma unroll
-                for (int w = 0; w < NW; ++w) tot += red[t][(is_q ? 0 : NW) + w];
-                const float val = round_bf16(xqk[t] * ((1.0f / sqrtf(tot * inv_d + p.eps)) * scale));
-                if (is_q) q_s[t][tid] = val;
-                else k_s[t][tid - DK] = val;
-            }
-        }
+        for (int t = 0; t < TM; ++t) dst[t * DK] = round_bf16(xqk[t] * fac_s[t][part]);
     }
     __syncthreads();
-    if (warp < T) {
+#pragma unroll
+    for (int t = 0; t < TM; ++t) {
         float kq = 0.0f;
-        for (int i = lane; i < DK; i += 32) kq = fmaf(k_s[warp][i], q_s[warp][i], kq);
+#pragma unroll
+        for (int i = lane; i < DK; i += 32) kq = fmaf(k_s[t][i], q_s[t][i], kq);
         kq = warp_sum(kq);
-        if (lane == 0) gq[warp][2] = kq;
+        if (lane == 0) kq_s[warp][t] = kq;
     }
-    __syncthreads();
+    __syncwarp();
 
     // ---- rows through the window
     const int sub = lane / LPR, cl = lane % LPR;
@@ -193,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[ch], 0, p.err));
         ok_all = ok_all && ok;
         if (!ok) continue;
-        for (int rr = warp * RPP + sub; rr < rc; rr += (kThreads / 32) * RPP) {
+        for (int rr = warp * RPP + sub; rr < rc; rr += kWarps * RPP) {
             const int row = ch * rc + rr;
             float4 *sp = reinterpret_cast<float4 *>(S + (size_t)row * DK);
             float4 s[NG];
@@ -202,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
             for (int t = 0; t < T; ++t) {
                 const float4 *k4 = reinterpret_cast<const float4 *>(k_s[t]);
                 const float4 *q4 = reinterpret_cast<const float4 *>(q_s[t]);
-                const float g = gq[t][0], beta = gq[t][1], kq = gq[t][2];
+                const float g = gb_s[t][0], beta = gb_s[t][1], kq = kq_s[warp][t];
                 float dk0 = 0.0f, dk1 = 0.0f, dq0 = 0.0f, dq1 = 0.0f;
 #pragma unroll
                 for (int j = 0; j < NG; ++j) {
@@ -251,26 +295,23 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
             p.y[(((size_t)b * T + t) * p.Hv + hv) * p.Dv + r0 + r] = f32_to_bf16(y_s[t][r]);
         }
 
-    // ---- conv_state after the kept prefix: rank 0 writes the shared q/k
-    // channels once every CTA of the cluster has read them
+    // ---- q/k conv_state after the kept prefix: rank 0 writes it once every
+    // CTA of the cluster has read it
     cluster_wait_acquire();
-    if (keep > 0) {
-        if (has_qk && rank == 0) write_conv_state<K>(p, b, c_qk, keep);
-        if (has_v) write_conv_state<K>(p, b, c_v, keep);
-    }
+    if (keep > 0 && has_qk && rank == 0) store_conv_rows<K>(p, b, c_qk, qk_rows);
     if (tid == 0) bulk_wait_read();   // the slice has been read out of shared memory
 }
 
-template <int DK, int K>
+template <int DK, int K, int TM>
 cudaError_t launch_t(const WindowParams &p, cudaStream_t st) {
     const int G = p.Hv / p.Hk;
     const int R = p.Dv / p.SN;
     static unsigned long long attr_done = 0;   // per instantiation, one bit per device
     cudaError_t ae = once_per_device(attr_done, [] {
-        cudaError_t e = cudaFuncSetAttribute(window_kernel<DK, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(window_kernel<DK, K, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)(kMaxRows * DK * sizeof(float)));
         if (e != cudaSuccess) return e;
-        return cudaFuncSetAttribute(window_kernel<DK, K>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return cudaFuncSetAttribute(window_kernel<DK, K, TM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     });
     if (ae != cudaSuccess) return ae;
     cudaLaunchConfig_t cfg = {};
@@ -285,7 +326,13 @@ cudaError_t launch_t(const WindowParams &p, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, window_kernel<DK, K>, p);
+    return cudaLaunchKernelEx(&cfg, window_kernel<DK, K, TM>, p);
+}
+
+// Token loops are unrolled to 4 for windows of up to 4 tokens, else to 8.
+template <int DK, int K>
+cudaError_t launch_tm(const WindowParams &p, cudaStream_t st) {
+    return p.T <= 4 ? launch_t<DK, K, 4>(p, st) : launch_t<DK, K, kMaxT>(p, st);
 }
 
 }  // namespace
@@ -301,15 +348,15 @@ cudaError_t launch_decode_window(const Sizes &s, const uint16_t *qkv, const uint
     WindowParams p{qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep, y, err,
                    s.B, s.T, s.Hk, s.Hv, s.Dv, s.C(), s.K, SN, s.eps};
     switch (s.Dk * 8 + s.K) {
-        case 32 * 8 + 2: return launch_t<32, 2>(p, st);
-        case 32 * 8 + 3: return launch_t<32, 3>(p, st);
-        case 32 * 8 + 4: return launch_t<32, 4>(p, st);
-        case 64 * 8 + 2: return launch_t<64, 2>(p, st);
-        case 64 * 8 + 3: return launch_t<64, 3>(p, st);
-        case 64 * 8 + 4: return launch_t<64, 4>(p, st);
-        case 128 * 8 + 2: return launch_t<128, 2>(p, st);
-        case 128 * 8 + 3: return launch_t<128, 3>(p, st);
-        case 128 * 8 + 4: return launch_t<128, 4>(p, st);
+        case 32 * 8 + 2: return launch_tm<32, 2>(p, st);
+        case 32 * 8 + 3: return launch_tm<32, 3>(p, st);
+        case 32 * 8 + 4: return launch_tm<32, 4>(p, st);
+        case 64 * 8 + 2: return launch_tm<64, 2>(p, st);
+        case 64 * 8 + 3: return launch_tm<64, 3>(p, st);
+        case 64 * 8 + 4: return launch_tm<64, 4>(p, st);
+        case 128 * 8 + 2: return launch_tm<128, 2>(p, st);
+        case 128 * 8 + 3: return launch_tm<128, 3>(p, st);
+        case 128 * 8 + 4: return launch_tm<128, 4>(p, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -597,6 +597,8 @@ WINDOW_CASES = [
     (1, 1, 16, 32, 128, 2, 1, [1]),
     (4, 2, 8, 128, 64, 4, 7, [7, 0, 1, 6]),
     (2, 1, 2, 32, 32, 3, 3, [1, 3]),          # keep < K-1: a kept row comes from the old conv_state
+    (2, 2, 6, 64, 64, 3, 4, [4, 2]),          # G = 3: clusters of 6 CTAs, uneven q/k channel shares
+    (1, 1, 16, 32, 32, 4, 6, [5]),            # clusters of 16 CTAs, 4 q/k channels each
 ]
 
 
