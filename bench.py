@@ -248,61 +248,38 @@ def bench_decode(gdn, w: wl.Workload, steps: int, warmup: int, dev, sampler) -> 
     if gdn.gdn_device_status() != gdn.GDN_OK:
         raise RuntimeError("device error word set during the decode benchmark")
 
-    # end to end through the public API: every step copies its inputs from
-    # pinned host memory and reads its y back to pinned host memory.  As a
-    # serving loop would, the copies run on their own streams, double-buffered
-    # and ordered by events, so step i+1's inputs travel while step i computes.
-    nbuf = 2
-    y_h = [torch.empty((d.B, d.Hv, d.Dv), dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
-    qkv_d = [torch.empty_like(qkv[0]) for _ in range(nbuf)]
-    a_d = [torch.empty_like(a[0]) for _ in range(nbuf)]
-    b_d = [torch.empty_like(b[0]) for _ in range(nbuf)]
-    y_d = [torch.empty_like(y) for _ in range(nbuf)]
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
-    ev_done = [torch.cuda.Event() for _ in range(nbuf)]
-    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
-    for k in range(nbuf):          # every event starts in the completed state
-        ev_done[k].record(stream)
-        ev_out[k].record(stream)
+    # end to end through the C ABI with host buffers: every step's inputs are
+    # copied in from pinned host memory and its y copied back out inside
+    # gdn_recurrent_decode_host_steps, which double-buffers them in a device
+    # staging area on its own copy streams, so step i+1's inputs travel while
+    # step i computes, as a serving loop would.
+    staging = torch.empty(gdn.gdn_decode_host_staging_size(d1), dtype=torch.uint8, device=dev)
+    y_h = torch.empty((n_in, d.B, d.Hv, d.Dv), dtype=torch.bfloat16).pin_memory()
 
-    def e2e_step(i):
-        j, k = i % n_in, i % nbuf
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(ev_done[k])            # step i-2 has finished reading slot k
-            qkv_d[k].copy_(qkv_h[j], non_blocking=True)
-            a_d[k].copy_(a_h[j], non_blocking=True)
-            b_d[k].copy_(b_h[j], non_blocking=True)
-            ev_in[k].record(s_in)
-        stream.wait_event(ev_in[k])
-        stream.wait_event(ev_out[k])                # y slot k has been read back
-        gdn.gdn_recurrent_decode(d1, qkv_d[k], conv_w, conv_state, a_d[k], b_d[k], A_log, dt_bias, state, None,
-                                 y_d[k], stream)
-        ev_done[k].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_done[k])
-            y_h[k].copy_(y_d[k], non_blocking=True)
-            ev_out[k].record(s_out)
+    def e2e_run(first, n):
+        done = 0
+        while done < n:
+            j = (first + done) % n_in
+            m = min(n - done, n_in - j)
+            gdn.gdn_recurrent_decode_host_steps(d1, m, qkv_h[j:j + m], a_h[j:j + m], b_h[j:j + m], y_h[j:j + m],
+                                                conv_w, conv_state, A_log, dt_bias, state, None, staging, stream)
+            done += m
 
-    for i in range(warmup):
-        e2e_step(i)
+    e2e_run(0, warmup)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall = time.perf_counter()
     e0.record(stream)
-    s_in.wait_stream(stream)
-    s_out.wait_stream(stream)
-    for i in range(steps):
-        e2e_step(i)
-    for k in range(nbuf):
-        stream.wait_event(ev_out[k])
+    e2e_run(warmup, steps)
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the end-to-end decode benchmark")
     e2e_ms = max(e0.elapsed_time(e1), t_wall * 1e3) / steps
-    qkv_d, a_d, b_d, y_h = qkv_d[0], a_d[0], b_d[0], y_h[0]
+    per_step = (d.B * d1.C, d.B * d.Hv, d.B * d.Hv * d.Dv)
     return {"ms": ms, "e2e_ms": e2e_ms,
-            "h2d": qkv_d.numel() * 2 + a_d.numel() * 2 + b_d.numel() * 2, "d2h": y_h.numel() * 2}
+            "h2d": per_step[0] * 2 + 2 * per_step[1] * 2, "d2h": per_step[2] * 2}
 
 
 def bench_decode_small(gdn, w: wl.Workload, dev, reps: int = 3) -> dict:

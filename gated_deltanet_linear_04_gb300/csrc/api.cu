@@ -228,6 +228,112 @@ gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qkv, const
                                              nullptr, nullptr, 0.0f, gdn::error_word(), (cudaStream_t)stream));
 }
 
+namespace {
+
+// One staging slot of gdn_recurrent_decode_host_steps: byte offsets of qkv,
+// a, b and y (each 256-byte aligned) and the slot size.
+struct HostSlot {
+    size_t qkv, a, b, y, bytes;
+};
+
+HostSlot host_slot(const gdn::Sizes &s) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    HostSlot h;
+    h.qkv = 0;
+    h.a = up((size_t)s.B * s.C() * 2);
+    h.b = h.a + up((size_t)s.B * s.Hv * 2);
+    h.y = h.b + up((size_t)s.B * s.Hv * 2);
+    h.bytes = h.y + up((size_t)s.B * s.Hv * s.Dv * 2);
+    return h;
+}
+
+}  // namespace
+
+size_t gdn_decode_host_staging_size(const gdn_dims *dims) {
+    gdn::Sizes s;
+    if (gdn::check_dims(dims, &s) != GDN_OK || s.T != 1) return 0;
+    return 2 * host_slot(s).bytes;
+}
+
+gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, const uint16_t *qkv_h,
+                                           const uint16_t *a_h, const uint16_t *b_h, uint16_t *y_h,
+                                           const uint16_t *conv_w, uint16_t *conv_state, const float *A_log,
+                                           const float *dt_bias, float *state, const uint8_t *row_mask,
+                                           void *staging, size_t staging_bytes, gdn_stream stream) {
+    gdn::Sizes s;
+    gdn_status st = gdn::check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    if (s.T != 1 || n_steps < 0) return GDN_ERR_INVALID_ARG;
+    if (s.Hv / s.Hk > 16) return GDN_ERR_UNSUPPORTED;
+    const size_t B = (size_t)s.B;
+    if (n_steps == 0 || B == 0) return GDN_OK;
+    if (qkv_h == nullptr || a_h == nullptr || b_h == nullptr || y_h == nullptr) return GDN_ERR_INVALID_ARG;
+    if (!ok_ptr(conv_w, B) || !ok_ptr(conv_state, B) || !ok_ptr(A_log, B) || !ok_ptr(dt_bias, B) ||
+        !ok_ptr(state, B) || !ok_ptr(row_mask, 0) || !ok_ptr(staging, B))
+        return GDN_ERR_INVALID_ARG;
+    const HostSlot h = host_slot(s);
+    if (staging_bytes < 2 * h.bytes) return GDN_ERR_INVALID_ARG;
+    const size_t nq = B * s.C(), na = B * s.Hv, ny = B * s.Hv * s.Dv;   // elements per step
+
+    cudaStream_t main = (cudaStream_t)stream, cin = nullptr, cout = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_done[2] = {}, ev_out[2] = {};
+    cudaError_t e = cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+        e = cudaEventCreateWithFlags(&ev_in[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_done[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_out[k], cudaEventDisableTiming);
+    }
+    // the copy streams start after everything already on `stream`; both slots
+    // start free (their "done" and "out" events complete at that point)
+    if (e == cudaSuccess) e = cudaEventRecord(ev_start, main);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev_start, 0);
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+        e = cudaEventRecord(ev_done[k], main);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_out[k], main);
+    }
+    for (int i = 0; i < n_steps && e == cudaSuccess; ++i) {
+        const int k = i & 1;
+        char *slot = static_cast<char *>(staging) + (size_t)k * h.bytes;
+        uint16_t *qkv_d = reinterpret_cast<uint16_t *>(slot + h.qkv);
+        uint16_t *a_d = reinterpret_cast<uint16_t *>(slot + h.a);
+        uint16_t *b_d = reinterpret_cast<uint16_t *>(slot + h.b);
+        uint16_t *y_d = reinterpret_cast<uint16_t *>(slot + h.y);
+        // step i's inputs, once step i-2 has finished reading the slot
+        e = cudaStreamWaitEvent(cin, ev_done[k], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(qkv_d, qkv_h + (size_t)i * nq, nq * 2, cudaMemcpyHostToDevice, cin);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(a_d, a_h + (size_t)i * na, na * 2, cudaMemcpyHostToDevice, cin);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(b_d, b_h + (size_t)i * na, na * 2, cudaMemcpyHostToDevice, cin);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_in[k], cin);
+        // the step, once its inputs are in and step i-2's y has left the slot
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(main, ev_in[k], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(main, ev_out[k], 0);
+        if (e == cudaSuccess)
+            e = gdn::launch_decode(s, qkv_d, conv_w, conv_state, a_d, b_d, A_log, dt_bias, state, row_mask, y_d,
+                                   nullptr, nullptr, 0.0f, gdn::error_word(), main);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_done[k], main);
+        // step i's y back to the host
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev_done[k], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(y_h + (size_t)i * ny, y_d, ny * 2, cudaMemcpyDeviceToHost, cout);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_out[k], cout);
+    }
+    // `stream` completes after the last y has arrived
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(main, ev_out[k], 0);
+    // streams and events are released once their pending work completes
+    for (int k = 0; k < 2; ++k) {
+        if (ev_in[k]) cudaEventDestroy(ev_in[k]);
+        if (ev_done[k]) cudaEventDestroy(ev_done[k]);
+        if (ev_out[k]) cudaEventDestroy(ev_out[k]);
+    }
+    if (ev_start) cudaEventDestroy(ev_start);
+    if (cin) cudaStreamDestroy(cin);
+    if (cout) cudaStreamDestroy(cout);
+    return gdn::from_cuda(e);
+}
+
 gdn_status gdn_recurrent_decode_gated(const gdn_dims *dims, const uint16_t *qkv, const uint16_t *conv_w,
                                       uint16_t *conv_state, const uint16_t *a, const uint16_t *b,
                                       const float *A_log, const float *dt_bias, float *state,

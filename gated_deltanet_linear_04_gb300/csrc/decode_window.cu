@@ -20,11 +20,11 @@
 // windows and taps are loaded at entry (the last warp computes the gates
 // while its loads are in flight), the new conv_state is taken from the window
 // already in registers, the token loops run branch-free to a compile-time
-// bound (4 or 8) over zero-padded tokens, the q/k normalisation factor is
-// formed once per (token, q or k), and each warp forms the k.q products it
-// needs itself.  Eight lanes walk a row through all
-// T tokens with the row in registers (a warp takes four rows at once, so a
-// row's dot products are 3-level shuffle sums; lane l holds the row's 16-byte
+// bound (4 or 8) over zero-padded tokens, and the q/k normalisation factor
+// is formed once per (token, q or k).  Eight lanes walk a row through all T
+// tokens with the row in registers: S_{t-1} k, the update, then y = S_t q
+// (each lane group carries two rows at once and a warp eight, so a row's dot
+// products are 3-level shuffle sums; lane l holds the row's 16-byte
 // column groups l, l + 8, ..., which keeps each quarter-warp's shared-memory
 // accesses on distinct banks); after token keep-1 the row is written back to
 // shared memory, so the slice stored at the end is the state after the kept
@@ -108,8 +108,11 @@ __device__ __forceinline__ void store_conv_rows(const WindowParams &p, int b, in
     for (int j = 0; j < K - 1; ++j) cs[(size_t)j * p.C] = rows[j];
 }
 
+// Four CTAs per SM (64 registers) except for loops to 6 tokens, which ran
+// their conv phase 2.5x slower at that bound and measured best at three
+// (T = 5: 182 -> 149 us at B=128; loops to 8 measured best at four).
 template <int DK, int K, int TM>
-__global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams p) {
+__global__ void __launch_bounds__(kThreads, TM == 6 ? 3 : 4) window_kernel(const WindowParams p) {
     constexpr int LPR = 8;             // lanes per row
     constexpr int RPP = 32 / LPR;      // rows per warp pass
     constexpr int NG = DK / 4 / LPR;   // 16-byte column groups per lane
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
     __shared__ float red[TM][kWarps];
     __shared__ float gb_s[TM][2];                  // g, beta per token
     __shared__ float fac_s[TM][2];                 // q and k normalisation factor per token
-    __shared__ float kq_s[kWarps][TM];             // k.q per token, one copy per warp
+    __shared__ uint16_t qk_rows_s[K - 1][2 * DK];  // new q/k conv_state rows, stored by rank 0 at the end
     __shared__ __align__(8) uint64_t bars[kMaxRows / kChunkRows];
 
     const int rc = min(R, kChunkRows);
@@ -175,10 +178,14 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
     float xqk[TM];
 #pragma unroll
     for (int t = 0; t < TM; ++t) xqk[t] = 0.0f;
-    uint16_t qk_rows[K - 1];
     if (has_qk) {
         wqk.conv_silu(xqk);
-        if (keep > 0) wqk.new_conv_rows(keep, qk_rows);
+        if (keep > 0) {
+            uint16_t rows[K - 1];
+            wqk.new_conv_rows(keep, rows);
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j) qk_rows_s[j][tid] = rows[j];
+        }
     }
 #pragma unroll
     for (int t = 0; t < TM; ++t)
@@ -220,65 +227,87 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
         for (int t = 0; t < TM; ++t) dst[t * DK] = round_bf16(xqk[t] * fac_s[t][part]);
     }
     __syncthreads();
-#pragma unroll
-    for (int t = 0; t < TM; ++t) {
-        float kq = 0.0f;
-#pragma unroll
-        for (int i = lane; i < DK; i += 32) kq = fmaf(k_s[t][i], q_s[t][i], kq);
-        kq = warp_sum(kq);
-        if (lane == 0) kq_s[warp][t] = kq;
-    }
-    __syncwarp();
 
-    // ---- rows through the window
+    // ---- rows through the window: each group of eight lanes carries two
+    // rows (RPP apart), two independent chains sharing the k / q loads
     const int sub = lane / LPR, cl = lane % LPR;
     bool ok_all = true;
-    for (int ch = 0; ch < nch; ++ch) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[ch], 0, p.err));
+    for (int p0 = warp * 2 * RPP; p0 < R; p0 += kWarps * 2 * RPP) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[p0 / rc], 0, p.err));
         ok_all = ok_all && ok;
         if (!ok) continue;
-        for (int rr = warp * RPP + sub; rr < rc; rr += kWarps * RPP) {
-            const int row = ch * rc + rr;
-            float4 *sp = reinterpret_cast<float4 *>(S + (size_t)row * DK);
-            float4 s[NG];
+        const int ra = p0 + sub, rb = ra + RPP;
+        float4 *spa = reinterpret_cast<float4 *>(S + (size_t)ra * DK);
+        float4 *spb = reinterpret_cast<float4 *>(S + (size_t)rb * DK);
+        float4 sa[NG], sb[NG];
 #pragma unroll
-            for (int j = 0; j < NG; ++j) s[j] = sp[j * LPR + cl];
-            for (int t = 0; t < T; ++t) {
-                const float4 *k4 = reinterpret_cast<const float4 *>(k_s[t]);
-                const float4 *q4 = reinterpret_cast<const float4 *>(q_s[t]);
-                const float g = gb_s[t][0], beta = gb_s[t][1], kq = kq_s[warp][t];
-                float dk0 = 0.0f, dk1 = 0.0f, dq0 = 0.0f, dq1 = 0.0f;
+        for (int j = 0; j < NG; ++j) {
+            sa[j] = spa[j * LPR + cl];
+            sb[j] = spb[j * LPR + cl];
+        }
+        for (int t = 0; t < T; ++t) {
+            const float4 *k4 = reinterpret_cast<const float4 *>(k_s[t]);
+            const float4 *q4 = reinterpret_cast<const float4 *>(q_s[t]);
+            const float g = gb_s[t][0], beta = gb_s[t][1];
+            // S_{t-1} k, then S_t = g S_{t-1} + delta k^T, then y = S_t q
+            float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < NG; ++j) {
+                const float4 kk = k4[j * LPR + cl];
+                a0 = fmaf(sa[j].x, kk.x, a0);
+                a1 = fmaf(sa[j].y, kk.y, a1);
+                a0 = fmaf(sa[j].z, kk.z, a0);
+                a1 = fmaf(sa[j].w, kk.w, a1);
+                b0 = fmaf(sb[j].x, kk.x, b0);
+                b1 = fmaf(sb[j].y, kk.y, b1);
+                b0 = fmaf(sb[j].z, kk.z, b0);
+                b1 = fmaf(sb[j].w, kk.w, b1);
+            }
+            float dka = a0 + a1, dkb = b0 + b1;
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) {
+                dka += __shfl_xor_sync(0xffffffffu, dka, o);
+                dkb += __shfl_xor_sync(0xffffffffu, dkb, o);
+            }
+            const float da = beta * (v_s[t][ra] - g * dka);
+            const float db = beta * (v_s[t][rb] - g * dkb);
+            a0 = a1 = b0 = b1 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < NG; ++j) {
+                const float4 kk = k4[j * LPR + cl];
+                sa[j].x = fmaf(da, kk.x, g * sa[j].x);
+                sa[j].y = fmaf(da, kk.y, g * sa[j].y);
+                sa[j].z = fmaf(da, kk.z, g * sa[j].z);
+                sa[j].w = fmaf(da, kk.w, g * sa[j].w);
+                sb[j].x = fmaf(db, kk.x, g * sb[j].x);
+                sb[j].y = fmaf(db, kk.y, g * sb[j].y);
+                sb[j].z = fmaf(db, kk.z, g * sb[j].z);
+                sb[j].w = fmaf(db, kk.w, g * sb[j].w);
+                const float4 qq = q4[j * LPR + cl];
+                a0 = fmaf(sa[j].x, qq.x, a0);
+                a1 = fmaf(sa[j].y, qq.y, a1);
+                a0 = fmaf(sa[j].z, qq.z, a0);
+                a1 = fmaf(sa[j].w, qq.w, a1);
+                b0 = fmaf(sb[j].x, qq.x, b0);
+                b1 = fmaf(sb[j].y, qq.y, b1);
+                b0 = fmaf(sb[j].z, qq.z, b0);
+                b1 = fmaf(sb[j].w, qq.w, b1);
+            }
+            float dqa = a0 + a1, dqb = b0 + b1;
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) {
+                dqa += __shfl_xor_sync(0xffffffffu, dqa, o);
+                dqb += __shfl_xor_sync(0xffffffffu, dqb, o);
+            }
+            if (cl == 0) {
+                y_s[t][ra] = dqa;
+                y_s[t][rb] = dqb;
+            }
+            if (t == keep - 1) {              // the state after the kept prefix
 #pragma unroll
                 for (int j = 0; j < NG; ++j) {
-                    const float4 kk = k4[j * LPR + cl], qq = q4[j * LPR + cl];
-                    dk0 = fmaf(s[j].x, kk.x, dk0);
-                    dk1 = fmaf(s[j].y, kk.y, dk1);
-                    dk0 = fmaf(s[j].z, kk.z, dk0);
-                    dk1 = fmaf(s[j].w, kk.w, dk1);
-                    dq0 = fmaf(s[j].x, qq.x, dq0);
-                    dq1 = fmaf(s[j].y, qq.y, dq1);
-                    dq0 = fmaf(s[j].z, qq.z, dq0);
-                    dq1 = fmaf(s[j].w, qq.w, dq1);
-                }
-                float dk = dk0 + dk1, dq = dq0 + dq1;
-#pragma unroll
-                for (int o = LPR / 2; o > 0; o >>= 1) {
-                    dk += __shfl_xor_sync(0xffffffffu, dk, o);
-                    dq += __shfl_xor_sync(0xffffffffu, dq, o);
-                }
-                const float delta = beta * (v_s[t][row] - g * dk);
-#pragma unroll
-                for (int j = 0; j < NG; ++j) {
-                    const float4 kk = k4[j * LPR + cl];
-                    s[j].x = fmaf(delta, kk.x, g * s[j].x);
-                    s[j].y = fmaf(delta, kk.y, g * s[j].y);
-                    s[j].z = fmaf(delta, kk.z, g * s[j].z);
-                    s[j].w = fmaf(delta, kk.w, g * s[j].w);
-                }
-                if (cl == 0) y_s[t][row] = fmaf(delta, kq, g * dq);
-                if (t == keep - 1) {              // the state after the kept prefix
-#pragma unroll
-                    for (int j = 0; j < NG; ++j) sp[j * LPR + cl] = s[j];
+                    spa[j * LPR + cl] = sa[j];
+                    spb[j * LPR + cl] = sb[j];
                 }
             }
         }
@@ -298,7 +327,12 @@ __global__ void __launch_bounds__(kThreads, 4) window_kernel(const WindowParams 
     // ---- q/k conv_state after the kept prefix: rank 0 writes it once every
     // CTA of the cluster has read it
     cluster_wait_acquire();
-    if (keep > 0 && has_qk && rank == 0) store_conv_rows<K>(p, b, c_qk, qk_rows);
+    if (keep > 0 && has_qk && rank == 0) {
+        uint16_t rows[K - 1];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) rows[j] = qk_rows_s[j][tid];
+        store_conv_rows<K>(p, b, c_qk, rows);
+    }
     if (tid == 0) bulk_wait_read();   // the slice has been read out of shared memory
 }
 
@@ -329,10 +363,15 @@ cudaError_t launch_t(const WindowParams &p, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, window_kernel<DK, K, TM>, p);
 }
 
-// Token loops are unrolled to 4 for windows of up to 4 tokens, else to 8.
+// Token loops run to the smallest of 2, 4, 6, 8 that holds the window (work
+// on padded tokens is not free: a 4-token window with loops to 8 measured
+// 172 vs 118 us at B=128).
 template <int DK, int K>
 cudaError_t launch_tm(const WindowParams &p, cudaStream_t st) {
-    return p.T <= 4 ? launch_t<DK, K, 4>(p, st) : launch_t<DK, K, kMaxT>(p, st);
+    if (p.T <= 2) return launch_t<DK, K, 2>(p, st);
+    if (p.T <= 4) return launch_t<DK, K, 4>(p, st);
+    if (p.T <= 6) return launch_t<DK, K, 6>(p, st);
+    return launch_t<DK, K, kMaxT>(p, st);
 }
 
 }  // namespace

@@ -55,6 +55,9 @@ _SIGS = {
     "gdn_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(GdnDims)] + [ctypes.c_void_p] * 9 +
                             [ctypes.c_int, ctypes.c_void_p]),
     "gdn_decode_window": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gdn_recurrent_decode_host_steps": (ctypes.c_int, [ctypes.POINTER(GdnDims), ctypes.c_int] + [_P] * 11 +
+                                        [ctypes.c_size_t, _P]),
+    "gdn_decode_host_staging_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims)]),
     "gdn_rmsnorm_gated": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, ctypes.c_float, _P, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_device_status": (ctypes.c_int, [_P]),
@@ -96,6 +99,19 @@ def _ptr(t: Optional[torch.Tensor], dtype: torch.dtype, name: str):
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if t.numel() > 0 and not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr() or None
+
+
+def _host_ptr(t: torch.Tensor, dtype: torch.dtype, name: str):
+    """A contiguous CPU tensor's address (page-locked ones copy asynchronously)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.is_cuda:
+        raise ValueError("%s must be a host (CPU) tensor" % name)
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     return t.data_ptr() or None
@@ -150,6 +166,35 @@ def gdn_decode_window(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state
                                    _ptr(A_log, F32, "A_log"), _ptr(dt_bias, F32, "dt_bias"),
                                    _ptr(state, F32, "state"), _ptr(keep, torch.int32, "keep"), _ptr(y, BF16, "y"),
                                    _stream(stream)), "gdn_decode_window")
+
+
+def gdn_decode_host_staging_size(dims) -> int:
+    d = make_dims(dims)
+    return int(lib().gdn_decode_host_staging_size(ctypes.byref(d)))
+
+
+def gdn_recurrent_decode_host_steps(dims, n_steps, qkv_h, a_h, b_h, y_h, conv_w, conv_state, A_log, dt_bias, state,
+                                    row_mask, staging, stream=None):
+    d = make_dims(dims)
+    n = int(n_steps)
+    for name, t, shape in (("qkv_h", qkv_h, (n, dims.B, d.Hk * d.Dk * 2 + d.Hv * d.Dv)),
+                           ("a_h", a_h, (n, dims.B, d.Hv)), ("b_h", b_h, (n, dims.B, d.Hv)),
+                           ("y_h", y_h, (n, dims.B, d.Hv, d.Dv))):
+        if tuple(t.shape[:len(shape)]) != shape or t.numel() != _numel(shape):
+            raise ValueError("%s must have shape %s, got %s" % (name, shape, tuple(t.shape)))
+    _check(lib().gdn_recurrent_decode_host_steps(
+        ctypes.byref(d), n, _host_ptr(qkv_h, BF16, "qkv_h"), _host_ptr(a_h, BF16, "a_h"),
+        _host_ptr(b_h, BF16, "b_h"), _host_ptr(y_h, BF16, "y_h"), _ptr(conv_w, BF16, "conv_w"),
+        _ptr(conv_state, BF16, "conv_state"), _ptr(A_log, F32, "A_log"), _ptr(dt_bias, F32, "dt_bias"),
+        _ptr(state, F32, "state"), _ptr(row_mask, U8, "row_mask"), _ptr(staging, torch.uint8, "staging"),
+        staging.numel(), _stream(stream)), "gdn_recurrent_decode_host_steps")
+
+
+def _numel(shape) -> int:
+    n = 1
+    for x in shape:
+        n *= x
+    return n
 
 
 def gdn_prefill_workspace_size(dims, chunk: int) -> int:
@@ -272,6 +317,21 @@ def recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state,
     y = torch.empty((dims.B, dims.Hv, dims.Dv), dtype=BF16, device=qkv.device)
     gdn_recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y, stream)
     return y
+
+
+def recurrent_decode_host_steps(dims, qkv_h, a_h, b_h, conv_w, conv_state, A_log, dt_bias, state, row_mask=None,
+                                y_h=None, staging=None, stream=None):
+    """len(qkv_h) decode steps with inputs in host memory ([n, B, ...], pinned
+    for overlapped copies); conv_state and state advance in place.  Returns
+    the host tensor y_h [n, B, Hv, Dv], valid once `stream` has completed."""
+    n = qkv_h.shape[0]
+    if y_h is None:
+        y_h = torch.empty((n, dims.B, dims.Hv, dims.Dv), dtype=BF16).pin_memory()
+    if staging is None:
+        staging = torch.empty(gdn_decode_host_staging_size(dims), dtype=torch.uint8, device=conv_state.device)
+    gdn_recurrent_decode_host_steps(dims, n, qkv_h, a_h, b_h, y_h, conv_w, conv_state, A_log, dt_bias, state,
+                                    row_mask, staging, stream)
+    return y_h
 
 
 def decode_window(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep=None, stream=None):

@@ -114,6 +114,39 @@ GDN_API gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qk
                                 const float *A_log, const float *dt_bias, float *state,
                                 const uint8_t *row_mask, uint16_t *y, gdn_stream stream);
 
+/* Decode steps fed from and returned to host memory: n_steps consecutive
+ * tokens of gdn_recurrent_decode (same arithmetic, same kernel), with each
+ * step's inputs copied in from host buffers and its y copied out to a host
+ * buffer inside the call, as a serving loop does.  (Same definitions as
+ * gdn_recurrent_decode.)
+ *   qkv_h      bf16 [n_steps, B, C]       host (in), step i's qkv at row i
+ *   a_h, b_h   bf16 [n_steps, B, Hv]      host (in)
+ *   y_h        bf16 [n_steps, B, Hv, Dv]  host (out)
+ *   conv_w, conv_state, A_log, dt_bias, state, row_mask: device, as in
+ *              gdn_recurrent_decode (row_mask applies to every step)
+ *   staging    device workspace of gdn_decode_host_staging_size(dims) bytes,
+ *              16-byte aligned: two slots of qkv, a, b and y, so that step
+ *              i+1's inputs travel and step i-1's y returns while step i runs
+ * Host buffers should be page-locked (cudaHostAlloc / pinned): pageable
+ * memory is accepted but its copies do not overlap the kernels.  The copies
+ * run on two streams created for the call (cudaMemcpyAsync, one per tensor
+ * and step) and ordered against `stream` with events; everything is enqueued
+ * before the call returns and `stream` completes after the last y has
+ * arrived, so synchronise `stream` before reading y_h.  Neither host buffer
+ * may be written (inputs) or read (y_h) before that.  n_steps = 0 is a no-op.
+ * Errors: GDN_ERR_INVALID_ARG for a bad argument or a short staging buffer,
+ * GDN_ERR_CUDA for a failed CUDA call (work already enqueued still runs). */
+GDN_API gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, const uint16_t *qkv_h,
+                                                   const uint16_t *a_h, const uint16_t *b_h, uint16_t *y_h,
+                                                   const uint16_t *conv_w, uint16_t *conv_state,
+                                                   const float *A_log, const float *dt_bias, float *state,
+                                                   const uint8_t *row_mask, void *staging, size_t staging_bytes,
+                                                   gdn_stream stream);
+
+/* Bytes of device staging gdn_recurrent_decode_host_steps needs (0 for bad
+ * dims). */
+GDN_API size_t gdn_decode_host_staging_size(const gdn_dims *dims);
+
 /* gdn_recurrent_decode followed by the layer's RMSNormGated.  The norm runs
  * in the decode kernel's epilogue when one CTA holds all Dv rows of a head
  * (for example Hv/Hk = 16 or Dv = 32 with few heads); when a head's rows are

@@ -105,3 +105,24 @@ def test_prefill_chunk_argument(lib):
     assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 64) == n0
     assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 32) == 0
     assert lib.gdn_prefill_workspace_size(ctypes.byref(_dims(B=0)), 0) == 0
+
+
+def test_decode_host_steps_staging_and_validation(lib):
+    d = _dims(B=3, T=1)
+    # two slots of qkv, a, b and y, each array rounded up to whole 256 bytes
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    C = 2 * d.Hk * d.Dk + d.Hv * d.Dv
+    n = lib.gdn_decode_host_staging_size(ctypes.byref(d))
+    assert n == 2 * (up(d.B * C * 2) + 2 * up(d.B * d.Hv * 2) + up(d.B * d.Hv * d.Dv * 2))
+    assert lib.gdn_decode_host_staging_size(ctypes.byref(_dims(T=2))) == 0
+    f = lib.gdn_recurrent_decode_host_steps
+    none = [None] * 11
+    assert f(ctypes.byref(d), -1, *none, 0, None) == 1            # negative step count
+    assert f(ctypes.byref(_dims(T=2)), 1, *none, 0, None) == 1    # steps are single tokens
+    assert f(ctypes.byref(d), 0, *none, 0, None) == 0             # no steps: nothing to do
+    assert f(ctypes.byref(d), 3, *none, 0, None) == 1             # null host buffers
+    # every pointer present and aligned, staging one byte short: rejected on
+    # the host before any CUDA call
+    buf = ctypes.create_string_buffer(4096)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert f(ctypes.byref(d), 3, *([p] * 11), n - 1, None) == 1
