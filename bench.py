@@ -588,6 +588,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="only the headline decode (no other sections)")
     ap.add_argument("--parts", default="decode_b1,rmsnorm,window,decode_gated,prefill,backward",
                     help="comma-separated sections to run after the headline decode")
+    ap.add_argument("--backward-workloads", default="prefill_t8192,prefill_ragged",
+                    help="workloads of the backward section (a subset keeps an ncu capture small)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -657,7 +659,7 @@ def main():
         decode_gated = bench_decode_gated(gdn, w, dev)
     backward = None
     if "backward" in parts:
-        backward = [bench_backward(gdn, wl.WORKLOADS[name], dev) for name in ("prefill_t8192", "prefill_ragged")]
+        backward = [bench_backward(gdn, wl.WORKLOADS[name], dev) for name in args.backward_workloads.split(",")]
     if "prefill" in parts:
         for name in ("prefill_t8192", "prefill_ragged"):
             for chunk in (0, 64):
