@@ -127,13 +127,6 @@ __device__ __forceinline__ float row_sum(float x) {
     return x;
 }
 
-// sum over the 4 row groups of a warp (lanes differing in bits 3-4)
-__device__ __forceinline__ float col_sum(float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 8);
-    x += __shfl_xor_sync(0xffffffffu, x, 16);
-    return x;
-}
-
 template <int DK>
 __global__ void __launch_bounds__(kThreads) backward_kernel(const BwdParams p) {
     constexpr int CW = DK / 8;
@@ -286,17 +279,27 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(const BwdParams p) {
                         dS[i][j] *= gg;
                     }
                 }
+                // sum the 2*CW partials (dq, dk) over the warp's four row
+                // groups in two exchanges that halve the vector: lanes whose
+                // rg differs in bit 0 swap halves (dq <-> dk), then lanes whose
+                // rg differs in bit 1 swap quarters, so each lane ends with
+                // CW/2 summed columns (of dq for even rg, dk for odd) and adds
+                // those; the pairwise sums are those of a per-column shuffle sum
+                const bool hi0 = (rg & 1) != 0, hi1 = (rg & 2) != 0;
+                float h[CW];
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
-                    dq_p[j] = col_sum(dq_p[j]);
-                    dk_p[j] = col_sum(dk_p[j]);
+                    const float send = hi0 ? dq_p[j] : dk_p[j];
+                    const float keep = hi0 ? dk_p[j] : dq_p[j];
+                    h[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
                 }
-                if (rg == 0) {
+                constexpr int HQ = CW / 2;
+                float *dst = (hi0 ? &s.red_k[tl][c0] : &s.red_q[tl][c0]) + (hi1 ? HQ : 0);
 #pragma unroll
-                    for (int j = 0; j < CW; ++j) {
-                        atomicAdd(&s.red_q[tl][c0 + j], dq_p[j]);
-                        atomicAdd(&s.red_k[tl][c0 + j], dk_p[j]);
-                    }
+                for (int j = 0; j < HQ; ++j) {
+                    const float send = hi1 ? h[j] : h[HQ + j];
+                    const float keep = hi1 ? h[HQ + j] : h[j];
+                    atomicAdd(dst + j, keep + __shfl_xor_sync(0xffffffffu, send, 16));
                 }
                 dg_p = warp_sum(dg_p);
                 db_p = warp_sum(db_p);
