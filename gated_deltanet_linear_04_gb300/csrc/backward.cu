@@ -14,18 +14,28 @@
 //   dg_t = <dS', S_{t-1}>       dS_{t-1} = g_t dS'
 // A masked step has zero gradients for its inputs and passes dS through.
 //
-// Work split: a CTA (4 warps) owns 32 state rows of one (b, hv) head; lane
-// (rg, cg) of warp w holds rows w*8 + rg*2 + {0, 1} and columns
-// [cg*Dk/8, (cg+1)*Dk/8), so a row's dot product is a 3-level shuffle sum over
-// the 8 lanes sharing rg.  The rows of the state evolve independently, so
-// the slice first runs the forward recurrence storing its rows every 32 steps
-// (checkpoints), then walks the chunks of 32 steps backwards: it recomputes
-// the chunk's states from the checkpoint into a history buffer (global memory,
-// L2-resident) keeping u per row, and runs the reverse steps with dS in
-// registers.  The sums over rows (dq, dk, dg, dbeta) are reduced within the
-// warp, collected per step in shared memory and added to the outputs with
-// atomics once per chunk; the atomics also sum over the row slices and over
-// the v-heads that share a k-head.  The call zeroes the outputs first.
+// The rows of S (and of dS) evolve independently, and the dS recursion
+// (dS += dy q^T, du = beta dS k, dS = g (dS - du k^T)) needs neither S nor v.
+// So the work splits into two launches:
+//  1. sweeps, one CTA (4 warps) per 32 state rows of a head and direction:
+//     the forward sweep stores S at the start of every 64-step span, the
+//     reverse sweep stores dS at the end of every span (and dS of the
+//     initial state, the output dstate_in); the two run side by side.
+//  2. spans, every (row slice, head, span) independently on a fixed grid of
+//     CTAs that each own a 32-step history buffer: from the span's S and dS
+//     it recomputes the span's first half to the middle, then for each half,
+//     last first, recomputes the half's states into the history buffer
+//     (global memory, L2-resident), keeping u per row in shared memory, and
+//     runs the full reverse steps with dS in registers.
+// Lane (rg, cg) of warp w holds rows w*8 + rg*2 + {0, 1} and columns
+// [cg*Dk/8, (cg+1)*Dk/8), so a row's dot product is a 3-level shuffle sum
+// over the 8 lanes sharing rg.  The sums over rows (dq, dk, dg, dbeta) are
+// reduced within the warp, collected per step in shared memory and added to
+// the outputs with atomics once per half-span; the atomics also sum over the
+// row slices and over the v-heads that share a k-head.  The call zeroes the
+// outputs first.  Where the row slices alone fill the GPU (two or more per
+// SM) the split buys no parallelism and costs the second sweep, so one
+// launch runs both sweeps per slice instead (checkpoints every half-span).
 #include "common.cuh"
 #include "internal.h"
 
@@ -34,7 +44,8 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kRows = 32;        // state rows per CTA
-constexpr int kC = 32;           // steps per chunk / checkpoint interval
+constexpr int kC = 32;           // steps per staged half-span (history length)
+constexpr int kSpan = 2 * kC;    // steps per span (checkpoint interval)
 
 struct BwdParams {
     const uint16_t *q, *k, *v;
@@ -43,8 +54,10 @@ struct BwdParams {
     const uint16_t *dy;
     const float *dstate_out;
     float *dq, *dk, *dv, *dg, *dbeta, *dstate_in;
-    float *ws;
-    int B, T, Hk, Hv, Dv, nck;
+    float *ck;      // S at the start of every span   [B, Hv, slices, nspan, kRows, Dk]
+    float *dck;     // dS at the end of every span    [B, Hv, slices, nspan, kRows, Dk]
+    float *hist;    // one [kC, kRows, Dk] history per span-kernel CTA
+    int B, T, Hk, Hv, Dv, nck, nspan;
 };
 
 template <int DK>
@@ -127,233 +140,423 @@ __device__ __forceinline__ float row_sum(float x) {
     return x;
 }
 
+// The two rows and Dk/8 columns of the state that one lane holds: rows
+// rl[0], rl[1] of the CTA's slice and the 16-byte column groups cg, cg + 8,
+// ... (element j at column col(j)), so the eight column lanes of a row read a
+// staged q / k row as 8 consecutive 16-byte words, free of bank conflicts.
 template <int DK>
-__global__ void __launch_bounds__(kThreads) backward_kernel(const BwdParams p) {
-    constexpr int CW = DK / 8;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    BwdSmem<DK> &s = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int rg = lane >> 3, cg = lane & 7;
-    const int slice = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
-    const int hk = hv / (p.Hv / p.Hk);
-    const int r0 = slice * kRows;
-    const int T = p.T;
-    const int c0 = cg * CW;
-    int rl[2];
-    rl[0] = warp * 8 + rg * 2;
-    rl[1] = rl[0] + 1;
-    const size_t head = (size_t)b * p.Hv + hv;
-    // this CTA's checkpoints [nck][kRows][DK] and chunk history [kC][kRows][DK]
-    const size_t cta = head * (p.Dv / kRows) + slice;
-    float *ck = p.ws + cta * (size_t)(p.nck + kC) * kRows * DK;
-    float *hist = ck + (size_t)p.nck * kRows * DK;
+struct Lanes {
+    static constexpr int CW = DK / 8;
+    int lane, rg, cg, rl[2];
 
-    auto load_rows = [&](const float *src, float (&x)[2][CW]) {   // src: [kRows][DK]
+    __device__ __forceinline__ Lanes() {
+        lane = threadIdx.x & 31;
+        rg = lane >> 3;
+        cg = lane & 7;
+        rl[0] = (int)(threadIdx.x >> 5) * 8 + rg * 2;
+        rl[1] = rl[0] + 1;
+    }
+    __device__ __forceinline__ int col(int j) const { return ((cg + 8 * (j >> 2)) << 2) + (j & 3); }
+    __device__ __forceinline__ void load(const float *src, float (&x)[2][CW]) const {   // src: [kRows][DK]
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < CW; j += 4) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(src + (size_t)rl[i] * DK + c0 + j);
+                const float4 v4 = *reinterpret_cast<const float4 *>(src + (size_t)rl[i] * DK + col(j));
                 x[i][j] = v4.x; x[i][j + 1] = v4.y; x[i][j + 2] = v4.z; x[i][j + 3] = v4.w;
             }
-    };
-    auto store_rows = [&](float *dst, const float (&x)[2][CW]) {
+    }
+    __device__ __forceinline__ void store(float *dst, const float (&x)[2][CW]) const {
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int j = 0; j < CW; j += 4)
-                *reinterpret_cast<float4 *>(dst + (size_t)rl[i] * DK + c0 + j) =
+                *reinterpret_cast<float4 *>(dst + (size_t)rl[i] * DK + col(j)) =
                     make_float4(x[i][j], x[i][j + 1], x[i][j + 2], x[i][j + 3]);
-    };
-    // one forward step of the two rows from the staged chunk; returns u per row
-    auto fwd_step = [&](float (&S)[2][CW], int tl, float (&u)[2]) {
-        const float gg = s.g[tl], bb = s.beta[tl];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            float kv = 0.0f;
-#pragma unroll
-            for (int j = 0; j < CW; ++j) kv = fmaf(S[i][j], s.k[tl][c0 + j], kv);
-            kv = gg * row_sum(kv);
-            u[i] = s.v[tl][rl[i]] - kv;
-            const float dl = bb * u[i];
-#pragma unroll
-            for (int j = 0; j < CW; ++j) S[i][j] = fmaf(dl, s.k[tl][c0 + j], gg * S[i][j]);
+    }
+    // the slice of a [Dv, DK] head array (or zeros for a null one)
+    __device__ __forceinline__ void load_or_zero(const float *src, float (&x)[2][CW]) const {
+        if (src != nullptr) {
+            load(src, x);
+            return;
         }
-    };
-
-    float S[2][CW];
-    if (p.state_in != nullptr) {
-        load_rows(p.state_in + (head * p.Dv + r0) * DK, S);
-    } else {
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int j = 0; j < CW; ++j) S[i][j] = 0.0f;
+            for (int j = 0; j < CW; ++j) x[i][j] = 0.0f;
     }
+};
 
-    // ---- forward sweep: checkpoint every kC steps
+// One forward step of the lane's two rows from the staged chunk; returns u
+// per row.
+template <int DK>
+__device__ __forceinline__ void fwd_step(const BwdSmem<DK> &s, const Lanes<DK> &L, float (&S)[2][DK / 8], int tl,
+                                         float (&u)[2]) {
+    constexpr int CW = DK / 8;
+    const float gg = s.g[tl], bb = s.beta[tl];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float kv = 0.0f;
+#pragma unroll
+        for (int j = 0; j < CW; ++j) kv = fmaf(S[i][j], s.k[tl][L.col(j)], kv);
+        kv = gg * row_sum(kv);
+        u[i] = s.v[tl][L.rl[i]] - kv;
+        const float dl = bb * u[i];
+#pragma unroll
+        for (int j = 0; j < CW; ++j) S[i][j] = fmaf(dl, s.k[tl][L.col(j)], gg * S[i][j]);
+    }
+}
+
+// One reverse step of dS alone: dS += dy q^T, ddelta = dS k, du = beta
+// ddelta, dS = g (dS - du k^T), in the operation order of the full reverse
+// step below, so both give the same dS bit for bit.
+template <int DK>
+__device__ __forceinline__ void dS_step(const BwdSmem<DK> &s, const Lanes<DK> &L, float (&dS)[2][DK / 8], int tl) {
+    constexpr int CW = DK / 8;
+    const float gg = s.g[tl], bb = s.beta[tl];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float dyv = s.dy[tl][L.rl[i]];
+        float dd = 0.0f;
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+            dS[i][j] = fmaf(dyv, s.q[tl][L.col(j)], dS[i][j]);
+            dd = fmaf(dS[i][j], s.k[tl][L.col(j)], dd);
+        }
+        dd = row_sum(dd);
+        const float du = bb * dd;
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+            dS[i][j] = fmaf(-du, s.k[tl][L.col(j)], dS[i][j]);
+            dS[i][j] *= gg;
+        }
+    }
+}
+
+// The full reverse over the half-span of kC steps at t0 (at least one valid
+// step): S is the state before it (clobbered), dS the gradient of the state
+// after it, returned as the gradient of the state before it.  Recomputes the
+// half-span's states into `hist` ([kC][kRows][DK]) and adds its gradients
+// to the outputs.  Block-wide.
+template <int DK>
+__device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s, const Lanes<DK> &L, float *hist,
+                                          int b, int hk, int hv, int r0, int t0, float (&S)[2][DK / 8],
+                                          float (&dS)[2][DK / 8]) {
+    constexpr int CW = DK / 8;
+    const int tid = threadIdx.x;
+    const int T = p.T;
+    stage_chunk<DK>(p, s, b, hk, hv, r0, t0, true);
+    for (int i = tid; i < kC * DK; i += kThreads) {
+        (&s.red_q[0][0])[i] = 0.0f;
+        (&s.red_k[0][0])[i] = 0.0f;
+    }
+    if (tid < kC) {
+        s.red_g[tid] = 0.0f;
+        s.red_b[tid] = 0.0f;
+    }
+    // recompute the half-span: hist[tl] = the state before step tl
+    for (int tl = 0; tl < kC; ++tl) {
+        L.store(hist + (size_t)tl * kRows * DK, S);
+        if (!s.m[tl]) continue;
+        float u[2];
+        fwd_step<DK>(s, L, S, tl, u);
+        if (L.cg == 0) {
+            s.u[tl][L.rl[0]] = u[0];
+            s.u[tl][L.rl[1]] = u[1];
+        }
+    }
+    __syncthreads();
+    // S is now the state after the half-span; walk it backwards, the state
+    // before each step read from the history one step ahead
+    float Sp[2][CW];
+    L.load(hist + (size_t)(kC - 1) * kRows * DK, Sp);
+    for (int tl = kC - 1; tl >= 0; --tl) {
+        float Sn[2][CW];   // S_{t-2}, for the next reverse step
+        if (tl > 0) L.load(hist + (size_t)(tl - 1) * kRows * DK, Sn);
+        if (s.m[tl]) {
+            const float gg = s.g[tl], bb = s.beta[tl];
+            float dq_p[CW], dk_p[CW];
+#pragma unroll
+            for (int j = 0; j < CW; ++j) dq_p[j] = dk_p[j] = 0.0f;
+            float dg_p = 0.0f, db_p = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float dyv = s.dy[tl][L.rl[i]];
+                const float ui = s.u[tl][L.rl[i]];
+                float dd = 0.0f;
+#pragma unroll
+                for (int j = 0; j < CW; ++j) {
+                    dS[i][j] = fmaf(dyv, s.q[tl][L.col(j)], dS[i][j]);
+                    dq_p[j] = fmaf(S[i][j], dyv, dq_p[j]);
+                    dd = fmaf(dS[i][j], s.k[tl][L.col(j)], dd);
+                }
+                dd = row_sum(dd);                       // ddelta of the row
+                const float dl = bb * ui;               // delta
+                const float du = bb * dd;
+                if (L.cg == 0) {
+                    db_p = fmaf(dd, ui, db_p);
+                    p.dv[(((size_t)b * T + t0 + tl) * p.Hv + hv) * p.Dv + r0 + L.rl[i]] = du;
+                }
+#pragma unroll
+                for (int j = 0; j < CW; ++j) {
+                    dk_p[j] = fmaf(dS[i][j], dl, dk_p[j]);
+                    dS[i][j] = fmaf(-du, s.k[tl][L.col(j)], dS[i][j]);
+                    dk_p[j] = fmaf(-gg * Sp[i][j], du, dk_p[j]);
+                    dg_p = fmaf(dS[i][j], Sp[i][j], dg_p);
+                    dS[i][j] *= gg;
+                }
+            }
+            // sum the 2*CW partials (dq, dk) over the warp's four row
+            // groups in two exchanges that halve the vector: lanes whose
+            // rg differs in bit 0 swap halves (dq <-> dk), then lanes whose
+            // rg differs in bit 1 swap quarters, so each lane ends with
+            // CW/2 summed columns (of dq for even rg, dk for odd) and adds
+            // those; the pairwise sums are those of a per-column shuffle sum
+            const bool hi0 = (L.rg & 1) != 0, hi1 = (L.rg & 2) != 0;
+            float h[CW];
+#pragma unroll
+            for (int j = 0; j < CW; ++j) {
+                const float send = hi0 ? dq_p[j] : dk_p[j];
+                const float keep = hi0 ? dk_p[j] : dq_p[j];
+                h[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+            constexpr int HQ = CW / 2;
+            float *dst = hi0 ? &s.red_k[tl][0] : &s.red_q[tl][0];
+            const int off = hi1 ? HQ : 0;
+#pragma unroll
+            for (int j = 0; j < HQ; ++j) {
+                const float send = hi1 ? h[j] : h[HQ + j];
+                const float keep = hi1 ? h[HQ + j] : h[j];
+                atomicAdd(dst + L.col(off + j), keep + __shfl_xor_sync(0xffffffffu, send, 16));
+            }
+            dg_p = warp_sum(dg_p);
+            db_p = warp_sum(db_p);
+            if (L.lane == 0) {
+                atomicAdd(&s.red_g[tl], dg_p);
+                atomicAdd(&s.red_b[tl], db_p);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < CW; ++j) {
+                S[i][j] = Sp[i][j];
+                Sp[i][j] = Sn[i][j];
+            }
+    }
+    __syncthreads();
+    // add the half-span's sums to the outputs (also summing over row slices
+    // and over the v-heads of the k-head)
+    const int n = min(kC, T - t0);
+    for (int i = tid; i < n * DK; i += kThreads) {
+        const int tl = i / DK, j = i % DK;
+        if (!s.m[tl]) continue;
+        const size_t o = (((size_t)b * T + t0 + tl) * p.Hk + hk) * DK + j;
+        atomicAdd(p.dq + o, s.red_q[tl][j]);
+        atomicAdd(p.dk + o, s.red_k[tl][j]);
+    }
+    if (tid < n && s.m[tid]) {
+        const size_t o = ((size_t)b * T + t0 + tid) * p.Hv + hv;
+        atomicAdd(p.dg + o, s.red_g[tid]);
+        atomicAdd(p.dbeta + o, s.red_b[tid]);
+    }
+    __syncthreads();
+}
+
+// Launch 1: per (row slice, head) a forward-sweep CTA (blockIdx.x < slices)
+// storing S at the start of every span, and a reverse-sweep CTA storing dS
+// at the end of every span and the gradient of the initial state.
+template <int DK>
+__global__ void __launch_bounds__(kThreads) bwd_sweep_kernel(const BwdParams p) {
+    constexpr int CW = DK / 8;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    BwdSmem<DK> &s = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
+    const Lanes<DK> L;
+    const int nsl = p.Dv / kRows;
+    const bool reverse = (int)blockIdx.x >= nsl;
+    const int slice = blockIdx.x % nsl, hv = blockIdx.y, b = blockIdx.z;
+    const int hk = hv / (p.Hv / p.Hk);
+    const int r0 = slice * kRows;
+    const size_t head = (size_t)b * p.Hv + hv;
+    const size_t rec = (head * nsl + slice) * (size_t)p.nspan * kRows * DK;   // this slice's span records
+    const size_t span_stride = (size_t)kRows * DK;
+
+    if (!reverse) {
+        float S[2][CW];
+        L.load_or_zero(p.state_in == nullptr ? nullptr : p.state_in + (head * p.Dv + r0) * DK, S);
+        for (int sp = 0; sp < p.nspan; ++sp) {
+            L.store(p.ck + rec + sp * span_stride, S);
+            for (int c = 2 * sp; c < min(2 * sp + 2, p.nck); ++c) {
+                if (!chunk_active(p, b, c * kC)) continue;   // the identity on the state
+                stage_chunk<DK>(p, s, b, hk, hv, r0, c * kC, false);
+                for (int tl = 0; tl < kC; ++tl) {
+                    if (!s.m[tl]) continue;
+                    float u[2];
+                    fwd_step<DK>(s, L, S, tl, u);
+                }
+                __syncthreads();
+            }
+        }
+    } else {
+        float dS[2][CW];
+        L.load_or_zero(p.dstate_out == nullptr ? nullptr : p.dstate_out + (head * p.Dv + r0) * DK, dS);
+        for (int sp = p.nspan - 1; sp >= 0; --sp) {
+            L.store(p.dck + rec + sp * span_stride, dS);
+            for (int c = min(2 * sp + 1, p.nck - 1); c >= 2 * sp; --c) {
+                if (!chunk_active(p, b, c * kC)) continue;   // dS passes through
+                stage_chunk<DK>(p, s, b, hk, hv, r0, c * kC, true);
+                for (int tl = kC - 1; tl >= 0; --tl)
+                    if (s.m[tl]) dS_step<DK>(s, L, dS, tl);
+                __syncthreads();
+            }
+        }
+        L.store(p.dstate_in + (head * p.Dv + r0) * DK, dS);
+    }
+}
+
+// Launch 2: every (span, row slice, head) item independently, CTA i taking
+// items i, i + gridDim.x, ... with its own history buffer.  A span's second
+// half is reversed first, from the state at its middle (the first half
+// recomputed from the span's S) and the span's end dS; then its first half
+// from the span's S and the dS that the second half left.
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 2) bwd_span_kernel(const BwdParams p, int n_items) {
+    constexpr int CW = DK / 8;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    BwdSmem<DK> &s = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
+    const Lanes<DK> L;
+    const int nsl = p.Dv / kRows;
+    float *hist = p.hist + (size_t)blockIdx.x * kC * kRows * DK;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int sp = item % p.nspan;
+        int rest = item / p.nspan;
+        const int slice = rest % nsl;
+        rest /= nsl;
+        const int hv = rest % p.Hv, b = rest / p.Hv;
+        const int hk = hv / (p.Hv / p.Hk);
+        const int r0 = slice * kRows;
+        const int c_lo = 2 * sp, c_hi = 2 * sp + 1;
+        const bool a_lo = chunk_active(p, b, c_lo * kC);
+        const bool a_hi = c_hi < p.nck && chunk_active(p, b, c_hi * kC);
+        if (!a_lo && !a_hi) continue;   // uniform: its gradients stay zero
+        const size_t rec = ((((size_t)b * p.Hv + hv) * nsl + slice) * p.nspan + sp) * kRows * DK;
+        float S[2][CW], dS[2][CW];
+        L.load(p.dck + rec, dS);
+        for (int h = 1; h >= 0; --h) {   // second half first
+            if (!(h ? a_hi : a_lo)) continue;
+            L.load(p.ck + rec, S);
+            if (h == 1 && a_lo) {        // the state at the middle of the span
+                stage_chunk<DK>(p, s, b, hk, hv, r0, c_lo * kC, false);
+                for (int tl = 0; tl < kC; ++tl) {
+                    if (!s.m[tl]) continue;
+                    float u[2];
+                    fwd_step<DK>(s, L, S, tl, u);
+                }
+                __syncthreads();
+            }
+            reverse_half<DK>(p, s, L, hist, b, hk, hv, r0, (c_lo + h) * kC, S, dS);
+        }
+    }
+}
+
+// Single launch for grids that fill the GPU on their own (at least two row
+// slices per SM), where the split form only adds work: one CTA per (row
+// slice, head) runs the forward sweep storing S at every half-span, then the
+// half-spans backwards with its own history buffer.
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 2) bwd_fused_kernel(const BwdParams p) {
+    constexpr int CW = DK / 8;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    BwdSmem<DK> &s = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
+    const Lanes<DK> L;
+    const int nsl = p.Dv / kRows;
+    const int slice = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+    const int hk = hv / (p.Hv / p.Hk);
+    const int r0 = slice * kRows;
+    const size_t head = (size_t)b * p.Hv + hv;
+    const size_t cta = head * nsl + slice;
+    float *ck = p.ck + cta * (size_t)p.nck * kRows * DK;
+    float *hist = p.hist + cta * (size_t)kC * kRows * DK;
+
+    float S[2][CW];
+    L.load_or_zero(p.state_in == nullptr ? nullptr : p.state_in + (head * p.Dv + r0) * DK, S);
     for (int c = 0; c < p.nck; ++c) {
-        store_rows(ck + (size_t)c * kRows * DK, S);
+        L.store(ck + (size_t)c * kRows * DK, S);
         if (!chunk_active(p, b, c * kC)) continue;   // the identity on the state
         stage_chunk<DK>(p, s, b, hk, hv, r0, c * kC, false);
         for (int tl = 0; tl < kC; ++tl) {
             if (!s.m[tl]) continue;
             float u[2];
-            fwd_step(S, tl, u);
+            fwd_step<DK>(s, L, S, tl, u);
         }
         __syncthreads();
     }
-
-    // ---- reverse sweep
     float dS[2][CW];
-    if (p.dstate_out != nullptr) {
-        load_rows(p.dstate_out + (head * p.Dv + r0) * DK, dS);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < CW; ++j) dS[i][j] = 0.0f;
-    }
+    L.load_or_zero(p.dstate_out == nullptr ? nullptr : p.dstate_out + (head * p.Dv + r0) * DK, dS);
     for (int c = p.nck - 1; c >= 0; --c) {
-        const int t0 = c * kC;
-        if (!chunk_active(p, b, t0)) continue;   // dS passes through; its gradients stay zero
-        stage_chunk<DK>(p, s, b, hk, hv, r0, t0, true);
-        for (int i = tid; i < kC * DK; i += kThreads) {
-            (&s.red_q[0][0])[i] = 0.0f;
-            (&s.red_k[0][0])[i] = 0.0f;
-        }
-        if (tid < kC) {
-            s.red_g[tid] = 0.0f;
-            s.red_b[tid] = 0.0f;
-        }
-        // recompute the chunk: hist[tl] = the state before step tl
-        load_rows(ck + (size_t)c * kRows * DK, S);
-        for (int tl = 0; tl < kC; ++tl) {
-            store_rows(hist + (size_t)tl * kRows * DK, S);
-            if (!s.m[tl]) continue;
-            float u[2];
-            fwd_step(S, tl, u);
-            if (cg == 0) {
-                s.u[tl][rl[0]] = u[0];
-                s.u[tl][rl[1]] = u[1];
-            }
-        }
-        __syncthreads();
-        // S is now the state after the chunk; walk it backwards, the state
-        // before each step read from the history one step ahead
-        float Sp[2][CW];
-        load_rows(hist + (size_t)(kC - 1) * kRows * DK, Sp);
-        for (int tl = kC - 1; tl >= 0; --tl) {
-            float Sn[2][CW];   // S_{t-2}, for the next reverse step
-            if (tl > 0) load_rows(hist + (size_t)(tl - 1) * kRows * DK, Sn);
-            if (s.m[tl]) {
-                const float gg = s.g[tl], bb = s.beta[tl];
-                float dq_p[CW], dk_p[CW];
-#pragma unroll
-                for (int j = 0; j < CW; ++j) dq_p[j] = dk_p[j] = 0.0f;
-                float dg_p = 0.0f, db_p = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float dyv = s.dy[tl][rl[i]];
-                    const float ui = s.u[tl][rl[i]];
-                    float dd = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < CW; ++j) {
-                        dS[i][j] = fmaf(dyv, s.q[tl][c0 + j], dS[i][j]);
-                        dq_p[j] = fmaf(S[i][j], dyv, dq_p[j]);
-                        dd = fmaf(dS[i][j], s.k[tl][c0 + j], dd);
-                    }
-                    dd = row_sum(dd);                       // ddelta of the row
-                    const float dl = bb * ui;               // delta
-                    const float du = bb * dd;
-                    if (cg == 0) {
-                        db_p = fmaf(dd, ui, db_p);
-                        p.dv[(((size_t)b * T + t0 + tl) * p.Hv + hv) * p.Dv + r0 + rl[i]] = du;
-                    }
-#pragma unroll
-                    for (int j = 0; j < CW; ++j) {
-                        dk_p[j] = fmaf(dS[i][j], dl, dk_p[j]);
-                        dS[i][j] = fmaf(-du, s.k[tl][c0 + j], dS[i][j]);
-                        dk_p[j] = fmaf(-gg * Sp[i][j], du, dk_p[j]);
-                        dg_p = fmaf(dS[i][j], Sp[i][j], dg_p);
-                        dS[i][j] *= gg;
-                    }
-                }
-                // sum the 2*CW partials (dq, dk) over the warp's four row
-                // groups in two exchanges that halve the vector: lanes whose
-                // rg differs in bit 0 swap halves (dq <-> dk), then lanes whose
-                // rg differs in bit 1 swap quarters, so each lane ends with
-                // CW/2 summed columns (of dq for even rg, dk for odd) and adds
-                // those; the pairwise sums are those of a per-column shuffle sum
-                const bool hi0 = (rg & 1) != 0, hi1 = (rg & 2) != 0;
-                float h[CW];
-#pragma unroll
-                for (int j = 0; j < CW; ++j) {
-                    const float send = hi0 ? dq_p[j] : dk_p[j];
-                    const float keep = hi0 ? dk_p[j] : dq_p[j];
-                    h[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-                }
-                constexpr int HQ = CW / 2;
-                float *dst = (hi0 ? &s.red_k[tl][c0] : &s.red_q[tl][c0]) + (hi1 ? HQ : 0);
-#pragma unroll
-                for (int j = 0; j < HQ; ++j) {
-                    const float send = hi1 ? h[j] : h[HQ + j];
-                    const float keep = hi1 ? h[HQ + j] : h[j];
-                    atomicAdd(dst + j, keep + __shfl_xor_sync(0xffffffffu, send, 16));
-                }
-                dg_p = warp_sum(dg_p);
-                db_p = warp_sum(db_p);
-                if (lane == 0) {
-                    atomicAdd(&s.red_g[tl], dg_p);
-                    atomicAdd(&s.red_b[tl], db_p);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int j = 0; j < CW; ++j) {
-                    S[i][j] = Sp[i][j];
-                    Sp[i][j] = Sn[i][j];
-                }
-        }
-        __syncthreads();
-        // add the chunk's sums to the outputs (also summing over row slices
-        // and over the v-heads of the k-head)
-        const int n = min(kC, T - t0);
-        for (int i = tid; i < n * DK; i += kThreads) {
-            const int tl = i / DK, j = i % DK;
-            if (!s.m[tl]) continue;
-            const size_t o = (((size_t)b * T + t0 + tl) * p.Hk + hk) * DK + j;
-            atomicAdd(p.dq + o, s.red_q[tl][j]);
-            atomicAdd(p.dk + o, s.red_k[tl][j]);
-        }
-        if (tid < n && s.m[tid]) {
-            const size_t o = ((size_t)b * T + t0 + tid) * p.Hv + hv;
-            atomicAdd(p.dg + o, s.red_g[tid]);
-            atomicAdd(p.dbeta + o, s.red_b[tid]);
-        }
-        __syncthreads();
+        if (!chunk_active(p, b, c * kC)) continue;   // dS passes through; its gradients stay zero
+        L.load(ck + (size_t)c * kRows * DK, S);
+        reverse_half<DK>(p, s, L, hist, b, hk, hv, r0, c * kC, S, dS);
     }
-    store_rows(p.dstate_in + (head * p.Dv + r0) * DK, dS);
+    L.store(p.dstate_in + (head * p.Dv + r0) * DK, dS);
+}
+
+// Workspace layout of either form: the fused form keeps S every half-span
+// (rec) and a history per CTA; the split form S and dS every span (2 x rec)
+// and a history per span-pass CTA.
+struct Layout {
+    bool fused;
+    int nsl, nck, nspan, items, slots;
+    size_t rec_floats, dck_floats, hist_floats;
+};
+
+Layout layout_of(const Sizes &s) {
+    Layout l;
+    l.nsl = s.Dv / kRows;
+    l.nck = (s.T + kC - 1) / kC;
+    l.nspan = (s.T + kSpan - 1) / kSpan;
+    const long slices = (long)s.B * s.Hv * l.nsl;
+    l.fused = slices >= 2L * num_sms();
+    if (l.fused) {
+        l.items = 0;
+        l.slots = (int)slices;
+        l.rec_floats = (size_t)slices * l.nck * kRows * s.Dk;
+        l.dck_floats = 0;
+    } else {
+        const long items = slices * l.nspan;
+        l.items = (int)items;
+        l.slots = (int)std::min<long>(items, 2L * num_sms());
+        l.rec_floats = (size_t)items * kRows * s.Dk;
+        l.dck_floats = l.rec_floats;
+    }
+    l.hist_floats = (size_t)l.slots * kC * kRows * s.Dk;
+    return l;
 }
 
 template <int DK>
-cudaError_t launch_bwd_t(const Sizes &s, const BwdParams &p, cudaStream_t st) {
+cudaError_t launch_bwd_t(const Sizes &s, const Layout &l, const BwdParams &p, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem<DK>);
-    static unsigned long long attr_done = 0;   // per instantiation, one bit per device
-    cudaError_t e = set_max_smem(attr_done, backward_kernel<DK>, smem);
+    static unsigned long long done_sweep = 0, done_span = 0, done_fused = 0;   // per instantiation, per device
+    cudaError_t e = set_max_smem(done_sweep, bwd_sweep_kernel<DK>, smem);
+    if (e == cudaSuccess) e = set_max_smem(done_span, bwd_span_kernel<DK>, smem);
+    if (e == cudaSuccess) e = set_max_smem(done_fused, bwd_fused_kernel<DK>, smem);
     if (e != cudaSuccess) return e;
-    backward_kernel<DK><<<dim3(s.Dv / kRows, s.Hv, s.B), kThreads, smem, st>>>(p);
+    if (l.fused) {
+        bwd_fused_kernel<DK><<<dim3(l.nsl, s.Hv, s.B), kThreads, smem, st>>>(p);
+        return cudaGetLastError();
+    }
+    bwd_sweep_kernel<DK><<<dim3(2 * l.nsl, s.Hv, s.B), kThreads, smem, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || l.items == 0) return e;
+    bwd_span_kernel<DK><<<l.slots, kThreads, smem, st>>>(p, l.items);
     return cudaGetLastError();
 }
-
-size_t nck_of(const Sizes &s) { return ((size_t)s.T + kC - 1) / kC; }
 
 }  // namespace
 
 size_t backward_workspace(const Sizes &s) {
-    const size_t ctas = (size_t)s.B * s.Hv * (s.Dv / kRows);
-    return ctas * (nck_of(s) + kC) * kRows * (size_t)s.Dk * sizeof(float);
+    const Layout l = layout_of(s);
+    return (l.rec_floats + l.dck_floats + l.hist_floats) * sizeof(float);
 }
 
 cudaError_t launch_backward(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -369,12 +572,16 @@ cudaError_t launch_backward(const Sizes &s, const uint16_t *q, const uint16_t *k
     if (e == cudaSuccess) e = cudaMemsetAsync(dg, 0, ng * sizeof(float), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, ng * sizeof(float), st);
     if (e != cudaSuccess) return e;
+    const Layout l = layout_of(s);
+    float *ck = static_cast<float *>(ws);
+    float *dck = ck + l.rec_floats;
+    float *hist = dck + l.dck_floats;
     BwdParams p{q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta, dstate_in,
-                static_cast<float *>(ws), s.B, s.T, s.Hk, s.Hv, s.Dv, (int)nck_of(s)};
+                ck, dck, hist, s.B, s.T, s.Hk, s.Hv, s.Dv, l.nck, l.nspan};
     switch (s.Dk) {
-        case 32: return launch_bwd_t<32>(s, p, st);
-        case 64: return launch_bwd_t<64>(s, p, st);
-        case 128: return launch_bwd_t<128>(s, p, st);
+        case 32: return launch_bwd_t<32>(s, l, p, st);
+        case 64: return launch_bwd_t<64>(s, l, p, st);
+        case 128: return launch_bwd_t<128>(s, l, p, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -25,6 +25,7 @@ BWD_CASES = [
     (2, 100, 2, 4, 128, 64, "allmasked_row", True, True),
     (1, 130, 1, 1, 64, 128, "sparse", False, False),
     (1, 1024, 1, 2, 128, 128, "random", True, True),     # long: error growth over many steps
+    (2, 70, 16, 64, 128, 128, "random", True, True),     # 512 row slices: the single-launch form
 ]
 
 
