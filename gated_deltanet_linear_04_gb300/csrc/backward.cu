@@ -66,9 +66,22 @@ struct BwdSmem {
     float v[kC][kRows], dy[kC][kRows], u[kC][kRows];
     float g[kC], beta[kC];
     int m[kC];
-    float red_q[kC][DK], red_k[kC][DK];
+    // per-step column sums of dq (at red_q(col)) and dk (at red_k(col)); see
+    // red_q / red_k below for the layout
+    float red[kC][2 * DK + 8];
     float red_g[kC], red_b[kC];
 };
+
+// Index of column c's dq / dk sum in a row of BwdSmem::red.  After the
+// transpose-reduction the four row groups of a warp add, for the same column
+// lane, dq of the lower column half (rg 0), dk of the lower half (rg 1), dq of
+// the upper half (rg 2) and dk of the upper half (rg 3): the k half starts one
+// bank over and (for Dk >= 64) the upper half is skewed by two banks, so the
+// four land on different banks.
+template <int DK>
+__device__ __forceinline__ int red_q(int c) { return DK >= 64 ? c + ((c >= DK / 2) ? 2 : 0) : c; }
+template <int DK>
+__device__ __forceinline__ int red_k(int c) { return DK + 5 + red_q<DK>(c); }
 
 // Stage steps [t0, t0 + n) of the chunk: q, k of the k-head, v and dy of the
 // CTA's rows, g, beta, the mask (steps past T or masked: m = 0).  Block-wide;
@@ -78,23 +91,21 @@ __device__ __forceinline__ void stage_chunk(const BwdParams &p, BwdSmem<DK> &s, 
                                             int t0, bool with_q_dy) {
     const int tid = threadIdx.x;
     const int T = p.T;
-    constexpr int V8 = DK / 8;   // 16-byte groups of a q / k row
-    for (int i = tid; i < kC * V8; i += kThreads) {
-        const int tl = i / V8, c8 = (i % V8) * 8, t = t0 + tl;
-        uint4 kk = make_uint4(0u, 0u, 0u, 0u), qq = kk;
+    constexpr int V4 = DK / 4;   // 4-column groups of a q / k row: one 16-byte store each
+    for (int i = tid; i < kC * V4; i += kThreads) {
+        const int tl = i / V4, c4 = (i % V4) * 4, t = t0 + tl;
+        uint2 kk = make_uint2(0u, 0u), qq = kk;
         if (t < T) {
-            const size_t off = (((size_t)b * T + t) * p.Hk + hk) * DK + c8;
-            kk = *reinterpret_cast<const uint4 *>(p.k + off);
-            if (with_q_dy) qq = *reinterpret_cast<const uint4 *>(p.q + off);
+            const size_t off = (((size_t)b * T + t) * p.Hk + hk) * DK + c4;
+            kk = *reinterpret_cast<const uint2 *>(p.k + off);
+            if (with_q_dy) qq = *reinterpret_cast<const uint2 *>(p.q + off);
         }
-        const uint32_t kw[4] = {kk.x, kk.y, kk.z, kk.w}, qw[4] = {qq.x, qq.y, qq.z, qq.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            s.k[tl][c8 + 2 * e] = __uint_as_float(kw[e] << 16);
-            s.k[tl][c8 + 2 * e + 1] = __uint_as_float(kw[e] & 0xffff0000u);
-            s.q[tl][c8 + 2 * e] = __uint_as_float(qw[e] << 16);
-            s.q[tl][c8 + 2 * e + 1] = __uint_as_float(qw[e] & 0xffff0000u);
-        }
+        *reinterpret_cast<float4 *>(&s.k[tl][c4]) =
+            make_float4(__uint_as_float(kk.x << 16), __uint_as_float(kk.x & 0xffff0000u),
+                        __uint_as_float(kk.y << 16), __uint_as_float(kk.y & 0xffff0000u));
+        *reinterpret_cast<float4 *>(&s.q[tl][c4]) =
+            make_float4(__uint_as_float(qq.x << 16), __uint_as_float(qq.x & 0xffff0000u),
+                        __uint_as_float(qq.y << 16), __uint_as_float(qq.y & 0xffff0000u));
     }
     for (int i = tid; i < kC * kRows; i += kThreads) {
         const int tl = i / kRows, r = i % kRows, t = t0 + tl;
@@ -247,8 +258,8 @@ __device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s,
     const int T = p.T;
     stage_chunk<DK>(p, s, b, hk, hv, r0, t0, true);
     for (int i = tid; i < kC * DK; i += kThreads) {
-        (&s.red_q[0][0])[i] = 0.0f;
-        (&s.red_k[0][0])[i] = 0.0f;
+        s.red[i / DK][red_q<DK>(i % DK)] = 0.0f;
+        s.red[i / DK][red_k<DK>(i % DK)] = 0.0f;
     }
     if (tid < kC) {
         s.red_g[tid] = 0.0f;
@@ -321,13 +332,14 @@ __device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s,
                 h[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
             }
             constexpr int HQ = CW / 2;
-            float *dst = hi0 ? &s.red_k[tl][0] : &s.red_q[tl][0];
             const int off = hi1 ? HQ : 0;
 #pragma unroll
             for (int j = 0; j < HQ; ++j) {
                 const float send = hi1 ? h[j] : h[HQ + j];
                 const float keep = hi1 ? h[HQ + j] : h[j];
-                atomicAdd(dst + L.col(off + j), keep + __shfl_xor_sync(0xffffffffu, send, 16));
+                const int c = L.col(off + j);
+                atomicAdd(&s.red[tl][hi0 ? red_k<DK>(c) : red_q<DK>(c)],
+                          keep + __shfl_xor_sync(0xffffffffu, send, 16));
             }
             dg_p = warp_sum(dg_p);
             db_p = warp_sum(db_p);
@@ -352,8 +364,8 @@ __device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s,
         const int tl = i / DK, j = i % DK;
         if (!s.m[tl]) continue;
         const size_t o = (((size_t)b * T + t0 + tl) * p.Hk + hk) * DK + j;
-        atomicAdd(p.dq + o, s.red_q[tl][j]);
-        atomicAdd(p.dk + o, s.red_k[tl][j]);
+        atomicAdd(p.dq + o, s.red[tl][red_q<DK>(j)]);
+        atomicAdd(p.dk + o, s.red[tl][red_k<DK>(j)]);
     }
     if (tid < n && s.m[tid]) {
         const size_t o = ((size_t)b * T + t0 + tid) * p.Hv + hv;
