@@ -61,6 +61,32 @@ def recurrence_flops_per_token(d: wl.Dims) -> int:
     return 7 * d.Dk * d.Dv * d.Hv
 
 
+def chunk_mma_flops(d: wl.Dims, C: int = 64) -> int:
+    """Tensor-core flops of one chunk of one head in the chunked form:
+    [K;Q]K^T (2C x C x Dk), U = T diag(beta) V (C x C x Dv), W = T diag(beta
+    gamma) K (C x C x Dk), D = U - W S0^T and the S0 part of Y (C x Dv x Dk
+    each), the state update D^T P (Dv x Dk x C) and the intra-chunk part of Y
+    (C x C x Dv), 2 flops per multiply-add."""
+    return 6 * C * C * d.Dk + 4 * C * C * d.Dv + 6 * C * d.Dv * d.Dk
+
+
+def active_chunks(mask, T: int, B: int, C: int = 64) -> int:
+    """Chunks of C steps holding at least one valid step (the chunked kernels
+    skip the others)."""
+    n = (T + C - 1) // C
+    if mask is None:
+        return B * n
+    m = mask.reshape(B, T)
+    pad = n * C - T
+    if pad:
+        m = torch.nn.functional.pad(m, (0, pad))
+    return int((m.reshape(B, n, C) != 0).any(dim=2).sum().item())
+
+
+# tf32 : bf16 dense tensor rate on GB300 (1.1 vs 2.25 PFLOP/s nominal)
+TF32_PER_BF16 = 1.1 / 2.25
+
+
 # ---------------------------------------------------------------------------
 # environment: peaks, clocks, ranks
 # ---------------------------------------------------------------------------
@@ -488,7 +514,7 @@ def bench_rmsnorm_gated(gdn, w: wl.Workload, dev, iters: int = 5) -> dict:
     return {"workload": w.name, "ms": round(ms, 4), "bytes": nbytes, "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
 
 
-def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int) -> dict:
+def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int, peaks: dict = None) -> dict:
     """Full core (conv + gates + recurrence) over one workload call."""
     d = w.dims
     gen = torch.Generator(device=dev)
@@ -571,11 +597,23 @@ def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int) -> dict:
         t_g[fused] = ev[0].elapsed_time(ev[1]) / iters
     if gdn.gdn_device_status() != gdn.GDN_OK:
         raise RuntimeError("device error word set during the gated prefill benchmark")
-    return {"workload": w.name, "chunk": chunk, "ms": round(ms, 4), "recurrence_ms": round(ms_rec, 4),
-            "tokens": n_valid, "tokens_per_s": n_valid / (ms / 1e3),
-            "recurrence_tflops": flops / (ms_rec / 1e3) / 1e12,
-            "recurrence_gated_norm_ms": {"gdn_prefill_gated": round(t_g[True], 4),
-                                         "prefill_then_norm": round(t_g[False], 4)}}
+    res = {"workload": w.name, "chunk": chunk, "ms": round(ms, 4), "recurrence_ms": round(ms_rec, 4),
+           "tokens": n_valid, "tokens_per_s": n_valid / (ms / 1e3),
+           "recurrence_tflops": flops / (ms_rec / 1e3) / 1e12,
+           "recurrence_gated_norm_ms": {"gdn_prefill_gated": round(t_g[True], 4),
+                                        "prefill_then_norm": round(t_g[False], 4)}}
+    if chunk == 64:
+        # tensor-core work of the chunked form over the chunks it computes,
+        # against the tf32 rate (measured bf16 peak x the nominal tf32 ratio)
+        n_ch = active_chunks(mask, d.T, d.B) * d.Hv
+        tflops = chunk_mma_flops(d) * n_ch / (ms_rec / 1e3) / 1e12
+        res["tensor"] = {"tflops": round(tflops, 2), "chunk_head_units": n_ch,
+                         "flops_per_unit": chunk_mma_flops(d)}
+        if peaks is not None:
+            peak = peaks["bf16_tflops"] * TF32_PER_BF16
+            res["tensor"].update({"peak_tflops": round(peak, 1), "frac_of_tf32_peak": round(tflops / peak, 4),
+                                  "peak_source": peaks["source"] + " bf16 x nominal tf32/bf16"})
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -664,7 +702,7 @@ def main():
         for name in ("prefill_t8192", "prefill_ragged"):
             for chunk in (0, 64):
                 try:
-                    prefill.append(bench_prefill(gdn, wl.WORKLOADS[name], dev, 3, chunk))
+                    prefill.append(bench_prefill(gdn, wl.WORKLOADS[name], dev, 3, chunk, peaks))
                 except gdn.GdnError as e:
                     if e.status != gdn.GDN_ERR_UNSUPPORTED:
                         raise

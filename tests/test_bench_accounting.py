@@ -1,0 +1,39 @@
+"""The byte and flop accounting bench.py reports its rooflines with, checked
+against counts done by hand (no GPU)."""
+import torch
+
+import bench
+from gated_deltanet_linear_04_gb300 import workloads as wl
+
+
+def test_decode_bytes_of_the_batched_decode_workload():
+    d = wl.WORKLOADS["decode_b128"].dims
+    by = bench.decode_bytes(d)
+    assert by["state_rw"] == 2 * 128 * 32 * 128 * 128 * 4          # 536.9 MB
+    C = 2 * 16 * 128 + 32 * 128
+    assert by["conv_state_rw"] == 2 * 128 * 3 * C * 2
+    assert sum(by.values()) == 552681728                           # the decode roofline's bytes
+
+
+def test_chunk_mma_flops_counts_each_product():
+    d = wl.WORKLOADS["prefill_t8192"].dims                          # Dk = Dv = 128
+    C = 64
+    products = [(2 * C, C, 128),      # [K;Q] K^T
+                (C, C, 128),          # U = T diag(beta) V
+                (C, C, 128),          # W = T diag(beta gamma) K
+                (C, 128, 128),        # D = U - W S0^T
+                (C, 128, 128),        # S0 part of Y
+                (128, 128, C),        # state update D^T P
+                (C, C, 128)]          # intra-chunk part of Y
+    assert bench.chunk_mma_flops(d) == sum(2 * m * n * k for m, n, k in products)
+
+
+def test_active_chunks_counts_chunks_with_a_valid_step():
+    T, B = 300, 5
+    lens = torch.tensor([0, 1, 64, 65, 300])
+    mask = wl.right_padded_mask(lens, T)
+    assert bench.active_chunks(mask, T, B) == 0 + 1 + 1 + 2 + 5
+    assert bench.active_chunks(None, T, B) == B * 5
+    holes = torch.zeros((1, T), dtype=torch.uint8)
+    holes[0, 130] = 1                                               # one valid step in chunk 2
+    assert bench.active_chunks(holes, T, 1) == 1
