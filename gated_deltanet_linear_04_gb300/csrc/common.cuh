@@ -158,6 +158,15 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
+// 3-D tiled TMA store of the box at (x = inner coordinate, y, z) of `tmap`
+// from shared memory, tracked by the issuing thread's bulk group (the box is
+// clipped at the tensor's bounds; x * element size must be a multiple of 16).
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int x, int y, int z, const void *smem_src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

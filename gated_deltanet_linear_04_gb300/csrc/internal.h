@@ -59,6 +59,11 @@ cudaError_t launch_decode_window(const Sizes &s, const uint16_t *qkv, const uint
                                  const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
                                  float *state, const int32_t *keep, uint16_t *y, unsigned *err, cudaStream_t st);
 
+// Encodes a 3-D row-major tensor map (d2 x d1 x d0, d0 innermost; box
+// box1 x box0 in the two inner dimensions, one deep in the outer), no swizzle.
+bool encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t d2,
+                    uint64_t d1, uint64_t d0, uint32_t box1, uint32_t box0);
+
 // Encodes a 2-D row-major tensor map (rows x cols, box rows x box_cols).
 bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
                     uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,

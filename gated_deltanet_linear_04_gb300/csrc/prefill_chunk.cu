@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
                                                                      const __grid_constant__ CUtensorMap tm_q,
                                                                      const __grid_constant__ CUtensorMap tm_v,
                                                                      const __grid_constant__ CUtensorMap tm_z,
+                                                                     const __grid_constant__ CUtensorMap tm_y,
                                                                      const ChunkParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_mma, bar_z;
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         // ---- S1: chunk inputs, log-decay prefix sums (warp 0)
         ok = mbar_wait(&bar_tma, (uint32_t)(it & 1), p.err);
         if (warp == 0) step_factors(lane, s_g[st], s_b[st], s_lg, s_gam, s_kc, s_beta, s_bg);
+        if (tid == 0) bulk_wait_read();   // the previous y store has read its tile (slot 9 is rebuilt below)
         ok = __syncthreads_and(ok) != 0;
         if (!ok) break;
 
@@ -299,9 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         }
         if (!wait_mma()) { ok = false; break; }
 
-        // ---- S9: y through a shared staging tile [64 steps][128 dv] bf16, then
-        // 16-byte stores of the valid steps (masked steps are zero)
+        // ---- S9: y through a shared staging tile [64 steps][128 dv] bf16
+        // (masked steps zero), then one TMA store of the tile clipped at T
         stage_y(tmem + lane_base + C_Y, sm, S_YST, s_m[st], row, half);
+        fence_proxy_async_smem();
         umma::fence_before_sync();
         __syncthreads();
         if constexpr (NORM) {
@@ -345,21 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
                 }
                 *reinterpret_cast<uint4 *>(yrow + c16 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
             }
+            fence_proxy_async_smem();
             ok = __syncthreads_and(ok) != 0;
             if (!ok) break;
         }
-        {
-            const int nv = min(kC, T - t0);
-            for (int i = tid; i < nv * (kD / 8); i += kThreads) {
-                const int r = i / (kD / 8), c8 = (i % (kD / 8)) * 8;
-                *reinterpret_cast<uint4 *>(p.y + (((size_t)b * T + t0 + r) * p.Hv + hv) * kD + c8) =
-                    *reinterpret_cast<const uint4 *>(sm + S_YST + (r * kD + c8) * 2);
-            }
+        if (tid == 0) {
+            tma_store_3d(&tm_y, hv * kD, t0, b, sm + S_YST);
+            bulk_commit();
         }
         zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), kD);
         c = cn;
     }
 
+    if (tid == 0) bulk_wait_read();   // the last y store has read its tile
     // ---- final state (only when every wait succeeded)
     if (__syncthreads_and(ok)) {
         const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
@@ -396,14 +397,16 @@ cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint
                                    const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
                                    const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st) {
     if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
-    CUtensorMap tk, tq, tv, tz;
+    CUtensorMap tk, tq, tv, tz, ty;
     const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
     if (!encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
-                        CU_TENSOR_MAP_SWIZZLE_NONE))
+                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_3d(&ty, y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)s.B, (uint64_t)s.T,
+                        (uint64_t)s.Hv * kD, kC, kD))
         return cudaErrorInvalidValue;
     tz = tv;   // unused without the norm
     if (z != nullptr && !encode_tmap_2d(&tz, z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC,
@@ -415,9 +418,9 @@ cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint
                   s.B, s.T, s.Hk, s.Hv};
     dim3 grid(s.Hv, s.B);
     if (z != nullptr)
-        prefill_chunk_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, tz, p);
+        prefill_chunk_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, tz, ty, p);
     else
-        prefill_chunk_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, tz, p);
+        prefill_chunk_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, tz, ty, p);
     return cudaGetLastError();
 }
 

@@ -262,8 +262,8 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
 // pass 2: the chunk chain of head (b, hv), state products only.  The caller
 // has initialised sh.bar0-2 and allocated 512 TMEM columns.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void state_head(const TwoPassParams &p, TwoPassShared &sh, uint8_t *sm, uint32_t base,
-                                           uint32_t tmem, int b, int hv) {
+__device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtensorMap *tm_y, TwoPassShared &sh,
+                                           uint8_t *sm, uint32_t base, uint32_t tmem, int b, int hv) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2, row = quad * 32 + lane;
     const int T = p.T;
@@ -392,26 +392,27 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, TwoPassShared
             umma::fence_after_sync();
             issue_dt_products(tmem, base, P2_DT, P2_P, P2_KT);
             umma::mma_commit(&sh.bar2);
+            bulk_wait_read();   // the previous chunk's y store has read the staging tile
         }
         if (!wait_mma()) { ok = false; break; }
         if (cn < nchunks) load_b(cn, it + 1);
 
+        // y: the staged tile leaves by one TMA store (clipped at T), which
+        // the next chunk's staging waits for
         stage_y(lane_tmem + C_Y, sm, P2_YST, sh.s_m[st], row, half);
+        fence_proxy_async_smem();
         umma::fence_before_sync();
         __syncthreads();
-        {
-            const int nv = min(kC, T - t0);
-            for (int i = tid; i < nv * (kD / 8); i += kThreads) {
-                const int r = i / (kD / 8), c8 = (i % (kD / 8)) * 8;
-                *reinterpret_cast<uint4 *>(p.y + (((size_t)b * T + t0 + r) * p.Hv + hv) * kD + c8) =
-                    *reinterpret_cast<const uint4 *>(sm + P2_YST + (r * kD + c8) * 2);
-            }
+        if (tid == 0) {
+            tma_store_3d(tm_y, hv * kD, t0, b, sm + P2_YST);
+            bulk_commit();
         }
         if (tid < kC) sh.s_m[st ^ 1][tid] = pf_m;
         zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), kD);
         c = cn;
     }
 
+    if (tid == 0) bulk_wait_read();   // the last y store has read the staging tile
     if (__syncthreads_and(ok)) {
         const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
 #pragma unroll
@@ -480,14 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
 }
 
 // separate form, pass 2: one CTA per (hv, row slot)
-__global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassParams p) {
+__global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const __grid_constant__ CUtensorMap tm_y,
+                                                                   const TwoPassParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ TwoPassShared sh;
     uint32_t base;
     uint8_t *sm = aligned_base(smem_raw, base);
     const uint32_t tmem = cta_setup(sh, 512);
     const int b = p.order != nullptr ? p.order[blockIdx.y] : (int)blockIdx.y;
-    state_head(p, sh, sm, base, tmem, b, blockIdx.x);
+    state_head(p, &tm_y, sh, sm, base, tmem, b, blockIdx.x);
     cta_teardown(tmem, 512);
 }
 
@@ -496,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const TwoPassP
 __global__ void __launch_bounds__(kThreads, 1) chunk_overlap_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                      const __grid_constant__ CUtensorMap tm_q,
                                                                      const __grid_constant__ CUtensorMap tm_v,
+                                                                     const __grid_constant__ CUtensorMap tm_y,
                                                                      const TwoPassParams p, const int n_heads) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ TwoPassShared sh;
@@ -507,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_overlap_kernel(const __grid
     if (is_state) {
         const int slot = blockIdx.x / p.Hv, hv = blockIdx.x % p.Hv;
         const int b = p.order != nullptr ? p.order[slot] : slot;
-        state_head(p, sh, sm, base, tmem, b, hv);
+        state_head(p, &tm_y, sh, sm, base, tmem, b, hv);
     } else {
         const int n_prep = (int)gridDim.x - n_heads;
         const long n_units = (long)p.nchunks * n_heads;
@@ -538,14 +541,16 @@ cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uin
                                     const uint8_t *mask, const int *order, uint16_t *y, void *blobs,
                                     unsigned *err, cudaStream_t st) {
     if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
-    CUtensorMap tk, tq, tv;
+    CUtensorMap tk, tq, tv, ty;
     const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
     if (!encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
-                        CU_TENSOR_MAP_SWIZZLE_NONE))
+                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_3d(&ty, y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)s.B, (uint64_t)s.T,
+                        (uint64_t)s.Hv * kD, kC, kD))
         return cudaErrorInvalidValue;
     static unsigned long long set1 = 0, set2 = 0, set3 = 0;   // one bit per device
     cudaError_t e = set_max_smem(set1, chunk_prep_kernel, kP1Smem);
@@ -579,12 +584,12 @@ cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uin
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, chunk_overlap_kernel, tk, tq, tv, p, n_heads);
+        return cudaLaunchKernelEx(&cfg, chunk_overlap_kernel, tk, tq, tv, ty, p, n_heads);
     }
     chunk_prep_kernel<<<dim3(nchunks, s.Hv, s.B), kThreads, kP1Smem, st>>>(tk, tq, tv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunk_state_kernel<<<dim3(s.Hv, s.B), kThreads, kP2Smem, st>>>(p);
+    chunk_state_kernel<<<dim3(s.Hv, s.B), kThreads, kP2Smem, st>>>(ty, p);
     return cudaGetLastError();
 }
 
