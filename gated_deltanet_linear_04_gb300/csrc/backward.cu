@@ -359,13 +359,15 @@ __device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s,
     __syncthreads();
     // add the half-span's sums to the outputs (also summing over row slices
     // and over the v-heads of the k-head)
+    // (four columns per reduction: they never straddle the skew at DK/2)
     const int n = min(kC, T - t0);
-    for (int i = tid; i < n * DK; i += kThreads) {
-        const int tl = i / DK, j = i % DK;
+    for (int i = tid; i < n * (DK / 4); i += kThreads) {
+        const int tl = i / (DK / 4), j = (i % (DK / 4)) * 4;
         if (!s.m[tl]) continue;
         const size_t o = (((size_t)b * T + t0 + tl) * p.Hk + hk) * DK + j;
-        atomicAdd(p.dq + o, s.red[tl][red_q<DK>(j)]);
-        atomicAdd(p.dk + o, s.red[tl][red_k<DK>(j)]);
+        const float *rq = &s.red[tl][red_q<DK>(j)], *rk = &s.red[tl][red_k<DK>(j)];
+        red_add_v4(p.dq + o, rq[0], rq[1], rq[2], rq[3]);
+        red_add_v4(p.dk + o, rk[0], rk[1], rk[2], rk[3]);
     }
     if (tid < n && s.m[tid]) {
         const size_t o = ((size_t)b * T + t0 + tid) * p.Hv + hv;
