@@ -250,6 +250,11 @@ gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qkv, const
 
 namespace {
 
+// Staging slots of gdn_recurrent_decode_host_steps: step i uses slot i %
+// kHostSlots, so inputs run up to kHostSlots - 1 steps ahead of the kernels
+// and a short stall of the copy path is absorbed.
+constexpr int kHostSlots = 4;
+
 // One staging slot of gdn_recurrent_decode_host_steps: byte offsets of qkv,
 // a, b and y (each 256-byte aligned) and the slot size.
 struct HostSlot {
@@ -272,7 +277,7 @@ HostSlot host_slot(const gdn::Sizes &s) {
 size_t gdn_decode_host_staging_size(const gdn_dims *dims) {
     gdn::Sizes s;
     if (gdn::check_dims(dims, &s) != GDN_OK || s.T != 1) return 0;
-    return 2 * host_slot(s).bytes;
+    return kHostSlots * host_slot(s).bytes;
 }
 
 gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, const uint16_t *qkv_h,
@@ -292,15 +297,15 @@ gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, co
         !ok_ptr(state, B) || !ok_ptr(row_mask, 0) || !ok_ptr(staging, B))
         return GDN_ERR_INVALID_ARG;
     const HostSlot h = host_slot(s);
-    if (staging_bytes < 2 * h.bytes) return GDN_ERR_INVALID_ARG;
+    if (staging_bytes < kHostSlots * h.bytes) return GDN_ERR_INVALID_ARG;
     const size_t nq = B * s.C(), na = B * s.Hv, ny = B * s.Hv * s.Dv;   // elements per step
 
     cudaStream_t main = (cudaStream_t)stream, cin = nullptr, cout = nullptr;
-    cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_done[2] = {}, ev_out[2] = {};
+    cudaEvent_t ev_start = nullptr, ev_in[kHostSlots] = {}, ev_done[kHostSlots] = {}, ev_out[kHostSlots] = {};
     cudaError_t e = cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
-    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+    for (int k = 0; k < kHostSlots && e == cudaSuccess; ++k) {
         e = cudaEventCreateWithFlags(&ev_in[k], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_done[k], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_out[k], cudaEventDisableTiming);
@@ -310,25 +315,25 @@ gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, co
     if (e == cudaSuccess) e = cudaEventRecord(ev_start, main);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev_start, 0);
-    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+    for (int k = 0; k < kHostSlots && e == cudaSuccess; ++k) {
         e = cudaEventRecord(ev_done[k], main);
         if (e == cudaSuccess) e = cudaEventRecord(ev_out[k], main);
     }
     for (int i = 0; i < n_steps && e == cudaSuccess; ++i) {
-        const int k = i & 1;
+        const int k = i % kHostSlots;
         char *slot = static_cast<char *>(staging) + (size_t)k * h.bytes;
         uint16_t *qkv_d = reinterpret_cast<uint16_t *>(slot + h.qkv);
         uint16_t *a_d = reinterpret_cast<uint16_t *>(slot + h.a);
         uint16_t *b_d = reinterpret_cast<uint16_t *>(slot + h.b);
         uint16_t *y_d = reinterpret_cast<uint16_t *>(slot + h.y);
-        // step i's inputs, once step i-2 has finished reading the slot
+        // step i's inputs, once the slot's previous step has finished reading it
         e = cudaStreamWaitEvent(cin, ev_done[k], 0);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(qkv_d, qkv_h + (size_t)i * nq, nq * 2, cudaMemcpyHostToDevice, cin);
         if (e == cudaSuccess) e = cudaMemcpyAsync(a_d, a_h + (size_t)i * na, na * 2, cudaMemcpyHostToDevice, cin);
         if (e == cudaSuccess) e = cudaMemcpyAsync(b_d, b_h + (size_t)i * na, na * 2, cudaMemcpyHostToDevice, cin);
         if (e == cudaSuccess) e = cudaEventRecord(ev_in[k], cin);
-        // the step, once its inputs are in and step i-2's y has left the slot
+        // the step, once its inputs are in and the slot's previous y has left it
         if (e == cudaSuccess) e = cudaStreamWaitEvent(main, ev_in[k], 0);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(main, ev_out[k], 0);
         if (e == cudaSuccess)
@@ -341,9 +346,9 @@ gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, co
         if (e == cudaSuccess) e = cudaEventRecord(ev_out[k], cout);
     }
     // `stream` completes after the last y has arrived
-    for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(main, ev_out[k], 0);
+    for (int k = 0; k < kHostSlots && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(main, ev_out[k], 0);
     // streams and events are released once their pending work completes
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kHostSlots; ++k) {
         if (ev_in[k]) cudaEventDestroy(ev_in[k]);
         if (ev_done[k]) cudaEventDestroy(ev_done[k]);
         if (ev_out[k]) cudaEventDestroy(ev_out[k]);

@@ -125,8 +125,9 @@ GDN_API gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qk
  *   conv_w, conv_state, A_log, dt_bias, state, row_mask: device, as in
  *              gdn_recurrent_decode (row_mask applies to every step)
  *   staging    device workspace of gdn_decode_host_staging_size(dims) bytes,
- *              16-byte aligned: two slots of qkv, a, b and y, so that step
- *              i+1's inputs travel and step i-1's y returns while step i runs
+ *              16-byte aligned: four slots of qkv, a, b and y, so that the
+ *              next steps' inputs travel and earlier steps' y return while
+ *              step i runs
  * Host buffers should be page-locked (cudaHostAlloc / pinned): pageable
  * memory is accepted but its copies do not overlap the kernels.  The copies
  * run on two streams created for the call (cudaMemcpyAsync, one per tensor

@@ -109,11 +109,11 @@ def test_prefill_chunk_argument(lib):
 
 def test_decode_host_steps_staging_and_validation(lib):
     d = _dims(B=3, T=1)
-    # two slots of qkv, a, b and y, each array rounded up to whole 256 bytes
+    # four slots of qkv, a, b and y, each array rounded up to whole 256 bytes
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     C = 2 * d.Hk * d.Dk + d.Hv * d.Dv
     n = lib.gdn_decode_host_staging_size(ctypes.byref(d))
-    assert n == 2 * (up(d.B * C * 2) + 2 * up(d.B * d.Hv * 2) + up(d.B * d.Hv * d.Dv * 2))
+    assert n == 4 * (up(d.B * C * 2) + 2 * up(d.B * d.Hv * 2) + up(d.B * d.Hv * d.Dv * 2))
     assert lib.gdn_decode_host_staging_size(ctypes.byref(_dims(T=2))) == 0
     f = lib.gdn_recurrent_decode_host_steps
     none = [None] * 11
