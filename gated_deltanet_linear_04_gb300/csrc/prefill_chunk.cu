@@ -13,7 +13,8 @@
 //   S6 D^T += S0 (-W)^T, Y^T = S0 (gQ)^T with S0 read from TMEM
 //   S7 D^T and P = M o Q K^T to shared memory; S <- 2^lg_63 S
 //   S8 Y^T += D^T P^T, S += D^T Kc^T
-//   S9 y staged in shared memory as bf16 and stored with 16-byte stores
+//   S9 y staged in shared memory as bf16 and stored by one TMA store of the
+//      tile (3-D tensor map, clipped at the row's T)
 // q, k, v tiles arrive by 2-D TMA (k and q 128B-swizzled straight into the
 // MMA operand layout), prefetched one chunk ahead.  Supports Dk = Dv = 128.
 // Shared memory: 13 slots of 16 KiB reused across the phases of a chunk.
