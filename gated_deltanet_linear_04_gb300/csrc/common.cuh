@@ -178,6 +178,14 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
                  : "memory");
 }
 
+// Programmatic dependent launch: the next grid on the stream may be scheduled
+// as soon as every CTA of this one has called grid_dep_launch; it then waits
+// (grid_dep_wait) for the previous grid to finish and its writes to be
+// visible before touching any buffer that grid may write.  Both are no-ops
+// for a grid launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // thread-block clusters
 // ---------------------------------------------------------------------------

@@ -89,12 +89,6 @@ __device__ __forceinline__ void load_conv_data(const DecodeParams &p, int b, int
     in.xnew = p.qkv[(size_t)b * p.C + c];
 }
 
-// Programmatic dependent launch: the next step's grid may be scheduled as
-// soon as every CTA of this one has started; it then waits (grid_dep_wait)
-// for this grid to finish and its writes to be visible before touching any
-// buffer this grid may write.
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // conv over [stored rows, new] followed by SiLU; nw gets the shifted window
 // (the new conv_state rows).

@@ -62,6 +62,11 @@ struct ConvWindow {
     float x[K - 1 + TM];
     float w[K];
 
+    // the taps (constant across calls: read before waiting on the previous grid)
+    __device__ __forceinline__ void load_taps(const WindowParams &p, int c) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) w[j] = bf16_to_f32(p.conv_w[(size_t)c * K + j]);
+    }
     __device__ __forceinline__ void load(const WindowParams &p, int b, int c) {
         constexpr int n = K - 1;
         const uint16_t *cs = p.conv_state + (size_t)b * n * p.C + c;
@@ -69,8 +74,6 @@ struct ConvWindow {
         for (int j = 0; j < n; ++j) x[j] = bf16_to_f32(cs[(size_t)j * p.C]);
 #pragma unroll
         for (int t = 0; t < TM; ++t) x[n + t] = t < p.T ? bf16_to_f32(p.qkv[((size_t)b * p.T + t) * p.C + c]) : 0.0f;
-#pragma unroll
-        for (int j = 0; j < K; ++j) w[j] = bf16_to_f32(p.conv_w[(size_t)c * K + j]);
     }
 
     // SiLU(conv) of tokens t < TM: taps j = 0 .. K-1 read x[t + j] (the
@@ -126,6 +129,18 @@ __global__ void __launch_bounds__(kThreads, TM == 6 ? 3 : 4) window_kernel(const
     const int hv = hk * G + hv_local;
     const int r0 = slice * R;
     const int T = p.T;
+    grid_dep_launch();
+
+    // before the wait only the constant taps; every other input (state,
+    // conv_state, qkv, gates, keep) may be written by the previous grid
+    const bool has_qk = tid < 2 * DK;
+    const int c_qk = tid < DK ? hk * DK + tid : p.Hk * DK + hk * DK + (tid - DK);
+    const bool has_v = tid < R;
+    const int c_v = 2 * p.Hk * DK + hv * p.Dv + r0 + tid;
+    ConvWindow<K, TM> wqk, wv;
+    if (has_qk) wqk.load_taps(p, c_qk);
+    if (has_v) wv.load_taps(p, c_v);
+    grid_dep_wait();
     int keep = p.keep == nullptr ? T : p.keep[b];
     keep = keep < 0 ? 0 : (keep > T ? T : keep);
 
@@ -156,11 +171,6 @@ __global__ void __launch_bounds__(kThreads, TM == 6 ? 3 : 4) window_kernel(const
     }
 
     // ---- every input load first: the q/k and v conv windows
-    const bool has_qk = tid < 2 * DK;
-    const int c_qk = tid < DK ? hk * DK + tid : p.Hk * DK + hk * DK + (tid - DK);
-    const bool has_v = tid < R;
-    const int c_v = 2 * p.Hk * DK + hv * p.Dv + r0 + tid;
-    ConvWindow<K, TM> wqk, wv;
     if (has_qk) wqk.load(p, b, c_qk);
     if (has_v) wv.load(p, b, c_v);
     // the gates, on the last warp while its conv window is in flight
@@ -353,13 +363,20 @@ cudaError_t launch_t(const WindowParams &p, cudaStream_t st) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)R * DK * sizeof(float);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = G * p.SN;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    // programmatic launch (the next grid scheduled while this one drains)
+    // only for grids larger than one resident wave, as for the decode step,
+    // and not for loops to 6 tokens (at three CTAs per SM it measured 1-2 %
+    // slower there, 1-2 % faster for 1, 3, 4 and 7 tokens)
+    const long ctas = (long)cfg.gridDim.x * cfg.gridDim.y * cfg.gridDim.z;
+    cfg.numAttrs = (TM != 6 && ctas > 4L * num_sms()) ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, window_kernel<DK, K, TM>, p);
 }
 
