@@ -215,7 +215,7 @@ __device__ __forceinline__ void p_tile(const float (&qk)[32], uint8_t *sm, uint3
 
 // One merge level: for each pair of S x S diagonal blocks (a = [q0, q0+S),
 // b = [q0+S, q0+2S)) of the unit lower triangular T, the lower-left block is
-// X = -T_bb A_ba T_aa.  Each task computes 4 adjacent columns of one row; sums
+// X = -T_bb A_ba T_aa.  Each work item computes 4 adjacent columns of one row; sums
 // run over full blocks because the triangular factors hold explicit zeros
 // above the diagonal.
 template <int S>

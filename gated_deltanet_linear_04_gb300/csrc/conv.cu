@@ -9,9 +9,9 @@
 //
 // Work split (memory-bound, ~2 bytes in + 2 bytes out per channel-token): one
 // warp owns one head segment (Dk q- or k-channels, or Dv v-channels) for a
-// task of 32 consecutive tokens (three 8-warp CTAs resident per SM).  Each
-// lane holds D/32 channels.  The taps and the K-1 window rows before the task
-// are loaded once; the task is walked in sub-tiles of 4 tokens with the next
+// tile of 32 consecutive tokens (three 8-warp CTAs resident per SM).  Each
+// lane holds D/32 channels.  The taps and the K-1 window rows before the tile
+// are loaded once; the tile is walked in sub-tiles of 4 tokens with the next
 // sub-tile's rows in flight, keeping the last K-1 *valid* rows in registers
 // (as packed bf16), so every qkv element is read once.  The sub-tile loop is
 // not unrolled: the unrolled form missed the instruction cache (measured
@@ -32,9 +32,9 @@
 namespace gdn {
 namespace {
 
-constexpr int kTask = 32;       // tokens per warp task (its validity bits are one warp ballot)
+constexpr int kTile = 32;       // tokens per warp tile (its validity bits are one warp ballot)
 constexpr int kSub = 4;         // tokens per sub-tile (one sub-tile's rows in flight ahead)
-static_assert(kTask == 32, "a task's validity bits are one 32-lane ballot");
+static_assert(kTile == 32, "a tile's validity bits are one 32-lane ballot");
 constexpr int kWarps = 8;       // head segments per CTA
 constexpr int kMaxHalo = 3;     // K - 1 for the largest supported K (4)
 
@@ -158,9 +158,9 @@ __device__ __forceinline__ void unpack(const typename RawRow<CPL>::type &r, floa
     }
 }
 
-// One head segment of D channels (c0 = first channel) over one task of kTask
+// One head segment of D channels (c0 = first channel) over one tile of kTile
 // tokens, walked in sub-tiles of kSub: the taps and the K-1 window rows
-// before the task are loaded once; the next sub-tile's rows are in flight
+// before the tile are loaded once; the next sub-tile's rows are in flight
 // while the current one is computed; the window of the last K-1 valid rows
 // travels in registers.
 // kind: 0 = q (rms-norm, scale 1/D), 1 = k (rms-norm, scale 1/sqrt(D)), 2 = v.
@@ -168,10 +168,10 @@ template <int D>
 __device__ __forceinline__ void conv_segment(const ConvParams &p, int kind, int c0, uint16_t *out_base,
                                              int out_head_stride, int b, int t0, int lane) {
     constexpr int CPL = D / 32;
-    constexpr int NS = kTask / kSub;
+    constexpr int NS = kTile / kSub;
     using Raw = typename RawRow<CPL>::type;
     const int c = c0 + lane * CPL;
-    const int nt = min(kTask, p.T - t0);
+    const int nt = min(kTile, p.T - t0);
 
     unsigned valid;   // bit i: step t0 + i is valid
     if (p.mask != nullptr) {
@@ -212,7 +212,7 @@ __device__ __forceinline__ void conv_segment(const ConvParams &p, int kind, int 
             w[i][j] = jj >= 0 ? p.conv_w[(size_t)(c + i) * p.K + jj] : (uint16_t)0;
         }
 
-    // window of the K-1 valid rows before the task (zeros for unused slots),
+    // window of the K-1 valid rows before the tile (zeros for unused slots),
     // kept as the raw bf16 rows
     int codes[kMaxHalo];
     find_halo(p.mask, b, p.T, t0, lane, codes);
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) conv_update_kernel(const ConvP
     const int seg = blockIdx.y * kWarps + warp;
     const int nseg = 2 * p.Hk + p.Hv;
     if (seg >= nseg) return;
-    const int t0 = blockIdx.x * kTask;
+    const int t0 = blockIdx.x * kTile;
     const int b = blockIdx.z;
     if (seg < p.Hk) {
         uint16_t *ob = p.q + ((size_t)b * p.T * p.Hk + seg) * DK;
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(256) gating_kernel(const uint16_t *__restrict_
 template <int DK, int DV>
 cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t st) {
     const int nseg = 2 * p.Hk + p.Hv;
-    dim3 grid((p.T + kTask - 1) / kTask, (nseg + kWarps - 1) / kWarps, p.B);
+    dim3 grid((p.T + kTile - 1) / kTile, (nseg + kWarps - 1) / kWarps, p.B);
     conv_update_kernel<DK, DV><<<grid, kWarps * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
