@@ -310,8 +310,8 @@ gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, co
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_done[k], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_out[k], cudaEventDisableTiming);
     }
-    // the copy streams start after everything already on `stream`; both slots
-    // start free (their "done" and "out" events complete at that point)
+    // the copy streams start after everything already on `stream`; every slot
+    // starts free (its "done" and "out" events complete at that point)
     if (e == cudaSuccess) e = cudaEventRecord(ev_start, main);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cin, ev_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cout, ev_start, 0);

@@ -18,24 +18,27 @@
 // (dS += dy q^T, du = beta dS k, dS = g (dS - du k^T)) needs neither S nor v.
 // So the work splits into two launches:
 //  1. sweeps, one CTA (4 warps) per 32 state rows of a head and direction:
-//     the forward sweep stores S at the start of every 64-step span, the
-//     reverse sweep stores dS at the end of every span (and dS of the
-//     initial state, the output dstate_in); the two run side by side.
-//  2. spans, every (row slice, head, span) independently on a fixed grid of
-//     CTAs that each own a 32-step history buffer: from the span's S and dS
-//     it recomputes the span's first half to the middle, then for each half,
-//     last first, recomputes the half's states into the history buffer
-//     (global memory, L2-resident), keeping u per row in shared memory, and
-//     runs the full reverse steps with dS in registers.
+//     the forward sweep stores S at the start of every 32-step chunk, the
+//     reverse sweep stores dS at the end of every chunk (and dS of the
+//     initial state, the output dstate_in); the two run side by side, each
+//     loading the next chunk's inputs into registers while it steps through
+//     the current one.
+//  2. chunks, every (row slice, head, chunk) independently on a fixed grid
+//     of CTAs that each own a 32-step history buffer: from the chunk's S it
+//     recomputes the chunk's states into the history buffer (global memory,
+//     L2-resident), keeping u per row in shared memory, then runs the full
+//     reverse steps from the chunk's end dS with dS in registers.
 // Lane (rg, cg) of warp w holds rows w*8 + rg*2 + {0, 1} and columns
 // [cg*Dk/8, (cg+1)*Dk/8), so a row's dot product is a 3-level shuffle sum
 // over the 8 lanes sharing rg.  The sums over rows (dq, dk, dg, dbeta) are
 // reduced within the warp, collected per step in shared memory and added to
-// the outputs with atomics once per half-span; the atomics also sum over the
+// the outputs with atomics once per chunk; the atomics also sum over the
 // row slices and over the v-heads that share a k-head.  The call zeroes the
 // outputs first.  Where the row slices alone fill the GPU (two or more per
 // SM) the split buys no parallelism and costs the second sweep, so one
-// launch runs both sweeps per slice instead (checkpoints every half-span).
+// launch runs both sweeps per slice instead.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -44,8 +47,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kRows = 32;        // state rows per CTA
-constexpr int kC = 32;           // steps per staged half-span (history length)
-constexpr int kSpan = 2 * kC;    // steps per span (checkpoint interval)
+constexpr int kC = 32;           // steps per staged chunk (checkpoint interval, history length)
 
 struct BwdParams {
     const uint16_t *q, *k, *v;
@@ -54,10 +56,10 @@ struct BwdParams {
     const uint16_t *dy;
     const float *dstate_out;
     float *dq, *dk, *dv, *dg, *dbeta, *dstate_in;
-    float *ck;      // S at the start of every span   [B, Hv, slices, nspan, kRows, Dk]
-    float *dck;     // dS at the end of every span    [B, Hv, slices, nspan, kRows, Dk]
-    float *hist;    // one [kC, kRows, Dk] history per span-kernel CTA
-    int B, T, Hk, Hv, Dv, nck, nspan;
+    float *ck;      // S at the start of every chunk   [B, Hv, slices, nck, kRows, Dk]
+    float *dck;     // dS at the end of every chunk    [B, Hv, slices, nck, kRows, Dk] (split form)
+    float *hist;    // one [kC, kRows, Dk] history per chunk-pass CTA
+    int B, T, Hk, Hv, Dv, nck;
 };
 
 template <int DK>
@@ -83,23 +85,76 @@ __device__ __forceinline__ int red_q(int c) { return DK >= 64 ? c + ((c >= DK / 
 template <int DK>
 __device__ __forceinline__ int red_k(int c) { return DK + 5 + red_q<DK>(c); }
 
-// Stage steps [t0, t0 + n) of the chunk: q, k of the k-head, v and dy of the
-// CTA's rows, g, beta, the mask (steps past T or masked: m = 0).  Block-wide;
-// ends with a barrier.  with_q_dy = false for the forward sweep.
+// One chunk's inputs on their way from global to shared memory: each
+// thread's share of the q / k rows (4 columns per word) and of the v / dy
+// entries of the CTA's rows, and (threads < kC) one step's g, beta, mask.
 template <int DK>
-__device__ __forceinline__ void stage_chunk(const BwdParams &p, BwdSmem<DK> &s, int b, int hk, int hv, int r0,
+struct ChunkRegs {
+    static constexpr int NQK = kC * DK / 4 / kThreads;
+    static constexpr int NV = kC * kRows / kThreads;
+    static_assert(NQK * 4 * kThreads == kC * DK && NV * kThreads == kC * kRows, "chunk does not split evenly");
+    uint2 k[NQK], q[NQK];
+    uint16_t v[NV], dy[NV];
+    float g, beta;
+    int m;
+};
+
+// Loads steps [t0, t0 + kC) of the chunk: q, k of the k-head, v and dy of the
+// CTA's rows, g, beta, the mask (steps past T or masked: m = 0; past T the
+// values are zeros, g one).  with_q_dy = false for the forward direction
+// (q and dy left zero).  No shared memory is touched, so the loads of the
+// next chunk can be in flight while the current one is stepped through.
+template <int DK>
+__device__ __forceinline__ void fetch_chunk(const BwdParams &p, ChunkRegs<DK> &r, int b, int hk, int hv, int r0,
                                             int t0, bool with_q_dy) {
     const int tid = threadIdx.x;
     const int T = p.T;
-    constexpr int V4 = DK / 4;   // 4-column groups of a q / k row: one 16-byte store each
-    for (int i = tid; i < kC * V4; i += kThreads) {
-        const int tl = i / V4, c4 = (i % V4) * 4, t = t0 + tl;
-        uint2 kk = make_uint2(0u, 0u), qq = kk;
+    constexpr int V4 = DK / 4;
+#pragma unroll
+    for (int n = 0; n < ChunkRegs<DK>::NQK; ++n) {
+        const int i = tid + n * kThreads;
+        const int t = t0 + i / V4, c4 = (i % V4) * 4;
+        r.k[n] = r.q[n] = make_uint2(0u, 0u);
         if (t < T) {
             const size_t off = (((size_t)b * T + t) * p.Hk + hk) * DK + c4;
-            kk = *reinterpret_cast<const uint2 *>(p.k + off);
-            if (with_q_dy) qq = *reinterpret_cast<const uint2 *>(p.q + off);
+            r.k[n] = *reinterpret_cast<const uint2 *>(p.k + off);
+            if (with_q_dy) r.q[n] = *reinterpret_cast<const uint2 *>(p.q + off);
         }
+    }
+#pragma unroll
+    for (int n = 0; n < ChunkRegs<DK>::NV; ++n) {
+        const int i = tid + n * kThreads;
+        const int t = t0 + i / kRows, rr = i % kRows;
+        r.v[n] = r.dy[n] = 0;
+        if (t < T) {
+            const size_t off = (((size_t)b * T + t) * p.Hv + hv) * p.Dv + r0 + rr;
+            r.v[n] = p.v[off];
+            if (with_q_dy) r.dy[n] = p.dy[off];
+        }
+    }
+    r.m = 0;
+    r.g = 1.0f;
+    r.beta = 0.0f;
+    if (tid < kC && t0 + tid < T) {
+        const int t = t0 + tid;
+        r.m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
+        const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
+        r.g = p.g[gi];
+        r.beta = p.beta[gi];
+    }
+}
+
+// Writes a fetched chunk to shared memory as f32 (q / k rows with 16-byte
+// stores).  The caller synchronises before and after.
+template <int DK>
+__device__ __forceinline__ void commit_chunk(BwdSmem<DK> &s, const ChunkRegs<DK> &r) {
+    const int tid = threadIdx.x;
+    constexpr int V4 = DK / 4;
+#pragma unroll
+    for (int n = 0; n < ChunkRegs<DK>::NQK; ++n) {
+        const int i = tid + n * kThreads;
+        const int tl = i / V4, c4 = (i % V4) * 4;
+        const uint2 kk = r.k[n], qq = r.q[n];
         *reinterpret_cast<float4 *>(&s.k[tl][c4]) =
             make_float4(__uint_as_float(kk.x << 16), __uint_as_float(kk.x & 0xffff0000u),
                         __uint_as_float(kk.y << 16), __uint_as_float(kk.y & 0xffff0000u));
@@ -107,31 +162,27 @@ __device__ __forceinline__ void stage_chunk(const BwdParams &p, BwdSmem<DK> &s, 
             make_float4(__uint_as_float(qq.x << 16), __uint_as_float(qq.x & 0xffff0000u),
                         __uint_as_float(qq.y << 16), __uint_as_float(qq.y & 0xffff0000u));
     }
-    for (int i = tid; i < kC * kRows; i += kThreads) {
-        const int tl = i / kRows, r = i % kRows, t = t0 + tl;
-        float vv = 0.0f, dd = 0.0f;
-        if (t < T) {
-            const size_t off = (((size_t)b * T + t) * p.Hv + hv) * p.Dv + r0 + r;
-            vv = bf16_to_f32(p.v[off]);
-            if (with_q_dy) dd = bf16_to_f32(p.dy[off]);
-        }
-        s.v[tl][r] = vv;
-        s.dy[tl][r] = dd;
+#pragma unroll
+    for (int n = 0; n < ChunkRegs<DK>::NV; ++n) {
+        const int i = tid + n * kThreads;
+        s.v[i / kRows][i % kRows] = bf16_to_f32(r.v[n]);
+        s.dy[i / kRows][i % kRows] = bf16_to_f32(r.dy[n]);
     }
     if (tid < kC) {
-        const int t = t0 + tid;
-        int m = 0;
-        float gg = 1.0f, bb = 0.0f;
-        if (t < T) {
-            m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
-            const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
-            gg = p.g[gi];
-            bb = p.beta[gi];
-        }
-        s.m[tid] = m;
-        s.g[tid] = gg;
-        s.beta[tid] = bb;
+        s.m[tid] = r.m;
+        s.g[tid] = r.g;
+        s.beta[tid] = r.beta;
     }
+}
+
+// Stages the chunk at t0 (fetch, then commit).  Block-wide; ends with a
+// barrier.
+template <int DK>
+__device__ __forceinline__ void stage_chunk(const BwdParams &p, BwdSmem<DK> &s, int b, int hk, int hv, int r0,
+                                            int t0, bool with_q_dy) {
+    ChunkRegs<DK> r;
+    fetch_chunk<DK>(p, r, b, hk, hv, r0, t0, with_q_dy);
+    commit_chunk<DK>(s, r);
     __syncthreads();
 }
 
@@ -244,15 +295,15 @@ __device__ __forceinline__ void dS_step(const BwdSmem<DK> &s, const Lanes<DK> &L
     }
 }
 
-// The full reverse over the half-span of kC steps at t0 (at least one valid
+// The full reverse over the chunk of kC steps at t0 (at least one valid
 // step): S is the state before it (clobbered), dS the gradient of the state
 // after it, returned as the gradient of the state before it.  Recomputes the
-// half-span's states into `hist` ([kC][kRows][DK]) and adds its gradients
-// to the outputs.  Block-wide.
+// chunk's states into `hist` ([kC][kRows][DK]) and adds its gradients to the
+// outputs.  Block-wide.
 template <int DK>
-__device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s, const Lanes<DK> &L, float *hist,
-                                          int b, int hk, int hv, int r0, int t0, float (&S)[2][DK / 8],
-                                          float (&dS)[2][DK / 8]) {
+__device__ __forceinline__ void reverse_chunk(const BwdParams &p, BwdSmem<DK> &s, const Lanes<DK> &L, float *hist,
+                                           int b, int hk, int hv, int r0, int t0, float (&S)[2][DK / 8],
+                                           float (&dS)[2][DK / 8]) {
     constexpr int CW = DK / 8;
     const int tid = threadIdx.x;
     const int T = p.T;
@@ -265,7 +316,7 @@ __device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s,
         s.red_g[tid] = 0.0f;
         s.red_b[tid] = 0.0f;
     }
-    // recompute the half-span: hist[tl] = the state before step tl
+    // recompute the chunk: hist[tl] = the state before step tl
     for (int tl = 0; tl < kC; ++tl) {
         L.store(hist + (size_t)tl * kRows * DK, S);
         if (!s.m[tl]) continue;
@@ -277,7 +328,7 @@ __device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s,
         }
     }
     __syncthreads();
-    // S is now the state after the half-span; walk it backwards, the state
+    // S is now the state after the chunk; walk it backwards, the state
     // before each step read from the history one step ahead
     float Sp[2][CW];
     L.load(hist + (size_t)(kC - 1) * kRows * DK, Sp);
@@ -357,7 +408,7 @@ __device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s,
             }
     }
     __syncthreads();
-    // add the half-span's sums to the outputs (also summing over row slices
+    // add the chunk's sums to the outputs (also summing over row slices
     // and over the v-heads of the k-head)
     // (four columns per reduction: they never straddle the skew at DK/2)
     const int n = min(kC, T - t0);
@@ -377,9 +428,32 @@ __device__ __forceinline__ void reverse_half(const BwdParams &p, BwdSmem<DK> &s,
     __syncthreads();
 }
 
+// The forward direction over every chunk of a row slice, S the initial
+// state on entry and the final one on exit: stores S at the start of chunk c
+// at ck + c * kRows * DK.  The next chunk's inputs are loaded into registers
+// while the current one is stepped through.  Block-wide.
+template <int DK>
+__device__ __forceinline__ void forward_sweep(const BwdParams &p, BwdSmem<DK> &s, const Lanes<DK> &L, int b, int hk,
+                                              int hv, int r0, float *ck, float (&S)[2][DK / 8]) {
+    ChunkRegs<DK> r;
+    fetch_chunk<DK>(p, r, b, hk, hv, r0, 0, false);
+    for (int c = 0; c < p.nck; ++c) {
+        L.store(ck + (size_t)c * kRows * DK, S);
+        commit_chunk<DK>(s, r);
+        __syncthreads();
+        if (c + 1 < p.nck) fetch_chunk<DK>(p, r, b, hk, hv, r0, (c + 1) * kC, false);
+        for (int tl = 0; tl < kC; ++tl) {
+            if (!s.m[tl]) continue;   // a masked step is the identity on the state
+            float u[2];
+            fwd_step<DK>(s, L, S, tl, u);
+        }
+        __syncthreads();
+    }
+}
+
 // Launch 1: per (row slice, head) a forward-sweep CTA (blockIdx.x < slices)
-// storing S at the start of every span, and a reverse-sweep CTA storing dS
-// at the end of every span and the gradient of the initial state.
+// storing S at the start of every chunk, and a reverse-sweep CTA storing dS
+// at the end of every chunk and the gradient of the initial state.
 template <int DK>
 __global__ void __launch_bounds__(kThreads) bwd_sweep_kernel(const BwdParams p) {
     constexpr int CW = DK / 8;
@@ -392,49 +466,35 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep_kernel(const BwdParams p) 
     const int hk = hv / (p.Hv / p.Hk);
     const int r0 = slice * kRows;
     const size_t head = (size_t)b * p.Hv + hv;
-    const size_t rec = (head * nsl + slice) * (size_t)p.nspan * kRows * DK;   // this slice's span records
-    const size_t span_stride = (size_t)kRows * DK;
+    const size_t rec = (head * nsl + slice) * (size_t)p.nck * kRows * DK;   // this slice's chunk records
 
     if (!reverse) {
         float S[2][CW];
         L.load_or_zero(p.state_in == nullptr ? nullptr : p.state_in + (head * p.Dv + r0) * DK, S);
-        for (int sp = 0; sp < p.nspan; ++sp) {
-            L.store(p.ck + rec + sp * span_stride, S);
-            for (int c = 2 * sp; c < min(2 * sp + 2, p.nck); ++c) {
-                if (!chunk_active(p, b, c * kC)) continue;   // the identity on the state
-                stage_chunk<DK>(p, s, b, hk, hv, r0, c * kC, false);
-                for (int tl = 0; tl < kC; ++tl) {
-                    if (!s.m[tl]) continue;
-                    float u[2];
-                    fwd_step<DK>(s, L, S, tl, u);
-                }
-                __syncthreads();
-            }
-        }
+        forward_sweep<DK>(p, s, L, b, hk, hv, r0, p.ck + rec, S);
     } else {
         float dS[2][CW];
         L.load_or_zero(p.dstate_out == nullptr ? nullptr : p.dstate_out + (head * p.Dv + r0) * DK, dS);
-        for (int sp = p.nspan - 1; sp >= 0; --sp) {
-            L.store(p.dck + rec + sp * span_stride, dS);
-            for (int c = min(2 * sp + 1, p.nck - 1); c >= 2 * sp; --c) {
-                if (!chunk_active(p, b, c * kC)) continue;   // dS passes through
-                stage_chunk<DK>(p, s, b, hk, hv, r0, c * kC, true);
-                for (int tl = kC - 1; tl >= 0; --tl)
-                    if (s.m[tl]) dS_step<DK>(s, L, dS, tl);
-                __syncthreads();
-            }
+        ChunkRegs<DK> r;
+        fetch_chunk<DK>(p, r, b, hk, hv, r0, (p.nck - 1) * kC, true);
+        for (int c = p.nck - 1; c >= 0; --c) {
+            L.store(p.dck + rec + (size_t)c * kRows * DK, dS);
+            commit_chunk<DK>(s, r);
+            __syncthreads();
+            if (c > 0) fetch_chunk<DK>(p, r, b, hk, hv, r0, (c - 1) * kC, true);
+            for (int tl = kC - 1; tl >= 0; --tl)
+                if (s.m[tl]) dS_step<DK>(s, L, dS, tl);   // a masked step passes dS through
+            __syncthreads();
         }
         L.store(p.dstate_in + (head * p.Dv + r0) * DK, dS);
     }
 }
 
-// Launch 2: every (span, row slice, head) item independently, CTA i taking
-// items i, i + gridDim.x, ... with its own history buffer.  A span's second
-// half is reversed first, from the state at its middle (the first half
-// recomputed from the span's S) and the span's end dS; then its first half
-// from the span's S and the dS that the second half left.
+// Launch 2: every (chunk, row slice, head) item independently, CTA i taking
+// items i, i + gridDim.x, ... with its own history buffer: the chunk's
+// reverse from its S and its end dS.
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 2) bwd_span_kernel(const BwdParams p, int n_items) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_chunk_kernel(const BwdParams p, int n_items) {
     constexpr int CW = DK / 8;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdSmem<DK> &s = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
@@ -442,41 +502,26 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_span_kernel(const BwdParams p
     const int nsl = p.Dv / kRows;
     float *hist = p.hist + (size_t)blockIdx.x * kC * kRows * DK;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int sp = item % p.nspan;
-        int rest = item / p.nspan;
+        const int c = item % p.nck;
+        int rest = item / p.nck;
         const int slice = rest % nsl;
         rest /= nsl;
         const int hv = rest % p.Hv, b = rest / p.Hv;
         const int hk = hv / (p.Hv / p.Hk);
         const int r0 = slice * kRows;
-        const int c_lo = 2 * sp, c_hi = 2 * sp + 1;
-        const bool a_lo = chunk_active(p, b, c_lo * kC);
-        const bool a_hi = c_hi < p.nck && chunk_active(p, b, c_hi * kC);
-        if (!a_lo && !a_hi) continue;   // uniform: its gradients stay zero
-        const size_t rec = ((((size_t)b * p.Hv + hv) * nsl + slice) * p.nspan + sp) * kRows * DK;
+        if (!chunk_active(p, b, c * kC)) continue;   // uniform: its gradients stay zero
+        const size_t rec = ((((size_t)b * p.Hv + hv) * nsl + slice) * p.nck + c) * kRows * DK;
         float S[2][CW], dS[2][CW];
         L.load(p.dck + rec, dS);
-        for (int h = 1; h >= 0; --h) {   // second half first
-            if (!(h ? a_hi : a_lo)) continue;
-            L.load(p.ck + rec, S);
-            if (h == 1 && a_lo) {        // the state at the middle of the span
-                stage_chunk<DK>(p, s, b, hk, hv, r0, c_lo * kC, false);
-                for (int tl = 0; tl < kC; ++tl) {
-                    if (!s.m[tl]) continue;
-                    float u[2];
-                    fwd_step<DK>(s, L, S, tl, u);
-                }
-                __syncthreads();
-            }
-            reverse_half<DK>(p, s, L, hist, b, hk, hv, r0, (c_lo + h) * kC, S, dS);
-        }
+        L.load(p.ck + rec, S);
+        reverse_chunk<DK>(p, s, L, hist, b, hk, hv, r0, c * kC, S, dS);
     }
 }
 
 // Single launch for grids that fill the GPU on their own (at least two row
 // slices per SM), where the split form only adds work: one CTA per (row
-// slice, head) runs the forward sweep storing S at every half-span, then the
-// half-spans backwards with its own history buffer.
+// slice, head) runs the forward sweep storing S at every chunk, then the
+// chunks backwards with its own history buffer.
 template <int DK>
 __global__ void __launch_bounds__(kThreads, 2) bwd_fused_kernel(const BwdParams p) {
     constexpr int CW = DK / 8;
@@ -494,33 +539,22 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_fused_kernel(const BwdParams 
 
     float S[2][CW];
     L.load_or_zero(p.state_in == nullptr ? nullptr : p.state_in + (head * p.Dv + r0) * DK, S);
-    for (int c = 0; c < p.nck; ++c) {
-        L.store(ck + (size_t)c * kRows * DK, S);
-        if (!chunk_active(p, b, c * kC)) continue;   // the identity on the state
-        stage_chunk<DK>(p, s, b, hk, hv, r0, c * kC, false);
-        for (int tl = 0; tl < kC; ++tl) {
-            if (!s.m[tl]) continue;
-            float u[2];
-            fwd_step<DK>(s, L, S, tl, u);
-        }
-        __syncthreads();
-    }
+    forward_sweep<DK>(p, s, L, b, hk, hv, r0, ck, S);
     float dS[2][CW];
     L.load_or_zero(p.dstate_out == nullptr ? nullptr : p.dstate_out + (head * p.Dv + r0) * DK, dS);
     for (int c = p.nck - 1; c >= 0; --c) {
         if (!chunk_active(p, b, c * kC)) continue;   // dS passes through; its gradients stay zero
         L.load(ck + (size_t)c * kRows * DK, S);
-        reverse_half<DK>(p, s, L, hist, b, hk, hv, r0, c * kC, S, dS);
+        reverse_chunk<DK>(p, s, L, hist, b, hk, hv, r0, c * kC, S, dS);
     }
     L.store(p.dstate_in + (head * p.Dv + r0) * DK, dS);
 }
 
-// Workspace layout of either form: the fused form keeps S every half-span
-// (rec) and a history per CTA; the split form S and dS every span (2 x rec)
-// and a history per span-pass CTA.
+// Workspace layout of either form: S at the start of every chunk (rec), the
+// split form also dS at the end of every chunk (dck), and a history per CTA.
 struct Layout {
     bool fused;
-    int nsl, nck, nspan, items, slots;
+    int nsl, nck, items, slots;
     size_t rec_floats, dck_floats, hist_floats;
 };
 
@@ -528,19 +562,17 @@ Layout layout_of(const Sizes &s) {
     Layout l;
     l.nsl = s.Dv / kRows;
     l.nck = (s.T + kC - 1) / kC;
-    l.nspan = (s.T + kSpan - 1) / kSpan;
     const long slices = (long)s.B * s.Hv * l.nsl;
     l.fused = slices >= 2L * num_sms();
+    l.rec_floats = (size_t)slices * l.nck * kRows * s.Dk;
     if (l.fused) {
         l.items = 0;
         l.slots = (int)slices;
-        l.rec_floats = (size_t)slices * l.nck * kRows * s.Dk;
         l.dck_floats = 0;
     } else {
-        const long items = slices * l.nspan;
+        const long items = slices * l.nck;
         l.items = (int)items;
         l.slots = (int)std::min<long>(items, 2L * num_sms());
-        l.rec_floats = (size_t)items * kRows * s.Dk;
         l.dck_floats = l.rec_floats;
     }
     l.hist_floats = (size_t)l.slots * kC * kRows * s.Dk;
@@ -550,9 +582,9 @@ Layout layout_of(const Sizes &s) {
 template <int DK>
 cudaError_t launch_bwd_t(const Sizes &s, const Layout &l, const BwdParams &p, cudaStream_t st) {
     const size_t smem = sizeof(BwdSmem<DK>);
-    static unsigned long long done_sweep = 0, done_span = 0, done_fused = 0;   // per instantiation, per device
+    static unsigned long long done_sweep = 0, done_chunk = 0, done_fused = 0;   // per instantiation, per device
     cudaError_t e = set_max_smem(done_sweep, bwd_sweep_kernel<DK>, smem);
-    if (e == cudaSuccess) e = set_max_smem(done_span, bwd_span_kernel<DK>, smem);
+    if (e == cudaSuccess) e = set_max_smem(done_chunk, bwd_chunk_kernel<DK>, smem);
     if (e == cudaSuccess) e = set_max_smem(done_fused, bwd_fused_kernel<DK>, smem);
     if (e != cudaSuccess) return e;
     if (l.fused) {
@@ -562,7 +594,7 @@ cudaError_t launch_bwd_t(const Sizes &s, const Layout &l, const BwdParams &p, cu
     bwd_sweep_kernel<DK><<<dim3(2 * l.nsl, s.Hv, s.B), kThreads, smem, st>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess || l.items == 0) return e;
-    bwd_span_kernel<DK><<<l.slots, kThreads, smem, st>>>(p, l.items);
+    bwd_chunk_kernel<DK><<<l.slots, kThreads, smem, st>>>(p, l.items);
     return cudaGetLastError();
 }
 
@@ -587,11 +619,12 @@ cudaError_t launch_backward(const Sizes &s, const uint16_t *q, const uint16_t *k
     if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, ng * sizeof(float), st);
     if (e != cudaSuccess) return e;
     const Layout l = layout_of(s);
+    if (!l.fused && (long)s.B * s.Hv * l.nsl * l.nck > (long)INT_MAX) return cudaErrorNotSupported;   // item index
     float *ck = static_cast<float *>(ws);
     float *dck = ck + l.rec_floats;
     float *hist = dck + l.dck_floats;
     BwdParams p{q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta, dstate_in,
-                ck, dck, hist, s.B, s.T, s.Hk, s.Hv, s.Dv, l.nck, l.nspan};
+                ck, dck, hist, s.B, s.T, s.Hk, s.Hv, s.Dv, l.nck};
     switch (s.Dk) {
         case 32: return launch_bwd_t<32>(s, l, p, st);
         case 64: return launch_bwd_t<64>(s, l, p, st);

@@ -311,10 +311,13 @@ GDN_API gdn_status gdn_prefill_noalloc(const gdn_dims *dims, const uint16_t *q, 
  *              when state_in is NULL); may equal dstate_out
  *   workspace  device scratch of gdn_prefill_backward_workspace_size() bytes,
  *              16-byte aligned (required when B * T > 0): the forward state
- *              and its gradient at every 64-step span boundary (2 x 16 KiB
- *              per 32 state rows and span at Dk = 128) and one 32-step
- *              history per CTA of the span pass (at most two per SM of the
- *              current device, so query the size on the device that runs it)
+ *              at the start of every 32-step chunk (16 KiB per 32 state rows
+ *              and chunk at Dk = 128), for batches with fewer than two row
+ *              slices of 32 rows per SM also its gradient at every chunk's
+ *              end, and one 32-step history per CTA of the pass that
+ *              reverses the chunks (one per row slice, or at most two per SM
+ *              of the current device, so query the size on the device that
+ *              runs it)
  * The outputs are summed with atomics, so for Hv/Hk > 2 or Dv > 32 their
  * last bits can differ between runs.  Supports Dk, Dv in {32, 64, 128}. */
 GDN_API size_t gdn_prefill_backward_workspace_size(const gdn_dims *dims);
