@@ -59,6 +59,7 @@ struct BwdParams {
     float *ck;      // S at the start of every chunk   [B, Hv, slices, nck, kRows, Dk]
     float *dck;     // dS at the end of every chunk    [B, Hv, slices, nck, kRows, Dk] (split form)
     float *hist;    // one [kC, kRows, Dk] history per chunk-pass CTA
+    const int *order;   // row slot -> batch row, longest first (masked batches), or null
     int B, T, Hk, Hv, Dv, nck;
 };
 
@@ -72,6 +73,7 @@ struct BwdSmem {
     // red_q / red_k below for the layout
     float red[kC][2 * DK + 8];
     float red_g[kC], red_b[kC];
+    int range[2];   // first and last valid step of the row (valid_chunks)
 };
 
 // Index of column c's dq / dk sum in a row of BwdSmem::red.  After the
@@ -192,6 +194,43 @@ __device__ __forceinline__ bool chunk_active(const BwdParams &p, int b, int t0) 
     const int t = t0 + (int)threadIdx.x;
     const bool m = threadIdx.x < kC && t < p.T && p.mask[(size_t)b * p.T + t] != 0;
     return __syncthreads_or(m) != 0;
+}
+
+// The chunks [c_begin, c_end) of row b from its first to its last valid
+// step ([0, nck) without a mask; empty for a wholly masked row): outside them
+// the state and its gradient pass through unchanged.  Block-wide.
+template <int DK>
+__device__ __forceinline__ void valid_chunks(const BwdParams &p, BwdSmem<DK> &s, int b, int &c_begin, int &c_end) {
+    if (p.mask == nullptr) {
+        c_begin = 0;
+        c_end = p.nck;
+        return;
+    }
+    if (threadIdx.x == 0) {
+        s.range[0] = INT_MAX;
+        s.range[1] = -1;
+    }
+    __syncthreads();
+    const uint8_t *mrow = p.mask + (size_t)b * p.T;
+    int lo = INT_MAX, hi = -1;
+#pragma unroll 8
+    for (int t = threadIdx.x; t < p.T; t += kThreads)
+        if (mrow[t] != 0) {
+            lo = min(lo, t);
+            hi = t;
+        }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if ((threadIdx.x & 31u) == 0) {
+        atomicMin(&s.range[0], lo);
+        atomicMax(&s.range[1], hi);
+    }
+    __syncthreads();
+    lo = s.range[0];
+    hi = s.range[1];
+    __syncthreads();
+    c_begin = hi < 0 ? 0 : lo / kC;
+    c_end = hi < 0 ? 0 : hi / kC + 1;
 }
 
 // sum over the 8 lanes of a row group (lanes differing in bits 0-2)
@@ -428,20 +467,22 @@ __device__ __forceinline__ void reverse_chunk(const BwdParams &p, BwdSmem<DK> &s
     __syncthreads();
 }
 
-// The forward direction over every chunk of a row slice, S the initial
-// state on entry and the final one on exit: stores S at the start of chunk c
-// at ck + c * kRows * DK.  The next chunk's inputs are loaded into registers
-// while the current one is stepped through.  Block-wide.
+// The forward direction over chunks [c_begin, c_end) of a row slice, S the
+// initial state on entry and the final one on exit: stores S at the start of
+// chunk c at ck + c * kRows * DK.  The next chunk's inputs are loaded into
+// registers while the current one is stepped through.  Block-wide.
 template <int DK>
 __device__ __forceinline__ void forward_sweep(const BwdParams &p, BwdSmem<DK> &s, const Lanes<DK> &L, int b, int hk,
-                                              int hv, int r0, float *ck, float (&S)[2][DK / 8]) {
+                                              int hv, int r0, int c_begin, int c_end, float *ck,
+                                              float (&S)[2][DK / 8]) {
+    if (c_begin >= c_end) return;
     ChunkRegs<DK> r;
-    fetch_chunk<DK>(p, r, b, hk, hv, r0, 0, false);
-    for (int c = 0; c < p.nck; ++c) {
+    fetch_chunk<DK>(p, r, b, hk, hv, r0, c_begin * kC, false);
+    for (int c = c_begin; c < c_end; ++c) {
         L.store(ck + (size_t)c * kRows * DK, S);
         commit_chunk<DK>(s, r);
         __syncthreads();
-        if (c + 1 < p.nck) fetch_chunk<DK>(p, r, b, hk, hv, r0, (c + 1) * kC, false);
+        if (c + 1 < c_end) fetch_chunk<DK>(p, r, b, hk, hv, r0, (c + 1) * kC, false);
         for (int tl = 0; tl < kC; ++tl) {
             if (!s.m[tl]) continue;   // a masked step is the identity on the state
             float u[2];
@@ -462,26 +503,29 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep_kernel(const BwdParams p) 
     const Lanes<DK> L;
     const int nsl = p.Dv / kRows;
     const bool reverse = (int)blockIdx.x >= nsl;
-    const int slice = blockIdx.x % nsl, hv = blockIdx.y, b = blockIdx.z;
+    const int slice = blockIdx.x % nsl, hv = blockIdx.y;
+    const int b = p.order != nullptr ? p.order[blockIdx.z] : (int)blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
     const int r0 = slice * kRows;
     const size_t head = (size_t)b * p.Hv + hv;
     const size_t rec = (head * nsl + slice) * (size_t)p.nck * kRows * DK;   // this slice's chunk records
+    int c_begin, c_end;
+    valid_chunks<DK>(p, s, b, c_begin, c_end);
 
     if (!reverse) {
         float S[2][CW];
         L.load_or_zero(p.state_in == nullptr ? nullptr : p.state_in + (head * p.Dv + r0) * DK, S);
-        forward_sweep<DK>(p, s, L, b, hk, hv, r0, p.ck + rec, S);
+        forward_sweep<DK>(p, s, L, b, hk, hv, r0, c_begin, c_end, p.ck + rec, S);
     } else {
         float dS[2][CW];
         L.load_or_zero(p.dstate_out == nullptr ? nullptr : p.dstate_out + (head * p.Dv + r0) * DK, dS);
         ChunkRegs<DK> r;
-        fetch_chunk<DK>(p, r, b, hk, hv, r0, (p.nck - 1) * kC, true);
-        for (int c = p.nck - 1; c >= 0; --c) {
+        if (c_begin < c_end) fetch_chunk<DK>(p, r, b, hk, hv, r0, (c_end - 1) * kC, true);
+        for (int c = c_end - 1; c >= c_begin; --c) {
             L.store(p.dck + rec + (size_t)c * kRows * DK, dS);
             commit_chunk<DK>(s, r);
             __syncthreads();
-            if (c > 0) fetch_chunk<DK>(p, r, b, hk, hv, r0, (c - 1) * kC, true);
+            if (c > c_begin) fetch_chunk<DK>(p, r, b, hk, hv, r0, (c - 1) * kC, true);
             for (int tl = kC - 1; tl >= 0; --tl)
                 if (s.m[tl]) dS_step<DK>(s, L, dS, tl);   // a masked step passes dS through
             __syncthreads();
@@ -529,20 +573,23 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_fused_kernel(const BwdParams 
     BwdSmem<DK> &s = *reinterpret_cast<BwdSmem<DK> *>(smem_raw);
     const Lanes<DK> L;
     const int nsl = p.Dv / kRows;
-    const int slice = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+    const int slice = blockIdx.x, hv = blockIdx.y;
+    const int b = p.order != nullptr ? p.order[blockIdx.z] : (int)blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
     const int r0 = slice * kRows;
     const size_t head = (size_t)b * p.Hv + hv;
     const size_t cta = head * nsl + slice;
     float *ck = p.ck + cta * (size_t)p.nck * kRows * DK;
     float *hist = p.hist + cta * (size_t)kC * kRows * DK;
+    int c_begin, c_end;
+    valid_chunks<DK>(p, s, b, c_begin, c_end);
 
     float S[2][CW];
     L.load_or_zero(p.state_in == nullptr ? nullptr : p.state_in + (head * p.Dv + r0) * DK, S);
-    forward_sweep<DK>(p, s, L, b, hk, hv, r0, ck, S);
+    forward_sweep<DK>(p, s, L, b, hk, hv, r0, c_begin, c_end, ck, S);
     float dS[2][CW];
     L.load_or_zero(p.dstate_out == nullptr ? nullptr : p.dstate_out + (head * p.Dv + r0) * DK, dS);
-    for (int c = p.nck - 1; c >= 0; --c) {
+    for (int c = c_end - 1; c >= c_begin; --c) {
         if (!chunk_active(p, b, c * kC)) continue;   // dS passes through; its gradients stay zero
         L.load(ck + (size_t)c * kRows * DK, S);
         reverse_chunk<DK>(p, s, L, hist, b, hk, hv, r0, c * kC, S, dS);
@@ -602,7 +649,7 @@ cudaError_t launch_bwd_t(const Sizes &s, const Layout &l, const BwdParams &p, cu
 
 size_t backward_workspace(const Sizes &s) {
     const Layout l = layout_of(s);
-    return (l.rec_floats + l.dck_floats + l.hist_floats) * sizeof(float);
+    return row_order_workspace(s) + (l.rec_floats + l.dck_floats + l.hist_floats) * sizeof(float);
 }
 
 cudaError_t launch_backward(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -620,11 +667,19 @@ cudaError_t launch_backward(const Sizes &s, const uint16_t *q, const uint16_t *k
     if (e != cudaSuccess) return e;
     const Layout l = layout_of(s);
     if (!l.fused && (long)s.B * s.Hv * l.nsl * l.nck > (long)INT_MAX) return cudaErrorNotSupported;   // item index
-    float *ck = static_cast<float *>(ws);
+    // rows longest first (the row order's scratch, a multiple of 256 bytes,
+    // leads the workspace)
+    const int *order = nullptr;
+    if (mask != nullptr && s.B > 1) {
+        e = launch_row_order(s, mask, ws, st);
+        if (e != cudaSuccess) return e;
+        order = static_cast<const int *>(ws);
+    }
+    float *ck = reinterpret_cast<float *>(static_cast<char *>(ws) + row_order_workspace(s));
     float *dck = ck + l.rec_floats;
     float *hist = dck + l.dck_floats;
     BwdParams p{q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta, dstate_in,
-                ck, dck, hist, s.B, s.T, s.Hk, s.Hv, s.Dv, l.nck};
+                ck, dck, hist, order, s.B, s.T, s.Hk, s.Hv, s.Dv, l.nck};
     switch (s.Dk) {
         case 32: return launch_bwd_t<32>(s, l, p, st);
         case 64: return launch_bwd_t<64>(s, l, p, st);
