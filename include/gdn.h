@@ -310,7 +310,8 @@ GDN_API gdn_status gdn_prefill_noalloc(const gdn_dims *dims, const uint16_t *q, 
  *   dstate_in  f32  [B, Hv, Dv, Dk] (out): gradient of the initial state (also
  *              when state_in is NULL); may equal dstate_out
  *   workspace  device scratch of gdn_prefill_backward_workspace_size() bytes,
- *              16-byte aligned (required when B * T > 0): the forward state
+ *              16-byte aligned (required when B * T > 0): a longest-first
+ *              row order for masked batches, the forward state
  *              at the start of every 32-step chunk (16 KiB per 32 state rows
  *              and chunk at Dk = 128), for batches with fewer than two row
  *              slices of 32 rows per SM also its gradient at every chunk's
