@@ -334,6 +334,95 @@ __device__ __forceinline__ void dS_step(const BwdSmem<DK> &s, const Lanes<DK> &L
     }
 }
 
+// One full reverse step at tl of the chunk staged at t0: X holds the state
+// after the step, Sp the state before it, dS the gradient of the state after
+// it (returned as that of the state before it).  X is read first (for dq)
+// and then reloaded with the state before step tl - 1 from the history, so
+// two buffers in alternating roles carry the walk with no copies.  Adds the
+// step's dq / dk column sums and dg / dbeta to the chunk's shared sums and
+// writes dv.  Block-wide (the mask is uniform).
+template <int DK>
+__device__ __forceinline__ void reverse_step(const BwdParams &p, BwdSmem<DK> &s, const Lanes<DK> &L,
+                                             const float *hist, int b, int hv, int r0, int t0, int tl,
+                                             float (&X)[2][DK / 8], const float (&Sp)[2][DK / 8],
+                                             float (&dS)[2][DK / 8]) {
+    constexpr int CW = DK / 8;
+    const bool live = s.m[tl] != 0;
+    float dq_p[CW];
+#pragma unroll
+    for (int j = 0; j < CW; ++j) dq_p[j] = 0.0f;
+    if (live) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float dyv = s.dy[tl][L.rl[i]];
+#pragma unroll
+            for (int j = 0; j < CW; ++j) dq_p[j] = fmaf(X[i][j], dyv, dq_p[j]);
+        }
+    }
+    if (tl > 0) L.load(hist + (size_t)(tl - 1) * kRows * DK, X);
+    if (!live) return;   // a masked step passes dS through
+    const float gg = s.g[tl], bb = s.beta[tl];
+    float dk_p[CW];
+#pragma unroll
+    for (int j = 0; j < CW; ++j) dk_p[j] = 0.0f;
+    float dg_p = 0.0f, db_p = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float dyv = s.dy[tl][L.rl[i]];
+        const float ui = s.u[tl][L.rl[i]];
+        float dd = 0.0f;
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+            dS[i][j] = fmaf(dyv, s.q[tl][L.col(j)], dS[i][j]);
+            dd = fmaf(dS[i][j], s.k[tl][L.col(j)], dd);
+        }
+        dd = row_sum(dd);                       // ddelta of the row
+        const float dl = bb * ui;               // delta
+        const float du = bb * dd;
+        if (L.cg == 0) {
+            db_p = fmaf(dd, ui, db_p);
+            p.dv[(((size_t)b * p.T + t0 + tl) * p.Hv + hv) * p.Dv + r0 + L.rl[i]] = du;
+        }
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+            dk_p[j] = fmaf(dS[i][j], dl, dk_p[j]);
+            dS[i][j] = fmaf(-du, s.k[tl][L.col(j)], dS[i][j]);
+            dk_p[j] = fmaf(-gg * Sp[i][j], du, dk_p[j]);
+            dg_p = fmaf(dS[i][j], Sp[i][j], dg_p);
+            dS[i][j] *= gg;
+        }
+    }
+    // sum the 2*CW partials (dq, dk) over the warp's four row groups in two
+    // exchanges that halve the vector: lanes whose rg differs in bit 0 swap
+    // halves (dq <-> dk), then lanes whose rg differs in bit 1 swap quarters,
+    // so each lane ends with CW/2 summed columns (of dq for even rg, dk for
+    // odd) and adds those; the pairwise sums are those of a per-column
+    // shuffle sum
+    const bool hi0 = (L.rg & 1) != 0, hi1 = (L.rg & 2) != 0;
+    float h[CW];
+#pragma unroll
+    for (int j = 0; j < CW; ++j) {
+        const float send = hi0 ? dq_p[j] : dk_p[j];
+        const float keep = hi0 ? dk_p[j] : dq_p[j];
+        h[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    constexpr int HQ = CW / 2;
+    const int off = hi1 ? HQ : 0;
+#pragma unroll
+    for (int j = 0; j < HQ; ++j) {
+        const float send = hi1 ? h[j] : h[HQ + j];
+        const float keep = hi1 ? h[HQ + j] : h[j];
+        const int c = L.col(off + j);
+        atomicAdd(&s.red[tl][hi0 ? red_k<DK>(c) : red_q<DK>(c)], keep + __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+    dg_p = warp_sum(dg_p);
+    db_p = warp_sum(db_p);
+    if (L.lane == 0) {
+        atomicAdd(&s.red_g[tl], dg_p);
+        atomicAdd(&s.red_b[tl], db_p);
+    }
+}
+
 // The full reverse over the chunk of kC steps at t0 (at least one valid
 // step): S is the state before it (clobbered), dS the gradient of the state
 // after it, returned as the gradient of the state before it.  Recomputes the
@@ -367,84 +456,15 @@ __device__ __forceinline__ void reverse_chunk(const BwdParams &p, BwdSmem<DK> &s
         }
     }
     __syncthreads();
-    // S is now the state after the chunk; walk it backwards, the state
-    // before each step read from the history one step ahead
-    float Sp[2][CW];
-    L.load(hist + (size_t)(kC - 1) * kRows * DK, Sp);
-    for (int tl = kC - 1; tl >= 0; --tl) {
-        float Sn[2][CW];   // S_{t-2}, for the next reverse step
-        if (tl > 0) L.load(hist + (size_t)(tl - 1) * kRows * DK, Sn);
-        if (s.m[tl]) {
-            const float gg = s.g[tl], bb = s.beta[tl];
-            float dq_p[CW], dk_p[CW];
-#pragma unroll
-            for (int j = 0; j < CW; ++j) dq_p[j] = dk_p[j] = 0.0f;
-            float dg_p = 0.0f, db_p = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float dyv = s.dy[tl][L.rl[i]];
-                const float ui = s.u[tl][L.rl[i]];
-                float dd = 0.0f;
-#pragma unroll
-                for (int j = 0; j < CW; ++j) {
-                    dS[i][j] = fmaf(dyv, s.q[tl][L.col(j)], dS[i][j]);
-                    dq_p[j] = fmaf(S[i][j], dyv, dq_p[j]);
-                    dd = fmaf(dS[i][j], s.k[tl][L.col(j)], dd);
-                }
-                dd = row_sum(dd);                       // ddelta of the row
-                const float dl = bb * ui;               // delta
-                const float du = bb * dd;
-                if (L.cg == 0) {
-                    db_p = fmaf(dd, ui, db_p);
-                    p.dv[(((size_t)b * T + t0 + tl) * p.Hv + hv) * p.Dv + r0 + L.rl[i]] = du;
-                }
-#pragma unroll
-                for (int j = 0; j < CW; ++j) {
-                    dk_p[j] = fmaf(dS[i][j], dl, dk_p[j]);
-                    dS[i][j] = fmaf(-du, s.k[tl][L.col(j)], dS[i][j]);
-                    dk_p[j] = fmaf(-gg * Sp[i][j], du, dk_p[j]);
-                    dg_p = fmaf(dS[i][j], Sp[i][j], dg_p);
-                    dS[i][j] *= gg;
-                }
-            }
-            // sum the 2*CW partials (dq, dk) over the warp's four row
-            // groups in two exchanges that halve the vector: lanes whose
-            // rg differs in bit 0 swap halves (dq <-> dk), then lanes whose
-            // rg differs in bit 1 swap quarters, so each lane ends with
-            // CW/2 summed columns (of dq for even rg, dk for odd) and adds
-            // those; the pairwise sums are those of a per-column shuffle sum
-            const bool hi0 = (L.rg & 1) != 0, hi1 = (L.rg & 2) != 0;
-            float h[CW];
-#pragma unroll
-            for (int j = 0; j < CW; ++j) {
-                const float send = hi0 ? dq_p[j] : dk_p[j];
-                const float keep = hi0 ? dk_p[j] : dq_p[j];
-                h[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-            constexpr int HQ = CW / 2;
-            const int off = hi1 ? HQ : 0;
-#pragma unroll
-            for (int j = 0; j < HQ; ++j) {
-                const float send = hi1 ? h[j] : h[HQ + j];
-                const float keep = hi1 ? h[HQ + j] : h[j];
-                const int c = L.col(off + j);
-                atomicAdd(&s.red[tl][hi0 ? red_k<DK>(c) : red_q<DK>(c)],
-                          keep + __shfl_xor_sync(0xffffffffu, send, 16));
-            }
-            dg_p = warp_sum(dg_p);
-            db_p = warp_sum(db_p);
-            if (L.lane == 0) {
-                atomicAdd(&s.red_g[tl], dg_p);
-                atomicAdd(&s.red_b[tl], db_p);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int j = 0; j < CW; ++j) {
-                S[i][j] = Sp[i][j];
-                Sp[i][j] = Sn[i][j];
-            }
+    // S is now the state after the chunk; walk it backwards with S and Y in
+    // alternating roles (see reverse_step), Y first the state before the
+    // chunk's last step
+    float Y[2][CW];
+    L.load(hist + (size_t)(kC - 1) * kRows * DK, Y);
+    static_assert(kC % 2 == 0, "the reverse walks the chunk in pairs of steps");
+    for (int tl = kC - 1; tl >= 1; tl -= 2) {
+        reverse_step<DK>(p, s, L, hist, b, hv, r0, t0, tl, S, Y, dS);
+        reverse_step<DK>(p, s, L, hist, b, hv, r0, t0, tl - 1, Y, S, dS);
     }
     __syncthreads();
     // add the chunk's sums to the outputs (also summing over row slices
