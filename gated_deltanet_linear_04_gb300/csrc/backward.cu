@@ -233,6 +233,10 @@ __device__ __forceinline__ void valid_chunks(const BwdParams &p, BwdSmem<DK> &s,
     c_end = hi < 0 ? 0 : hi / kC + 1;
 }
 
+// Four partial sums of a dot product (the lane's columns j with j % 4 = 0..3,
+// four independent chains instead of one) added in a fixed order.
+__device__ __forceinline__ float sum4(const float (&x)[4]) { return (x[0] + x[1]) + (x[2] + x[3]); }
+
 // sum over the 8 lanes of a row group (lanes differing in bits 0-2)
 __device__ __forceinline__ float row_sum(float x) {
     x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -297,10 +301,10 @@ __device__ __forceinline__ void fwd_step(const BwdSmem<DK> &s, const Lanes<DK> &
     const float gg = s.g[tl], bb = s.beta[tl];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        float kv = 0.0f;
+        float kv4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int j = 0; j < CW; ++j) kv = fmaf(S[i][j], s.k[tl][L.col(j)], kv);
-        kv = gg * row_sum(kv);
+        for (int j = 0; j < CW; ++j) kv4[j & 3] = fmaf(S[i][j], s.k[tl][L.col(j)], kv4[j & 3]);
+        const float kv = gg * row_sum(sum4(kv4));
         u[i] = s.v[tl][L.rl[i]] - kv;
         const float dl = bb * u[i];
 #pragma unroll
@@ -318,13 +322,13 @@ __device__ __forceinline__ void dS_step(const BwdSmem<DK> &s, const Lanes<DK> &L
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const float dyv = s.dy[tl][L.rl[i]];
-        float dd = 0.0f;
+        float dd4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int j = 0; j < CW; ++j) {
             dS[i][j] = fmaf(dyv, s.q[tl][L.col(j)], dS[i][j]);
-            dd = fmaf(dS[i][j], s.k[tl][L.col(j)], dd);
+            dd4[j & 3] = fmaf(dS[i][j], s.k[tl][L.col(j)], dd4[j & 3]);
         }
-        dd = row_sum(dd);
+        const float dd = row_sum(sum4(dd4));
         const float du = bb * dd;
 #pragma unroll
         for (int j = 0; j < CW; ++j) {
@@ -370,15 +374,16 @@ __device__ __forceinline__ void reverse_step(const BwdParams &p, BwdSmem<DK> &s,
     for (int i = 0; i < 2; ++i) {
         const float dyv = s.dy[tl][L.rl[i]];
         const float ui = s.u[tl][L.rl[i]];
-        float dd = 0.0f;
+        float dd4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int j = 0; j < CW; ++j) {
             dS[i][j] = fmaf(dyv, s.q[tl][L.col(j)], dS[i][j]);
-            dd = fmaf(dS[i][j], s.k[tl][L.col(j)], dd);
+            dd4[j & 3] = fmaf(dS[i][j], s.k[tl][L.col(j)], dd4[j & 3]);
         }
-        dd = row_sum(dd);                       // ddelta of the row
+        const float dd = row_sum(sum4(dd4));    // ddelta of the row
         const float dl = bb * ui;               // delta
         const float du = bb * dd;
+        const float ngdu = -gg * du;
         if (L.cg == 0) {
             db_p = fmaf(dd, ui, db_p);
             p.dv[(((size_t)b * p.T + t0 + tl) * p.Hv + hv) * p.Dv + r0 + L.rl[i]] = du;
@@ -387,7 +392,7 @@ __device__ __forceinline__ void reverse_step(const BwdParams &p, BwdSmem<DK> &s,
         for (int j = 0; j < CW; ++j) {
             dk_p[j] = fmaf(dS[i][j], dl, dk_p[j]);
             dS[i][j] = fmaf(-du, s.k[tl][L.col(j)], dS[i][j]);
-            dk_p[j] = fmaf(-gg * Sp[i][j], du, dk_p[j]);
+            dk_p[j] = fmaf(Sp[i][j], ngdu, dk_p[j]);
             dg_p = fmaf(dS[i][j], Sp[i][j], dg_p);
             dS[i][j] *= gg;
         }
