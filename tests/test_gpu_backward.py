@@ -26,6 +26,7 @@ BWD_CASES = [
     (1, 130, 1, 1, 64, 128, "sparse", False, False),
     (1, 1024, 1, 2, 128, 128, "random", True, True),     # long: error growth over many steps
     (2, 70, 16, 64, 128, 128, "random", True, True),     # 512 row slices: the single-launch form
+    (1, 50, 16, 80, 64, 128, None, True, False),         # 320 row slices, no mask: single launch, Dk = 64
 ]
 
 
