@@ -28,7 +28,10 @@ its reason, in the design notes of the repository):
 
 Pinned by ``tests/test_oracle_pins.py`` against closed forms, invariants,
 library routines and hand-derived values in ``tests/golden/``.  The chunked
-form (``chunked_head``) is pinned against the sequential definition.
+form (``chunked_head``) is pinned against the sequential definition.  The
+reverse pass (``head_recurrence_bwd``) is pinned by central finite
+differences of the forward (``tests/test_oracle_bwd_pins.py``), and the
+chunked reverse (``chunked_head_bwd``) against it.
 """
 from __future__ import annotations
 
@@ -588,3 +591,120 @@ def chunked_head(q, k, v, g, beta, S0, mask=None, chunk=64):
         y[sl] = Y
     y[~valid] = 0.0
     return y, S
+
+
+def chunked_head_bwd(q, k, v, g, beta, S0, dy, dST=None, mask=None, chunk=64):
+    """Gradients of chunked_head (the reverse of its chunk products), the same
+    values as head_recurrence_bwd; exists to pin the derivation of a chunked
+    backward.  The forward pass keeps each chunk's start state S0; then the
+    chunks in reverse, G the gradient of the state at the chunk's end (dST,
+    or 0, for the last one), with the forward quantities of chunked_head and
+    R = V - diag(gamma) K S0^T, Z = diag(beta) R (so Dl = Tm Z), P = M o Q K^T,
+    F = exp(lg_n - lg), E[r,i] = exp(lg_r - lg_i):
+      dDl  = diag(F) K G^T + P^T dY        dP = dY Dl^T
+      dZ   = Tm^T dDl                      dA = -(dZ Dl^T), strictly lower
+      dR   = diag(beta) dZ                 dV = dR
+      dQ   = diag(gamma) dY S0 + (dP o M) K
+      dK   = diag(F) Dl G + (dP o M)^T Q - diag(gamma) dR S0 + (H + H^T) K,
+             H = dA o beta_r E (strictly lower)
+      dbeta= rowsum(dZ o R) + rowsum(dA o E o K K^T)
+      dS0  = gamma_n G + dY^T diag(gamma) Q - dR^T diag(gamma) K   (G of the
+             chunk before)
+    and the decays through their log prefix sums: gamma_r = exp(lg_r) (in the
+    Q S0^T and K S0^T terms), E (in A and M), F and gamma_n (in S_C); then
+    dlog g_i = sum_{r >= i} dlg_r and dg = dlog g / g.  Masked steps enter
+    with g = 1, beta = 0 and dy = 0; their dg and dbeta are zero."""
+    from scipy.linalg import solve_triangular
+
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    g = np.asarray(g, np.float64).copy()
+    beta = np.asarray(beta, np.float64).copy()
+    dy = np.asarray(dy, np.float64).copy()
+    T, Dk = q.shape
+    Dv = v.shape[1]
+    valid = np.ones(T, bool) if mask is None else (np.asarray(mask) != 0)
+    g[~valid] = 1.0
+    beta[~valid] = 0.0
+    dy[~valid] = 0.0
+    S = np.zeros((Dv, Dk)) if S0 is None else np.array(S0, dtype=np.float64, copy=True)
+    starts = list(range(0, T, chunk))
+    S_at = []
+    for c0 in starts:                                   # forward: each chunk's start state
+        S_at.append(S.copy())
+        sl = slice(c0, min(c0 + chunk, T))
+        _, S = _chunk_forward(q[sl], k[sl], v[sl], g[sl], beta[sl], S, solve_triangular)
+    out = {"dq": np.zeros((T, Dk)), "dk": np.zeros((T, Dk)), "dv": np.zeros((T, Dv)), "dg": np.zeros(T),
+           "dbeta": np.zeros(T)}
+    G = np.zeros((Dv, Dk)) if dST is None else np.array(dST, dtype=np.float64, copy=True)
+    for c0, S0c in zip(reversed(starts), reversed(S_at)):
+        sl = slice(c0, min(c0 + chunk, T))
+        Qc, Kc, Vc, gc, bc, dYc = q[sl], k[sl], v[sl], g[sl], beta[sl], dy[sl]
+        f, _ = _chunk_forward(Qc, Kc, Vc, gc, bc, S0c, solve_triangular)
+        lg, gam, E, Tm, Dl, M = f["lg"], f["gam"], f["E"], f["Tm"], f["Dl"], f["M"]
+        n = Qc.shape[0]
+        KK = Kc @ Kc.T
+        P = M * (Qc @ Kc.T)
+        F = np.exp(lg[-1] - lg)
+        R = Vc - gam[:, None] * (Kc @ S0c.T)
+        Z = bc[:, None] * R
+        # S_C = gamma_n S0 + Dl^T diag(F) K
+        dDl = F[:, None] * (Kc @ G.T) + P.T @ dYc
+        dF = np.sum((Dl @ G) * Kc, axis=1)
+        dgam_n = np.sum(G * S0c)
+        dK = F[:, None] * (Dl @ G)
+        dS0 = gam[-1] * G
+        # Y = diag(gamma) Q S0^T + P Dl
+        dQ = gam[:, None] * (dYc @ S0c)
+        dS0 += dYc.T @ (gam[:, None] * Qc)
+        dgam = np.sum(dYc * (Qc @ S0c.T), axis=1)
+        dP = dYc @ Dl.T
+        dPM = dP * M
+        dQ += dPM @ Kc
+        dK += dPM.T @ Qc
+        dE = dP * (Qc @ Kc.T) * np.tril(np.ones((n, n)))
+        # Dl = Tm Z, Tm = (I + A)^-1
+        dZ = Tm.T @ dDl
+        dA = -np.tril(dZ @ Dl.T, -1)
+        dR = bc[:, None] * dZ
+        dbeta = np.sum(dZ * R, axis=1)
+        # R = V - diag(gamma) K S0^T
+        dV = dR
+        dK -= gam[:, None] * (dR @ S0c)
+        dS0 -= dR.T @ (gam[:, None] * Kc)
+        dgam -= np.sum(dR * (Kc @ S0c.T), axis=1)
+        # A[r,i] = beta_r E[r,i] (K K^T)[r,i], i < r
+        dbeta += np.sum(dA * E * KK, axis=1)
+        H = dA * bc[:, None] * E
+        dK += (H + H.T) @ Kc
+        dE += dA * bc[:, None] * KK
+        # the decays through lg
+        X = dE * E
+        dlg = dgam * gam + X.sum(axis=1) - X.sum(axis=0) - dF * F
+        dlg[-1] += np.sum(dF * F) + dgam_n * gam[-1]
+        dlog_g = np.cumsum(dlg[::-1])[::-1]
+        out["dq"][sl] = dQ
+        out["dk"][sl] = dK
+        out["dv"][sl] = dV
+        out["dg"][sl] = dlog_g / gc
+        out["dbeta"][sl] = dbeta
+        G = dS0
+    out["dg"][~valid] = 0.0
+    out["dbeta"][~valid] = 0.0
+    out["dS0"] = G
+    return out
+
+
+def _chunk_forward(Qc, Kc, Vc, gc, bc, S0c, solve_triangular):
+    """One chunk of chunked_head: its intermediate products and end state."""
+    n = Qc.shape[0]
+    lg = np.cumsum(np.log(gc))
+    gam = np.exp(lg)
+    E = np.exp(lg[:, None] - lg[None, :])
+    A = np.tril(bc[:, None] * E * (Kc @ Kc.T), -1)
+    Tm = solve_triangular(np.eye(n) + A, np.eye(n), lower=True, unit_diagonal=True)
+    Dl = Tm @ (bc[:, None] * Vc) - Tm @ ((bc * gam)[:, None] * Kc) @ S0c.T
+    M = np.tril(E)
+    S = gam[-1] * S0c + Dl.T @ (np.exp(lg[-1] - lg)[:, None] * Kc)
+    return {"lg": lg, "gam": gam, "E": E, "Tm": Tm, "Dl": Dl, "M": M}, S

@@ -130,3 +130,27 @@ def test_bwd_sums_q_k_gradients_over_shared_heads(oracle_mod):
                     km[t, j] -= h
                 fd[t, j] = (loss(qp, kp) - loss(qm, km)) / (2 * h)
         assert np.abs(out[which][0, :, 0] - fd).max() <= 1e-6 * max(1.0, np.abs(fd).max()), which
+
+
+@pytest.mark.parametrize("T,Dk,Dv,chunk,seed,masked,with_s0", [
+    (9, 4, 3, 4, 1, False, True),      # two full chunks and a one-step tail
+    (20, 8, 6, 7, 2, True, True),      # chunk size that divides nothing
+    (33, 16, 8, 64, 3, True, False),   # one partial chunk
+    (50, 8, 8, 1, 4, False, True),     # chunks of one step: the sequential reverse itself
+    (70, 8, 12, 16, 5, True, True),
+])
+def test_chunked_bwd_matches_sequential_reverse(T, Dk, Dv, chunk, seed, masked, with_s0, oracle_mod):
+    """The chunked backward (the reverse of the chunk products, in numpy) and
+    the step-by-step reverse (in C) are independent derivations of the same
+    gradient; they agree to rounding."""
+    x, Wy, WS = _inputs(T, Dk, Dv, seed, masked, with_s0)
+    ref = oracle_mod.head_recurrence_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], Wy, WS, x["mask"])
+    got = oracle_mod.chunked_head_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["S0"], Wy, WS, x["mask"],
+                                      chunk=chunk)
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dS0"):
+        err = np.linalg.norm(got[name] - ref[name]) / max(np.linalg.norm(ref[name]), 1e-300)
+        assert err < 1e-12, (name, err)
+    if x["mask"] is not None:
+        off = x["mask"] == 0
+        for name in ("dq", "dk", "dv", "dg", "dbeta"):
+            assert np.all(got[name][off] == 0.0), name
