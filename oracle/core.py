@@ -701,7 +701,9 @@ def _chunk_forward(Qc, Kc, Vc, gc, bc, S0c, solve_triangular):
     n = Qc.shape[0]
     lg = np.cumsum(np.log(gc))
     gam = np.exp(lg)
-    E = np.exp(lg[:, None] - lg[None, :])
+    # decay ratios on and below the diagonal (exponents <= 0); zero above,
+    # where the unused ratios could overflow
+    E = np.tril(np.exp(np.tril(lg[:, None] - lg[None, :])))
     A = np.tril(bc[:, None] * E * (Kc @ Kc.T), -1)
     Tm = solve_triangular(np.eye(n) + A, np.eye(n), lower=True, unit_diagonal=True)
     Dl = Tm @ (bc[:, None] * Vc) - Tm @ ((bc * gam)[:, None] * Kc) @ S0c.T
