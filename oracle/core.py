@@ -610,10 +610,12 @@ def chunked_head_bwd(q, k, v, g, beta, S0, dy, dST=None, mask=None, chunk=64):
       dbeta= rowsum(dZ o R) + rowsum(dA o E o K K^T)
       dS0  = gamma_n G + dY^T diag(gamma) Q - dR^T diag(gamma) K   (G of the
              chunk before)
-    and the decays through their log prefix sums: gamma_r = exp(lg_r) (in the
-    Q S0^T and K S0^T terms), E (in A and M), F and gamma_n (in S_C); then
-    dlog g_i = sum_{r >= i} dlg_r and dg = dlog g / g.  Masked steps enter
-    with g = 1, beta = 0 and dy = 0; their dg and dbeta are zero."""
+    and the decays: gamma_r = exp(lg_r) (in the Q S0^T and K S0^T terms), E
+    (in A and M), F and gamma_n (in S_C) with lg_r = sum_{i<=r} log g_i, so
+    dlog g_t collects the terms that log g_t scales (gamma_r for r >= t, F_r
+    for r < t, gamma_n, E[r,i] for i < t <= r) and dg = dlog g / g.  Masked
+    steps enter with g = 1, beta = 0 and dy = 0; their dg and dbeta are
+    zero."""
     from scipy.linalg import solve_triangular
 
     q = np.asarray(q, np.float64)
@@ -679,11 +681,15 @@ def chunked_head_bwd(q, k, v, g, beta, S0, dy, dST=None, mask=None, chunk=64):
         H = dA * bc[:, None] * E
         dK += (H + H.T) @ Kc
         dE += dA * bc[:, None] * KK
-        # the decays through lg
+        # the decays: log g_t shifts lg_r for every r >= t, so it scales
+        # gamma_r (r >= t), F_r (r < t), gamma_n and E[r,i] for i < t <= r;
+        # summing exactly those terms (each carries the factor g_t) keeps
+        # dlog g_t / g_t accurate where g_t is tiny, which differences of
+        # prefix sums do not
         X = dE * E
-        dlg = dgam * gam + X.sum(axis=1) - X.sum(axis=0) - dF * F
-        dlg[-1] += np.sum(dF * F) + dgam_n * gam[-1]
-        dlog_g = np.cumsum(dlg[::-1])[::-1]
+        a_g = dgam * gam
+        f_g = dF * F
+        dlog_g = np.array([a_g[t:].sum() + f_g[:t].sum() + X[t:, :t].sum() for t in range(n)]) + dgam_n * gam[-1]
         out["dq"][sl] = dQ
         out["dk"][sl] = dK
         out["dv"][sl] = dV
