@@ -1,7 +1,7 @@
 """Thin Python binding of the C ABI in include/gdn.h (ctypes).
 
-Argument marshalling only: every function here checks tensor dtypes, devices
-and contiguity, passes raw device pointers and the current CUDA stream to the
+Argument marshalling only: every function here checks tensor dtypes, devices,
+contiguity and element counts, passes raw device pointers and the current CUDA stream to the
 library, and raises ``GdnError`` on a non-zero status.  All arithmetic runs in
 the CUDA kernels of libgdn.so; there is no fallback.  PyTorch provides device
 memory and streams.
@@ -130,6 +130,28 @@ def _check(status: int, where: str):
         raise GdnError(status, where)
 
 
+class _Counts:
+    """Element counts of every buffer of the ABI for given dims (the layouts
+    of include/gdn.h); the library sees only addresses, so the binding
+    compares each tensor's size with these before passing it on."""
+
+    def __init__(self, d: GdnDims):
+        B, T, Hk, Hv, Dk, Dv, K = d.B, d.T, d.Hk, d.Hv, d.Dk, d.Dv, d.K
+        C = 2 * Hk * Dk + Hv * Dv
+        self.qkv, self.conv_w, self.conv_state = B * T * C, C * K, B * (K - 1) * C
+        self.mask, self.qk, self.v, self.gate = B * T, B * T * Hk * Dk, B * T * Hv * Dv, B * T * Hv
+        self.head, self.state, self.row, self.norm_w = Hv, B * Hv * Dv * Dk, B, Dv
+        self.g_vec = B * T * Hv * Dk
+
+
+def _sizes(where: str, *items):
+    """Raises if a given tensor's element count differs from the expected one
+    (items: (name, tensor or None, count))."""
+    for name, t, n in items:
+        if isinstance(t, torch.Tensor) and t.numel() != n:
+            raise ValueError("%s: %s must hold %d elements for these dims, got %d" % (where, name, n, t.numel()))
+
+
 BF16, F32, U8 = torch.bfloat16, torch.float32, torch.uint8
 
 
@@ -138,6 +160,10 @@ BF16, F32, U8 = torch.bfloat16, torch.float32, torch.uint8
 # ---------------------------------------------------------------------------
 def gdn_conv_update(dims, qkv, conv_w, conv_state, mask, q, k, v, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_conv_update", ("qkv", qkv, n.qkv), ("conv_w", conv_w, n.conv_w),
+           ("conv_state", conv_state, n.conv_state), ("mask", mask, n.mask), ("q", q, n.qk), ("k", k, n.qk),
+           ("v", v, n.v))
     _check(lib().gdn_conv_update(ctypes.byref(d), _ptr(qkv, BF16, "qkv"), _ptr(conv_w, BF16, "conv_w"),
                                  _ptr(conv_state, BF16, "conv_state"), _ptr(mask, U8, "mask"), _ptr(q, BF16, "q"),
                                  _ptr(k, BF16, "k"), _ptr(v, BF16, "v"), _stream(stream)), "gdn_conv_update")
@@ -145,6 +171,9 @@ def gdn_conv_update(dims, qkv, conv_w, conv_state, mask, q, k, v, stream=None):
 
 def gdn_gating(dims, a, b, A_log, dt_bias, g, beta, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_gating", ("a", a, n.gate), ("b", b, n.gate), ("A_log", A_log, n.head), ("dt_bias", dt_bias, n.head),
+           ("g", g, n.gate), ("beta", beta, n.gate))
     _check(lib().gdn_gating(ctypes.byref(d), _ptr(a, BF16, "a"), _ptr(b, BF16, "b"), _ptr(A_log, F32, "A_log"),
                             _ptr(dt_bias, F32, "dt_bias"), _ptr(g, F32, "g"), _ptr(beta, F32, "beta"),
                             _stream(stream)), "gdn_gating")
@@ -152,6 +181,10 @@ def gdn_gating(dims, a, b, A_log, dt_bias, g, beta, stream=None):
 
 def gdn_recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, y, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_recurrent_decode", ("qkv", qkv, n.qkv), ("conv_w", conv_w, n.conv_w),
+           ("conv_state", conv_state, n.conv_state), ("a", a, n.gate), ("b", b, n.gate), ("A_log", A_log, n.head),
+           ("dt_bias", dt_bias, n.head), ("state", state, n.state), ("row_mask", row_mask, n.row), ("y", y, n.v))
     _check(lib().gdn_recurrent_decode(ctypes.byref(d), _ptr(qkv, BF16, "qkv"), _ptr(conv_w, BF16, "conv_w"),
                                       _ptr(conv_state, BF16, "conv_state"), _ptr(a, BF16, "a"), _ptr(b, BF16, "b"),
                                       _ptr(A_log, F32, "A_log"), _ptr(dt_bias, F32, "dt_bias"),
@@ -161,6 +194,10 @@ def gdn_recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, st
 
 def gdn_decode_window(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep, y, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_decode_window", ("qkv", qkv, n.qkv), ("conv_w", conv_w, n.conv_w),
+           ("conv_state", conv_state, n.conv_state), ("a", a, n.gate), ("b", b, n.gate), ("A_log", A_log, n.head),
+           ("dt_bias", dt_bias, n.head), ("state", state, n.state), ("keep", keep, n.row), ("y", y, n.v))
     _check(lib().gdn_decode_window(ctypes.byref(d), _ptr(qkv, BF16, "qkv"), _ptr(conv_w, BF16, "conv_w"),
                                    _ptr(conv_state, BF16, "conv_state"), _ptr(a, BF16, "a"), _ptr(b, BF16, "b"),
                                    _ptr(A_log, F32, "A_log"), _ptr(dt_bias, F32, "dt_bias"),
@@ -176,6 +213,10 @@ def gdn_decode_host_staging_size(dims) -> int:
 def gdn_recurrent_decode_host_steps(dims, n_steps, qkv_h, a_h, b_h, y_h, conv_w, conv_state, A_log, dt_bias, state,
                                     row_mask, staging, stream=None):
     d = make_dims(dims)
+    n1 = _Counts(d)
+    _sizes("gdn_recurrent_decode_host_steps", ("conv_w", conv_w, n1.conv_w),
+           ("conv_state", conv_state, n1.conv_state), ("A_log", A_log, n1.head), ("dt_bias", dt_bias, n1.head),
+           ("state", state, n1.state), ("row_mask", row_mask, n1.row))
     n = int(n_steps)
     for name, t, shape in (("qkv_h", qkv_h, (n, dims.B, d.Hk * d.Dk * 2 + d.Hv * d.Dv)),
                            ("a_h", a_h, (n, dims.B, d.Hv)), ("b_h", b_h, (n, dims.B, d.Hv)),
@@ -204,6 +245,10 @@ def gdn_prefill_workspace_size(dims, chunk: int) -> int:
 
 def gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, workspace=None, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_prefill", ("q", q, n.qk), ("k", k, n.qk), ("v", v, n.v), ("g", g, n.gate), ("beta", beta, n.gate),
+           ("state_in", state_in, n.state), ("state_out", state_out, n.state), ("mask", mask, n.mask),
+           ("y", y, n.v))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     ws_ptr = None if workspace is None else (workspace.data_ptr() or None)
     _check(lib().gdn_prefill(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
@@ -215,6 +260,11 @@ def gdn_prefill(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, w
 def gdn_recurrent_decode_gated(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask, z, norm_w,
                                norm_eps, out, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_recurrent_decode_gated", ("qkv", qkv, n.qkv), ("conv_w", conv_w, n.conv_w),
+           ("conv_state", conv_state, n.conv_state), ("a", a, n.gate), ("b", b, n.gate), ("A_log", A_log, n.head),
+           ("dt_bias", dt_bias, n.head), ("state", state, n.state), ("row_mask", row_mask, n.row), ("z", z, n.v),
+           ("norm_w", norm_w, n.norm_w), ("out", out, n.v))
     _check(lib().gdn_recurrent_decode_gated(ctypes.byref(d), _ptr(qkv, BF16, "qkv"), _ptr(conv_w, BF16, "conv_w"),
                                             _ptr(conv_state, BF16, "conv_state"), _ptr(a, BF16, "a"),
                                             _ptr(b, BF16, "b"), _ptr(A_log, F32, "A_log"),
@@ -227,6 +277,10 @@ def gdn_recurrent_decode_gated(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bi
 def gdn_prefill_gated(dims, q, k, v, g, beta, state_in, state_out, mask, z, norm_w, norm_eps, out, chunk=0,
                       workspace=None, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_prefill_gated", ("q", q, n.qk), ("k", k, n.qk), ("v", v, n.v), ("g", g, n.gate),
+           ("beta", beta, n.gate), ("state_in", state_in, n.state), ("state_out", state_out, n.state),
+           ("mask", mask, n.mask), ("z", z, n.v), ("norm_w", norm_w, n.norm_w), ("out", out, n.v))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     ws_ptr = None if workspace is None else (workspace.data_ptr() or None)
     _check(lib().gdn_prefill_gated(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
@@ -244,6 +298,11 @@ def gdn_prefill_backward_workspace_size(dims) -> int:
 def gdn_prefill_backward(dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta, dstate_in,
                          workspace, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_prefill_backward", ("q", q, n.qk), ("k", k, n.qk), ("v", v, n.v), ("g", g, n.gate),
+           ("beta", beta, n.gate), ("state_in", state_in, n.state), ("mask", mask, n.mask), ("dy", dy, n.v),
+           ("dstate_out", dstate_out, n.state), ("dq", dq, n.qk), ("dk", dk, n.qk), ("dv", dv, n.v),
+           ("dg", dg, n.gate), ("dbeta", dbeta, n.gate), ("dstate_in", dstate_in, n.state))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     ws_ptr = None if workspace is None else (workspace.data_ptr() or None)
     _check(lib().gdn_prefill_backward(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
@@ -259,6 +318,10 @@ def gdn_prefill_noalloc(dims, q, k, v, g, beta, state_in, state_out, mask, y, ch
     """gdn_prefill with the library's own fixed scratch (no workspace, no
     allocation); for callers that cannot allocate device memory."""
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_prefill_noalloc", ("q", q, n.qk), ("k", k, n.qk), ("v", v, n.v), ("g", g, n.gate),
+           ("beta", beta, n.gate), ("state_in", state_in, n.state), ("state_out", state_out, n.state),
+           ("mask", mask, n.mask), ("y", y, n.v))
     _check(lib().gdn_prefill_noalloc(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
                                      _ptr(g, F32, "g"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
                                      _ptr(state_out, F32, "state_out"), _ptr(mask, U8, "mask"),
@@ -267,6 +330,8 @@ def gdn_prefill_noalloc(dims, q, k, v, g, beta, state_in, state_out, mask, y, ch
 
 def gdn_rmsnorm_gated(dims, y, z, norm_w, norm_eps, out, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_rmsnorm_gated", ("y", y, n.v), ("z", z, n.v), ("norm_w", norm_w, n.norm_w), ("out", out, n.v))
     _check(lib().gdn_rmsnorm_gated(ctypes.byref(d), _ptr(y, BF16, "y"), _ptr(z, BF16, "z"),
                                    _ptr(norm_w, F32, "norm_w"), float(norm_eps), _ptr(out, BF16, "out"),
                                    _stream(stream)), "gdn_rmsnorm_gated")
@@ -274,6 +339,10 @@ def gdn_rmsnorm_gated(dims, y, z, norm_w, norm_eps, out, stream=None):
 
 def gdn_prefill_vec(dims, q, k, v, g_vec, beta, state_in, state_out, mask, y, stream=None):
     d = make_dims(dims)
+    n = _Counts(d)
+    _sizes("gdn_prefill_vec", ("q", q, n.qk), ("k", k, n.qk), ("v", v, n.v), ("g_vec", g_vec, n.g_vec),
+           ("beta", beta, n.gate), ("state_in", state_in, n.state), ("state_out", state_out, n.state),
+           ("mask", mask, n.mask), ("y", y, n.v))
     _check(lib().gdn_prefill_vec(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
                                  _ptr(g_vec, F32, "g_vec"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
                                  _ptr(state_out, F32, "state_out"), _ptr(mask, U8, "mask"), _ptr(y, BF16, "y"),
