@@ -37,3 +37,13 @@ def test_active_chunks_counts_chunks_with_a_valid_step():
     holes = torch.zeros((1, T), dtype=torch.uint8)
     holes[0, 130] = 1                                               # one valid step in chunk 2
     assert bench.active_chunks(holes, T, 1) == 1
+
+
+def test_profiled_traffic_only_for_the_profiled_source(monkeypatch):
+    """roofline.traffic comes from the committed decode profile while the
+    decode kernel's source hashes to the value recorded there, else null."""
+    got = bench.profiled_traffic("decode_b128_ncu.md", ["decode.cu", "common.cuh"])
+    assert got is not None and 4.0e8 < got < 6.0e8                  # read + write bytes of one launch
+    monkeypatch.setattr(bench, "source_hash", lambda *names: "0" * 16)
+    assert bench.profiled_traffic("decode_b128_ncu.md", ["decode.cu", "common.cuh"]) is None
+    assert bench.profiled_traffic("no_such_profile.md", ["decode.cu"]) is None
