@@ -39,11 +39,15 @@ def test_active_chunks_counts_chunks_with_a_valid_step():
     assert bench.active_chunks(holes, T, 1) == 1
 
 
-def test_profiled_traffic_only_for_the_profiled_source(monkeypatch):
-    """roofline.traffic comes from the committed decode profile while the
-    decode kernel's source hashes to the value recorded there, else null."""
-    got = bench.profiled_traffic("decode_b128_ncu.md", ["decode.cu", "common.cuh"])
-    assert got is not None and 4.0e8 < got < 6.0e8                  # read + write bytes of one launch
+def test_profiled_traffic_only_for_the_profiled_source(monkeypatch, tmp_path):
+    """roofline.traffic comes from a committed profile summary only while the
+    profiled kernel source hashes to the value recorded in it, else null."""
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "k.md").write_text("source_hash: abcdef0123456789   (note)\n"
+                                                "dram_bytes_per_launch: 495584000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda *names: "abcdef0123456789")
+    assert bench.profiled_traffic("k.md", ["decode.cu"]) == 495584000.0
     monkeypatch.setattr(bench, "source_hash", lambda *names: "0" * 16)
-    assert bench.profiled_traffic("decode_b128_ncu.md", ["decode.cu", "common.cuh"]) is None
-    assert bench.profiled_traffic("no_such_profile.md", ["decode.cu"]) is None
+    assert bench.profiled_traffic("k.md", ["decode.cu"]) is None
+    assert bench.profiled_traffic("missing.md", ["decode.cu"]) is None
