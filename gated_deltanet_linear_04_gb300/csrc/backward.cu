@@ -26,17 +26,21 @@
 //  2. chunks, every (row slice, head, chunk) independently on a fixed grid
 //     of CTAs that each own a 32-step history buffer: from the chunk's S it
 //     recomputes the chunk's states into the history buffer (global memory,
-//     L2-resident), keeping u per row in shared memory, then runs the full
-//     reverse steps from the chunk's end dS with dS in registers.
-// Lane (rg, cg) of warp w holds rows w*8 + rg*2 + {0, 1} and columns
-// [cg*Dk/8, (cg+1)*Dk/8), so a row's dot product is a 3-level shuffle sum
-// over the 8 lanes sharing rg.  The sums over rows (dq, dk, dg, dbeta) are
+//     read back while it is still in L2 as far as it fits), keeping u per
+//     row in shared memory, then runs the full reverse steps from the
+//     chunk's end dS with dS in registers.
+// Every CTA walks only the chunks from its row's first to its last valid
+// step, and with a mask the rows are handed out longest first.
+// Lane (rg, cg) of warp w holds rows w*8 + rg*2 + {0, 1} and the Dk/8
+// columns of the 16-byte column groups cg, cg + 8, ... (see Lanes), so a
+// row's dot product is a 3-level shuffle sum over the 8 lanes sharing rg.  The sums over rows (dq, dk, dg, dbeta) are
 // reduced within the warp, collected per step in shared memory and added to
 // the outputs with atomics once per chunk; the atomics also sum over the
 // row slices and over the v-heads that share a k-head.  The call zeroes the
 // outputs first.  Where the row slices alone fill the GPU (two or more per
 // SM) the split buys no parallelism and costs the second sweep, so one
-// launch runs both sweeps per slice instead.
+// launch runs, per slice, the forward sweep and then the chunks in reverse,
+// carrying dS from chunk to chunk.
 #include <climits>
 
 #include "common.cuh"
