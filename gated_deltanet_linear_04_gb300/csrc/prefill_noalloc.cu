@@ -11,7 +11,10 @@
 // and outputs.
 //
 // Every GPU that loads the library holds the array (32 KiB) until the process
-// exits.  All calls share it: two calls whose work overlaps on the GPU (on
+// exits.  The array is too small for the per-chunk images of the two-pass
+// chunked form, so chunk = 64 always runs the single pass here: the same
+// results, but slower than gdn_prefill with its full workspace when the batch
+// has fewer heads than the GPU has SMs.  All calls share it: two calls whose work overlaps on the GPU (on
 // different streams, or from different host threads) race on it and must be
 // ordered by the caller.  Each call writes all of the scratch it reads before
 // reading it, so nothing has to be cleared between calls.
@@ -32,7 +35,9 @@ void *g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device, looked up once
-// per device (in host code the array's name is not a device address).
+// per device (in host code the array's name is not a device address).  The
+// address is cached for the life of the process; a device reset between calls
+// would leave it stale, which the header states is not supported.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -23,6 +23,9 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libgdn.so")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = range(5)
 
+# batch rows gdn_prefill_noalloc accepts (GDN_NOALLOC_MAX_ROWS in gdn.h)
+GDN_NOALLOC_MAX_ROWS = 4096
+
 
 class GdnError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -484,9 +487,9 @@ def prefill_vec(dims, q, k, v, g_vec, beta, state_in=None, mask=None, stream=Non
 
 
 def core_prefill(dims, qkv, conv_w, a, b, A_log, dt_bias, conv_state=None, state_in=None, mask=None, chunk=0,
-                 stream=None):
+                 stream=None, use_workspace=True):
     """conv -> gates -> recurrence; returns (y, state_out).  conv_state (if
     given) is updated in place."""
     q, k, v = conv_update(dims, qkv, conv_w, conv_state, mask, stream)
     g, beta = gating(dims, a, b, A_log, dt_bias, stream)
-    return prefill(dims, q, k, v, g, beta, state_in, mask, chunk, None, stream)
+    return prefill(dims, q, k, v, g, beta, state_in, mask, chunk, None, stream, use_workspace)

@@ -130,8 +130,11 @@ GDN_API gdn_status gdn_recurrent_decode(const gdn_dims *dims, const uint16_t *qk
  *              step i runs
  * Host buffers should be page-locked (cudaHostAlloc / pinned): pageable
  * memory is accepted but its copies do not overlap the kernels.  The copies
- * run on two streams created for the call (cudaMemcpyAsync, one per tensor
- * and step) and ordered against `stream` with events; everything is enqueued
+ * run on two copy streams of the library (cudaMemcpyAsync, one per tensor and
+ * step) and are ordered against `stream` with events; the streams and events
+ * are created on a device's first call and kept until the process exits, and
+ * calls from several host threads enqueue one after the other (a lock per
+ * device; their copies then share the two streams).  Everything is enqueued
  * before the call returns and `stream` completes after the last y has
  * arrived, so synchronise `stream` before reading y_h.  Neither host buffer
  * may be written (inputs) or read (y_h) before that.  n_steps = 0 is a no-op.
@@ -286,9 +289,19 @@ GDN_API gdn_status gdn_prefill_vec(const gdn_dims *dims, const uint16_t *q, cons
  *   dims->B above GDN_NOALLOC_MAX_ROWS gives GDN_ERR_UNSUPPORTED.
  * The first call on each device looks up that array's device address
  * (cudaGetSymbolAddress, with that device current); make it before capturing
- * any stream.  All calls share the array: calls that overlap on the GPU (other
- * streams, other host threads) race on it, so order them.  Nothing in it needs
- * clearing between calls.  No allocation is made by this call. */
+ * any stream.  The address is kept for the life of the process: a device
+ * reset (cudaDeviceReset, or a reset of the primary context) between calls
+ * leaves it stale and is not supported.  All calls share the array: calls that
+ * overlap on the GPU (other streams, other host threads) race on it, so order
+ * them.  Nothing in it needs clearing between calls.  No allocation is made by
+ * this call.
+ * Speed: the array holds only the row order, not the per-chunk images of the
+ * two-pass chunked form, so with chunk = 64 this call always runs the single
+ * pass.  Results are bit-identical to gdn_prefill's, but when B * Hv is below
+ * the number of SMs the single pass keeps only B * Hv SMs busy: at B = 1,
+ * Hv = 32, T = 8192 it takes about 2.7 times as long as gdn_prefill given
+ * its full workspace.  With B * Hv at or above the SM count both calls run
+ * the same kernels. */
 #define GDN_NOALLOC_MAX_ROWS 4096
 GDN_API gdn_status gdn_prefill_noalloc(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
                                        const uint16_t *v, const float *g, const float *beta,

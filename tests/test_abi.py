@@ -126,3 +126,10 @@ def test_decode_host_steps_staging_and_validation(lib):
     buf = ctypes.create_string_buffer(4096)
     p = (ctypes.addressof(buf) + 15) // 16 * 16
     assert f(ctypes.byref(d), 3, *([p] * 11), n - 1, None) == 1
+
+
+def test_binding_constants_match_the_header():
+    from gated_deltanet_linear_04_gb300 import gdn
+    txt = open(HEADER).read()
+    m = re.search(r"#define\s+GDN_NOALLOC_MAX_ROWS\s+(\d+)", txt)
+    assert m and int(m.group(1)) == gdn.GDN_NOALLOC_MAX_ROWS
