@@ -86,6 +86,22 @@ def active_chunks(mask, T: int, B: int, C: int = 64) -> int:
 # tf32 : bf16 dense tensor rate on GB300 (1.1 vs 2.25 PFLOP/s nominal)
 TF32_PER_BF16 = 1.1 / 2.25
 
+# FP32 pipe of GB300: 152 SMs x 128 FP32 lanes, one fused multiply-add
+# (2 flops) per lane and clock
+GB300_SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def fp32_peak_tflops(sm_mhz: float) -> float:
+    return GB300_SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def conv_bytes(d: wl.Dims, n_valid: int) -> int:
+    """Algorithmic bytes of one conv_update call: every valid token's qkv row
+    read and its q, k, v rows written (bf16), the taps, and the conv_state read
+    and written; padded tokens' zero outputs are written too (B*T*C*2 out)."""
+    return n_valid * d.C * 2 + d.B * d.T * d.C * 2 + d.C * d.K * 2 + 2 * d.B * (d.K - 1) * d.C * 2
+
 
 # ---------------------------------------------------------------------------
 # environment: peaks, clocks, ranks
@@ -97,8 +113,9 @@ def load_peaks() -> dict:
             j = json.load(f)
         return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
                 "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
-                "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+                "sm_max_mhz": float(j.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
 
 
 class ClockSampler:
@@ -234,6 +251,93 @@ def oracle_decode_rate(w: wl.Workload, budget_s: float) -> dict:
     by = decode_bytes(d)
     return {"steps": steps, "seconds": t_used, "state_gbs": by["state_rw"] * steps / t_used / 1e9,
             "tokens_per_s": d.B * steps / t_used, "cores": threads}
+
+
+def oracle_prefill_rate(w: wl.Workload, heads_per_row: int = 0, vec: bool = False, budget_s: float = 0.0) -> dict:
+    """The oracle over whole heads of a prefill workload: every batch row, at
+    the workload's full T and row lengths, `heads_per_row` v-heads of it,
+    drawn with the workload's distributions (the dims reduced to those heads:
+    one k-head shared by them; all Hv heads = the workload itself, its own
+    seeded inputs).  The heads run in parallel, one per core.  Without
+    `heads_per_row`, a first run with one head per core sizes a second, timed
+    run to about `budget_s` seconds (at most the whole workload).  With `vec`,
+    the recurrence with one decay factor per key channel over the same shapes
+    (gates drawn like the vectorized benchmark's).  Returns tokens/s of the
+    whole workload: valid head-steps done / Hv / seconds."""
+    d = w.dims
+    cores = os.cpu_count() or 1
+    if not heads_per_row:
+        n0 = min(d.Hv, max(1, cores // d.B))
+        first = oracle_prefill_rate(w, n0, vec)
+        if budget_s <= 0:
+            return first
+        n_h = min(d.Hv, max(n0, int(n0 * budget_s / max(first["seconds"], 1e-3)) // n0 * n0))
+        return first if n_h == n0 else oracle_prefill_rate(w, n_h, vec)
+    import oracle
+    oracle.build_oracle()
+    n_h = heads_per_row
+    ds = d if n_h == d.Hv else d.with_(Hk=1, Hv=n_h)
+    seed = 1000 + w.index
+    p = wl.make_params(ds, seed)
+    a = wl.make_activations(ds, seed + 7919)
+    st = wl.make_states(ds, seed + 15485863, w.conv_state, w.state)
+    lens = wl.workload_lengths(w) if w.ragged else torch.full((d.B,), d.T, dtype=torch.int64)
+    mask = wl.right_padded_mask(lens, d.T).numpy() if w.ragged else None
+    pairs = [(b, hv) for b in range(ds.B) for hv in range(ds.Hv)]
+    threads = min(cores, len(pairs))
+    s0 = st["state"].numpy().astype(np.float64)
+    if not vec:
+        bits = {k: wl.bf16_bits(v) for k, v in (("qkv", a["qkv"]), ("a", a["a"]), ("b", a["b"]),
+                                                 ("conv_w", p["conv_w"]), ("conv_state", st["conv_state"]))}
+        t0 = time.perf_counter()
+        oracle.layer_core(ds, bits["qkv"], bits["conv_w"], bits["a"], bits["b"], p["A_log"].numpy(),
+                          p["dt_bias"].numpy(), bits["conv_state"], s0, mask, pairs, threads)
+        sec = time.perf_counter() - t0
+        what = "full core (conv, gates, recurrence)"
+    else:
+        gen = torch.Generator().manual_seed(6000 + w.index)
+        q = torch.randn((ds.B, ds.T, ds.Hk, ds.Dk), generator=gen)
+        k = torch.randn((ds.B, ds.T, ds.Hk, ds.Dk), generator=gen)
+        q = (q / q.norm(dim=-1, keepdim=True) / ds.Dk ** 0.5).to(torch.bfloat16)
+        k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+        v = torch.randn((ds.B, ds.T, ds.Hv, ds.Dv), generator=gen).to(torch.bfloat16)
+        gv = torch.exp(-torch.rand((ds.B, ds.T, ds.Hv, ds.Dk), generator=gen) * 0.5).double().numpy()
+        beta = torch.sigmoid(torch.randn((ds.B, ds.T, ds.Hv), generator=gen)).double().numpy()
+        t0 = time.perf_counter()
+        oracle.recurrence_vec(ds, wl.bf16_bits(q), wl.bf16_bits(k), wl.bf16_bits(v), gv, beta, s0, mask, threads)
+        sec = time.perf_counter() - t0
+        what = "recurrence with per-channel decay"
+    head_steps = int(lens.sum().item()) * n_h
+    return {"value": round(head_steps / d.Hv / sec, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "seconds": round(sec, 3),
+            "sample": "%d of %d v-heads per row, all %d rows at T=%d (%d valid head-steps), f64 oracle %s" % (
+                n_h, d.Hv, d.B, d.T, head_steps, what)}
+
+
+def oracle_decode_b1_rate(w: wl.Workload, budget_s: float) -> dict:
+    """The oracle over the single-sequence decode workload's first carried
+    steps (all heads), as many as fit the time budget."""
+    import oracle
+    oracle.build_oracle()
+    d = w.dims
+    inp = wl.workload_inputs(w)
+    cw = wl.bf16_bits(inp["conv_w"])
+    A_log, dt = inp["A_log"].numpy(), inp["dt_bias"].numpy()
+    cs = wl.bf16_bits(inp["conv_state"])
+    st = inp["state"].numpy().astype(np.float64)
+    threads = min(os.cpu_count() or 1, d.B * d.Hv)
+    steps, t_used = 0, 0.0
+    while t_used < budget_s and steps < w.steps:
+        s_in = wl.decode_step_inputs(w, steps)
+        sb = [{k: wl.bf16_bits(s_in[k]) for k in ("qkv", "a", "b")}]
+        t0 = time.perf_counter()
+        _, st, cs = oracle.decode(d, sb, cw, A_log, dt, cs, st, threads=threads)
+        t_used += time.perf_counter() - t0
+        steps += 1
+    return {"value": round(d.B * steps / t_used, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "seconds": round(t_used, 3),
+            "sample": "first %d of %d carried decode steps (all %d heads), f64 oracle" % (steps, w.steps,
+                                                                                         d.B * d.Hv)}
 
 
 # ---------------------------------------------------------------------------
@@ -557,6 +661,8 @@ def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int, peaks: dict 
         if record:
             ev[0].record(stream)
         gdn.gdn_conv_update(d, qkv, conv_w, conv_state, mask, q, k, v, stream)
+        if record:
+            ev[3].record(stream)
         gdn.gdn_gating(d, a, b, A_log, dt_bias, g, beta, stream)
         if record:
             ev[1].record(stream)
@@ -566,15 +672,16 @@ def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int, peaks: dict 
 
     once()
     torch.cuda.synchronize()
-    t_tot, t_rec = 0.0, 0.0
+    t_tot, t_rec, t_conv = 0.0, 0.0, 0.0
     for _ in range(iters):
         once(True)
         torch.cuda.synchronize()
         t_tot += ev[0].elapsed_time(ev[2])
         t_rec += ev[1].elapsed_time(ev[2])
+        t_conv += ev[0].elapsed_time(ev[3])
     if gdn.gdn_device_status() != gdn.GDN_OK:
         raise RuntimeError("device error word set during the prefill benchmark")
-    ms, ms_rec = t_tot / iters, t_rec / iters
+    ms, ms_rec, ms_conv = t_tot / iters, t_rec / iters, t_conv / iters
     flops = recurrence_flops_per_token(d) * n_valid
 
     # the layer's gated RMS norm on top of the recurrence: the gated entry
@@ -605,22 +712,86 @@ def bench_prefill(gdn, w: wl.Workload, dev, iters: int, chunk: int, peaks: dict 
     if gdn.gdn_device_status() != gdn.GDN_OK:
         raise RuntimeError("device error word set during the gated prefill benchmark")
     res = {"workload": w.name, "chunk": chunk, "ms": round(ms, 4), "recurrence_ms": round(ms_rec, 4),
-           "tokens": n_valid, "tokens_per_s": n_valid / (ms / 1e3),
+           "conv_ms": round(ms_conv, 4), "tokens": n_valid, "tokens_per_s": n_valid / (ms / 1e3),
            "recurrence_tflops": flops / (ms_rec / 1e3) / 1e12,
            "recurrence_gated_norm_ms": {"gdn_prefill_gated": round(t_g[True], 4),
                                         "prefill_then_norm": round(t_g[False], 4)}}
+    peaks = peaks or load_peaks()
     if chunk == 64:
         # tensor-core work of the chunked form over the chunks it computes,
         # against the tf32 rate (measured bf16 peak x the nominal tf32 ratio)
         n_ch = active_chunks(mask, d.T, d.B) * d.Hv
         tflops = chunk_mma_flops(d) * n_ch / (ms_rec / 1e3) / 1e12
-        res["tensor"] = {"tflops": round(tflops, 2), "chunk_head_units": n_ch,
-                         "flops_per_unit": chunk_mma_flops(d)}
-        if peaks is not None:
-            peak = peaks["bf16_tflops"] * TF32_PER_BF16
-            res["tensor"].update({"peak_tflops": round(peak, 1), "frac_of_tf32_peak": round(tflops / peak, 4),
-                                  "peak_source": peaks["source"] + " bf16 x nominal tf32/bf16"})
+        peak = peaks["bf16_tflops"] * TF32_PER_BF16
+        res["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": round(peak, 1),
+                           "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                           "algorithmic_flops": chunk_mma_flops(d) * n_ch, "units": n_ch,
+                           "unit_name": "chunk of 64 steps x head", "flops_per_unit": chunk_mma_flops(d),
+                           "kernel": "the chunked recurrence launch (tcgen05 kind::tf32 and kind::f16 products)",
+                           "peak_source": peaks["source"] + " bf16 x nominal tf32/bf16 (1.1/2.25)"}
+    else:
+        # the sequential form: 7 Dk Dv flops per head-step on the FP32 pipe
+        tfl = flops / (ms_rec / 1e3) / 1e12
+        peak = fp32_peak_tflops(peaks["sm_max_mhz"])
+        res["roofline"] = {"bound": "alu", "achieved": round(tfl, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                           "frac": round(tfl / peak, 4), "traffic": None, "algorithmic_flops": flops,
+                           "units": n_valid * d.Hv, "unit_name": "head-step",
+                           "flops_per_unit": 7 * d.Dk * d.Dv, "kernel": "prefill_seq_kernel",
+                           "peak_source": "152 SMs x 128 FP32 lanes x 2 flops x %.0f MHz" % peaks["sm_max_mhz"]}
+    cb = conv_bytes(d, n_valid)
+    res["conv_roofline"] = {"bound": "hbm", "achieved": round(cb / (ms_conv / 1e3) / 1e9, 1),
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(cb / (ms_conv / 1e3) / 1e9 / peaks["hbm_gbs"], 4), "traffic": None,
+                            "algorithmic_bytes": cb, "kernel": "conv_update_kernel + conv_state_kernel",
+                            "peak_source": peaks["source"]}
     return res
+
+
+def bench_prefill_vec(gdn, w: wl.Workload, dev, iters: int = 3, peaks: dict = None) -> dict:
+    """The recurrence with one decay factor per key channel (g [B, T, Hv, Dk])
+    over a prefill workload's shapes, sequential form, from device-drawn
+    inputs: q/k unit-norm-scaled like the conv output, g in (e^-0.5, 1)."""
+    d = w.dims
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(6000 + w.index)
+    q = torch.randn((d.B, d.T, d.Hk, d.Dk), generator=gen, device=dev)
+    k = torch.randn((d.B, d.T, d.Hk, d.Dk), generator=gen, device=dev)
+    q = (q / q.norm(dim=-1, keepdim=True) / d.Dk ** 0.5).to(torch.bfloat16)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    v = torch.randn((d.B, d.T, d.Hv, d.Dv), generator=gen, device=dev).to(torch.bfloat16)
+    gv = torch.exp(-torch.rand((d.B, d.T, d.Hv, d.Dk), generator=gen, device=dev) * 0.5)
+    beta = torch.sigmoid(torch.randn((d.B, d.T, d.Hv), generator=gen, device=dev))
+    s0 = (torch.randn((d.B, d.Hv, d.Dv, d.Dk), generator=gen, device=dev) * 0.05 if w.state == "normal"
+          else torch.zeros((d.B, d.Hv, d.Dv, d.Dk), device=dev))
+    mask, n_valid = None, d.B * d.T
+    if w.ragged:
+        lens = wl.workload_lengths(w)
+        mask = wl.right_padded_mask(lens, d.T).to(dev)
+        n_valid = int(lens.sum())
+    y = torch.empty((d.B, d.T, d.Hv, d.Dv), dtype=torch.bfloat16, device=dev)
+    s_out = torch.empty_like(s0)
+    stream = torch.cuda.current_stream()
+    gdn.gdn_prefill_vec(d, q, k, v, gv, beta, s0, s_out, mask, y, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        gdn.gdn_prefill_vec(d, q, k, v, gv, beta, s0, s_out, mask, y, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if gdn.gdn_device_status() != gdn.GDN_OK:
+        raise RuntimeError("device error word set during the vectorized-gating benchmark")
+    ms = e0.elapsed_time(e1) / iters
+    peaks = peaks or load_peaks()
+    flops = recurrence_flops_per_token(d) * n_valid
+    tfl = flops / (ms / 1e3) / 1e12
+    peak = fp32_peak_tflops(peaks["sm_max_mhz"])
+    return {"workload": w.name, "ms": round(ms, 4), "tokens": n_valid, "tokens_per_s": round(n_valid / (ms / 1e3), 1),
+            "roofline": {"bound": "alu", "achieved": round(tfl, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                         "frac": round(tfl / peak, 4), "traffic": None, "algorithmic_flops": flops,
+                         "units": n_valid * d.Hv, "unit_name": "head-step", "flops_per_unit": 7 * d.Dk * d.Dv,
+                         "kernel": "prefill_seq_kernel (per-channel decay)",
+                         "peak_source": "152 SMs x 128 FP32 lanes x 2 flops x %.0f MHz" % peaks["sm_max_mhz"]}}
 
 
 # ---------------------------------------------------------------------------
@@ -631,7 +802,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-prefill", action="store_true", help="only the headline decode (no other sections)")
-    ap.add_argument("--parts", default="decode_b1,rmsnorm,window,decode_gated,prefill,backward",
+    ap.add_argument("--parts", default="decode_b1,rmsnorm,window,decode_gated,prefill,prefill_vec,backward",
                     help="comma-separated sections to run after the headline decode")
     ap.add_argument("--backward-workloads", default="prefill_t8192,prefill_ragged",
                     help="workloads of the backward section (a subset keeps an ncu capture small)")
@@ -696,6 +867,8 @@ def main():
     parts = set() if args.no_prefill else set(args.parts.split(","))
     if "decode_b1" in parts:
         small_decode = bench_decode_small(gdn, wl.WORKLOADS["decode_b1"], dev)
+        if rank == 0 and not args.no_cpu:
+            small_decode["cpu_baseline"] = oracle_decode_b1_rate(wl.WORKLOADS["decode_b1"], args.cpu_budget_s / 4)
     if "rmsnorm" in parts:
         gated_norm = bench_rmsnorm_gated(gdn, wl.WORKLOADS["prefill_ragged"], dev)
     if "window" in parts:
@@ -705,15 +878,29 @@ def main():
     backward = None
     if "backward" in parts:
         backward = [bench_backward(gdn, wl.WORKLOADS[name], dev) for name in args.backward_workloads.split(",")]
+    prefill_vec = None
+    if "prefill_vec" in parts:
+        prefill_vec = bench_prefill_vec(gdn, wl.WORKLOADS["prefill_t8192"], dev, 3, peaks)
+        if rank == 0 and not args.no_cpu:
+            prefill_vec["cpu_baseline"] = oracle_prefill_rate(wl.WORKLOADS["prefill_t8192"], vec=True,
+                                                              budget_s=args.cpu_budget_s / 2)
     if "prefill" in parts:
         for name in ("prefill_t8192", "prefill_ragged"):
+            entries = []
             for chunk in (0, 64):
                 try:
-                    prefill.append(bench_prefill(gdn, wl.WORKLOADS[name], dev, 3, chunk, peaks))
+                    entries.append(bench_prefill(gdn, wl.WORKLOADS[name], dev, 3, chunk, peaks))
                 except gdn.GdnError as e:
                     if e.status != gdn.GDN_ERR_UNSUPPORTED:
                         raise
-                    prefill.append({"workload": name, "chunk": chunk, "unavailable": "chunked form not built"})
+                    entries.append({"workload": name, "chunk": chunk, "unavailable": "chunked form not built"})
+            if rank == 0 and not args.no_cpu:
+                # the oracle on a bounded sample of the same workload, once per
+                # workload: the same figure stands beside both forms
+                cb = oracle_prefill_rate(wl.WORKLOADS[name], budget_s=args.cpu_budget_s)
+                for e_ in entries:
+                    e_["cpu_baseline"] = cb
+            prefill.extend(entries)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -750,6 +937,7 @@ def main():
         "gpu_launches": args.steps,
         "clocks": clocks,
         "prefill": prefill,
+        "prefill_vec": prefill_vec,
         "decode_b1": small_decode,
         "rmsnorm_gated": gated_norm,
         "decode_window": window,

@@ -51,3 +51,34 @@ def test_profiled_traffic_only_for_the_profiled_source(monkeypatch, tmp_path):
     monkeypatch.setattr(bench, "source_hash", lambda *names: "0" * 16)
     assert bench.profiled_traffic("k.md", ["decode.cu"]) is None
     assert bench.profiled_traffic("missing.md", ["decode.cu"]) is None
+
+
+def test_fp32_peak_from_unit_counts_and_clock():
+    # 152 SMs x 128 FP32 lanes x one FMA (2 flops) per clock at 2070 MHz
+    assert abs(bench.fp32_peak_tflops(2070.0) - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
+    assert 80.0 < bench.fp32_peak_tflops(2070.0) < 81.0
+
+
+def test_conv_bytes_of_the_prefill_workload():
+    d = wl.WORKLOADS["prefill_t8192"].dims
+    C = 2 * 16 * 128 + 32 * 128                                     # 8192 channels
+    n = d.B * d.T
+    # qkv in and q/k/v out (bf16) per token, the taps, conv_state in and out
+    assert bench.conv_bytes(d, n) == n * C * 2 * 2 + C * 4 * 2 + 2 * 3 * C * 2
+    # padded tokens read nothing but still get their zero outputs written
+    assert bench.conv_bytes(d, 0) == n * C * 2 + C * 4 * 2 + 2 * 3 * C * 2
+
+
+def test_oracle_prefill_rate_reports_a_bounded_sample():
+    """The CPU baseline of a prefill entry: whole heads at the workload's T,
+    the tokens/s figure scaled from the heads it ran to all Hv heads."""
+    w = wl.Workload("small", 9, wl.Dims(B=2, T=96, Hk=2, Hv=4, Dk=32, Dv=32), ragged=True, len_lo=10,
+                    len_hi=96)
+    r = bench.oracle_prefill_rate(w, heads_per_row=2)
+    lens = wl.workload_lengths(w)
+    assert r["kind"] == "oracle" and r["unit"] == "tokens/s" and r["cores"] >= 1
+    steps = int(lens.sum()) * 2
+    assert "(%d valid head-steps)" % steps in r["sample"]
+    assert abs(r["value"] - steps / 4 / r["seconds"]) <= 0.06 * r["value"] + 1.0
+    rv = bench.oracle_prefill_rate(w, heads_per_row=1, vec=True)
+    assert rv["value"] > 0 and "per-channel" in rv["sample"]

@@ -369,6 +369,42 @@ def test_prefill_in_place_and_split_is_bitwise(gdn):
     assert torch.equal(st, full_s)
 
 
+@pytest.mark.parametrize("mk,use_ws", [(None, True), (None, False), ("random", True)])
+def test_prefill_chunked_prefix_consistency(gdn, mk, use_ws):
+    """prefill(T1) then prefill(T2) from the state it returns equals
+    prefill(T1 + T2) in the chunked form, within the state and y bounds,
+    with T1 not a multiple of the chunk length, so the second call's chunks
+    start in the middle of the first call's chunk grid (the pages' serving
+    loop replays a prefix and continues from its state)."""
+    d = wl.Dims(B=2, T=333, Hk=2, Hv=4, Dk=128, Dv=128)
+    T1 = 141
+    mask = make_mask(mk, d.B, d.T, 88)
+    r = recurrence_inputs(d, 88, mask)
+    full_y, full_s = gdn.prefill(d, *(to_dev(r[x]) for x in ("q", "k", "v", "g", "beta")), to_dev(r["state"]),
+                                 to_dev(mask), 64, use_workspace=use_ws)
+    st = to_dev(r["state"]).clone()
+    ys = []
+    for lo, hi in ((0, T1), (T1, d.T)):
+        dd = d.with_(T=hi - lo)
+        sl = lambda x: to_dev(r[x][:, lo:hi].contiguous())
+        m = None if mask is None else to_dev(mask[:, lo:hi].contiguous())
+        y, _ = gdn.prefill(dd, sl("q"), sl("k"), sl("v"), sl("g"), sl("beta"), st, m, 64, state_out=st,
+                           use_workspace=use_ws)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    split_y = torch.cat(ys, 1)
+    U.assert_y_close(U.bf16_dev_to_f64(split_y), U.bf16_dev_to_f64(full_y), "split y vs one call")
+    U.assert_state_close(st.cpu().numpy(), full_s.cpu().numpy().astype(np.float64), "split state vs one call")
+    yr, sr = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                               r["beta"].numpy().astype(np.float64), r["state"].numpy().astype(np.float64),
+                               np_mask(mask))
+    U.assert_y_close(U.bf16_dev_to_f64(split_y), yr, "split y vs oracle")
+    U.assert_state_close(st.cpu().numpy(), sr, "split state vs oracle")
+    if mask is not None:
+        assert np.all(U.bits(split_y)[mask.numpy() == 0] == 0), "padded y must be exactly zero"
+
+
 # ---------------------------------------------------------------------------
 # the composed core (configuration "tiny" and masked variants)
 # ---------------------------------------------------------------------------
@@ -390,13 +426,19 @@ def test_core_prefill_tiny(gdn, mk):
     assert np.array_equal(U.bits(cs), ref["conv_state"])
 
 
-def test_state_tolerance_after_4096_steps(gdn):
+@pytest.mark.parametrize("chunk,use_ws", [(0, True), (64, True), (64, False)])
+def test_state_tolerance_after_4096_steps(gdn, chunk, use_ws):
+    """The f32 state bound after T = 4096 from a nonzero initial state, in
+    the sequential form and in both chunked forms (two passes when the
+    workspace is given to these few heads, the single pass without it)."""
     d = wl.Dims(B=1, T=4096, Hk=1, Hv=2, Dk=128, Dv=128)
     inp = inputs_for(d, 4096)
+    assert float(inp["state"].abs().max()) > 0
     y, s = gdn.core_prefill(d, to_dev(inp["qkv"]), to_dev(inp["conv_w"]), to_dev(inp["a"]), to_dev(inp["b"]),
                             to_dev(inp["A_log"]), to_dev(inp["dt_bias"]), to_dev(inp["conv_state"]).clone(),
-                            to_dev(inp["state"]))
+                            to_dev(inp["state"]), None, chunk, None, use_ws)
     torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
     ref = oracle.layer_core(d, U.bits(inp["qkv"]), U.bits(inp["conv_w"]), U.bits(inp["a"]), U.bits(inp["b"]),
                             inp["A_log"].numpy(), inp["dt_bias"].numpy(), U.bits(inp["conv_state"]),
                             inp["state"].numpy().astype(np.float64))
