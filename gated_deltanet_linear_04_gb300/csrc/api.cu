@@ -9,6 +9,8 @@
 
 namespace gdn {
 
+constexpr int kMaxDevicesHost = 64;
+
 // One word per device, set by kernels whose bounded waits give up.
 __device__ unsigned g_error_word;
 
@@ -107,6 +109,25 @@ bool encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtyp
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, int rank,
+                 const uint64_t *dims, const uint32_t *box, CUtensorMapSwizzle swizzle) {
+    const auto fn = tmap_encoder();
+    if (fn == nullptr || rank < 1 || rank > 5) return false;
+    cuuint64_t gdims[5], strides[4];
+    cuuint32_t gbox[5], estr[5];
+    cuuint64_t pitch = (cuuint64_t)elem_bytes;
+    for (int i = 0; i < rank; ++i) {
+        gdims[i] = dims[i];
+        gbox[i] = box[i];
+        estr[i] = 1;
+        if (i > 0) strides[i - 1] = pitch;
+        pitch *= dims[i];
+    }
+    return fn(map, dtype, (cuuint32_t)rank, const_cast<void *>(base), gdims, strides, gbox, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t rows,
                     uint64_t cols, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle) {
     const auto fn = tmap_encoder();
@@ -129,7 +150,6 @@ static gdn_status prefill_impl(const gdn_dims *dims, const uint16_t *q, const ui
     gdn_status st = check_dims(dims, &s);
     if (st != GDN_OK) return st;
     if (chunk != 0 && chunk != 64) return GDN_ERR_UNSUPPORTED;
-    if (chunk == 64 && (s.Dk != 128 || s.Dv != 128)) return GDN_ERR_UNSUPPORTED;
     const size_t BT = (size_t)s.B * s.T;
     const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
     if (!ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT) || !ok_ptr(g, BT) || !ok_ptr(beta, BT) ||
@@ -214,7 +234,8 @@ gdn_status gdn_conv_update(const gdn_dims *dims, const uint16_t *qkv, const uint
         !ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT))
         return GDN_ERR_INVALID_ARG;
     if (BT == 0) return GDN_OK;
-    return gdn::from_cuda(gdn::launch_conv_update(s, qkv, conv_w, conv_state, mask, q, k, v, (cudaStream_t)stream));
+    return gdn::from_cuda(gdn::launch_conv_update(s, qkv, conv_w, conv_state, mask, q, k, v, gdn::error_word(),
+                                                  (cudaStream_t)stream));
 }
 
 gdn_status gdn_gating(const gdn_dims *dims, const uint16_t *a, const uint16_t *b, const float *A_log,
@@ -261,6 +282,49 @@ struct HostSlot {
     size_t qkv, a, b, y, bytes;
 };
 
+// The copy streams and events of gdn_recurrent_decode_host_steps, created on
+// a device's first call and kept for the life of the process (creating them
+// on every call cost about as much host time as a few decode steps).  A
+// call holds the device's mutex while it enqueues, so calls from several
+// host threads do not interleave their records and waits on the shared
+// events.
+struct HostLoop {
+    cudaStream_t cin = nullptr, cout = nullptr;
+    cudaEvent_t start = nullptr, in[kHostSlots] = {}, done[kHostSlots] = {}, out[kHostSlots] = {};
+    std::mutex mu;
+    bool ready = false;
+};
+HostLoop g_host_loop[gdn::kMaxDevicesHost];
+
+cudaError_t host_loop_setup(HostLoop &h) {
+    if (h.ready) return cudaSuccess;
+    cudaError_t e = cudaStreamCreateWithFlags(&h.cin, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.cout, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
+    for (int k = 0; k < kHostSlots && e == cudaSuccess; ++k) {
+        e = cudaEventCreateWithFlags(&h.in[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.done[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.out[k], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        // release what was made; the next call tries again
+        for (int k = 0; k < kHostSlots; ++k) {
+            if (h.in[k]) cudaEventDestroy(h.in[k]);
+            if (h.done[k]) cudaEventDestroy(h.done[k]);
+            if (h.out[k]) cudaEventDestroy(h.out[k]);
+            h.in[k] = h.done[k] = h.out[k] = nullptr;
+        }
+        if (h.start) cudaEventDestroy(h.start);
+        if (h.cin) cudaStreamDestroy(h.cin);
+        if (h.cout) cudaStreamDestroy(h.cout);
+        h.start = nullptr;
+        h.cin = h.cout = nullptr;
+        return e;
+    }
+    h.ready = true;
+    return cudaSuccess;
+}
+
 HostSlot host_slot(const gdn::Sizes &s) {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     HostSlot h;
@@ -300,16 +364,14 @@ gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, co
     if (staging_bytes < kHostSlots * h.bytes) return GDN_ERR_INVALID_ARG;
     const size_t nq = B * s.C(), na = B * s.Hv, ny = B * s.Hv * s.Dv;   // elements per step
 
-    cudaStream_t main = (cudaStream_t)stream, cin = nullptr, cout = nullptr;
-    cudaEvent_t ev_start = nullptr, ev_in[kHostSlots] = {}, ev_done[kHostSlots] = {}, ev_out[kHostSlots] = {};
-    cudaError_t e = cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
-    for (int k = 0; k < kHostSlots && e == cudaSuccess; ++k) {
-        e = cudaEventCreateWithFlags(&ev_in[k], cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_done[k], cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_out[k], cudaEventDisableTiming);
-    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= gdn::kMaxDevicesHost) return GDN_ERR_CUDA;
+    HostLoop &hl = g_host_loop[dev];
+    std::lock_guard<std::mutex> lk(hl.mu);
+    cudaError_t e = host_loop_setup(hl);
+    if (e != cudaSuccess) return gdn::from_cuda(e);
+    cudaStream_t main = (cudaStream_t)stream, cin = hl.cin, cout = hl.cout;
+    cudaEvent_t ev_start = hl.start, *ev_in = hl.in, *ev_done = hl.done, *ev_out = hl.out;
     // the copy streams start after everything already on `stream`; every slot
     // starts free (its "done" and "out" events complete at that point)
     if (e == cudaSuccess) e = cudaEventRecord(ev_start, main);
@@ -347,15 +409,6 @@ gdn_status gdn_recurrent_decode_host_steps(const gdn_dims *dims, int n_steps, co
     }
     // `stream` completes after the last y has arrived
     for (int k = 0; k < kHostSlots && e == cudaSuccess; ++k) e = cudaStreamWaitEvent(main, ev_out[k], 0);
-    // streams and events are released once their pending work completes
-    for (int k = 0; k < kHostSlots; ++k) {
-        if (ev_in[k]) cudaEventDestroy(ev_in[k]);
-        if (ev_done[k]) cudaEventDestroy(ev_done[k]);
-        if (ev_out[k]) cudaEventDestroy(ev_out[k]);
-    }
-    if (ev_start) cudaEventDestroy(ev_start);
-    if (cin) cudaStreamDestroy(cin);
-    if (cout) cudaStreamDestroy(cout);
     return gdn::from_cuda(e);
 }
 
@@ -403,7 +456,7 @@ size_t gdn_prefill_workspace_size(const gdn_dims *dims, int chunk) {
     if (gdn::check_dims(dims, &s) != GDN_OK) return 0;
     if (chunk != 0 && chunk != 64) return 0;
     size_t n = gdn::row_order_workspace(s);
-    if (chunk == 64 && s.Dk == 128 && s.Dv == 128 && s.B > 0 && s.T > 0 && gdn::prefill_two_pass_pays(s))
+    if (chunk == 64 && s.B > 0 && s.T > 0 && gdn::prefill_two_pass_pays(s))
         n += gdn::prefill_two_pass_workspace(s);
     return n;
 }

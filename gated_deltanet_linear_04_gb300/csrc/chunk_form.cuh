@@ -39,6 +39,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "internal.h"
 #include "umma.cuh"
 
 namespace gdn {
@@ -51,6 +52,91 @@ constexpr uint32_t kSlot = 16384;
 
 // TMEM columns
 constexpr uint32_t C_QK = 0, C_D = 64, C_W = 128, C_Y = 192, C_S = 256;
+
+// Tensor maps of the chunked kernels (host side).  k and q as [B*T][Hk][Dk]
+// with a [64 steps][1 head][64 channels] box, 128-byte swizzled (a chunk's
+// tile is two such boxes, channels 0-63 and 64-127); v and z as [B*T][Hv][Dv]
+// with a [64][1][128] box; y as [B][T][Hv][Dv] with a [1][64][1][128] box.
+// The kernels always work on 128-wide tiles: with Dk or Dv below 128 the
+// boxes run past the head's channels, the loads read zeros there and the y
+// store writes only the first Dv channels, so the padded rows and columns of
+// every product are exact zeros and the results are those of the true sizes.
+struct ChunkMaps {
+    CUtensorMap k, q, v, z, y;
+};
+
+inline bool encode_chunk_maps(ChunkMaps *m, const Sizes &s, const uint16_t *q, const uint16_t *k,
+                              const uint16_t *v, const uint16_t *z, uint16_t *y) {
+    const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
+    const uint64_t dk[3] = {(uint64_t)s.Dk, (uint64_t)s.Hk, rows};
+    const uint64_t dv[3] = {(uint64_t)s.Dv, (uint64_t)s.Hv, rows};
+    const uint64_t dy[4] = {(uint64_t)s.Dv, (uint64_t)s.Hv, (uint64_t)s.T, (uint64_t)s.B};
+    const uint32_t bk[3] = {64, 1, (uint32_t)kC}, bv[3] = {(uint32_t)kD, 1, (uint32_t)kC};
+    const uint32_t by[4] = {(uint32_t)kD, 1, (uint32_t)kC, 1};
+    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_tmap(&m->k, k, bf, 2, 3, dk, bk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&m->q, q, bf, 2, 3, dk, bk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&m->v, v, bf, 2, 3, dv, bv, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap(&m->y, y, bf, 2, 4, dy, by, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    m->z = m->v;   // unused without the gated norm
+    return z == nullptr || encode_tmap(&m->z, z, bf, 2, 3, dv, bv, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Chunk c's k, q (128B-swizzled K-halves) and v tiles of head (hk, hv) of the
+// rows starting at flat row `rowg` = b * T + c * 64 into the KQ and V slots.
+__device__ __forceinline__ void load_chunk_tiles(uint8_t *sm, uint32_t kq_off, uint32_t v_off, const CUtensorMap *tm_k,
+                                                 const CUtensorMap *tm_q, const CUtensorMap *tm_v, int hk, int hv,
+                                                 int rowg, uint64_t *bar) {
+    mbar_expect_tx(bar, 4 * 8192 + 16384);
+    tma_load_3d(sm + kq_off, tm_k, 0, hk, rowg, bar);
+    tma_load_3d(sm + kq_off + kSlot, tm_k, 64, hk, rowg, bar);
+    tma_load_3d(sm + kq_off + 8192, tm_q, 0, hk, rowg, bar);
+    tma_load_3d(sm + kq_off + kSlot + 8192, tm_q, 64, hk, rowg, bar);
+    tma_load_3d(sm + v_off, tm_v, 0, hv, rowg, bar);
+}
+
+// The f32 state of head (b, hv) between global memory and the S columns of
+// TMEM: thread `row` (= dv) moves columns [64 half, +64) of its row; rows at
+// or past Dv and columns at or past Dk are zeros in TMEM and are not stored.
+__device__ __forceinline__ void state_to_tmem(const float *state_in, uint32_t s_tmem, int b, int hv, int Hv, int Dk,
+                                              int Dv, int row, int half) {
+    const bool row_ok = row < Dv && state_in != nullptr;
+    const size_t off = (((size_t)b * Hv + hv) * Dv + row) * Dk;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        float r[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const int col = half * 64 + cc * 32 + j;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row_ok && col < Dk) x = *reinterpret_cast<const float4 *>(state_in + off + col);
+            r[j] = x.x; r[j + 1] = x.y; r[j + 2] = x.z; r[j + 3] = x.w;
+        }
+        umma::tmem_st32(s_tmem + half * 64 + cc * 32, r);
+    }
+    umma::tmem_st_wait();
+}
+
+__device__ __forceinline__ void state_from_tmem(float *state_out, uint32_t s_tmem, int b, int hv, int Hv, int Dk,
+                                                int Dv, int row, int half) {
+    const size_t off = (((size_t)b * Hv + hv) * Dv + row) * Dk;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        float sv[32];
+        umma::tmem_ld32(s_tmem + half * 64 + cc * 32, sv);
+        umma::tmem_ld_wait();
+        if (row < Dv) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const int col = half * 64 + cc * 32 + j;
+                if (col < Dk)
+                    *reinterpret_cast<float4 *>(state_out + off + col) =
+                        make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+            }
+        }
+    }
+}
 
 // A / T working matrix, row-major; groups of 4 columns are XOR-permuted by the
 // row (r % 8) so that row-per-thread float4 stores spread over all banks while

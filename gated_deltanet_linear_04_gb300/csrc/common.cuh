@@ -158,6 +158,24 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
+// 3-D tiled TMA load: box at (x = inner coordinate, y, z) of `tmap` (x times
+// the element size a multiple of 16 bytes; out-of-range rows read as zeros).
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 4-D tiled TMA store of the box at (x, y, z, w) of `tmap` from shared memory,
+// tracked by the issuing thread's bulk group (clipped at the tensor's bounds).
+__device__ __forceinline__ void tma_store_4d(const void *tmap, int x, int y, int z, int w, const void *smem_src) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(smem_src))
+                 : "memory");
+}
+
 // 3-D tiled TMA store of the box at (x = inner coordinate, y, z) of `tmap`
 // from shared memory, tracked by the issuing thread's bulk group (the box is
 // clipped at the tensor's bounds; x * element size must be a multiple of 16).

@@ -9,18 +9,20 @@
 //
 // Work split (memory-bound, ~2 bytes in + 2 bytes out per channel-token): one
 // warp owns one head segment (Dk q- or k-channels, or Dv v-channels) for a
-// tile of 32 consecutive tokens (three 8-warp CTAs resident per SM).  Each
-// lane holds D/32 channels.  The taps and the K-1 window rows before the tile
-// are loaded once; the tile is walked in sub-tiles of 4 tokens with the next
-// sub-tile's rows in flight, keeping the last K-1 *valid* rows in registers
-// (as packed bf16), so every qkv element is read once.  The sub-tile loop is
-// not unrolled: the unrolled form missed the instruction cache (measured
-// 1.2x slower).  The rms-norm is a warp shuffle sum.
+// tile of 32 consecutive tokens (three 8-warp CTAs resident per SM).  The
+// tile's rows arrive in shared memory by one TMA copy (a [32 x D] box of a
+// 3-D tensor map over qkv, clipped at the row's T), issued first, so every
+// resident warp has its whole tile in flight while it loads the taps and the
+// K-1 window rows before the tile.  Each lane then holds D/32 channels; the
+// window of the last K-1 *valid* rows travels in registers.  The arithmetic
+// runs on channel pairs with the packed two-wide f32 instructions of sm_100,
+// and the q/k rms-norm sums four tokens per warp reduction (six shuffles).
 //
 // Masked steps ("skip" reading): they do not enter the conv window; their q/k/v
-// are written as zeros.  The K-1 valid rows preceding a tile are found by a
-// warp-ballot scan backwards over the mask (128 steps per iteration through
-// wholly masked stretches); missing rows come from conv_state.
+// are written as zeros.  A tile without a valid step copies nothing.  The K-1
+// valid rows preceding a tile are found by a warp-ballot scan backwards over
+// the mask (128 steps per iteration through wholly masked stretches); missing
+// rows come from conv_state.
 // The new conv_state is written by a second, tiny kernel that runs after the
 // first on the stream, because tiles anywhere in the row may still read the
 // old conv_state.
@@ -43,6 +45,7 @@ struct ConvParams {
     const uint16_t *conv_state;   // may be null (zeros)
     const uint8_t *mask;          // may be null
     uint16_t *q, *k, *v;
+    unsigned *err;
     int B, T, Hk, Hv, C, K;
     float eps;
 };
@@ -158,17 +161,86 @@ __device__ __forceinline__ void unpack(const typename RawRow<CPL>::type &r, floa
     }
 }
 
+// Channel pairs of one lane: CPL channels as NP float2 (CPL = 1 uses the
+// low half only).  The arithmetic on them is the packed two-wide f32 form of
+// sm_100 (fma.rn.f32x2 and friends), each half rounded exactly like the
+// scalar instruction, so a pair costs one instruction where two scalars did.
+template <int CPL> struct Pairs { static constexpr int NP = CPL >= 2 ? CPL / 2 : 1; float2 v[NP]; };
+
+template <int CPL>
+__device__ __forceinline__ Pairs<CPL> unpack_pairs(const typename RawRow<CPL>::type &r) {
+    Pairs<CPL> o;
+    if constexpr (CPL == 4) {
+        o.v[0] = make_float2(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u));
+        o.v[1] = make_float2(__uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+    } else if constexpr (CPL == 2) {
+        o.v[0] = make_float2(__uint_as_float(r << 16), __uint_as_float(r & 0xffff0000u));
+    } else {
+        o.v[0] = make_float2(bf16_to_f32(r), 0.0f);
+    }
+    return o;
+}
+
+// Two bf16 (RNE) in one 32-bit word, low half first.
+__device__ __forceinline__ uint32_t pack_bf16x2(float2 x) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int CPL>
+__device__ __forceinline__ void store_pairs(uint16_t *p, const Pairs<CPL> &x) {
+    if constexpr (CPL == 4) *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16x2(x.v[0]), pack_bf16x2(x.v[1]));
+    else if constexpr (CPL == 2) *reinterpret_cast<uint32_t *>(p) = pack_bf16x2(x.v[0]);
+    else *p = f32_to_bf16(x.v[0].x);
+}
+
+// silu(u) = u * sigmoid(u) on a pair, with the hardware base-2 exponential
+// and reciprocal (the same operations as the scalar silu of common.cuh)
+__device__ __forceinline__ float2 silu2(float2 u) {
+    const float2 t = __fmul2_rn(u, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+    float e0, e1;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t.x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t.y));
+    const float2 d = __fadd2_rn(make_float2(e0, e1), make_float2(1.0f, 1.0f));
+    return __fmul2_rn(u, make_float2(rcp_fast(d.x), rcp_fast(d.y)));
+}
+
+// Warp sums of four per-lane values s[0..3] (one per token of a sub-tile) in
+// six shuffles: two halving exchanges hand each lane half, then a quarter,
+// of the tokens, and three more rounds finish the sum.  The result is the
+// total of token ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1).
+__device__ __forceinline__ float warp_sum4(const float (&s)[4], int lane) {
+    const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+    float a0 = h16 ? s[2] : s[0], a1 = h16 ? s[3] : s[1];
+    const float b0 = h16 ? s[0] : s[2], b1 = h16 ? s[1] : s[3];
+    a0 += __shfl_xor_sync(0xffffffffu, b0, 16);
+    a1 += __shfl_xor_sync(0xffffffffu, b1, 16);
+    float k = h8 ? a1 : a0;
+    const float o = h8 ? a0 : a1;
+    k += __shfl_xor_sync(0xffffffffu, o, 8);
+    k += __shfl_xor_sync(0xffffffffu, k, 4);
+    k += __shfl_xor_sync(0xffffffffu, k, 2);
+    k += __shfl_xor_sync(0xffffffffu, k, 1);
+    return k;
+}
+
 // One head segment of D channels (c0 = first channel) over one tile of kTile
 // tokens, walked in sub-tiles of kSub: the taps and the K-1 window rows
 // before the tile are loaded once; the next sub-tile's rows are in flight
 // while the current one is computed; the window of the last K-1 valid rows
-// travels in registers.
+// travels in registers (as f32 pairs).  A sub-tile is computed in two
+// phases: conv + SiLU of its (up to) four tokens with their sums of squares,
+// then one four-token warp reduction for the q/k norm, then the scaled
+// stores.
 // kind: 0 = q (rms-norm, scale 1/D), 1 = k (rms-norm, scale 1/sqrt(D)), 2 = v.
 template <int D>
-__device__ __forceinline__ void conv_segment(const ConvParams &p, int kind, int c0, uint16_t *out_base,
+__device__ __forceinline__ void conv_segment(const ConvParams &p, const CUtensorMap *tm, uint8_t *tile,
+                                             uint64_t *bar, int kind, int c0, uint16_t *out_base,
                                              int out_head_stride, int b, int t0, int lane) {
     constexpr int CPL = D / 32;
+    constexpr int NP = Pairs<CPL>::NP;
     constexpr int NS = kTile / kSub;
+    static_assert(kSub == 4, "the norm reduction sums four tokens at once");
     using Raw = typename RawRow<CPL>::type;
     const int c = c0 + lane * CPL;
     const int nt = min(kTile, p.T - t0);
@@ -188,122 +260,142 @@ __device__ __forceinline__ void conv_segment(const ConvParams &p, int kind, int 
         return;
     }
 
-    // rows of sub-tile s in flight into buffer `slot` (masked or absent rows read nothing)
-    Raw buf[2][kSub];
-    auto issue = [&](int s, int slot) {
-#pragma unroll
-        for (int r = 0; r < kSub; ++r) {
-            const int tl = s * kSub + r;
-            buf[slot][r] = Raw{};
-            if (tl < nt && ((valid >> tl) & 1u))
-                buf[slot][r] = load_raw<CPL>(p.qkv + ((size_t)b * p.T + t0 + tl) * p.C + c);
-        }
-    };
-    issue(0, 0);
+    // the tile's rows [32][D] by one TMA copy (rows past T read as zeros)
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_expect_tx(bar, kTile * D * 2);
+        tma_load_3d(tile, tm, c0, t0, b, bar);
+    }
+    __syncwarp();   // the barrier's initialisation is seen by every lane before it waits
 
-    // taps, right-aligned to 4 (tap K-1 of the page's weight -> slot 3), kept
-    // as bf16 bit patterns (exact; unpacked at use)
-    uint16_t w[CPL][4];
+    // taps, right-aligned to 4 (tap K-1 of the page's weight -> slot 3), as
+    // f32 pairs (bf16 values, exact)
+    float2 tap[4][NP];
 #pragma unroll
-    for (int i = 0; i < CPL; ++i)
+    for (int j = 0; j < 4; ++j) {
+        const int jj = j - (4 - p.K);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int jj = j - (4 - p.K);
-            w[i][j] = jj >= 0 ? p.conv_w[(size_t)(c + i) * p.K + jj] : (uint16_t)0;
+        for (int i = 0; i < NP; ++i) {
+            float lo = 0.0f, hi = 0.0f;
+            if (jj >= 0) {
+                lo = bf16_to_f32(p.conv_w[(size_t)(c + 2 * i) * p.K + jj]);
+                if (CPL >= 2) hi = bf16_to_f32(p.conv_w[(size_t)(c + 2 * i + 1) * p.K + jj]);
+            }
+            tap[j][i] = make_float2(lo, hi);
         }
+    }
 
-    // window of the K-1 valid rows before the tile (zeros for unused slots),
-    // kept as the raw bf16 rows
+    // window of the K-1 valid rows before the tile (zeros for unused slots)
     int codes[kMaxHalo];
     find_halo(p.mask, b, p.T, t0, lane, codes);
-    Raw win[kMaxHalo];
+    Pairs<CPL> win[kMaxHalo];
 #pragma unroll
     for (int j = 0; j < kMaxHalo; ++j) {
         const int code = codes[j];
         const bool used = j >= kMaxHalo - (p.K - 1);
-        win[j] = Raw{};
+        Raw r = Raw{};
         if (used) {
             if (code >= 0) {
-                win[j] = load_raw<CPL>(p.qkv + ((size_t)b * p.T + code) * p.C + c);
+                r = load_raw<CPL>(p.qkv + ((size_t)b * p.T + code) * p.C + c);
             } else if (p.conv_state != nullptr && p.K - 1 + code >= 0) {
-                win[j] = load_raw<CPL>(p.conv_state + ((size_t)b * (p.K - 1) + (p.K - 1 + code)) * p.C + c);
+                r = load_raw<CPL>(p.conv_state + ((size_t)b * (p.K - 1) + (p.K - 1 + code)) * p.C + c);
             }
         }
+        win[j] = unpack_pairs<CPL>(r);
     }
+
+    // every lane waits for the copy (bounded; on expiry the error word is set
+    // and the tile is left unwritten)
+    if (!mbar_wait(bar, 0, p.err)) return;
+    const uint16_t *rows = reinterpret_cast<const uint16_t *>(tile) + lane * CPL;
 
     const float inv_d = 1.0f / (float)D;
     const float scale = kind == 0 ? inv_d : (kind == 1 ? 1.0f / sqrtf((float)D) : 1.0f);
-    // one sub-tile from buffer SLOT (a compile-time index, so the rows stay
-    // in registers); the sub-tile loop itself is not unrolled, which keeps the
-    // code within the instruction cache
-    auto sub_tile = [&](auto slot_c, int s) {
-        constexpr int SLOT = decltype(slot_c)::value;
+    // sub-tiles of four tokens: conv + SiLU of each valid token with its sum
+    // of squares, one four-token warp reduction for the q/k norm, the stores;
+    // the sub-tile loop is not unrolled, which keeps the code within the
+    // instruction cache
+#pragma unroll 1
+    for (int s = 0; s < NS && s * kSub < nt; ++s) {
+        Pairs<CPL> x[kSub];
+        float ss[kSub];
 #pragma unroll
         for (int r = 0; r < kSub; ++r) {
             const int tl = s * kSub + r;
-            if (tl >= nt) break;
-            uint16_t *op = out_ptr(t0 + tl);
-            if (!((valid >> tl) & 1u)) {
-                store_zero<CPL>(op);
-                continue;
-            }
-            float xr[CPL], w0[CPL], w1[CPL], w2[CPL];
-            unpack<CPL>(buf[SLOT][r], xr);
-            unpack<CPL>(win[0], w0);
-            unpack<CPL>(win[1], w1);
-            unpack<CPL>(win[2], w2);
-            float x[CPL];
-            float ss = 0.0f;
+            ss[r] = 0.0f;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) {
-                float u = bf16_to_f32(w[i][0]) * w0[i];
-                u = fmaf(bf16_to_f32(w[i][1]), w1[i], u);
-                u = fmaf(bf16_to_f32(w[i][2]), w2[i], u);
-                u = fmaf(bf16_to_f32(w[i][3]), xr[i], u);
-                x[i] = silu(u);
-                ss = fmaf(x[i], x[i], ss);
-            }
-            if (kind != 2) {
-                ss = warp_sum(ss);
-                const float rs = (1.0f / sqrtf(ss * inv_d + p.eps)) * scale;
+            for (int i = 0; i < NP; ++i) x[r].v[i] = make_float2(0.0f, 0.0f);
+            if (tl < nt && ((valid >> tl) & 1u)) {
+                const Pairs<CPL> xr = unpack_pairs<CPL>(load_raw<CPL>(rows + tl * D));
+                float2 sq = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int i = 0; i < CPL; ++i) x[i] *= rs;
+                for (int i = 0; i < NP; ++i) {
+                    float2 u = __fmul2_rn(tap[0][i], win[0].v[i]);
+                    u = __ffma2_rn(tap[1][i], win[1].v[i], u);
+                    u = __ffma2_rn(tap[2][i], win[2].v[i], u);
+                    u = __ffma2_rn(tap[3][i], xr.v[i], u);
+                    x[r].v[i] = silu2(u);
+                    sq = __ffma2_rn(x[r].v[i], x[r].v[i], sq);
+                }
+                ss[r] = CPL >= 2 ? sq.x + sq.y : sq.x;
+                win[0] = win[1];
+                win[1] = win[2];
+                win[2] = xr;
             }
-            store_bf16<CPL>(op, x);
-            win[0] = win[1];
-            win[1] = win[2];
-            win[2] = buf[SLOT][r];
         }
-    };
-#pragma unroll 1
-    for (int s = 0; s < NS && s * kSub < nt; s += 2) {
-        if (s + 1 < NS) issue(s + 1, 1);
-        sub_tile(std::integral_constant<int, 0>{}, s);
-        if (s + 1 >= NS || (s + 1) * kSub >= nt) break;
-        if (s + 2 < NS) issue(s + 2, 0);
-        sub_tile(std::integral_constant<int, 1>{}, s + 1);
+        if (kind != 2) {
+            // each lane normalises one token; the four factors are then
+            // broadcast from lanes 0, 8, 16 and 24
+            const float tot = warp_sum4(ss, lane);
+            const float rs_mine = (1.0f / sqrtf(tot * inv_d + p.eps)) * scale;
+#pragma unroll
+            for (int r = 0; r < kSub; ++r) {
+                const float rs = __shfl_sync(0xffffffffu, rs_mine, ((r >> 1) << 4) | ((r & 1) << 3));
+#pragma unroll
+                for (int i = 0; i < NP; ++i) x[r].v[i] = __fmul2_rn(x[r].v[i], make_float2(rs, rs));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kSub; ++r) {
+            const int tl = s * kSub + r;
+            if (tl < nt) store_pairs<CPL>(out_ptr(t0 + tl), x[r]);   // masked steps: zeros
+        }
     }
 }
 
+// Shared memory of a CTA: one [kTile x max(DK, DV)] bf16 tile per warp, from
+// a 128-byte aligned base (the TMA destination alignment).
 template <int DK, int DV>
-__global__ void __launch_bounds__(kWarps * 32, 3) conv_update_kernel(const ConvParams p) {
+constexpr uint32_t conv_smem_bytes() {
+    return (uint32_t)kWarps * kTile * (DK > DV ? DK : DV) * 2 + 128;
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kWarps * 32, 3) conv_update_kernel(const __grid_constant__ CUtensorMap tm_qk,
+                                                                     const __grid_constant__ CUtensorMap tm_v,
+                                                                     const ConvParams p) {
+    extern __shared__ __align__(128) uint8_t conv_smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kWarps];
+    uint8_t *conv_smem = conv_smem_raw + (((smem_u32(conv_smem_raw) + 127u) & ~127u) - smem_u32(conv_smem_raw));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seg = blockIdx.y * kWarps + warp;
     const int nseg = 2 * p.Hk + p.Hv;
     if (seg >= nseg) return;
     const int t0 = blockIdx.x * kTile;
     const int b = blockIdx.z;
+    uint8_t *tile = conv_smem + (size_t)warp * kTile * (DK > DV ? DK : DV) * 2;
     if (seg < p.Hk) {
         uint16_t *ob = p.q + ((size_t)b * p.T * p.Hk + seg) * DK;
-        conv_segment<DK>(p, 0, seg * DK, ob, p.Hk * DK, b, t0, lane);
+        conv_segment<DK>(p, &tm_qk, tile, &bars[warp], 0, seg * DK, ob, p.Hk * DK, b, t0, lane);
     } else if (seg < 2 * p.Hk) {
         const int hk = seg - p.Hk;
         uint16_t *ob = p.k + ((size_t)b * p.T * p.Hk + hk) * DK;
-        conv_segment<DK>(p, 1, seg * DK, ob, p.Hk * DK, b, t0, lane);
+        conv_segment<DK>(p, &tm_qk, tile, &bars[warp], 1, seg * DK, ob, p.Hk * DK, b, t0, lane);
     } else {
         const int hv = seg - 2 * p.Hk;
         uint16_t *ob = p.v + ((size_t)b * p.T * p.Hv + hv) * DV;
-        conv_segment<DV>(p, 2, 2 * p.Hk * DK + hv * DV, ob, p.Hv * DV, b, t0, lane);
+        conv_segment<DV>(p, &tm_v, tile, &bars[warp], 2, 2 * p.Hk * DK + hv * DV, ob, p.Hv * DV, b, t0, lane);
     }
 }
 
@@ -346,17 +438,29 @@ __global__ void __launch_bounds__(256) gating_kernel(const uint16_t *__restrict_
 
 template <int DK, int DV>
 cudaError_t launch_conv_t(const ConvParams &p, cudaStream_t st) {
+    // 3-D maps over qkv [B][T][C] with a [32 tokens x D channels] box (the
+    // box is clipped at each row's T, so a tile never reads the next row)
+    CUtensorMap tqk, tv;
+    if (!encode_tmap_3d(&tqk, p.qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.B, (uint64_t)p.T,
+                        (uint64_t)p.C, kTile, DK) ||
+        !encode_tmap_3d(&tv, p.qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)p.B, (uint64_t)p.T,
+                        (uint64_t)p.C, kTile, DV))
+        return cudaErrorInvalidValue;
+    static unsigned long long attr_done = 0;   // per instantiation, one bit per device
+    cudaError_t e = set_max_smem(attr_done, conv_update_kernel<DK, DV>, conv_smem_bytes<DK, DV>());
+    if (e != cudaSuccess) return e;
     const int nseg = 2 * p.Hk + p.Hv;
     dim3 grid((p.T + kTile - 1) / kTile, (nseg + kWarps - 1) / kWarps, p.B);
-    conv_update_kernel<DK, DV><<<grid, kWarps * 32, 0, st>>>(p);
+    conv_update_kernel<DK, DV><<<grid, kWarps * 32, conv_smem_bytes<DK, DV>(), st>>>(tqk, tv, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_conv_update(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
-                               const uint8_t *mask, uint16_t *q, uint16_t *k, uint16_t *v, cudaStream_t st) {
-    ConvParams p{qkv, conv_w, conv_state, mask, q, k, v, s.B, s.T, s.Hk, s.Hv, s.C(), s.K, s.eps};
+                               const uint8_t *mask, uint16_t *q, uint16_t *k, uint16_t *v, unsigned *err,
+                               cudaStream_t st) {
+    ConvParams p{qkv, conv_w, conv_state, mask, q, k, v, err, s.B, s.T, s.Hk, s.Hv, s.C(), s.K, s.eps};
     cudaError_t e = cudaErrorInvalidValue;
 #define GDN_CONV_CASE(DK_, DV_) \
     if (s.Dk == DK_ && s.Dv == DV_) e = launch_conv_t<DK_, DV_>(p, st);

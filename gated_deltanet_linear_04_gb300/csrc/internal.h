@@ -45,7 +45,8 @@ cudaError_t set_max_smem(unsigned long long &done, K kernel, size_t bytes) {
 }
 
 cudaError_t launch_conv_update(const Sizes &s, const uint16_t *qkv, const uint16_t *conv_w, uint16_t *conv_state,
-                               const uint8_t *mask, uint16_t *q, uint16_t *k, uint16_t *v, cudaStream_t st);
+                               const uint8_t *mask, uint16_t *q, uint16_t *k, uint16_t *v, unsigned *err,
+                               cudaStream_t st);
 
 cudaError_t launch_gating(const Sizes &s, const uint16_t *a, const uint16_t *b, const float *A_log,
                           const float *dt_bias, float *g, float *beta, cudaStream_t st);
@@ -63,6 +64,12 @@ cudaError_t launch_decode_window(const Sizes &s, const uint16_t *qkv, const uint
 // box1 x box0 in the two inner dimensions, one deep in the outer), no swizzle.
 bool encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t d2,
                     uint64_t d1, uint64_t d0, uint32_t box1, uint32_t box0);
+
+// Encodes a dense row-major tensor map of `rank` dimensions (dims and box
+// innermost first).  A box may be wider than its dimension: the elements past
+// the end read as zeros (loads) or are not written (stores).
+bool encode_tmap(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, int rank,
+                 const uint64_t *dims, const uint32_t *box, CUtensorMapSwizzle swizzle);
 
 // Encodes a 2-D row-major tensor map (rows x cols, box rows x box_cols).
 bool encode_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,

@@ -15,8 +15,10 @@
 //   S8 Y^T += D^T P^T, S += D^T Kc^T
 //   S9 y staged in shared memory as bf16 and stored by one TMA store of the
 //      tile (3-D tensor map, clipped at the row's T)
-// q, k, v tiles arrive by 2-D TMA (k and q 128B-swizzled straight into the
-// MMA operand layout), prefetched one chunk ahead.  Supports Dk = Dv = 128.
+// q, k, v tiles arrive by TMA (k and q 128B-swizzled straight into the
+// MMA operand layout), prefetched one chunk ahead.  Head sizes Dk, Dv of 32,
+// 64 or 128 all run on 128-wide tiles (chunk_form.cuh: the columns past the
+// head read as zeros), so a chunk costs the same at every head size.
 // Shared memory: 13 slots of 16 KiB reused across the phases of a chunk.
 // Chunks whose 64 steps are all masked are skipped: their y is written zero and
 // their inputs are never staged.
@@ -66,7 +68,7 @@ struct ChunkParams {
     const float *norm_w;
     float norm_eps;
     unsigned *err;
-    int B, T, Hk, Hv;
+    int B, T, Hk, Hv, Dk, Dv;
 };
 
 template <bool NORM>
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         if constexpr (NORM) prefetch_tmap(&tm_z);
     }
     if constexpr (NORM) {
-        for (int i = tid; i < kD; i += kThreads) s_w[i] = p.norm_w[i];
+        for (int i = tid; i < kD; i += kThreads) s_w[i] = i < p.Dv ? p.norm_w[i] : 0.0f;
     }
     if (warp == 0) {
         umma::tmem_alloc(&tmem_slot, kTmemCols);
@@ -128,21 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
     // ---- initial state -> TMEM S (row = dv, columns = dk); half 0: dk 0-63, half 1: 64-127
-    {
-        const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            float r[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.state_in != nullptr) x = *reinterpret_cast<const float4 *>(p.state_in + off + c * 32 + j);
-                r[j] = x.x; r[j + 1] = x.y; r[j + 2] = x.z; r[j + 3] = x.w;
-            }
-            umma::tmem_st32(tmem + lane_base + C_S + half * 64 + c * 32, r);
-        }
-        umma::tmem_st_wait();
-    }
+    state_to_tmem(p.state_in, tmem + lane_base + C_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
 
     // per-step g, beta, mask of a chunk: gathered into registers early (threads
     // < 64, one step each) and published to shared memory later, so the global
@@ -171,15 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         }
     };
     auto issue_tma = [&](int c) {
-        if (tid == 0) {
-            mbar_expect_tx(&bar_tma, 4 * 8192 + 16384);
-            const int rowg = b * T + c * kC;
-            tma_load_2d(sm + S_KQ, &tm_k, hk * kD, rowg, &bar_tma);
-            tma_load_2d(sm + S_KQ + kSlot, &tm_k, hk * kD + 64, rowg, &bar_tma);
-            tma_load_2d(sm + S_KQ + 8192, &tm_q, hk * kD, rowg, &bar_tma);
-            tma_load_2d(sm + S_KQ + kSlot + 8192, &tm_q, hk * kD + 64, rowg, &bar_tma);
-            tma_load_2d(sm + S_V, &tm_v, hv * kD, rowg, &bar_tma);
-        }
+        if (tid == 0) load_chunk_tiles(sm, S_KQ, S_V, &tm_k, &tm_q, &tm_v, hk, hv, b * T + c * kC, &bar_tma);
     };
 
     uint32_t mma_phase = 0;
@@ -203,10 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     };
 
     ChunkScan<kThreads> scan(p.mask == nullptr ? nullptr : p.mask + (size_t)b * T, T, scan_bits);
-    uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * kD + (size_t)hv * kD;
-    const size_t y_stride = (size_t)p.Hv * kD;
+    uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * p.Dv + (size_t)hv * p.Dv;
+    const size_t y_stride = (size_t)p.Hv * p.Dv;
     int c = scan.next_active(0);
-    zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), kD);
+    zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), p.Dv);
     if (c < nchunks) {
         issue_tma(c);
         gather_steps(c);
@@ -278,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             // the gQ slot is free now: bring in this chunk's z tile
             if (tid == 0) {
                 mbar_expect_tx(&bar_z, 16384);
-                tma_load_2d(sm + S_Z, &tm_z, hv * kD, b * T + t0, &bar_z);
+                tma_load_3d(sm + S_Z, &tm_z, 0, hv, b * T + t0, &bar_z);
                 z_pending = true;
                 z_parity = (uint32_t)(it & 1);
             }
@@ -330,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             }
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
             ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-            const float rs = 1.0f / sqrtf(ss * (1.0f / (float)kD) + p.norm_eps);
+            const float rs = 1.0f / sqrtf(ss * (1.0f / (float)p.Dv) + p.norm_eps);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int c16 = j * 4 + qd;
@@ -354,27 +334,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             if (!ok) break;
         }
         if (tid == 0) {
-            tma_store_3d(&tm_y, hv * kD, t0, b, sm + S_YST);
+            tma_store_4d(&tm_y, 0, hv, t0, b, sm + S_YST);
             bulk_commit();
         }
-        zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), kD);
+        zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), p.Dv);
         c = cn;
     }
 
     if (tid == 0) bulk_wait_read();   // the last y store has read its tile
     // ---- final state (only when every wait succeeded)
     if (__syncthreads_and(ok)) {
-        const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
-#pragma unroll
-        for (int cpart = 0; cpart < 2; ++cpart) {
-            float sv[32];
-            umma::tmem_ld32(tmem + lane_base + C_S + half * 64 + cpart * 32, sv);
-            umma::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(p.state_out + off + cpart * 32 + j) =
-                    make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
-        }
+        state_from_tmem(p.state_out, tmem + lane_base + C_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
     } else if (tid == 0) {
         // a wait gave up: give in-flight MMAs (and a z copy) a bounded chance to drain
         mbar_wait(&bar_mma, mma_phase & 1u, nullptr);
@@ -397,31 +367,18 @@ cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint
                                    const float *g, const float *beta, const float *state_in, float *state_out,
                                    const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
                                    const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st) {
-    if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
-    CUtensorMap tk, tq, tv, tz, ty;
-    const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
-    if (!encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tmap_3d(&ty, y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)s.B, (uint64_t)s.T,
-                        (uint64_t)s.Hv * kD, kC, kD))
-        return cudaErrorInvalidValue;
-    tz = tv;   // unused without the norm
-    if (z != nullptr && !encode_tmap_2d(&tz, z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC,
-                                        kD, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
+    if (s.Dk > kD || s.Dv > kD) return cudaErrorNotSupported;
+    ChunkMaps m;
+    if (!encode_chunk_maps(&m, s, q, k, v, z, y)) return cudaErrorInvalidValue;
     cudaError_t e = z != nullptr ? set_smem_attr<true>() : set_smem_attr<false>();
     if (e != cudaSuccess) return e;
     ChunkParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y, norm_w, norm_eps, err,
-                  s.B, s.T, s.Hk, s.Hv};
+                  s.B, s.T, s.Hk, s.Hv, s.Dk, s.Dv};
     dim3 grid(s.Hv, s.B);
     if (z != nullptr)
-        prefill_chunk_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, tz, ty, p);
+        prefill_chunk_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(m.k, m.q, m.v, m.z, m.y, p);
     else
-        prefill_chunk_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tk, tq, tv, tz, ty, p);
+        prefill_chunk_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(m.k, m.q, m.v, m.z, m.y, p);
     return cudaGetLastError();
 }
 

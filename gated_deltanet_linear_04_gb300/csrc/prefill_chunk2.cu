@@ -78,7 +78,7 @@ struct TwoPassParams {
     uint8_t *blobs;
     int *ready;         // overlapped form: one flag per blob (zeroed before launch); else null
     unsigned *err;
-    int B, T, Hk, Hv, nchunks;
+    int B, T, Hk, Hv, Dk, Dv, nchunks;
 };
 
 // Static shared memory of both roles.
@@ -159,15 +159,7 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
         sh.s_g[tid] = gg;
         sh.s_b[tid] = bb;
     }
-    if (tid == 0) {
-        mbar_expect_tx(&sh.bar0, 4 * 8192 + 16384);
-        const int rowg = b * T + t0;
-        tma_load_2d(sm + P1_KQ, tm_k, hk * kD, rowg, &sh.bar0);
-        tma_load_2d(sm + P1_KQ + kSlot, tm_k, hk * kD + 64, rowg, &sh.bar0);
-        tma_load_2d(sm + P1_KQ + 8192, tm_q, hk * kD, rowg, &sh.bar0);
-        tma_load_2d(sm + P1_KQ + kSlot + 8192, tm_q, hk * kD + 64, rowg, &sh.bar0);
-        tma_load_2d(sm + P1_V, tm_v, hv * kD, rowg, &sh.bar0);
-    }
+    if (tid == 0) load_chunk_tiles(sm, P1_KQ, P1_V, tm_k, tm_q, tm_v, hk, hv, b * T + t0, &sh.bar0);
     __syncthreads();
 
     auto wait_mma = [&]() {
@@ -271,21 +263,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
     const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
 
     // initial state -> TMEM S (row = dv, columns = dk); half 0: dk 0-63, half 1: 64-127
-    {
-        const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            float r[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.state_in != nullptr) x = *reinterpret_cast<const float4 *>(p.state_in + off + cc * 32 + j);
-                r[j] = x.x; r[j + 1] = x.y; r[j + 2] = x.z; r[j + 3] = x.w;
-            }
-            umma::tmem_st32(lane_tmem + C_S + half * 64 + cc * 32, r);
-        }
-        umma::tmem_st_wait();
-    }
+    state_to_tmem(p.state_in, lane_tmem + C_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
     (void)lane;
 
     int pf_m = 0;
@@ -335,10 +313,10 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
     };
 
     ChunkScan<kThreads> scan(p.mask == nullptr ? nullptr : p.mask + (size_t)b * T, T, sh.scan_bits);
-    uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * kD + (size_t)hv * kD;
-    const size_t y_stride = (size_t)p.Hv * kD;
+    uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * p.Dv + (size_t)hv * p.Dv;
+    const size_t y_stride = (size_t)p.Hv * p.Dv;
     int c = scan.next_active(0);
-    zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), kD);
+    zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), p.Dv);
     if (c < nchunks) {
         load_a(c, 0);
         load_b(c, 0);
@@ -404,27 +382,17 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         umma::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            tma_store_3d(tm_y, hv * kD, t0, b, sm + P2_YST);
+            tma_store_4d(tm_y, 0, hv, t0, b, sm + P2_YST);
             bulk_commit();
         }
         if (tid < kC) sh.s_m[st ^ 1][tid] = pf_m;
-        zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), kD);
+        zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), p.Dv);
         c = cn;
     }
 
     if (tid == 0) bulk_wait_read();   // the last y store has read the staging tile
     if (__syncthreads_and(ok)) {
-        const size_t off = (((size_t)b * p.Hv + hv) * kD + row) * kD + half * 64;
-#pragma unroll
-        for (int cpart = 0; cpart < 2; ++cpart) {
-            float sv[32];
-            umma::tmem_ld32(lane_tmem + C_S + half * 64 + cpart * 32, sv);
-            umma::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(p.state_out + off + cpart * 32 + j) =
-                    make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
-        }
+        state_from_tmem(p.state_out, lane_tmem + C_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
     } else if (tid == 0) {
         // a wait gave up: give in-flight MMAs and copies a bounded chance to drain
         mbar_wait(&sh.bar2, mma_phase & 1u, nullptr);
@@ -540,18 +508,10 @@ cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uin
                                     const float *g, const float *beta, const float *state_in, float *state_out,
                                     const uint8_t *mask, const int *order, uint16_t *y, void *blobs,
                                     unsigned *err, cudaStream_t st) {
-    if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
-    CUtensorMap tk, tq, tv, ty;
-    const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
-    if (!encode_tmap_2d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap_2d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hk * kD, kC, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap_2d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, (uint64_t)s.Hv * kD, kC, kD,
-                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tmap_3d(&ty, y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)s.B, (uint64_t)s.T,
-                        (uint64_t)s.Hv * kD, kC, kD))
-        return cudaErrorInvalidValue;
+    if (s.Dk > kD || s.Dv > kD) return cudaErrorNotSupported;
+    ChunkMaps m;
+    if (!encode_chunk_maps(&m, s, q, k, v, nullptr, y)) return cudaErrorInvalidValue;
+    const CUtensorMap &tk = m.k, &tq = m.q, &tv = m.v, &ty = m.y;
     static unsigned long long set1 = 0, set2 = 0, set3 = 0;   // one bit per device
     cudaError_t e = set_max_smem(set1, chunk_prep_kernel, kP1Smem);
     if (e == cudaSuccess) e = set_max_smem(set2, chunk_state_kernel, kP2Smem);
@@ -561,7 +521,7 @@ cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uin
     const int n_heads = s.B * s.Hv;
     const size_t n_blobs = blob_count(s);
     TwoPassParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y,
-                    static_cast<uint8_t *>(blobs), nullptr, err, s.B, s.T, s.Hk, s.Hv, nchunks};
+                    static_cast<uint8_t *>(blobs), nullptr, err, s.B, s.T, s.Hk, s.Hv, s.Dk, s.Dv, nchunks};
 
     // Overlapped form when the producers (all SMs but the heads') outnumber
     // the heads about three to one: a chunk image takes the producers roughly

@@ -225,8 +225,10 @@ GDN_API gdn_status gdn_decode_window(const gdn_dims *dims, const uint16_t *qkv, 
  * Wholly masked 64-step chunks cost only their zero y stores.
  * The chunked form reads q, k, v of masked steps (their contribution is then
  * cancelled exactly), so those entries must hold finite values; the zeros
- * gdn_conv_update writes there qualify.  It supports Dk = Dv = 128 (other
- * sizes give GDN_ERR_UNSUPPORTED).
+ * gdn_conv_update writes there qualify.  It supports every Dk, Dv in
+ * {32, 64, 128}: smaller heads run in the same 128-wide tiles, the channels
+ * past the head read as zeros and are never written, so a chunk costs what it
+ * costs at 128 and the results are those of the true sizes.
  */
 GDN_API gdn_status gdn_prefill(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
                        const uint16_t *v, const float *g, const float *beta,

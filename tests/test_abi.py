@@ -102,7 +102,10 @@ def test_prefill_chunk_argument(lib):
     # the optional row-order workspace: a few bytes per batch row, whole 256s
     n0 = lib.gdn_prefill_workspace_size(ctypes.byref(d), 0)
     assert n0 > 0 and n0 % 256 == 0 and n0 >= 8 * d.B
-    assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 64) == n0
+    # chunked with fewer heads than SMs: plus the two-pass images, one 145 KiB
+    # blob per head and chunk of 64 steps and a ready flag each (any head size)
+    n_blobs = d.B * d.Hv * ((d.T + 63) // 64)
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 64) == n0 + n_blobs * 148480 + 256
     assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 32) == 0
     assert lib.gdn_prefill_workspace_size(ctypes.byref(_dims(B=0)), 0) == 0
 

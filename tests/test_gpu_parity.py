@@ -343,12 +343,38 @@ def test_prefill_two_pass_equals_single_pass(gdn, B, T, Hk, Hv, mk, st):
     U.assert_state_close(s2.cpu().numpy(), sr)
 
 
-def test_prefill_chunked_rejects_other_head_sizes(gdn):
-    d = wl.Dims(B=1, T=8, Hk=1, Hv=2, Dk=64, Dv=128)
-    r = recurrence_inputs(d, 1)
-    with pytest.raises(gdn.GdnError) as e:
-        gdn.prefill(d, *(to_dev(r[x]) for x in ("q", "k", "v", "g", "beta")), None, None, chunk=64)
-    assert e.value.status == gdn.GDN_ERR_UNSUPPORTED
+CHUNK_SMALL_HEAD_CASES = [
+    # B, T, Hk, Hv, Dk, Dv, mask, state   (head sizes below 128: zero-padded 128-wide tiles)
+    (1, 8, 1, 2, 32, 32, None, "zeros"),
+    (2, 130, 1, 2, 64, 64, "right", "normal"),
+    (1, 200, 2, 4, 32, 128, None, "normal"),
+    (2, 97, 1, 3, 128, 64, "random", "normal"),
+    (3, 333, 1, 2, 64, 32, "blocks", "normal"),
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,Dk,Dv,mk,st", CHUNK_SMALL_HEAD_CASES)
+def test_prefill_chunked_small_heads(gdn, B, T, Hk, Hv, Dk, Dv, mk, st):
+    """The chunked form at Dk, Dv of 32 and 64 against the oracle, in the
+    single pass and in the two-pass form, which agree bit for bit."""
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv)
+    mask = make_mask(mk, B, T, 9 + T)
+    r = recurrence_inputs(d, 900 + T, mask)
+    state_in = r["state"] if st == "normal" else None
+    dev = [to_dev(r[n]) for n in ("q", "k", "v", "g", "beta")]
+    y1, s1 = gdn.prefill(d, *dev, to_dev(state_in), to_dev(mask), chunk=64, use_workspace=False)
+    y2, s2 = gdn.prefill(d, *dev, to_dev(state_in), to_dev(mask), chunk=64, use_workspace=True)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert gdn.gdn_prefill_workspace_size(d, 64) > gdn.gdn_prefill_workspace_size(d, 0), "two passes expected"
+    s0 = None if state_in is None else state_in.numpy().astype(np.float64)
+    yr, sr = oracle.recurrence(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                               r["beta"].numpy().astype(np.float64), s0, np_mask(mask))
+    U.assert_y_close(U.bf16_dev_to_f64(y1), yr)
+    U.assert_state_close(s1.cpu().numpy(), sr)
+    assert torch.equal(y1, y2) and torch.equal(s1, s2)
+    if mask is not None:
+        assert np.all(U.bits(y1)[mask.numpy() == 0] == 0), "padded y must be exactly zero"
 
 
 def test_prefill_in_place_and_split_is_bitwise(gdn):
@@ -582,6 +608,8 @@ GATED_PREFILL_CASES = [
     (64, 1, 160, 8, 160, 128, 128, "blocks"),
     (0, 2, 100, 2, 4, 64, 32, "random"),
     (0, 1, 77, 1, 2, 128, 128, None),
+    (64, 2, 100, 80, 80, 64, 64, "random"),       # head size 64, the norm in the epilogue (mean over Dv)
+    (64, 2, 90, 1, 2, 32, 64, "right"),
 ]
 
 
