@@ -53,14 +53,17 @@ constexpr uint32_t kSlot = 16384;
 // TMEM columns
 constexpr uint32_t C_QK = 0, C_D = 64, C_W = 128, C_Y = 192, C_S = 256;
 
-// Tensor maps of the chunked kernels (host side).  k and q as [B*T][Hk][Dk]
-// with a [64 steps][1 head][64 channels] box, 128-byte swizzled (a chunk's
-// tile is two such boxes, channels 0-63 and 64-127); v and z as [B*T][Hv][Dv]
-// with a [64][1][128] box; y as [B][T][Hv][Dv] with a [1][64][1][128] box.
-// The kernels always work on 128-wide tiles: with Dk or Dv below 128 the
-// boxes run past the head's channels, the loads read zeros there and the y
-// store writes only the first Dv channels, so the padded rows and columns of
-// every product are exact zeros and the results are those of the true sizes.
+// Tensor maps of the chunked kernels (host side).  The kernels always work on
+// 128-wide tiles.  At a head size of 128 the maps are plain row-major views:
+// k and q [B*T][Hk*128] with a [64 steps][64 channels] box, 128-byte swizzled
+// (a chunk's tile is two boxes, channels 0-63 and 64-127 of the head); v and
+// z [B*T][Hv*128] with a [64][128] box; y [B][T][Hv*128] with a [1][64][128]
+// box.  Below 128 the head is a dimension of its own: k and q [B*T][Hk][Dk]
+// with a [64][1][64] box, v and z [B*T][Hv][Dv] with a [64][1][128] box, y
+// [B][T][Hv][Dv] with a [1][64][1][128] box; the boxes run past the head's
+// channels, the loads read zeros there and the y store writes only the first
+// Dv channels, so the padded rows and columns of every product are exact
+// zeros and the results are those of the true sizes.
 struct ChunkMaps {
     CUtensorMap k, q, v, z, y;
 };
@@ -68,32 +71,78 @@ struct ChunkMaps {
 inline bool encode_chunk_maps(ChunkMaps *m, const Sizes &s, const uint16_t *q, const uint16_t *k,
                               const uint16_t *v, const uint16_t *z, uint16_t *y) {
     const uint64_t rows = (uint64_t)s.B * (uint64_t)s.T;
-    const uint64_t dk[3] = {(uint64_t)s.Dk, (uint64_t)s.Hk, rows};
-    const uint64_t dv[3] = {(uint64_t)s.Dv, (uint64_t)s.Hv, rows};
-    const uint64_t dy[4] = {(uint64_t)s.Dv, (uint64_t)s.Hv, (uint64_t)s.T, (uint64_t)s.B};
-    const uint32_t bk[3] = {64, 1, (uint32_t)kC}, bv[3] = {(uint32_t)kD, 1, (uint32_t)kC};
-    const uint32_t by[4] = {(uint32_t)kD, 1, (uint32_t)kC, 1};
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!encode_tmap(&m->k, k, bf, 2, 3, dk, bk, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap(&m->q, q, bf, 2, 3, dk, bk, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tmap(&m->v, v, bf, 2, 3, dv, bv, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tmap(&m->y, y, bf, 2, 4, dy, by, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return false;
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B, ns = CU_TENSOR_MAP_SWIZZLE_NONE;
+    bool ok = true;
+    if (s.Dk == kD) {
+        const uint64_t dk[2] = {(uint64_t)s.Hk * kD, rows};
+        const uint32_t bk[2] = {64, (uint32_t)kC};
+        ok = encode_tmap(&m->k, k, bf, 2, 2, dk, bk, sw) && encode_tmap(&m->q, q, bf, 2, 2, dk, bk, sw);
+    } else {
+        const uint64_t dk[3] = {(uint64_t)s.Dk, (uint64_t)s.Hk, rows};
+        const uint32_t bk[3] = {64, 1, (uint32_t)kC};
+        ok = encode_tmap(&m->k, k, bf, 2, 3, dk, bk, sw) && encode_tmap(&m->q, q, bf, 2, 3, dk, bk, sw);
+    }
+    if (!ok) return false;
+    auto vmap = [&](CUtensorMap *t, const uint16_t *ptr) {
+        if (s.Dv == kD) {
+            const uint64_t dv[2] = {(uint64_t)s.Hv * kD, rows};
+            const uint32_t bv[2] = {(uint32_t)kD, (uint32_t)kC};
+            return encode_tmap(t, ptr, bf, 2, 2, dv, bv, ns);
+        }
+        const uint64_t dv[3] = {(uint64_t)s.Dv, (uint64_t)s.Hv, rows};
+        const uint32_t bv[3] = {(uint32_t)kD, 1, (uint32_t)kC};
+        return encode_tmap(t, ptr, bf, 2, 3, dv, bv, ns);
+    };
+    if (!vmap(&m->v, v)) return false;
+    if (s.Dv == kD) {
+        const uint64_t dy[3] = {(uint64_t)s.Hv * kD, (uint64_t)s.T, (uint64_t)s.B};
+        const uint32_t by[3] = {(uint32_t)kD, (uint32_t)kC, 1};
+        ok = encode_tmap(&m->y, y, bf, 2, 3, dy, by, ns);
+    } else {
+        const uint64_t dy[4] = {(uint64_t)s.Dv, (uint64_t)s.Hv, (uint64_t)s.T, (uint64_t)s.B};
+        const uint32_t by[4] = {(uint32_t)kD, 1, (uint32_t)kC, 1};
+        ok = encode_tmap(&m->y, y, bf, 2, 4, dy, by, ns);
+    }
+    if (!ok) return false;
     m->z = m->v;   // unused without the gated norm
-    return z == nullptr || encode_tmap(&m->z, z, bf, 2, 3, dv, bv, CU_TENSOR_MAP_SWIZZLE_NONE);
+    return z == nullptr || vmap(&m->z, z);
 }
 
 // Chunk c's k, q (128B-swizzled K-halves) and v tiles of head (hk, hv) of the
-// rows starting at flat row `rowg` = b * T + c * 64 into the KQ and V slots.
+// rows starting at flat row `rowg` = b * T + c * 64 into the KQ and V slots
+// (the maps' forms above: Dk, Dv of 128 or below).
 __device__ __forceinline__ void load_chunk_tiles(uint8_t *sm, uint32_t kq_off, uint32_t v_off, const CUtensorMap *tm_k,
-                                                 const CUtensorMap *tm_q, const CUtensorMap *tm_v, int hk, int hv,
-                                                 int rowg, uint64_t *bar) {
+                                                 const CUtensorMap *tm_q, const CUtensorMap *tm_v, int Dk, int Dv,
+                                                 int hk, int hv, int rowg, uint64_t *bar) {
     mbar_expect_tx(bar, 4 * 8192 + 16384);
-    tma_load_3d(sm + kq_off, tm_k, 0, hk, rowg, bar);
-    tma_load_3d(sm + kq_off + kSlot, tm_k, 64, hk, rowg, bar);
-    tma_load_3d(sm + kq_off + 8192, tm_q, 0, hk, rowg, bar);
-    tma_load_3d(sm + kq_off + kSlot + 8192, tm_q, 64, hk, rowg, bar);
-    tma_load_3d(sm + v_off, tm_v, 0, hv, rowg, bar);
+    if (Dk == kD) {
+        tma_load_2d(sm + kq_off, tm_k, hk * kD, rowg, bar);
+        tma_load_2d(sm + kq_off + kSlot, tm_k, hk * kD + 64, rowg, bar);
+        tma_load_2d(sm + kq_off + 8192, tm_q, hk * kD, rowg, bar);
+        tma_load_2d(sm + kq_off + kSlot + 8192, tm_q, hk * kD + 64, rowg, bar);
+    } else {
+        tma_load_3d(sm + kq_off, tm_k, 0, hk, rowg, bar);
+        tma_load_3d(sm + kq_off + kSlot, tm_k, 64, hk, rowg, bar);
+        tma_load_3d(sm + kq_off + 8192, tm_q, 0, hk, rowg, bar);
+        tma_load_3d(sm + kq_off + kSlot + 8192, tm_q, 64, hk, rowg, bar);
+    }
+    if (Dv == kD) tma_load_2d(sm + v_off, tm_v, hv * kD, rowg, bar);
+    else tma_load_3d(sm + v_off, tm_v, 0, hv, rowg, bar);
+}
+
+// The chunk's [64 steps][128] tile of y (or z, for loads) of head hv at step
+// t0 of batch row b, in the map form of the head size.
+__device__ __forceinline__ void store_chunk_y(const CUtensorMap *tm_y, int Dv, int hv, int t0, int b,
+                                              const uint8_t *src) {
+    if (Dv == kD) tma_store_3d(tm_y, hv * kD, t0, b, src);
+    else tma_store_4d(tm_y, 0, hv, t0, b, src);
+}
+
+__device__ __forceinline__ void load_chunk_z(uint8_t *dst, const CUtensorMap *tm_z, int Dv, int hv, int rowg,
+                                             uint64_t *bar) {
+    if (Dv == kD) tma_load_2d(dst, tm_z, hv * kD, rowg, bar);
+    else tma_load_3d(dst, tm_z, 0, hv, rowg, bar);
 }
 
 // The f32 state of head (b, hv) between global memory and the S columns of

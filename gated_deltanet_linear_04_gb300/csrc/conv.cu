@@ -316,39 +316,61 @@ __device__ __forceinline__ void conv_segment(const ConvParams &p, const CUtensor
     // of squares, one four-token warp reduction for the q/k norm, the stores;
     // the sub-tile loop is not unrolled, which keeps the code within the
     // instruction cache
+    // conv + SiLU of one token from its K window rows (oldest first), with
+    // its sum of squares
+    auto conv_token = [&](const Pairs<CPL> &r0, const Pairs<CPL> &r1, const Pairs<CPL> &r2, const Pairs<CPL> &r3,
+                          Pairs<CPL> &x, float &ss) {
+        float2 sq = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            float2 u = __fmul2_rn(tap[0][i], r0.v[i]);
+            u = __ffma2_rn(tap[1][i], r1.v[i], u);
+            u = __ffma2_rn(tap[2][i], r2.v[i], u);
+            u = __ffma2_rn(tap[3][i], r3.v[i], u);
+            x.v[i] = silu2(u);
+            sq = __ffma2_rn(x.v[i], x.v[i], sq);
+        }
+        ss = CPL >= 2 ? sq.x + sq.y : sq.x;
+    };
 #pragma unroll 1
     for (int s = 0; s < NS && s * kSub < nt; ++s) {
         Pairs<CPL> x[kSub];
         float ss[kSub];
+        if (((valid >> (s * kSub)) & 0xFu) == 0xFu) {
+            // four valid tokens: the window rolls by static register indices
+            Pairs<CPL> xr[kSub];
 #pragma unroll
-        for (int r = 0; r < kSub; ++r) {
-            const int tl = s * kSub + r;
-            ss[r] = 0.0f;
+            for (int r = 0; r < kSub; ++r) xr[r] = unpack_pairs<CPL>(load_raw<CPL>(rows + (s * kSub + r) * D));
+            conv_token(win[0], win[1], win[2], xr[0], x[0], ss[0]);
+            conv_token(win[1], win[2], xr[0], xr[1], x[1], ss[1]);
+            conv_token(win[2], xr[0], xr[1], xr[2], x[2], ss[2]);
+            conv_token(xr[0], xr[1], xr[2], xr[3], x[3], ss[3]);
+            win[0] = xr[1];
+            win[1] = xr[2];
+            win[2] = xr[3];
+        } else {
+            // masked steps (or the tile's end) inside: token by token, only
+            // valid tokens entering the window
 #pragma unroll
-            for (int i = 0; i < NP; ++i) x[r].v[i] = make_float2(0.0f, 0.0f);
-            if (tl < nt && ((valid >> tl) & 1u)) {
-                const Pairs<CPL> xr = unpack_pairs<CPL>(load_raw<CPL>(rows + tl * D));
-                float2 sq = make_float2(0.0f, 0.0f);
+            for (int r = 0; r < kSub; ++r) {
+                const int tl = s * kSub + r;
+                ss[r] = 0.0f;
 #pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    float2 u = __fmul2_rn(tap[0][i], win[0].v[i]);
-                    u = __ffma2_rn(tap[1][i], win[1].v[i], u);
-                    u = __ffma2_rn(tap[2][i], win[2].v[i], u);
-                    u = __ffma2_rn(tap[3][i], xr.v[i], u);
-                    x[r].v[i] = silu2(u);
-                    sq = __ffma2_rn(x[r].v[i], x[r].v[i], sq);
+                for (int i = 0; i < NP; ++i) x[r].v[i] = make_float2(0.0f, 0.0f);
+                if (tl < nt && ((valid >> tl) & 1u)) {
+                    const Pairs<CPL> xr = unpack_pairs<CPL>(load_raw<CPL>(rows + tl * D));
+                    conv_token(win[0], win[1], win[2], xr, x[r], ss[r]);
+                    win[0] = win[1];
+                    win[1] = win[2];
+                    win[2] = xr;
                 }
-                ss[r] = CPL >= 2 ? sq.x + sq.y : sq.x;
-                win[0] = win[1];
-                win[1] = win[2];
-                win[2] = xr;
             }
         }
         if (kind != 2) {
             // each lane normalises one token; the four factors are then
             // broadcast from lanes 0, 8, 16 and 24
             const float tot = warp_sum4(ss, lane);
-            const float rs_mine = (1.0f / sqrtf(tot * inv_d + p.eps)) * scale;
+            const float rs_mine = rsqrtf(tot * inv_d + p.eps) * scale;
 #pragma unroll
             for (int r = 0; r < kSub; ++r) {
                 const float rs = __shfl_sync(0xffffffffu, rs_mine, ((r >> 1) << 4) | ((r & 1) << 3));

@@ -79,14 +79,15 @@ struct ChunkScan {
 
 // Zero y for steps [t_begin, t_end) of one row: `width` bf16 values per step
 // (a multiple of 8) starting at `first` (16-byte aligned), rows `stride`
-// elements apart.  Called by the whole block; plain 16-byte stores.
+// elements apart.  Called by the whole block, whose size is a multiple of
+// width / 8: each thread keeps one 16-byte column group and steps through
+// the rows (plain 16-byte stores, no division in the loop).
 __device__ __forceinline__ void zero_y_rows(uint16_t *first, size_t stride, int t_begin, int t_end, int width) {
-    const long long per = width / 8;
-    const long long n = (long long)(t_end - t_begin) * per;
-    for (long long i = threadIdx.x; i < n; i += blockDim.x) {
-        const long long t = t_begin + i / per, c8 = (i % per) * 8;
+    const int per = width >> 3;
+    const int c8 = (int)(threadIdx.x % (unsigned)per) * 8;
+    const int rows_per_pass = (int)blockDim.x / per;
+    for (int t = t_begin + (int)(threadIdx.x / (unsigned)per); t < t_end; t += rows_per_pass)
         *reinterpret_cast<uint4 *>(first + (size_t)t * stride + (size_t)c8) = make_uint4(0u, 0u, 0u, 0u);
-    }
 }
 
 }  // namespace gdn

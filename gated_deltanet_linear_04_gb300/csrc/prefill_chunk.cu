@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         }
     };
     auto issue_tma = [&](int c) {
-        if (tid == 0) load_chunk_tiles(sm, S_KQ, S_V, &tm_k, &tm_q, &tm_v, hk, hv, b * T + c * kC, &bar_tma);
+        if (tid == 0)
+            load_chunk_tiles(sm, S_KQ, S_V, &tm_k, &tm_q, &tm_v, p.Dk, p.Dv, hk, hv, b * T + c * kC, &bar_tma);
     };
 
     uint32_t mma_phase = 0;
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             // the gQ slot is free now: bring in this chunk's z tile
             if (tid == 0) {
                 mbar_expect_tx(&bar_z, 16384);
-                tma_load_3d(sm + S_Z, &tm_z, 0, hv, b * T + t0, &bar_z);
+                load_chunk_z(sm + S_Z, &tm_z, p.Dv, hv, b * T + t0, &bar_z);
                 z_pending = true;
                 z_parity = (uint32_t)(it & 1);
             }
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             if (!ok) break;
         }
         if (tid == 0) {
-            tma_store_4d(&tm_y, 0, hv, t0, b, sm + S_YST);
+            store_chunk_y(&tm_y, p.Dv, hv, t0, b, sm + S_YST);
             bulk_commit();
         }
         zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), p.Dv);

@@ -52,13 +52,25 @@ constexpr uint32_t B_KT = kGroupA, B_P = kGroupA + 32768;
 constexpr uint32_t kGroupB = 32768 + 16384;
 constexpr size_t kBlobBytes = (size_t)kGroupA + kGroupB;
 
-// pass 1 shared memory: the single-pass slot map (13 slots of 16 KiB); after
-// the products that read them, K/Q/V and (bV)^T hold P, U^T and -W
-constexpr uint32_t P1_KQ = 0 * kSlot, P1_V = 2 * kSlot, P1_GQ = 3 * kSlot, P1_KT = 5 * kSlot,
-                   P1_BV = 7 * kSlot, P1_BK = 9 * kSlot, P1_A = 11 * kSlot, P1_T = 12 * kSlot;
-constexpr uint32_t P1_P = P1_KQ;          // slot 0, after [K;Q] K^T and the builds
-constexpr uint32_t P1_UT = 1 * kSlot;     // slots 1-2, after the U/W products
-constexpr uint32_t P1_NW = P1_BV;         // slots 7-8, after the U product
+// pass 1 shared memory: 13 slots of 16 KiB in one of two maps.  A unit's k/q
+// and v tiles arrive in its KQ (two slots) and V slots; once the products
+// have read them, KQ and V hold P and U^T and (bV)^T holds -W.  The outputs
+// (gQ, Kc^T, -W, P, U^T) then leave by bulk stores while the next unit
+// starts.  The BK pair and the A slot are free at the end of a unit, and the
+// next unit's k/q and v tiles are fetched into them as soon as the U/W
+// products complete, so the two maps alternate:
+//   map 0: KQ 6-7, V 8,  gQ 0-1, Kc^T 2-3, bV 4-5, bK 9-10, A 11, T 12
+//   map 1: KQ 9-10, V 11, gQ 0-1, Kc^T 2-3, bV 4-5, bK 6-7,  A 8,  T 12
+// (map 0's bK/A are map 1's KQ/V and the other way round).  Every other
+// slot of a unit is one of the previous unit's outputs or T, written only
+// after the previous stores have read them out.
+struct PrepMap {
+    uint32_t kq, v, gq, kt, bv, bk, a, t;
+};
+__device__ __forceinline__ PrepMap prep_map(int parity) {
+    return parity == 0 ? PrepMap{6 * kSlot, 8 * kSlot, 0, 2 * kSlot, 4 * kSlot, 9 * kSlot, 11 * kSlot, 12 * kSlot}
+                       : PrepMap{9 * kSlot, 11 * kSlot, 0, 2 * kSlot, 4 * kSlot, 6 * kSlot, 8 * kSlot, 12 * kSlot};
+}
 constexpr uint32_t kP1Smem = 13 * kSlot + 1024;
 
 // pass 2 shared memory: group A and group B images, then D^T and y staging
@@ -126,45 +138,83 @@ __device__ __forceinline__ bool wait_ready(const int *flag, unsigned *err) {
 }
 
 // ---------------------------------------------------------------------------
-// pass 1: the state-independent part of chunk c of head (b, hv).  The caller
-// has initialised sh.bar0 / sh.bar1 and allocated >= 256 TMEM columns; the
-// phases count completions of those barriers across calls.  Returns false if
-// a wait gave up.  Ends with a block barrier, shared memory free again.
+// pass 1: the state-independent part of chunk c of head (b, hv), one unit of a
+// producer's sequence.  The producer keeps across its units: the TMA and MMA
+// barrier phases, the gates of the current unit (threads < 64, in registers),
+// whether the previous unit's stores are still to be published, and which
+// map the current unit uses.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensorMap *tm_k, const CUtensorMap *tm_q,
-                                          const CUtensorMap *tm_v, TwoPassShared &sh, uint8_t *sm, uint32_t base,
-                                          uint32_t tmem, int c, int b, int hv, uint32_t &tma_phase,
-                                          uint32_t &mma_phase) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2, row = quad * 32 + lane;
-    const int hk = hv / (p.Hv / p.Hk);
-    const int T = p.T, t0 = c * kC;
-    const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
-    float *As = reinterpret_cast<float *>(sm + P1_A);
-    float *Ys = reinterpret_cast<float *>(sm + P1_T);
+struct Producer {
+    uint32_t tma_phase = 0, mma_phase = 0;
+    int parity = 0;
+    float gg = 1.0f, bb = 0.0f;   // this thread's step of the current unit (threads < 64)
+    int *pending_flag = nullptr;  // ready flag of the previous unit, published once its stores are complete
+    bool tma_pending = false;     // thread 0: a prefetch is in flight
+};
 
-    // the chunk's gates; a wholly masked chunk is skipped here and in pass 2
-    float gg = 1.0f, bb = 0.0f;
+// Gates (and whether the chunk holds a valid step) of unit (c, b, hv) into
+// this thread's registers; returns whether the chunk holds a valid step
+// (block-wide when there is a mask).
+__device__ __forceinline__ bool unit_gates(const TwoPassParams &p, int c, int b, int hv, float &gg, float &bb) {
+    const int tid = threadIdx.x, t = c * kC + tid;
+    gg = 1.0f;
+    bb = 0.0f;
     int m = 0;
-    if (tid < kC && t0 + tid < T) {
-        const size_t gi = ((size_t)b * T + t0 + tid) * p.Hv + hv;
-        m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t0 + tid] != 0);
+    if (tid < kC && t < p.T) {
+        const size_t gi = ((size_t)b * p.T + t) * p.Hv + hv;
+        m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * p.T + t] != 0);
         if (m) {
             gg = p.g[gi];
             bb = p.beta[gi];
         }
     }
-    if (!__syncthreads_or(m)) return true;
-    if (tid < kC) {
-        sh.s_g[tid] = gg;
-        sh.s_b[tid] = bb;
+    return p.mask == nullptr ? true : __syncthreads_or(m) != 0;
+}
+
+// k/q and v tiles of unit (c, b, hv) into the KQ and V slots of `m` (thread 0)
+__device__ __forceinline__ void unit_tiles(const TwoPassParams &p, const CUtensorMap *tm_k, const CUtensorMap *tm_q,
+                                           const CUtensorMap *tm_v, TwoPassShared &sh, uint8_t *sm,
+                                           const PrepMap &m, int c, int b, int hv) {
+    load_chunk_tiles(sm, m.kq, m.v, tm_k, tm_q, tm_v, p.Dk, p.Dv, hv / (p.Hv / p.Hk), hv, b * p.T + c * kC, &sh.bar0);
+}
+
+// Publishes the previous unit's image once its stores have completed (thread 0).
+__device__ __forceinline__ void publish_pending(Producer &pr) {
+    if (pr.pending_flag != nullptr) {
+        bulk_wait_all();    // the writes are done, not only read out
+        __threadfence();    // ... and so is the meta store
+        publish_ready(pr.pending_flag);
+        pr.pending_flag = nullptr;
     }
-    if (tid == 0) load_chunk_tiles(sm, P1_KQ, P1_V, tm_k, tm_q, tm_v, hk, hv, b * T + t0, &sh.bar0);
-    __syncthreads();
+}
+
+// One unit.  Its k/q/v tiles are in flight on sh.bar0 into the KQ/V slots of
+// map pr.parity and its gates are in pr.gg/pr.bb.  `next` (c, b, hv; c < 0
+// for none) is the producer's next unit: its tiles are fetched once this
+// unit's U/W products have completed.  Returns false if a wait gave up.
+// Ends with a block barrier; the unit's stores are committed, and with ready
+// flags their publication is left to the next unit (or publish_pending).
+__device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensorMap *tm_k, const CUtensorMap *tm_q,
+                                          const CUtensorMap *tm_v, TwoPassShared &sh, uint8_t *sm, uint32_t base,
+                                          uint32_t tmem, Producer &pr, int c, int b, int hv, int nc, int nb,
+                                          int nhv) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2, row = quad * 32 + lane;
+    const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
+    const PrepMap M = prep_map(pr.parity);
+    float *As = reinterpret_cast<float *>(sm + M.a);
+    float *Ys = reinterpret_cast<float *>(sm + M.t);
+
+    if (tid < kC) {
+        sh.s_g[tid] = pr.gg;
+        sh.s_b[tid] = pr.bb;
+    }
+    // the previous unit's outputs (this unit's gQ ... T slots) have been read out
+    if (tid == 0) bulk_wait_read();
 
     auto wait_mma = [&]() {
-        bool w = mbar_wait(&sh.bar1, mma_phase & 1u, p.err);
-        ++mma_phase;
+        bool w = mbar_wait(&sh.bar1, pr.mma_phase & 1u, p.err);
+        ++pr.mma_phase;
         w = __syncthreads_and(w) != 0;
         umma::fence_after_sync();
         return w;
@@ -176,49 +226,59 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
         umma::fence_after_sync();
     };
 
-    bool ok = mbar_wait(&sh.bar0, tma_phase & 1u, p.err);
-    ++tma_phase;
+    bool ok = mbar_wait(&sh.bar0, pr.tma_phase & 1u, p.err);
+    ++pr.tma_phase;
+    if (tid == 0) pr.tma_pending = false;
+    __syncthreads();   // gates in shared memory, the previous stores read out
     if (warp == 0) step_factors(lane, sh.s_g, sh.s_b, sh.s_lg, sh.s_gam, sh.s_kc, sh.s_beta, sh.s_bg);
     ok = __syncthreads_and(ok) != 0;
     if (ok) {
         if (tid == 0) {
             umma::fence_after_sync();
-            issue_kq(tmem, base, P1_KQ);
+            issue_kq(tmem, base, M.kq);
             umma::mma_commit(&sh.bar1);
         }
-        build_gq(sm, P1_KQ, P1_GQ, sh.s_gam, tid);
-        build_kt_bk(sm, P1_KQ, P1_KT, P1_BK, sh.s_kc, sh.s_bg, tid);
-        build_bv(sm, P1_V, P1_BV, sh.s_beta, tid);
+        build_gq(sm, M.kq, M.gq, sh.s_gam, tid);
+        build_kt_bk(sm, M.kq, M.kt, M.bk, sh.s_kc, sh.s_bg, tid);
+        build_bv(sm, M.v, M.bv, sh.s_beta, tid);
         ok = wait_mma();
     }
     if (ok) {
-        // A from K K^T (quads 0-1); P from Q K^T (quads 2-3) into the dead K/Q slot
+        // A from K K^T (quads 0-1); P from Q K^T (quads 2-3) into the dead KQ slot
         if (quad < 2) {
             build_a(lane_tmem + C_QK, As, sh.s_lg, sh.s_beta, row, half);
         } else {
             float qk[32];
             umma::tmem_ld32(lane_tmem + C_QK + half * 32, qk);
             umma::tmem_ld_wait();
-            p_tile(qk, sm, P1_P, sh.s_lg, row, half);
+            p_tile(qk, sm, M.kq, sh.s_lg, row, half);
         }
+        // the previous unit's stores have had this unit's builds to complete
+        if (tid == 0) publish_pending(pr);
         __syncthreads();
         invert_unit_lower(As, Ys, tid);
-        t_to_tf32(As, sm, P1_T, tid);
+        t_to_tf32(As, sm, M.t, tid);
         publish();
         if (tid == 0) {
-            issue_uw(tmem, base, P1_T, P1_BV, P1_BK);
+            issue_uw(tmem, base, M.t, M.bv, M.bk);
             umma::mma_commit(&sh.bar1);
         }
         ok = wait_mma();
     }
     if (ok) {
-        neg_w_tile(lane_tmem + C_W, sm, P1_NW, row, half);
+        // bK and A are free: fetch the next unit's tiles there (the next map's KQ and V)
+        if (tid == 0 && nc >= 0) {
+            unit_tiles(p, tm_k, tm_q, tm_v, sh, sm, prep_map(pr.parity ^ 1), nc, nb, nhv);
+            pr.tma_pending = true;
+        }
+        neg_w_tile(lane_tmem + C_W, sm, M.bv, row, half);
         float uv[32];
         umma::tmem_ld32(lane_tmem + C_D + half * 32, uv);
         umma::tmem_ld_wait();
+        const uint32_t ut = M.kq + kSlot;   // U^T: the KQ pair's second slot and the V slot
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
-            *reinterpret_cast<float4 *>(sm + P1_UT + ut_off(row, half * 8 + jj)) =
+            *reinterpret_cast<float4 *>(sm + ut + ut_off(row, half * 8 + jj)) =
                 make_float4(uv[4 * jj], uv[4 * jj + 1], uv[4 * jj + 2], uv[4 * jj + 3]);
         fence_proxy_async_smem();
         umma::fence_before_sync();
@@ -227,24 +287,20 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
             const size_t bi = blob_index(p, b, hv, c);
             uint8_t *blob = p.blobs + bi * kBlobBytes;
             *reinterpret_cast<float *>(blob + B_META) = sh.s_gam[kC - 1];
-            bulk_store(blob + B_GQ, sm + P1_GQ, 32768);
-            bulk_store(blob + B_NW, sm + P1_NW, 32768);
-            bulk_store(blob + B_UT, sm + P1_UT, 32768);
-            bulk_store(blob + B_KT, sm + P1_KT, 32768);
-            bulk_store(blob + B_P, sm + P1_P, 16384);
+            bulk_store(blob + B_GQ, sm + M.gq, 32768);
+            bulk_store(blob + B_NW, sm + M.bv, 32768);
+            bulk_store(blob + B_UT, sm + ut, 32768);
+            bulk_store(blob + B_KT, sm + M.kt, 32768);
+            bulk_store(blob + B_P, sm + M.kq, 16384);
             bulk_commit();
-            if (p.ready != nullptr) {
-                bulk_wait_all();                       // the writes are done, not only read out
-                __threadfence();                       // ... and so is the meta store
-                publish_ready(p.ready + bi);
-            } else {
-                bulk_wait_read();
-            }
+            if (p.ready != nullptr) pr.pending_flag = p.ready + bi;
         }
     } else if (tid == 0) {
-        // a wait gave up: give in-flight MMAs a bounded chance to drain
-        mbar_wait(&sh.bar1, mma_phase & 1u, nullptr);
+        // a wait gave up: give in-flight MMAs and copies a bounded chance to drain
+        mbar_wait(&sh.bar1, pr.mma_phase & 1u, nullptr);
+        if (pr.tma_pending) mbar_wait(&sh.bar0, pr.tma_phase & 1u, nullptr);
     }
+    pr.parity ^= 1;
     umma::fence_before_sync();
     __syncthreads();
     return ok;
@@ -382,7 +438,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         umma::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            tma_store_4d(tm_y, 0, hv, t0, b, sm + P2_YST);
+            store_chunk_y(tm_y, p.Dv, hv, t0, b, sm + P2_YST);
             bulk_commit();
         }
         if (tid < kC) sh.s_m[st ^ 1][tid] = pf_m;
@@ -443,8 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
     uint32_t base;
     uint8_t *sm = aligned_base(smem_raw, base);
     const uint32_t tmem = cta_setup(sh, 256);
-    uint32_t tma_phase = 0, mma_phase = 0;
-    prep_unit(p, &tm_k, &tm_q, &tm_v, sh, sm, base, tmem, blockIdx.x, blockIdx.z, blockIdx.y, tma_phase, mma_phase);
+    Producer pr;
+    const int c = blockIdx.x, b = blockIdx.z, hv = blockIdx.y;
+    if (unit_gates(p, c, b, hv, pr.gg, pr.bb)) {
+        if (threadIdx.x == 0) unit_tiles(p, &tm_k, &tm_q, &tm_v, sh, sm, prep_map(0), c, b, hv);
+        prep_unit(p, &tm_k, &tm_q, &tm_v, sh, sm, base, tmem, pr, c, b, hv, -1, 0, 0);
+        if (threadIdx.x == 0) bulk_wait_read();   // the stores have read shared memory
+    }
     cta_teardown(tmem, 256);
 }
 
@@ -480,14 +541,40 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_overlap_kernel(const __grid
         const int b = p.order != nullptr ? p.order[slot] : slot;
         state_head(p, &tm_y, sh, sm, base, tmem, b, hv);
     } else {
+        // producer: units u = (chunk u / n_heads, head u % n_heads) in steps of
+        // the producer count; wholly masked chunks are passed over
         const int n_prep = (int)gridDim.x - n_heads;
         const long n_units = (long)p.nchunks * n_heads;
-        uint32_t tma_phase = 0, mma_phase = 0;
-        for (long u = (long)blockIdx.x - n_heads; u < n_units; u += n_prep) {
-            const int c = (int)(u / n_heads), h = (int)(u % n_heads);
-            if (!prep_unit(p, &tm_k, &tm_q, &tm_v, sh, sm, base, tmem, c, h / p.Hv, h % p.Hv, tma_phase,
-                           mma_phase))
+        Producer pr;
+        float ng = 1.0f, nb = 0.0f;
+        // the first unit of `from` or after it that holds a valid step, its gates in (ng, nb)
+        auto next_active = [&](long from) {
+            long v = from;
+            for (; v < n_units; v += n_prep) {
+                const int h = (int)(v % n_heads);
+                if (unit_gates(p, (int)(v / n_heads), h / p.Hv, h % p.Hv, ng, nb)) break;
+            }
+            return v;
+        };
+        long u = next_active((long)blockIdx.x - n_heads);
+        if (u < n_units && threadIdx.x == 0) {
+            const int h = (int)(u % n_heads);
+            unit_tiles(p, &tm_k, &tm_q, &tm_v, sh, sm, prep_map(0), (int)(u / n_heads), h / p.Hv, h % p.Hv);
+        }
+        while (u < n_units) {
+            pr.gg = ng;
+            pr.bb = nb;
+            const long un = next_active(u + n_prep);
+            const int h = (int)(u % n_heads), hn = (int)(un % n_heads);
+            const bool more = un < n_units;
+            if (!prep_unit(p, &tm_k, &tm_q, &tm_v, sh, sm, base, tmem, pr, (int)(u / n_heads), h / p.Hv, h % p.Hv,
+                           more ? (int)(un / n_heads) : -1, more ? hn / p.Hv : 0, more ? hn % p.Hv : 0))
                 break;
+            u = un;
+        }
+        if (threadIdx.x == 0) {
+            publish_pending(pr);   // the last unit's image
+            bulk_wait_read();
         }
     }
     cta_teardown(tmem, cols);
