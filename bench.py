@@ -810,6 +810,11 @@ def main():
                     help="comma-separated sections to run after the headline decode")
     ap.add_argument("--backward-workloads", default="prefill_t8192,prefill_ragged",
                     help="workloads of the backward section (a subset keeps an ncu capture small)")
+    ap.add_argument("--prefill-workloads", default="prefill_t8192,prefill_ragged",
+                    help="workloads of the prefill section (a subset keeps an ncu capture small)")
+    ap.add_argument("--prefill-t", type=int, default=0,
+                    help="run the prefill section at this T instead of the workload's (profiling captures of a "
+                         "small case only; the benchmark figures use the workloads' own T)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
@@ -889,11 +894,16 @@ def main():
             prefill_vec["cpu_baseline"] = oracle_prefill_rate(wl.WORKLOADS["prefill_t8192"], vec=True,
                                                               budget_s=args.cpu_budget_s / 2)
     if "prefill" in parts:
-        for name in ("prefill_t8192", "prefill_ragged"):
+        for name in args.prefill_workloads.split(","):
             entries = []
+            w_p = wl.WORKLOADS[name]
+            if args.prefill_t > 0:
+                w_p = wl.Workload(w_p.name + "_t%d" % args.prefill_t, w_p.index, w_p.dims.with_(T=args.prefill_t),
+                                  w_p.steps, w_p.conv_state, w_p.state, w_p.ragged, min(w_p.len_lo, args.prefill_t),
+                                  min(w_p.len_hi, args.prefill_t))
             for chunk in (0, 64):
                 try:
-                    entries.append(bench_prefill(gdn, wl.WORKLOADS[name], dev, 3, chunk, peaks))
+                    entries.append(bench_prefill(gdn, w_p, dev, 3, chunk, peaks))
                 except gdn.GdnError as e:
                     if e.status != gdn.GDN_ERR_UNSUPPORTED:
                         raise
@@ -901,7 +911,7 @@ def main():
             if rank == 0 and not args.no_cpu:
                 # the oracle on a bounded sample of the same workload, once per
                 # workload: the same figure stands beside both forms
-                cb = oracle_prefill_rate(wl.WORKLOADS[name], budget_s=args.cpu_budget_s)
+                cb = oracle_prefill_rate(w_p, budget_s=args.cpu_budget_s)
                 for e_ in entries:
                     e_["cpu_baseline"] = cb
             prefill.extend(entries)

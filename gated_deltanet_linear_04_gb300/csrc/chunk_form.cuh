@@ -359,31 +359,28 @@ __device__ __forceinline__ void merge_level(float *As, float *Ys, int tid) {
     constexpr int NT = (32 / S) * S * G4;
     const int pi = tid / (S * G4), rem = tid % (S * G4), r = rem / G4, c = (rem % G4) * 4, q0 = pi * 2 * S;
     if (tid < NT) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // packed two-wide FMAs: each half rounds like fmaf
+        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < S; ++m) {
             const float a = As[aidx(q0 + S + r, q0 + m)];
             const float4 t = ld4(As + aidx(q0 + m, q0 + c));
-            acc.x = fmaf(a, t.x, acc.x);
-            acc.y = fmaf(a, t.y, acc.y);
-            acc.z = fmaf(a, t.z, acc.z);
-            acc.w = fmaf(a, t.w, acc.w);
+            lo = __ffma2_rn(make_float2(a, a), make_float2(t.x, t.y), lo);
+            hi = __ffma2_rn(make_float2(a, a), make_float2(t.z, t.w), hi);
         }
-        st4(Ys + (pi * S + r) * S + c, acc);
+        st4(Ys + (pi * S + r) * S + c, make_float4(lo.x, lo.y, hi.x, hi.y));
     }
     __syncthreads();
     if (tid < NT) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < S; ++m) {
             const float t = As[aidx(q0 + S + r, q0 + S + m)];
             const float4 yv = ld4(Ys + (pi * S + m) * S + c);
-            acc.x = fmaf(t, yv.x, acc.x);
-            acc.y = fmaf(t, yv.y, acc.y);
-            acc.z = fmaf(t, yv.z, acc.z);
-            acc.w = fmaf(t, yv.w, acc.w);
+            lo = __ffma2_rn(make_float2(t, t), make_float2(yv.x, yv.y), lo);
+            hi = __ffma2_rn(make_float2(t, t), make_float2(yv.z, yv.w), hi);
         }
-        st4(As + aidx(q0 + S + r, q0 + c), make_float4(-acc.x, -acc.y, -acc.z, -acc.w));
+        st4(As + aidx(q0 + S + r, q0 + c), make_float4(-lo.x, -lo.y, -hi.x, -hi.y));
     }
     __syncthreads();
 }
@@ -449,18 +446,22 @@ __device__ __forceinline__ void dt_tile(const float (&dv)[32], uint8_t *sm, uint
         st_tf32x4(sm, dt_off + half * kSlot + umma::sw128(row, j * 4), dv[j], dv[j + 1], dv[j + 2], dv[j + 3]);
 }
 
-// S <- gl S in TMEM (the products that read S0 must have completed)
+// S <- gl S in TMEM (the products that read S0 must have completed); both
+// halves of the thread's 64 columns are loaded before one wait
 __device__ __forceinline__ void decay_state(uint32_t s_tmem, float gl, int half) {
+    float sa[32], sb[32];
+    umma::tmem_ld32(s_tmem + half * 64, sa);
+    umma::tmem_ld32(s_tmem + half * 64 + 32, sb);
+    umma::tmem_ld_wait();
 #pragma unroll
-    for (int cpart = 0; cpart < 2; ++cpart) {
-        float sv[32];
-        const uint32_t col = half * 64 + cpart * 32;
-        umma::tmem_ld32(s_tmem + col, sv);
-        umma::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] *= gl;
-        umma::tmem_st32(s_tmem + col, sv);
+    for (int j = 0; j < 32; j += 2) {
+        const float2 a2 = __fmul2_rn(make_float2(sa[j], sa[j + 1]), make_float2(gl, gl));
+        const float2 b2 = __fmul2_rn(make_float2(sb[j], sb[j + 1]), make_float2(gl, gl));
+        sa[j] = a2.x; sa[j + 1] = a2.y;
+        sb[j] = b2.x; sb[j + 1] = b2.y;
     }
+    umma::tmem_st32(s_tmem + half * 64, sa);
+    umma::tmem_st32(s_tmem + half * 64 + 32, sb);
 }
 
 // ---------------------------------------------------------------------------
@@ -516,17 +517,27 @@ __device__ __forceinline__ void issue_dt_products(uint32_t tmem, uint32_t base, 
 }
 
 // y of the chunk from the Y accumulator into a bf16 staging tile [64 steps][128 dv]
-// (masked steps are written as zeros)
+// (masked steps are written as zeros).  Thread `row` holds one dv for 32
+// steps; the lanes of a pair (dv even, dv + 1) swap one value per two steps,
+// so that each writes two adjacent dv of one step as one 32-bit word.
 __device__ __forceinline__ void stage_y(uint32_t y_tmem, uint8_t *sm, uint32_t yst_off, const int *s_m, int row,
                                         int half) {
     float yv[32];
     umma::tmem_ld32(y_tmem + half * 32, yv);
+    const unsigned valid = __ballot_sync(0xffffffffu, s_m[half * 32 + (threadIdx.x & 31)] != 0);
     umma::tmem_ld_wait();
-    uint16_t *Yst = reinterpret_cast<uint16_t *>(sm + yst_off);
+    uint32_t *Yst = reinterpret_cast<uint32_t *>(sm + yst_off);
+    const bool odd = (row & 1) != 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int r = half * 32 + j;
-        Yst[r * kD + row] = s_m[r] ? f32_to_bf16(yv[j]) : (uint16_t)0;
+    for (int j = 0; j < 32; j += 2) {
+        // even lanes keep step j and receive the partner's; odd lanes step j + 1
+        const float mine = odd ? yv[j + 1] : yv[j];
+        const float other = __shfl_xor_sync(0xffffffffu, odd ? yv[j] : yv[j + 1], 1);
+        const int r = half * 32 + j + (odd ? 1 : 0);
+        const bool m = (valid >> (j + (odd ? 1 : 0))) & 1u;
+        const float lo = odd ? other : mine, hi = odd ? mine : other;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(m ? lo : 0.0f, m ? hi : 0.0f);
+        Yst[(r * kD + (row & ~1)) >> 1] = *reinterpret_cast<const uint32_t *>(&h);
     }
 }
 

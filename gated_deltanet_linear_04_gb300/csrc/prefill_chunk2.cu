@@ -28,8 +28,14 @@
 //
 // Workspace blob per (b, hv, chunk), laid out like pass 2's shared memory so
 // that one 1-D bulk copy brings in each group:
-//   group A  [GQ 32 KiB][-W 32 KiB][U^T 32 KiB][meta 1 KiB: 2^lg_63]
-//   group B  [Kc^T 32 KiB][P 16 KiB]
+//   group A  [-W | gQ 64 KiB][U^T 32 KiB][meta 1 KiB: 2^lg_63]
+//   group B  [P | Kc^T 48 KiB]
+// -W and gQ are interleaved by K-tile (-W's 64 rows, then gQ's 64 rows, of
+// each 32-column tile) so that together they are one N = 128 B operand, and
+// P and Kc^T likewise (P's 64 rows, then Kc^T's 128) one N = 192 operand:
+// pass 2 runs the two products that read S0 as one MMA per K step into the
+// adjacent D and Y accumulators, and the two that read D^T as one into the
+// adjacent Y and S accumulators.
 // U^T is plain f32 [128 dv][64 steps] with each row's 16-byte groups permuted
 // (group j stored at j ^ (dv % 16)) so that a warp's row-per-thread accesses
 // spread over the banks.  After the blobs come the ready flags (one int per
@@ -46,9 +52,9 @@ namespace {
 using namespace chunkform;
 
 // blob layout
-constexpr uint32_t B_GQ = 0, B_NW = 32768, B_UT = 65536, B_META = 98304;
+constexpr uint32_t B_NWGQ = 0, B_UT = 65536, B_META = 98304;   // [-W_kt 8 KiB | gQ_kt 8 KiB] x 4
 constexpr uint32_t kGroupA = 98304 + 1024;
-constexpr uint32_t B_KT = kGroupA, B_P = kGroupA + 32768;
+constexpr uint32_t B_PKT = kGroupA;                            // [P_kt 8 KiB | Kc^T_kt 16 KiB] x 2
 constexpr uint32_t kGroupB = 32768 + 16384;
 constexpr size_t kBlobBytes = (size_t)kGroupA + kGroupB;
 
@@ -74,8 +80,8 @@ __device__ __forceinline__ PrepMap prep_map(int parity) {
 constexpr uint32_t kP1Smem = 13 * kSlot + 1024;
 
 // pass 2 shared memory: group A and group B images, then D^T and y staging
-constexpr uint32_t P2_GQ = B_GQ, P2_NW = B_NW, P2_UT = B_UT, P2_META = B_META;
-constexpr uint32_t P2_KT = kGroupA, P2_P = kGroupA + 32768;
+constexpr uint32_t P2_NWGQ = B_NWGQ, P2_UT = B_UT, P2_META = B_META;
+constexpr uint32_t P2_PKT = B_PKT;
 constexpr uint32_t P2_DT = kGroupA + kGroupB;            // 32 KiB
 constexpr uint32_t P2_YST = P2_DT + 32768;               // 16 KiB
 constexpr uint32_t kP2Smem = P2_YST + 16384 + 1024;
@@ -287,11 +293,17 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
             const size_t bi = blob_index(p, b, hv, c);
             uint8_t *blob = p.blobs + bi * kBlobBytes;
             *reinterpret_cast<float *>(blob + B_META) = sh.s_gam[kC - 1];
-            bulk_store(blob + B_GQ, sm + M.gq, 32768);
-            bulk_store(blob + B_NW, sm + M.bv, 32768);
+#pragma unroll
+            for (int kt = 0; kt < 4; ++kt) {
+                bulk_store(blob + B_NWGQ + kt * 16384, sm + M.bv + kt * 8192, 8192);
+                bulk_store(blob + B_NWGQ + kt * 16384 + 8192, sm + M.gq + kt * 8192, 8192);
+            }
             bulk_store(blob + B_UT, sm + ut, 32768);
-            bulk_store(blob + B_KT, sm + M.kt, 32768);
-            bulk_store(blob + B_P, sm + M.kq, 16384);
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                bulk_store(blob + B_PKT + kt * 24576, sm + M.kq + kt * 8192, 8192);
+                bulk_store(blob + B_PKT + kt * 24576 + 8192, sm + M.kt + kt * kSlot, 16384);
+            }
             bulk_commit();
             if (p.ready != nullptr) pr.pending_flag = p.ready + bi;
         }
@@ -307,6 +319,34 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
 }
 
 // ---------------------------------------------------------------------------
+// pass 2 TMEM columns: D | Y | S adjacent, so that
+//   [D^T | Y^T] = [U^T | 0] + S0 [-W ; gQ]^T        (N = 128, K = 128)
+//   [Y^T | S]  += D^T [P ; Kc^T]^T                    (N = 192, K = 64)
+// run as one MMA per K step each, S0 read from TMEM (tf32 by truncation).
+// Each accumulator sees its MMAs in the single pass's order, so the results
+// match it bit for bit (Y's zero start adds nothing).
+// ---------------------------------------------------------------------------
+constexpr uint32_t C2_D = 64, C2_Y = 128, C2_S = 192;
+
+__device__ __forceinline__ void issue_s0_merged(uint32_t tmem, uint32_t base) {
+    const uint32_t id = umma::idesc(128, 128, umma::kFmtTF32);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        umma::mma_tf32_tmem_a(tmem + C2_D, tmem + C2_S + 8 * k,
+                              umma::desc_sw128(base + P2_NWGQ + (k >> 2) * 16384 + (k & 3) * 32), id, true);
+}
+
+__device__ __forceinline__ void issue_dt_merged(uint32_t tmem, uint32_t base) {
+    const uint32_t id = umma::idesc(128, 192, umma::kFmtTF32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t kt = k >> 2, ko = (k & 3) * 32;
+        umma::mma_tf32(tmem + C2_Y, umma::desc_sw128(base + P2_DT + kt * kSlot + ko),
+                       umma::desc_sw128(base + P2_PKT + kt * 24576 + ko), id, true);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // pass 2: the chunk chain of head (b, hv), state products only.  The caller
 // has initialised sh.bar0-2 and allocated 512 TMEM columns.
 // ---------------------------------------------------------------------------
@@ -319,7 +359,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
     const uint32_t lane_tmem = tmem + ((uint32_t)(quad * 32) << 16);
 
     // initial state -> TMEM S (row = dv, columns = dk); half 0: dk 0-63, half 1: 64-127
-    state_to_tmem(p.state_in, lane_tmem + C_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
+    state_to_tmem(p.state_in, lane_tmem + C2_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
     (void)lane;
 
     int pf_m = 0;
@@ -337,7 +377,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
             const size_t bi = blob_index(p, b, hv, c);
             if (p.ready != nullptr && !flag_gave_up) flag_gave_up = !wait_ready(p.ready + bi, p.err);
             mbar_expect_tx(&sh.bar0, kGroupA);
-            bulk_load(sm + P2_GQ, p.blobs + bi * kBlobBytes, kGroupA, &sh.bar0);
+            bulk_load(sm + P2_NWGQ, p.blobs + bi * kBlobBytes, kGroupA, &sh.bar0);
             a_pending = true;
             a_parity = (uint32_t)(it & 1);
         }
@@ -346,7 +386,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         if (tid == 0) {
             // group B of chunk c is loaded after group A, whose flag covers the whole blob
             mbar_expect_tx(&sh.bar1, kGroupB);
-            bulk_load(sm + P2_KT, p.blobs + blob_index(p, b, hv, c) * kBlobBytes + kGroupA, kGroupB, &sh.bar1);
+            bulk_load(sm + P2_PKT, p.blobs + blob_index(p, b, hv, c) * kBlobBytes + kGroupA, kGroupB, &sh.bar1);
             b_pending = true;
             b_parity = (uint32_t)(it & 1);
         }
@@ -390,31 +430,35 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         const int cn = scan.next_active(c + 1);
         if (cn < nchunks) gather_mask(cn);
 
-        // U^T -> the D accumulator, which the S0 (-W)^T product then adds to
+        // U^T -> the D accumulator and zeros -> Y, which the S0 [-W ; gQ]^T
+        // product then adds to
         {
-            float r[32];
+            float r[32], z[32];
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
                 const float4 v = *reinterpret_cast<const float4 *>(sm + P2_UT + ut_off(row, half * 8 + jj));
                 r[4 * jj] = v.x; r[4 * jj + 1] = v.y; r[4 * jj + 2] = v.z; r[4 * jj + 3] = v.w;
             }
-            umma::tmem_st32(lane_tmem + C_D + half * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = 0.0f;
+            umma::tmem_st32(lane_tmem + C2_D + half * 32, r);
+            umma::tmem_st32(lane_tmem + C2_Y + half * 32, z);
             umma::tmem_st_wait();
         }
         const float gl = *reinterpret_cast<const float *>(sm + P2_META);
         publish();
         if (tid == 0) {
-            issue_s0_products(tmem, base, P2_NW, P2_GQ);
+            issue_s0_merged(tmem, base);
             umma::mma_commit(&sh.bar2);
         }
         if (!wait_mma()) { ok = false; break; }
         // group A has been consumed: fetch the next chunk's
         if (cn < nchunks) load_a(cn, it + 1);
 
-        decay_state(lane_tmem + C_S, gl, half);
+        decay_state(lane_tmem + C2_S, gl, half);
         {
             float dv[32];
-            umma::tmem_ld32(lane_tmem + C_D + half * 32, dv);
+            umma::tmem_ld32(lane_tmem + C2_D + half * 32, dv);
             umma::tmem_ld_wait();
             dt_tile(dv, sm, P2_DT, row, half);
         }
@@ -424,7 +468,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         if (!ok) break;
         if (tid == 0) {
             umma::fence_after_sync();
-            issue_dt_products(tmem, base, P2_DT, P2_P, P2_KT);
+            issue_dt_merged(tmem, base);
             umma::mma_commit(&sh.bar2);
             bulk_wait_read();   // the previous chunk's y store has read the staging tile
         }
@@ -433,7 +477,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
 
         // y: the staged tile leaves by one TMA store (clipped at T), which
         // the next chunk's staging waits for
-        stage_y(lane_tmem + C_Y, sm, P2_YST, sh.s_m[st], row, half);
+        stage_y(lane_tmem + C2_Y, sm, P2_YST, sh.s_m[st], row, half);
         fence_proxy_async_smem();
         umma::fence_before_sync();
         __syncthreads();
@@ -448,7 +492,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
 
     if (tid == 0) bulk_wait_read();   // the last y store has read the staging tile
     if (__syncthreads_and(ok)) {
-        state_from_tmem(p.state_out, lane_tmem + C_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
+        state_from_tmem(p.state_out, lane_tmem + C2_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
     } else if (tid == 0) {
         // a wait gave up: give in-flight MMAs and copies a bounded chance to drain
         mbar_wait(&sh.bar2, mma_phase & 1u, nullptr);

@@ -152,12 +152,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) 
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Round an f32 to the nearest tf32 value (10 explicit mantissa bits, ties away
-// from zero), returned as f32 bits with the low 13 bits clear.
+// Round a finite f32 to the nearest tf32 value (10 explicit mantissa bits,
+// ties away from zero), returned as f32 bits with the low 13 bits clear: half
+// of the dropped bits' weight (bit 12) is added to the magnitude bits, which
+// carries into the kept bits exactly when the dropped part is at least half an
+// ulp, then the dropped bits are cleared.  Two integer operations at the
+// integer pipe's full rate.
 __device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 }  // namespace umma
