@@ -22,8 +22,8 @@
 //   Y^T += D^T P^T   tf32         -> Y columns
 //   S  += D^T Kc^T   tf32         -> S columns (S pre-scaled by 2^lg_63)
 // The state products read S straight from TMEM as their A operand (tf32 by
-// truncation); every other f32 operand is rounded to tf32 (cvt.rna) when it
-// is written to shared memory.
+// truncation); every other f32 operand is rounded to tf32 (to nearest, ties
+// away from zero: umma::to_tf32) when it is written to shared memory.
 //
 // Threads: 256 (8 warps).  Warp w reaches TMEM lanes [32 (w % 4), +32): its
 // thread `row` = 32 (w % 4) + lane is one accumulator row; `half` = w / 4

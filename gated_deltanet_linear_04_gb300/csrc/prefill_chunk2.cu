@@ -23,8 +23,11 @@
 //     first B*Hv CTAs run the state chains while the others produce the chunk
 //     images in chunk order; each image is published with a ready flag
 //     (bulk stores complete, proxy fence, release store) that the state CTA
-//     acquires before its bulk load.  Every wait is bounded and sets the
-//     device error word if it gives up.
+//     acquires before its bulk load.  A producer fetches its next unit's
+//     tiles while the current unit finishes, and publishes a unit once the
+//     next one has done its operand builds, so it never waits for its own
+//     stores to land.  Every wait is bounded and sets the device error word
+//     if it gives up.
 //
 // Workspace blob per (b, hv, chunk), laid out like pass 2's shared memory so
 // that one 1-D bulk copy brings in each group:
