@@ -298,6 +298,12 @@ struct Lanes {
 
 // One forward step of the lane's two rows from the staged chunk; returns u
 // per row.
+// The step loops below run on adjacent column pairs (j, j + 1 with j even:
+// the lane's columns come in runs of four) with the packed two-wide f32
+// instructions; each half rounds like the scalar instruction and the four
+// partial sums keep their order, so every value is the scalar loop's.
+__device__ __forceinline__ float2 pair(const float *x, int j) { return make_float2(x[j], x[j + 1]); }
+
 template <int DK>
 __device__ __forceinline__ void fwd_step(const BwdSmem<DK> &s, const Lanes<DK> &L, float (&S)[2][DK / 8], int tl,
                                          float (&u)[2]) {
@@ -305,14 +311,23 @@ __device__ __forceinline__ void fwd_step(const BwdSmem<DK> &s, const Lanes<DK> &
     const float gg = s.g[tl], bb = s.beta[tl];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        float kv4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float2 kv01 = make_float2(0.0f, 0.0f), kv23 = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int j = 0; j < CW; ++j) kv4[j & 3] = fmaf(S[i][j], s.k[tl][L.col(j)], kv4[j & 3]);
+        for (int j = 0; j < CW; j += 4) {
+            kv01 = __ffma2_rn(pair(S[i], j), pair(s.k[tl], L.col(j)), kv01);
+            kv23 = __ffma2_rn(pair(S[i], j + 2), pair(s.k[tl], L.col(j + 2)), kv23);
+        }
+        const float kv4[4] = {kv01.x, kv01.y, kv23.x, kv23.y};
         const float kv = gg * row_sum(sum4(kv4));
         u[i] = s.v[tl][L.rl[i]] - kv;
         const float dl = bb * u[i];
+        const float2 g2 = make_float2(gg, gg), dl2 = make_float2(dl, dl);
 #pragma unroll
-        for (int j = 0; j < CW; ++j) S[i][j] = fmaf(dl, s.k[tl][L.col(j)], gg * S[i][j]);
+        for (int j = 0; j < CW; j += 2) {
+            const float2 r = __ffma2_rn(dl2, pair(s.k[tl], L.col(j)), __fmul2_rn(g2, pair(S[i], j)));
+            S[i][j] = r.x;
+            S[i][j + 1] = r.y;
+        }
     }
 }
 
@@ -326,18 +341,25 @@ __device__ __forceinline__ void dS_step(const BwdSmem<DK> &s, const Lanes<DK> &L
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const float dyv = s.dy[tl][L.rl[i]];
-        float dd4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const float2 dy2 = make_float2(dyv, dyv);
+        float2 dd01 = make_float2(0.0f, 0.0f), dd23 = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int j = 0; j < CW; ++j) {
-            dS[i][j] = fmaf(dyv, s.q[tl][L.col(j)], dS[i][j]);
-            dd4[j & 3] = fmaf(dS[i][j], s.k[tl][L.col(j)], dd4[j & 3]);
+        for (int j = 0; j < CW; j += 4) {
+            const float2 a = __ffma2_rn(dy2, pair(s.q[tl], L.col(j)), pair(dS[i], j));
+            const float2 c = __ffma2_rn(dy2, pair(s.q[tl], L.col(j + 2)), pair(dS[i], j + 2));
+            dS[i][j] = a.x; dS[i][j + 1] = a.y; dS[i][j + 2] = c.x; dS[i][j + 3] = c.y;
+            dd01 = __ffma2_rn(a, pair(s.k[tl], L.col(j)), dd01);
+            dd23 = __ffma2_rn(c, pair(s.k[tl], L.col(j + 2)), dd23);
         }
+        const float dd4[4] = {dd01.x, dd01.y, dd23.x, dd23.y};
         const float dd = row_sum(sum4(dd4));
         const float du = bb * dd;
+        const float2 ndu2 = make_float2(-du, -du), g2 = make_float2(gg, gg);
 #pragma unroll
-        for (int j = 0; j < CW; ++j) {
-            dS[i][j] = fmaf(-du, s.k[tl][L.col(j)], dS[i][j]);
-            dS[i][j] *= gg;
+        for (int j = 0; j < CW; j += 2) {
+            const float2 r = __fmul2_rn(__ffma2_rn(ndu2, pair(s.k[tl], L.col(j)), pair(dS[i], j)), g2);
+            dS[i][j] = r.x;
+            dS[i][j + 1] = r.y;
         }
     }
 }

@@ -231,35 +231,34 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm) decode_kernel(const D
         float4 sa[NG];
 #pragma unroll
         for (int j = 0; j < NG; ++j) sa[j] = spa[j * LPR + cl];
-        float a0 = 0.0f, a1 = 0.0f;
+        // column pairs on the packed two-wide f32 instructions (each half
+        // rounds like the scalar one; the pair's halves are the two partial
+        // sums of the row's dot products)
+        float2 pa = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
             const float4 kk = k4[j * LPR + cl];
-            a0 = fmaf(sa[j].x, kk.x, a0);
-            a1 = fmaf(sa[j].y, kk.y, a1);
-            a0 = fmaf(sa[j].z, kk.z, a0);
-            a1 = fmaf(sa[j].w, kk.w, a1);
+            pa = __ffma2_rn(make_float2(sa[j].x, sa[j].y), make_float2(kk.x, kk.y), pa);
+            pa = __ffma2_rn(make_float2(sa[j].z, sa[j].w), make_float2(kk.z, kk.w), pa);
         }
-        float dka = a0 + a1;
+        float dka = pa.x + pa.y;
 #pragma unroll
         for (int o = LPR / 2; o > 0; o >>= 1) dka += __shfl_xor_sync(0xffffffffu, dka, o);
         const float da = beta * (v_s[ra] - g * dka);
-        a0 = a1 = 0.0f;
+        const float2 g2 = make_float2(g, g), da2 = make_float2(da, da);
+        pa = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int j = 0; j < NG; ++j) {
             const float4 kk = k4[j * LPR + cl];
-            sa[j].x = fmaf(da, kk.x, g * sa[j].x);
-            sa[j].y = fmaf(da, kk.y, g * sa[j].y);
-            sa[j].z = fmaf(da, kk.z, g * sa[j].z);
-            sa[j].w = fmaf(da, kk.w, g * sa[j].w);
+            const float2 lo = __ffma2_rn(da2, make_float2(kk.x, kk.y), __fmul2_rn(g2, make_float2(sa[j].x, sa[j].y)));
+            const float2 hi = __ffma2_rn(da2, make_float2(kk.z, kk.w), __fmul2_rn(g2, make_float2(sa[j].z, sa[j].w)));
+            sa[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
             spa[j * LPR + cl] = sa[j];
             const float4 qq = q4[j * LPR + cl];
-            a0 = fmaf(sa[j].x, qq.x, a0);
-            a1 = fmaf(sa[j].y, qq.y, a1);
-            a0 = fmaf(sa[j].z, qq.z, a0);
-            a1 = fmaf(sa[j].w, qq.w, a1);
+            pa = __ffma2_rn(lo, make_float2(qq.x, qq.y), pa);
+            pa = __ffma2_rn(hi, make_float2(qq.z, qq.w), pa);
         }
-        float dqa = a0 + a1;
+        float dqa = pa.x + pa.y;
 #pragma unroll
         for (int o = LPR / 2; o > 0; o >>= 1) dqa += __shfl_xor_sync(0xffffffffu, dqa, o);
         if (cl == 0) y_s[ra] = dqa;

@@ -259,21 +259,20 @@ __global__ void __launch_bounds__(kThreads, TM == 6 ? 3 : 4) window_kernel(const
             const float4 *k4 = reinterpret_cast<const float4 *>(k_s[t]);
             const float4 *q4 = reinterpret_cast<const float4 *>(q_s[t]);
             const float g = gb_s[t][0], beta = gb_s[t][1];
-            // S_{t-1} k, then S_t = g S_{t-1} + delta k^T, then y = S_t q
-            float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
+            // S_{t-1} k, then S_t = g S_{t-1} + delta k^T, then y = S_t q, on
+            // column pairs with the packed two-wide f32 instructions (each
+            // half rounds like the scalar one; the pair's halves are the two
+            // partial sums)
+            float2 pa = make_float2(0.0f, 0.0f), pb = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int j = 0; j < NG; ++j) {
                 const float4 kk = k4[j * LPR + cl];
-                a0 = fmaf(sa[j].x, kk.x, a0);
-                a1 = fmaf(sa[j].y, kk.y, a1);
-                a0 = fmaf(sa[j].z, kk.z, a0);
-                a1 = fmaf(sa[j].w, kk.w, a1);
-                b0 = fmaf(sb[j].x, kk.x, b0);
-                b1 = fmaf(sb[j].y, kk.y, b1);
-                b0 = fmaf(sb[j].z, kk.z, b0);
-                b1 = fmaf(sb[j].w, kk.w, b1);
+                pa = __ffma2_rn(make_float2(sa[j].x, sa[j].y), make_float2(kk.x, kk.y), pa);
+                pa = __ffma2_rn(make_float2(sa[j].z, sa[j].w), make_float2(kk.z, kk.w), pa);
+                pb = __ffma2_rn(make_float2(sb[j].x, sb[j].y), make_float2(kk.x, kk.y), pb);
+                pb = __ffma2_rn(make_float2(sb[j].z, sb[j].w), make_float2(kk.z, kk.w), pb);
             }
-            float dka = a0 + a1, dkb = b0 + b1;
+            float dka = pa.x + pa.y, dkb = pb.x + pb.y;
 #pragma unroll
             for (int o = LPR / 2; o > 0; o >>= 1) {
                 dka += __shfl_xor_sync(0xffffffffu, dka, o);
@@ -281,29 +280,24 @@ __global__ void __launch_bounds__(kThreads, TM == 6 ? 3 : 4) window_kernel(const
             }
             const float da = beta * (v_s[t][ra] - g * dka);
             const float db = beta * (v_s[t][rb] - g * dkb);
-            a0 = a1 = b0 = b1 = 0.0f;
+            const float2 g2 = make_float2(g, g), da2 = make_float2(da, da), db2 = make_float2(db, db);
+            pa = pb = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int j = 0; j < NG; ++j) {
                 const float4 kk = k4[j * LPR + cl];
-                sa[j].x = fmaf(da, kk.x, g * sa[j].x);
-                sa[j].y = fmaf(da, kk.y, g * sa[j].y);
-                sa[j].z = fmaf(da, kk.z, g * sa[j].z);
-                sa[j].w = fmaf(da, kk.w, g * sa[j].w);
-                sb[j].x = fmaf(db, kk.x, g * sb[j].x);
-                sb[j].y = fmaf(db, kk.y, g * sb[j].y);
-                sb[j].z = fmaf(db, kk.z, g * sb[j].z);
-                sb[j].w = fmaf(db, kk.w, g * sb[j].w);
                 const float4 qq = q4[j * LPR + cl];
-                a0 = fmaf(sa[j].x, qq.x, a0);
-                a1 = fmaf(sa[j].y, qq.y, a1);
-                a0 = fmaf(sa[j].z, qq.z, a0);
-                a1 = fmaf(sa[j].w, qq.w, a1);
-                b0 = fmaf(sb[j].x, qq.x, b0);
-                b1 = fmaf(sb[j].y, qq.y, b1);
-                b0 = fmaf(sb[j].z, qq.z, b0);
-                b1 = fmaf(sb[j].w, qq.w, b1);
+                float2 lo = __ffma2_rn(da2, make_float2(kk.x, kk.y), __fmul2_rn(g2, make_float2(sa[j].x, sa[j].y)));
+                float2 hi = __ffma2_rn(da2, make_float2(kk.z, kk.w), __fmul2_rn(g2, make_float2(sa[j].z, sa[j].w)));
+                sa[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                pa = __ffma2_rn(lo, make_float2(qq.x, qq.y), pa);
+                pa = __ffma2_rn(hi, make_float2(qq.z, qq.w), pa);
+                lo = __ffma2_rn(db2, make_float2(kk.x, kk.y), __fmul2_rn(g2, make_float2(sb[j].x, sb[j].y)));
+                hi = __ffma2_rn(db2, make_float2(kk.z, kk.w), __fmul2_rn(g2, make_float2(sb[j].z, sb[j].w)));
+                sb[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                pb = __ffma2_rn(lo, make_float2(qq.x, qq.y), pb);
+                pb = __ffma2_rn(hi, make_float2(qq.z, qq.w), pb);
             }
-            float dqa = a0 + a1, dqb = b0 + b1;
+            float dqa = pa.x + pa.y, dqb = pb.x + pb.y;
 #pragma unroll
             for (int o = LPR / 2; o > 0; o >>= 1) {
                 dqa += __shfl_xor_sync(0xffffffffu, dqa, o);
