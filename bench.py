@@ -70,6 +70,20 @@ def chunk_mma_flops(d: wl.Dims, C: int = 64) -> int:
     return 6 * C * C * d.Dk + 4 * C * C * d.Dv + 6 * C * d.Dv * d.Dk
 
 
+def backward_chunk_mma_flops(d: wl.Dims, C: int = 64) -> int:
+    """Tensor-core flops of one chunk of one head in the chunked backward,
+    2 flops per multiply-add: the chunked forward that keeps the chunk states
+    (chunk_mma_flops); the chain images (K K^T again 2C x C x Dk, Wb = T^T F K
+    C x C x Dk, dY^T P and its product with T Dv x C x C each, Cq = dY^T
+    gamma Q Dv x Dk x C); the chain (G Wb^T and the state-gradient update, Dv
+    x C x Dk each); gradients I ([K;Q] K^T, S0 [gamma K; gamma Q]^T Dv x 2C x
+    Dk, [dY; dZ] D^T 2C x C x Dv); gradients II (S0^T [dY; dZ]^T Dk x 2C x
+    Dv, G^T D^T Dk x C x Dv, K^T [dPM; H + H^T]^T Dk x 2C x C, Q^T dPM Dk x C
+    x C)."""
+    own = 16 * C * C * d.Dk + 8 * C * C * d.Dv + 16 * C * d.Dv * d.Dk
+    return chunk_mma_flops(d, C) + own
+
+
 def active_chunks(mask, T: int, B: int, C: int = 64) -> int:
     """Chunks of C steps holding at least one valid step (the chunked kernels
     skip the others)."""
@@ -494,10 +508,12 @@ def bench_decode_small(gdn, w: wl.Workload, dev, reps: int = 3) -> dict:
             "gbs_graph_l2_resident": round(by / (us_g / 1e6) / 1e9, 1)}
 
 
-def bench_backward(gdn, w: wl.Workload, dev, iters: int = 3) -> dict:
+def bench_backward(gdn, w: wl.Workload, dev, peaks, chunk: int = 0, iters: int = 3) -> dict:
     """The backward pass of the recurrence over one workload call (gradients of
     y and of the final state with respect to q, k, v, g, beta and the initial
-    state), from device-generated inputs of the workload's shapes."""
+    state), from device-generated inputs of the workload's shapes; chunk = 0
+    the sequential form, 64 the chunked form on the tensor cores (its roofline:
+    the MMA flops of the whole call, forward included, against the tf32 rate)."""
     d = w.dims
     gen = torch.Generator(device=dev)
     gen.manual_seed(5000 + w.index)
@@ -519,11 +535,13 @@ def bench_backward(gdn, w: wl.Workload, dev, iters: int = 3) -> dict:
     outs = [torch.empty((d.B, d.T, d.Hk, d.Dk), device=dev), torch.empty((d.B, d.T, d.Hk, d.Dk), device=dev),
             torch.empty((d.B, d.T, d.Hv, d.Dv), device=dev), torch.empty((d.B, d.T, d.Hv), device=dev),
             torch.empty((d.B, d.T, d.Hv), device=dev), torch.empty((d.B, d.Hv, d.Dv, d.Dk), device=dev)]
-    ws = torch.empty(gdn.gdn_prefill_backward_workspace_size(d), dtype=torch.uint8, device=dev)
+    size_fn = gdn.gdn_prefill_backward_chunked_workspace_size if chunk else gdn.gdn_prefill_backward_workspace_size
+    call = gdn.gdn_prefill_backward_chunked if chunk else gdn.gdn_prefill_backward
+    ws = torch.empty(size_fn(d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def once():
-        gdn.gdn_prefill_backward(d, q, k, v, g, beta, s0, mask, dy, None, *outs, ws, stream)
+        call(d, q, k, v, g, beta, s0, mask, dy, None, *outs, ws, stream)
 
     once()
     torch.cuda.synchronize()
@@ -536,8 +554,21 @@ def bench_backward(gdn, w: wl.Workload, dev, iters: int = 3) -> dict:
     if gdn.gdn_device_status() != gdn.GDN_OK:
         raise RuntimeError("device error word set during the backward benchmark")
     ms = e0.elapsed_time(e1) / iters
-    return {"workload": w.name, "ms": round(ms, 4), "tokens": n_valid, "tokens_per_s": round(n_valid / (ms / 1e3), 1),
-            "workspace_mb": round(ws.numel() / 2 ** 20, 1)}
+    res = {"workload": w.name, "chunk": chunk, "ms": round(ms, 4), "tokens": n_valid,
+           "tokens_per_s": round(n_valid / (ms / 1e3), 1), "workspace_mb": round(ws.numel() / 2 ** 20, 1)}
+    if chunk:
+        n_ch = active_chunks(mask, d.T, d.B) * d.Hv
+        fl = backward_chunk_mma_flops(d) * n_ch
+        tflops = fl / (ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"] * TF32_PER_BF16
+        res["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": round(peak, 1),
+                           "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                           "algorithmic_flops": fl, "units": n_ch, "unit_name": "chunk of 64 steps x head",
+                           "flops_per_unit": backward_chunk_mma_flops(d),
+                           "kernel": "the whole chunked backward call (forward with chunk records, chain images, "
+                                     "reverse chain, two gradient passes)",
+                           "peak_source": peaks["source"] + " bf16 x nominal tf32/bf16 (1.1/2.25)"}
+    return res
 
 
 def bench_decode_gated(gdn, w: wl.Workload, dev, iters: int = 200) -> dict:
@@ -910,7 +941,8 @@ def main():
         decode_gated = bench_decode_gated(gdn, w, dev)
     backward = None
     if "backward" in parts:
-        backward = [bench_backward(gdn, wl.WORKLOADS[name], dev) for name in args.backward_workloads.split(",")]
+        backward = [bench_backward(gdn, wl.WORKLOADS[name], dev, peaks, chunk)
+                    for name in args.backward_workloads.split(",") for chunk in (0, 64)]
     prefill_vec = None
     if "prefill_vec" in parts:
         prefill_vec = bench_prefill_vec(gdn, wl.WORKLOADS["prefill_t8192"], dev, 3, peaks)

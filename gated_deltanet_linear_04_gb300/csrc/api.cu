@@ -490,6 +490,47 @@ gdn_status gdn_selftest_timeout(gdn_stream stream) {
     return GDN_OK;
 }
 
+namespace gdn {
+
+// Shared validation and dispatch of the two backward entry points.
+gdn_status backward_impl(bool chunked, const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
+                         const uint16_t *v, const float *g, const float *beta, const float *state_in,
+                         const uint8_t *mask, const uint16_t *dy, const float *dstate_out, float *dq, float *dk,
+                         float *dv, float *dg, float *dbeta, float *dstate_in, void *workspace, size_t ws_bytes,
+                         gdn_stream stream) {
+    Sizes s;
+    gdn_status st = check_dims(dims, &s);
+    if (st != GDN_OK) return st;
+    if (chunked && (s.Dk != 128 || s.Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    const size_t BT = (size_t)s.B * s.T;
+    const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
+    if (!ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT) || !ok_ptr(g, BT) || !ok_ptr(beta, BT) ||
+        !ok_ptr(state_in, 0) || !ok_ptr(mask, 0) || !ok_ptr(dy, BT) || !ok_ptr(dstate_out, 0) || !ok_ptr(dq, BT) ||
+        !ok_ptr(dk, BT) || !ok_ptr(dv, BT) || !ok_ptr(dg, BT) || !ok_ptr(dbeta, BT) || !ok_ptr(dstate_in, nstate))
+        return GDN_ERR_INVALID_ARG;
+    if (s.B == 0) return GDN_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (s.T == 0) {
+        // no steps: the initial state's gradient is that of the final state
+        if (dstate_out == nullptr) return from_cuda(cudaMemsetAsync(dstate_in, 0, nstate * sizeof(float), cs));
+        if (dstate_out == dstate_in) return GDN_OK;
+        return from_cuda(
+            cudaMemcpyAsync(dstate_in, dstate_out, nstate * sizeof(float), cudaMemcpyDeviceToDevice, cs));
+    }
+    const size_t need = chunked ? backward_chunked_workspace(s) : backward_workspace(s);
+    if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return GDN_ERR_INVALID_ARG;
+    if (chunked) {
+        unsigned *err = error_word();
+        if (err == nullptr) return GDN_ERR_CUDA;
+        return from_cuda(launch_backward_chunked(s, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv,
+                                                 dg, dbeta, dstate_in, workspace, err, cs));
+    }
+    return from_cuda(launch_backward(s, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta,
+                                     dstate_in, workspace, cs));
+}
+
+}  // namespace gdn
+
 size_t gdn_prefill_backward_workspace_size(const gdn_dims *dims) {
     gdn::Sizes s;
     if (gdn::check_dims(dims, &s) != GDN_OK) return 0;
@@ -501,30 +542,24 @@ gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q, const u
                                 const uint16_t *dy, const float *dstate_out, float *dq, float *dk, float *dv,
                                 float *dg, float *dbeta, float *dstate_in, void *workspace, size_t ws_bytes,
                                 gdn_stream stream) {
+    return gdn::backward_impl(false, dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta,
+                              dstate_in, workspace, ws_bytes, stream);
+}
+
+size_t gdn_prefill_backward_chunked_workspace_size(const gdn_dims *dims) {
     gdn::Sizes s;
-    gdn_status st = gdn::check_dims(dims, &s);
-    if (st != GDN_OK) return st;
-    const size_t BT = (size_t)s.B * s.T;
-    const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
-    if (!gdn::ok_ptr(q, BT) || !gdn::ok_ptr(k, BT) || !gdn::ok_ptr(v, BT) || !gdn::ok_ptr(g, BT) ||
-        !gdn::ok_ptr(beta, BT) || !gdn::ok_ptr(state_in, 0) || !gdn::ok_ptr(mask, 0) || !gdn::ok_ptr(dy, BT) ||
-        !gdn::ok_ptr(dstate_out, 0) || !gdn::ok_ptr(dq, BT) || !gdn::ok_ptr(dk, BT) || !gdn::ok_ptr(dv, BT) ||
-        !gdn::ok_ptr(dg, BT) || !gdn::ok_ptr(dbeta, BT) || !gdn::ok_ptr(dstate_in, nstate))
-        return GDN_ERR_INVALID_ARG;
-    if (s.B == 0) return GDN_OK;
-    cudaStream_t cs = (cudaStream_t)stream;
-    if (s.T == 0) {
-        // no steps: the initial state's gradient is that of the final state
-        if (dstate_out == nullptr)
-            return gdn::from_cuda(cudaMemsetAsync(dstate_in, 0, nstate * sizeof(float), cs));
-        if (dstate_out == dstate_in) return GDN_OK;
-        return gdn::from_cuda(
-            cudaMemcpyAsync(dstate_in, dstate_out, nstate * sizeof(float), cudaMemcpyDeviceToDevice, cs));
-    }
-    if (workspace == nullptr || ws_bytes < gdn::backward_workspace(s) || !gdn::aligned16(workspace))
-        return GDN_ERR_INVALID_ARG;
-    return gdn::from_cuda(gdn::launch_backward(s, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg,
-                                               dbeta, dstate_in, workspace, cs));
+    if (gdn::check_dims(dims, &s) != GDN_OK || s.Dk != 128 || s.Dv != 128) return 0;
+    return gdn::backward_chunked_workspace(s);
+}
+
+gdn_status gdn_prefill_backward_chunked(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
+                                        const uint16_t *v, const float *g, const float *beta,
+                                        const float *state_in, const uint8_t *mask, const uint16_t *dy,
+                                        const float *dstate_out, float *dq, float *dk, float *dv, float *dg,
+                                        float *dbeta, float *dstate_in, void *workspace, size_t ws_bytes,
+                                        gdn_stream stream) {
+    return gdn::backward_impl(true, dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta,
+                              dstate_in, workspace, ws_bytes, stream);
 }
 
 gdn_status gdn_rmsnorm_gated(const gdn_dims *dims, const uint16_t *y, const uint16_t *z, const float *norm_w,

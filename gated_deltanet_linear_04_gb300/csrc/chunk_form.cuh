@@ -169,6 +169,7 @@ __device__ __forceinline__ void state_to_tmem(const float *state_in, uint32_t s_
 
 __device__ __forceinline__ void state_from_tmem(float *state_out, uint32_t s_tmem, int b, int hv, int Hv, int Dk,
                                                 int Dv, int row, int half) {
+    if (state_out == nullptr) return;
     const size_t off = (((size_t)b * Hv + hv) * Dv + row) * Dk;
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
@@ -446,13 +447,52 @@ __device__ __forceinline__ void dt_tile(const float (&dv)[32], uint8_t *sm, uint
         st_tf32x4(sm, dt_off + half * kSlot + umma::sw128(row, j * 4), dv[j], dv[j + 1], dv[j + 2], dv[j + 3]);
 }
 
+// ---------------------------------------------------------------------------
+// per-chunk records for the chunked backward (global memory, f32), in the
+// order the 256 threads of a chunk CTA hold them: thread (row, half) keeps
+// the 64 columns [64 half, +64) of TMEM lane `row` of a [128][128] matrix
+// (float4 j of them at float4 index (16 half + j) 128 + row), or the 32
+// columns [32 half, +32) of a [128][64] one (float4 index (8 half + j) 128 +
+// row), so that a warp touches 512 contiguous bytes per access.
+// ---------------------------------------------------------------------------
+constexpr size_t kRec128 = 128 * 128, kRec64 = 128 * 64;   // floats per record
+
+__device__ __forceinline__ float4 *rec128_at(float *rec, int row, int half, int j) {
+    return reinterpret_cast<float4 *>(rec) + ((half * 16 + j) * 128 + row);
+}
+__device__ __forceinline__ const float4 *rec128_at(const float *rec, int row, int half, int j) {
+    return reinterpret_cast<const float4 *>(rec) + ((half * 16 + j) * 128 + row);
+}
+__device__ __forceinline__ float4 *rec64_at(float *rec, int row, int half, int j) {
+    return reinterpret_cast<float4 *>(rec) + ((half * 8 + j) * 128 + row);
+}
+__device__ __forceinline__ const float4 *rec64_at(const float *rec, int row, int half, int j) {
+    return reinterpret_cast<const float4 *>(rec) + ((half * 8 + j) * 128 + row);
+}
+
+// a [128][64] record row held in registers (32 columns of this thread)
+__device__ __forceinline__ void store_rec64(float *rec, int row, int half, const float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *rec64_at(rec, row, half, j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
 // S <- gl S in TMEM (the products that read S0 must have completed); both
-// halves of the thread's 64 columns are loaded before one wait
-__device__ __forceinline__ void decay_state(uint32_t s_tmem, float gl, int half) {
+// halves of the thread's 64 columns are loaded before one wait.  With `rec`,
+// S before the decay (the chunk's start state) is also stored as a record.
+__device__ __forceinline__ void decay_state(uint32_t s_tmem, float gl, int half, float *rec = nullptr,
+                                            int row = 0) {
     float sa[32], sb[32];
     umma::tmem_ld32(s_tmem + half * 64, sa);
     umma::tmem_ld32(s_tmem + half * 64 + 32, sb);
     umma::tmem_ld_wait();
+    if (rec != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            *rec128_at(rec, row, half, j) = make_float4(sa[4 * j], sa[4 * j + 1], sa[4 * j + 2], sa[4 * j + 3]);
+            *rec128_at(rec, row, half, 8 + j) = make_float4(sb[4 * j], sb[4 * j + 1], sb[4 * j + 2], sb[4 * j + 3]);
+        }
+    }
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         const float2 a2 = __fmul2_rn(make_float2(sa[j], sa[j + 1]), make_float2(gl, gl));

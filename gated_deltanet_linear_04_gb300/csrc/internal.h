@@ -98,7 +98,8 @@ cudaError_t launch_prefill_seq_vec(const Sizes &s, const uint16_t *q, const uint
 cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                    const float *g, const float *beta, const float *state_in, float *state_out,
                                    const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
-                                   const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st);
+                                   const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st,
+                                   float *rec_s = nullptr, float *rec_d = nullptr);
 
 // Failure-path self-test (selftest.cu): a kernel whose bounded wait runs out.
 cudaError_t launch_selftest_timeout(unsigned *err, cudaStream_t st);
@@ -120,6 +121,18 @@ bool prefill_two_pass_pays(const Sizes &s);
 cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                     const float *g, const float *beta, const float *state_in, float *state_out,
                                     const uint8_t *mask, const int *order, uint16_t *y, void *blobs,
-                                    unsigned *err, cudaStream_t st);
+                                    unsigned *err, cudaStream_t st, float *rec_s = nullptr,
+                                    float *rec_d = nullptr);
+
+// Chunked backward (backward_chunk.cu, Dk = Dv = 128): workspace bytes and the
+// launch (outputs zeroed by the launch, then written or accumulated).  The
+// forward's records (rec_s, rec_d above) are taken by the chunked forward
+// kernels on the way.
+size_t backward_chunked_workspace(const Sizes &s);
+cudaError_t launch_backward_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                    const float *g, const float *beta, const float *state_in, const uint8_t *mask,
+                                    const uint16_t *dy, const float *dstate_out, float *dq, float *dk, float *dv,
+                                    float *dg, float *dbeta, float *dstate_in, void *ws, unsigned *err,
+                                    cudaStream_t st);
 
 }  // namespace gdn

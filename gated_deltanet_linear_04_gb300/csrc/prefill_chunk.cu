@@ -69,9 +69,13 @@ struct ChunkParams {
     float norm_eps;
     unsigned *err;
     int B, T, Hk, Hv, Dk, Dv;
+    // optional records for the chunked backward (chunk_form.cuh layout, index
+    // (b Hv + hv) nchunks + c): the state at every chunk's start, D^T of every chunk
+    float *rec_s, *rec_d;
 };
 
-template <bool NORM>
+// REC: also store the records of the chunked backward (p.rec_s, p.rec_d)
+template <bool NORM, bool REC>
 __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                      const __grid_constant__ CUtensorMap tm_q,
                                                                      const __grid_constant__ CUtensorMap tm_v,
@@ -264,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
                 z_parity = (uint32_t)(it & 1);
             }
         }
-        decay_state(tmem + lane_base + C_S, s_gam[kC - 1], half);
+        const size_t ci = ((size_t)b * p.Hv + hv) * nchunks + c;
+        if constexpr (REC) decay_state(tmem + lane_base + C_S, s_gam[kC - 1], half, p.rec_s + ci * kRec128, row);
+        else decay_state(tmem + lane_base + C_S, s_gam[kC - 1], half);
         {
             // both TMEM reads in flight before the one wait
             float dv[32], qk[32];
@@ -272,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             if (quad >= 2) umma::tmem_ld32(tmem + lane_base + C_QK + half * 32, qk);
             umma::tmem_ld_wait();
             dt_tile(dv, sm, S_DT, row, half);
+            if constexpr (REC) store_rec64(p.rec_d + ci * kRec64, row, half, dv);
             if (quad >= 2) p_tile(qk, sm, S_P, s_lg, row, half);
         }
         publish();
@@ -356,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool NORM>
+template <bool NORM, bool REC>
 cudaError_t set_smem_attr() {
     static unsigned long long attr_done = 0;   // per instantiation, one bit per device
-    return set_max_smem(attr_done, prefill_chunk_kernel<NORM>, kSmemBytes);
+    return set_max_smem(attr_done, prefill_chunk_kernel<NORM, REC>, kSmemBytes);
 }
 
 }  // namespace
@@ -367,19 +374,25 @@ cudaError_t set_smem_attr() {
 cudaError_t launch_prefill_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                    const float *g, const float *beta, const float *state_in, float *state_out,
                                    const uint8_t *mask, const int *order, uint16_t *y, const uint16_t *z,
-                                   const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st) {
+                                   const float *norm_w, float norm_eps, unsigned *err, cudaStream_t st,
+                                   float *rec_s, float *rec_d) {
     if (s.Dk > kD || s.Dv > kD) return cudaErrorNotSupported;
     ChunkMaps m;
     if (!encode_chunk_maps(&m, s, q, k, v, z, y)) return cudaErrorInvalidValue;
-    cudaError_t e = z != nullptr ? set_smem_attr<true>() : set_smem_attr<false>();
+    const bool rec = rec_s != nullptr && rec_d != nullptr;
+    if (rec && z != nullptr) return cudaErrorNotSupported;
+    cudaError_t e = z != nullptr ? set_smem_attr<true, false>()
+                                 : (rec ? set_smem_attr<false, true>() : set_smem_attr<false, false>());
     if (e != cudaSuccess) return e;
     ChunkParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y, norm_w, norm_eps, err,
-                  s.B, s.T, s.Hk, s.Hv, s.Dk, s.Dv};
+                  s.B, s.T, s.Hk, s.Hv, s.Dk, s.Dv, rec_s, rec_d};
     dim3 grid(s.Hv, s.B);
     if (z != nullptr)
-        prefill_chunk_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(m.k, m.q, m.v, m.z, m.y, p);
+        prefill_chunk_kernel<true, false><<<grid, kThreads, kSmemBytes, st>>>(m.k, m.q, m.v, m.z, m.y, p);
+    else if (rec)
+        prefill_chunk_kernel<false, true><<<grid, kThreads, kSmemBytes, st>>>(m.k, m.q, m.v, m.z, m.y, p);
     else
-        prefill_chunk_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(m.k, m.q, m.v, m.z, m.y, p);
+        prefill_chunk_kernel<false, false><<<grid, kThreads, kSmemBytes, st>>>(m.k, m.q, m.v, m.z, m.y, p);
     return cudaGetLastError();
 }
 

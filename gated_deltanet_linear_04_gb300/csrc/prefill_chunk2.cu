@@ -100,6 +100,9 @@ struct TwoPassParams {
     int *ready;         // overlapped form: one flag per blob (zeroed before launch); else null
     unsigned *err;
     int B, T, Hk, Hv, Dk, Dv, nchunks;
+    // optional records for the chunked backward (chunk_form.cuh layout, one
+    // per blob index): the state at every chunk's start and D^T of every chunk
+    float *rec_s, *rec_d;
 };
 
 // Static shared memory of both roles.
@@ -353,6 +356,8 @@ __device__ __forceinline__ void issue_dt_merged(uint32_t tmem, uint32_t base) {
 // pass 2: the chunk chain of head (b, hv), state products only.  The caller
 // has initialised sh.bar0-2 and allocated 512 TMEM columns.
 // ---------------------------------------------------------------------------
+// REC: also store the records of the chunked backward (p.rec_s, p.rec_d)
+template <bool REC>
 __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtensorMap *tm_y, TwoPassShared &sh,
                                            uint8_t *sm, uint32_t base, uint32_t tmem, int b, int hv) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -458,12 +463,15 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         // group A has been consumed: fetch the next chunk's
         if (cn < nchunks) load_a(cn, it + 1);
 
-        decay_state(lane_tmem + C2_S, gl, half);
+        const size_t ci = blob_index(p, b, hv, c);
+        if constexpr (REC) decay_state(lane_tmem + C2_S, gl, half, p.rec_s + ci * kRec128, row);
+        else decay_state(lane_tmem + C2_S, gl, half);
         {
             float dv[32];
             umma::tmem_ld32(lane_tmem + C2_D + half * 32, dv);
             umma::tmem_ld_wait();
             dt_tile(dv, sm, P2_DT, row, half);
+            if constexpr (REC) store_rec64(p.rec_d + ci * kRec64, row, half, dv);
         }
         publish();
         ok = __syncthreads_and(mbar_wait(&sh.bar1, (uint32_t)(it & 1), p.err)) != 0;
@@ -557,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_prep_kernel(const __grid_co
 }
 
 // separate form, pass 2: one CTA per (hv, row slot)
+template <bool REC>
 __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const __grid_constant__ CUtensorMap tm_y,
                                                                    const TwoPassParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -565,12 +574,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_state_kernel(const __grid_c
     uint8_t *sm = aligned_base(smem_raw, base);
     const uint32_t tmem = cta_setup(sh, 512);
     const int b = p.order != nullptr ? p.order[blockIdx.y] : (int)blockIdx.y;
-    state_head(p, &tm_y, sh, sm, base, tmem, b, blockIdx.x);
+    state_head<REC>(p, &tm_y, sh, sm, base, tmem, b, blockIdx.x);
     cta_teardown(tmem, 512);
 }
 
 // overlapped form (cooperative launch, all CTAs resident): CTAs [0, n_heads)
 // run the state chains, the others produce the chunk images in chunk order
+template <bool REC>
 __global__ void __launch_bounds__(kThreads, 1) chunk_overlap_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                      const __grid_constant__ CUtensorMap tm_q,
                                                                      const __grid_constant__ CUtensorMap tm_v,
@@ -586,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_overlap_kernel(const __grid
     if (is_state) {
         const int slot = blockIdx.x / p.Hv, hv = blockIdx.x % p.Hv;
         const int b = p.order != nullptr ? p.order[slot] : slot;
-        state_head(p, &tm_y, sh, sm, base, tmem, b, hv);
+        state_head<REC>(p, &tm_y, sh, sm, base, tmem, b, hv);
     } else {
         // producer: units u = (chunk u / n_heads, head u % n_heads) in steps of
         // the producer count; wholly masked chunks are passed over
@@ -641,29 +651,37 @@ bool prefill_two_pass_pays(const Sizes &s) { return (long)s.B * s.Hv < num_sms()
 cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                     const float *g, const float *beta, const float *state_in, float *state_out,
                                     const uint8_t *mask, const int *order, uint16_t *y, void *blobs,
-                                    unsigned *err, cudaStream_t st) {
+                                    unsigned *err, cudaStream_t st, float *rec_s, float *rec_d) {
     if (s.Dk > kD || s.Dv > kD) return cudaErrorNotSupported;
     ChunkMaps m;
     if (!encode_chunk_maps(&m, s, q, k, v, nullptr, y)) return cudaErrorInvalidValue;
     const CUtensorMap &tk = m.k, &tq = m.q, &tv = m.v, &ty = m.y;
-    static unsigned long long set1 = 0, set2 = 0, set3 = 0;   // one bit per device
+    const bool rec = rec_s != nullptr && rec_d != nullptr;
+    static unsigned long long set1 = 0, set2 = 0, set3 = 0, set4 = 0, set5 = 0;   // one bit per device
     cudaError_t e = set_max_smem(set1, chunk_prep_kernel, kP1Smem);
-    if (e == cudaSuccess) e = set_max_smem(set2, chunk_state_kernel, kP2Smem);
-    if (e == cudaSuccess) e = set_max_smem(set3, chunk_overlap_kernel, kFusedSmem);
+    if (e == cudaSuccess)
+        e = rec ? set_max_smem(set4, chunk_state_kernel<true>, kP2Smem)
+                : set_max_smem(set2, chunk_state_kernel<false>, kP2Smem);
+    if (e == cudaSuccess)
+        e = rec ? set_max_smem(set5, chunk_overlap_kernel<true>, kFusedSmem)
+                : set_max_smem(set3, chunk_overlap_kernel<false>, kFusedSmem);
     if (e != cudaSuccess) return e;
     const int nchunks = (s.T + kC - 1) / kC;
     const int n_heads = s.B * s.Hv;
     const size_t n_blobs = blob_count(s);
     TwoPassParams p{g, beta, state_in, state_out, mask, mask != nullptr ? order : nullptr, y,
-                    static_cast<uint8_t *>(blobs), nullptr, err, s.B, s.T, s.Hk, s.Hv, s.Dk, s.Dv, nchunks};
+                    static_cast<uint8_t *>(blobs), nullptr, err, s.B, s.T, s.Hk, s.Hv, s.Dk, s.Dv, nchunks,
+                    rec_s, rec_d};
 
     // Overlapped form when the producers (all SMs but the heads') outnumber
     // the heads about three to one: a chunk image takes the producers roughly
     // three times as long as the state pass takes to consume one.
     int per_sm = 0;
     if (4 * n_heads <= num_sms() &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_overlap_kernel, kThreads, kFusedSmem) ==
-            cudaSuccess &&
+        (rec ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_overlap_kernel<true>, kThreads,
+                                                             kFusedSmem)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_overlap_kernel<false>, kThreads,
+                                                             kFusedSmem)) == cudaSuccess &&
         per_sm >= 1) {
         p.ready = reinterpret_cast<int *>(static_cast<uint8_t *>(blobs) + n_blobs * kBlobBytes);
         e = cudaMemsetAsync(p.ready, 0, n_blobs * sizeof(int), st);
@@ -678,12 +696,14 @@ cudaError_t launch_prefill_two_pass(const Sizes &s, const uint16_t *q, const uin
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, chunk_overlap_kernel, tk, tq, tv, ty, p, n_heads);
+        return rec ? cudaLaunchKernelEx(&cfg, chunk_overlap_kernel<true>, tk, tq, tv, ty, p, n_heads)
+                   : cudaLaunchKernelEx(&cfg, chunk_overlap_kernel<false>, tk, tq, tv, ty, p, n_heads);
     }
     chunk_prep_kernel<<<dim3(nchunks, s.Hv, s.B), kThreads, kP1Smem, st>>>(tk, tq, tv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunk_state_kernel<<<dim3(s.Hv, s.B), kThreads, kP2Smem, st>>>(ty, p);
+    if (rec) chunk_state_kernel<true><<<dim3(s.Hv, s.B), kThreads, kP2Smem, st>>>(ty, p);
+    else chunk_state_kernel<false><<<dim3(s.Hv, s.B), kThreads, kP2Smem, st>>>(ty, p);
     return cudaGetLastError();
 }
 

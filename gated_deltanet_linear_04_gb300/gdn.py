@@ -53,6 +53,8 @@ _SIGS = {
                           [ctypes.c_float, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "gdn_prefill_backward_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims)]),
     "gdn_prefill_backward": (ctypes.c_int, [ctypes.POINTER(GdnDims)] + [_P] * 16 + [ctypes.c_size_t, _P]),
+    "gdn_prefill_backward_chunked_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims)]),
+    "gdn_prefill_backward_chunked": (ctypes.c_int, [ctypes.POINTER(GdnDims)] + [_P] * 16 + [ctypes.c_size_t, _P]),
     "gdn_prefill_vec": (ctypes.c_int, [ctypes.POINTER(GdnDims), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_prefill_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(GdnDims), ctypes.c_int]),
     "gdn_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(GdnDims)] + [ctypes.c_void_p] * 9 +
@@ -298,23 +300,39 @@ def gdn_prefill_backward_workspace_size(dims) -> int:
     return int(lib().gdn_prefill_backward_workspace_size(ctypes.byref(d)))
 
 
-def gdn_prefill_backward(dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta, dstate_in,
-                         workspace, stream=None):
+def _backward_call(name, dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta, dstate_in,
+                   workspace, stream):
     d = make_dims(dims)
     n = _Counts(d)
-    _sizes("gdn_prefill_backward", ("q", q, n.qk), ("k", k, n.qk), ("v", v, n.v), ("g", g, n.gate),
+    _sizes(name, ("q", q, n.qk), ("k", k, n.qk), ("v", v, n.v), ("g", g, n.gate),
            ("beta", beta, n.gate), ("state_in", state_in, n.state), ("mask", mask, n.mask), ("dy", dy, n.v),
            ("dstate_out", dstate_out, n.state), ("dq", dq, n.qk), ("dk", dk, n.qk), ("dv", dv, n.v),
            ("dg", dg, n.gate), ("dbeta", dbeta, n.gate), ("dstate_in", dstate_in, n.state))
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     ws_ptr = None if workspace is None else (workspace.data_ptr() or None)
-    _check(lib().gdn_prefill_backward(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
-                                      _ptr(g, F32, "g"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
-                                      _ptr(mask, U8, "mask"), _ptr(dy, BF16, "dy"),
-                                      _ptr(dstate_out, F32, "dstate_out"), _ptr(dq, F32, "dq"), _ptr(dk, F32, "dk"),
-                                      _ptr(dv, F32, "dv"), _ptr(dg, F32, "dg"), _ptr(dbeta, F32, "dbeta"),
-                                      _ptr(dstate_in, F32, "dstate_in"), ws_ptr, ws_bytes, _stream(stream)),
-           "gdn_prefill_backward")
+    _check(getattr(lib(), name)(ctypes.byref(d), _ptr(q, BF16, "q"), _ptr(k, BF16, "k"), _ptr(v, BF16, "v"),
+                                _ptr(g, F32, "g"), _ptr(beta, F32, "beta"), _ptr(state_in, F32, "state_in"),
+                                _ptr(mask, U8, "mask"), _ptr(dy, BF16, "dy"),
+                                _ptr(dstate_out, F32, "dstate_out"), _ptr(dq, F32, "dq"), _ptr(dk, F32, "dk"),
+                                _ptr(dv, F32, "dv"), _ptr(dg, F32, "dg"), _ptr(dbeta, F32, "dbeta"),
+                                _ptr(dstate_in, F32, "dstate_in"), ws_ptr, ws_bytes, _stream(stream)), name)
+
+
+def gdn_prefill_backward(dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta, dstate_in,
+                         workspace, stream=None):
+    _backward_call("gdn_prefill_backward", dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg,
+                   dbeta, dstate_in, workspace, stream)
+
+
+def gdn_prefill_backward_chunked_workspace_size(dims) -> int:
+    d = make_dims(dims)
+    return int(lib().gdn_prefill_backward_chunked_workspace_size(ctypes.byref(d)))
+
+
+def gdn_prefill_backward_chunked(dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk, dv, dg, dbeta,
+                                 dstate_in, workspace, stream=None):
+    _backward_call("gdn_prefill_backward_chunked", dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, dq, dk,
+                   dv, dg, dbeta, dstate_in, workspace, stream)
 
 
 def gdn_prefill_noalloc(dims, q, k, v, g, beta, state_in, state_out, mask, y, chunk=0, stream=None):
@@ -453,9 +471,12 @@ def prefill_gated(dims, q, k, v, g, beta, z, norm_w, norm_eps=1e-6, state_in=Non
     return out, state_out
 
 
-def prefill_backward(dims, q, k, v, g, beta, dy, state_in=None, mask=None, dstate_out=None, stream=None):
+def prefill_backward(dims, q, k, v, g, beta, dy, state_in=None, mask=None, dstate_out=None, stream=None, chunk=0):
     """Gradients of the recurrence; returns a dict dq, dk [B,T,Hk,Dk], dv
-    [B,T,Hv,Dv], dg, dbeta [B,T,Hv], dstate_in [B,Hv,Dv,Dk] (float32)."""
+    [B,T,Hv,Dv], dg, dbeta [B,T,Hv], dstate_in [B,Hv,Dv,Dk] (float32).
+    chunk = 0: sequential form; 64: chunked form on the tensor cores (Dk = Dv = 128)."""
+    if chunk not in (0, 64):
+        raise ValueError("prefill_backward: chunk must be 0 or 64")
     dev = q.device
     B, T = dims.B, dims.T
     out = {"dq": torch.empty((B, T, dims.Hk, dims.Dk), dtype=F32, device=dev),
@@ -464,10 +485,12 @@ def prefill_backward(dims, q, k, v, g, beta, dy, state_in=None, mask=None, dstat
            "dg": torch.empty((B, T, dims.Hv), dtype=F32, device=dev),
            "dbeta": torch.empty((B, T, dims.Hv), dtype=F32, device=dev),
            "dstate_in": torch.empty((B, dims.Hv, dims.Dv, dims.Dk), dtype=F32, device=dev)}
-    nws = gdn_prefill_backward_workspace_size(dims)
+    size_fn, call = ((gdn_prefill_backward_chunked_workspace_size, gdn_prefill_backward_chunked) if chunk
+                     else (gdn_prefill_backward_workspace_size, gdn_prefill_backward))
+    nws = size_fn(dims)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws > 0 else None
-    gdn_prefill_backward(dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, out["dq"], out["dk"], out["dv"],
-                         out["dg"], out["dbeta"], out["dstate_in"], ws, stream)
+    call(dims, q, k, v, g, beta, state_in, mask, dy, dstate_out, out["dq"], out["dk"], out["dv"], out["dg"],
+         out["dbeta"], out["dstate_in"], ws, stream)
     return out
 
 

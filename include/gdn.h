@@ -344,6 +344,34 @@ GDN_API gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q,
                                         float *dbeta, float *dstate_in, void *workspace, size_t ws_bytes,
                                         gdn_stream stream);
 
+/* The same gradients in chunked form on the tensor cores (Dk = Dv = 128 only;
+ * other head sizes return GDN_ERR_UNSUPPORTED): the derivative of the chunked
+ * forward's products (chunks of 64 steps, tf32 operands with f32
+ * accumulation, like gdn_prefill with chunk = 64), with the gradient of the
+ * state carried backwards from chunk to chunk.  The call runs the chunked
+ * forward first, keeping every chunk's start state and D^T, then four
+ * launches (chain images, the reverse chain, two gradient passes).
+ * Arguments, outputs and mask semantics as gdn_prefill_backward; the
+ * gradients agree with the sequential form within the tf32 rounding of the
+ * products (about 3e-4 relative L2 against an f64 reference).
+ *   workspace  device scratch of gdn_prefill_backward_chunked_workspace_size()
+ *              bytes, 16-byte aligned (required when B * T > 0): the row
+ *              order, a bf16 y of the forward, per chunk of each (b, hv) head
+ *              161 KiB of chain images and 192 KiB of f32 records (start
+ *              state, D^T, state gradient, dZ^T), and, when B * Hv is below
+ *              the SM count, the two-pass forward's chunk images (sharing
+ *              space with the chain images).  About 353 KiB per 64 steps of
+ *              each head: 1.4 GB at B = 1, Hv = 32, T = 8192.
+ * The outputs are summed with atomics (dq, dk over the Hv/Hk v-heads of each
+ * k-head); dv, dg, dbeta and dstate_in are written once. */
+GDN_API size_t gdn_prefill_backward_chunked_workspace_size(const gdn_dims *dims);
+GDN_API gdn_status gdn_prefill_backward_chunked(const gdn_dims *dims, const uint16_t *q, const uint16_t *k,
+                                                const uint16_t *v, const float *g, const float *beta,
+                                                const float *state_in, const uint8_t *mask, const uint16_t *dy,
+                                                const float *dstate_out, float *dq, float *dk, float *dv,
+                                                float *dg, float *dbeta, float *dstate_in, void *workspace,
+                                                size_t ws_bytes, gdn_stream stream);
+
 /* Bytes of the optional gdn_prefill workspace for these sizes and this chunk
  * mode (0 or 64): about 8 bytes per batch row, rounded up to 256.  Returns 0
  * for invalid or unsupported arguments. */

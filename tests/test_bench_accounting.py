@@ -82,3 +82,23 @@ def test_oracle_prefill_rate_reports_a_bounded_sample():
     assert abs(r["value"] - steps / 4 / r["seconds"]) <= 0.06 * r["value"] + 1.0
     rv = bench.oracle_prefill_rate(w, heads_per_row=1, vec=True)
     assert rv["value"] > 0 and "per-channel" in rv["sample"]
+
+
+def test_backward_chunk_flops_product_by_product():
+    # every product of the chunked backward (M, N, K) at C = 64, Dk = Dv = 128,
+    # 2 flops per multiply-add, counted one by one
+    d = wl.Dims(B=1, T=64, Hk=1, Hv=1, Dk=128, Dv=128)
+    C, D = 64, 128
+    products = [
+        # the forward with chunk records
+        (2 * C, C, D), (C, C, D), (C, C, D), (C, D, D), (C, D, D), (C, C, D), (D, D, C),
+        # chain images: [K;Q] K^T, Wb, dY^T P, (dY^T P) T, Cq
+        (2 * C, C, D), (D, C, C), (D, C, C), (D, C, C), (D, D, C),
+        # reverse chain: dZ^T += G Wb^T, G += dZ^T diag(beta) (-gamma K)
+        (D, C, D), (D, D, C),
+        # gradients I: [K;Q] K^T, S0 [gamma K; gamma Q]^T, [dY; dZ] D^T
+        (2 * C, C, D), (D, 2 * C, D), (2 * C, C, D),
+        # gradients II: S0^T [dY; dZ]^T, G^T D^T, K^T [dPM; H + H^T]^T, Q^T dPM
+        (D, 2 * C, D), (D, C, D), (D, 2 * C, C), (D, C, C),
+    ]
+    assert bench.backward_chunk_mma_flops(d) == sum(2 * m * n * k for m, n, k in products)

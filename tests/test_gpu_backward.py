@@ -73,3 +73,65 @@ def test_backward_without_steps_passes_the_state_gradient(gdn):  # noqa: F811
                                dstate_out=to_dev(dso))
     torch.cuda.synchronize()
     assert torch.equal(out["dstate_in"].cpu(), dso)
+
+
+# Chunked form (tensor cores, Dk = Dv = 128): the same oracle, the same bound.
+BWD_CHUNKED_CASES = [
+    # B, T, Hk, Hv, mask, state_in, dstate_out
+    (1, 40, 1, 1, None, True, True),            # one partial chunk
+    (1, 200, 1, 2, None, True, False),          # several chunks and a ragged tail
+    (2, 77, 1, 2, "random", True, True),
+    (2, 300, 2, 4, "blocks", False, True),      # wholly masked chunks skipped
+    (2, 100, 2, 4, "allmasked_row", True, True),
+    (1, 130, 1, 1, "sparse", False, False),
+    (3, 129, 1, 3, "right", True, True),
+    (1, 1024, 1, 2, "random", True, True),      # long: the carried gradient over 16 chunks
+    (2, 70, 16, 80, None, True, True),          # 160 heads: the single-pass forward
+]
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv,mk,si,ds", BWD_CHUNKED_CASES)
+def test_backward_chunked_matches_oracle(gdn, B, T, Hk, Hv, mk, si, ds):  # noqa: F811
+    d = wl.Dims(B=B, T=T, Hk=Hk, Hv=Hv, Dk=128, Dv=128)
+    mask = make_mask(mk, B, T, 31 + T)
+    r = recurrence_inputs(d, 3100 + T, mask)
+    gen = torch.Generator().manual_seed(77 + T)
+    dy = (torch.randn((B, T, Hv, 128), generator=gen) * 0.1).to(torch.bfloat16)
+    dso = torch.randn((B, Hv, 128, 128), generator=gen) * 0.01 if ds else None
+    s_in = r["state"] if si else None
+    out = gdn.prefill_backward(d, to_dev(r["q"]), to_dev(r["k"]), to_dev(r["v"]), to_dev(r["g"]), to_dev(r["beta"]),
+                               to_dev(dy), state_in=to_dev(s_in), mask=to_dev(mask), dstate_out=to_dev(dso), chunk=64)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    ref = oracle.recurrence_bwd(d, r["q_bits"], r["k_bits"], r["v_bits"], r["g"].numpy().astype(np.float64),
+                                r["beta"].numpy().astype(np.float64),
+                                None if s_in is None else s_in.numpy().astype(np.float64),
+                                U.bf16_dev_to_f64(dy), None if dso is None else dso.numpy().astype(np.float64),
+                                np_mask(mask))
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dstate_in"):
+        got = out[name].cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got)), name
+        if np.abs(ref[name]).max() == 0.0:
+            assert np.all(got == 0.0), name
+            continue
+        U.assert_state_close(got, ref[name], name + " (chunked)", tol=GRAD_REL_L2)
+    if mask is not None:
+        off = mask.numpy() == 0
+        for name in ("dv", "dg", "dbeta"):
+            assert np.all(out[name].cpu().numpy()[off] == 0.0), name + ": masked steps must be zero"
+        offk = np.repeat(off[:, :, None], Hk, axis=2)
+        for name in ("dq", "dk"):
+            assert np.all(out[name].cpu().numpy()[offk] == 0.0), name + ": masked steps must be zero"
+
+
+def test_backward_chunked_rejects_small_heads(gdn):  # noqa: F811
+    d = wl.Dims(B=1, T=64, Hk=1, Hv=1, Dk=64, Dv=64)
+    assert gdn.gdn_prefill_backward_chunked_workspace_size(d) == 0
+    z = lambda *s: torch.zeros(s, device="cuda:0")
+    zb = lambda *s: torch.zeros(s, dtype=torch.bfloat16, device="cuda:0")
+    with pytest.raises(gdn.GdnError) as err:
+        gdn.gdn_prefill_backward_chunked(d, zb(1, 64, 1, 64), zb(1, 64, 1, 64), zb(1, 64, 1, 64), z(1, 64, 1),
+                                         z(1, 64, 1), None, None, zb(1, 64, 1, 64), None, z(1, 64, 1, 64),
+                                         z(1, 64, 1, 64), z(1, 64, 1, 64), z(1, 64, 1), z(1, 64, 1),
+                                         z(1, 1, 64, 64), torch.zeros(256, dtype=torch.uint8, device="cuda:0"))
+    assert err.value.status == gdn.GDN_ERR_UNSUPPORTED
