@@ -866,6 +866,9 @@ def main():
                     help="workloads of the backward section (a subset keeps an ncu capture small)")
     ap.add_argument("--prefill-workloads", default="prefill_t8192,prefill_ragged",
                     help="workloads of the prefill section (a subset keeps an ncu capture small)")
+    ap.add_argument("--backward-t", type=int, default=0,
+                    help="run the backward workloads at this sequence length instead (small profiling captures)")
+    ap.add_argument("--backward-chunks", default="0,64", help="backward forms to time: 0 sequential, 64 chunked")
     ap.add_argument("--prefill-t", type=int, default=0,
                     help="run the prefill section at this T instead of the workload's (profiling captures of a "
                          "small case only; the benchmark figures use the workloads' own T)")
@@ -941,8 +944,15 @@ def main():
         decode_gated = bench_decode_gated(gdn, w, dev)
     backward = None
     if "backward" in parts:
-        backward = [bench_backward(gdn, wl.WORKLOADS[name], dev, peaks, chunk)
-                    for name in args.backward_workloads.split(",") for chunk in (0, 64)]
+        backward = []
+        for name in args.backward_workloads.split(","):
+            w_b = wl.WORKLOADS[name]
+            if args.backward_t > 0:
+                w_b = wl.Workload(w_b.name + "_t%d" % args.backward_t, w_b.index, w_b.dims.with_(T=args.backward_t),
+                                  w_b.steps, w_b.conv_state, w_b.state, w_b.ragged, min(w_b.len_lo, args.backward_t),
+                                  min(w_b.len_hi, args.backward_t))
+            for chunk in [int(x) for x in args.backward_chunks.split(",")]:
+                backward.append(bench_backward(gdn, w_b, dev, peaks, chunk))
     prefill_vec = None
     if "prefill_vec" in parts:
         prefill_vec = bench_prefill_vec(gdn, wl.WORKLOADS["prefill_t8192"], dev, 3, peaks)
