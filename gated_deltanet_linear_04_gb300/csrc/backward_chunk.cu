@@ -66,7 +66,7 @@ constexpr size_t kImgBytes = I_NGK + 32768;
 // ---- outputs of launch 3 for launch 4, in the same space, one per chunk
 constexpr uint32_t O_B3 = 0;          // [dP o M ; H + H^T] [128][64] tf32, 2 K-tiles of 16 KiB
 constexpr uint32_t O_DPMT = 32768;    // (dP o M)^T [64][64] tf32, 2 K-tiles of 8 KiB
-constexpr uint32_t O_PART = 49152;    // 64 f32: dlog g_t without the F dF terms
+constexpr uint32_t O_PART = 49152;    // 64 f32: dlog g_t without the F dF and <G, S0> terms
 constexpr size_t kOutBytes = O_PART + 256;
 static_assert(kOutBytes <= kImgBytes, "the second outputs reuse the image space");
 static_assert(kImgA % 1024 == 0 && I_NGK % 1024 == 0 && kImgBytes % 1024 == 0, "tiles on 1 KiB boundaries");
@@ -334,24 +334,25 @@ constexpr uint32_t L_DYT = 7 * kSlot;   // dY^T [128 dv][64 i]; then Z1 = dY^T P
 constexpr uint32_t L_GQT = 9 * kSlot;   // (gamma Q)^T [128 dk][64 i]
 constexpr uint32_t L_PT = 11 * kSlot;   // P^T [64 r][64 i] (element (r, i) = P[i][r]), 2 K-tiles of 8 KiB
 constexpr uint32_t L_A = 12 * kSlot;    // A, then T, plain f32 [64][64]
+constexpr uint32_t L_CQS = 9 * kSlot;   // Cq staged for its bulk store (slots 9-12, dead by then)
+constexpr uint32_t L_META = L_DY + 8192;   // beta and 2^lg_63 staged (past the inverse's 4 KiB scratch)
 constexpr uint32_t kLSmem = 13 * kSlot + 1024;
 // TMEM: QK 0-63 (then X1^T), Z1 64-127, Wb^T 128-191, Cq 256-383
 constexpr uint32_t L_CQK = 0, L_CZ1 = 64, L_CWB = 128, L_CCQ = 256;
 
-__global__ void __launch_bounds__(kThreads, 1) bc_image_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                                const __grid_constant__ CUtensorMap tm_q,
-                                                                const __grid_constant__ CUtensorMap tm_dy,
-                                                                const BcParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ BcShared sh;
-    uint32_t base;
-    uint8_t *sm = aligned_smem(smem_raw, base);
+// One chain image: chunk c of head (b, hv), whose gates and step factors
+// chunk_gates has put in shared memory; the TMA and MMA barrier phases carry
+// over from unit to unit.  Every byte of the image leaves by bulk stores from
+// shared memory (Wb and (-gamma K)^T as operand tiles, Cq, X1^T and the meta
+// staged in the thread order of the chain), committed and waited for before
+// returning, so the image is complete in memory when this returns true.
+__device__ __forceinline__ bool image_unit(const BcParams &p, const CUtensorMap *tm_k, const CUtensorMap *tm_q,
+                                           const CUtensorMap *tm_dy, BcShared &sh, uint8_t *sm, uint32_t base,
+                                           uint32_t tmem, int c, int b, int hv, uint32_t &tma_phase,
+                                           uint32_t &mma_phase) {
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quad = warp & 3, half = warp >> 2, row = quad * 32 + (tid & 31);
-    const int c = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
-    if (!chunk_gates(p, sh, c, b, hv)) return;
-    const uint32_t tmem = bc_setup(sh, 512);
     const uint32_t lt = tmem + ((uint32_t)(quad * 32) << 16);
     float *As = reinterpret_cast<float *>(sm + L_A);
     float *Ys = reinterpret_cast<float *>(sm + L_DY);
@@ -359,10 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) bc_image_kernel(const __grid_cons
 
     if (tid == 0) {
         mbar_expect_tx(&sh.bar0, kKQVBytes);
-        issue_kq_tile(sm, L_KQ, L_DY, &tm_k, &tm_q, &tm_dy, hk, hv, b * p.T + c * kC, &sh.bar0);
+        issue_kq_tile(sm, L_KQ, L_DY, tm_k, tm_q, tm_dy, hk, hv, b * p.T + c * kC, &sh.bar0);
     }
-    uint32_t mma_phase = 0;
-    bool ok = wait_all(&sh.bar0, 0, p.err);
+    bool ok = wait_all(&sh.bar0, tma_phase++ & 1u, p.err);
     if (ok) {
         if (tid == 0) {
             issue_kq(tmem, base, L_KQ);
@@ -422,19 +422,21 @@ __global__ void __launch_bounds__(kThreads, 1) bc_image_kernel(const __grid_cons
             put_transposed<32>(sm, L_KT, 8192, 0, row, wb, half * 32);  // Wb [r][dk]
         }
         {
+            // Cq, in the chain's thread order, into the dead (gamma Q)^T, P^T and A slots
             float ca[32], cb[32];
             umma::tmem_ld32(lt + L_CCQ + half * 64, ca);
             umma::tmem_ld32(lt + L_CCQ + half * 64 + 32, cb);
             umma::tmem_ld_wait();
-            float *cq = reinterpret_cast<float *>(img + I_CQ);
+            float *cq = reinterpret_cast<float *>(sm + L_CQS);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 *rec128_at(cq, row, half, j) = make_float4(ca[4 * j], ca[4 * j + 1], ca[4 * j + 2], ca[4 * j + 3]);
                 *rec128_at(cq, row, half, 8 + j) = make_float4(cb[4 * j], cb[4 * j + 1], cb[4 * j + 2], cb[4 * j + 3]);
             }
         }
-        if (tid < kC) reinterpret_cast<float *>(img + I_META)[tid] = sh.s_beta[tid];
-        if (tid == 0) reinterpret_cast<float *>(img + I_META)[64] = sh.s_gam[kC - 1];
+        float *meta = reinterpret_cast<float *>(sm + L_META);
+        if (tid < kC) meta[tid] = sh.s_beta[tid];
+        if (tid == 0) meta[64] = sh.s_gam[kC - 1];
         publish_operands();
         if (tid == 0) {
             // X1^T = Z1 T (into the dead QK columns)
@@ -448,19 +450,45 @@ __global__ void __launch_bounds__(kThreads, 1) bc_image_kernel(const __grid_cons
             umma::mma_commit(&sh.bar2);
             bulk_store(img + I_WB, sm + L_KT, 32768);
             bulk_store(img + I_NGK, sm + L_NGK, 32768);
-            bulk_commit();
+            bulk_store(img + I_CQ, sm + L_CQS, 65536);
+            bulk_store(img + I_META, sm + L_META, 512);
         }
         ok = wait_all(&sh.bar2, mma_phase++ & 1u, p.err);
     }
     if (ok) {
+        // X1^T into the Z1 tile's slots (the product that read them is done)
         float x1[32];
         umma::tmem_ld32(lt + L_CQK + half * 32, x1);
         umma::tmem_ld_wait();
-        store_rec64(reinterpret_cast<float *>(img + I_X1), row, half, x1);
+        store_rec64(reinterpret_cast<float *>(sm + L_DYT), row, half, x1);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) bulk_store(img + I_X1, sm + L_DYT, 32768);
     } else if (tid == 0) {
         mbar_wait(&sh.bar2, mma_phase & 1u, nullptr);   // give in-flight MMAs a bounded chance to drain
     }
-    if (tid == 0) bulk_wait_read();
+    if (tid == 0) {
+        bulk_commit();
+        bulk_wait_all();   // the image is in memory (and shared memory free for the next unit)
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    return ok;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) bc_image_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                const __grid_constant__ CUtensorMap tm_q,
+                                                                const __grid_constant__ CUtensorMap tm_dy,
+                                                                const BcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ BcShared sh;
+    uint32_t base;
+    uint8_t *sm = aligned_smem(smem_raw, base);
+    const int c = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+    if (!chunk_gates(p, sh, c, b, hv)) return;
+    const uint32_t tmem = bc_setup(sh, 512);
+    uint32_t tma_phase = 0, mma_phase = 0;
+    image_unit(p, &tm_k, &tm_q, &tm_dy, sh, sm, base, tmem, c, b, hv, tma_phase, mma_phase);
     bc_teardown(tmem, 512);
 }
 
@@ -489,18 +517,38 @@ __device__ __forceinline__ int prev_active(const uint8_t *mrow, int T, int from,
     return -1;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) bc_chain_kernel(const BcParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ BcShared sh;
-    uint32_t base;
-    uint8_t *sm = aligned_smem(smem_raw, base);
+// Bounded wait (acquire) for a chunk image's ready flag, then order it
+// before the async-proxy bulk loads that read the image.
+__device__ __forceinline__ bool wait_image(const int *flag, unsigned *err) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v != 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        __nanosleep(64);
+    }
+    if (err) atomicOr(err, kErrMbarTimeout);
+    return false;
+}
+
+// Publishes an image whose bulk stores this thread has seen complete.
+__device__ __forceinline__ void publish_image(int *flag) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
+
+// The reverse chain of head (b, hv).  With `ready` (overlapped form), each
+// chunk's image is waited for by its flag before it is loaded; after one
+// wait has given up no further one is made.
+__device__ __forceinline__ void chain_head(const BcParams &p, BcShared &sh, uint8_t *sm, uint32_t base,
+                                           uint32_t tmem, int b, int hv, const int *ready) {
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quad = warp & 3, half = warp >> 2, row = quad * 32 + (tid & 31);
-    const int hv = blockIdx.x;
-    const int b = p.order != nullptr ? p.order[blockIdx.y] : (int)blockIdx.y;
     const int T = p.T;
-    const uint32_t tmem = bc_setup(sh, 256);
     const uint32_t lt = tmem + ((uint32_t)(quad * 32) << 16);
+    bool flag_gave_up = false;   // thread 0
     const uint8_t *mrow = p.mask == nullptr ? nullptr : p.mask + (size_t)b * T;
 
     // G = the gradient of the final state -> TMEM
@@ -510,6 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1) bc_chain_kernel(const BcParams p)
     uint32_t a_par = 0, b_par = 0;
     auto load_a = [&](int ch, int it) {
         if (tid == 0) {
+            if (ready != nullptr && !flag_gave_up)
+                flag_gave_up = !wait_image(ready + chunk_index(p, b, hv, ch), p.err);
             mbar_expect_tx(&sh.bar0, kImgA);
             bulk_load(sm, p.img + chunk_index(p, b, hv, ch) * kImgBytes, kImgA, &sh.bar0);
             a_pending = true;
@@ -632,7 +682,53 @@ __global__ void __launch_bounds__(kThreads, 1) bc_chain_kernel(const BcParams p)
         if (a_pending) mbar_wait(&sh.bar0, a_par, nullptr);
         if (b_pending) mbar_wait(&sh.bar1, b_par, nullptr);
     }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) bc_chain_kernel(const BcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ BcShared sh;
+    uint32_t base;
+    uint8_t *sm = aligned_smem(smem_raw, base);
+    const int b = p.order != nullptr ? p.order[blockIdx.y] : (int)blockIdx.y;
+    const uint32_t tmem = bc_setup(sh, 256);
+    chain_head(p, sh, sm, base, tmem, b, blockIdx.x, nullptr);
     bc_teardown(tmem, 256);
+}
+
+// Overlapped form of launches 1 and 2 (cooperative, all CTAs resident): CTAs
+// [0, n_heads) run the reverse chains, the others produce the chain images
+// from the last chunk backwards (unit u: chunk nchunks - 1 - u / n_heads of
+// head u % n_heads, in steps of the producer count), publishing each with a
+// ready flag once its bulk stores are complete.
+__global__ void __launch_bounds__(kThreads, 1) bc_overlap_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                  const __grid_constant__ CUtensorMap tm_q,
+                                                                  const __grid_constant__ CUtensorMap tm_dy,
+                                                                  const BcParams p, const int n_heads, int *ready) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ BcShared sh;
+    uint32_t base;
+    uint8_t *sm = aligned_smem(smem_raw, base);
+    const bool is_chain = (int)blockIdx.x < n_heads;
+    const uint32_t cols = is_chain ? 256u : 512u;
+    const uint32_t tmem = bc_setup(sh, cols);
+    if (is_chain) {
+        const int slot = blockIdx.x / p.Hv, hv = blockIdx.x % p.Hv;
+        const int b = p.order != nullptr ? p.order[slot] : slot;
+        chain_head(p, sh, sm, base, tmem, b, hv, ready);
+    } else {
+        const int n_prep = (int)gridDim.x - n_heads;
+        const long n_units = (long)p.nchunks * n_heads;
+        uint32_t tma_phase = 0, mma_phase = 0;
+        for (long u = (long)blockIdx.x - n_heads; u < n_units; u += n_prep) {
+            const int c = p.nchunks - 1 - (int)(u / n_heads), h = (int)(u % n_heads);
+            const int slot = h / p.Hv, hv = h % p.Hv;
+            const int b = p.order != nullptr ? p.order[slot] : slot;
+            if (!chunk_gates(p, sh, c, b, hv)) continue;   // the chain skips it too
+            if (!image_unit(p, &tm_k, &tm_q, &tm_dy, sh, sm, base, tmem, c, b, hv, tma_phase, mma_phase)) break;
+            if (threadIdx.x == 0) publish_image(ready + chunk_index(p, b, hv, c));
+        }
+    }
+    bc_teardown(tmem, cols);
 }
 
 // ===========================================================================
@@ -679,24 +775,19 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
         mbar_expect_tx(&sh.bar0, kKQVBytes + 16384);
         issue_kq_tile(sm, A_KQ, A_V, &tm_k, &tm_q, &tm_v, hk, hv, b * T + t0, &sh.bar0);
         tma_load_2d(sm + A_DY, &tm_dy, hv * kD, b * T + t0, &sh.bar0);
-        sh.s_scalar[0] = 0.0f;
     }
     if (tid < kC) {
         sh.s_vec[0][tid] = 0.0f;   // dbeta of the dA term
     }
-    // S0 -> TMEM; <G, S0> (the gamma_63 term of dlog g)
+    // S0 -> TMEM; the dZ^T and D^T records are fetched now and used after the first products
+    float z[32], dl[32];   // dZ^T[dv = row][r = 32 half + j], D^T likewise
     {
-        float s0[64], gv[64];
+        float s0[64];
         load_rec128(p.rec_s + ci * kRec128, row, half, s0);
-        load_rec128(p.rec_g + ci * kRec128, row, half, gv);
+        load_rec64(p.rec_z + ci * kRec64, row, half, z);
+        load_rec64(p.rec_d + ci * kRec64, row, half, dl);
         tmem_put64(lt + A_CS0 + half * 64, s0);
-        float acc = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) acc = fmaf(gv[j], s0[j], acc);
-        acc = warp_sum(acc);
         umma::tmem_st_wait();
-        __syncthreads();   // s_scalar zeroed
-        if (lane == 0) atomicAdd(&sh.s_scalar[0], acc);
     }
     uint32_t mma_phase = 0;
     bool ok = wait_all(&sh.bar0, 0, p.err);
@@ -716,7 +807,6 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
         }
         ok = wait_all(&sh.bar2, mma_phase++ & 1u, p.err);
     }
-    float z[32];   // dZ^T[dv = row][r = 32 half + j]
     if (ok) {
         // E o K K^T (quads 0-1) and P (quads 2-3), plain
         {
@@ -739,13 +829,8 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
             }
         }
         // [dY ; dZ] as the A operand (the [gamma K ; gamma Q] tiles are dead), D as B
-        {
-            float dl[32];
-            load_rec64(p.rec_z + ci * kRec64, row, half, z);
-            load_rec64(p.rec_d + ci * kRec64, row, half, dl);
-            put_transposed<32>(sm, A_GKQ, 16384, 64, row, z, half * 32);
-            put_transposed<32>(sm, A_KQ, 8192, 0, row, dl, half * 32);
-        }
+        put_transposed<32>(sm, A_GKQ, 16384, 64, row, z, half * 32);
+        put_transposed<32>(sm, A_KQ, 8192, 0, row, dl, half * 32);
         build_dy_rows(sm, A_DY, A_GKQ, 16384, sh.s_ok, tid);
         publish_operands();
         if (tid == 0) {
@@ -779,6 +864,11 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
         ok = wait_all(&sh.bar2, mma_phase++ & 1u, p.err);
     }
     if (ok) {
+        // per step: gamma_r dgamma_r (s_vec[1]) and the dZ o R part of dbeta (s_vec[2])
+        if (tid < kC) {
+            sh.s_vec[1][tid] = (sh.s_red[0][0][tid] + sh.s_red[0][1][tid]) + (sh.s_red[0][2][tid] + sh.s_red[0][3][tid]);
+            sh.s_vec[2][tid] = (sh.s_red[1][0][tid] + sh.s_red[1][1][tid]) + (sh.s_red[1][2][tid] + sh.s_red[1][3][tid]);
+        }
         // the [dY ; dZ] and D tiles are dead: B3, (dP o M)^T and H take their place
         float x[32];
         umma::tmem_ld32(lt + A_CQK + half * 32, x);
@@ -840,14 +930,33 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
             }
             dt_tile(hh, sm, A_B3, row, half);
         }
-        // row prefix sums of X = dP o P + dA o A over i < r: Xa[r][t] <- sum_{i<t} X[r][i] (t <= r)
-        if (tid < kC) {
-            const int r = tid;
-            float run = 0.0f;
-            for (int t = 0; t <= r; ++t) {
-                const float xv = Xa[aidx(r, t)] + EKK[aidx(r, t)];
-                Xa[aidx(r, t)] = run;
-                run += xv;
+        // row prefix sums of X = dP o P + dA o A over i < r, four threads per
+        // row of 16 columns each: Xa[r][t] <- sum_{i<t} X[r][i]
+        {
+            const int r = tid >> 2, q = tid & 3;
+            float v[16], run = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int i = 16 * q + e;
+                v[e] = i < r ? Xa[aidx(r, i)] + EKK[aidx(r, i)] : 0.0f;
+                run += v[e];
+            }
+            // the preceding groups' total, taken from the previous lane's
+            // inclusive sum: never formed by a subtraction, which would lose a
+            // tiny prefix next to a large group (gates near 1e-16 make the
+            // terms of one step's dlog g that small)
+            float incl = run;
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, incl, o, 4);
+                if (q >= o) incl += n;
+            }
+            const float prev = __shfl_up_sync(0xffffffffu, incl, 1, 4);
+            float acc = q == 0 ? 0.0f : prev;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                Xa[aidx(r, 16 * q + e)] = acc;
+                acc += v[e];
             }
         }
         fence_proxy_async_smem();
@@ -858,17 +967,30 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
             bulk_store(out + O_DPMT, sm + A_DPMT, 16384);
             bulk_commit();
         }
+        // column sums over r >= t of the prefix sums (the staircase sum_{r>=t,
+        // i<t} X[r][i]) and of gamma_r dgamma_r, four threads per step t
+        {
+            const int t = tid & (kC - 1), q = tid >> 6;
+            float sx = 0.0f, sa = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int r = 16 * q + e;
+                if (r >= t) {
+                    sx += Xa[aidx(r, t)];
+                    sa += sh.s_vec[1][r];
+                }
+            }
+            sh.s_red[0][q][t] = sx;
+            sh.s_red[1][q][t] = sa;
+        }
+        __syncthreads();
         if (tid < kC) {
             const int t = tid;
-            // sum_{r>=t, i<t} X[r][i], sum_{r>=t} gamma_r dgamma_r, and dbeta
-            float sx = 0.0f, sa = 0.0f;
-            for (int r = t; r < kC; ++r) {
-                sx += Xa[aidx(r, t)];
-                sa += (sh.s_red[0][0][r] + sh.s_red[0][1][r]) + (sh.s_red[0][2][r] + sh.s_red[0][3][r]);
-            }
-            reinterpret_cast<float *>(out + O_PART)[t] = sa + sx + sh.s_scalar[0] * sh.s_gam[kC - 1];
-            const float db1 = (sh.s_red[1][0][t] + sh.s_red[1][1][t]) + (sh.s_red[1][2][t] + sh.s_red[1][3][t]);
-            if (t0 + t < T && sh.s_ok[t] != 0.0f) p.dbeta[((size_t)b * T + t0 + t) * p.Hv + hv] = db1 + sh.s_vec[0][t];
+            const float sx = (sh.s_red[0][0][t] + sh.s_red[0][1][t]) + (sh.s_red[0][2][t] + sh.s_red[0][3][t]);
+            const float sa = (sh.s_red[1][0][t] + sh.s_red[1][1][t]) + (sh.s_red[1][2][t] + sh.s_red[1][3][t]);
+            reinterpret_cast<float *>(out + O_PART)[t] = sa + sx;
+            if (t0 + t < T && sh.s_ok[t] != 0.0f)
+                p.dbeta[((size_t)b * T + t0 + t) * p.Hv + hv] = sh.s_vec[2][t] + sh.s_vec[0][t];
         }
     } else if (tid == 0) {
         mbar_wait(&sh.bar2, mma_phase & 1u, nullptr);
@@ -914,12 +1036,24 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad2_kernel(const __grid_cons
         issue_kq_tile(sm, B_KQ, B_DY, &tm_k, &tm_q, &tm_dy, hk, hv, b * T + t0, &sh.bar0);
         bulk_load(sm + B_B3, out + O_B3, 32768, &sh.bar0);
     }
+    if (tid == 0) sh.s_scalar[0] = 0.0f;
+    // S0^T and dZ into their tiles; G and D^T fetched now for the second
+    // product; <G, S0> (the gamma_63 term of dlog g)
+    float gv[64], dl[32];
     {
         float s0[64], z[32];
         load_rec128(p.rec_s + ci * kRec128, row, half, s0);
         load_rec64(p.rec_z + ci * kRec64, row, half, z);
+        load_rec128(p.rec_g + ci * kRec128, row, half, gv);
+        load_rec64(p.rec_d + ci * kRec64, row, half, dl);
         put_transposed<64>(sm, B_A, 16384, 0, row, s0, half * 64);     // S0^T [dk][dv]
         put_transposed<32>(sm, B_B, 16384, 64, row, z, half * 32);     // dZ [r][dv], rows 64-127
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc = fmaf(gv[j], s0[j], acc);
+        acc = warp_sum(acc);
+        __syncthreads();   // s_scalar zeroed
+        if (lane == 0) atomicAdd(&sh.s_scalar[0], acc);
     }
     uint32_t mma_phase = 0;
     bool ok = wait_all(&sh.bar0, 0, p.err);
@@ -945,9 +1079,6 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad2_kernel(const __grid_cons
         ok = wait_all(&sh.bar2, mma_phase++ & 1u, p.err);
     }
     if (ok) {
-        float gv[64], dl[32];
-        load_rec128(p.rec_g + ci * kRec128, row, half, gv);
-        load_rec64(p.rec_d + ci * kRec64, row, half, dl);
         put_transposed<64>(sm, B_A, 16384, 0, row, gv, half * 64);     // G^T [dk][dv]
         put_transposed<32>(sm, B_B, 8192, 0, row, dl, half * 32);      // D [r][dv]
         publish_operands();
@@ -1020,7 +1151,7 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad2_kernel(const __grid_cons
             const int t = tid;
             float pre = 0.0f;
             for (int r = 0; r < t; ++r) pre += sh.s_vec[1][r];
-            const float dlog = reinterpret_cast<const float *>(out + O_PART)[t] + pre;
+            const float dlog = reinterpret_cast<const float *>(out + O_PART)[t] + pre + sh.s_scalar[0] * sh.s_gam[kC - 1];
             if (t0 + t < T && sh.s_ok[t] != 0.0f) p.dg[((size_t)b * T + t0 + t) * p.Hv + hv] = dlog / sh.s_g[t];
         }
     } else if (tid == 0) {
@@ -1032,7 +1163,7 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad2_kernel(const __grid_cons
 
 struct BcLayout {
     int nchunks;
-    size_t n, y_bytes, region, rec_floats;
+    size_t n, y_bytes, region, rec_floats, flag_bytes;
 };
 
 BcLayout bc_layout(const Sizes &s) {
@@ -1045,6 +1176,7 @@ BcLayout bc_layout(const Sizes &s) {
     // bytes), so the size does not depend on the device's SM count
     l.region = l.n * kImgBytes;
     l.rec_floats = 2 * kRec128 + 2 * kRec64;
+    l.flag_bytes = (l.n * sizeof(int) + 255) & ~(size_t)255;   // the overlapped form's ready flags
     return l;
 }
 
@@ -1052,7 +1184,7 @@ BcLayout bc_layout(const Sizes &s) {
 
 size_t backward_chunked_workspace(const Sizes &s) {
     const BcLayout l = bc_layout(s);
-    return row_order_workspace(s) + l.y_bytes + l.region + l.n * l.rec_floats * sizeof(float);
+    return row_order_workspace(s) + l.y_bytes + l.region + l.n * l.rec_floats * sizeof(float) + l.flag_bytes;
 }
 
 cudaError_t launch_backward_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -1085,6 +1217,7 @@ cudaError_t launch_backward_chunked(const Sizes &s, const uint16_t *q, const uin
     float *rec_d = rec_s + l.n * kRec128;
     float *rec_g = rec_d + l.n * kRec64;
     float *rec_z = rec_g + l.n * kRec128;
+    int *ready = reinterpret_cast<int *>(rec_z + l.n * kRec64);
 
     // the forward, keeping every chunk's start state and D^T
     if (prefill_two_pass_workspace(s) > l.region) return cudaErrorInvalidValue;
@@ -1099,21 +1232,47 @@ cudaError_t launch_backward_chunked(const Sizes &s, const uint16_t *q, const uin
     ChunkMaps mk, mv;   // k, q and dY (in the v slot); v
     if (!encode_chunk_maps(&mk, s, q, k, dy, nullptr, y) || !encode_chunk_maps(&mv, s, q, k, v, nullptr, y))
         return cudaErrorInvalidValue;
-    static unsigned long long set1 = 0, set2 = 0, set3 = 0, set4 = 0;   // one bit per device
+    static unsigned long long set1 = 0, set2 = 0, set3 = 0, set4 = 0, set5 = 0;   // one bit per device
+    constexpr uint32_t kOverlapSmem = kLSmem > kRSmem ? kLSmem : kRSmem;
     e = set_max_smem(set1, bc_image_kernel, kLSmem);
     if (e == cudaSuccess) e = set_max_smem(set2, bc_chain_kernel, kRSmem);
     if (e == cudaSuccess) e = set_max_smem(set3, bc_grad1_kernel, kASmem);
     if (e == cudaSuccess) e = set_max_smem(set4, bc_grad2_kernel, kBSmem);
+    if (e == cudaSuccess) e = set_max_smem(set5, bc_overlap_kernel, kOverlapSmem);
     if (e != cudaSuccess) return e;
     BcParams p{g, beta, mask, order, rec_s, rec_d, rec_g, rec_z, region, dstate_out,
                dq, dk, dv, dg, dbeta, dstate_in, err, s.B, s.T, s.Hk, s.Hv, l.nchunks};
     const dim3 chunks(l.nchunks, s.Hv, s.B);
-    bc_image_kernel<<<chunks, kThreads, kLSmem, st>>>(mk.k, mk.q, mk.v, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    bc_chain_kernel<<<dim3(s.Hv, s.B), kThreads, kRSmem, st>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // chain images and the reverse chain: overlapped in one cooperative launch
+    // when the heads leave most SMs to the image producers, else two launches
+    const int n_heads = s.B * s.Hv;
+    int per_sm = 0;
+    if (4 * n_heads <= num_sms() &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bc_overlap_kernel, kThreads, kOverlapSmem) ==
+            cudaSuccess &&
+        per_sm >= 1) {
+        e = cudaMemsetAsync(ready, 0, l.n * sizeof(int), st);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(num_sms() * per_sm);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kOverlapSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, bc_overlap_kernel, mk.k, mk.q, mk.v, p, n_heads, ready);
+        if (e != cudaSuccess) return e;
+    } else {
+        bc_image_kernel<<<chunks, kThreads, kLSmem, st>>>(mk.k, mk.q, mk.v, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        bc_chain_kernel<<<dim3(s.Hv, s.B), kThreads, kRSmem, st>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     bc_grad1_kernel<<<chunks, kThreads, kASmem, st>>>(mk.k, mk.q, mv.v, mk.v, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -349,8 +349,9 @@ GDN_API gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q,
  * forward's products (chunks of 64 steps, tf32 operands with f32
  * accumulation, like gdn_prefill with chunk = 64), with the gradient of the
  * state carried backwards from chunk to chunk.  The call runs the chunked
- * forward first, keeping every chunk's start state and D^T, then four
- * launches (chain images, the reverse chain, two gradient passes).
+ * forward first, keeping every chunk's start state and D^T, then the chain
+ * images and the reverse chain (one cooperative launch when B * Hv is at
+ * most a quarter of the SM count, else two) and two gradient passes.
  * Arguments, outputs and mask semantics as gdn_prefill_backward; the
  * gradients agree with the sequential form within the tf32 rounding of the
  * products (about 3e-4 relative L2 against an f64 reference).
@@ -360,8 +361,9 @@ GDN_API gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q,
  *              161 KiB of chain images and 192 KiB of f32 records (start
  *              state, D^T, state gradient, dZ^T), and, when B * Hv is below
  *              the SM count, the two-pass forward's chunk images (sharing
- *              space with the chain images).  About 353 KiB per 64 steps of
- *              each head: 1.4 GB at B = 1, Hv = 32, T = 8192.
+ *              space with the chain images), and a ready flag per chunk.
+ *              About 353 KiB per 64 steps of each head: 1.4 GB at B = 1,
+ *              Hv = 32, T = 8192.
  * The outputs are summed with atomics (dq, dk over the Hv/Hk v-heads of each
  * k-head); dv, dg, dbeta and dstate_in are written once. */
 GDN_API size_t gdn_prefill_backward_chunked_workspace_size(const gdn_dims *dims);
