@@ -501,7 +501,7 @@ gdn_status backward_impl(bool chunked, const gdn_dims *dims, const uint16_t *q, 
     Sizes s;
     gdn_status st = check_dims(dims, &s);
     if (st != GDN_OK) return st;
-    if (chunked && (s.Dk != 128 || s.Dv != 128)) return GDN_ERR_UNSUPPORTED;
+    if (chunked && (s.Dk > 128 || s.Dv > 128)) return GDN_ERR_UNSUPPORTED;
     const size_t BT = (size_t)s.B * s.T;
     const size_t nstate = (size_t)s.B * s.Hv * s.Dv * s.Dk;
     if (!ok_ptr(q, BT) || !ok_ptr(k, BT) || !ok_ptr(v, BT) || !ok_ptr(g, BT) || !ok_ptr(beta, BT) ||
@@ -548,7 +548,7 @@ gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q, const u
 
 size_t gdn_prefill_backward_chunked_workspace_size(const gdn_dims *dims) {
     gdn::Sizes s;
-    if (gdn::check_dims(dims, &s) != GDN_OK || s.Dk != 128 || s.Dv != 128) return 0;
+    if (gdn::check_dims(dims, &s) != GDN_OK || s.Dk > 128 || s.Dv > 128) return 0;
     return gdn::backward_chunked_workspace(s);
 }
 

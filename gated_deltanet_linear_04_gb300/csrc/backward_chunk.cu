@@ -1,5 +1,9 @@
 // Backward pass of the recurrence in chunked (WY / UT-transform) form on the
-// 5th-generation tensor cores, for Dk = Dv = 128.
+// 5th-generation tensor cores.  Every head size of the chunked forward (Dk,
+// Dv of 32, 64 or 128) runs on 128-wide tiles and records: the tiles' columns
+// past the head load as zeros, so the padded rows and columns of every
+// product and record are exact zeros, and the global writes are clipped to
+// the head.
 //
 // The pages ("mlex 0.1.2, src/models/gated_delta.rs", the per-timestep loop;
 // "mlx-bun 0.4.0 -> 1.0.0, package/src/model/qwen3-delta.ts",
@@ -81,7 +85,7 @@ struct BcParams {
     const float *dstate_out;
     float *dq, *dk, *dv, *dg, *dbeta, *dstate_in;
     unsigned *err;
-    int B, T, Hk, Hv, nchunks;
+    int B, T, Hk, Hv, Dk, Dv, nchunks;
 };
 
 struct BcShared {
@@ -269,14 +273,31 @@ __device__ __forceinline__ void tmem_put64(uint32_t taddr, const float (&v)[64])
 // counted on `bar`, whose single arrival (with the expected bytes) the caller
 // makes once for everything that phase loads.
 constexpr uint32_t kKQVBytes = 4 * 8192 + 16384;
+
+// A plain [64][128] bf16 tile (v or dY) of head hx, in the map form of the
+// head size (chunk_form.cuh: 2-D at Dv = 128, else the padded 3-D form whose
+// columns past the head read as zeros).
+__device__ __forceinline__ void issue_x_tile(uint8_t *dst, const CUtensorMap *tm_x, int Dv, int hx, int rowg,
+                                             uint64_t *bar) {
+    if (Dv == kD) tma_load_2d(dst, tm_x, hx * kD, rowg, bar);
+    else tma_load_3d(dst, tm_x, 0, hx, rowg, bar);
+}
+
 __device__ __forceinline__ void issue_kq_tile(uint8_t *sm, uint32_t kq_off, uint32_t x_off, const CUtensorMap *tm_k,
-                                              const CUtensorMap *tm_q, const CUtensorMap *tm_x, int hk, int hx,
-                                              int rowg, uint64_t *bar) {
-    tma_load_2d(sm + kq_off, tm_k, hk * kD, rowg, bar);
-    tma_load_2d(sm + kq_off + kSlot, tm_k, hk * kD + 64, rowg, bar);
-    tma_load_2d(sm + kq_off + 8192, tm_q, hk * kD, rowg, bar);
-    tma_load_2d(sm + kq_off + kSlot + 8192, tm_q, hk * kD + 64, rowg, bar);
-    tma_load_2d(sm + x_off, tm_x, hx * kD, rowg, bar);
+                                              const CUtensorMap *tm_q, const CUtensorMap *tm_x, int Dk, int Dv,
+                                              int hk, int hx, int rowg, uint64_t *bar) {
+    if (Dk == kD) {
+        tma_load_2d(sm + kq_off, tm_k, hk * kD, rowg, bar);
+        tma_load_2d(sm + kq_off + kSlot, tm_k, hk * kD + 64, rowg, bar);
+        tma_load_2d(sm + kq_off + 8192, tm_q, hk * kD, rowg, bar);
+        tma_load_2d(sm + kq_off + kSlot + 8192, tm_q, hk * kD + 64, rowg, bar);
+    } else {
+        tma_load_3d(sm + kq_off, tm_k, 0, hk, rowg, bar);
+        tma_load_3d(sm + kq_off + kSlot, tm_k, 64, hk, rowg, bar);
+        tma_load_3d(sm + kq_off + 8192, tm_q, 0, hk, rowg, bar);
+        tma_load_3d(sm + kq_off + kSlot + 8192, tm_q, 64, hk, rowg, bar);
+    }
+    issue_x_tile(sm + x_off, tm_x, Dv, hx, rowg, bar);
 }
 
 // barriers and TMEM of a CTA; returns the TMEM base
@@ -360,7 +381,7 @@ __device__ __forceinline__ bool image_unit(const BcParams &p, const CUtensorMap 
 
     if (tid == 0) {
         mbar_expect_tx(&sh.bar0, kKQVBytes);
-        issue_kq_tile(sm, L_KQ, L_DY, tm_k, tm_q, tm_dy, hk, hv, b * p.T + c * kC, &sh.bar0);
+        issue_kq_tile(sm, L_KQ, L_DY, tm_k, tm_q, tm_dy, p.Dk, p.Dv, hk, hv, b * p.T + c * kC, &sh.bar0);
     }
     bool ok = wait_all(&sh.bar0, tma_phase++ & 1u, p.err);
     if (ok) {
@@ -552,7 +573,7 @@ __device__ __forceinline__ void chain_head(const BcParams &p, BcShared &sh, uint
     const uint8_t *mrow = p.mask == nullptr ? nullptr : p.mask + (size_t)b * T;
 
     // G = the gradient of the final state -> TMEM
-    state_to_tmem(p.dstate_out, lt + R_CG, b, hv, p.Hv, kD, kD, row, half);
+    state_to_tmem(p.dstate_out, lt + R_CG, b, hv, p.Hv, p.Dk, p.Dv, row, half);
 
     bool a_pending = false, b_pending = false;   // thread 0: copies in flight
     uint32_t a_par = 0, b_par = 0;
@@ -653,7 +674,7 @@ __device__ __forceinline__ void chain_head(const BcParams &p, BcShared &sh, uint
             for (int j = 0; j < 32; ++j) {
                 const int r = half * 32 + j;
                 z[j] *= meta[r];
-                if (t0 + r < T) p.dv[(((size_t)b * T + t0 + r) * p.Hv + hv) * kD + row] = z[j];
+                if (t0 + r < T && row < p.Dv) p.dv[(((size_t)b * T + t0 + r) * p.Hv + hv) * p.Dv + row] = z[j];
             }
             dt_tile(z, sm, R_DZB, row, half);
         }
@@ -675,7 +696,7 @@ __device__ __forceinline__ void chain_head(const BcParams &p, BcShared &sh, uint
         c = cn;
     }
     if (__syncthreads_and(ok)) {
-        state_from_tmem(p.dstate_in, lt + R_CG, b, hv, p.Hv, kD, kD, row, half);
+        state_from_tmem(p.dstate_in, lt + R_CG, b, hv, p.Hv, p.Dk, p.Dv, row, half);
     } else if (tid == 0) {
         // a wait gave up: give in-flight MMAs and copies a bounded chance to drain
         mbar_wait(&sh.bar2, mma_phase & 1u, nullptr);
@@ -773,8 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
     if (tid == 0) {
         // one arrival for the phase, with every byte it brings in
         mbar_expect_tx(&sh.bar0, kKQVBytes + 16384);
-        issue_kq_tile(sm, A_KQ, A_V, &tm_k, &tm_q, &tm_v, hk, hv, b * T + t0, &sh.bar0);
-        tma_load_2d(sm + A_DY, &tm_dy, hv * kD, b * T + t0, &sh.bar0);
+        issue_kq_tile(sm, A_KQ, A_V, &tm_k, &tm_q, &tm_v, p.Dk, p.Dv, hk, hv, b * T + t0, &sh.bar0);
+        issue_x_tile(sm + A_DY, &tm_dy, p.Dv, hv, b * T + t0, &sh.bar0);
     }
     if (tid < kC) {
         sh.s_vec[0][tid] = 0.0f;   // dbeta of the dA term
@@ -1033,7 +1054,7 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad2_kernel(const __grid_cons
     if (tid == 0) {
         // k, q and dY tiles and B3: one arrival for the phase, with every byte
         mbar_expect_tx(&sh.bar0, kKQVBytes + 32768);
-        issue_kq_tile(sm, B_KQ, B_DY, &tm_k, &tm_q, &tm_dy, hk, hv, b * T + t0, &sh.bar0);
+        issue_kq_tile(sm, B_KQ, B_DY, &tm_k, &tm_q, &tm_dy, p.Dk, p.Dv, hk, hv, b * T + t0, &sh.bar0);
         bulk_load(sm + B_B3, out + O_B3, 32768, &sh.bar0);
     }
     if (tid == 0) sh.s_scalar[0] = 0.0f;
@@ -1129,15 +1150,16 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad2_kernel(const __grid_cons
         umma::tmem_ld32(lt + B_CR + half * 32, ra);
         umma::tmem_ld32(lt + B_CR + 64 + half * 32, rb);
         umma::tmem_ld_wait();
-        const size_t qk_row = (size_t)p.Hk * kD;
-        float *dq0 = p.dq + ((size_t)b * T + t0) * qk_row + (size_t)hk * kD + row;
-        float *dk0 = p.dk + ((size_t)b * T + t0) * qk_row + (size_t)hk * kD + row;
+        const size_t qk_row = (size_t)p.Hk * p.Dk;
+        const bool col_ok = row < p.Dk;   // padded columns past the head are not written
+        float *dq0 = p.dq + ((size_t)b * T + t0) * qk_row + (size_t)hk * p.Dk + (col_ok ? row : 0);
+        float *dk0 = p.dk + ((size_t)b * T + t0) * qk_row + (size_t)hk * p.Dk + (col_ok ? row : 0);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int r = half * 32 + j;
             const float fmg = sh.s_kc[r] * mg[j];
             fg[j] = fmg * kq_elem(sm, B_KQ, r, row);
-            if (t0 + r < T && sh.s_ok[r] != 0.0f) {
+            if (col_ok && t0 + r < T && sh.s_ok[r] != 0.0f) {
                 atomicAdd(dq0 + (size_t)r * qk_row, fmaf(sh.s_gam[r], q1[j], ra[j]));
                 atomicAdd(dk0 + (size_t)r * qk_row, fmaf(-sh.s_bg[r], k1[j], fmg) + rb[j]);
             }
@@ -1192,7 +1214,7 @@ cudaError_t launch_backward_chunked(const Sizes &s, const uint16_t *q, const uin
                                     const uint16_t *dy, const float *dstate_out, float *dq, float *dk, float *dv,
                                     float *dg, float *dbeta, float *dstate_in, void *ws, unsigned *err,
                                     cudaStream_t st) {
-    if (s.Dk != kD || s.Dv != kD) return cudaErrorNotSupported;
+    if (s.Dk > kD || s.Dv > kD) return cudaErrorNotSupported;
     const size_t nqk = (size_t)s.B * s.T * s.Hk * s.Dk, nv = (size_t)s.B * s.T * s.Hv * s.Dv;
     const size_t ng = (size_t)s.B * s.T * s.Hv;
     cudaError_t e = cudaMemsetAsync(dq, 0, nqk * sizeof(float), st);
@@ -1241,7 +1263,7 @@ cudaError_t launch_backward_chunked(const Sizes &s, const uint16_t *q, const uin
     if (e == cudaSuccess) e = set_max_smem(set5, bc_overlap_kernel, kOverlapSmem);
     if (e != cudaSuccess) return e;
     BcParams p{g, beta, mask, order, rec_s, rec_d, rec_g, rec_z, region, dstate_out,
-               dq, dk, dv, dg, dbeta, dstate_in, err, s.B, s.T, s.Hk, s.Hv, l.nchunks};
+               dq, dk, dv, dg, dbeta, dstate_in, err, s.B, s.T, s.Hk, s.Hv, s.Dk, s.Dv, l.nchunks};
     const dim3 chunks(l.nchunks, s.Hv, s.B);
     // chain images and the reverse chain: overlapped in one cooperative launch
     // when the heads leave most SMs to the image producers, else two launches

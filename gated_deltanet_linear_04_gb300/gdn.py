@@ -474,7 +474,7 @@ def prefill_gated(dims, q, k, v, g, beta, z, norm_w, norm_eps=1e-6, state_in=Non
 def prefill_backward(dims, q, k, v, g, beta, dy, state_in=None, mask=None, dstate_out=None, stream=None, chunk=0):
     """Gradients of the recurrence; returns a dict dq, dk [B,T,Hk,Dk], dv
     [B,T,Hv,Dv], dg, dbeta [B,T,Hv], dstate_in [B,Hv,Dv,Dk] (float32).
-    chunk = 0: sequential form; 64: chunked form on the tensor cores (Dk = Dv = 128)."""
+    chunk = 0: sequential form; 64: chunked form on the tensor cores."""
     if chunk not in (0, 64):
         raise ValueError("prefill_backward: chunk must be 0 or 64")
     dev = q.device

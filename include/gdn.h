@@ -344,8 +344,8 @@ GDN_API gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q,
                                         float *dbeta, float *dstate_in, void *workspace, size_t ws_bytes,
                                         gdn_stream stream);
 
-/* The same gradients in chunked form on the tensor cores (Dk = Dv = 128 only;
- * other head sizes return GDN_ERR_UNSUPPORTED): the derivative of the chunked
+/* The same gradients in chunked form on the tensor cores (Dk, Dv in {32, 64,
+ * 128}, all on 128-wide tiles whose padding is exact zeros): the derivative of the chunked
  * forward's products (chunks of 64 steps, tf32 operands with f32
  * accumulation, like gdn_prefill with chunk = 64), with the gradient of the
  * state carried backwards from chunk to chunk.  The call runs the chunked

@@ -102,3 +102,46 @@ def test_prefill_ragged(gdn, chunk):
     order = np.argsort(lens.numpy())
     pairs = [(int(order[0]), 5), (int(order[-1]), 63), (int(order[len(order) // 2]), 30)]
     _prefill_case(gdn, "prefill_ragged", pairs, chunk)
+
+
+@pytest.mark.parametrize("chunk", [0, 64])
+def test_backward_t8192(gdn, chunk):
+    """The backward pass at the single-sequence prefill workload's size (B=1,
+    T=8192, 32 v-heads on 16 k-heads), q/k/v/g/beta from the workload's own
+    conv and gates, dy and the final state's gradient seeded.  Sampled heads
+    against the f64 reverse pass: dv, dg, dbeta, dstate_in of four v-heads and
+    dq, dk of the two k-heads they share (sums over both v-heads)."""
+    w = wl.WORKLOADS["prefill_t8192"]
+    inp = wl.workload_inputs(w)
+    d = inp["dims"]
+    q, k, v, _ = oracle.conv_update(d, wl.bf16_bits(inp["qkv"]), wl.bf16_bits(inp["conv_w"]),
+                                    wl.bf16_bits(inp["conv_state"]), None)
+    g, beta = oracle.gating(wl.bf16_bits(inp["a"]), wl.bf16_bits(inp["b"]), inp["A_log"].numpy(),
+                            inp["dt_bias"].numpy())
+    g32, b32 = g.astype(np.float32), beta.astype(np.float32)
+    t = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(DEV)
+    gen = torch.Generator().manual_seed(4242)
+    dy = (torch.randn((d.B, d.T, d.Hv, d.Dv), generator=gen) * 0.1).to(torch.bfloat16)
+    dso = torch.randn((d.B, d.Hv, d.Dv, d.Dk), generator=gen) * 0.01
+    s_in = inp["state"]
+    out = gdn.prefill_backward(d, t(q), t(k), t(v), torch.from_numpy(g32).to(DEV), torch.from_numpy(b32).to(DEV),
+                               dy.to(DEV), state_in=s_in.to(DEV), dstate_out=dso.to(DEV), chunk=chunk)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    G = d.Hv // d.Hk
+    for hk in (0, 13):
+        dq_ref = np.zeros((d.T, d.Dk))
+        dk_ref = np.zeros((d.T, d.Dk))
+        for hv in range(hk * G, hk * G + G):
+            r = oracle.head_recurrence_bwd(oracle.bf16_to_f64(q[0, :, hk]), oracle.bf16_to_f64(k[0, :, hk]),
+                                           oracle.bf16_to_f64(v[0, :, hv]), g32[0, :, hv].astype(np.float64),
+                                           b32[0, :, hv].astype(np.float64), s_in[0, hv].numpy().astype(np.float64),
+                                           U.bf16_dev_to_f64(dy[0, :, hv]), dso[0, hv].numpy().astype(np.float64))
+            dq_ref += r["dq"]
+            dk_ref += r["dk"]
+            for name, rn, got in (("dv", "dv", out["dv"][0, :, hv]), ("dg", "dg", out["dg"][0, :, hv]),
+                                  ("dbeta", "dbeta", out["dbeta"][0, :, hv]),
+                                  ("dstate_in", "dS0", out["dstate_in"][0, hv])):
+                U.assert_state_close(got.cpu().numpy(), r[rn], "%s (hv %d, chunk %d)" % (name, hv, chunk), tol=1e-3)
+        U.assert_state_close(out["dq"][0, :, hk].cpu().numpy(), dq_ref, "dq (hk %d, chunk %d)" % (hk, chunk), tol=1e-3)
+        U.assert_state_close(out["dk"][0, :, hk].cpu().numpy(), dk_ref, "dk (hk %d, chunk %d)" % (hk, chunk), tol=1e-3)
