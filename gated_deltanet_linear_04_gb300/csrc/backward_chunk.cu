@@ -1185,14 +1185,13 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad2_kernel(const __grid_cons
 
 struct BcLayout {
     int nchunks;
-    size_t n, y_bytes, region, rec_floats, flag_bytes;
+    size_t n, region, rec_floats, flag_bytes;
 };
 
 BcLayout bc_layout(const Sizes &s) {
     BcLayout l;
     l.nchunks = (s.T + kC - 1) / kC;
     l.n = (size_t)s.B * s.Hv * l.nchunks;
-    l.y_bytes = ((size_t)s.B * s.T * s.Hv * s.Dv * 2 + 255) & ~(size_t)255;
     // the chain images also hold the two-pass forward's blobs and ready
     // flags (145 KiB and 4 bytes per chunk, the flags rounded up to 256
     // bytes), so the size does not depend on the device's SM count
@@ -1206,7 +1205,7 @@ BcLayout bc_layout(const Sizes &s) {
 
 size_t backward_chunked_workspace(const Sizes &s) {
     const BcLayout l = bc_layout(s);
-    return row_order_workspace(s) + l.y_bytes + l.region + l.n * l.rec_floats * sizeof(float) + l.flag_bytes;
+    return row_order_workspace(s) + l.region + l.n * l.rec_floats * sizeof(float) + l.flag_bytes;
 }
 
 cudaError_t launch_backward_chunked(const Sizes &s, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -1231,8 +1230,9 @@ cudaError_t launch_backward_chunked(const Sizes &s, const uint16_t *q, const uin
         order = static_cast<const int *>(ws);
     }
     uint8_t *w = static_cast<uint8_t *>(ws) + row_order_workspace(s);
-    uint16_t *y = reinterpret_cast<uint16_t *>(w);
-    w += l.y_bytes;
+    // the forward in record mode writes no y; its y tensor map is encoded on
+    // dy (the same shape), which nothing writes
+    uint16_t *y = const_cast<uint16_t *>(dy);
     uint8_t *region = w;
     w += l.region;
     float *rec_s = reinterpret_cast<float *>(w);

@@ -74,7 +74,8 @@ struct ChunkParams {
     float *rec_s, *rec_d;
 };
 
-// REC: also store the records of the chunked backward (p.rec_s, p.rec_d)
+// REC: store the records of the chunked backward (p.rec_s, p.rec_d) instead
+// of y, which the backward does not read
 template <bool NORM, bool REC>
 __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                      const __grid_constant__ CUtensorMap tm_q,
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * p.Dv + (size_t)hv * p.Dv;
     const size_t y_stride = (size_t)p.Hv * p.Dv;
     int c = scan.next_active(0);
-    zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), p.Dv);
+    if constexpr (!REC) zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), p.Dv);   // REC: y is not needed
     if (c < nchunks) {
         issue_tma(c);
         gather_steps(c);
@@ -292,8 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
 
         // ---- S9: y through a shared staging tile [64 steps][128 dv] bf16
         // (masked steps zero), then one TMA store of the tile clipped at T
-        stage_y(tmem + lane_base + C_Y, sm, S_YST, s_m[st], row, half);
-        fence_proxy_async_smem();
+        if constexpr (!REC) {
+            stage_y(tmem + lane_base + C_Y, sm, S_YST, s_m[st], row, half);
+            fence_proxy_async_smem();
+        }
         umma::fence_before_sync();
         __syncthreads();
         if constexpr (NORM) {
@@ -341,11 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             ok = __syncthreads_and(ok) != 0;
             if (!ok) break;
         }
-        if (tid == 0) {
-            store_chunk_y(&tm_y, p.Dv, hv, t0, b, sm + S_YST);
-            bulk_commit();
+        if constexpr (!REC) {
+            if (tid == 0) {
+                store_chunk_y(&tm_y, p.Dv, hv, t0, b, sm + S_YST);
+                bulk_commit();
+            }
+            zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), p.Dv);
         }
-        zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), p.Dv);
         c = cn;
     }
 

@@ -356,7 +356,8 @@ __device__ __forceinline__ void issue_dt_merged(uint32_t tmem, uint32_t base) {
 // pass 2: the chunk chain of head (b, hv), state products only.  The caller
 // has initialised sh.bar0-2 and allocated 512 TMEM columns.
 // ---------------------------------------------------------------------------
-// REC: also store the records of the chunked backward (p.rec_s, p.rec_d)
+// REC: store the records of the chunked backward (p.rec_s, p.rec_d) instead
+// of y, which the backward does not read
 template <bool REC>
 __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtensorMap *tm_y, TwoPassShared &sh,
                                            uint8_t *sm, uint32_t base, uint32_t tmem, int b, int hv) {
@@ -420,7 +421,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
     uint16_t *y_row0 = p.y + (size_t)b * T * p.Hv * p.Dv + (size_t)hv * p.Dv;
     const size_t y_stride = (size_t)p.Hv * p.Dv;
     int c = scan.next_active(0);
-    zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), p.Dv);
+    if constexpr (!REC) zero_y_rows(y_row0, y_stride, 0, min(c * kC, T), p.Dv);   // REC: y is not needed
     if (c < nchunks) {
         load_a(c, 0);
         load_b(c, 0);
@@ -488,16 +489,20 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
 
         // y: the staged tile leaves by one TMA store (clipped at T), which
         // the next chunk's staging waits for
-        stage_y(lane_tmem + C2_Y, sm, P2_YST, sh.s_m[st], row, half);
-        fence_proxy_async_smem();
+        if constexpr (!REC) {
+            stage_y(lane_tmem + C2_Y, sm, P2_YST, sh.s_m[st], row, half);
+            fence_proxy_async_smem();
+        }
         umma::fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
-            store_chunk_y(tm_y, p.Dv, hv, t0, b, sm + P2_YST);
-            bulk_commit();
+        if constexpr (!REC) {
+            if (tid == 0) {
+                store_chunk_y(tm_y, p.Dv, hv, t0, b, sm + P2_YST);
+                bulk_commit();
+            }
         }
         if (tid < kC) sh.s_m[st ^ 1][tid] = pf_m;
-        zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), p.Dv);
+        if constexpr (!REC) zero_y_rows(y_row0, y_stride, min((c + 1) * kC, T), min(cn * kC, T), p.Dv);
         c = cn;
     }
 

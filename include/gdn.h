@@ -357,7 +357,7 @@ GDN_API gdn_status gdn_prefill_backward(const gdn_dims *dims, const uint16_t *q,
  * products (about 3e-4 relative L2 against an f64 reference).
  *   workspace  device scratch of gdn_prefill_backward_chunked_workspace_size()
  *              bytes, 16-byte aligned (required when B * T > 0): the row
- *              order, a bf16 y of the forward, per chunk of each (b, hv) head
+ *              order, then per chunk of each (b, hv) head
  *              161 KiB of chain images and 192 KiB of f32 records (start
  *              state, D^T, state gradient, dZ^T), and, when B * Hv is below
  *              the SM count, the two-pass forward's chunk images (sharing

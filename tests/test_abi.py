@@ -140,19 +140,14 @@ def test_binding_constants_match_the_header():
 
 def test_backward_chunked_workspace_sizes(lib):
     # per chunk of 64 steps of each (b, hv) head: 161 KiB of chain images,
-    # 192 KiB of f32 records and a ready flag, after the row order and the
-    # forward's bf16 y
+    # 192 KiB of f32 records and a ready flag, after the row order
     d = _dims(B=2, T=130, Hk=1, Hv=2, Dk=128, Dv=128)
     n = 2 * 2 * 3
     order = lib.gdn_prefill_workspace_size(ctypes.byref(d), 0)
-    y = (2 * 130 * 2 * 128 * 2 + 255) // 256 * 256
     flags = (n * 4 + 255) // 256 * 256
-    assert lib.gdn_prefill_backward_chunked_workspace_size(ctypes.byref(d)) == \
-        order + y + n * (164864 + 196608) + flags
+    assert lib.gdn_prefill_backward_chunked_workspace_size(ctypes.byref(d)) == order + n * (164864 + 196608) + flags
     # smaller heads run on the same 128-wide tiles and records: the same size
-    # but for the y of the forward
     for dk, dv in ((64, 128), (128, 64), (32, 32)):
         small = _dims(B=2, T=130, Hk=1, Hv=2, Dk=dk, Dv=dv)
-        y_s = (2 * 130 * 2 * dv * 2 + 255) // 256 * 256
         assert lib.gdn_prefill_backward_chunked_workspace_size(ctypes.byref(small)) == \
-            order + y_s + n * (164864 + 196608) + flags
+            order + n * (164864 + 196608) + flags
