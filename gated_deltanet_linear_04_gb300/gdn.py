@@ -402,6 +402,20 @@ def gating(dims, a, b, A_log, dt_bias, stream=None):
     return g, beta
 
 
+def shard_rows(B: int, world: int, rank: int):
+    """Rows [start, stop) of a batch of B rows that rank `rank` of `world`
+    takes when one call is split across ranks by batch row: contiguous, the
+    sizes differing by at most one.  Every (b, head) owns its state, conv
+    channels and outputs, so the ranks exchange nothing: each runs the same
+    call on its rows (dims with B = stop - start, every per-row tensor sliced
+    on its batch dimension) and the results are those of the whole batch."""
+    if world < 1 or not 0 <= rank < world or B < 0:
+        raise ValueError("shard_rows: need world >= 1, 0 <= rank < world, B >= 0")
+    q, r = divmod(B, world)
+    start = rank * q + min(rank, r)
+    return start, start + q + (1 if rank < r else 0)
+
+
 def recurrent_decode(dims, qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, row_mask=None, stream=None):
     """One token; conv_state and state are updated in place.  Returns y [B, Hv, Dv]."""
     y = torch.empty((dims.B, dims.Hv, dims.Dv), dtype=BF16, device=qkv.device)
