@@ -33,9 +33,10 @@
 //     written as the chain's shared-memory images;
 //  2. chain, one CTA per head walking its chunks backwards with G in TMEM:
 //     dZ^T = X1^T + G Wb^T, then G <- gamma_63 G + Cq + (dZ^T diag(beta))
-//     (-gamma K); it stores G and dZ^T of every chunk and writes dv;
-//  3. gradients I, one CTA per chunk: gamma S0 products, dP and dZ D^T, the
-//     64 x 64 terms (dP o M, H + H^T, the dlog g staircase, dbeta);
+//     (-gamma K); it stores G and dZ^T of every chunk;
+//  3. gradients I, one CTA per chunk: dv = beta dZ, gamma S0 products, dP
+//     and dZ D^T, the 64 x 64 terms (dP o M, H + H^T, the dlog g staircase,
+//     dbeta);
 //  4. gradients II, one CTA per chunk: dQ^T and dK^T on the tensor cores
 //     (M = 128 = Dk), the F dF terms and dg; dq and dk are added with
 //     atomics (summed over the v-heads of a k-head).
@@ -663,19 +664,15 @@ __device__ __forceinline__ void chain_head(const BcParams &p, BcShared &sh, uint
             }
             tmem_put64(lt + R_CG + half * 64, gv);
         }
-        // dZ^T: record, dv = beta dZ, and dZ^T diag(beta) as the A operand
+        // dZ^T: its record, and dZ^T diag(beta) as the A operand (dv = beta dZ
+        // is written by the first gradient pass, off the chain)
         {
             float z[32];
             umma::tmem_ld32(lt + R_CZ + half * 32, z);
             umma::tmem_ld_wait();
             store_rec64(p.rec_z + ci * kRec64, row, half, z);
-            const int t0 = c * kC;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = half * 32 + j;
-                z[j] *= meta[r];
-                if (t0 + r < T && row < p.Dv) p.dv[(((size_t)b * T + t0 + r) * p.Hv + hv) * p.Dv + row] = z[j];
-            }
+            for (int j = 0; j < 32; ++j) z[j] *= meta[half * 32 + j];
             dt_tile(z, sm, R_DZB, row, half);
         }
         umma::tmem_st_wait();
@@ -852,6 +849,15 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
         // [dY ; dZ] as the A operand (the [gamma K ; gamma Q] tiles are dead), D as B
         put_transposed<32>(sm, A_GKQ, 16384, 64, row, z, half * 32);
         put_transposed<32>(sm, A_KQ, 8192, 0, row, dl, half * 32);
+        // dv = beta dZ (a warp's 32 threads write 128 contiguous bytes per step)
+        if (row < p.Dv) {
+            float *dv0 = p.dv + (((size_t)b * T + t0) * p.Hv + hv) * p.Dv + row;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int r = half * 32 + j;
+                if (t0 + r < T) dv0[(size_t)r * p.Hv * p.Dv] = sh.s_beta[r] * z[j];
+            }
+        }
         build_dy_rows(sm, A_DY, A_GKQ, 16384, sh.s_ok, tid);
         publish_operands();
         if (tid == 0) {
