@@ -33,7 +33,10 @@
 //     written as the chain's shared-memory images;
 //  2. chain, one CTA per head walking its chunks backwards with G in TMEM:
 //     dZ^T = X1^T + G Wb^T, then G <- gamma_63 G + Cq + (dZ^T diag(beta))
-//     (-gamma K); it stores G and dZ^T of every chunk;
+//     (-gamma K); it stores G and dZ^T of every chunk.  When the heads take
+//     at most a quarter of the SMs, 1 and 2 run as one cooperative launch
+//     (the other CTAs produce the images, last chunk first, each published
+//     by a ready flag that its chain acquires before loading it);
 //  3. gradients I, one CTA per chunk: dv = beta dZ, gamma S0 products, dP
 //     and dZ D^T, the 64 x 64 terms (dP o M, H + H^T, the dlog g staircase,
 //     dbeta);
