@@ -806,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad1_kernel(const __grid_cons
         float s0[64];
         load_rec128(p.rec_s + ci * kRec128, row, half, s0);
         load_rec64(p.rec_z + ci * kRec64, row, half, z);
-        load_rec64(p.rec_d + ci * kRec64, row, half, dl);
+        load_dt_record(p.rec_d + ci * kRec64, row, half, dl);
         tmem_put64(lt + A_CS0 + half * 64, s0);
         umma::tmem_st_wait();
     }
@@ -1075,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1) bc_grad2_kernel(const __grid_cons
         load_rec128(p.rec_s + ci * kRec128, row, half, s0);
         load_rec64(p.rec_z + ci * kRec64, row, half, z);
         load_rec128(p.rec_g + ci * kRec128, row, half, gv);
-        load_rec64(p.rec_d + ci * kRec64, row, half, dl);
+        load_dt_record(p.rec_d + ci * kRec64, row, half, dl);
         put_transposed<64>(sm, B_A, 16384, 0, row, s0, half * 64);     // S0^T [dk][dv]
         put_transposed<32>(sm, B_B, 16384, 64, row, z, half * 32);     // dZ [r][dv], rows 64-127
         float acc = 0.0f;

@@ -470,6 +470,19 @@ __device__ __forceinline__ const float4 *rec64_at(const float *rec, int row, int
     return reinterpret_cast<const float4 *>(rec) + ((half * 8 + j) * 128 + row);
 }
 
+// The D^T record is the shared-memory D^T operand tile itself (dt_tile
+// below: [128 dv][64 r] tf32, two 128B-swizzled K-tiles of 16 KiB), bulk-
+// stored as it is; thread (row, half) reads its 32 columns [32 half, +32)
+// back from row `row` of K-tile `half` (16-byte group j at j ^ (row % 8)).
+__device__ __forceinline__ void load_dt_record(const float *rec, int row, int half, float (&v)[32]) {
+    const float4 *base = reinterpret_cast<const float4 *>(rec) + half * 1024 + row * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float4 x = base[j ^ (row & 7)];
+        v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+    }
+}
+
 // a [128][64] record row held in registers (32 columns of this thread)
 __device__ __forceinline__ void store_rec64(float *rec, int row, int half, const float (&v)[32]) {
 #pragma unroll

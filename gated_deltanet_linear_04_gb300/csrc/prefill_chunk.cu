@@ -279,7 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             if (quad >= 2) umma::tmem_ld32(tmem + lane_base + C_QK + half * 32, qk);
             umma::tmem_ld_wait();
             dt_tile(dv, sm, S_DT, row, half);
-            if constexpr (REC) store_rec64(p.rec_d + ci * kRec64, row, half, dv);
             if (quad >= 2) p_tile(qk, sm, S_P, s_lg, row, half);
         }
         publish();
@@ -288,6 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         if (tid == 0) {
             issue_dt_products(tmem, base, S_DT, S_P, S_KT);
             umma::mma_commit(&bar_mma);
+            if constexpr (REC) {
+                // the D^T record: the operand tile itself, stored while the
+                // products run (read out before the next chunk's S1 wait)
+                bulk_store(p.rec_d + ci * kRec64, sm + S_DT, 32768);
+                bulk_commit();
+            }
         }
         if (!wait_mma()) { ok = false; break; }
 

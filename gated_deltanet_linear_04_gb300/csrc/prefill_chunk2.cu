@@ -459,6 +459,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         if (tid == 0) {
             issue_s0_merged(tmem, base);
             umma::mma_commit(&sh.bar2);
+            if constexpr (REC) bulk_wait_read();   // the previous D^T record has read the tile rewritten below
         }
         if (!wait_mma()) { ok = false; break; }
         // group A has been consumed: fetch the next chunk's
@@ -472,7 +473,6 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
             umma::tmem_ld32(lane_tmem + C2_D + half * 32, dv);
             umma::tmem_ld_wait();
             dt_tile(dv, sm, P2_DT, row, half);
-            if constexpr (REC) store_rec64(p.rec_d + ci * kRec64, row, half, dv);
         }
         publish();
         ok = __syncthreads_and(mbar_wait(&sh.bar1, (uint32_t)(it & 1), p.err)) != 0;
@@ -482,7 +482,14 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
             umma::fence_after_sync();
             issue_dt_merged(tmem, base);
             umma::mma_commit(&sh.bar2);
-            bulk_wait_read();   // the previous chunk's y store has read the staging tile
+            if constexpr (REC) {
+                // the D^T record: the operand tile itself, stored while the
+                // product runs (read out before the next chunk rewrites it)
+                bulk_store(p.rec_d + ci * kRec64, sm + P2_DT, 32768);
+                bulk_commit();
+            } else {
+                bulk_wait_read();   // the previous chunk's y store has read the staging tile
+            }
         }
         if (!wait_mma()) { ok = false; break; }
         if (cn < nchunks) load_b(cn, it + 1);
