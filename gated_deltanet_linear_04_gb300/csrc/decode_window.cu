@@ -11,9 +11,11 @@
 // src/models/gated_delta.rs", GatedDeltaNet::forward (conv window, conv1d +
 // silu, q/k normalisation, beta, g).
 //
-// Same layout as the single-token kernel: a cluster per (b, hk) group of the
-// G v-heads x SN row slices, each CTA bulk-copies its R x Dk state slice into
-// shared memory while it computes the conv/norm/gates of the T tokens.  A
+// Layout of the single-token kernel: a cluster per (b, hk) group of the G
+// v-heads x SN row slices (here SN = 1, a whole head per CTA, unless the
+// heads are too few to fill the GPU), each CTA bulk-copies its R x Dk state
+// slice into shared memory while it computes the conv/norm/gates of the T
+// tokens.  A
 // CTA's life is a chain (inputs -> conv -> norm -> rows -> stores) with the
 // state copy hidden under its first links, and with several CTAs per SM the
 // links also compete for issue slots, so the chain is kept short: the conv
@@ -111,11 +113,12 @@ __device__ __forceinline__ void store_conv_rows(const WindowParams &p, int b, in
     for (int j = 0; j < K - 1; ++j) cs[(size_t)j * p.C] = rows[j];
 }
 
-// Four CTAs per SM (64 registers) except for loops to 6 tokens, which ran
-// their conv phase 2.5x slower at that bound and measured best at three
-// (T = 5: 182 -> 149 us at B=128; loops to 8 measured best at four).
+// Three CTAs per SM (80 registers, no spills) for loops to at most 6
+// tokens, where a CTA holds all 128 rows of a head (64 KiB of state: room for
+// three in shared memory anyway); four (64 registers) for loops to 8, which
+// take half a head per CTA.
 template <int DK, int K, int TM>
-__global__ void __launch_bounds__(kThreads, TM == 6 ? 3 : 4) window_kernel(const WindowParams p) {
+__global__ void __launch_bounds__(kThreads, TM == 8 ? 4 : 3) window_kernel(const WindowParams p) {
     constexpr int LPR = 8;             // lanes per row
     constexpr int RPP = 32 / LPR;      // rows per warp pass
     constexpr int NG = DK / 4 / LPR;   // 16-byte column groups per lane
@@ -367,10 +370,10 @@ cudaError_t launch_t(const WindowParams &p, cudaStream_t st) {
     cfg.attrs = attr;
     // programmatic launch (the next grid scheduled while this one drains)
     // only for grids larger than one resident wave, as for the decode step,
-    // and not for loops to 6 tokens (at three CTAs per SM it measured 1-2 %
-    // slower there, 1-2 % faster for 1, 3, 4 and 7 tokens)
+    // and not for loops to 6 tokens (it measured 1-2 % slower there, 1-2 %
+    // faster for 1, 3, 4 and 7 tokens)
     const long ctas = (long)cfg.gridDim.x * cfg.gridDim.y * cfg.gridDim.z;
-    cfg.numAttrs = (TM != 6 && ctas > 4L * num_sms()) ? 2 : 1;
+    cfg.numAttrs = (TM != 6 && ctas > (TM == 8 ? 4L : 3L) * num_sms()) ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, window_kernel<DK, K, TM>, p);
 }
 
@@ -391,8 +394,15 @@ cudaError_t launch_decode_window(const Sizes &s, const uint16_t *qkv, const uint
                                  const uint16_t *a, const uint16_t *b, const float *A_log, const float *dt_bias,
                                  float *state, const int32_t *keep, uint16_t *y, unsigned *err, cudaStream_t st) {
     if (s.T < 1 || s.T > kMaxT) return cudaErrorNotSupported;
+    // Up to 6 tokens a CTA takes all Dv rows of its head unless the heads are
+    // too few to fill the GPU: the q/k conv and normalisation, which every
+    // CTA of a k-head repeats, are then shared by twice the rows (two row
+    // slices per head measured 112.6 against 105.4 us per 4-token window at
+    // B=128, the work down from 12k to 8.4k warp instructions per 64 rows).
+    // For 7 or 8 tokens the rows' longer chain favours more, smaller CTAs
+    // (188 against 169 us at 7 tokens with whole heads).
     const int G = s.Hv / s.Hk;
-    int SN = (s.Dv >= 64 && G * 2 <= 8) ? 2 : 1;
+    int SN = (s.T > 6 && s.Dv >= 64 && G * 2 <= 8) ? 2 : 1;
     const long heads = (long)s.B * s.Hv;
     while (SN * 2 <= s.Dv / 16 && G * SN * 2 <= 8 && heads * SN < 2L * num_sms()) SN *= 2;
     WindowParams p{qkv, conv_w, conv_state, a, b, A_log, dt_bias, state, keep, y, err,
