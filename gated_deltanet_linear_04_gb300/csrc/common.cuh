@@ -136,6 +136,11 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// ... every committed group but the most recent one
+__device__ __forceinline__ void bulk_wait_all_but_newest() {
+    asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
+}
+
 // Wait until every committed bulk store has finished reading its shared-memory
 // source (the global writes may still be in flight; they complete with the
 // grid).  Enough before a CTA exits or reuses the buffer.

@@ -281,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
             dt_tile(dv, sm, S_DT, row, half);
             if (quad >= 2) p_tile(qk, sm, S_P, s_lg, row, half);
         }
+        umma::tmem_st_wait();   // the decayed state is in TMEM before the product accumulates onto it
         publish();
 
         // ---- S8: Y^T += D^T P^T ; S += D^T Kc^T

@@ -63,9 +63,11 @@ constexpr size_t kBlobBytes = (size_t)kGroupA + kGroupB;
 
 // pass 1 shared memory: 13 slots of 16 KiB in one of two maps.  A unit's k/q
 // and v tiles arrive in its KQ (two slots) and V slots; once the products
-// have read them, KQ and V hold P and U^T and (bV)^T holds -W.  The outputs
-// (gQ, Kc^T, -W, P, U^T) then leave by bulk stores while the next unit
-// starts.  The BK pair and the A slot are free at the end of a unit, and the
+// have read them, KQ and V hold P and U^T and (bV)^T holds -W.  Each output
+// leaves by bulk stores once it is final (gQ and Kc^T after the builds, P
+// after its tile, -W and U^T at the unit's end), so that the next unit, whose
+// builds overwrite these slots, waits only for the last 64 KiB to be read
+// out.  The BK pair and the A slot are free at the end of a unit, and the
 // next unit's k/q and v tiles are fetched into them as soon as the U/W
 // products complete, so the two maps alternate:
 //   map 0: KQ 6-7, V 8,  gQ 0-1, Kc^T 2-3, bV 4-5, bK 9-10, A 11, T 12
@@ -190,10 +192,14 @@ __device__ __forceinline__ void unit_tiles(const TwoPassParams &p, const CUtenso
     load_chunk_tiles(sm, m.kq, m.v, tm_k, tm_q, tm_v, p.Dk, p.Dv, hv / (p.Hv / p.Hk), hv, b * p.T + c * kC, &sh.bar0);
 }
 
-// Publishes the previous unit's image once its stores have completed (thread 0).
-__device__ __forceinline__ void publish_pending(Producer &pr) {
+// Publishes the previous unit's image once its stores have completed (thread
+// 0).  Inside a unit the newest store group is that unit's own gQ / Kc^T,
+// which need not be waited for.
+__device__ __forceinline__ void publish_pending(Producer &pr, bool own_group_pending) {
     if (pr.pending_flag != nullptr) {
-        bulk_wait_all();    // the writes are done, not only read out
+        // the writes are done, not only read out
+        if (own_group_pending) bulk_wait_all_but_newest();
+        else bulk_wait_all();
         __threadfence();    // ... and so is the meta store
         publish_ready(pr.pending_flag);
         pr.pending_flag = nullptr;
@@ -253,7 +259,18 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
         build_gq(sm, M.kq, M.gq, sh.s_gam, tid);
         build_kt_bk(sm, M.kq, M.kt, M.bk, sh.s_kc, sh.s_bg, tid);
         build_bv(sm, M.v, M.bv, sh.s_beta, tid);
+        fence_proxy_async_smem();   // gQ and Kc^T leave now (below), not with the rest
         ok = wait_mma();
+    }
+    uint8_t *const blob = p.blobs + blob_index(p, b, hv, c) * kBlobBytes;
+    if (ok && tid == 0) {
+        // gQ and Kc^T are final: store them while the unit goes on, so that
+        // only -W and U^T are left for the unit's end
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) bulk_store(blob + B_NWGQ + kt * 16384 + 8192, sm + M.gq + kt * 8192, 8192);
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt) bulk_store(blob + B_PKT + kt * 24576 + 8192, sm + M.kt + kt * kSlot, 16384);
+        bulk_commit();
     }
     if (ok) {
         // A from K K^T (quads 0-1); P from Q K^T (quads 2-3) into the dead KQ slot
@@ -265,9 +282,15 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
             umma::tmem_ld_wait();
             p_tile(qk, sm, M.kq, sh.s_lg, row, half);
         }
+        fence_proxy_async_smem();   // P leaves as soon as it is written
         // the previous unit's stores have had this unit's builds to complete
-        if (tid == 0) publish_pending(pr);
+        if (tid == 0) publish_pending(pr, true);
         __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) bulk_store(blob + B_PKT + kt * 24576, sm + M.kq + kt * 8192, 8192);
+            bulk_commit();
+        }
         invert_unit_lower(As, Ys, tid);
         t_to_tf32(As, sm, M.t, tid);
         publish();
@@ -296,22 +319,12 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
         umma::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
-            const size_t bi = blob_index(p, b, hv, c);
-            uint8_t *blob = p.blobs + bi * kBlobBytes;
             *reinterpret_cast<float *>(blob + B_META) = sh.s_gam[kC - 1];
 #pragma unroll
-            for (int kt = 0; kt < 4; ++kt) {
-                bulk_store(blob + B_NWGQ + kt * 16384, sm + M.bv + kt * 8192, 8192);
-                bulk_store(blob + B_NWGQ + kt * 16384 + 8192, sm + M.gq + kt * 8192, 8192);
-            }
+            for (int kt = 0; kt < 4; ++kt) bulk_store(blob + B_NWGQ + kt * 16384, sm + M.bv + kt * 8192, 8192);
             bulk_store(blob + B_UT, sm + ut, 32768);
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                bulk_store(blob + B_PKT + kt * 24576, sm + M.kq + kt * 8192, 8192);
-                bulk_store(blob + B_PKT + kt * 24576 + 8192, sm + M.kt + kt * kSlot, 16384);
-            }
             bulk_commit();
-            if (p.ready != nullptr) pr.pending_flag = p.ready + bi;
+            if (p.ready != nullptr) pr.pending_flag = p.ready + blob_index(p, b, hv, c);
         }
     } else if (tid == 0) {
         // a wait gave up: give in-flight MMAs and copies a bounded chance to drain
@@ -474,6 +487,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
             umma::tmem_ld_wait();
             dt_tile(dv, sm, P2_DT, row, half);
         }
+        umma::tmem_st_wait();   // the decayed state is in TMEM before the product accumulates onto it
         publish();
         ok = __syncthreads_and(mbar_wait(&sh.bar1, (uint32_t)(it & 1), p.err)) != 0;
         if (tid == 0) b_pending = false;
@@ -642,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_overlap_kernel(const __grid
             u = un;
         }
         if (threadIdx.x == 0) {
-            publish_pending(pr);   // the last unit's image
+            publish_pending(pr, false);   // the last unit's image
             bulk_wait_read();
         }
     }
