@@ -445,16 +445,36 @@ __global__ void __launch_bounds__(256) conv_state_kernel(const ConvParams p, uin
         if (j < n) conv_state[((size_t)b * n + j) * p.C + c] = vals[j];
 }
 
+// Each thread steps its head index by the grid stride modulo Hv instead of
+// dividing every element's index (a 64-bit remainder per element was a large
+// part of this kernel's instructions); with SMEM (Hv up to kGateSmemHeads)
+// the per-head constants exp(A_log) and dt_bias sit in shared memory.  The
+// arithmetic per element is the same either way.
+constexpr int kGateSmemHeads = 2048;
+template <bool SMEM>
 __global__ void __launch_bounds__(256) gating_kernel(const uint16_t *__restrict__ a, const uint16_t *__restrict__ bb,
                                                      const float *__restrict__ A_log,
                                                      const float *__restrict__ dt_bias, float *__restrict__ g,
                                                      float *__restrict__ beta, size_t n, int Hv) {
+    __shared__ float gate_consts[SMEM ? 2 * kGateSmemHeads : 1];   // [Hv] exp(A_log), [Hv] dt_bias
+    if constexpr (SMEM) {
+        for (int h = threadIdx.x; h < Hv; h += blockDim.x) {
+            gate_consts[h] = expf(A_log[h]);
+            gate_consts[kGateSmemHeads + h] = dt_bias[h];
+        }
+        __syncthreads();
+    }
     const size_t stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const int h = (int)(i % (size_t)Hv);
-        const float x = bf16_to_f32(a[i]) + dt_bias[h];
-        g[i] = expf(-expf(A_log[h]) * softplus(x));
+    const int hstep = (int)(stride % (size_t)Hv);
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int h = (int)(i % (size_t)Hv);
+    for (; i < n; i += stride) {
+        const float ea = SMEM ? gate_consts[h] : expf(A_log[h]);
+        const float x = bf16_to_f32(a[i]) + (SMEM ? gate_consts[kGateSmemHeads + h] : dt_bias[h]);
+        g[i] = expf(-ea * softplus(x));
         beta[i] = sigmoid(bf16_to_f32(bb[i]));
+        h += hstep;
+        if (h >= Hv) h -= Hv;
     }
 }
 
@@ -506,7 +526,11 @@ cudaError_t launch_gating(const Sizes &s, const uint16_t *a, const uint16_t *b, 
     size_t blocks = (n + threads - 1) / threads;
     const size_t cap = (size_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    gating_kernel<<<(unsigned)blocks, threads, 0, st>>>(a, b, A_log, dt_bias, g, beta, n, s.Hv);
+    if (blocks == 0) return cudaSuccess;
+    if (s.Hv <= kGateSmemHeads)
+        gating_kernel<true><<<(unsigned)blocks, threads, 0, st>>>(a, b, A_log, dt_bias, g, beta, n, s.Hv);
+    else
+        gating_kernel<false><<<(unsigned)blocks, threads, 0, st>>>(a, b, A_log, dt_bias, g, beta, n, s.Hv);
     return cudaGetLastError();
 }
 
