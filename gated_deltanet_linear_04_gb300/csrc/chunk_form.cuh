@@ -351,37 +351,59 @@ __device__ __forceinline__ void p_tile(const float (&qk)[32], uint8_t *sm, uint3
 
 // One merge level: for each pair of S x S diagonal blocks (a = [q0, q0+S),
 // b = [q0+S, q0+2S)) of the unit lower triangular T, the lower-left block is
-// X = -T_bb A_ba T_aa.  Each work item computes 4 adjacent columns of one row; sums
-// run over full blocks because the triangular factors hold explicit zeros
-// above the diagonal.
-template <int S>
+// X = -T_bb A_ba T_aa.  Sums run over full blocks because the triangular
+// factors hold explicit zeros above the diagonal.  A work item computes 4
+// adjacent columns of RB rows, rows rg, rg + S/RB, ..., so that each loaded
+// row of the right factor serves RB rows, and the rows a warp reads the left
+// factor from at once differ in (row mod 8), i.e. in their bank swizzle.
+// Each output element is the same sequence of fused multiply-adds as with
+// one row per thread.  At S = 32 (cycles per level in an instrumented copy):
+// one row per thread (256 threads, every warp loading the whole right
+// factor) 2.8k, four rows (64 threads, too few to hide the load latency)
+// 2.5k, two rows (128 threads) 1.9k.
+template <int S, int RB>
 __device__ __forceinline__ void merge_level(float *As, float *Ys, int tid) {
-    constexpr int G4 = S / 4;
-    constexpr int NT = (32 / S) * S * G4;
-    const int pi = tid / (S * G4), rem = tid % (S * G4), r = rem / G4, c = (rem % G4) * 4, q0 = pi * 2 * S;
+    constexpr int G4 = S / 4;          // column groups of 4
+    constexpr int RG = S / RB;         // row groups
+    constexpr int NT = (32 / S) * RG * G4;
+    const int pi = tid / (RG * G4), rem = tid % (RG * G4), rg = rem / G4, c = (rem % G4) * 4, q0 = pi * 2 * S;
     if (tid < NT) {
         // packed two-wide FMAs: each half rounds like fmaf
-        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+        float2 lo[RB], hi[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) lo[i] = hi[i] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < S; ++m) {
-            const float a = As[aidx(q0 + S + r, q0 + m)];
             const float4 t = ld4(As + aidx(q0 + m, q0 + c));
-            lo = __ffma2_rn(make_float2(a, a), make_float2(t.x, t.y), lo);
-            hi = __ffma2_rn(make_float2(a, a), make_float2(t.z, t.w), hi);
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const float a = As[aidx(q0 + S + rg + i * RG, q0 + m)];
+                lo[i] = __ffma2_rn(make_float2(a, a), make_float2(t.x, t.y), lo[i]);
+                hi[i] = __ffma2_rn(make_float2(a, a), make_float2(t.z, t.w), hi[i]);
+            }
         }
-        st4(Ys + (pi * S + r) * S + c, make_float4(lo.x, lo.y, hi.x, hi.y));
+#pragma unroll
+        for (int i = 0; i < RB; ++i)
+            st4(Ys + (pi * S + rg + i * RG) * S + c, make_float4(lo[i].x, lo[i].y, hi[i].x, hi[i].y));
     }
     __syncthreads();
     if (tid < NT) {
-        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+        float2 lo[RB], hi[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) lo[i] = hi[i] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < S; ++m) {
-            const float t = As[aidx(q0 + S + r, q0 + S + m)];
             const float4 yv = ld4(Ys + (pi * S + m) * S + c);
-            lo = __ffma2_rn(make_float2(t, t), make_float2(yv.x, yv.y), lo);
-            hi = __ffma2_rn(make_float2(t, t), make_float2(yv.z, yv.w), hi);
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const float t = As[aidx(q0 + S + rg + i * RG, q0 + S + m)];
+                lo[i] = __ffma2_rn(make_float2(t, t), make_float2(yv.x, yv.y), lo[i]);
+                hi[i] = __ffma2_rn(make_float2(t, t), make_float2(yv.z, yv.w), hi[i]);
+            }
         }
-        st4(As + aidx(q0 + S + r, q0 + c), make_float4(-lo.x, -lo.y, -hi.x, -hi.y));
+#pragma unroll
+        for (int i = 0; i < RB; ++i)
+            st4(As + aidx(q0 + S + rg + i * RG, q0 + c), make_float4(-lo[i].x, -lo[i].y, -hi[i].x, -hi[i].y));
     }
     __syncthreads();
 }
@@ -412,9 +434,9 @@ __device__ __forceinline__ void invert_unit_lower(float *As, float *Ys, int tid)
         }
         __syncthreads();
     }
-    merge_level<8>(As, Ys, tid);
-    merge_level<16>(As, Ys, tid);
-    merge_level<32>(As, Ys, tid);
+    merge_level<8, 1>(As, Ys, tid);
+    merge_level<16, 2>(As, Ys, tid);
+    merge_level<32, 2>(As, Ys, tid);
 }
 
 // T -> tf32 B operand [r][i] (2 K-tiles of 8 KiB)
