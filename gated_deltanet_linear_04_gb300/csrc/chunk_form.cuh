@@ -279,30 +279,45 @@ __device__ __forceinline__ void build_gq(uint8_t *sm, uint32_t kq_off, uint32_t 
 }
 
 // Kc^T[dk][r] and (b g K)^T[dk][r]: lanes take consecutive dk (conflict-free
-// reads along a K row), each thread 4 consecutive r
+// reads along a K row and conflict-free 16-byte stores, a quarter-warp's
+// eight dk rows on eight swizzle phases), each thread 4 consecutive r of two
+// row quads (warp w: rows 4w and 4w + 32), so the per-row factors are loaded
+// once per quad rather than once per element group
 __device__ __forceinline__ void build_kt_bk(uint8_t *sm, uint32_t kq_off, uint32_t kt_off, uint32_t bk_off,
                                             const float *s_kc, const float *s_bg, int tid) {
-    for (int i = tid; i < kD * kC / 4; i += kThreads) {
-        const int dk = i & (kD - 1), r = (i >> 7) * 4;
-        const float k0 = kq_elem(sm, kq_off, r, dk), k1 = kq_elem(sm, kq_off, r + 1, dk),
-                    k2 = kq_elem(sm, kq_off, r + 2, dk), k3 = kq_elem(sm, kq_off, r + 3, dk);
-        const uint32_t off = (r >> 5) * kSlot + umma::sw128(dk, (r & 31) * 4);
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+    for (int rp = 0; rp < 2; ++rp) {
+        const int r = (w + 8 * rp) * 4;
         const float4 kc = ld4(s_kc + r), bg = ld4(s_bg + r);
-        st_tf32x4(sm, kt_off + off, kc.x * k0, kc.y * k1, kc.z * k2, kc.w * k3);
-        st_tf32x4(sm, bk_off + off, bg.x * k0, bg.y * k1, bg.z * k2, bg.w * k3);
+#pragma unroll
+        for (int j = 0; j < kD / 32; ++j) {
+            const int dk = lane + 32 * j;
+            const float k0 = kq_elem(sm, kq_off, r, dk), k1 = kq_elem(sm, kq_off, r + 1, dk),
+                        k2 = kq_elem(sm, kq_off, r + 2, dk), k3 = kq_elem(sm, kq_off, r + 3, dk);
+            const uint32_t off = (r >> 5) * kSlot + umma::sw128(dk, (r & 31) * 4);
+            st_tf32x4(sm, kt_off + off, kc.x * k0, kc.y * k1, kc.z * k2, kc.w * k3);
+            st_tf32x4(sm, bk_off + off, bg.x * k0, bg.y * k1, bg.z * k2, bg.w * k3);
+        }
     }
 }
 
-// (b V)^T[dv][i]
+// (b V)^T[dv][i]: the same thread layout
 __device__ __forceinline__ void build_bv(uint8_t *sm, uint32_t v_off, uint32_t bv_off, const float *s_beta,
                                          int tid) {
     const uint16_t *Vs = reinterpret_cast<const uint16_t *>(sm + v_off);
-    for (int i = tid; i < kD * kC / 4; i += kThreads) {
-        const int dv = i & (kD - 1), r = (i >> 7) * 4;
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+    for (int rp = 0; rp < 2; ++rp) {
+        const int r = (w + 8 * rp) * 4;
         const float4 be = ld4(s_beta + r);
-        st_tf32x4(sm, bv_off + (r >> 5) * kSlot + umma::sw128(dv, (r & 31) * 4),
-                  be.x * bf16_to_f32(Vs[r * kD + dv]), be.y * bf16_to_f32(Vs[(r + 1) * kD + dv]),
-                  be.z * bf16_to_f32(Vs[(r + 2) * kD + dv]), be.w * bf16_to_f32(Vs[(r + 3) * kD + dv]));
+#pragma unroll
+        for (int j = 0; j < kD / 32; ++j) {
+            const int dv = lane + 32 * j;
+            st_tf32x4(sm, bv_off + (r >> 5) * kSlot + umma::sw128(dv, (r & 31) * 4),
+                      be.x * bf16_to_f32(Vs[r * kD + dv]), be.y * bf16_to_f32(Vs[(r + 1) * kD + dv]),
+                      be.z * bf16_to_f32(Vs[(r + 2) * kD + dv]), be.w * bf16_to_f32(Vs[(r + 3) * kD + dv]));
+        }
     }
 }
 
