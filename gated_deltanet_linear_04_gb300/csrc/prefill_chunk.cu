@@ -137,17 +137,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     // ---- initial state -> TMEM S (row = dv, columns = dk); half 0: dk 0-63, half 1: 64-127
     state_to_tmem(p.state_in, tmem + lane_base + C_S, b, hv, p.Hv, p.Dk, p.Dv, row, half);
 
-    // per-step g, beta, mask of a chunk: gathered into registers early (threads
-    // < 64, one step each) and published to shared memory later, so the global
-    // load latency never sits in front of a block barrier
+    // per-step g, beta, mask of a chunk: gathered into registers early (the
+    // last two warps, one step per thread) and published to shared memory
+    // later, so the global load latency never sits in front of a block
+    // barrier; those warps also issue the next chunk's TMA, so that the first
+    // two warps, which run A and the inverse's first phase, are not held up
+    constexpr int kStepT0 = kThreads - kC;
     float pf_g = 1.0f, pf_b = 0.0f;
     int pf_m = 0;
     auto gather_steps = [&](int c) {
         pf_g = 1.0f;
         pf_b = 0.0f;
         pf_m = 0;
-        const int t = c * kC + tid;
-        if (tid < kC && t < T) {
+        const int i = tid - kStepT0;
+        const int t = c * kC + i;
+        if (i >= 0 && t < T) {
             const size_t gi = ((size_t)b * T + t) * p.Hv + hv;
             pf_m = p.mask == nullptr ? 1 : (p.mask[(size_t)b * T + t] != 0);
             if (pf_m) {
@@ -157,14 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         }
     };
     auto publish_steps = [&](int slot) {
-        if (tid < kC) {
-            s_g[slot][tid] = pf_g;
-            s_b[slot][tid] = pf_b;
-            s_m[slot][tid] = pf_m;
+        const int i = tid - kStepT0;
+        if (i >= 0) {
+            s_g[slot][i] = pf_g;
+            s_b[slot][i] = pf_b;
+            s_m[slot][i] = pf_m;
         }
     };
     auto issue_tma = [&](int c) {
-        if (tid == 0)
+        if (tid == kThreads - 1)
             load_chunk_tiles(sm, S_KQ, S_V, &tm_k, &tm_q, &tm_v, p.Dk, p.Dv, hk, hv, b * T + c * kC, &bar_tma);
     };
 
@@ -205,9 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
     for (int it = 0; c < nchunks && ok; ++it) {
         const int st = it & 1;
         const int t0 = c * kC;
-        // ---- S1: chunk inputs, log-decay prefix sums (warp 0)
+        // ---- S1: chunk inputs, log-decay prefix sums (warp 0 for the first
+        // chunk; later ones have them from the previous chunk's S8)
         ok = mbar_wait(&bar_tma, (uint32_t)(it & 1), p.err);
-        if (warp == 0) step_factors(lane, s_g[st], s_b[st], s_lg, s_gam, s_kc, s_beta, s_bg);
+        if (it == 0 && warp == 0) step_factors(lane, s_g[st], s_b[st], s_lg, s_gam, s_kc, s_beta, s_bg);
         if (tid == 0) bulk_wait_read();   // the previous y store has read its tile (slot 9 is rebuilt below)
         ok = __syncthreads_and(ok) != 0;
         if (!ok) break;
@@ -284,7 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         umma::tmem_st_wait();   // the decayed state is in TMEM before the product accumulates onto it
         publish();
 
-        // ---- S8: Y^T += D^T P^T ; S += D^T Kc^T
+        // ---- S8: Y^T += D^T P^T ; S += D^T Kc^T; while they run, warp 1
+        // forms the next chunk's step factors (this chunk's are dead after S7)
+        if (warp == 1 && cn < nchunks)
+            step_factors(lane, s_g[st ^ 1], s_b[st ^ 1], s_lg, s_gam, s_kc, s_beta, s_bg);
         if (tid == 0) {
             issue_dt_products(tmem, base, S_DT, S_P, S_KT);
             umma::mma_commit(&bar_mma);
