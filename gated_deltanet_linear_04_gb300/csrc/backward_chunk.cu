@@ -172,17 +172,24 @@ __device__ __forceinline__ void put_transposed(uint8_t *sm, uint32_t dst, uint32
 
 // (sign * scale o X)^T [128 dk][64 r] tf32 (2 K-tiles of 16 KiB) from the K
 // (row_base 0) or Q (row_base 64) rows of the bf16 KQ tile; scale null = 1.
-// Lanes take consecutive dk, each thread 4 consecutive r.
+// Lanes take consecutive dk, each thread 4 consecutive r of two row quads
+// (warp w: rows 4w and 4w + 32), the quad's factors loaded once.
 __device__ __forceinline__ void build_xt(uint8_t *sm, uint32_t kq_off, int row_base, uint32_t dst,
                                          const float *scale, float sign, int tid) {
-    for (int i = tid; i < kD * kC / 4; i += kThreads) {
-        const int dk = i & (kD - 1), r = (i >> 7) * 4;
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+    for (int rp = 0; rp < 2; ++rp) {
+        const int r = (w + 8 * rp) * 4;
         const float4 sc = scale != nullptr ? ld4(scale + r) : make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-        st_tf32x4(sm, dst + (r >> 5) * kSlot + umma::sw128(dk, (r & 31) * 4),
-                  sign * sc.x * kq_elem(sm, kq_off, row_base + r, dk),
-                  sign * sc.y * kq_elem(sm, kq_off, row_base + r + 1, dk),
-                  sign * sc.z * kq_elem(sm, kq_off, row_base + r + 2, dk),
-                  sign * sc.w * kq_elem(sm, kq_off, row_base + r + 3, dk));
+#pragma unroll
+        for (int j = 0; j < kD / 32; ++j) {
+            const int dk = lane + 32 * j;
+            st_tf32x4(sm, dst + (r >> 5) * kSlot + umma::sw128(dk, (r & 31) * 4),
+                      sign * sc.x * kq_elem(sm, kq_off, row_base + r, dk),
+                      sign * sc.y * kq_elem(sm, kq_off, row_base + r + 1, dk),
+                      sign * sc.z * kq_elem(sm, kq_off, row_base + r + 2, dk),
+                      sign * sc.w * kq_elem(sm, kq_off, row_base + r + 3, dk));
+        }
     }
 }
 
@@ -221,13 +228,20 @@ __device__ __forceinline__ void build_dy_rows(uint8_t *sm, uint32_t dy_off, uint
     }
 }
 
-// dY^T [128 dv][64 r] tf32 (2 K-tiles of 16 KiB), invalid steps 0
+// dY^T [128 dv][64 r] tf32 (2 K-tiles of 16 KiB), invalid steps 0 (the
+// thread layout of build_xt)
 __device__ __forceinline__ void build_dyt(uint8_t *sm, uint32_t dy_off, uint32_t dst, const float *s_ok, int tid) {
-    for (int i = tid; i < kD * kC / 4; i += kThreads) {
-        const int dv = i & (kD - 1), r = (i >> 7) * 4;
-        st_tf32x4(sm, dst + (r >> 5) * kSlot + umma::sw128(dv, (r & 31) * 4), dy_at(sm, dy_off, s_ok, r, dv),
-                  dy_at(sm, dy_off, s_ok, r + 1, dv), dy_at(sm, dy_off, s_ok, r + 2, dv),
-                  dy_at(sm, dy_off, s_ok, r + 3, dv));
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+    for (int rp = 0; rp < 2; ++rp) {
+        const int r = (w + 8 * rp) * 4;
+#pragma unroll
+        for (int j = 0; j < kD / 32; ++j) {
+            const int dv = lane + 32 * j;
+            st_tf32x4(sm, dst + (r >> 5) * kSlot + umma::sw128(dv, (r & 31) * 4), dy_at(sm, dy_off, s_ok, r, dv),
+                      dy_at(sm, dy_off, s_ok, r + 1, dv), dy_at(sm, dy_off, s_ok, r + 2, dv),
+                      dy_at(sm, dy_off, s_ok, r + 3, dv));
+        }
     }
 }
 
