@@ -17,7 +17,7 @@
 //   [K;Q] K^T        bf16 x bf16  -> QK columns (rows 0-63 K K^T, 64-127 Q K^T)
 //   U^T = (bV)^T T^T tf32         -> D columns
 //   W^T = (bgK)^T T^T tf32        -> W columns
-//   D^T += S0 (-W)^T tf32         -> D columns (accumulates onto U^T)
+//   S0 (-W)^T    tf32             -> W columns; D^T = U^T + that, added in f32
 //   Y^T = S0 (gQ)^T  tf32         -> Y columns
 //   Y^T += D^T P^T   tf32         -> Y columns
 //   S  += D^T Kc^T   tf32         -> S columns (S pre-scaled by 2^lg_63)
@@ -580,14 +580,16 @@ __device__ __forceinline__ void issue_uw(uint32_t tmem, uint32_t base, uint32_t 
     }
 }
 
-// D^T += S0 (-W)^T and Y^T = S0 (gQ)^T, S0 read from TMEM (tf32, K = 128)
+// S0 (-W)^T into the W columns (free once -W has been read out) and
+// Y^T = S0 (gQ)^T, S0 read from TMEM (tf32, K = 128); D^T = U^T + S0 (-W)^T
+// is then formed in f32 by the threads that build the D^T tile
 __device__ __forceinline__ void issue_s0_products(uint32_t tmem, uint32_t base, uint32_t nw_off,
                                                   uint32_t gq_off) {
     const uint32_t id = umma::idesc(128, 64, umma::kFmtTF32);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
         const uint32_t kt = k >> 2, ko = (k & 3) * 32, a = tmem + C_S + 8 * k;
-        umma::mma_tf32_tmem_a(tmem + C_D, a, umma::desc_sw128(base + nw_off + kt * 8192 + ko), id, true);
+        umma::mma_tf32_tmem_a(tmem + C_W, a, umma::desc_sw128(base + nw_off + kt * 8192 + ko), id, k > 0);
         umma::mma_tf32_tmem_a(tmem + C_Y, a, umma::desc_sw128(base + gq_off + kt * 8192 + ko), id, k > 0);
     }
 }

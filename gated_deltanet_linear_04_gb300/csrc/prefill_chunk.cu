@@ -10,7 +10,8 @@
 //   S4 T = (I + A)^-1 by blocked doubling (8x8 diagonal blocks, then 16-,
 //      32-, 64-wide merges X = -T_bb A_ba T_aa) on the CUDA cores
 //   S5 U^T, W^T; -W to shared memory
-//   S6 D^T += S0 (-W)^T, Y^T = S0 (gQ)^T with S0 read from TMEM
+//   S6 S0 (-W)^T (into the W columns), Y^T = S0 (gQ)^T with S0 read from
+//      TMEM; D^T = U^T + S0 (-W)^T is added in f32 in S7
 //   S7 D^T and P = M o Q K^T to shared memory; S <- 2^lg_63 S
 //   S8 Y^T += D^T P^T, S += D^T Kc^T
 //   S9 y staged in shared memory as bf16 and stored by one TMA store of the
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         neg_w_tile(tmem + lane_base + C_W, sm, S_NW, row, half);
         publish();
 
-        // ---- S6: D^T += S0 (-W)^T ; Y^T = S0 (gQ)^T
+        // ---- S6: S0 (-W)^T -> W columns ; Y^T = S0 (gQ)^T
         if (tid == 0) {
             // A = the f32 state itself, read from TMEM (used as tf32)
             issue_s0_products(tmem, base, S_NW, S_GQ);
@@ -279,11 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_chunk_kernel(const __grid
         if constexpr (REC) decay_state(tmem + lane_base + C_S, s_gam[kC - 1], half, p.rec_s + ci * kRec128, row);
         else decay_state(tmem + lane_base + C_S, s_gam[kC - 1], half);
         {
-            // both TMEM reads in flight before the one wait
-            float dv[32], qk[32];
+            // the TMEM reads in flight before the one wait; D^T = U^T + S0 (-W)^T
+            float dv[32], dp[32], qk[32];
             umma::tmem_ld32(tmem + lane_base + C_D + half * 32, dv);
+            umma::tmem_ld32(tmem + lane_base + C_W + half * 32, dp);
             if (quad >= 2) umma::tmem_ld32(tmem + lane_base + C_QK + half * 32, qk);
             umma::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dv[j] += dp[j];
             dt_tile(dv, sm, S_DT, row, half);
             if (quad >= 2) p_tile(qk, sm, S_P, s_lg, row, half);
         }

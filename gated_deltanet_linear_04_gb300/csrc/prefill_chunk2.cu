@@ -10,8 +10,8 @@
 // writes the results to the workspace as images of the shared-memory tiles
 // the products read.  Pass 2 ("state") keeps one CTA per head walking the
 // chunks in order, but per chunk it only bulk-copies the images back and runs
-// the state products (D^T += S0 (-W)^T with U^T as the accumulator's start,
-// Y^T = S0 (gQ)^T, then Y^T += D^T P^T and S += D^T Kc^T) and the output.
+// the state products (S0 (-W)^T and Y^T = S0 (gQ)^T, D^T = U^T + S0 (-W)^T
+// added in f32, then Y^T += D^T P^T and S += D^T Kc^T) and the output.
 // Both passes run the single-pass kernel's arithmetic on the same operand
 // bits, so y and the state are bit-identical to it.
 //
@@ -339,11 +339,12 @@ __device__ __forceinline__ bool prep_unit(const TwoPassParams &p, const CUtensor
 
 // ---------------------------------------------------------------------------
 // pass 2 TMEM columns: D | Y | S adjacent, so that
-//   [D^T | Y^T] = [U^T | 0] + S0 [-W ; gQ]^T        (N = 128, K = 128)
+//   [D'^T | Y^T] = S0 [-W ; gQ]^T                    (N = 128, K = 128)
 //   [Y^T | S]  += D^T [P ; Kc^T]^T                    (N = 192, K = 64)
-// run as one MMA per K step each, S0 read from TMEM (tf32 by truncation).
-// Each accumulator sees its MMAs in the single pass's order, so the results
-// match it bit for bit (Y's zero start adds nothing).
+// run as one MMA per K step each, S0 read from TMEM (tf32 by truncation),
+// with D^T = U^T + D'^T added in f32 as the D^T tile is built.  Each
+// accumulator sees its MMAs in the single pass's order and the addition is
+// the single pass's, so the results match it bit for bit.
 // ---------------------------------------------------------------------------
 constexpr uint32_t C2_D = 64, C2_Y = 128, C2_S = 192;
 
@@ -352,7 +353,7 @@ __device__ __forceinline__ void issue_s0_merged(uint32_t tmem, uint32_t base) {
 #pragma unroll
     for (int k = 0; k < 16; ++k)
         umma::mma_tf32_tmem_a(tmem + C2_D, tmem + C2_S + 8 * k,
-                              umma::desc_sw128(base + P2_NWGQ + (k >> 2) * 16384 + (k & 3) * 32), id, true);
+                              umma::desc_sw128(base + P2_NWGQ + (k >> 2) * 16384 + (k & 3) * 32), id, k > 0);
 }
 
 __device__ __forceinline__ void issue_dt_merged(uint32_t tmem, uint32_t base) {
@@ -441,6 +442,7 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         gather_mask(c);
         if (tid < kC) sh.s_m[0][tid] = pf_m;
     }
+    umma::fence_before_sync();   // the initial state's TMEM stores, before the first product
     __syncthreads();
 
     for (int it = 0; c < nchunks && ok; ++it) {
@@ -452,27 +454,22 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         const int cn = scan.next_active(c + 1);
         if (cn < nchunks) gather_mask(cn);
 
-        // U^T -> the D accumulator and zeros -> Y, which the S0 [-W ; gQ]^T
-        // product then adds to
-        {
-            float r[32], z[32];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const float4 v = *reinterpret_cast<const float4 *>(sm + P2_UT + ut_off(row, half * 8 + jj));
-                r[4 * jj] = v.x; r[4 * jj + 1] = v.y; r[4 * jj + 2] = v.z; r[4 * jj + 3] = v.w;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = 0.0f;
-            umma::tmem_st32(lane_tmem + C2_D + half * 32, r);
-            umma::tmem_st32(lane_tmem + C2_Y + half * 32, z);
-            umma::tmem_st_wait();
-        }
+        // [D'^T | Y^T] = S0 [-W ; gQ]^T (the previous chunk's TMEM reads were
+        // ordered before the barrier of the wait above); while it runs, this
+        // thread's U^T row comes out of the image, which the next chunk's
+        // group A overwrites
         const float gl = *reinterpret_cast<const float *>(sm + P2_META);
-        publish();
         if (tid == 0) {
+            umma::fence_after_sync();
             issue_s0_merged(tmem, base);
             umma::mma_commit(&sh.bar2);
             if constexpr (REC) bulk_wait_read();   // the previous D^T record has read the tile rewritten below
+        }
+        float ut[32];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const float4 v = *reinterpret_cast<const float4 *>(sm + P2_UT + ut_off(row, half * 8 + jj));
+            ut[4 * jj] = v.x; ut[4 * jj + 1] = v.y; ut[4 * jj + 2] = v.z; ut[4 * jj + 3] = v.w;
         }
         if (!wait_mma()) { ok = false; break; }
         // group A has been consumed: fetch the next chunk's
@@ -485,6 +482,8 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
             float dv[32];
             umma::tmem_ld32(lane_tmem + C2_D + half * 32, dv);
             umma::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dv[j] = ut[j] + dv[j];   // D^T = U^T + S0 (-W)^T, as the single pass adds
             dt_tile(dv, sm, P2_DT, row, half);
         }
         umma::tmem_st_wait();   // the decayed state is in TMEM before the product accumulates onto it
