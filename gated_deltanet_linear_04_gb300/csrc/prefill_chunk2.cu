@@ -448,18 +448,19 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
     for (int it = 0; c < nchunks && ok; ++it) {
         const int st = it & 1;
         const int t0 = c * kC;
-        ok = __syncthreads_and(mbar_wait(&sh.bar0, (uint32_t)(it & 1), p.err)) != 0;
+        // every thread waits for group A itself; the block agrees on the
+        // outcome at the product's wait below (no barrier of its own here)
+        const bool got_a = mbar_wait(&sh.bar0, (uint32_t)(it & 1), p.err);
         if (tid == 0) a_pending = false;
-        if (!ok) break;
         const int cn = scan.next_active(c + 1);
         if (cn < nchunks) gather_mask(cn);
 
         // [D'^T | Y^T] = S0 [-W ; gQ]^T (the previous chunk's TMEM reads were
-        // ordered before the barrier of the wait above); while it runs, this
+        // ordered before the barrier that ended it); while it runs, this
         // thread's U^T row comes out of the image, which the next chunk's
         // group A overwrites
         const float gl = *reinterpret_cast<const float *>(sm + P2_META);
-        if (tid == 0) {
+        if (tid == 0 && got_a) {
             umma::fence_after_sync();
             issue_s0_merged(tmem, base);
             umma::mma_commit(&sh.bar2);
@@ -470,6 +471,16 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
         for (int jj = 0; jj < 8; ++jj) {
             const float4 v = *reinterpret_cast<const float4 *>(sm + P2_UT + ut_off(row, half * 8 + jj));
             ut[4 * jj] = v.x; ut[4 * jj + 1] = v.y; ut[4 * jj + 2] = v.z; ut[4 * jj + 3] = v.w;
+        }
+        {
+            // thread 0 issued nothing if its wait gave up: then nobody waits
+            // on the product's barrier
+            const bool all_a = __syncthreads_and(got_a) != 0;
+            if (!all_a) {
+                if (tid == 0 && got_a) mbar_wait(&sh.bar2, mma_phase & 1u, nullptr);   // drain what was issued
+                ok = false;
+                break;
+            }
         }
         if (!wait_mma()) { ok = false; break; }
         // group A has been consumed: fetch the next chunk's
