@@ -498,8 +498,15 @@ __device__ __forceinline__ void state_head(const TwoPassParams &p, const CUtenso
             dt_tile(dv, sm, P2_DT, row, half);
         }
         umma::tmem_st_wait();   // the decayed state is in TMEM before the product accumulates onto it
-        publish();
-        ok = __syncthreads_and(mbar_wait(&sh.bar1, (uint32_t)(it & 1), p.err)) != 0;
+        // group B waited for by every thread, and the D^T tile published,
+        // at one barrier
+        {
+            const bool got_b = mbar_wait(&sh.bar1, (uint32_t)(it & 1), p.err);
+            fence_proxy_async_smem();
+            umma::fence_before_sync();
+            ok = __syncthreads_and(got_b) != 0;
+            umma::fence_after_sync();
+        }
         if (tid == 0) b_pending = false;
         if (!ok) break;
         if (tid == 0) {
