@@ -51,7 +51,7 @@ def test_reference_arm_under_torchrun_prints_one_line():
     env = dict(os.environ, OMP_NUM_THREADS="2")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
-           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-budget-s", "0.1"]
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3", "--ref-budget-s", "0.5"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
@@ -59,6 +59,7 @@ def test_reference_arm_under_torchrun_prints_one_line():
     j = json.loads(lines[0])
     assert j["impl"] == "reference" and j["unit"] == "GB/s" and j["value"] > 0
     assert j["cpu_baseline"]["kind"] == "oracle"
+    assert j["steps"] == 2 and j["warmup"] == 3   # the requested timed and untimed steps
     assert j["e2e"]["h2d_bytes_per_step"] == 0
 
 
